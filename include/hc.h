@@ -1,0 +1,148 @@
+/*
+ * hc.h -- C ABI of the width-sharded ("halo-exchange") Conv2d for GB300.
+ *
+ * What it computes: the Shard(3) convolution of the NVIDIA technical blog
+ * "Perception model training for autonomous vehicles with tensor
+ * parallelism" (design section: input and output Shard(3) along W, weight and
+ * bias Replicate; backward grad_input Shard(3), grad_weight / grad_bias
+ * _Partial; Figures 1 and 2: halo exchange, concat, local conv, crop) and of
+ * its Chinese write-up at kwkr.cn news/18980 (section 2.2: halo exchange,
+ * concat, crop, and in backward zero-padding plus exchange of grad_output;
+ * section 3.2: the exchange / local F.conv2d / crop override).  The W shards
+ * are virtual: equal column blocks of one tensor in one GPU's memory.  A shard
+ * reads its halo columns straight from its neighbours' blocks (zeros past the
+ * image edge); the per-shard _Partial gradients are summed in a fixed order.
+ *
+ * Conventions for every call:
+ *   - Tensors are fp32, NCHW, contiguous, in device memory, 16-byte aligned.
+ *     Weights are [C_out][C_in/groups][kh][kw]; bias and grad_bias [C_out].
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     allocates no device memory and does not synchronise, except in
+ *     hc_sync_check.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on it.
+ *   - Argument errors are returned before anything is launched.  A failed
+ *     launch returns HC_ERR_CUDA.  A kernel that gives up waiting records
+ *     HC_ERR_TIMEOUT in a device status word that hc_sync_check reports.
+ *   - Results are deterministic: no floating-point atomics; every sum has a
+ *     fixed order, so repeated calls give bit-identical outputs.
+ */
+#ifndef HC_H
+#define HC_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HC_OK = 0,
+    HC_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer  */
+    HC_ERR_UNSUPPORTED = 2,   /* valid convolution, but not a supported plan */
+    HC_ERR_WORKSPACE = 3,     /* workspace missing or too small              */
+    HC_ERR_CUDA = 4,          /* a CUDA call or launch failed                */
+    HC_ERR_TIMEOUT = 5        /* a kernel gave up waiting (see hc_sync_check)*/
+} hc_status;
+
+/* The convolution (input, weight, bias, stride, padding, groups -- the
+ * arguments of the _conv_forward override, kwkr.cn section 3.2) plus the
+ * number of W shards.  Square stride and padding; no dilation. */
+typedef struct {
+    int N, C_in, H, W, C_out, kh, kw, stride, padding, groups, num_shards;
+} hc_conv_desc;
+
+/* One shard of the plan: input columns [in_begin, in_end) (its Shard(3)
+ * block), halo_left / halo_right columns read from the neighbouring blocks,
+ * and the output columns [out_begin, out_end) it owns after the crop. */
+typedef struct {
+    int in_begin, in_end, halo_left, halo_right, out_begin, out_end;
+} hc_shard_extent;
+
+/* Kernel families; HC_ALGO_AUTO picks the fastest one that supports the desc. */
+typedef enum {
+    HC_ALGO_AUTO = 0,
+    HC_ALGO_DIRECT = 1,       /* plain direct convolution, any groups / stride  */
+    HC_ALGO_DEPTHWISE = 2,    /* groups == C, odd k, stride 1, padding (k-1)/2  */
+    HC_ALGO_TC_3XTF32 = 3     /* groups == 1: tcgen05 implicit GEMM, 3xTF32     */
+} hc_algo;
+
+/* Shard(3) plan (NVIDIA blog, design section; kwkr.cn 2.1 and 2.2).
+ * W is split into num_shards blocks of Wl = W / num_shards columns.  Shard r
+ * owns input columns [r*Wl, (r+1)*Wl) and output columns
+ * [r*Wl/stride, (r+1)*Wl/stride) (the last shard also takes output columns
+ * past W/stride).  halo_left is the number of columns left of its block that
+ * its owned outputs read (padding for the layouts here), halo_right the number
+ * right of it (k - padding - stride when positive): for the pages' 5x5 /
+ * padding 2 / stride 1 example, 2 and 2.
+ *   ext   out: num_shards entries (caller-owned host memory).
+ *   H_out, W_out  out (may be NULL): output size, (in + 2p - k) / s + 1.
+ * Returns HC_ERR_INVALID_ARG for an invalid convolution, HC_ERR_UNSUPPORTED
+ * when W % num_shards, Wl % stride or padding % stride is non-zero, or when a
+ * halo is wider than Wl (a halo may only come from the adjacent shards). */
+hc_status hc_shard_plan(const hc_conv_desc* d, hc_shard_extent* ext, int* H_out, int* W_out);
+
+/* Workspace bytes that hc_conv2d_fwd (pass 0) or hc_conv2d_bwd (pass 1) needs
+ * for this desc with HC_ALGO_AUTO (use hc_conv2d_workspace_size_algo for a
+ * fixed algorithm).  Zero is a valid answer; ws may then be NULL. */
+hc_status hc_conv2d_workspace_size(const hc_conv_desc* d, int pass, size_t* bytes);
+hc_status hc_conv2d_workspace_size_algo(const hc_conv_desc* d, int pass, hc_algo algo, size_t* bytes);
+
+/* Which algorithm HC_ALGO_AUTO runs for this desc and pass. */
+hc_status hc_conv2d_select(const hc_conv_desc* d, int pass, hc_algo* algo);
+
+/* Forward (NVIDIA blog Figure 1; kwkr.cn 2.2 steps 1-3 and 3.2): per shard,
+ * halo exchange + concat, local conv, crop to the owned output columns; the
+ * shards' outputs together form y (Shard(3)).
+ *   x    [N][C_in][H][W]           in
+ *   w    [C_out][C_in/groups][kh][kw] in (Replicate)
+ *   bias [C_out] or NULL           in
+ *   y    [N][C_out][H_out][W_out]  out
+ *   ws, ws_bytes: workspace of at least hc_conv2d_workspace_size(d, 0) bytes. */
+hc_status hc_conv2d_fwd(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                        void* ws, size_t ws_bytes, void* stream);
+hc_status hc_conv2d_fwd_algo(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                             void* ws, size_t ws_bytes, void* stream, hc_algo algo);
+
+/* Backward (NVIDIA blog design section and Figure 2; kwkr.cn 2.2): per shard,
+ * the grad_output block is extended by the halo of its neighbours' grad_output
+ * (zeros past the image edge), grad_input of the owned input columns is the
+ * local transposed conv, and the shard's _Partial grad_weight / grad_bias are
+ * the local sums over its own output columns.  The partials are then summed
+ * over shards in shard order (the pages' cross-device reduce-sum).
+ *   x, w, gy   in ([N][C_out][H_out][W_out] for gy)
+ *   gx         out [N][C_in][H][W], or NULL to skip
+ *   gw         out [C_out][C_in/groups][kh][kw], or NULL to skip
+ *   gb         out [C_out], or NULL to skip
+ *   gw_partials out [num_shards][C_out][C_in/groups][kh][kw], or NULL
+ *   gb_partials out [num_shards][C_out], or NULL
+ *   ws, ws_bytes: workspace of at least hc_conv2d_workspace_size(d, 1) bytes. */
+hc_status hc_conv2d_bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
+                        float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes, void* stream);
+hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                             float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
+                             void* stream, hc_algo algo);
+
+/* Halo exchange + concat made explicit (kwkr.cn 2.2 steps 1-2): for every
+ * shard r, x_ext[r] = [left halo | own block | right halo] of x, zeros past
+ * the image edge.  x_ext is [num_shards][N][C_in][H][We] with
+ * We = max over shards of halo_left + Wl + halo_right; a shard with narrower
+ * halos leaves its unused trailing columns zero.  A pure copy (bit-exact). */
+hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream);
+
+/* Synchronises `stream`, then returns (and clears) the first error a kernel
+ * recorded in the device status word, HC_ERR_CUDA for an asynchronous CUDA
+ * error, or HC_OK. */
+hc_status hc_sync_check(void* stream);
+
+/* Static English text for a status code. */
+const char* hc_status_string(hc_status s);
+
+/* Number of kernels this library has launched since it was loaded. */
+unsigned long long hc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_H */

@@ -1,0 +1,256 @@
+// api.cu -- the C ABI: argument checks, the shard plan, algorithm choice,
+// workspace layout and dispatch to the kernels.  Host code only.
+#include <string.h>
+
+#include "common.cuh"
+
+namespace hc {
+
+std::atomic<unsigned long long> g_launches{0};
+
+static int out_size(int in, int k, int s, int p) {
+    const int span = in + 2 * p - k;
+    return span < 0 ? 0 : span / s + 1;
+}
+
+static bool desc_valid(const hc_conv_desc* d) {
+    if (!d) return false;
+    if (d->N <= 0 || d->C_in <= 0 || d->H <= 0 || d->W <= 0 || d->C_out <= 0) return false;
+    if (d->kh <= 0 || d->kw <= 0 || d->stride <= 0 || d->padding < 0 || d->groups <= 0) return false;
+    if (d->num_shards <= 0) return false;
+    if (d->C_in % d->groups || d->C_out % d->groups) return false;
+    if (out_size(d->H, d->kh, d->stride, d->padding) <= 0) return false;
+    if (out_size(d->W, d->kw, d->stride, d->padding) <= 0) return false;
+    // every tensor must stay below 2^31 elements per (n, c) plane and 2^40 overall
+    const double elems = (double)d->N * d->C_in * d->H * d->W;
+    return elems < 1.0e12;
+}
+
+// Shard(3) plan.  Shard r owns input block [r*Wl, (r+1)*Wl) and output
+// columns [r*Wl/s, (r+1)*Wl/s) (the last shard up to W_out); its halos are
+// the columns outside its block that those outputs read.
+hc_status make_plan(const hc_conv_desc* d, Plan* p) {
+    if (!desc_valid(d)) return HC_ERR_INVALID_ARG;
+    const int S = d->num_shards, s = d->stride, pad = d->padding;
+    if (S > kMaxShards) return HC_ERR_UNSUPPORTED;
+    if (d->W % S) return HC_ERR_UNSUPPORTED;
+    const int Wl = d->W / S;
+    if (Wl % s || pad % s) return HC_ERR_UNSUPPORTED;
+    p->S = S;
+    p->Wl = Wl;
+    p->Ho = out_size(d->H, d->kh, s, pad);
+    p->Wo = out_size(d->W, d->kw, s, pad);
+    p->We = 0;
+    for (int r = 0; r < S; r++) {
+        hc_shard_extent e;
+        e.in_begin = r * Wl;
+        e.in_end = (r + 1) * Wl;
+        e.out_begin = r * (Wl / s);
+        e.out_end = (r == S - 1) ? p->Wo : (r + 1) * (Wl / s);
+        if (e.out_end > p->Wo) e.out_end = p->Wo;
+        if (e.out_begin > e.out_end) e.out_begin = e.out_end;
+        e.halo_left = e.halo_right = 0;
+        if (e.out_end > e.out_begin) {
+            const int lo = e.out_begin * s - pad;
+            const int hi = (e.out_end - 1) * s - pad + d->kw;  // one past the last column read
+            if (lo < e.in_begin) e.halo_left = e.in_begin - lo;
+            if (hi > e.in_end) e.halo_right = hi - e.in_end;
+        }
+        if (e.halo_left > Wl || e.halo_right > Wl) return HC_ERR_UNSUPPORTED;
+        const int we = e.halo_left + Wl + e.halo_right;
+        if (we > p->We) p->We = we;
+        p->ext[r] = e;
+    }
+    return HC_OK;
+}
+
+static bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
+
+static size_t wsize(const hc_conv_desc* d) {
+    return (size_t)d->C_out * (d->C_in / d->groups) * d->kh * d->kw;
+}
+
+static size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+static bool algo_supported(const hc_conv_desc* d, const Plan& p, hc_algo a) {
+    switch (a) {
+        case HC_ALGO_DIRECT: return true;
+        case HC_ALGO_DEPTHWISE: return depthwise_supported(d, p);
+        default: return false;
+    }
+}
+
+static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
+    if (depthwise_supported(d, p)) return HC_ALGO_DEPTHWISE;
+    return HC_ALGO_DIRECT;
+}
+
+// Workspace layout of the backward pass (bytes, each piece 256-aligned):
+//   DIRECT:    [gw partials S*wsize][gb partials S*C_out]
+//   DEPTHWISE: [gw partials S*C*K*K][gb partials S*C][tile partials]
+static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
+    size_t b = round256(sizeof(float) * p.S * wsize(d)) + round256(sizeof(float) * p.S * d->C_out);
+    if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
+    return b;
+}
+
+static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* bytes) {
+    if (!bytes || (pass != 0 && pass != 1)) return HC_ERR_INVALID_ARG;
+    Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    if (a == HC_ALGO_AUTO) a = pick(d, p);
+    if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
+    *bytes = pass == 0 ? 0 : bwd_ws_bytes(d, p, a);
+    return HC_OK;
+}
+
+static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, const float* b, float* y, void* ws,
+                     size_t ws_bytes, void* stream, hc_algo a) {
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y) || (b && !aligned16(b)))
+        return HC_ERR_INVALID_ARG;
+    if (a == HC_ALGO_AUTO) a = pick(d, p);
+    if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
+    (void)ws;
+    (void)ws_bytes;
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (a) {
+        case HC_ALGO_DEPTHWISE: return launch_depthwise_fwd(d, p, x, w, b, y, s);
+        case HC_ALGO_DIRECT: return launch_direct_fwd(d, p, x, w, b, y, s);
+        default: return HC_ERR_UNSUPPORTED;
+    }
+}
+
+static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
+                     float* gb, float* gwp_out, float* gbp_out, void* ws, size_t ws_bytes, void* stream,
+                     hc_algo a) {
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    if (!x || !w || !gy || !aligned16(x) || !aligned16(w) || !aligned16(gy)) return HC_ERR_INVALID_ARG;
+    for (const void* q : {(const void*)gx, (const void*)gw, (const void*)gb, (const void*)gwp_out,
+                          (const void*)gbp_out})
+        if (q && !aligned16(q)) return HC_ERR_INVALID_ARG;
+    if (a == HC_ALGO_AUTO) a = pick(d, p);
+    if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
+    const size_t need = bwd_ws_bytes(d, p, a);
+    if (ws_bytes < need || (need && !ws) || !aligned16(ws)) return HC_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* wsp = (char*)ws;
+    float* gwp = (float*)wsp;
+    wsp += round256(sizeof(float) * p.S * wsize(d));
+    float* gbp = (float*)wsp;
+    wsp += round256(sizeof(float) * p.S * d->C_out);
+    if (gwp_out) gwp = gwp_out;
+    if (gbp_out) gbp = gbp_out;
+    const bool want_w = gw || gwp_out;
+    const bool want_b = gb || gbp_out;
+    switch (a) {
+        case HC_ALGO_DEPTHWISE:
+            st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s);
+            break;
+        case HC_ALGO_DIRECT:
+            if (gx && (st = launch_direct_gx(d, p, w, gy, gx, s))) return st;
+            if (want_w || want_b)
+                st = launch_direct_partials(d, p, x, gy, want_w ? gwp : nullptr, want_b ? gbp : nullptr, s);
+            break;
+        default: return HC_ERR_UNSUPPORTED;
+    }
+    if (st) return st;
+    // _Partial -> full: sum the shards' partials in shard order.
+    if (gw && (st = launch_sum_rows(gwp, gw, p.S, (long long)wsize(d), s))) return st;
+    if (gb && (st = launch_sum_rows(gbp, gb, p.S, d->C_out, s))) return st;
+    return HC_OK;
+}
+
+}  // namespace hc
+
+using namespace hc;
+
+extern "C" {
+
+hc_status hc_shard_plan(const hc_conv_desc* d, hc_shard_extent* ext, int* H_out, int* W_out) {
+    if (!d || !ext) return HC_ERR_INVALID_ARG;
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    memcpy(ext, p.ext, sizeof(hc_shard_extent) * p.S);
+    if (H_out) *H_out = p.Ho;
+    if (W_out) *W_out = p.Wo;
+    return HC_OK;
+}
+
+hc_status hc_conv2d_workspace_size(const hc_conv_desc* d, int pass, size_t* bytes) {
+    return ws_size(d, pass, HC_ALGO_AUTO, bytes);
+}
+
+hc_status hc_conv2d_workspace_size_algo(const hc_conv_desc* d, int pass, hc_algo algo, size_t* bytes) {
+    return ws_size(d, pass, algo, bytes);
+}
+
+hc_status hc_conv2d_select(const hc_conv_desc* d, int pass, hc_algo* algo) {
+    if (!algo || (pass != 0 && pass != 1)) return HC_ERR_INVALID_ARG;
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    *algo = pick(d, p);
+    return HC_OK;
+}
+
+hc_status hc_conv2d_fwd(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                        void* ws, size_t ws_bytes, void* stream) {
+    return fwd(d, x, w, bias, y, ws, ws_bytes, stream, HC_ALGO_AUTO);
+}
+
+hc_status hc_conv2d_fwd_algo(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                             void* ws, size_t ws_bytes, void* stream, hc_algo algo) {
+    return fwd(d, x, w, bias, y, ws, ws_bytes, stream, algo);
+}
+
+hc_status hc_conv2d_bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
+                        float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes, void* stream) {
+    return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, HC_ALGO_AUTO);
+}
+
+hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                             float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
+                             void* stream, hc_algo algo) {
+    return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo);
+}
+
+hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream) {
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    if (!x || !x_ext) return HC_ERR_INVALID_ARG;
+    if (p.S > kMaxKernelShards) return HC_ERR_UNSUPPORTED;
+    return launch_halo_gather(d, p, x, x_ext, (cudaStream_t)stream);
+}
+
+hc_status hc_sync_check(void* stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+    }
+    if (cudaGetLastError() != cudaSuccess) return HC_ERR_CUDA;
+    return HC_OK;
+}
+
+const char* hc_status_string(hc_status s) {
+    switch (s) {
+        case HC_OK: return "ok";
+        case HC_ERR_INVALID_ARG: return "invalid argument";
+        case HC_ERR_UNSUPPORTED: return "unsupported shard plan or convolution";
+        case HC_ERR_WORKSPACE: return "workspace missing or too small";
+        case HC_ERR_CUDA: return "CUDA error";
+        case HC_ERR_TIMEOUT: return "a kernel gave up waiting";
+    }
+    return "unknown status";
+}
+
+unsigned long long hc_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

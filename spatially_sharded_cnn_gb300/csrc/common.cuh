@@ -1,0 +1,62 @@
+// common.cuh -- internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "hc.h"
+
+namespace hc {
+
+constexpr int kMaxShards = 1024;     // host-side plan
+constexpr int kMaxKernelShards = 64; // shards a kernel takes per-shard tables for
+
+// Host-side shard plan (see hc_shard_plan): uniform block width Wl; the
+// per-shard halo widths and owned output columns.
+struct Plan {
+    int S = 0, Wl = 0, Ho = 0, Wo = 0;
+    int We = 0;  // widest extended tile: max_r(halo_left + Wl + halo_right)
+    hc_shard_extent ext[kMaxShards];
+};
+
+hc_status make_plan(const hc_conv_desc* d, Plan* p);
+
+// Count of kernel launches issued by the library.
+extern std::atomic<unsigned long long> g_launches;
+
+inline hc_status launched() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaPeekAtLastError() == cudaSuccess ? HC_OK : (cudaGetLastError(), HC_ERR_CUDA);
+}
+
+inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
+
+// ---- kernel launchers (one translation unit each) -------------------------
+hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* x, float* x_ext, cudaStream_t st);
+
+// direct (any groups, stride, padding)
+hc_status launch_direct_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                            float* y, cudaStream_t st);
+hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w, const float* gy, float* gx,
+                           cudaStream_t st);
+// per-shard partials gw_part [S][C_out][C_in/g][kh][kw], gb_part [S][C_out] (either may be null)
+hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
+                                 float* gw_part, float* gb_part, cudaStream_t st);
+
+// depthwise K x K, stride 1, padding (K-1)/2, 128-column tiles inside a shard
+bool depthwise_supported(const hc_conv_desc* d, const Plan& p);
+size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p);
+hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
+                               const float* b, float* y, cudaStream_t st);
+// tile partials go to ws; then reduced to shard partials gwp / gbp ([S][C][K*K], [S][C])
+hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
+                               const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
+                               bool want_weight_grads, cudaStream_t st);
+
+// fixed-order sums
+// out[k] = sum_{r < rows} in[r * count + k], r ascending
+hc_status launch_sum_rows(const float* in, float* out, int rows, long long count, cudaStream_t st);
+
+}  // namespace hc

@@ -1,0 +1,191 @@
+// direct.cu -- plain direct convolution for any groups, stride and padding:
+// the general path the specialised kernels are measured against, and the one
+// used for layouts they do not cover.
+//
+// Sharding (NVIDIA blog "Perception model training for autonomous vehicles
+// with tensor parallelism", design section; kwkr.cn news/18980 section 2.2):
+// an output column owned by shard r reads its halo columns directly from the
+// neighbouring shards' blocks of x (zeros past the image edge); the weight and
+// bias gradients are produced per shard (_Partial) over the shard's own output
+// columns and summed afterwards in shard order.
+#include "common.cuh"
+
+namespace hc {
+namespace {
+
+struct ConvDims {
+    int N, Ci, H, W, Co, kh, kw, s, p, Cgi, Cgo, Ho, Wo;
+};
+
+ConvDims dims_of(const hc_conv_desc* d, const Plan& pl) {
+    return ConvDims{d->N, d->C_in, d->H, d->W, d->C_out, d->kh, d->kw, d->stride, d->padding,
+                    d->C_in / d->groups, d->C_out / d->groups, pl.Ho, pl.Wo};
+}
+
+unsigned grid_for(long long n, int threads) {
+    const long long b = (n + threads - 1) / threads;
+    return (unsigned)(b < 152LL * 32 ? b : 152LL * 32);
+}
+
+// y[n,co,i,j] = b[co] + sum_{ci',u,v} w[co,ci',u,v] * x[n,ci,i*s-p+u,j*s-p+v]
+__global__ void direct_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                  const float* __restrict__ b, float* __restrict__ y, ConvDims D) {
+    const long long total = (long long)D.N * D.Co * D.Ho * D.Wo;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(q % D.Wo);
+        const int i = (int)((q / D.Wo) % D.Ho);
+        const int co = (int)((q / ((long long)D.Wo * D.Ho)) % D.Co);
+        const int n = (int)(q / ((long long)D.Wo * D.Ho * D.Co));
+        const int ci0 = (co / D.Cgo) * D.Cgi;
+        float acc = b ? __ldg(b + co) : 0.0f;
+        for (int cl = 0; cl < D.Cgi; cl++) {
+            const float* xp = x + ((long long)n * D.Ci + ci0 + cl) * D.H * D.W;
+            const float* wp = w + ((long long)co * D.Cgi + cl) * D.kh * D.kw;
+            for (int u = 0; u < D.kh; u++) {
+                const int h = i * D.s - D.p + u;
+                if (h < 0 || h >= D.H) continue;
+                for (int v = 0; v < D.kw; v++) {
+                    const int c = j * D.s - D.p + v;
+                    if (c < 0 || c >= D.W) continue;
+                    acc = fmaf(__ldg(wp + u * D.kw + v), __ldg(xp + (long long)h * D.W + c), acc);
+                }
+            }
+        }
+        y[q] = acc;
+    }
+}
+
+// gx[n,ci,h,c] = sum over (co in the group, u, v) with (h+p-u) and (c+p-v)
+// divisible by s of w[co,ci',u,v] * gy[n,co,(h+p-u)/s,(c+p-v)/s]
+__global__ void direct_gx_kernel(const float* __restrict__ w, const float* __restrict__ gy, float* __restrict__ gx,
+                                 ConvDims D) {
+    const long long total = (long long)D.N * D.Ci * D.H * D.W;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(q % D.W);
+        const int h = (int)((q / D.W) % D.H);
+        const int ci = (int)((q / ((long long)D.W * D.H)) % D.Ci);
+        const int n = (int)(q / ((long long)D.W * D.H * D.Ci));
+        const int g = ci / D.Cgi, cl = ci % D.Cgi;
+        float acc = 0.0f;
+        for (int co = g * D.Cgo; co < (g + 1) * D.Cgo; co++) {
+            const float* gp = gy + ((long long)n * D.Co + co) * D.Ho * D.Wo;
+            const float* wp = w + ((long long)co * D.Cgi + cl) * D.kh * D.kw;
+            for (int u = 0; u < D.kh; u++) {
+                const int ti = h + D.p - u;
+                if (ti < 0 || ti % D.s) continue;
+                const int i = ti / D.s;
+                if (i >= D.Ho) continue;
+                for (int v = 0; v < D.kw; v++) {
+                    const int tj = c + D.p - v;
+                    if (tj < 0 || tj % D.s) continue;
+                    const int j = tj / D.s;
+                    if (j >= D.Wo) continue;
+                    acc = fmaf(__ldg(wp + u * D.kw + v), __ldg(gp + (long long)i * D.Wo + j), acc);
+                }
+            }
+        }
+        gx[q] = acc;
+    }
+}
+
+// Fixed-order block reduction: warp shuffle tree, then warp 0 adds the
+// per-warp sums in warp order.  Result valid in thread 0.
+__device__ float block_sum(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.0f;
+    if (threadIdx.x == 0)
+        for (int k = 0; k < (int)(blockDim.x >> 5); k++) t += red[k];
+    __syncthreads();
+    return t;
+}
+
+// One block per (weight element, shard): the shard's _Partial gradient
+//   gw_part[r, co, ci', u, v] = sum_{n, i, j in own(r)} gy[n,co,i,j] * x[n,ci,i*s-p+u,j*s-p+v]
+__global__ void direct_gw_partial_kernel(const float* __restrict__ x, const float* __restrict__ gy,
+                                         float* __restrict__ gw_part, ConvDims D, long long wsz, int S, int own_w,
+                                         int last_end) {
+    __shared__ float red[32];
+    const long long k = blockIdx.x;
+    const int r = blockIdx.y;
+    const int v = (int)(k % D.kw);
+    const int u = (int)((k / D.kw) % D.kh);
+    const int cl = (int)((k / ((long long)D.kw * D.kh)) % D.Cgi);
+    const int co = (int)(k / ((long long)D.kw * D.kh * D.Cgi));
+    const int ci = (co / D.Cgo) * D.Cgi + cl;
+    const int j0 = r * own_w, j1 = (r == S - 1) ? last_end : j0 + own_w;
+    const int nj = j1 > j0 ? j1 - j0 : 0;
+    const long long terms = (long long)D.N * D.Ho * nj;
+    float acc = 0.0f;
+    for (long long q = threadIdx.x; q < terms; q += blockDim.x) {
+        const int j = j0 + (int)(q % nj);
+        const int i = (int)((q / nj) % D.Ho);
+        const int n = (int)(q / ((long long)nj * D.Ho));
+        const int h = i * D.s - D.p + u, c = j * D.s - D.p + v;
+        if (h < 0 || h >= D.H || c < 0 || c >= D.W) continue;
+        acc = fmaf(__ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j),
+                   __ldg(x + (((long long)n * D.Ci + ci) * D.H + h) * D.W + c), acc);
+    }
+    const float t = block_sum(acc, red);
+    if (threadIdx.x == 0) gw_part[(long long)r * wsz + k] = t;
+}
+
+// gb_part[r, co] = sum_{n, i, j in own(r)} gy[n,co,i,j]
+__global__ void direct_gb_partial_kernel(const float* __restrict__ gy, float* __restrict__ gb_part, ConvDims D,
+                                         int S, int own_w, int last_end) {
+    __shared__ float red[32];
+    const int co = blockIdx.x, r = blockIdx.y;
+    const int j0 = r * own_w, j1 = (r == S - 1) ? last_end : j0 + own_w;
+    const int nj = j1 > j0 ? j1 - j0 : 0;
+    const long long terms = (long long)D.N * D.Ho * nj;
+    float acc = 0.0f;
+    for (long long q = threadIdx.x; q < terms; q += blockDim.x) {
+        const int j = j0 + (int)(q % nj);
+        const int i = (int)((q / nj) % D.Ho);
+        const int n = (int)(q / ((long long)nj * D.Ho));
+        acc += __ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j);
+    }
+    const float t = block_sum(acc, red);
+    if (threadIdx.x == 0) gb_part[(long long)r * D.Co + co] = t;
+}
+
+}  // namespace
+
+hc_status launch_direct_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                            float* y, cudaStream_t st) {
+    const ConvDims D = dims_of(d, p);
+    direct_fwd_kernel<<<grid_for((long long)D.N * D.Co * D.Ho * D.Wo, 256), 256, 0, st>>>(x, w, b, y, D);
+    return launched();
+}
+
+hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w, const float* gy, float* gx,
+                           cudaStream_t st) {
+    const ConvDims D = dims_of(d, p);
+    direct_gx_kernel<<<grid_for((long long)D.N * D.Ci * D.H * D.W, 256), 256, 0, st>>>(w, gy, gx, D);
+    return launched();
+}
+
+hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
+                                 float* gw_part, float* gb_part, cudaStream_t st) {
+    const ConvDims D = dims_of(d, p);
+    const long long wsz = (long long)D.Co * D.Cgi * D.kh * D.kw;
+    const int own_w = p.Wl / d->stride;
+    if (gw_part) {
+        if (wsz > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+        direct_gw_partial_kernel<<<dim3((unsigned)wsz, p.S), 256, 0, st>>>(x, gy, gw_part, D, wsz, p.S, own_w,
+                                                                           p.Wo);
+        hc_status s = launched();
+        if (s) return s;
+    }
+    if (gb_part) {
+        direct_gb_partial_kernel<<<dim3(D.Co, p.S), 256, 0, st>>>(gy, gb_part, D, p.S, own_w, p.Wo);
+        return launched();
+    }
+    return HC_OK;
+}
+
+}  // namespace hc

@@ -1,0 +1,154 @@
+"""Thin ctypes binding of libhc.so (include/hc.h), same names as the C ABI.
+
+Argument marshalling only: tensors may be given as torch tensors (their
+``data_ptr()`` is passed), as integer device addresses, or as None for a NULL
+pointer; a ``torch.cuda.Stream`` or an integer cudaStream_t selects the
+stream.  Every computation runs in the library's CUDA kernels; there is no
+fallback.  Importing this module raises ImportError when the library has not
+been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libhc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with spatially_sharded_cnn_gb300.build.build() "
+                      "(nvcc, sm_103a); there is no CPU fallback")
+
+_lib = C.CDLL(LIB_PATH)
+
+HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_TIMEOUT = range(6)
+HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32 = range(4)
+
+
+class hc_conv_desc(C.Structure):
+    _fields_ = [(n, C.c_int) for n in
+                ("N", "C_in", "H", "W", "C_out", "kh", "kw", "stride", "padding", "groups", "num_shards")]
+
+
+class hc_shard_extent(C.Structure):
+    _fields_ = [(n, C.c_int) for n in
+                ("in_begin", "in_end", "halo_left", "halo_right", "out_begin", "out_end")]
+
+
+class HcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {hc_status_string(status)} ({status})")
+        self.status = status
+
+
+def desc(cfg: dict) -> hc_conv_desc:
+    """hc_conv_desc from a dict with the field names of the C struct."""
+    return hc_conv_desc(*(int(cfg[k]) for k, _ in hc_conv_desc._fields_))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return C.c_void_p(t)
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return C.c_void_p(s)
+    return C.c_void_p(s.cuda_stream)
+
+
+_P = C.c_void_p
+_D = C.POINTER(hc_conv_desc)
+_lib.hc_shard_plan.argtypes = [_D, C.POINTER(hc_shard_extent), C.POINTER(C.c_int), C.POINTER(C.c_int)]
+_lib.hc_conv2d_workspace_size.argtypes = [_D, C.c_int, C.POINTER(C.c_size_t)]
+_lib.hc_conv2d_workspace_size_algo.argtypes = [_D, C.c_int, C.c_int, C.POINTER(C.c_size_t)]
+_lib.hc_conv2d_select.argtypes = [_D, C.c_int, C.POINTER(C.c_int)]
+_lib.hc_conv2d_fwd.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P]
+_lib.hc_conv2d_fwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
+_lib.hc_conv2d_bwd.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
+_lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
+_lib.hc_halo_gather.argtypes = [_D, _P, _P, _P]
+_lib.hc_sync_check.argtypes = [_P]
+_lib.hc_status_string.argtypes = [C.c_int]
+_lib.hc_status_string.restype = C.c_char_p
+_lib.hc_launch_count.restype = C.c_ulonglong
+for _n in ("hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo", "hc_conv2d_select",
+           "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
+           "hc_sync_check"):
+    getattr(_lib, _n).restype = C.c_int
+
+EXPORTS = [
+    "hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo", "hc_conv2d_select",
+    "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
+    "hc_sync_check", "hc_status_string", "hc_launch_count",
+]
+
+
+def hc_status_string(status: int) -> str:
+    return _lib.hc_status_string(int(status)).decode()
+
+
+def hc_shard_plan(d: hc_conv_desc):
+    """Returns (status, [extent tuples], H_out, W_out)."""
+    ext = (hc_shard_extent * max(1, d.num_shards))()
+    ho, wo = C.c_int(0), C.c_int(0)
+    st = _lib.hc_shard_plan(C.byref(d), ext, C.byref(ho), C.byref(wo))
+    if st:
+        return st, None, None, None
+    return st, [tuple(getattr(e, f) for f, _ in hc_shard_extent._fields_) for e in ext[:d.num_shards]], ho.value, wo.value
+
+
+def hc_conv2d_workspace_size(d: hc_conv_desc, pass_: int, algo: int | None = None):
+    """Returns (status, bytes)."""
+    b = C.c_size_t(0)
+    if algo is None:
+        st = _lib.hc_conv2d_workspace_size(C.byref(d), pass_, C.byref(b))
+    else:
+        st = _lib.hc_conv2d_workspace_size_algo(C.byref(d), pass_, int(algo), C.byref(b))
+    return st, b.value
+
+
+def hc_conv2d_select(d: hc_conv_desc, pass_: int):
+    a = C.c_int(0)
+    st = _lib.hc_conv2d_select(C.byref(d), pass_, C.byref(a))
+    return st, a.value
+
+
+def hc_conv2d_fwd(d, x, w, bias, y, ws=None, ws_bytes=0, stream=None, algo=None) -> int:
+    if algo is None:
+        return _lib.hc_conv2d_fwd(C.byref(d), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(ws), int(ws_bytes),
+                                  _stream(stream))
+    return _lib.hc_conv2d_fwd_algo(C.byref(d), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(ws), int(ws_bytes),
+                                   _stream(stream), int(algo))
+
+
+def hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None, ws=None, ws_bytes=0, stream=None,
+                  algo=None) -> int:
+    args = [C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw), _ptr(gb), _ptr(gw_partials),
+            _ptr(gb_partials), _ptr(ws), int(ws_bytes), _stream(stream)]
+    if algo is None:
+        return _lib.hc_conv2d_bwd(*args)
+    return _lib.hc_conv2d_bwd_algo(*args, int(algo))
+
+
+def hc_halo_gather(d, x, x_ext, stream=None) -> int:
+    return _lib.hc_halo_gather(C.byref(d), _ptr(x), _ptr(x_ext), _stream(stream))
+
+
+def hc_sync_check(stream=None) -> int:
+    return _lib.hc_sync_check(_stream(stream))
+
+
+def hc_launch_count() -> int:
+    return int(_lib.hc_launch_count())
+
+
+def check(status: int, what: str = "hc call") -> None:
+    """Raise HcError unless status is HC_OK."""
+    if status != HC_OK:
+        raise HcError(status, what)

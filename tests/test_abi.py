@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every function include/hc.h declares; the shard plan and the argument
+checks behave as documented."""
+import itertools
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle_pins as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hc():
+    from spatially_sharded_cnn_gb300 import build
+    build.build()
+    from spatially_sharded_cnn_gb300 import hc as mod
+    return mod
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(hc_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(hc):
+    names = declared_functions()
+    assert len(names) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", hc.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (hc_\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(hc._lib, n)
+    assert set(hc.EXPORTS) <= set(names)
+
+
+def test_status_strings(hc):
+    for s in range(6):
+        assert hc.hc_status_string(s) and hc.hc_status_string(s) != "unknown status"
+    assert hc.hc_status_string(99) == "unknown status"
+
+
+def test_plan_matches_oracle(hc, orc):
+    for W, S, k, s, p in itertools.product((8, 12, 16, 32, 48), (1, 2, 3, 4, 8), (1, 2, 3, 4, 5, 7),
+                                            (1, 2, 4), (0, 1, 2, 3)):
+        cfg = P.cfg_of(2, 3, 9, W, 3, k, s, p, 1, S)
+        if W + 2 * p < k:
+            continue
+        st, ext, Ho, Wo = hc.hc_shard_plan(hc.desc(cfg))
+        rc, plan, oHo, oWo = orc.shard_plan(cfg)
+        if rc:
+            assert st == hc.HC_ERR_UNSUPPORTED, (cfg, st, rc)
+            continue
+        assert st == hc.HC_OK, cfg
+        assert ext == plan and (Ho, Wo) == (oHo, oWo), cfg
+
+
+def test_plan_pages_example(hc):
+    # (7,3,512,2048) over 4 shards -> 4 blocks of 512 columns; 5x5/p2/s1 -> 2-column halos
+    st, ext, Ho, Wo = hc.hc_shard_plan(hc.desc(P.cfg_of(7, 3, 512, 2048, 3, 5, 1, 2, 1, 4)))
+    assert st == 0 and (Ho, Wo) == (512, 2048)
+    assert [e[1] - e[0] for e in ext] == [512] * 4
+    assert all(e[2] == 2 and e[3] == 2 for e in ext)
+
+
+def test_argument_errors_before_launch(hc):
+    d = hc.desc(P.cfg_of(1, 4, 16, 32, 4, 5, 1, 2, 1, 4))
+    # null tensors
+    assert hc.hc_conv2d_fwd(d, None, None, None, None) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_conv2d_bwd(d, None, None, None, None, None, None) == hc.HC_ERR_INVALID_ARG
+    # misaligned pointers (never dereferenced: the check comes first)
+    assert hc.hc_conv2d_fwd(d, 4, 16, None, 32) == hc.HC_ERR_INVALID_ARG
+    # invalid descs
+    for bad in (dict(N=0), dict(groups=3), dict(stride=0), dict(padding=-1), dict(num_shards=0), dict(kh=40)):
+        dd = hc.desc(dict(P.cfg_of(1, 4, 16, 32, 4, 5, 1, 2, 1, 4), **bad))
+        assert hc.hc_conv2d_fwd(dd, 256, 256, None, 256) == hc.HC_ERR_INVALID_ARG, bad
+        assert hc.hc_shard_plan(dd)[0] == hc.HC_ERR_INVALID_ARG, bad
+    # unsupported plans
+    for bad in (dict(num_shards=3), dict(W=10, num_shards=5, kh=7, kw=7, padding=3)):
+        dd = hc.desc(dict(P.cfg_of(1, 4, 16, 32, 4, 5, 1, 2, 1, 4), **bad))
+        assert hc.hc_conv2d_fwd(dd, 256, 256, None, 256) == hc.HC_ERR_UNSUPPORTED, bad
+    # an algorithm that does not cover the desc
+    assert hc.hc_conv2d_fwd(d, 256, 256, None, 256, algo=hc.HC_ALGO_DEPTHWISE) == hc.HC_ERR_UNSUPPORTED
+    # too small a workspace for the backward pass
+    st, nb = hc.hc_conv2d_workspace_size(d, 1)
+    assert st == 0 and nb > 0
+    assert hc.hc_conv2d_bwd(d, 256, 256, 256, 256, 256, 256, None, None, 256, nb - 1) == hc.HC_ERR_WORKSPACE
+
+
+def test_algorithm_choice(hc):
+    dw = hc.desc(P.cfg_of(7, 256, 128, 512, 256, 7, 1, 3, 256, 4))
+    assert hc.hc_conv2d_select(dw, 0) == (0, hc.HC_ALGO_DEPTHWISE)
+    assert hc.hc_conv2d_select(dw, 1) == (0, hc.HC_ALGO_DEPTHWISE)
+    small = hc.desc(P.cfg_of(1, 4, 16, 32, 4, 5, 1, 2, 1, 4))
+    st, a = hc.hc_conv2d_select(small, 0)
+    assert st == 0 and a in (hc.HC_ALGO_DIRECT, hc.HC_ALGO_TC_3XTF32)
+    # depthwise tiles are 128 columns inside a shard: 64-column shards fall back
+    odd = hc.desc(P.cfg_of(1, 8, 16, 256, 8, 7, 1, 3, 8, 4))
+    assert hc.hc_conv2d_select(odd, 0) == (0, hc.HC_ALGO_DIRECT)

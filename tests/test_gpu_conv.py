@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (normwise max relative error, max|gpu - oracle| / max|oracle| per
+output tensor): forward and grad_input 1e-5, grad_weight / grad_bias and their
+per-shard partials 1e-4.  Halo gathers and one-hot (delta) kernels on dyadic
+inputs must match bit for bit; two runs of the same call must be identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hc_run as R
+import oracle_pins as P
+from spatially_sharded_cnn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_FWD = 1e-5
+TOL_W = 1e-4
+
+
+@pytest.fixture(scope="module")
+def hc():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from spatially_sharded_cnn_gb300 import build
+    build.build()
+    from spatially_sharded_cnn_gb300 import hc as mod
+    return mod
+
+
+def config1():
+    """Dense 5x5 / s1 / p2, (1,4,16,32), 4 shards of width 8; seed 0."""
+    cfg = P.cfg_of(1, 4, 16, 32, 4, 5, 1, 2, 1, 4)
+    x = synth.uniform((1, 4, 16, 32), -1, 1, 0, 1)
+    w = synth.normal((4, 4, 5, 5), 0.1, 0, 2)
+    b = synth.normal((4,), 0.1, 0, 3)
+    gy = synth.normal((1, 4, 16, 32), 1.0, 0, 4)
+    return cfg, x, w, b, gy
+
+
+def dw_case(N, C, H, W, K, S, seed=1):
+    cfg = P.cfg_of(N, C, H, W, C, K, 1, (K - 1) // 2, C, S)
+    x = synth.normal((N, C, H, W), 1.0, seed, 1)
+    w = synth.trunc_normal((C, 1, K, K), 0.02, seed, 2)
+    b = synth.normal((C,), 0.1, seed, 3)
+    gy = synth.normal((N, C, H, W), 1.0, seed, 4)
+    return cfg, x, w, b, gy
+
+
+def generic_case(cfg, seed=2):
+    x, w, b, gy = P.rand_case(cfg, seed)
+    return cfg, x, w, b, gy
+
+
+CASES = {
+    "config1_dense5x5": config1,
+    "dw7_ragged_S4": lambda: dw_case(2, 3, 70, 512, 7, 4),
+    "dw7_S2_two_tiles_per_shard": lambda: dw_case(1, 2, 40, 512, 7, 2),
+    "dw7_S1": lambda: dw_case(1, 2, 33, 256, 7, 1),
+    "dw5_S2": lambda: dw_case(2, 2, 45, 256, 5, 2),
+    "dw3_S4": lambda: dw_case(1, 3, 31, 512, 3, 4),
+    "dw7_H1": lambda: dw_case(1, 2, 1, 256, 7, 2),
+    "dw7_narrow_shards_direct": lambda: dw_case(1, 4, 20, 64, 7, 4),
+    "grouped_strided": lambda: generic_case(P.cfg_of(2, 6, 12, 16, 4, 3, 2, 2, 2, 2)),
+    "stem4x4s4": lambda: generic_case(P.cfg_of(1, 3, 16, 64, 8, 4, 4, 0, 1, 4)),
+    "down2x2s2_S8": lambda: generic_case(P.cfg_of(1, 4, 8, 32, 6, 2, 2, 0, 1, 8)),
+    "pointwise1x1": lambda: generic_case(P.cfg_of(2, 5, 6, 16, 7, 1, 1, 0, 1, 2)),
+}
+
+
+def check_case(hc, orc, cfg, x, w, b, gy, algo=None):
+    y = R.fwd(cfg, x, w, b, algo)
+    ref = orc.conv2d_fwd(cfg, x, w, b)
+    assert R.normwise(y, ref) <= TOL_FWD, R.normwise(y, ref)
+    out = R.bwd(cfg, x, w, gy, algo)
+    gx_ref = orc.conv2d_bwd_input(cfg, w, gy)
+    gw_ref = orc.conv2d_bwd_weight(cfg, x, gy)
+    gb_ref = orc.conv2d_bwd_bias(cfg, gy)
+    assert R.normwise(out["gx"], gx_ref) <= TOL_FWD, R.normwise(out["gx"], gx_ref)
+    assert R.normwise(out["gw"], gw_ref) <= TOL_W, R.normwise(out["gw"], gw_ref)
+    assert R.normwise(out["gb"], gb_ref) <= TOL_W, R.normwise(out["gb"], gb_ref)
+    # per-shard _Partial values against the oracle's sharded backward
+    _, gwp_ref, gbp_ref = orc.sharded_bwd(cfg, x, w, gy)
+    assert R.normwise(out["gw_partials"], gwp_ref) <= TOL_W
+    assert R.normwise(out["gb_partials"], gbp_ref) <= TOL_W
+    return y, out
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity_auto(hc, orc, name):
+    check_case(hc, orc, *CASES[name]())
+
+
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "stem4x4s4"])
+def test_parity_direct(hc, orc, name):
+    check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_DIRECT)
+
+
+@pytest.mark.parametrize("name", ["dw7_ragged_S4", "dw5_S2", "dw3_S4"])
+def test_parity_depthwise_explicit(hc, orc, name):
+    cfg = CASES[name]()[0]
+    st, algo = hc.hc_conv2d_select(hc.desc(cfg), 1)
+    assert st == 0 and algo == hc.HC_ALGO_DEPTHWISE
+    check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_DEPTHWISE)
+
+
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided"])
+def test_deterministic(hc, name):
+    cfg, x, w, b, gy = CASES[name]()
+    y1, y2 = R.fwd(cfg, x, w, b), R.fwd(cfg, x, w, b)
+    o1, o2 = R.bwd(cfg, x, w, gy), R.bwd(cfg, x, w, gy)
+    assert np.array_equal(y1, y2)
+    for k in o1:
+        assert np.array_equal(o1[k], o2[k]), k
+
+
+@pytest.mark.parametrize("cfg", [P.cfg_of(2, 3, 5, 32, 3, 5, 1, 2, 1, 4), P.cfg_of(1, 2, 4, 48, 2, 7, 1, 3, 2, 4),
+                                 P.cfg_of(1, 2, 3, 16, 2, 3, 2, 2, 1, 2), P.cfg_of(1, 2, 3, 16, 2, 2, 2, 0, 1, 8)])
+def test_halo_gather_bit_exact(hc, orc, cfg):
+    x = synth.normal((cfg["N"], cfg["C_in"], cfg["H"], cfg["W"]), 1.0, 3, 1)
+    d = hc.desc(cfg)
+    st, plan, _, _ = hc.hc_shard_plan(d)
+    We = max(e[2] + (e[1] - e[0]) + e[3] for e in plan)
+    xe = R.Guarded((cfg["num_shards"], cfg["N"], cfg["C_in"], cfg["H"], We))
+    hc.check(hc.hc_halo_gather(d, R.dev(x), xe.view), "halo")
+    hc.check(hc.hc_sync_check(), "halo sync")
+    got = xe.numpy()
+    for r, e in enumerate(plan):
+        ref = orc.halo_extend(cfg, r, x)
+        wr = ref.shape[-1]
+        assert np.array_equal(got[r, ..., :wr], ref), r
+        assert np.all(got[r, ..., wr:] == 0)
+
+
+@pytest.mark.parametrize("K,S,groups", [(7, 4, "dw"), (5, 4, "dw"), (3, 2, "dw"), (5, 4, "dense"), (3, 2, "dense")])
+def test_delta_kernels_bit_exact(hc, K, S, groups):
+    """One-hot kernels on dyadic inputs: every output is one input value (or a
+    zero of the padding), so the result must be the shifted input exactly, at
+    every tap and across every shard edge."""
+    p = (K - 1) // 2
+    C = 2
+    W = 128 * S if groups == "dw" else 8 * S
+    cfg = P.cfg_of(1, C, 11, W, C, K, 1, p, C if groups == "dw" else 1, S)
+    x = synth.dyadic((1, C, 11, W), 6, 4, 5, 1)
+    xp = np.pad(x, ((0, 0), (0, 0), (p, p), (p, p)))
+    for u in range(K):
+        for v in range(K):
+            w = np.zeros((C, 1 if groups == "dw" else C, K, K), np.float32)
+            for c in range(C):
+                w[c, 0 if groups == "dw" else c, u, v] = 1.0
+            y = R.fwd(cfg, x, w, None)
+            assert np.array_equal(y, xp[:, :, u:u + 11, v:v + W]), (u, v)
+
+
+@pytest.mark.slow
+def test_config2_full_size_sampled(hc, orc):
+    """Depthwise 7x7, (7,256,128,512), 4 shards -- the size and launch the bench
+    times -- checked on sampled outputs that the oracle computes one by one:
+    random positions plus every shard-edge column of some rows."""
+    N, C, H, W, K, S = 7, 256, 128, 512, 7, 4
+    cfg = P.cfg_of(N, C, H, W, C, K, 1, 3, C, S)
+    x = synth.normal((N, C, H, W), 1.0, 0, 1)
+    w = synth.trunc_normal((C, 1, K, K), 0.02, 0, 2)
+    b = np.zeros((C,), np.float32)
+    gy = synth.normal((N, C, H, W), 1.0, 0, 4)
+    y = R.fwd(cfg, x, w, b)
+    out = R.bwd(cfg, x, w, gy)
+    rng = np.random.default_rng(0)
+    pts = [tuple(int(rng.integers(0, s)) for s in (N, C, H, W)) for _ in range(3000)]
+    for col in (0, 1, 2, 3, 125, 126, 127, 128, 129, 130, 255, 256, 257, 383, 384, 385, 509, 510, 511):
+        for hrow in (0, 1, 2, 64, 125, 126, 127):
+            pts.append((int(rng.integers(0, N)), int(rng.integers(0, C)), hrow, col))
+    yg = np.array([y[p] for p in pts])
+    yr = np.array([orc.fwd_at(cfg, x, w, b, *p) for p in pts])
+    assert R.normwise(yg, yr) <= TOL_FWD
+    gg = np.array([out["gx"][p] for p in pts])
+    gr = np.array([orc.gx_at(cfg, w, gy, *p) for p in pts])
+    assert R.normwise(gg, gr) <= TOL_FWD
+    chans = [0, 1, 100, 255]
+    gwp_ref = np.array([[[orc.gw_at(cfg, x, gy, c, 0, u, v, r * 128, (r + 1) * 128) for u in range(K) for v in range(K)]
+                         for c in chans] for r in range(S)])
+    gwp = out["gw_partials"][:, chans, 0].reshape(S, len(chans), K * K)
+    assert R.normwise(gwp, gwp_ref) <= TOL_W
+    assert R.normwise(out["gw"][chans, 0].reshape(len(chans), K * K), gwp_ref.sum(0)) <= TOL_W
+    gbp_ref = np.array([[orc.gb_at(cfg, gy, c, r * 128, (r + 1) * 128) for c in chans] for r in range(S)])
+    assert R.normwise(out["gb_partials"][:, chans], gbp_ref) <= TOL_W
+    assert R.normwise(out["gb"][chans], gbp_ref.sum(0)) <= TOL_W
+    # properties that hold at any size: sum over shards of the partials is the full gradient
+    assert np.abs(out["gw_partials"].astype(np.float64).sum(0) - out["gw"]).max() <= 1e-5 * np.abs(out["gw"]).max()
