@@ -130,6 +130,34 @@ hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float*
  * halos leaves its unused trailing columns zero.  A pure copy (bit-exact). */
 hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream);
 
+/* Depthwise backward that allocates nothing.  The pages have no counterpart:
+ * this entry point exists for callers that may not allocate device memory at
+ * the point of the call -- for example code running under another framework's
+ * memory allocator that forbids raw cudaMalloc, or a latency-critical loop that
+ * must not allocate after start-up (cudaMalloc can block and synchronise the
+ * device) -- and so cannot provide the workspace hc_conv2d_bwd takes.
+ *
+ * It computes exactly what hc_conv2d_bwd_algo(..., HC_ALGO_DEPTHWISE) computes
+ * (same kernels, same arguments minus the workspace), but keeps its scratch
+ * (the per-tile and per-shard partial weight / bias gradients) in a 16 MiB
+ * statically sized device array that lives in the library: every GPU that
+ * loads the library holds those 16 MiB until the process exits.  The caller
+ * still passes all inputs and outputs.
+ *   - Sizes whose scratch would exceed 16 MiB are rejected with
+ *     HC_ERR_WORKSPACE before anything is launched; so are descs the depthwise
+ *     kernels do not cover (HC_ERR_UNSUPPORTED).
+ *   - The first call on a device looks up that device's address of the array
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     every scratch value a call reads is written earlier in the same call, so
+ *     nothing needs clearing, but calls that overlap on the GPU (different
+ *     streams, or different host threads) race on it and must be serialised
+ *     by the caller. */
+hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, const float* x, const float* w, const float* gy,
+                                          float* gx, float* gw, float* gb, float* gw_partials, float* gb_partials,
+                                          void* stream);
+
 /* Synchronises `stream`, then returns (and clears) the first error a kernel
  * recorded in the device status word, HC_ERR_CUDA for an asynchronous CUDA
  * error, or HC_OK. */

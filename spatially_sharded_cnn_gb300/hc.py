@@ -73,6 +73,8 @@ _lib.hc_conv2d_fwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_
 _lib.hc_conv2d_bwd.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_halo_gather.argtypes = [_D, _P, _P, _P]
+_lib.hc_conv2d_bwd_depthwise_noalloc.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+_lib.hc_conv2d_bwd_depthwise_noalloc.restype = C.c_int
 _lib.hc_sync_check.argtypes = [_P]
 _lib.hc_status_string.argtypes = [C.c_int]
 _lib.hc_status_string.restype = C.c_char_p
@@ -85,7 +87,7 @@ for _n in ("hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_siz
 EXPORTS = [
     "hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo", "hc_conv2d_select",
     "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
-    "hc_sync_check", "hc_status_string", "hc_launch_count",
+    "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
 ]
 
 
@@ -134,6 +136,13 @@ def hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None, w
     if algo is None:
         return _lib.hc_conv2d_bwd(*args)
     return _lib.hc_conv2d_bwd_algo(*args, int(algo))
+
+
+def hc_conv2d_bwd_depthwise_noalloc(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None,
+                                    stream=None) -> int:
+    """Depthwise backward with library-owned scratch: no workspace argument."""
+    return _lib.hc_conv2d_bwd_depthwise_noalloc(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw),
+                                                _ptr(gb), _ptr(gw_partials), _ptr(gb_partials), _stream(stream))
 
 
 def hc_halo_gather(d, x, x_ext, stream=None) -> int:
