@@ -236,7 +236,7 @@ hc_status hc_sync_check(void* stream) {
         return HC_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return HC_ERR_CUDA;
-    return HC_OK;
+    return dw_take_status();
 }
 
 const char* hc_status_string(hc_status s) {

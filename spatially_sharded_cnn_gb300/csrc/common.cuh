@@ -1,6 +1,7 @@
 // common.cuh -- internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,16 @@ inline hc_status launched() {
 }
 
 inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
+
+// TMA descriptor for a tensor of `rank` dims (dims[0] innermost), strides in
+// bytes for dims 1..rank-1, zero fill out of bounds.
+hc_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Device status words of the kernels that wait on barriers: returns (and
+// clears) the first error recorded since the last call.  Call after the
+// stream has been synchronised.
+hc_status dw_take_status();
 
 // ---- kernel launchers (one translation unit each) -------------------------
 hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* x, float* x_ext, cudaStream_t st);

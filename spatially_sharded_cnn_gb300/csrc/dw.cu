@@ -2,84 +2,125 @@
 // the ConvNeXt depthwise layer the pages single out for the halo exchange
 // (kwkr.cn news/18980 sections 3.2 and 6.2).
 //
-// Tiling.  A CTA owns one (n, c) plane and one 128-column tile of it; tiles
-// never straddle a shard, so a tile at a shard edge takes its halo columns
-// from the neighbouring shard's block (the halo exchange of NVIDIA blog
-// "Perception model training for autonomous vehicles with tensor
-// parallelism", Figure 1), and zeros past the image edge.  The CTA walks down
-// the plane in 32-row tiles; each tile plus its halo (32 + K - 1 rows,
-// 128 + 8 columns) is staged in shared memory with cp.async, double buffered
-// so the next tile streams in while the current one is computed.  Only the
-// owned 128 columns are written (the crop).
+// Work items.  An item is one (n, c) plane x one 128-column tile of it.  Tiles
+// never straddle a shard, so a tile at a shard edge reads its halo columns from
+// the neighbouring shard's block (the halo exchange of NVIDIA blog "Perception
+// model training for autonomous vehicles with tensor parallelism", Figure 1)
+// and zeros past the image edge; only the tile's own 128 columns are written
+// (the crop).  Every CTA takes one contiguous range of items.  The forward
+// orders them (c, n, column tile), so a tile's horizontal neighbours run just
+// before and after it and its halo columns are L2 hits; the backward orders
+// them (c, column tile, n), so the weight gradient of one (c, column tile)
+// accumulates in registers across consecutive images.
+//
+// Kernels are persistent (a fixed number of CTAs per SM).  One thread streams the tiles in with
+// TMA (a 3-D box of rows h0-P .. h0+TH+P-1 and columns c0-4 .. c0+131 of one
+// plane; the box start is 16-byte aligned and out-of-image parts are
+// zero-filled by the copy engine) into a three-stage ring of shared-memory
+// buffers guarded by mbarriers; the next job's weights are fetched one job
+// ahead through shared memory.  Every barrier wait is bounded: a CTA that
+// gives up records HC_ERR_TIMEOUT in a status word (read by hc_sync_check),
+// waits for its own copies still in flight, and returns.
 //
 // Each thread computes an 8-row x 4-column block: per input row it reads 12
 // floats (three 16-byte shared loads) and issues up to 7 * 4 * K FMAs with the
-// plane's K*K weights held in registers.
+// plane's K*K weights in registers.
 //
-// Backward (one kernel): warps 0-3 compute grad_input (the same stencil over
-// the grad_output tile with the kernel flipped); warps 4-7 accumulate the
-// weight and bias gradients of the tile's own grad_output elements against
-// the input tile, keep them in registers over all the CTA's row tiles, and
-// finally reduce them across the four warps (warp shuffles, then a fixed-order
-// sum of the per-warp values) into one partial per (shard, c, tile, n).  A
-// second kernel sums those partials in a fixed order into the per-shard
-// _Partial gradients.
+// Backward (one kernel, every warp runs both phases on its own block):
+//   phase A  grad_input = the same stencil over the grad_output tile with the
+//            kernel flipped (gx[h][c] = sum_{u,v} w[K-1-u][K-1-v] gy[h+u-P][c+v-P]);
+//   phase B  weight / bias gradients of the block's own grad_output elements,
+//            gw[u][v] += gy[h][c] * x[h+u-P][c+v-P], accumulated in registers over
+//            all consecutive items of the same (c, column tile) and then reduced
+//            across the CTA (warp shuffles, then the per-warp sums in warp
+//            order) into one partial per run.
+// dw_shard_partials_kernel then sums the partials of each (shard, c) in a
+// fixed order: the per-shard _Partial gradients.
 #include "common.cuh"
 
 namespace hc {
 namespace {
 
-constexpr int TW = 128;       // tile width (columns)
-constexpr int TH = 32;        // tile height (rows)
-constexpr int SMW = TW + 8;   // staged row: 4 halo columns on each side
-constexpr int FWD_THREADS = 128;
-constexpr int BWD_THREADS = 256;
+constexpr int TW = 128;        // tile width (columns)
+constexpr int SMW = TW + 8;    // staged row: 4 halo columns on each side
+constexpr int FWD_WARPS = 8;   // forward: 64-row tiles, two CTAs per SM
+constexpr int FWD_CTAS = 2;
+constexpr int BWD_WARPS = 8;   // backward: 64-row tiles, one CTA per SM
+constexpr int NSTAGE = 3;      // depth of the shared-memory ring
+constexpr int WSLOT = 64;      // floats per weight slot (K*K weights + bias)
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 
-template <int K>
+__device__ int g_dw_status;
+
+template <int K, int WARPS>
 struct Geo {
     static constexpr int P = (K - 1) / 2;
-    static constexpr int R = TH + 2 * P;       // staged rows
-    static constexpr int TILE = R * SMW;       // floats per staged tile
+    static constexpr int TH = 8 * WARPS;                           // rows per tile
+    static constexpr int R = TH + 2 * P;                           // staged rows
+    static constexpr int TILE = ((R * SMW + 31) / 32) * 32;        // floats per buffer (128-byte multiple)
+    static constexpr unsigned BYTES = (unsigned)(R * SMW * 4);     // bytes one TMA box delivers
 };
 
-__device__ __forceinline__ void cp_async16(float* smem, const float* gmem, bool valid) {
-    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    const int n = valid ? 16 : 0;  // 0 source bytes: the 16 bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(gmem), "r"(n) : "memory");
+// ---- mbarrier / TMA helpers ------------------------------------------------
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
-// A load the compiler cannot repeat later: keeps the K*K weights resident in
-// registers instead of re-fetching them inside the unrolled stencil.
-__device__ __forceinline__ float ld_keep(const float* p) {
-    float v;
-    asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
-    return v;
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete, for at most kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+__device__ __forceinline__ void tma_load_3d(float* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
 }
 
-__device__ __forceinline__ void bar_all() { asm volatile("bar.sync 0, %0;\n" ::"n"(256) : "memory"); }
+// 4-byte asynchronous global -> shared copy (weights of the next job).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-
-// Stage rows [h0 - P, h0 + TH + P) and columns [c0 - 4, c0 + TW + 4) of one
-// plane; everything outside the image is zero.  W is a multiple of 4 and c0 of
-// 128, so every 16-byte piece is either fully inside or fully outside.
-template <int K>
-__device__ __forceinline__ void stage_tile(float* sm, const float* plane, int H, int W, int h0, int c0, int tid,
-                                           int nthr) {
-    constexpr int P = Geo<K>::P, R = Geo<K>::R, V = SMW / 4;
-    for (int q = tid; q < R * V; q += nthr) {
-        const int rr = q / V, cc = q - rr * V;
-        const int h = h0 - P + rr, c = c0 - 4 + 4 * cc;
-        const bool ok = h >= 0 && h < H && c >= 0 && c < W;
-        cp_async16(sm + rr * SMW + 4 * cc, ok ? plane + (long long)h * W + c : plane, ok);
+// A CTA that timed out: record it, then let thread 0 wait (bounded) for the
+// copies it issued and nobody consumed, so none lands after the CTA is gone.
+__device__ void give_up(uint64_t* full, int first_unconsumed, int issued) {
+    if (threadIdx.x == 0) {
+        atomicCAS(&g_dw_status, 0, (int)HC_ERR_TIMEOUT);
+        for (int j = first_unconsumed; j < issued; j++)
+            mbar_wait(full + (j % NSTAGE), (unsigned)((j / NSTAGE) & 1));
     }
 }
 
+// ---- the stencil ------------------------------------------------------------
 // acc[r][jj] += sum_{u,v} wt[u][v] * tile[row0 + r + u][4*lane + jj + v - P + 4]
 template <int K>
 __device__ __forceinline__ void stencil_8x4(const float* sm, int row0, int lane, const float (&wt)[K][K],
                                             float (&acc)[8][4]) {
-    constexpr int P = Geo<K>::P;
+    constexpr int P = (K - 1) / 2;
 #pragma unroll
     for (int i = 0; i < 8 + 2 * P; i++) {
         const float4* rp = reinterpret_cast<const float4*>(sm + (row0 + i) * SMW + 4 * lane);
@@ -98,210 +139,324 @@ __device__ __forceinline__ void stencil_8x4(const float* sm, int row0, int lane,
     }
 }
 
+// Half-block forms used by the backward: rows row0 .. row0+3 of the block.
 template <int K>
-__global__ void __launch_bounds__(FWD_THREADS, 4) dw_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                                                             const float* __restrict__ bias, float* __restrict__ y,
-                                                             int C, int H, int W, int col_tiles) {
-    extern __shared__ __align__(16) float smem[];
-    constexpr int TILE = Geo<K>::TILE;
-    const int plane = blockIdx.x / col_tiles;
-    const int c0 = (blockIdx.x - plane * col_tiles) * TW;
-    const int c = plane % C;
-    const float* xp = x + (long long)plane * H * W;
-    float* yp = y + (long long)plane * H * W;
+__device__ __forceinline__ void stencil_4x4(const float* sm, int row0, int lane, const float (&wt)[K][K],
+                                            float (&acc)[4][4]) {
+    constexpr int P = (K - 1) / 2;
+#pragma unroll
+    for (int i = 0; i < 4 + 2 * P; i++) {
+        const float4* rp = reinterpret_cast<const float4*>(sm + (row0 + i) * SMW + 4 * lane);
+        const float4 a = rp[0], b = rp[1], c = rp[2];
+        const float xs[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int u = i - r;
+            if (u >= 0 && u < K) {
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+                    for (int v = 0; v < K; v++) acc[r][jj] = fmaf(wt[u][v], xs[jj + v - P + 4], acc[r][jj]);
+            }
+        }
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void correlate_4x4(const float* sm, int row0, int lane, const float (&g)[4][4],
+                                              float (&gw)[K][K]) {
+    constexpr int P = (K - 1) / 2;
+#pragma unroll
+    for (int i = 0; i < 4 + 2 * P; i++) {
+        const float4* rp = reinterpret_cast<const float4*>(sm + (row0 + i) * SMW + 4 * lane);
+        const float4 a = rp[0], b = rp[1], c = rp[2];
+        const float xr[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int u = i - r;
+            if (u >= 0 && u < K) {
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+                    for (int v = 0; v < K; v++) gw[u][v] = fmaf(g[r][jj], xr[jj + v - P + 4], gw[u][v]);
+            }
+        }
+    }
+}
+
+struct Sched {
+    int N, C, H, W, col_tiles, items;
+    int tile_fastest;  // 1: items ordered (c, n, column tile); 0: (c, column tile, n)
+    __device__ __forceinline__ void decode(int item, int& n, int& c, int& ct) const {
+        if (tile_fastest) {
+            ct = item % col_tiles;
+            const int rest = item / col_tiles;
+            n = rest % N;
+            c = rest / N;
+        } else {
+            n = item % N;
+            const int rest = item / N;
+            ct = rest % col_tiles;
+            c = rest / col_tiles;
+        }
+    }
+    __device__ __forceinline__ void range(int& i0, int& i1) const {
+        i0 = (int)((long long)blockIdx.x * items / gridDim.x);
+        i1 = (int)((long long)(blockIdx.x + 1) * items / gridDim.x);
+    }
+};
+
+// ---- forward ----------------------------------------------------------------
+template <int K>
+__global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
+    dw_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ w,
+                  const float* __restrict__ bias, float* __restrict__ y, Sched sc) {
+    using G = Geo<K, FWD_WARPS>;
+    constexpr int P = G::P, TH = G::TH, KK = K * K;
+    extern __shared__ __align__(1024) float smem[];
+    float* tiles = smem;                              // [NSTAGE][TILE]
+    float* wsm = smem + NSTAGE * G::TILE;             // [2][WSLOT]
+    uint64_t* full = reinterpret_cast<uint64_t*>(wsm + 2 * WSLOT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int i0, i1;
+    sc.range(i0, i1);
+    if (i0 >= i1) return;
+    const int ntiles = (sc.H + TH - 1) / TH;
+    const int jobs = (i1 - i0) * ntiles;
+
+    auto issue = [&](int q) {
+        int n, c, ct;
+        sc.decode(i0 + q / ntiles, n, c, ct);
+        uint64_t* bar = full + (q % NSTAGE);
+        mbar_expect_tx(bar, G::BYTES);
+        tma_load_3d(tiles + (q % NSTAGE) * G::TILE, &xmap, ct * TW - 4, (q % ntiles) * TH - P, n * sc.C + c, bar);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
+        fence_barrier_init();
+    }
+    {
+        int n, c, ct;
+        sc.decode(i0, n, c, ct);
+        if (tid < KK) wsm[tid] = __ldg(w + c * KK + tid);
+        if (tid == KK) wsm[KK] = bias ? __ldg(bias + c) : 0.0f;
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
 
     float wt[K][K];
+    float bv = 0.0f;
+    int cur_c = -1;
+    for (int q = 0; q < jobs; q++) {
+        const int t = q % ntiles;
+        int n, c, ct;
+        sc.decode(i0 + q / ntiles, n, c, ct);
+        const bool has_next = q + 1 < jobs;
+        if (has_next && tid <= KK) {  // next job's weights, straight into shared memory
+            int nn, cn, ctn;
+            sc.decode(i0 + (q + 1) / ntiles, nn, cn, ctn);
+            float* dst = wsm + ((q + 1) & 1) * WSLOT + tid;
+            if (tid < KK)
+                cp_async4(dst, w + cn * KK + tid);
+            else if (bias)
+                cp_async4(dst, bias + cn);
+            else
+                *dst = 0.0f;
+        }
+        if (c != cur_c) {
+            const float* ws = wsm + (q & 1) * WSLOT;
 #pragma unroll
-    for (int u = 0; u < K; u++)
+            for (int u = 0; u < K; u++)
 #pragma unroll
-        for (int v = 0; v < K; v++) wt[u][v] = ld_keep(w + (c * K + u) * K + v);
-    const float bv = bias ? __ldg(bias + c) : 0.0f;
-
-    const int ntiles = (H + TH - 1) / TH;
-    stage_tile<K>(smem, xp, H, W, 0, c0, tid, FWD_THREADS);
-    cp_async_commit();
-    for (int t = 0; t < ntiles; t++) {
-        if (t + 1 < ntiles) stage_tile<K>(smem + ((t + 1) & 1) * TILE, xp, H, W, (t + 1) * TH, c0, tid, FWD_THREADS);
-        cp_async_commit();
-        cp_async_wait1();
-        __syncthreads();
-        const float* sm = smem + (t & 1) * TILE;
+                for (int v = 0; v < K; v++) wt[u][v] = ws[u * K + v];
+            bv = ws[KK];
+            cur_c = c;
+        }
+        const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
+        if (__syncthreads_or(!ok)) {
+            give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
+            return;
+        }
+        const float* sm = tiles + (q % NSTAGE) * G::TILE;
         float acc[8][4];
 #pragma unroll
         for (int r = 0; r < 8; r++)
 #pragma unroll
             for (int jj = 0; jj < 4; jj++) acc[r][jj] = bv;
         stencil_8x4<K>(sm, warp * 8, lane, wt, acc);
+        float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
 #pragma unroll
         for (int r = 0; r < 8; r++) {
             const int h = t * TH + warp * 8 + r;
-            if (h < H)
-                *reinterpret_cast<float4*>(yp + (long long)h * W + c0 + 4 * lane) =
+            if (h < sc.H)
+                *reinterpret_cast<float4*>(yp + (long long)h * sc.W) =
                     make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
-        __syncthreads();  // the buffer just read is refilled by the next iteration's prefetch
+        cp_async_wait_all();
+        __syncthreads();  // this job's buffer is free again; the next weights are in place
+        if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
     }
 }
 
+// ---- backward ---------------------------------------------------------------
 struct BwdArgs {
-    const float* x;
     const float* w;
-    const float* gy;
     float* gx;
     float* tile_part;
-    int N, C, H, W, col_tiles, tiles_per_shard, want_wb;
+    int tiles_per_shard;
+    int want_wb;
 };
 
-// Both roles run the same staging loop (every thread stages its share of
-// both tiles) and meet at the same CTA-wide barriers.
 template <int K>
-__device__ __forceinline__ void bwd_stage(const BwdArgs& a, float* smem, const float* gp, const float* xp, int t,
-                                          int s, int c0) {
-    constexpr int TILE = Geo<K>::TILE;
-    stage_tile<K>(smem + 2 * s * TILE, gp, a.H, a.W, t * TH, c0, threadIdx.x, BWD_THREADS);
-    if (a.want_wb) stage_tile<K>(smem + (2 * s + 1) * TILE, xp, a.H, a.W, t * TH, c0, threadIdx.x, BWD_THREADS);
-}
+__global__ void __launch_bounds__(BWD_WARPS * 32, 1)
+    dw_bwd_kernel(const __grid_constant__ CUtensorMap gymap, const __grid_constant__ CUtensorMap xmap, BwdArgs a,
+                  Sched sc) {
+    using G = Geo<K, BWD_WARPS>;
+    constexpr int P = G::P, TH = G::TH, KK = K * K;
+    extern __shared__ __align__(1024) float smem[];
+    float* tiles = smem;                              // [NSTAGE][gy, x][TILE]
+    float* wsm = smem + 2 * NSTAGE * G::TILE;         // [2][WSLOT]
+    float* red = wsm + 2 * WSLOT;                     // [BWD_WARPS][KK + 1]
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + BWD_WARPS * WSLOT);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int i0, i1;
+    sc.range(i0, i1);
+    if (i0 >= i1) return;
+    const int ntiles = (sc.H + TH - 1) / TH;
+    const int jobs = (i1 - i0) * ntiles;
+    const bool want_wb = a.want_wb != 0;
 
-// Warps 0-3: grad_input of the tile = the stencil over the grad_output tile
-// with the kernel flipped (gx[h][c] = sum_{u,v} w[K-1-u][K-1-v] gy[h+u-P][c+v-P]).
-template <int K>
-__device__ __forceinline__ void bwd_gx_role(const BwdArgs& a, float* smem, int plane, int c, int c0) {
-    constexpr int TILE = Geo<K>::TILE;
-    const float* gp = a.gy + (long long)plane * a.H * a.W;
-    const float* xp = a.x + (long long)plane * a.H * a.W;
-    float* gxp = a.gx ? a.gx + (long long)plane * a.H * a.W : nullptr;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float wf[K][K];
-#pragma unroll
-    for (int u = 0; u < K; u++)
-#pragma unroll
-        for (int v = 0; v < K; v++) wf[u][v] = ld_keep(a.w + (c * K + (K - 1 - u)) * K + (K - 1 - v));
-    const int ntiles = (a.H + TH - 1) / TH;
-    bwd_stage<K>(a, smem, gp, xp, 0, 0, c0);
-    cp_async_commit();
-    for (int t = 0; t < ntiles; t++) {
-        if (t + 1 < ntiles) bwd_stage<K>(a, smem, gp, xp, t + 1, (t + 1) & 1, c0);
-        cp_async_commit();
-        cp_async_wait1();
-        bar_all();
-        if (gxp) {
-            const float* gys = smem + 2 * (t & 1) * TILE;
-            float acc[8][4];
-#pragma unroll
-            for (int r = 0; r < 8; r++)
-#pragma unroll
-                for (int jj = 0; jj < 4; jj++) acc[r][jj] = 0.0f;
-            stencil_8x4<K>(gys, warp * 8, lane, wf, acc);
-#pragma unroll
-            for (int r = 0; r < 8; r++) {
-                const int h = t * TH + warp * 8 + r;
-                if (h < a.H)
-                    *reinterpret_cast<float4*>(gxp + (long long)h * a.W + c0 + 4 * lane) =
-                        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-            }
-        }
-        bar_all();
+    auto issue = [&](int q) {
+        int n, c, ct;
+        sc.decode(i0 + q / ntiles, n, c, ct);
+        uint64_t* bar = full + (q % NSTAGE);
+        float* st = tiles + (q % NSTAGE) * 2 * G::TILE;
+        mbar_expect_tx(bar, want_wb ? 2 * G::BYTES : G::BYTES);
+        const int x0 = ct * TW - 4, y0 = (q % ntiles) * TH - P, z = n * sc.C + c;
+        tma_load_3d(st, &gymap, x0, y0, z, bar);
+        if (want_wb) tma_load_3d(st + G::TILE, &xmap, x0, y0, z, bar);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
+        fence_barrier_init();
     }
-}
+    {
+        int n, c, ct;
+        sc.decode(i0, n, c, ct);
+        if (tid < KK) wsm[tid] = __ldg(a.w + c * KK + tid);
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
 
-// Warps 4-7: weight and bias gradients of the tile's own grad_output block,
-// gw[u][v] += gy[h][c] * x[h+u-P][c+v-P], kept in registers over all row
-// tiles, then reduced across the four warps into one partial.
-template <int K>
-__device__ __forceinline__ void bwd_gw_role(const BwdArgs& a, float* smem, int plane, int n, int c, int ct, int c0) {
-    constexpr int P = Geo<K>::P, TILE = Geo<K>::TILE, KK = K * K;
-    const float* gp = a.gy + (long long)plane * a.H * a.W;
-    const float* xp = a.x + (long long)plane * a.H * a.W;
-    const int wq = (threadIdx.x >> 5) - 4, lane = threadIdx.x & 31;
-    float gw[K][K];
+    float wf[K][K];  // flipped kernel
+    float gw[K][K];  // weight-gradient accumulators of the current run
+    float gbs = 0.0f;
 #pragma unroll
     for (int u = 0; u < K; u++)
 #pragma unroll
         for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
-    float gbs = 0.0f;
-    const int ntiles = (a.H + TH - 1) / TH;
-    bwd_stage<K>(a, smem, gp, xp, 0, 0, c0);
-    cp_async_commit();
-    for (int t = 0; t < ntiles; t++) {
-        if (t + 1 < ntiles) bwd_stage<K>(a, smem, gp, xp, t + 1, (t + 1) & 1, c0);
-        cp_async_commit();
-        cp_async_wait1();
-        bar_all();
-        if (a.want_wb) {
-            const float* gys = smem + 2 * (t & 1) * TILE;
-            const float* xs_t = gys + TILE;
-            // own grad_output block: tile rows wq*8 .. wq*8+7, columns 4*lane .. 4*lane+3
-            float g[8][4];
+    int cur_c = -1;
+    int run_n0 = -1;  // first image of the current (c, column tile) run
+    for (int q = 0; q < jobs; q++) {
+        const int t = q % ntiles;
+        int n, c, ct;
+        sc.decode(i0 + q / ntiles, n, c, ct);
+        if (run_n0 < 0) run_n0 = n;
+        const bool has_next = q + 1 < jobs;
+        int nn = 0, cn = c, ctn = ct;
+        if (has_next) sc.decode(i0 + (q + 1) / ntiles, nn, cn, ctn);
+        if (has_next && tid < KK) cp_async4(wsm + ((q + 1) & 1) * WSLOT + tid, a.w + cn * KK + tid);
+        if (c != cur_c) {
+            const float* ws = wsm + (q & 1) * WSLOT;
 #pragma unroll
-            for (int r = 0; r < 8; r++) {
-                const float4 q = *reinterpret_cast<const float4*>(gys + (P + wq * 8 + r) * SMW + 4 + 4 * lane);
-                g[r][0] = q.x;
-                g[r][1] = q.y;
-                g[r][2] = q.z;
-                g[r][3] = q.w;
-                gbs += (q.x + q.y) + (q.z + q.w);
-            }
+            for (int u = 0; u < K; u++)
 #pragma unroll
-            for (int i = 0; i < 8 + 2 * P; i++) {
-                const float4* rp = reinterpret_cast<const float4*>(xs_t + (wq * 8 + i) * SMW + 4 * lane);
-                const float4 p0 = rp[0], p1 = rp[1], p2 = rp[2];
-                const float xr[12] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w, p2.x, p2.y, p2.z, p2.w};
+                for (int v = 0; v < K; v++) wf[u][v] = ws[(K - 1 - u) * K + (K - 1 - v)];
+            cur_c = c;
+        }
+        const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
+        if (__syncthreads_or(!ok)) {
+            give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
+            return;
+        }
+        const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
+        const float* xs = gys + G::TILE;
+        if (a.gx) {  // phase A, in two 4-row halves (keeps the unrolled body small)
+            float* gp = a.gx + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+#pragma unroll 1
+            for (int half = 0; half < 2; half++) {
+                const int row0 = warp * 8 + 4 * half;
+                float acc[4][4];
 #pragma unroll
-                for (int r = 0; r < 8; r++) {
-                    const int u = i - r;
-                    if (u >= 0 && u < K) {
+                for (int r = 0; r < 4; r++)
 #pragma unroll
-                        for (int jj = 0; jj < 4; jj++)
+                    for (int jj = 0; jj < 4; jj++) acc[r][jj] = 0.0f;
+                stencil_4x4<K>(gys, row0, lane, wf, acc);
 #pragma unroll
-                            for (int v = 0; v < K; v++) gw[u][v] = fmaf(g[r][jj], xr[jj + v - P + 4], gw[u][v]);
-                    }
+                for (int r = 0; r < 4; r++) {
+                    const int h = t * TH + row0 + r;
+                    if (h < sc.H)
+                        *reinterpret_cast<float4*>(gp + (long long)h * sc.W) =
+                            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
                 }
             }
         }
-        bar_all();
-    }
-    if (!a.want_wb) return;
-    // shuffle tree inside each warp, then the four warp sums in warp order
-    float* red = smem;  // [4][KK + 1]; every staged tile has been consumed
+        if (want_wb) {  // phase B, in two 4-row halves
+#pragma unroll 1
+            for (int half = 0; half < 2; half++) {
+                const int row0 = warp * 8 + 4 * half;
+                float g[4][4];
 #pragma unroll
-    for (int u = 0; u < K; u++)
+                for (int r = 0; r < 4; r++) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(gys + (P + row0 + r) * SMW + 4 + 4 * lane);
+                    g[r][0] = v4.x;
+                    g[r][1] = v4.y;
+                    g[r][2] = v4.z;
+                    g[r][3] = v4.w;
+                    gbs += (v4.x + v4.y) + (v4.z + v4.w);
+                }
+                correlate_4x4<K>(xs, row0, lane, g, gw);
+            }
+            // flush at the end of a (c, column tile) run
+            const bool last_tile = t == ntiles - 1;
+            if (last_tile && (!has_next || cn != c || ctn != ct)) {
 #pragma unroll
-        for (int v = 0; v < K; v++) {
-            float s = gw[u][v];
+                for (int u = 0; u < K; u++)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) red[wq * (KK + 1) + u * K + v] = s;
+                    for (int v = 0; v < K; v++) {
+                        float s = gw[u][v];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                        if (lane == 0) red[warp * WSLOT + u * K + v] = s;
+                        gw[u][v] = 0.0f;
+                    }
+                float s = gbs;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0) red[warp * WSLOT + KK] = s;
+                gbs = 0.0f;
+                __syncthreads();
+                if (tid <= KK) {
+                    float tot = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + tid];
+                    const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
+                    float* slot = a.tile_part + (((long long)r * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
+                    for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + tid] = m == run_n0 ? tot : 0.0f;
+                }
+                run_n0 = -1;
+            }
         }
-    {
-        float s = gbs;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) red[wq * (KK + 1) + KK] = s;
-    }
-    asm volatile("bar.sync 1, 128;\n" ::: "memory");  // the four weight-role warps only
-    const int k = threadIdx.x - 128;
-    if (k <= KK) {
-        const float s = ((red[k] + red[(KK + 1) + k]) + red[2 * (KK + 1) + k]) + red[3 * (KK + 1) + k];
-        const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
-        a.tile_part[((((long long)r * a.C + c) * a.tiles_per_shard + tt) * a.N + n) * (KK + 1) + k] = s;
+        cp_async_wait_all();
+        __syncthreads();
+        if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
     }
 }
 
-template <int K>
-__global__ void __launch_bounds__(BWD_THREADS, 2) dw_bwd_kernel(BwdArgs a) {
-    extern __shared__ __align__(16) float smem[];
-    const int plane = blockIdx.x / a.col_tiles;
-    const int ct = blockIdx.x - plane * a.col_tiles;
-    const int n = plane / a.C, c = plane - n * a.C;
-    if (threadIdx.x < 128)
-        bwd_gx_role<K>(a, smem, plane, c, ct * TW);
-    else
-        bwd_gw_role<K>(a, smem, plane, n, c, ct, ct * TW);
-}
-
-// Shard partials: gwp[r][c][k] = sum over (tile tt, image n) of the tile
-// partials, tt then n ascending; gbp[r][c] likewise from the last slot.
+// Shard partials: gwp[r][c][k] = sum over (tile tt, image n) of the partials,
+// tt then n ascending; gbp[r][c] likewise from the last slot.
 __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, float* __restrict__ gwp,
                                          float* __restrict__ gbp, int S, int C, int rows, int KK) {
     const long long total = (long long)S * C * (KK + 1);
@@ -320,41 +475,79 @@ __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, fl
     }
 }
 
-int ksize(const hc_conv_desc* d) { return d->kh; }
+int sm_count() {
+    static int n[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!n[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev] = v > 0 ? v : 1;
+    }
+    return n[dev];
+}
+
+// Tensor map of an NCHW fp32 tensor viewed as [N*C][H][W], box = one staged tile.
+template <int K, int WARPS>
+hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d) {
+    const uint64_t dims[3] = {(uint64_t)d->W, (uint64_t)d->H, (uint64_t)d->N * d->C_in};
+    const uint64_t strides[2] = {(uint64_t)d->W * 4, (uint64_t)d->H * d->W * 4};
+    const uint32_t box[3] = {(uint32_t)SMW, (uint32_t)Geo<K, WARPS>::R, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm) {
+    Sched sc{d->N, d->C_in, d->H, d->W, d->W / TW, 0, tile_fastest};
+    sc.items = d->N * d->C_in * sc.col_tiles;
+    const int g = sm_count() * ctas_per_sm;
+    *grid = g < sc.items ? g : sc.items;
+    return sc;
+}
 
 template <int K>
 hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const float* b, float* y, cudaStream_t st) {
-    const int col_tiles = d->W / TW;
-    const long long blocks = (long long)d->N * d->C_in * col_tiles;
-    const size_t smem = 2 * sizeof(float) * Geo<K>::TILE;
+    using G = Geo<K, FWD_WARPS>;
+    CUtensorMap xm;
+    hc_status s = plane_map<K, FWD_WARPS>(&xm, x, d);
+    if (s) return s;
+    int grid;
+    const Sched sc = sched_of(d, &grid, 1, FWD_CTAS);  // horizontal neighbours back to back: their halos hit L2
+    const size_t smem = sizeof(float) * (NSTAGE * G::TILE + 2 * WSLOT) + NSTAGE * sizeof(uint64_t);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(dw_fwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    dw_fwd_kernel<K><<<(unsigned)blocks, FWD_THREADS, smem, st>>>(x, w, b, y, d->C_in, d->H, d->W, col_tiles);
+    dw_fwd_kernel<K><<<grid, FWD_WARPS * 32, smem, st>>>(xm, w, b, y, sc);
     return launched();
 }
 
 template <int K>
 hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy, float* gx,
                 float* tile_part, float* gwp, float* gbp, bool want_wb, cudaStream_t st) {
-    const int col_tiles = d->W / TW, tps = p.Wl / TW;
-    const long long blocks = (long long)d->N * d->C_in * col_tiles;
-    const size_t smem = 4 * sizeof(float) * Geo<K>::TILE;
+    using G = Geo<K, BWD_WARPS>;
+    if (!gx && !want_wb) return HC_OK;
+    CUtensorMap gm, xm;
+    hc_status s = plane_map<K, BWD_WARPS>(&gm, gy, d);
+    if (s || (s = plane_map<K, BWD_WARPS>(&xm, x, d))) return s;
+    int grid;
+    const Sched sc = sched_of(d, &grid, 0, 1);  // runs of one (c, column tile): gw stays in registers
+    const int tps = p.Wl / TW;
+    const size_t smem =
+        sizeof(float) * (2 * NSTAGE * G::TILE + 2 * WSLOT + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(dw_bwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    if (!gx && !want_wb) return HC_OK;
-    BwdArgs a{x, w, gy, gx, tile_part, d->N, d->C_in, d->H, d->W, col_tiles, tps, want_wb ? 1 : 0};
-    dw_bwd_kernel<K><<<(unsigned)blocks, BWD_THREADS, smem, st>>>(a);
-    hc_status s = launched();
+    BwdArgs a{w, gx, tile_part, tps, want_wb ? 1 : 0};
+    dw_bwd_kernel<K><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+    s = launched();
     if (s || !want_wb) return s;
     const long long total = (long long)p.S * d->C_in * (K * K + 1);
-    const unsigned grid = (unsigned)((total + 255) / 256);
-    dw_shard_partials_kernel<<<grid, 256, 0, st>>>(tile_part, gwp, gbp, p.S, d->C_in, tps * d->N, K * K);
+    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, p.S, d->C_in,
+                                                                             tps * d->N, K * K);
     return launched();
 }
 
@@ -368,14 +561,14 @@ bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
 }
 
 size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p) {
-    const int K = ksize(d);
+    const int K = d->kh;
     return (size_t)p.S * d->C_in * (p.Wl / TW) * d->N * (K * K + 1);
 }
 
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* b, float* y, cudaStream_t st) {
     (void)p;
-    switch (ksize(d)) {
+    switch (d->kh) {
         case 3: return fwd_k<3>(d, x, w, b, y, st);
         case 5: return fwd_k<5>(d, x, w, b, y, st);
         case 7: return fwd_k<7>(d, x, w, b, y, st);
@@ -386,12 +579,25 @@ hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
                                bool want_weight_grads, cudaStream_t st) {
-    switch (ksize(d)) {
+    switch (d->kh) {
         case 3: return bwd_k<3>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
         case 5: return bwd_k<5>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
         case 7: return bwd_k<7>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
     }
     return HC_ERR_UNSUPPORTED;
+}
+
+hc_status dw_take_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dw_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+    }
+    if (v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_dw_status, &zero, sizeof(int));
+    }
+    return (hc_status)v;
 }
 
 }  // namespace hc
