@@ -38,8 +38,9 @@ def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return dict(hbm=float(d["hbm_gbs"]), sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), src="measured")
-    return dict(hbm=6800.0, sm_max_mhz=2070.0, src="fallback")
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]), sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, sm_max_mhz=2070.0, src="fallback")
 
 
 class DepthwiseWorkload:
@@ -74,6 +75,45 @@ class DepthwiseWorkload:
         b = np.zeros((c["C_out"],), np.float32)
         gy = synth.normal((c["N"], c["C_out"], c["H"], c["W"]), 1.0, self.seed, 4)
         return x, w, b, gy
+
+
+class DenseWorkload:
+    """Dense 5x5 conv 128->128, stride 1, padding 2, fp32 via 3xTF32 on the tensor
+    cores, x (7,128,128,1024) N(0,1), weight Kaiming-normal, bias N(0,0.01),
+    grad_output N(0,1), 4 W-shards of width 256."""
+    name = "dense5x5_fwd_bwd"
+
+    def __init__(self, N=7, C=128, H=128, W=1024, K=5, S=4, seed=0):
+        self.cfg = dict(N=N, C_in=C, H=H, W=W, C_out=C, kh=K, kw=K, stride=1, padding=(K - 1) // 2, groups=1,
+                        num_shards=S)
+        self.K = K
+        self.E = N * C * H * W
+        self.seed = seed
+        self.flops_pass = 2.0 * N * H * W * C * C * K * K   # one of forward / grad_input / grad_weight
+        self.flops = 3 * self.flops_pass
+        self.flops_bwd = 2 * self.flops_pass
+        self.bytes = 5 * 4 * self.E
+        self.bytes_bwd = 3 * 4 * self.E
+
+    def describe(self):
+        c = self.cfg
+        return {"workload": f"dense {self.K}x{self.K} conv {c['C_in']}->{c['C_out']} fwd+bwd, x ({c['N']},{c['C_in']},"
+                            f"{c['H']},{c['W']}) fp32 (3xTF32 tensor cores), {c['num_shards']} W-shards of width "
+                            f"{c['W'] // c['num_shards']}",
+                "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [self.K, self.K], "padding": c["padding"],
+                "groups": 1, "num_shards": c["num_shards"], "l2": "inputs (470 MB each) larger than L2; no flush"}
+
+    def inputs(self):
+        from spatially_sharded_cnn_gb300 import synth
+        c = self.cfg
+        x = synth.normal((c["N"], c["C_in"], c["H"], c["W"]), 1.0, self.seed, 1)
+        w = synth.kaiming_normal((c["C_out"], c["C_in"], self.K, self.K), c["C_in"] * self.K * self.K, self.seed, 2)
+        b = synth.normal((c["C_out"],), 0.01, self.seed, 3)
+        gy = synth.normal((c["N"], c["C_out"], c["H"], c["W"]), 1.0, self.seed, 4)
+        return x, w, b, gy
+
+
+WORKLOADS = {"dw7": DepthwiseWorkload, "dense5x5": DenseWorkload}
 
 
 # ---------------------------------------------------------------------------
@@ -212,9 +252,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dw7")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    wl = DepthwiseWorkload()
+    wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         return run_reference(args, wl)
 
@@ -244,11 +285,14 @@ def main():
     d = hc.desc(wl.cfg)
     st, ws_bytes = hc.hc_conv2d_workspace_size(d, 1)
     hc.check(st, "workspace")
+    st, ws_fwd = hc.hc_conv2d_workspace_size(d, 0)
+    hc.check(st, "workspace")
+    ws_bytes = max(ws_bytes, ws_fwd)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def fwd():
-        hc.check(hc.hc_conv2d_fwd(d, xd, wd, bd, yd, None, 0, stream), "fwd")
+        hc.check(hc.hc_conv2d_fwd(d, xd, wd, bd, yd, ws, ws_bytes, stream), "fwd")
 
     def bwd():
         hc.check(hc.hc_conv2d_bwd(d, xd, wd, gyd, gxd, gwd, gbd, None, None, ws, ws_bytes, stream), "bwd")
@@ -292,7 +336,13 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     ms_step = elapsed_ms / K
-    value = world * wl.bytes / (ms_step * 1e-3) / 1e9
+    dense = isinstance(wl, DenseWorkload)
+    if dense:
+        value = world * wl.flops / (ms_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        value = world * wl.bytes / (ms_step * 1e-3) / 1e9
+        unit = "GB/s"
 
     # end to end: host buffers, copies inside the timed region
     xh = torch.from_numpy(x).pin_memory()
@@ -327,29 +377,41 @@ def main():
     # roofline of the dominant kernel (the fused depthwise backward, one launch
     # per hc_conv2d_bwd call plus two tiny fixed-order reductions)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    e2e_value = world * (wl.flops / 1e12 if dense else wl.bytes / 1e9) / (e2e_ms * 1e-3)
     alu_peak = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
     bwd_tflops = wl.flops_bwd / (bwd_ms * 1e-3) / 1e12
     bwd_gbs = wl.bytes_bwd / (bwd_ms * 1e-3) / 1e9
-    roof = {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": bwd_tflops, "peak": alu_peak,
-            "unit": "TFLOP/s", "frac": bwd_tflops / alu_peak,
-            "traffic": traffic_for("dw_bwd_kernel<7>", os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc",
-                                                                    "dw.cu")),
-            "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
-            "hbm": {"achieved": bwd_gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": bwd_gbs / peaks["hbm"],
-                    "peak_source": peaks["src"]},
+    if dense:
+        # forward call = operand preparation + one tensor-core GEMM pass; the peak is the
+        # measured bf16 dense rate x the nominal tf32/bf16 ratio (1.1 / 2.25), / 3 for 3xTF32
+        tf32_peak = peaks["bf16"] * (1.1 / 2.25)
+        fwd_tflops = wl.flops_pass / (fwd_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "tc_conv_kernel (forward call incl. operand prep)",
+                "achieved": fwd_tflops, "peak": tf32_peak / 3, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)",
+                "frac": fwd_tflops / (tf32_peak / 3), "traffic": None,
+                "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
+                "ms_per_launch": fwd_ms}
+    else:
+        roof = {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": bwd_tflops, "peak": alu_peak,
+                "unit": "TFLOP/s", "frac": bwd_tflops / alu_peak,
+                "traffic": traffic_for("dw_bwd_kernel<7>", os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc",
+                                                                        "dw.cu")),
+                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                "hbm": {"achieved": bwd_gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": bwd_gbs / peaks["hbm"],
+                        "peak_source": peaks["src"]},
             "ms_per_launch": bwd_ms}
     if world > 1:
         dist.barrier()
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": wl.describe(),
-                "hbm_frac": value / world / peaks["hbm"],
+                "hbm_frac": None if dense else value / world / peaks["hbm"],
                 "phases_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
-                "e2e": {"value": world * wl.bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "e2e": {"value": e2e_value, "unit": unit,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and not dense:
             v, cores, sample = cpu_oracle_sample(wl)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)

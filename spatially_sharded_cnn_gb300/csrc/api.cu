@@ -76,22 +76,30 @@ static bool algo_supported(const hc_conv_desc* d, const Plan& p, hc_algo a) {
     switch (a) {
         case HC_ALGO_DIRECT: return true;
         case HC_ALGO_DEPTHWISE: return depthwise_supported(d, p);
+        case HC_ALGO_TC_3XTF32: return tc_supported(d, p);
         default: return false;
     }
 }
 
 static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
     if (depthwise_supported(d, p)) return HC_ALGO_DEPTHWISE;
+    if (tc_supported(d, p)) return HC_ALGO_TC_3XTF32;
     return HC_ALGO_DIRECT;
 }
 
 // Workspace layout of the backward pass (bytes, each piece 256-aligned):
 //   DIRECT:    [gw partials S*wsize][gb partials S*C_out]
 //   DEPTHWISE: [gw partials S*C*K*K][gb partials S*C][tile partials]
+//   TC_3XTF32: [gw partials][gb partials][NHWC hi/lo copies, weights hi/lo, split-K partials]
 static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
     size_t b = round256(sizeof(float) * p.S * wsize(d)) + round256(sizeof(float) * p.S * d->C_out);
     if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
+    if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.S)) + tc_ws_bytes(d, p, 1);
     return b;
+}
+
+static size_t fwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
+    return a == HC_ALGO_TC_3XTF32 ? tc_ws_bytes(d, p, 0) : 0;
 }
 
 static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* bytes) {
@@ -101,7 +109,7 @@ static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* byt
     if (st) return st;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
     if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
-    *bytes = pass == 0 ? 0 : bwd_ws_bytes(d, p, a);
+    *bytes = pass == 0 ? fwd_ws_bytes(d, p, a) : bwd_ws_bytes(d, p, a);
     return HC_OK;
 }
 
@@ -114,10 +122,11 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
         return HC_ERR_INVALID_ARG;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
     if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
-    (void)ws;
-    (void)ws_bytes;
+    const size_t need = fwd_ws_bytes(d, p, a);
+    if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     switch (a) {
+        case HC_ALGO_TC_3XTF32: return launch_tc_fwd(d, p, x, w, b, y, ws, s);
         case HC_ALGO_DEPTHWISE: return launch_depthwise_fwd(d, p, x, w, b, y, s);
         case HC_ALGO_DIRECT: return launch_direct_fwd(d, p, x, w, b, y, s);
         default: return HC_ERR_UNSUPPORTED;
@@ -137,7 +146,7 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     if (a == HC_ALGO_AUTO) a = pick(d, p);
     if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
     const size_t need = bwd_ws_bytes(d, p, a);
-    if (ws_bytes < need || (need && !ws) || !aligned16(ws)) return HC_ERR_WORKSPACE;
+    if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char* wsp = (char*)ws;
     float* gwp = (float*)wsp;
@@ -152,6 +161,13 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
         case HC_ALGO_DEPTHWISE:
             st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s);
             break;
+        case HC_ALGO_TC_3XTF32: {
+            float* btmp = (float*)wsp;
+            wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.S));
+            if ((gx || want_w) && (st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s))) return st;
+            if (want_b) st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl, btmp, s);
+            break;
+        }
         case HC_ALGO_DIRECT:
             if (gx && (st = launch_direct_gx(d, p, w, gy, gx, s))) return st;
             if (want_w || want_b)
@@ -236,7 +252,8 @@ hc_status hc_sync_check(void* stream) {
         return HC_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return HC_ERR_CUDA;
-    return dw_take_status();
+    const hc_status a = dw_take_status(), b = tc_take_status();
+    return a ? a : b;
 }
 
 const char* hc_status_string(hc_status s) {

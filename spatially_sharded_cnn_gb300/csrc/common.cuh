@@ -43,6 +43,7 @@ hc_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const
 // clears) the first error recorded since the last call.  Call after the
 // stream has been synchronised.
 hc_status dw_take_status();
+hc_status tc_take_status();
 
 // ---- kernel launchers (one translation unit each) -------------------------
 hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* x, float* x_ext, cudaStream_t st);
@@ -65,6 +66,24 @@ hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
                                bool want_weight_grads, cudaStream_t st);
+
+// dense conv on tcgen05 (3xTF32 implicit GEMM): groups 1, stride 1, odd k,
+// padding (k-1)/2, C_in and C_out multiples of 128
+bool tc_supported(const hc_conv_desc* d, const Plan& p);
+int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p);
+size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
+hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                        float* y, void* ws, cudaStream_t st);
+// grad_input (if gx) and the per-shard weight-gradient partials gwp (if want_w)
+hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
+                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st);
+
+// Per-shard bias-gradient partials gbp[S][Co] in two fixed-order stages,
+// using tmp[bias_grad_ws_floats(Co, S)].
+constexpr int kBiasSlices = 64;
+size_t bias_grad_ws_floats(int Co, int S);
+hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
+                                    float* tmp, cudaStream_t st);
 
 // fixed-order sums
 // out[k] = sum_{r < rows} in[r * count + k], r ascending

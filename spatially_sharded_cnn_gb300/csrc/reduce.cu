@@ -22,7 +22,46 @@ __global__ void sum_rows_kernel(const float* __restrict__ in, float* __restrict_
     }
 }
 
+// Bias-gradient partial sums, stage 1: block (slice, co, r) sums grad_output over
+// its slice of the (n, i) rows and shard r's own output columns, in a fixed
+// order (strided thread sums, then a shuffle tree and the warp sums in order).
+// part[(slice * S + r) * Co + co].
+__global__ void bias_slices_kernel(const float* __restrict__ gy, float* __restrict__ part, int N, int Co, int Ho,
+                                   int Wo, int S, int own_w, int slices) {
+    __shared__ float red[32];
+    const int slice = blockIdx.x, co = blockIdx.y, r = blockIdx.z;
+    const int j0 = r * own_w, j1 = (r == S - 1) ? Wo : j0 + own_w;
+    const int nj = j1 - j0;
+    const long long nrows = (long long)N * Ho;
+    const long long r0 = nrows * slice / slices, r1 = nrows * (slice + 1) / slices;
+    float acc = 0.0f;
+    for (long long row = r0; row < r1; row++) {
+        const int n = (int)(row / Ho), i = (int)(row % Ho);
+        const float* p = gy + (((long long)n * Co + co) * Ho + i) * Wo + j0;
+        for (int j = threadIdx.x; j < nj; j += blockDim.x) acc += __ldg(p + j);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < (int)(blockDim.x >> 5); k++) t += red[k];
+        part[((long long)slice * S + r) * Co + co] = t;
+    }
+}
+
 }  // namespace
+
+size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co; }
+
+hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
+                                    float* tmp, cudaStream_t st) {
+    bias_slices_kernel<<<dim3(kBiasSlices, Co, S), 128, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, kBiasSlices);
+    hc_status s = launched();
+    if (s) return s;
+    return launch_sum_rows(tmp, gbp, kBiasSlices, (long long)S * Co, st);  // slices in order
+}
 
 hc_status launch_sum_rows(const float* in, float* out, int rows, long long count, cudaStream_t st) {
     const int threads = 256;

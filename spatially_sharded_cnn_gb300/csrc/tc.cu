@@ -1,0 +1,803 @@
+// tc.cu -- dense (groups = 1) convolution as an implicit GEMM on the 5th-
+// generation tensor cores (tcgen05, accumulators in tensor memory), with
+// FP32 accuracy from 3xTF32: every operand is split as a = a_hi + a_lo with
+// a_hi = tf32(a), a_lo = tf32(a - a_hi), and each product is taken as
+// a_hi*b_hi + a_hi*b_lo + a_lo*b_hi (the a_lo*b_lo term is below fp32
+// rounding), all accumulated in fp32 in TMEM.
+//
+// The W shards (NVIDIA blog "Perception model training for autonomous
+// vehicles with tensor parallelism", design section and Figures 1-2; kwkr.cn
+// news/18980 section 2.2): an output tile is one row segment of a shard's
+// owned output columns, so the TMA boxes that feed it read the halo columns
+// from the neighbouring shards' blocks and zeros past the image edge (the
+// copy engine's out-of-bounds fill); the weight gradient is accumulated per
+// shard over that shard's own output columns (its _Partial value), split
+// further along the pixels to fill the GPU, and summed in a fixed order.
+//
+// Passes (all share one persistent, warp-specialised kernel):
+//   conv   (forward, and grad_input of a stride-1 conv as the conv of
+//          grad_output with the flipped, transposed kernel):
+//          D[m][px] = sum over taps (u,v) and 32-channel chunks of
+//          A[m][(u,v,c)] * X[n][h+u-p][w+v-p][c]; A = weights, B = the
+//          activation in NHWC (channels contiguous), one 4-D TMA box per
+//          (tap, chunk).
+//   wgrad  G[co][ci] of one tap = sum over a shard's pixels of
+//          gy[co][px] * x[ci][px + tap]; A = grad_output in NCHW (pixels
+//          contiguous), B = one of four copies of x shifted right by 0..3
+//          columns, so that every tap's column shift starts on a 16-byte
+//          boundary (a TMA box's innermost coordinate must); row shifts and
+//          padding come from the box's coordinates and zero fill.
+// All operands are K-major tiles with the 128-byte swizzle.
+//
+// Accuracy: the tensor core's fp32 accumulation loses about one unit in the
+// last place per MMA step, so a long K would lose ~1e-5.  The MMA warp
+// therefore accumulates groups of 8 k-chunks (96 MMAs) in one of two TMEM
+// buffers and the epilogue warps add the groups up in fp32 registers.
+//
+// Warp roles (320 threads, one CTA per SM): warp 0 issues TMA loads into an
+// mbarrier-guarded shared-memory ring, warp 1 issues tcgen05.mma into the two
+// TMEM buffers in turn, warps 2-9 (two per TMEM lane quarter, one column half
+// each) drain finished groups (tcgen05.ld) and store the tile.  Every wait is
+// bounded: on timeout the CTA records HC_ERR_TIMEOUT, drains its outstanding
+// copies and MMAs, frees its tensor memory and exits.
+#include "common.cuh"
+
+namespace hc {
+namespace {
+
+constexpr int BM = 128;             // accumulator rows (TMEM lanes)
+constexpr int BK = 32;              // tf32 per k-chunk = one 128-byte swizzle row
+constexpr int TC_SMEM_RING = 196 * 1024;
+constexpr long long kWait = 4000000000LL;  // clock cycles, about 2 s
+
+__device__ int g_tc_status;
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+__device__ __forceinline__ unsigned su32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, unsigned parity) {
+    unsigned ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(su32(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Bounded wait; also gives up early once another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, volatile int* abort_flag) {
+    if (mbar_try(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try(b, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWait) {
+            *abort_flag = 1;
+            atomicCAS(&g_tc_status, 0, (int)HC_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+            "r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(su32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];\n" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_5d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, int c4,
+                                       uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+        "%6}], [%7];\n" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_alloc(uint32_t* slot, unsigned cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(slot)), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, unsigned cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
+                 : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32, one CTA.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start,
+// leading and stride byte offsets in 16-byte units, version 1 at bit 46,
+// layout type 2 = SWIZZLE_128B at bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(const void* p, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((su32(p) >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::tf32: D fp32, A and B tf32, majors, N, M.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+struct TcParams {
+    int mode;       // 0: conv (forward / stride-1 grad_input), 1: weight gradient
+    int units;      // work units
+    int stages;     // ring depth
+    int chunks;     // k-chunks per unit (conv mode)
+    int group;      // k-chunks accumulated in TMEM before the epilogue adds them up in fp32
+    // conv mode
+    int N, Ho, Wo, M, Kc, kh, kw, pad, tiles_w, mblocks;
+    const float* bias;
+    float* out;     // NCHW [N][M][Ho][Wo]
+    // wgrad mode
+    int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // row_chunks = own_w / 32
+    long long shard_chunks;                               // N * Ho * row_chunks
+    float* part;    // [S][J][taps][Co][Ci]
+};
+
+struct Unit {
+    int m0;             // first accumulator row (output channel)
+    int n, ho, w0;      // conv: output row segment
+    int tap, ci0, r, j; // wgrad
+    long long c_begin, c_end;
+};
+
+__device__ __forceinline__ Unit decode(const TcParams& p, int t, int BN) {
+    Unit u{};
+    if (p.mode == 0) {
+        u.m0 = (t % p.mblocks) * BM;
+        int rest = t / p.mblocks;
+        u.w0 = (rest % p.tiles_w) * BN;
+        rest /= p.tiles_w;
+        u.ho = rest % p.Ho;
+        u.n = rest / p.Ho;
+        u.c_begin = 0;
+        u.c_end = p.chunks;
+    } else {
+        u.m0 = (t % p.mblocks) * BM;
+        int rest = t / p.mblocks;
+        u.ci0 = (rest % p.nblocks) * BN;
+        rest /= p.nblocks;
+        u.tap = rest % p.taps;
+        rest /= p.taps;
+        u.j = rest % p.J;
+        u.r = rest / p.J;
+        u.c_begin = p.shard_chunks * u.j / p.J;
+        u.c_end = p.shard_chunks * (u.j + 1) / p.J;
+    }
+    return u;
+}
+
+struct Smem {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t buf_full[2];
+    uint64_t buf_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+constexpr int TC_EPI_WARPS = 8;                    // two per TMEM lane quarter, one column half each
+constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
+
+// One persistent CTA per SM.  BN = accumulator columns (pixels of an output
+// row segment in conv mode, input channels in wgrad mode).
+template <int BN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_conv_kernel(const __grid_constant__ CUtensorMap amap_hi, const __grid_constant__ CUtensorMap amap_lo,
+                   const __grid_constant__ CUtensorMap bmap_hi, const __grid_constant__ CUtensorMap bmap_lo,
+                   TcParams p) {
+    extern __shared__ __align__(1024) unsigned char dsmem[];
+    unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle needs 1 KB
+    __shared__ Smem sh;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr uint32_t a_bytes = BM * 128;            // 128 rows x 32 tf32
+    constexpr uint32_t b_bytes = BN * 128;
+    constexpr uint32_t stage_bytes = 2 * a_bytes + 2 * b_bytes;
+    volatile int* abort_flag = &sh.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; s++) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&sh.buf_full[b], 1);
+            mbar_init(&sh.buf_empty[b], TC_EPI_WARPS);
+        }
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 0) tc_alloc(&sh.tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        long long it = 0;  // chunk counter = ring position
+        for (int t = blockIdx.x; t < p.units && !*abort_flag; t += gridDim.x) {
+            const Unit u = decode(p, t, BN);
+            for (long long c = u.c_begin; c < u.c_end; c++, it++) {
+                const int s = (int)(it % p.stages);
+                if (it >= p.stages && !mbar_wait(&sh.empty[s], (unsigned)(((it / p.stages) - 1) & 1), abort_flag))
+                    break;
+                unsigned char* st = ring + (size_t)s * stage_bytes;
+                mbar_expect_tx(&sh.full[s], stage_bytes);
+                if (p.mode == 0) {
+                    const int cpt = p.Kc / BK;
+                    const int tap = (int)(c / cpt), cb = (int)(c % cpt);
+                    const int uu = tap / p.kw, vv = tap % p.kw;
+                    const int ka = tap * p.Kc + cb * BK;
+                    tma_2d(st, &amap_hi, ka, u.m0, &sh.full[s]);
+                    tma_2d(st + a_bytes, &amap_lo, ka, u.m0, &sh.full[s]);
+                    const int wx = u.w0 + vv - p.pad, hy = u.ho + uu - p.pad;
+                    tma_4d(st + 2 * a_bytes, &bmap_hi, cb * BK, wx, hy, u.n, &sh.full[s]);
+                    tma_4d(st + 2 * a_bytes + b_bytes, &bmap_lo, cb * BK, wx, hy, u.n, &sh.full[s]);
+                } else {
+                    // pixel chunk c of shard r: (n, ho, 32-column piece); the tap's column
+                    // shift s = v - pad is read from the copy shifted right by jc = (-s) mod 4
+                    const int wc = (int)(c % p.row_chunks);
+                    const long long rest = c / p.row_chunks;
+                    const int ho = (int)(rest % p.Ho), n = (int)(rest / p.Ho);
+                    const int w = u.r * p.own_w + wc * BK;
+                    const int uu = u.tap / p.kw, sft = u.tap % p.kw - p.pad;
+                    const int jc = ((-sft) % 4 + 4) % 4;
+                    tma_4d(st, &amap_hi, w, ho, u.m0, n, &sh.full[s]);
+                    tma_4d(st + a_bytes, &amap_lo, w, ho, u.m0, n, &sh.full[s]);
+                    tma_5d(st + 2 * a_bytes, &bmap_hi, w + sft + jc, ho + uu - p.pad, u.ci0, n, jc, &sh.full[s]);
+                    tma_5d(st + 2 * a_bytes + b_bytes, &bmap_lo, w + sft + jc, ho + uu - p.pad, u.ci0, n, jc,
+                           &sh.full[s]);
+                }
+            }
+        }
+        if (*abort_flag) {
+            // wait (bounded, ignoring the abort flag) for the last copy issued into each stage
+            int zero = 0;
+            for (long long k = it - p.stages > 0 ? it - p.stages : 0; k < it; k++)
+                mbar_wait(&sh.full[k % p.stages], (unsigned)((k / p.stages) & 1), &zero);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        const uint32_t idesc = idesc_tf32(BM, BN, 0, 0);
+        long long it = 0;
+        long long g = 0;  // group counter = TMEM buffer position
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.units && ok && !*abort_flag; t += gridDim.x) {
+            const Unit u = decode(p, t, BN);
+            for (long long c0 = u.c_begin; c0 < u.c_end && ok; c0 += p.group, g++) {
+                const int b = (int)(g & 1);
+                if (g >= 2 && !mbar_wait(&sh.buf_empty[b], (unsigned)(((g >> 1) - 1) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * 256);
+                const long long c1 = c0 + p.group < u.c_end ? c0 + p.group : u.c_end;
+                bool first = true;
+                for (long long c = c0; c < c1; c++, it++) {
+                    const int s = (int)(it % p.stages);
+                    if (!mbar_wait(&sh.full[s], (unsigned)((it / p.stages) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    unsigned char* st = ring + (size_t)s * stage_bytes;
+                    unsigned char *ahi = st, *alo = st + a_bytes, *bhi = st + 2 * a_bytes, *blo = bhi + b_bytes;
+#pragma unroll
+                    for (int k = 0; k < BK / 8; k++) {  // 8 tf32 = 32 bytes along the swizzled row
+                        const uint64_t dah = sdesc(ahi + 32 * k, 16, 1024), dal = sdesc(alo + 32 * k, 16, 1024);
+                        const uint64_t dbh = sdesc(bhi + 32 * k, 16, 1024), dbl = sdesc(blo + 32 * k, 16, 1024);
+                        tc_mma(d, dal, dbh, idesc, first ? 0u : 1u);
+                        tc_mma(d, dah, dbl, idesc, 1u);
+                        tc_mma(d, dah, dbh, idesc, 1u);
+                        first = false;
+                    }
+                    tc_commit(&sh.empty[s]);  // frees the stage once these MMAs have read it
+                }
+                if (ok) tc_commit(&sh.buf_full[b]);
+            }
+        }
+        // every MMA issued has completed before tensor memory is released
+        tc_commit(&sh.drain);
+        int zero = 0;
+        mbar_wait(&sh.drain, 0, &zero);
+    } else if (warp >= 2) {
+        // ---------------- epilogue ----------------
+        const int ew = warp - 2;
+        const int q = warp & 3;                // TMEM lane quarter this warp may access
+        const int half = ew >> 2;              // column half
+        const int row = 32 * q + lane;
+        constexpr int HC = BN / 2;             // columns per thread
+        long long g = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.units && ok && !*abort_flag; t += gridDim.x) {
+            const Unit u = decode(p, t, BN);
+            float acc[HC];
+#pragma unroll
+            for (int i = 0; i < HC; i++) acc[i] = 0.0f;
+            for (long long c0 = u.c_begin; c0 < u.c_end; c0 += p.group, g++) {
+                const int b = (int)(g & 1);
+                if (!mbar_wait(&sh.buf_full[b], (unsigned)((g >> 1) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256 + half * HC);
+#pragma unroll
+                for (int cc = 0; cc < HC; cc += 32) {
+                    float v[32];
+                    tc_ld32(base + (uint32_t)cc, v);
+#pragma unroll
+                    for (int i = 0; i < 32; i++) acc[cc + i] += v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.buf_empty[b]);
+            }
+            if (!ok) break;
+            if (p.mode == 0) {
+                const int m = u.m0 + row;
+                const float bv = p.bias ? __ldg(p.bias + m) : 0.0f;
+                float* dst = p.out + (((long long)u.n * p.M + m) * p.Ho + u.ho) * p.Wo + u.w0 + half * HC;
+#pragma unroll
+                for (int k = 0; k < HC; k += 4)
+                    *reinterpret_cast<float4*>(dst + k) =
+                        make_float4(acc[k] + bv, acc[k + 1] + bv, acc[k + 2] + bv, acc[k + 3] + bv);
+            } else {
+                const int co = u.m0 + row;
+                float* dst = p.part + ((((long long)u.r * p.J + u.j) * p.taps + u.tap) * p.Co + co) * p.Ci + u.ci0 +
+                             half * HC;
+#pragma unroll
+                for (int k = 0; k < HC; k += 4)
+                    *reinterpret_cast<float4*>(dst + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tc_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Operand preparation.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// NCHW [N][C][H][W] -> NHWC [N][H][W][Cp] split into tf32 hi / lo (channels
+// C..Cp-1 zero).  32x32 (channel x column) tiles through shared memory so
+// both the reads and the writes are coalesced.
+__global__ void prep_nhwc_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo, int C,
+                                 int H, int W, int Cp) {
+    __shared__ float t[32][33];
+    const int w0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    const int nh = blockIdx.z;  // n * H + h
+    const int n = nh / H, h = nh % H;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, w = w0 + threadIdx.x;
+        t[i][threadIdx.x] = (c < C && w < W) ? __ldg(x + (((long long)n * C + c) * H + h) * W + w) : 0.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int w = w0 + i, c = c0 + threadIdx.x;
+        if (w < W && c < Cp) {
+            const float v = t[threadIdx.x][i];
+            const float vh = tf32_rna(v);
+            const long long o = (((long long)n * H + h) * W + w) * Cp + c;
+            hi[o] = vh;
+            lo[o] = tf32_rna(v - vh);
+        }
+    }
+}
+
+// Weights as the A operand of the conv pass: A[m][(u*kw+v)*Kc + c], hi / lo.
+//   forward:    m = co, c = ci, value w[co][ci][u][v]
+//   grad_input: m = ci, c = co, value w[co][ci][kh-1-u][kw-1-v]
+__global__ void prep_weight_kernel(const float* __restrict__ w, float* __restrict__ hi, float* __restrict__ lo,
+                                   int Co, int Ci, int kh, int kw, int Mp, int Kc, int transpose) {
+    const long long ktot = (long long)kh * kw * Kc;
+    const long long total = (long long)Mp * ktot;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(q / ktot);
+        const int k = (int)(q % ktot);
+        const int tap = k / Kc, c = k % Kc;
+        const int u = tap / kw, v = tap % kw;
+        float val = 0.0f;
+        if (!transpose) {
+            if (m < Co && c < Ci) val = __ldg(w + (((long long)m * Ci + c) * kh + u) * kw + v);
+        } else {
+            if (m < Ci && c < Co) val = __ldg(w + (((long long)c * Ci + m) * kh + (kh - 1 - u)) * kw + (kw - 1 - v));
+        }
+        const float vh = tf32_rna(val);
+        hi[q] = vh;
+        lo[q] = tf32_rna(val - vh);
+    }
+}
+
+// NCHW -> NCHW tf32 hi / lo (the grad_output operand of the weight gradient).
+__global__ void prep_split_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                  long long n4) {
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
+        float4 h, l;
+        h.x = tf32_rna(v.x); l.x = tf32_rna(v.x - h.x);
+        h.y = tf32_rna(v.y); l.y = tf32_rna(v.y - h.y);
+        h.z = tf32_rna(v.z); l.z = tf32_rna(v.z - h.z);
+        h.w = tf32_rna(v.w); l.w = tf32_rna(v.w - h.w);
+        reinterpret_cast<float4*>(hi)[q] = h;
+        reinterpret_cast<float4*>(lo)[q] = l;
+    }
+}
+
+// Column-shifted tf32 hi / lo copies of x for the weight gradient:
+// c[j][n][c][h][i] = x[n][c][h][i - j] (zero outside [0, W)), j = 0..3, i < Wc = W + 4.
+// A tap's column shift s is then read from copy (-s) mod 4 at a 16-byte-aligned
+// column.  One block per input row: the row is staged in shared memory once
+// and the four shifted rows are written with 16-byte stores.
+__global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                  long long rows, int W, int Wc) {
+    extern __shared__ float rowbuf[];  // [W + 8]: 4 zeros, the row, 4 zeros
+    const long long row = blockIdx.x;
+    const float* src = x + row * W;
+    for (int i = threadIdx.x; i < W + 8; i += blockDim.x) {
+        const int c = i - 4;
+        rowbuf[i] = (c >= 0 && c < W) ? __ldg(src + c) : 0.0f;
+    }
+    __syncthreads();
+    const int v4 = Wc / 4;
+    for (int q = threadIdx.x; q < 4 * v4; q += blockDim.x) {
+        const int j = q / v4, i0 = (q - j * v4) * 4;
+        // element i of copy j is x[i - j] = rowbuf[i - j + 4]
+        float4 h, l;
+        const float a = rowbuf[i0 - j + 4], b = rowbuf[i0 - j + 5], c = rowbuf[i0 - j + 6], d = rowbuf[i0 - j + 7];
+        h.x = tf32_rna(a); l.x = tf32_rna(a - h.x);
+        h.y = tf32_rna(b); l.y = tf32_rna(b - h.y);
+        h.z = tf32_rna(c); l.z = tf32_rna(c - h.z);
+        h.w = tf32_rna(d); l.w = tf32_rna(d - h.w);
+        const long long o = ((long long)j * rows + row) * Wc + i0;
+        *reinterpret_cast<float4*>(hi + o) = h;
+        *reinterpret_cast<float4*>(lo + o) = l;
+    }
+}
+
+// Weight-gradient partials: gwp[r][co][ci][tap] = sum_j part[r][j][tap][co][ci] (j ascending).
+__global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ gwp, int S, int J, int taps,
+                                    int Co, int Ci) {
+    const long long per = (long long)taps * Co * Ci;
+    const long long total = (long long)S * per;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(q / per);
+        const long long rem = q % per;  // ((co * Ci) + ci) * taps + tap
+        const int tap = (int)(rem % taps);
+        const long long coci = rem / taps;
+        const float* src = part + ((long long)r * J * taps + tap) * Co * Ci + coci;
+        float s = 0.0f;
+        for (int j = 0; j < J; j++) s += src[(long long)j * per];
+        gwp[q] = s;
+    }
+}
+
+int sm_count_tc() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n = v > 0 ? v : 1;
+    }
+    return n;
+}
+
+int pick_bn(int own_out_w) {
+    if (own_out_w % 256 == 0) return 256;
+    if (own_out_w % 128 == 0) return 128;
+    return 0;
+}
+
+template <int BN>
+hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi, const CUtensorMap& blo,
+                    TcParams p, cudaStream_t st) {
+    static bool attr = false;
+    const int smem = TC_SMEM_RING + 1024;
+    if (!attr) {
+        cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr = true;
+    }
+    const int stage_bytes = 2 * BM * 128 + 2 * BN * 128;
+    p.stages = TC_SMEM_RING / stage_bytes;
+    if (p.stages > 8) p.stages = 8;
+    const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
+    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(ahi, alo, bhi, blo, p);
+    return launched();
+}
+
+hc_status launch_conv_pass(int BN, const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi,
+                           const CUtensorMap& blo, TcParams p, cudaStream_t st) {
+    p.group = 8;
+    if (BN == 256) return launch_bn<256>(ahi, alo, bhi, blo, p, st);
+    if (BN == 128) return launch_bn<128>(ahi, alo, bhi, blo, p, st);
+    return HC_ERR_UNSUPPORTED;
+}
+
+// NHWC activation map for the conv pass: dims (Cp, W, H, N), box (32, BN, 1, 1).
+hc_status act_map_conv(CUtensorMap* m, const float* base, int N, int H, int W, int Cp, int BN) {
+    const uint64_t dims[4] = {(uint64_t)Cp, (uint64_t)W, (uint64_t)H, (uint64_t)N};
+    const uint64_t strides[3] = {(uint64_t)Cp * 4, (uint64_t)W * Cp * 4, (uint64_t)H * W * Cp * 4};
+    const uint32_t box[4] = {32, (uint32_t)BN, 1, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Weight map: dims (Ktot, Mp), box (32, 128).
+hc_status weight_map(CUtensorMap* m, const float* base, int Mp, long long ktot) {
+    const uint64_t dims[2] = {(uint64_t)ktot, (uint64_t)Mp};
+    const uint64_t strides[1] = {(uint64_t)ktot * 4};
+    const uint32_t box[2] = {32, 128};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// NCHW map for K-major weight-gradient tiles (pixels contiguous): dims (W, H, C, N),
+// box (32, 1, rows, 1): smem [rows channels][32 pixels].
+hc_status nchw_map(CUtensorMap* m, const float* base, int N, int C, int H, int W, int rows) {
+    const uint64_t dims[4] = {(uint64_t)W, (uint64_t)H, (uint64_t)C, (uint64_t)N};
+    const uint64_t strides[3] = {(uint64_t)W * 4, (uint64_t)H * W * 4, (uint64_t)C * H * W * 4};
+    const uint32_t box[4] = {32, 1, (uint32_t)rows, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// The four column-shifted copies: dims (Wc, H, C, N, 4), box (32, 1, rows, 1, 1).
+hc_status shifted_map(CUtensorMap* m, const float* base, int N, int C, int H, int Wc, int rows) {
+    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)H, (uint64_t)C, (uint64_t)N, 4};
+    const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)H * Wc * 4, (uint64_t)C * H * Wc * 4,
+                                 (uint64_t)N * C * H * Wc * 4};
+    const uint32_t box[5] = {32, 1, (uint32_t)rows, 1, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// weight-gradient tiles: 128 output channels x 128 input channels of one tap
+constexpr int WG_BN = 128;
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+bool tc_supported(const hc_conv_desc* d, const Plan& p) {
+    if (d->groups != 1 || d->stride != 1 || d->kh != d->kw || d->padding != (d->kh - 1) / 2 || d->kh % 2 == 0)
+        return false;
+    if (d->C_out % BM || d->C_in % BM) return false;  // forward rows and grad_input rows in 128-blocks
+    if (!pick_bn(p.Wl) || d->padding > 3) return false;
+    if (p.Ho != d->H || p.Wo != d->W || d->W % 4) return false;
+    return true;
+}
+
+int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
+    const int KK = d->kh * d->kw;
+    const long long units0 = (long long)(d->C_out / BM) * KK * (d->C_in / WG_BN) * p.S;
+    const long long chunks = (long long)d->N * p.Ho * (p.Wl / 32);
+    // enough units for about four waves, each unit at least 64 chunks long
+    long long J = (4LL * sm_count_tc() + units0 - 1) / units0;
+    if (J > chunks / 64) J = chunks / 64;
+    if (J < 1) J = 1;
+    return (int)J;
+}
+
+// Workspace: forward  [x NHWC hi][x NHWC lo][A hi][A lo]
+//            backward [gy NHWC hi][lo][A' hi][lo][gy NCHW hi][lo][x shifted hi][lo][split-K partials]
+size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
+    const int KK = d->kh * d->kw;
+    const size_t nx = (size_t)d->N * d->C_in * d->H * d->W;
+    const size_t ng = (size_t)d->N * d->C_out * p.Ho * p.Wo;
+    const size_t wsz = (size_t)d->C_out * KK * d->C_in;
+    if (pass == 0) return 2 * al256(4 * nx) + 2 * al256(4 * wsz);
+    const size_t nsh = 4 * (size_t)d->N * d->C_in * d->H * (d->W + 4);
+    const int J = tc_wgrad_splits(d, p);
+    const size_t part = al256(4 * (size_t)p.S * J * wsz);
+    return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
+}
+
+hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                        float* y, void* ws, cudaStream_t st) {
+    const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
+    const size_t nx = (size_t)d->N * Ci * d->H * d->W, wsz = (size_t)Co * KK * Ci;
+    char* q = (char*)ws;
+    float* xh = (float*)q;
+    q += al256(4 * nx);
+    float* xl = (float*)q;
+    q += al256(4 * nx);
+    float* ah = (float*)q;
+    q += al256(4 * wsz);
+    float* al = (float*)q;
+    prep_nhwc_kernel<<<dim3(cdiv(d->W, 32), cdiv(Ci, 32), d->N * d->H), dim3(32, 8), 0, st>>>(x, xh, xl, Ci, d->H,
+                                                                                           d->W, Ci);
+    hc_status s = launched();
+    if (s) return s;
+    prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Co, Ci, 0);
+    if ((s = launched())) return s;
+    const int BN = pick_bn(p.Wl);
+    TcParams tp{};
+    tp.mode = 0;
+    tp.N = d->N;
+    tp.Ho = p.Ho;
+    tp.Wo = p.Wo;
+    tp.M = Co;
+    tp.Kc = Ci;
+    tp.kh = K;
+    tp.kw = K;
+    tp.pad = d->padding;
+    tp.tiles_w = p.Wo / BN;
+    tp.mblocks = Co / BM;
+    tp.chunks = KK * (Ci / BK);
+    tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
+    tp.bias = b;
+    tp.out = y;
+    CUtensorMap mah, mal, mbh, mbl;
+    if ((s = weight_map(&mah, ah, Co, (long long)KK * Ci)) || (s = weight_map(&mal, al, Co, (long long)KK * Ci)) ||
+        (s = act_map_conv(&mbh, xh, d->N, d->H, d->W, Ci, BN)) ||
+        (s = act_map_conv(&mbl, xl, d->N, d->H, d->W, Ci, BN)))
+        return s;
+    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st);
+}
+
+hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
+                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+    const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
+    const size_t ng = (size_t)d->N * Co * p.Ho * p.Wo, wsz = (size_t)Co * KK * Ci;
+    const int Wc = d->W + 4;
+    const size_t nsh = 4 * (size_t)d->N * Ci * d->H * Wc;
+    char* q = (char*)ws;
+    float* gh = (float*)q;
+    q += al256(4 * ng);
+    float* gl = (float*)q;
+    q += al256(4 * ng);
+    float* ah = (float*)q;
+    q += al256(4 * wsz);
+    float* al = (float*)q;
+    q += al256(4 * wsz);
+    float* gch = (float*)q;
+    q += al256(4 * ng);
+    float* gcl = (float*)q;
+    q += al256(4 * ng);
+    float* sh = (float*)q;
+    q += al256(4 * nsh);
+    float* sl = (float*)q;
+    q += al256(4 * nsh);
+    float* part = (float*)q;
+    hc_status s;
+    if (gx) {  // grad_input = conv of grad_output with the flipped, transposed kernel
+        prep_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(Co, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(gy, gh, gl, Co,
+                                                                                                p.Ho, p.Wo, Co);
+        if ((s = launched())) return s;
+        prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Ci, Co, 1);
+        if ((s = launched())) return s;
+        const int BN = pick_bn(p.Wl);
+        TcParams tp{};
+        tp.mode = 0;
+        tp.N = d->N;
+        tp.Ho = d->H;
+        tp.Wo = d->W;
+        tp.M = Ci;
+        tp.Kc = Co;
+        tp.kh = K;
+        tp.kw = K;
+        tp.pad = K - 1 - d->padding;
+        tp.tiles_w = d->W / BN;
+        tp.mblocks = Ci / BM;
+        tp.chunks = KK * (Co / BK);
+        tp.units = tp.mblocks * d->N * d->H * tp.tiles_w;
+        tp.bias = nullptr;
+        tp.out = gx;
+        CUtensorMap mah, mal, mbh, mbl;
+        if ((s = weight_map(&mah, ah, Ci, (long long)KK * Co)) ||
+            (s = weight_map(&mal, al, Ci, (long long)KK * Co)) ||
+            (s = act_map_conv(&mbh, gh, d->N, p.Ho, p.Wo, Co, BN)) ||
+            (s = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)))
+            return s;
+        if ((s = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return s;
+    }
+    if (want_w) {
+        prep_split_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, (long long)ng / 4);
+        if ((s = launched())) return s;
+        const long long rows = (long long)d->N * Ci * d->H;
+        if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, d->W, Wc);
+        if ((s = launched())) return s;
+        TcParams tp{};
+        tp.mode = 1;
+        tp.Co = Co;
+        tp.Ci = Ci;
+        tp.S = p.S;
+        tp.J = tc_wgrad_splits(d, p);
+        tp.own_w = p.Wl;
+        tp.row_chunks = p.Wl / 32;
+        tp.Ho = p.Ho;
+        tp.kh = K;
+        tp.kw = K;
+        tp.pad = d->padding;
+        tp.taps = KK;
+        tp.mblocks = Co / BM;
+        tp.nblocks = Ci / WG_BN;
+        tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
+        tp.units = tp.mblocks * tp.nblocks * KK * tp.J * p.S;
+        tp.part = part;
+        CUtensorMap mah, mal, mbh, mbl;
+        if ((s = nchw_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (s = nchw_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_BN)) ||
+            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_BN)))
+            return s;
+        if ((s = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return s;
+        const long long total = (long long)p.S * wsz;
+        wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, KK, Co, Ci);
+        if ((s = launched())) return s;
+    }
+    return HC_OK;
+}
+
+hc_status tc_take_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+    }
+    if (v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int));
+    }
+    return (hc_status)v;
+}
+
+}  // namespace hc

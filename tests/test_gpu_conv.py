@@ -47,6 +47,15 @@ def dw_case(N, C, H, W, K, S, seed=1):
     return cfg, x, w, b, gy
 
 
+def tc_case(N, Ci, H, W, Co, K, S, seed=3):
+    cfg = P.cfg_of(N, Ci, H, W, Co, K, 1, (K - 1) // 2, 1, S)
+    x = synth.normal((N, Ci, H, W), 1.0, seed, 1)
+    w = synth.normal((Co, Ci, K, K), (2.0 / (Ci * K * K)) ** 0.5, seed, 2)
+    b = synth.normal((Co,), 0.01, seed, 3)
+    gy = synth.normal((N, Co, H, W), 1.0, seed, 4)
+    return cfg, x, w, b, gy
+
+
 def generic_case(cfg, seed=2):
     x, w, b, gy = P.rand_case(cfg, seed)
     return cfg, x, w, b, gy
@@ -65,6 +74,11 @@ CASES = {
     "stem4x4s4": lambda: generic_case(P.cfg_of(1, 3, 16, 64, 8, 4, 4, 0, 1, 4)),
     "down2x2s2_S8": lambda: generic_case(P.cfg_of(1, 4, 8, 32, 6, 2, 2, 0, 1, 8)),
     "pointwise1x1": lambda: generic_case(P.cfg_of(2, 5, 6, 16, 7, 1, 1, 0, 1, 2)),
+    # tensor-core (3xTF32) path: C_in, C_out multiples of 128
+    "tc_5x5_S2": lambda: tc_case(1, 128, 6, 256, 128, 5, 2),
+    "tc_3x3_two_mblocks": lambda: tc_case(1, 128, 5, 256, 256, 3, 1),
+    "tc_1x1": lambda: tc_case(2, 256, 4, 128, 128, 1, 1),
+    "tc_5x5_ragged_two_tiles": lambda: tc_case(1, 128, 7, 512, 128, 5, 1),
 }
 
 
@@ -104,7 +118,14 @@ def test_parity_depthwise_explicit(hc, orc, name):
     check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_DEPTHWISE)
 
 
-@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided"])
+@pytest.mark.parametrize("name", ["tc_5x5_S2", "tc_3x3_two_mblocks", "tc_1x1", "tc_5x5_ragged_two_tiles"])
+def test_parity_tensor_cores_explicit(hc, orc, name):
+    cfg = CASES[name]()[0]
+    assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, hc.HC_ALGO_TC_3XTF32)
+    check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_TC_3XTF32)
+
+
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2"])
 def test_deterministic(hc, name):
     cfg, x, w, b, gy = CASES[name]()
     y1, y2 = R.fwd(cfg, x, w, b), R.fwd(cfg, x, w, b)
@@ -186,4 +207,37 @@ def test_config2_full_size_sampled(hc, orc):
     assert R.normwise(out["gb_partials"][:, chans], gbp_ref) <= TOL_W
     assert R.normwise(out["gb"][chans], gbp_ref.sum(0)) <= TOL_W
     # properties that hold at any size: sum over shards of the partials is the full gradient
+    assert np.abs(out["gw_partials"].astype(np.float64).sum(0) - out["gw"]).max() <= 1e-5 * np.abs(out["gw"]).max()
+
+
+@pytest.mark.slow
+def test_config3_full_size_sampled(hc, orc):
+    """Dense 5x5 128->128, (7,128,128,1024), 4 shards on the tensor-core path,
+    checked on sampled outputs the oracle computes one by one (random positions
+    plus shard-edge columns) and on sampled per-shard weight-gradient partials."""
+    N, C, H, W, K, S = 7, 128, 128, 1024, 5, 4
+    cfg = P.cfg_of(N, C, H, W, C, K, 1, 2, 1, S)
+    assert hc.hc_conv2d_select(hc.desc(cfg), 1) == (0, hc.HC_ALGO_TC_3XTF32)
+    x = synth.normal((N, C, H, W), 1.0, 0, 1)
+    w = synth.kaiming_normal((C, C, K, K), C * K * K, 0, 2)
+    b = synth.normal((C,), 0.01, 0, 3)
+    gy = synth.normal((N, C, H, W), 1.0, 0, 4)
+    y = R.fwd(cfg, x, w, b)
+    out = R.bwd(cfg, x, w, gy)
+    rng = np.random.default_rng(1)
+    pts = [tuple(int(rng.integers(0, s)) for s in (N, C, H, W)) for _ in range(1500)]
+    for col in (0, 1, 254, 255, 256, 257, 511, 512, 767, 768, 1022, 1023):
+        for hrow in (0, 1, 64, 126, 127):
+            pts.append((int(rng.integers(0, N)), int(rng.integers(0, C)), hrow, col))
+    yr = np.array([orc.fwd_at(cfg, x, w, b, *p) for p in pts])
+    assert R.normwise(np.array([y[p] for p in pts]), yr) <= TOL_FWD
+    gr = np.array([orc.gx_at(cfg, w, gy, *p) for p in pts])
+    assert R.normwise(np.array([out["gx"][p] for p in pts]), gr) <= TOL_FWD
+    wpts = [tuple(int(rng.integers(0, s)) for s in (C, C, K, K)) for _ in range(6)] + [(0, 0, 0, 0), (127, 127, 4, 4)]
+    got, ref = [], []
+    for r in range(S):
+        for (co, ci, u, v) in wpts:
+            got.append(out["gw_partials"][r, co, ci, u, v])
+            ref.append(orc.gw_at(cfg, x, gy, co, ci, u, v, r * 256, (r + 1) * 256))
+    assert R.normwise(np.array(got), np.array(ref)) <= TOL_W
     assert np.abs(out["gw_partials"].astype(np.float64).sum(0) - out["gw"]).max() <= 1e-5 * np.abs(out["gw"]).max()
