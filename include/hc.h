@@ -158,6 +158,47 @@ hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, const float* x,
                                           float* gx, float* gw, float* gb, float* gw_partials, float* gb_partials,
                                           void* stream);
 
+/* ---- ConvNeXt block pointwise ops (channels first, shard-local: no halo) ----
+ * The pages train ConvNeXt-XL (NVIDIA blog, design section), whose blocks put
+ * a LayerNorm over channels, a GELU and a layer scale + residual around the
+ * depthwise and 1x1 convolutions.  Tensors are [N][C][HW] fp32 (NCHW with H*W
+ * flattened), device memory, 16-byte aligned; gamma / beta are [C].  Parameter
+ * gradients are per-block partial sums added in a fixed order (the workspace
+ * holds the partials).  Invalid sizes or pointers: HC_ERR_INVALID_ARG. */
+
+/* Workspace bytes for hc_layernorm_c_bwd and hc_layerscale_residual_bwd. */
+hc_status hc_pointwise_workspace_size(int N, int C, long long HW, size_t* bytes);
+
+/* LayerNorm over C at every (n, position): mean, biased variance,
+ * y = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c].  mean / rstd
+ * ([N][HW], may be NULL) keep the statistics for the backward pass. */
+hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const float* gamma, const float* beta,
+                             float eps, float* y, float* mean, float* rstd, void* stream);
+
+/* LayerNorm backward: with xhat = (x - mean) * rstd and g = gy * gamma,
+ * gx = rstd * (g - mean_c(g) - xhat * mean_c(g * xhat));
+ * ggamma[c] = sum gy * xhat, gbeta[c] = sum gy over n and positions (either
+ * may be NULL; then ws may be NULL too). */
+hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const float* gamma, const float* mean,
+                             const float* rstd, const float* gy, float* gx, float* ggamma, float* gbeta, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* GELU, exact form y = x * (1 + erf(x / sqrt 2)) / 2, over n elements. */
+hc_status hc_gelu_fwd(long long n, const float* x, float* y, void* stream);
+
+/* GELU backward: gx = gy * (Phi(x) + x * exp(-x^2 / 2) / sqrt(2 pi)). */
+hc_status hc_gelu_bwd(long long n, const float* x, const float* gy, float* gx, void* stream);
+
+/* Layer scale and residual: out = res + gamma[c] * branch. */
+hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
+                                     const float* gamma, float* out, void* stream);
+
+/* Backward: gbranch = gamma[c] * gy (NULL to skip), ggamma[c] = sum branch * gy;
+ * the residual's gradient is gy itself. */
+hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
+                                     const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
+                                     void* stream);
+
 /* Synchronises `stream`, then returns (and clears) the first error a kernel
  * recorded in the device status word, HC_ERR_CUDA for an asynchronous CUDA
  * error, or HC_OK. */

@@ -85,6 +85,13 @@ size_t bias_grad_ws_floats(int Co, int S);
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
                                     float* tmp, cudaStream_t st);
 
+// out[k] = sum over rows r (ascending, in groups of kColumnGroup) of in[r * stride + k];
+// tmp holds column_sum_tmp_floats(rows, count) floats.
+constexpr int kColumnGroup = 64;
+size_t column_sum_tmp_floats(int rows, int count);
+hc_status launch_column_sum(const float* in, float* out, int rows, int count, long long stride, float* tmp,
+                            cudaStream_t st);
+
 // fixed-order sums
 // out[k] = sum_{r < rows} in[r * count + k], r ascending
 hc_status launch_sum_rows(const float* in, float* out, int rows, long long count, cudaStream_t st);

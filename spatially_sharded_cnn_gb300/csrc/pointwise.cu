@@ -1,0 +1,331 @@
+// pointwise.cu -- the shard-local ops of a ConvNeXt block (the pages' model,
+// NVIDIA blog "Perception model training for autonomous vehicles with tensor
+// parallelism": ConvNeXt-XL blocks): channels-first LayerNorm over C,
+// exact-erf GELU, and layer scale + residual, forward and backward.  None of
+// them reads across W, so they need no halo; their parameter gradients are
+// per-block partial sums added in block order (deterministic).
+//
+// Tensors are [N][C][HW] fp32 (NCHW with the spatial dims flattened).
+#include "common.cuh"
+
+namespace hc {
+namespace {
+
+constexpr int LN_PIX = 32;       // pixels per LayerNorm block
+constexpr int LN_THREADS = 256;  // 8 channel groups x 32 pixels
+
+// LayerNorm over C at every (n, pixel): mean, biased variance (two passes over
+// the staged tile), y = (x - mean) * rstd * gamma[c] + beta[c].
+__global__ void __launch_bounds__(LN_THREADS) ln_fwd_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                                            const float* __restrict__ beta, float eps,
+                                                            float* __restrict__ y, float* __restrict__ mean,
+                                                            float* __restrict__ rstd, int C, long long HW,
+                                                            long long blocks_per_image) {
+    extern __shared__ float tile[];  // [C][LN_PIX]
+    __shared__ float red[8][LN_PIX];
+    __shared__ float stat[2][LN_PIX];
+    const long long b = blockIdx.x;
+    const int n = (int)(b / blocks_per_image);
+    const long long p0 = (b % blocks_per_image) * LN_PIX;
+    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;  // 8 groups of channels
+    const long long p = p0 + px;
+    const bool valid = p < HW;
+    const float* xb = x + (long long)n * C * HW;
+    for (int c = g; c < C; c += 8) tile[c * LN_PIX + px] = valid ? __ldg(xb + (long long)c * HW + p) : 0.0f;
+    // mean
+    float s = 0.0f;
+    for (int c = g; c < C; c += 8) s += tile[c * LN_PIX + px];
+    red[g][px] = s;
+    __syncthreads();
+    if (g == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < 8; k++) t += red[k][px];
+        stat[0][px] = t / C;
+    }
+    __syncthreads();
+    const float mu = stat[0][px];
+    float v = 0.0f;
+    for (int c = g; c < C; c += 8) {
+        const float d = tile[c * LN_PIX + px] - mu;
+        v = fmaf(d, d, v);
+    }
+    red[g][px] = v;
+    __syncthreads();
+    if (g == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < 8; k++) t += red[k][px];
+        stat[1][px] = rsqrtf(t / C + eps);
+    }
+    __syncthreads();
+    const float rs = stat[1][px];
+    if (valid) {
+        float* yb = y + (long long)n * C * HW;
+        for (int c = g; c < C; c += 8)
+            yb[(long long)c * HW + p] = (tile[c * LN_PIX + px] - mu) * rs * __ldg(gamma + c) + __ldg(beta + c);
+        if (g == 0) {
+            if (mean) mean[(long long)n * HW + p] = mu;
+            if (rstd) rstd[(long long)n * HW + p] = rs;
+        }
+    }
+}
+
+// LayerNorm backward: with xhat = (x - mean) * rstd and g = gy * gamma,
+// gx = rstd * (g - mean_c(g) - xhat * mean_c(g * xhat)); the block's partial
+// ggamma / gbeta (sums over its pixels of gy * xhat and gy) go to part[b][2][C].
+__global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                                            const float* __restrict__ mean,
+                                                            const float* __restrict__ rstd,
+                                                            const float* __restrict__ gy, float* __restrict__ gx,
+                                                            float* __restrict__ part, int C, long long HW,
+                                                            long long blocks_per_image) {
+    extern __shared__ float sm[];  // xhat [C][LN_PIX], gy [C][LN_PIX]
+    float* th = sm;
+    float* tg = sm + C * LN_PIX;
+    __shared__ float red[2][8][LN_PIX];
+    __shared__ float stat[2][LN_PIX];
+    const long long b = blockIdx.x;
+    const int n = (int)(b / blocks_per_image);
+    const long long p0 = (b % blocks_per_image) * LN_PIX;
+    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;
+    const long long p = p0 + px;
+    const bool valid = p < HW;
+    const float mu = valid ? __ldg(mean + (long long)n * HW + p) : 0.0f;
+    const float rs = valid ? __ldg(rstd + (long long)n * HW + p) : 0.0f;
+    const float* xb = x + (long long)n * C * HW;
+    const float* gb = gy + (long long)n * C * HW;
+    float s1 = 0.0f, s2 = 0.0f;
+    for (int c = g; c < C; c += 8) {
+        const float xh = valid ? (__ldg(xb + (long long)c * HW + p) - mu) * rs : 0.0f;
+        const float gv = valid ? __ldg(gb + (long long)c * HW + p) : 0.0f;
+        th[c * LN_PIX + px] = xh;
+        tg[c * LN_PIX + px] = gv;
+        const float gg = gv * __ldg(gamma + c);
+        s1 += gg;
+        s2 = fmaf(gg, xh, s2);
+    }
+    red[0][g][px] = s1;
+    red[1][g][px] = s2;
+    __syncthreads();
+    if (g == 0) {
+        float a = 0.0f, c2 = 0.0f;
+        for (int k = 0; k < 8; k++) {
+            a += red[0][k][px];
+            c2 += red[1][k][px];
+        }
+        stat[0][px] = a / C;
+        stat[1][px] = c2 / C;
+    }
+    __syncthreads();
+    const float mg = stat[0][px], mgx = stat[1][px];
+    if (valid) {
+        float* gxb = gx + (long long)n * C * HW;
+        for (int c = g; c < C; c += 8) {
+            const float xh = th[c * LN_PIX + px];
+            const float gg = tg[c * LN_PIX + px] * __ldg(gamma + c);
+            gxb[(long long)c * HW + p] = rs * (gg - mg - xh * mgx);
+        }
+    }
+    // per-channel partials over this block's pixels (pixel order 0..31)
+    if (part) {
+        float* pb = part + b * 2 * C;
+        for (int c = threadIdx.x; c < C; c += LN_THREADS) {
+            float a = 0.0f, bb = 0.0f;
+            for (int k = 0; k < LN_PIX; k++) {
+                a = fmaf(tg[c * LN_PIX + k], th[c * LN_PIX + k], a);
+                bb += tg[c * LN_PIX + k];
+            }
+            pb[c] = a;
+            pb[C + c] = bb;
+        }
+    }
+}
+
+// GELU, exact form: x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2.
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+// d/dx GELU = Phi(x) + x * exp(-x^2 / 2) / sqrt(2 pi)
+__device__ __forceinline__ float gelu_d(float v) {
+    return 0.5f * (1.0f + erff(v * 0.70710678118654752f)) + v * 0.39894228040143268f * expf(-0.5f * v * v);
+}
+
+__global__ void gelu_fwd_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
+    const long long n4 = n / 4;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
+        reinterpret_cast<float4*>(y)[q] = make_float4(gelu_f(v.x), gelu_f(v.y), gelu_f(v.z), gelu_f(v.w));
+    }
+    for (long long q = n4 * 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n;
+         q += (long long)gridDim.x * blockDim.x)
+        y[q] = gelu_f(__ldg(x + q));
+}
+
+__global__ void gelu_bwd_kernel(const float* __restrict__ x, const float* __restrict__ gy, float* __restrict__ gx,
+                                long long n) {
+    const long long n4 = n / 4;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
+        const float4 g = __ldg(reinterpret_cast<const float4*>(gy) + q);
+        reinterpret_cast<float4*>(gx)[q] =
+            make_float4(g.x * gelu_d(v.x), g.y * gelu_d(v.y), g.z * gelu_d(v.z), g.w * gelu_d(v.w));
+    }
+    for (long long q = n4 * 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n;
+         q += (long long)gridDim.x * blockDim.x)
+        gx[q] = __ldg(gy + q) * gelu_d(__ldg(x + q));
+}
+
+// out = res + gamma[c] * branch; one block per (n, c) plane chunk.
+__global__ void ls_fwd_kernel(const float* __restrict__ res, const float* __restrict__ br,
+                              const float* __restrict__ gamma, float* __restrict__ out, int C, long long HW,
+                              int chunks) {
+    const long long plane = blockIdx.x / chunks;
+    const int chunk = blockIdx.x % chunks;
+    const float gm = __ldg(gamma + plane % C);
+    const long long b0 = HW * chunk / chunks, b1 = HW * (chunk + 1) / chunks;
+    const long long off = plane * HW;
+    for (long long q = b0 + threadIdx.x; q < b1; q += blockDim.x) out[off + q] = fmaf(gm, __ldg(br + off + q), __ldg(res + off + q));
+}
+
+// gbranch = gamma[c] * gy; partial ggamma of this chunk = sum branch * gy (fixed order).
+__global__ void ls_bwd_kernel(const float* __restrict__ br, const float* __restrict__ gamma,
+                              const float* __restrict__ gy, float* __restrict__ gbr, float* __restrict__ part, int C,
+                              long long HW, int chunks) {
+    __shared__ float red[32];
+    const long long plane = blockIdx.x / chunks;
+    const int chunk = blockIdx.x % chunks;
+    const float gm = __ldg(gamma + plane % C);
+    const long long b0 = HW * chunk / chunks, b1 = HW * (chunk + 1) / chunks;
+    const long long off = plane * HW;
+    float acc = 0.0f;
+    for (long long q = b0 + threadIdx.x; q < b1; q += blockDim.x) {
+        const float g = __ldg(gy + off + q);
+        if (gbr) gbr[off + q] = gm * g;
+        acc = fmaf(__ldg(br + off + q), g, acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < (int)(blockDim.x >> 5); k++) t += red[k];
+        part[blockIdx.x] = t;  // [plane][chunk]
+    }
+}
+
+// ggamma[c] = sum over (n, chunk) of part[(n * C + c) * chunks + chunk], n then chunk ascending.
+__global__ void ls_reduce_kernel(const float* __restrict__ part, float* __restrict__ gg, int N, int C, int chunks) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float t = 0.0f;
+    for (int n = 0; n < N; n++)
+        for (int k = 0; k < chunks; k++) t += part[((long long)n * C + c) * chunks + k];
+    gg[c] = t;
+}
+
+constexpr int LS_CHUNKS = 16;
+
+bool al16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
+
+unsigned grid_elems(long long n) {
+    const long long b = (n / 4 + 255) / 256;
+    return (unsigned)(b < 1 ? 1 : (b > 152LL * 32 ? 152LL * 32 : b));
+}
+
+}  // namespace
+}  // namespace hc
+
+using namespace hc;
+
+extern "C" {
+
+hc_status hc_pointwise_workspace_size(int N, int C, long long HW, size_t* bytes) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !bytes) return HC_ERR_INVALID_ARG;
+    const long long ln_blocks = (long long)N * ((HW + LN_PIX - 1) / LN_PIX);
+    if (ln_blocks > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+    const size_t ln = sizeof(float) * ((size_t)ln_blocks * 2 * C + column_sum_tmp_floats((int)ln_blocks, C) + 64);
+    const size_t ls = sizeof(float) * (size_t)N * C * LS_CHUNKS;
+    *bytes = ln > ls ? ln : ls;
+    return HC_OK;
+}
+
+hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const float* gamma, const float* beta,
+                             float eps, float* y, float* mean, float* rstd, void* stream) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !beta || !y || !(eps >= 0.0f)) return HC_ERR_INVALID_ARG;
+    const size_t smem = sizeof(float) * (size_t)C * LN_PIX;
+    if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(ln_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr = true;
+    }
+    const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
+    ln_fwd_kernel<<<(unsigned)(N * bpi), LN_THREADS, smem, (cudaStream_t)stream>>>(x, gamma, beta, eps, y, mean, rstd, C,
+                                                                                 HW, bpi);
+    return launched();
+}
+
+hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const float* gamma, const float* mean,
+                             const float* rstd, const float* gy, float* gx, float* ggamma, float* gbeta, void* ws,
+                             size_t ws_bytes, void* stream) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !mean || !rstd || !gy || !gx) return HC_ERR_INVALID_ARG;
+    size_t need = 0;
+    hc_pointwise_workspace_size(N, C, HW, &need);
+    const bool want_p = ggamma || gbeta;
+    if (want_p && (ws_bytes < need || !ws || !al16(ws))) return HC_ERR_WORKSPACE;
+    const size_t smem = sizeof(float) * (size_t)2 * C * LN_PIX;
+    if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr = true;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
+    const long long blocks = N * bpi;
+    float* part = want_p ? (float*)ws : nullptr;
+    ln_bwd_kernel<<<(unsigned)blocks, LN_THREADS, smem, st>>>(x, gamma, mean, rstd, gy, gx, part, C, HW, bpi);
+    hc_status s = launched();
+    if (s || !want_p) return s;
+    // part is [blocks][2][C]: summed over blocks in block order
+    float* tmp = part + (size_t)blocks * 2 * C;
+    if (ggamma && (s = launch_column_sum(part, ggamma, (int)blocks, C, 2 * (long long)C, tmp, st))) return s;
+    if (gbeta && (s = launch_column_sum(part + C, gbeta, (int)blocks, C, 2 * (long long)C, tmp, st))) return s;
+    return HC_OK;
+}
+
+hc_status hc_gelu_fwd(long long n, const float* x, float* y, void* stream) {
+    if (n <= 0 || !x || !y || !al16(x) || !al16(y)) return HC_ERR_INVALID_ARG;
+    gelu_fwd_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(x, y, n);
+    return launched();
+}
+
+hc_status hc_gelu_bwd(long long n, const float* x, const float* gy, float* gx, void* stream) {
+    if (n <= 0 || !x || !gy || !gx || !al16(x) || !al16(gy) || !al16(gx)) return HC_ERR_INVALID_ARG;
+    gelu_bwd_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(x, gy, gx, n);
+    return launched();
+}
+
+hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
+                                     const float* gamma, float* out, void* stream) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !res || !branch || !gamma || !out) return HC_ERR_INVALID_ARG;
+    ls_fwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, (cudaStream_t)stream>>>(res, branch, gamma, out,
+                                                                                            C, HW, LS_CHUNKS);
+    return launched();
+}
+
+hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
+                                     const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
+                                     void* stream) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !branch || !gamma || !gy || !ggamma) return HC_ERR_INVALID_ARG;
+    size_t need = 0;
+    hc_pointwise_workspace_size(N, C, HW, &need);
+    if (ws_bytes < need || !ws || !al16(ws)) return HC_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    float* part = (float*)ws;
+    ls_bwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, st>>>(branch, gamma, gy, gbranch, part, C, HW,
+                                                                          LS_CHUNKS);
+    hc_status s = launched();
+    if (s) return s;
+    ls_reduce_kernel<<<(C + 127) / 128, 128, 0, st>>>(part, ggamma, N, C, LS_CHUNKS);
+    return launched();
+}
+
+}  // extern "C"

@@ -51,7 +51,37 @@ __global__ void bias_slices_kernel(const float* __restrict__ gy, float* __restri
     }
 }
 
+// Column sums, stage 1: tmp[g][k] = sum over rows r in group g (ascending) of
+// in[r * stride + k].
+__global__ void column_group_kernel(const float* __restrict__ in, float* __restrict__ tmp, int rows, int count,
+                                    long long stride, int group) {
+    const long long total = (long long)((rows + group - 1) / group) * count;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int k = (int)(q % count), g = (int)(q / count);
+        const int r0 = g * group, r1 = r0 + group < rows ? r0 + group : rows;
+        float s = 0.0f;
+        for (int r = r0; r < r1; r++) s += __ldg(in + r * stride + k);
+        tmp[q] = s;
+    }
+}
+
 }  // namespace
+
+size_t column_sum_tmp_floats(int rows, int count) {
+    return (size_t)((rows + kColumnGroup - 1) / kColumnGroup) * count;
+}
+
+hc_status launch_column_sum(const float* in, float* out, int rows, int count, long long stride, float* tmp,
+                            cudaStream_t st) {
+    const long long total = (long long)((rows + kColumnGroup - 1) / kColumnGroup) * count;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    column_group_kernel<<<(unsigned)blocks, 256, 0, st>>>(in, tmp, rows, count, stride, kColumnGroup);
+    hc_status s = launched();
+    if (s) return s;
+    return launch_sum_rows(tmp, out, (rows + kColumnGroup - 1) / kColumnGroup, count, st);
+}
 
 size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co; }
 

@@ -75,6 +75,17 @@ _lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_
 _lib.hc_halo_gather.argtypes = [_D, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.restype = C.c_int
+_I, _L, _F = C.c_int, C.c_longlong, C.c_float
+_lib.hc_pointwise_workspace_size.argtypes = [_I, _I, _L, C.POINTER(C.c_size_t)]
+_lib.hc_layernorm_c_fwd.argtypes = [_I, _I, _L, _P, _P, _P, _F, _P, _P, _P, _P]
+_lib.hc_layernorm_c_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
+_lib.hc_gelu_fwd.argtypes = [_L, _P, _P, _P]
+_lib.hc_gelu_bwd.argtypes = [_L, _P, _P, _P, _P]
+_lib.hc_layerscale_residual_fwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P]
+_lib.hc_layerscale_residual_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
+for _n in ("hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
+           "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd"):
+    getattr(_lib, _n).restype = C.c_int
 _lib.hc_sync_check.argtypes = [_P]
 _lib.hc_status_string.argtypes = [C.c_int]
 _lib.hc_status_string.restype = C.c_char_p
@@ -88,6 +99,8 @@ EXPORTS = [
     "hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo", "hc_conv2d_select",
     "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
     "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
+    "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
+    "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd",
 ]
 
 
@@ -147,6 +160,41 @@ def hc_conv2d_bwd_depthwise_noalloc(d, x, w, gy, gx, gw, gb, gw_partials=None, g
 
 def hc_halo_gather(d, x, x_ext, stream=None) -> int:
     return _lib.hc_halo_gather(C.byref(d), _ptr(x), _ptr(x_ext), _stream(stream))
+
+
+def hc_pointwise_workspace_size(N, C_, HW):
+    b = C.c_size_t(0)
+    st = _lib.hc_pointwise_workspace_size(int(N), int(C_), int(HW), C.byref(b))
+    return st, b.value
+
+
+def hc_layernorm_c_fwd(N, C_, HW, x, gamma, beta, eps, y, mean=None, rstd=None, stream=None) -> int:
+    return _lib.hc_layernorm_c_fwd(int(N), int(C_), int(HW), _ptr(x), _ptr(gamma), _ptr(beta), float(eps), _ptr(y),
+                                   _ptr(mean), _ptr(rstd), _stream(stream))
+
+
+def hc_layernorm_c_bwd(N, C_, HW, x, gamma, mean, rstd, gy, gx, ggamma=None, gbeta=None, ws=None, ws_bytes=0,
+                       stream=None) -> int:
+    return _lib.hc_layernorm_c_bwd(int(N), int(C_), int(HW), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(gy),
+                                   _ptr(gx), _ptr(ggamma), _ptr(gbeta), _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def hc_gelu_fwd(n, x, y, stream=None) -> int:
+    return _lib.hc_gelu_fwd(int(n), _ptr(x), _ptr(y), _stream(stream))
+
+
+def hc_gelu_bwd(n, x, gy, gx, stream=None) -> int:
+    return _lib.hc_gelu_bwd(int(n), _ptr(x), _ptr(gy), _ptr(gx), _stream(stream))
+
+
+def hc_layerscale_residual_fwd(N, C_, HW, res, branch, gamma, out, stream=None) -> int:
+    return _lib.hc_layerscale_residual_fwd(int(N), int(C_), int(HW), _ptr(res), _ptr(branch), _ptr(gamma), _ptr(out),
+                                           _stream(stream))
+
+
+def hc_layerscale_residual_bwd(N, C_, HW, branch, gamma, gy, gbranch, ggamma, ws, ws_bytes, stream=None) -> int:
+    return _lib.hc_layerscale_residual_bwd(int(N), int(C_), int(HW), _ptr(branch), _ptr(gamma), _ptr(gy),
+                                           _ptr(gbranch), _ptr(ggamma), _ptr(ws), int(ws_bytes), _stream(stream))
 
 
 def hc_sync_check(stream=None) -> int:
