@@ -165,7 +165,8 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
             float* btmp = (float*)wsp;
             wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.S));
             if ((gx || want_w) && (st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s))) return st;
-            if (want_b) st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl, btmp, s);
+            if (want_b)
+                st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl / d->stride, btmp, s);
             break;
         }
         case HC_ALGO_DIRECT:

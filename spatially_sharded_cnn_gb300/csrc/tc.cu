@@ -177,7 +177,8 @@ struct TcParams {
     // conv mode
     int N, Ho, Wo, M, Kc, kh, kw, pad, tiles_w, mblocks;
     const float* bias;
-    float* out;     // NCHW [N][M][Ho][Wo]
+    float* out;     // NCHW [N][M][Ho][Wo], or with d2s > 0 the image [N][d2s_c][Ho*d2s][Wo*d2s]
+    int d2s, d2s_c; // depth-to-space store: row m = (u*d2s + v)*d2s_c + c goes to pixel (ho*d2s+u, wo*d2s+v)
     // wgrad mode
     int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // row_chunks = own_w / 32
     long long shard_chunks;                               // N * Ho * row_chunks
@@ -388,7 +389,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lane == 0) mbar_arrive(&sh.buf_empty[b]);
             }
             if (!ok) break;
-            if (p.mode == 0) {
+            if (p.mode == 0 && p.d2s) {
+                const int m = u.m0 + row, sd = p.d2s;
+                if (m < sd * sd * p.d2s_c) {
+                    const int tap = m / p.d2s_c, c = m - tap * p.d2s_c, uu = tap / sd, vv = tap - uu * sd;
+                    const int Wimg = p.Wo * sd;
+                    float* dst = p.out + (((long long)u.n * p.d2s_c + c) * p.Ho * sd + u.ho * sd + uu) * Wimg +
+                                 (long long)(u.w0 + half * HC) * sd + vv;
+#pragma unroll
+                    for (int k = 0; k < HC; k++) dst[(long long)k * sd] = acc[k];
+                }
+            } else if (p.mode == 0) {
                 const int m = u.m0 + row;
                 const float bv = p.bias ? __ldg(p.bias + m) : 0.0f;
                 float* dst = p.out + (((long long)u.n * p.M + m) * p.Ho + u.ho) * p.Wo + u.w0 + half * HC;
@@ -517,6 +528,99 @@ __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict
     }
 }
 
+// Space-to-depth for a k = stride = s convolution without padding (each output
+// pixel reads one s x s block): channel k = (u*s + v)*C + c of output pixel
+// (ho, wo) is x[c][ho*s + u][wo*s + v]; channels k >= s*s*C are zero.
+//   NHWC form [N][Ho][Wo][Kp] (the forward's B operand), tf32 hi / lo.
+__global__ void prep_s2d_nhwc_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                     int C, int H, int W, int s, int Kp, long long total) {
+    const int Ho = H / s, Wo = W / s;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int k = (int)(q % Kp);
+        const long long pix = q / Kp;
+        const int wo = (int)(pix % Wo);
+        const long long r2 = pix / Wo;
+        const int ho = (int)(r2 % Ho), n = (int)(r2 / Ho);
+        float v = 0.0f;
+        if (k < s * s * C) {
+            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
+            v = __ldg(x + (((long long)n * C + c) * H + ho * s + uu) * W + wo * s + vv);
+        }
+        const float h = tf32_rna(v);
+        hi[q] = h;
+        lo[q] = tf32_rna(v - h);
+    }
+}
+//   planar form [N][Kp][Ho][Wo] (the weight gradient's B operand: pixels contiguous).
+__global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                       int C, int H, int W, int s, int Kp, long long total) {
+    const int Ho = H / s, Wo = W / s;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int wo = (int)(q % Wo);
+        const long long r1 = q / Wo;
+        const int ho = (int)(r1 % Ho);
+        const long long r2 = r1 / Ho;
+        const int k = (int)(r2 % Kp), n = (int)(r2 / Kp);
+        float v = 0.0f;
+        if (k < s * s * C) {
+            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
+            v = __ldg(x + (((long long)n * C + c) * H + ho * s + uu) * W + wo * s + vv);
+        }
+        const float h = tf32_rna(v);
+        hi[q] = h;
+        lo[q] = tf32_rna(v - h);
+    }
+}
+// Weights in space-to-depth order: forward A[co][k] = w[co][c][u][v];
+// grad_input (transpose) A[k][co] = w[co][c][u][v]; k = (u*s + v)*C + c < s*s*C.
+__global__ void prep_weight_s2d_kernel(const float* __restrict__ w, float* __restrict__ hi, float* __restrict__ lo,
+                                       int Co, int C, int s, int Kp, int transpose) {
+    const long long total = (long long)Co * Kp;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        int co, k;
+        if (!transpose) {
+            co = (int)(q / Kp);
+            k = (int)(q % Kp);
+        } else {
+            k = (int)(q / Co);
+            co = (int)(q % Co);
+        }
+        float v = 0.0f;
+        if (k < s * s * C) {
+            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
+            v = __ldg(w + (((long long)co * C + c) * s + uu) * s + vv);
+        }
+        const float h = tf32_rna(v);
+        hi[q] = h;
+        lo[q] = tf32_rna(v - h);
+    }
+}
+// Weight-gradient partials in space-to-depth order back to [S][Co][C][s][s]:
+// gwp[r][co][c][u][v] = sum_j part[r][j][co][(u*s + v)*C + c] (j ascending).
+__global__ void wgrad_reduce_s2d_kernel(const float* __restrict__ part, float* __restrict__ gwp, int S, int J, int Co,
+                                        int C, int s, int Kp) {
+    const long long per = (long long)Co * C * s * s;
+    const long long total = (long long)S * per;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(q / per);
+        long long rem = q % per;
+        const int vv = (int)(rem % s);
+        rem /= s;
+        const int uu = (int)(rem % s);
+        rem /= s;
+        const int c = (int)(rem % C), co = (int)(rem / C);
+        const int k = (uu * s + vv) * C + c;
+        const float* src = part + ((long long)r * J * Co + co) * Kp + k;
+        float t = 0.0f;
+        for (int j = 0; j < J; j++) t += src[(long long)j * Co * Kp];
+        gwp[q] = t;
+    }
+}
+
 // Weight-gradient partials: gwp[r][co][ci][tap] = sum_j part[r][j][tap][co][ci] (j ascending).
 __global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ gwp, int S, int J, int taps,
                                     int Co, int Ci) {
@@ -599,9 +703,9 @@ hc_status nchw_map(CUtensorMap* m, const float* base, int N, int C, int H, int W
     const uint32_t box[4] = {32, 1, (uint32_t)rows, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// The four column-shifted copies: dims (Wc, H, C, N, 4), box (32, 1, rows, 1, 1).
-hc_status shifted_map(CUtensorMap* m, const float* base, int N, int C, int H, int Wc, int rows) {
-    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)H, (uint64_t)C, (uint64_t)N, 4};
+// Column-shifted copies: dims (Wc, H, C, N, copies), box (32, 1, rows, 1, 1).
+hc_status shifted_map(CUtensorMap* m, const float* base, int N, int C, int H, int Wc, int rows, int copies = 4) {
+    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)H, (uint64_t)C, (uint64_t)N, (uint64_t)copies};
     const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)H * Wc * 4, (uint64_t)C * H * Wc * 4,
                                  (uint64_t)N * C * H * Wc * 4};
     const uint32_t box[5] = {32, 1, (uint32_t)rows, 1, 1};
@@ -613,10 +717,23 @@ size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 // weight-gradient tiles: 128 output channels x 128 input channels of one tap
 constexpr int WG_BN = 128;
 
+
+// k = stride = s >= 2 without padding: every output pixel reads its own s x s
+// block, so the conv is a 1x1 conv of the space-to-depth image.
+bool is_s2d(const hc_conv_desc* d) {
+    return d->groups == 1 && d->stride >= 2 && d->kh == d->stride && d->kw == d->stride && d->padding == 0;
+}
+int s2d_kp(const hc_conv_desc* d) { return (d->stride * d->stride * d->C_in + 127) / 128 * 128; }
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
 bool tc_supported(const hc_conv_desc* d, const Plan& p) {
+    if (is_s2d(d)) {
+        const int s = d->stride;
+        return d->C_out % BM == 0 && d->H % s == 0 && d->W % s == 0 && pick_bn(p.Wl / s) != 0 &&
+               (p.Wl / s) % 32 == 0 && p.Wo == d->W / s && p.Ho == d->H / s;
+    }
     if (d->groups != 1 || d->stride != 1 || d->kh != d->kw || d->padding != (d->kh - 1) / 2 || d->kh % 2 == 0)
         return false;
     if (d->C_out % BM || d->C_in % BM) return false;  // forward rows and grad_input rows in 128-blocks
@@ -626,9 +743,11 @@ bool tc_supported(const hc_conv_desc* d, const Plan& p) {
 }
 
 int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
-    const int KK = d->kh * d->kw;
-    const long long units0 = (long long)(d->C_out / BM) * KK * (d->C_in / WG_BN) * p.S;
-    const long long chunks = (long long)d->N * p.Ho * (p.Wl / 32);
+    const bool sd = is_s2d(d);
+    const int KK = sd ? 1 : d->kh * d->kw;
+    const int nb = sd ? s2d_kp(d) / WG_BN : d->C_in / WG_BN;
+    const long long units0 = (long long)(d->C_out / BM) * KK * nb * p.S;
+    const long long chunks = (long long)d->N * p.Ho * ((p.Wl / d->stride) / 32);
     // enough units for about four waves, each unit at least 64 chunks long
     long long J = (4LL * sm_count_tc() + units0 - 1) / units0;
     if (J > chunks / 64) J = chunks / 64;
@@ -639,6 +758,13 @@ int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
 // Workspace: forward  [x NHWC hi][x NHWC lo][A hi][A lo]
 //            backward [gy NHWC hi][lo][A' hi][lo][gy NCHW hi][lo][x shifted hi][lo][split-K partials]
 size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
+    if (is_s2d(d)) {  // forward [s2d NHWC hi][lo][A hi][lo]; backward [gy NHWC hi][lo][A' hi][lo][gy NCHW hi][lo][s2d planar hi][lo][partials]
+        const size_t npx = (size_t)d->N * p.Ho * p.Wo, kp = s2d_kp(d);
+        const size_t ns = npx * kp, ng = npx * d->C_out, wsz = (size_t)d->C_out * kp;
+        if (pass == 0) return 2 * al256(4 * ns) + 2 * al256(4 * wsz);
+        const size_t part = al256(4 * (size_t)p.S * tc_wgrad_splits(d, p) * wsz);
+        return 4 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ns) + part;
+    }
     const int KK = d->kh * d->kw;
     const size_t nx = (size_t)d->N * d->C_in * d->H * d->W;
     const size_t ng = (size_t)d->N * d->C_out * p.Ho * p.Wo;
@@ -650,8 +776,142 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
 }
 
+static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                         float* y, void* ws, cudaStream_t st) {
+    const int s = d->stride, Co = d->C_out, Kp = s2d_kp(d);
+    const size_t ns = (size_t)d->N * p.Ho * p.Wo * Kp, wsz = (size_t)Co * Kp;
+    char* q = (char*)ws;
+    float* xh = (float*)q;
+    q += al256(4 * ns);
+    float* xl = (float*)q;
+    q += al256(4 * ns);
+    float* ah = (float*)q;
+    q += al256(4 * wsz);
+    float* al = (float*)q;
+    prep_s2d_nhwc_kernel<<<cdiv((long long)ns, 256) < 152u * 64 ? cdiv((long long)ns, 256) : 152u * 64, 256, 0, st>>>(
+        x, xh, xl, d->C_in, d->H, d->W, s, Kp, (long long)ns);
+    hc_status e = launched();
+    if (e) return e;
+    prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, d->C_in, s, Kp, 0);
+    if ((e = launched())) return e;
+    const int BN = pick_bn(p.Wl / s);
+    TcParams tp{};
+    tp.mode = 0;
+    tp.N = d->N;
+    tp.Ho = p.Ho;
+    tp.Wo = p.Wo;
+    tp.M = Co;
+    tp.Kc = Kp;
+    tp.kh = 1;
+    tp.kw = 1;
+    tp.pad = 0;
+    tp.tiles_w = p.Wo / BN;
+    tp.mblocks = Co / BM;
+    tp.chunks = Kp / BK;
+    tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
+    tp.bias = b;
+    tp.out = y;
+    CUtensorMap mah, mal, mbh, mbl;
+    if ((e = weight_map(&mah, ah, Co, Kp)) || (e = weight_map(&mal, al, Co, Kp)) ||
+        (e = act_map_conv(&mbh, xh, d->N, p.Ho, p.Wo, Kp, BN)) || (e = act_map_conv(&mbl, xl, d->N, p.Ho, p.Wo, Kp, BN)))
+        return e;
+    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st);
+}
+
+static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
+                         float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+    const int s = d->stride, Co = d->C_out, Ci = d->C_in, Kp = s2d_kp(d);
+    const size_t npx = (size_t)d->N * p.Ho * p.Wo, ns = npx * Kp, ng = npx * Co, wsz = (size_t)Co * Kp;
+    char* q = (char*)ws;
+    float* gh = (float*)q;
+    q += al256(4 * ng);
+    float* gl = (float*)q;
+    q += al256(4 * ng);
+    float* ah = (float*)q;
+    q += al256(4 * wsz);
+    float* al = (float*)q;
+    q += al256(4 * wsz);
+    float* gch = (float*)q;
+    q += al256(4 * ng);
+    float* gcl = (float*)q;
+    q += al256(4 * ng);
+    float* sh = (float*)q;
+    q += al256(4 * ns);
+    float* sl = (float*)q;
+    q += al256(4 * ns);
+    float* part = (float*)q;
+    const int BN = pick_bn(p.Wl / s);
+    hc_status e;
+    if (gx) {  // D[(u,v,c)][px] = sum_co w[co][c][u][v] gy[co][px], stored depth-to-space
+        prep_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(Co, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(gy, gh, gl, Co,
+                                                                                                p.Ho, p.Wo, Co);
+        if ((e = launched())) return e;
+        prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, s, Kp, 1);
+        if ((e = launched())) return e;
+        TcParams tp{};
+        tp.mode = 0;
+        tp.N = d->N;
+        tp.Ho = p.Ho;
+        tp.Wo = p.Wo;
+        tp.M = Kp;
+        tp.Kc = Co;
+        tp.kh = 1;
+        tp.kw = 1;
+        tp.pad = 0;
+        tp.tiles_w = p.Wo / BN;
+        tp.mblocks = Kp / BM;
+        tp.chunks = Co / BK;
+        tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
+        tp.out = gx;
+        tp.d2s = s;
+        tp.d2s_c = Ci;
+        CUtensorMap mah, mal, mbh, mbl;
+        if ((e = weight_map(&mah, ah, Kp, Co)) || (e = weight_map(&mal, al, Kp, Co)) ||
+            (e = act_map_conv(&mbh, gh, d->N, p.Ho, p.Wo, Co, BN)) ||
+            (e = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)))
+            return e;
+        if ((e = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return e;
+    }
+    if (want_w) {  // G[co][(u,v,c)] = sum over a shard's pixels of gy[co][px] s2d[(u,v,c)][px]
+        prep_split_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, (long long)ng / 4);
+        if ((e = launched())) return e;
+        prep_s2d_planar_kernel<<<cdiv((long long)ns, 256) < 152u * 64 ? cdiv((long long)ns, 256) : 152u * 64, 256, 0,
+                                 st>>>(x, sh, sl, Ci, d->H, d->W, s, Kp, (long long)ns);
+        if ((e = launched())) return e;
+        TcParams tp{};
+        tp.mode = 1;
+        tp.Co = Co;
+        tp.Ci = Kp;
+        tp.S = p.S;
+        tp.J = tc_wgrad_splits(d, p);
+        tp.own_w = p.Wl / s;
+        tp.row_chunks = tp.own_w / 32;
+        tp.Ho = p.Ho;
+        tp.kh = 1;
+        tp.kw = 1;
+        tp.pad = 0;
+        tp.taps = 1;
+        tp.mblocks = Co / BM;
+        tp.nblocks = Kp / WG_BN;
+        tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
+        tp.units = tp.mblocks * tp.nblocks * tp.J * p.S;
+        tp.part = part;
+        CUtensorMap mah, mal, mbh, mbl;
+        if ((e = nchw_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (e = nchw_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (e = shifted_map(&mbh, sh, d->N, Kp, p.Ho, p.Wo, WG_BN, 1)) ||
+            (e = shifted_map(&mbl, sl, d->N, Kp, p.Ho, p.Wo, WG_BN, 1)))
+            return e;
+        if ((e = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return e;
+        const long long total = (long long)p.S * Co * Ci * s * s;
+        wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, Co, Ci, s, Kp);
+        if ((e = launched())) return e;
+    }
+    return HC_OK;
+}
+
 hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                         float* y, void* ws, cudaStream_t st) {
+    if (is_s2d(d)) return s2d_fwd(d, p, x, w, b, y, ws, st);
     const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
     const size_t nx = (size_t)d->N * Ci * d->H * d->W, wsz = (size_t)Co * KK * Ci;
     char* q = (char*)ws;
@@ -695,6 +955,7 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
                         float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+    if (is_s2d(d)) return s2d_bwd(d, p, x, w, gy, gx, gwp, want_w, ws, st);
     const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
     const size_t ng = (size_t)d->N * Co * p.Ho * p.Wo, wsz = (size_t)Co * KK * Ci;
     const int Wc = d->W + 4;

@@ -56,6 +56,15 @@ def tc_case(N, Ci, H, W, Co, K, S, seed=3):
     return cfg, x, w, b, gy
 
 
+def tc_strided_case(N, Ci, H, W, Co, s, S, seed=4):
+    cfg = P.cfg_of(N, Ci, H, W, Co, s, s, 0, 1, S)
+    x = synth.uniform((N, Ci, H, W), 0.0, 1.0, seed, 1)
+    w = synth.trunc_normal((Co, Ci, s, s), 0.02, seed, 2)
+    b = synth.normal((Co,), 0.01, seed, 3)
+    gy = synth.normal((N, Co, H // s, W // s), 1.0, seed, 4)
+    return cfg, x, w, b, gy
+
+
 def generic_case(cfg, seed=2):
     x, w, b, gy = P.rand_case(cfg, seed)
     return cfg, x, w, b, gy
@@ -79,6 +88,9 @@ CASES = {
     "tc_3x3_two_mblocks": lambda: tc_case(1, 128, 5, 256, 256, 3, 1),
     "tc_1x1": lambda: tc_case(2, 256, 4, 128, 128, 1, 1),
     "tc_5x5_ragged_two_tiles": lambda: tc_case(1, 128, 7, 512, 128, 5, 1),
+    # strided k = stride convs through space-to-depth (stem- and downsample-like)
+    "tc_stem4x4s4": lambda: tc_strided_case(2, 3, 12, 512, 128, 4, 1),
+    "tc_down2x2s2_S2": lambda: tc_strided_case(1, 128, 6, 512, 256, 2, 2),
 }
 
 
@@ -118,7 +130,8 @@ def test_parity_depthwise_explicit(hc, orc, name):
     check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_DEPTHWISE)
 
 
-@pytest.mark.parametrize("name", ["tc_5x5_S2", "tc_3x3_two_mblocks", "tc_1x1", "tc_5x5_ragged_two_tiles"])
+@pytest.mark.parametrize("name", ["tc_5x5_S2", "tc_3x3_two_mblocks", "tc_1x1", "tc_5x5_ragged_two_tiles",
+                                  "tc_stem4x4s4", "tc_down2x2s2_S2"])
 def test_parity_tensor_cores_explicit(hc, orc, name):
     cfg = CASES[name]()[0]
     assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, hc.HC_ALGO_TC_3XTF32)
