@@ -1,24 +1,34 @@
 """Benchmark of the width-sharded (halo-exchange) Conv2d, forward + backward.
 
-One step = one pass of the whole hot path over one batch: hc_conv2d_fwd (shard
-plan, halo exchange + concat, local conv, crop) then hc_conv2d_bwd (grad_output
-halo, grad_input, per-shard _Partial grad_weight / grad_bias, fixed-order
-reduction), through the C ABI on the current CUDA stream.
+One step = one pass of the whole hot path over one batch, through the C ABI on
+the current CUDA stream: hc_conv2d_fwd (shard plan, halo exchange + concat,
+local conv, crop) then hc_conv2d_bwd (grad_output halo, grad_input, per-shard
+_Partial grad_weight / grad_bias, fixed-order reduction).
 
-Default workload: ConvNeXt depthwise 7x7, padding 3, groups = C, fp32,
-x (7,256,128,512) N(0,1), weight (256,1,7,7) trunc-normal std 0.02, bias 0,
-grad_output N(0,1), 4 W-shards of width 128; seed 0.  Metric: algorithmic HBM
-bytes per step (x + y forward; x + grad_output + grad_input backward) over the
-step time, in GB/s.  Inputs are 470 MB each, larger than the 129 MB L2, so no
-L2 flush is needed between steps.
+Workloads (--workload):
+  dw7       (default) ConvNeXt depthwise 7x7, padding 3, groups = C, fp32,
+            x (7,256,128,512) N(0,1), weight (256,1,7,7) trunc-normal std 0.02,
+            bias 0, grad_output N(0,1), 4 W-shards of width 128.  Metric:
+            algorithmic HBM bytes per step (x + y forward; x + grad_output +
+            grad_input backward) over the step time, GB/s.
+  dense5x5  dense 5x5 conv 128->128 (3xTF32 tensor cores), x (7,128,128,1024),
+            4 W-shards of width 256; TFLOP/s of the fp32 convolution FLOPs.
+  block     ConvNeXt-XL stage-1 block on the stem output of a (7,3,512,4096)
+            U[0,1] image, 8 W-shards: 4x4/s4 stem 3->256, depthwise 7x7,
+            LayerNorm over C, 1x1 256->1024, GELU, 1x1 1024->256, layer scale
+            1e-6 + residual; forward + backward; TFLOP/s of the conv FLOPs.
+  dwdown    depthwise 7x7 then 2x2/s2 downsample 256->512 on x
+            (7,256,128,2048), 8 W-shards; forward + backward; TFLOP/s.
+All inputs are larger than the 129 MB L2, so no flush is needed between steps.
 
-Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload ...]
 For N > 1 it runs under torch.distributed.run, one replica per GPU (each rank
 its own batch; no data-path collective), and reports the whole-job total.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -43,77 +53,333 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, sm_max_mhz=2070.0, src="fallback")
 
 
-class DepthwiseWorkload:
-    name = "convnext_dw7x7_fwd_bwd"
+def conv_cfg(N, Ci, H, W, Co, k, s, p, g, S):
+    return dict(N=N, C_in=Ci, H=H, W=W, C_out=Co, kh=k, kw=k, stride=s, padding=p, groups=g, num_shards=S)
 
-    def __init__(self, N=7, C=256, H=128, W=512, K=7, S=4, seed=0):
-        self.cfg = dict(N=N, C_in=C, H=H, W=W, C_out=C, kh=K, kw=K, stride=1, padding=(K - 1) // 2, groups=C,
-                        num_shards=S)
-        self.K = K
-        self.E = N * C * H * W
-        self.seed = seed
-        # algorithmic bytes: forward reads x, writes y; backward reads x and gy, writes gx
-        self.bytes_fwd = 2 * 4 * self.E
-        self.bytes_bwd = 3 * 4 * self.E
-        self.bytes = self.bytes_fwd + self.bytes_bwd
-        self.flops_bwd = 2 * 2 * K * K * self.E
-        self.flops = 3 * 2 * K * K * self.E
+
+def conv_flops(cfg):
+    Ho = (cfg["H"] + 2 * cfg["padding"] - cfg["kh"]) // cfg["stride"] + 1
+    Wo = (cfg["W"] + 2 * cfg["padding"] - cfg["kw"]) // cfg["stride"] + 1
+    return 2.0 * cfg["N"] * Ho * Wo * cfg["C_out"] * (cfg["C_in"] // cfg["groups"]) * cfg["kh"] * cfg["kw"]
+
+
+def tc_peak(peaks):
+    """3xTF32 peak (fp32-equivalent): measured bf16 dense rate x the nominal
+    tf32/bf16 ratio (1.1 / 2.25 PFLOP/s), / 3 for the three TF32 passes."""
+    return peaks["bf16"] * (1.1 / 2.25) / 3
+
+
+def alu_peak(peaks, sms):
+    return sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
+class Runner:
+    """Device state shared by the workloads: the C ABI, a stream, one workspace,
+    and per-op CUDA events for the op breakdown."""
+
+    def __init__(self, hc, torch, dev, stream):
+        self.hc, self.torch, self.dev, self.stream = hc, torch, dev, stream
+        self.ws = None
+        self.ws_bytes = 0
+        self.mark = None  # when set: list collecting (name, start event, end event)
+
+    def empty(self, shape):
+        return self.torch.empty(shape, dtype=self.torch.float32, device=self.dev)
+
+    def upload(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def reserve(self, nbytes):
+        if nbytes > self.ws_bytes:
+            self.ws = self.torch.empty(nbytes // 4 + 64, dtype=self.torch.float32, device=self.dev)
+            self.ws_bytes = nbytes
+
+    def op(self, name, fn):
+        if self.mark is None:
+            fn()
+            return
+        e0, e1 = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        fn()
+        e1.record(self.stream)
+        self.mark.append((name, e0, e1))
+
+    def conv_fwd(self, d, x, w, b, y):
+        self.hc.check(self.hc.hc_conv2d_fwd(d, x, w, b, y, self.ws, self.ws_bytes, self.stream), "fwd")
+
+    def conv_bwd(self, d, x, w, gy, gx, gw, gb):
+        self.hc.check(self.hc.hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, self.stream),
+                      "bwd")
+
+    def conv_ws(self, d):
+        st, a = self.hc.hc_conv2d_workspace_size(d, 0)
+        self.hc.check(st, "ws")
+        st, b = self.hc.hc_conv2d_workspace_size(d, 1)
+        self.hc.check(st, "ws")
+        return max(a, b, 16)
+
+
+class ConvWorkload:
+    """A single sharded convolution, forward + backward."""
+
+    def __init__(self, name, cfg, gen, unit, desc):
+        self.name, self.cfg, self.gen, self.unit, self.desc = name, cfg, gen, unit, desc
+        self.E = cfg["N"] * cfg["C_in"] * cfg["H"] * cfg["W"]
+        self.flops = 3 * conv_flops(cfg)
+        self.bytes = 5 * 4 * self.E
+        self.dense = cfg["groups"] == 1
 
     def describe(self):
         c = self.cfg
-        return {"workload": f"depthwise {self.K}x{self.K} conv fwd+bwd, x ({c['N']},{c['C_in']},{c['H']},{c['W']}) "
-                            f"fp32, {c['num_shards']} W-shards of width {c['W'] // c['num_shards']}",
-                "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [self.K, self.K],
+        return {"workload": self.desc, "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [c["kh"], c["kw"]],
                 "padding": c["padding"], "groups": c["groups"], "num_shards": c["num_shards"],
                 "l2": "inputs (470 MB each) larger than L2; no flush"}
 
-    def inputs(self):
-        from spatially_sharded_cnn_gb300 import synth
-        c = self.cfg
-        x = synth.normal((c["N"], c["C_in"], c["H"], c["W"]), 1.0, self.seed, 1)
-        w = synth.trunc_normal((c["C_out"], 1, self.K, self.K), 0.02, self.seed, 2)
-        b = np.zeros((c["C_out"],), np.float32)
-        gy = synth.normal((c["N"], c["C_out"], c["H"], c["W"]), 1.0, self.seed, 4)
-        return x, w, b, gy
+    def setup(self, R):
+        self.R = R
+        self.host = self.gen()
+        x, w, b, gy = self.host
+        self.x, self.w, self.b, self.gy = (R.upload(a) for a in (x, w, b, gy))
+        self.y, self.gx = R.torch.empty_like(self.x), R.torch.empty_like(self.x)
+        self.gw, self.gb = R.torch.empty_like(self.w), R.torch.empty_like(self.b)
+        self.d = R.hc.desc(self.cfg)
+        R.reserve(R.conv_ws(self.d))
+
+    def fwd(self):
+        self.R.op("conv_fwd", lambda: self.R.conv_fwd(self.d, self.x, self.w, self.b, self.y))
+
+    def bwd(self):
+        self.R.op("conv_bwd", lambda: self.R.conv_bwd(self.d, self.x, self.w, self.gy, self.gx, self.gw, self.gb))
+
+    def host_io(self):
+        t = self.R.torch
+        x, w, b, gy = self.host
+        self.h_in = [(self.x, t.from_numpy(x).pin_memory()), (self.gy, t.from_numpy(gy).pin_memory())]
+        self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in (self.y, self.gx, self.gw, self.gb)]
+
+    def value(self, ms):
+        return self.flops / (ms * 1e-3) / 1e12 if self.dense else self.bytes / (ms * 1e-3) / 1e9
+
+    def roofline(self, ops_ms, peaks, sms):
+        if self.dense:
+            peak = tc_peak(peaks)
+            a = conv_flops(self.cfg) / (ops_ms["conv_fwd"] * 1e-3) / 1e12
+            return {"bound": "tensor", "kernel": "tc_conv_kernel<256> (forward call incl. operand prep)",
+                    "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
+                    "traffic": None,
+                    "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
+                    "ms_per_launch": ops_ms["conv_fwd"]}
+        alu = alu_peak(peaks, sms)
+        bms = ops_ms["conv_bwd"]
+        a = 2 * conv_flops(self.cfg) / (bms * 1e-3) / 1e12
+        gbs = 3 * 4 * self.E / (bms * 1e-3) / 1e9
+        return {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": a, "peak": alu, "unit": "TFLOP/s",
+                "frac": a / alu,
+                "traffic": traffic_for("dw_bwd_kernel<7>", os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc",
+                                                                        "dw.cu")),
+                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                        "peak_source": peaks["src"]},
+                "ms_per_launch": bms}
 
 
-class DenseWorkload:
-    """Dense 5x5 conv 128->128, stride 1, padding 2, fp32 via 3xTF32 on the tensor
-    cores, x (7,128,128,1024) N(0,1), weight Kaiming-normal, bias N(0,0.01),
-    grad_output N(0,1), 4 W-shards of width 256."""
-    name = "dense5x5_fwd_bwd"
+def gen_dw7(seed=0):
+    from spatially_sharded_cnn_gb300 import synth
+    x = synth.normal((7, 256, 128, 512), 1.0, seed, 1)
+    w = synth.trunc_normal((256, 1, 7, 7), 0.02, seed, 2)
+    b = np.zeros((256,), np.float32)
+    gy = synth.normal((7, 256, 128, 512), 1.0, seed, 4)
+    return x, w, b, gy
 
-    def __init__(self, N=7, C=128, H=128, W=1024, K=5, S=4, seed=0):
-        self.cfg = dict(N=N, C_in=C, H=H, W=W, C_out=C, kh=K, kw=K, stride=1, padding=(K - 1) // 2, groups=1,
-                        num_shards=S)
-        self.K = K
-        self.E = N * C * H * W
-        self.seed = seed
-        self.flops_pass = 2.0 * N * H * W * C * C * K * K   # one of forward / grad_input / grad_weight
-        self.flops = 3 * self.flops_pass
-        self.flops_bwd = 2 * self.flops_pass
-        self.bytes = 5 * 4 * self.E
-        self.bytes_bwd = 3 * 4 * self.E
+
+def gen_dense5x5(seed=0):
+    from spatially_sharded_cnn_gb300 import synth
+    x = synth.normal((7, 128, 128, 1024), 1.0, seed, 1)
+    w = synth.kaiming_normal((128, 128, 5, 5), 128 * 25, seed, 2)
+    b = synth.normal((128,), 0.01, seed, 3)
+    gy = synth.normal((7, 128, 128, 1024), 1.0, seed, 4)
+    return x, w, b, gy
+
+
+class BlockWorkload:
+    """ConvNeXt-XL stage-1 block on the stem output of a (7,3,512,4096) image, 8 W-shards."""
+
+    unit = "TFLOP/s"
+
+    def __init__(self):
+        N, S = 7, 8
+        self.N, self.S = N, S
+        self.stem = conv_cfg(N, 3, 512, 4096, 256, 4, 4, 0, 1, S)
+        self.dw = conv_cfg(N, 256, 128, 1024, 256, 7, 1, 3, 256, S)
+        self.pw1 = conv_cfg(N, 256, 128, 1024, 1024, 1, 1, 0, 1, S)
+        self.pw2 = conv_cfg(N, 1024, 128, 1024, 256, 1, 1, 0, 1, S)
+        self.HW = 128 * 1024
+        fwd = sum(conv_flops(c) for c in (self.stem, self.dw, self.pw1, self.pw2))
+        # backward: grad_input and grad_weight of dw / pw1 / pw2, grad_weight of the stem
+        bwd = conv_flops(self.stem) + 2 * sum(conv_flops(c) for c in (self.dw, self.pw1, self.pw2))
+        self.flops = fwd + bwd
 
     def describe(self):
-        c = self.cfg
-        return {"workload": f"dense {self.K}x{self.K} conv {c['C_in']}->{c['C_out']} fwd+bwd, x ({c['N']},{c['C_in']},"
-                            f"{c['H']},{c['W']}) fp32 (3xTF32 tensor cores), {c['num_shards']} W-shards of width "
-                            f"{c['W'] // c['num_shards']}",
-                "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [self.K, self.K], "padding": c["padding"],
-                "groups": 1, "num_shards": c["num_shards"], "l2": "inputs (470 MB each) larger than L2; no flush"}
+        return {"workload": "ConvNeXt-XL stage-1 block fwd+bwd on the stem output of a (7,3,512,4096) U[0,1] image: "
+                            "4x4/s4 stem 3->256, depthwise 7x7, LayerNorm(C), 1x1 256->1024, GELU, 1x1 1024->256, "
+                            "layer scale 1e-6 + residual; fp32; 8 W-shards",
+                "shape": [7, 3, 512, 4096], "num_shards": 8, "l2": "activations (0.9-3.8 GB) larger than L2; no flush"}
 
-    def inputs(self):
+    def setup(self, R):
         from spatially_sharded_cnn_gb300 import synth
-        c = self.cfg
-        x = synth.normal((c["N"], c["C_in"], c["H"], c["W"]), 1.0, self.seed, 1)
-        w = synth.kaiming_normal((c["C_out"], c["C_in"], self.K, self.K), c["C_in"] * self.K * self.K, self.seed, 2)
-        b = synth.normal((c["C_out"],), 0.01, self.seed, 3)
-        gy = synth.normal((c["N"], c["C_out"], c["H"], c["W"]), 1.0, self.seed, 4)
-        return x, w, b, gy
+        self.R = R
+        hc, t = R.hc, R.torch
+        N, HW = self.N, self.HW
+        self.h_img = synth.uniform((N, 3, 512, 4096), 0.0, 1.0, 0, 1)
+        self.h_gy = synth.normal((N, 256, 128, 1024), 1.0, 0, 9)
+        self.img, self.gy = R.upload(self.h_img), R.upload(self.h_gy)
+        self.w_stem = R.upload(synth.trunc_normal((256, 3, 4, 4), 0.02, 0, 2))
+        self.w_dw = R.upload(synth.trunc_normal((256, 1, 7, 7), 0.02, 0, 3))
+        self.w1 = R.upload(synth.trunc_normal((1024, 256, 1, 1), 0.02, 0, 4))
+        self.w2 = R.upload(synth.trunc_normal((256, 1024, 1, 1), 0.02, 0, 5))
+        self.b256, self.b1024 = t.zeros(256, device=R.dev), t.zeros(1024, device=R.dev)
+        self.ln_g, self.ln_b = t.ones(256, device=R.dev), t.zeros(256, device=R.dev)
+        self.ls_g = t.full((256,), 1e-6, device=R.dev)
+        a256, a1024 = (N, 256, 128, 1024), (N, 1024, 128, 1024)
+        self.s, self.dwo, self.ln, self.b2, self.out = (R.empty(a256) for _ in range(5))
+        self.mean, self.rstd = R.empty((N, HW)), R.empty((N, HW))
+        self.h, self.a = R.empty(a1024), R.empty(a1024)
+        self.g_b2, self.g_l, self.g_d, self.g_s = (R.empty(a256) for _ in range(4))
+        self.g_a = R.empty(a1024)
+        self.gw_stem, self.gb_stem = t.empty_like(self.w_stem), t.empty(256, device=R.dev)
+        self.gw_dw, self.gb_dw = t.empty_like(self.w_dw), t.empty(256, device=R.dev)
+        self.gw1, self.gb1 = t.empty_like(self.w1), t.empty(1024, device=R.dev)
+        self.gw2, self.gb2 = t.empty_like(self.w2), t.empty(256, device=R.dev)
+        self.g_lng, self.g_lnb, self.g_ls = (t.empty(256, device=R.dev) for _ in range(3))
+        self.d = {k: hc.desc(getattr(self, k)) for k in ("stem", "dw", "pw1", "pw2")}
+        st, pwb = hc.hc_pointwise_workspace_size(N, 1024, HW)
+        hc.check(st)
+        R.reserve(max([R.conv_ws(d) for d in self.d.values()] + [pwb]))
+
+    def fwd(self):
+        R, hc, N, HW = self.R, self.R.hc, self.N, self.HW
+        R.op("stem_fwd", lambda: R.conv_fwd(self.d["stem"], self.img, self.w_stem, self.b256, self.s))
+        R.op("dw_fwd", lambda: R.conv_fwd(self.d["dw"], self.s, self.w_dw, self.b256, self.dwo))
+        R.op("ln_fwd", lambda: hc.check(hc.hc_layernorm_c_fwd(N, 256, HW, self.dwo, self.ln_g, self.ln_b, 1e-6, self.ln,
+                                                              self.mean, self.rstd, R.stream)))
+        R.op("pw1_fwd", lambda: R.conv_fwd(self.d["pw1"], self.ln, self.w1, self.b1024, self.h))
+        R.op("gelu_fwd", lambda: hc.check(hc.hc_gelu_fwd(N * 1024 * HW, self.h, self.a, R.stream)))
+        R.op("pw2_fwd", lambda: R.conv_fwd(self.d["pw2"], self.a, self.w2, self.b256, self.b2))
+        R.op("ls_fwd", lambda: hc.check(hc.hc_layerscale_residual_fwd(N, 256, HW, self.s, self.b2, self.ls_g, self.out,
+                                                                      R.stream)))
+
+    def bwd(self):
+        R, hc, N, HW = self.R, self.R.hc, self.N, self.HW
+        R.op("ls_bwd", lambda: hc.check(hc.hc_layerscale_residual_bwd(N, 256, HW, self.b2, self.ls_g, self.gy,
+                                                                      self.g_b2, self.g_ls, R.ws, R.ws_bytes,
+                                                                      R.stream)))
+        R.op("pw2_bwd", lambda: R.conv_bwd(self.d["pw2"], self.a, self.w2, self.g_b2, self.g_a, self.gw2, self.gb2))
+        R.op("gelu_bwd", lambda: hc.check(hc.hc_gelu_bwd(N * 1024 * HW, self.h, self.g_a, self.g_a, R.stream)))
+        R.op("pw1_bwd", lambda: R.conv_bwd(self.d["pw1"], self.ln, self.w1, self.g_a, self.g_l, self.gw1, self.gb1))
+        R.op("ln_bwd", lambda: hc.check(hc.hc_layernorm_c_bwd(N, 256, HW, self.dwo, self.ln_g, self.mean, self.rstd,
+                                                              self.g_l, self.g_d, self.g_lng, self.g_lnb, R.ws,
+                                                              R.ws_bytes, R.stream)))
+        R.op("dw_bwd", lambda: R.conv_bwd(self.d["dw"], self.s, self.w_dw, self.g_d, self.g_s, self.gw_dw, self.gb_dw))
+        R.op("residual_add", lambda: hc.check(hc.hc_add_inplace(N * 256 * HW, self.g_s, self.gy, R.stream)))
+        R.op("stem_bwd", lambda: R.conv_bwd(self.d["stem"], self.img, self.w_stem, self.g_s, None, self.gw_stem,
+                                            self.gb_stem))
+
+    def host_io(self):
+        t = self.R.torch
+        self.h_in = [(self.img, t.from_numpy(self.h_img).pin_memory()), (self.gy, t.from_numpy(self.h_gy).pin_memory())]
+        outs = (self.out, self.gw_stem, self.gb_stem, self.gw_dw, self.gw1, self.gw2, self.g_lng, self.g_lnb, self.g_ls)
+        self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in outs]
+
+    def value(self, ms):
+        return self.flops / (ms * 1e-3) / 1e12
+
+    def roofline(self, ops_ms, peaks, sms):
+        peak = tc_peak(peaks)
+        a = conv_flops(self.pw1) / (ops_ms["pw1_fwd"] * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "tc_conv_kernel<128> (1x1 256->1024 forward call incl. operand prep)",
+                "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
+                "traffic": None,
+                "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
+                "ms_per_launch": ops_ms["pw1_fwd"]}
 
 
-WORKLOADS = {"dw7": DepthwiseWorkload, "dense5x5": DenseWorkload}
+class DwDownWorkload:
+    """Depthwise 7x7 then 2x2/s2 downsample 256->512 on (7,256,128,2048), 8 W-shards."""
+
+    unit = "TFLOP/s"
+
+    def __init__(self):
+        self.dw = conv_cfg(7, 256, 128, 2048, 256, 7, 1, 3, 256, 8)
+        self.down = conv_cfg(7, 256, 128, 2048, 512, 2, 2, 0, 1, 8)
+        self.flops = 3 * (conv_flops(self.dw) + conv_flops(self.down))
+
+    def describe(self):
+        return {"workload": "depthwise 7x7 (p3, groups=C) then 2x2/s2 downsample 256->512 fwd+bwd on x "
+                            "(7,256,128,2048) fp32, 8 W-shards of width 256",
+                "shape": [7, 256, 128, 2048], "num_shards": 8, "l2": "activations (1.9 GB) larger than L2; no flush"}
+
+    def setup(self, R):
+        from spatially_sharded_cnn_gb300 import synth
+        self.R = R
+        hc, t = R.hc, R.torch
+        self.h_x = synth.normal((7, 256, 128, 2048), 1.0, 0, 1)
+        self.h_gz = synth.normal((7, 512, 64, 1024), 1.0, 0, 9)
+        self.x, self.gz = R.upload(self.h_x), R.upload(self.h_gz)
+        self.w_dw = R.upload(synth.trunc_normal((256, 1, 7, 7), 0.02, 0, 2))
+        self.w_dn = R.upload(synth.trunc_normal((512, 256, 2, 2), 0.02, 0, 3))
+        self.b256, self.b512 = t.zeros(256, device=R.dev), t.zeros(512, device=R.dev)
+        self.dwo, self.gd, self.gx = (t.empty_like(self.x) for _ in range(3))
+        self.z = t.empty_like(self.gz)
+        self.gw_dw, self.gb_dw = t.empty_like(self.w_dw), t.empty(256, device=R.dev)
+        self.gw_dn, self.gb_dn = t.empty_like(self.w_dn), t.empty(512, device=R.dev)
+        self.d = {k: hc.desc(getattr(self, k)) for k in ("dw", "down")}
+        R.reserve(max(R.conv_ws(d) for d in self.d.values()))
+
+    def fwd(self):
+        R = self.R
+        R.op("dw_fwd", lambda: R.conv_fwd(self.d["dw"], self.x, self.w_dw, self.b256, self.dwo))
+        R.op("down_fwd", lambda: R.conv_fwd(self.d["down"], self.dwo, self.w_dn, self.b512, self.z))
+
+    def bwd(self):
+        R = self.R
+        R.op("down_bwd", lambda: R.conv_bwd(self.d["down"], self.dwo, self.w_dn, self.gz, self.gd, self.gw_dn,
+                                            self.gb_dn))
+        R.op("dw_bwd", lambda: R.conv_bwd(self.d["dw"], self.x, self.w_dw, self.gd, self.gx, self.gw_dw, self.gb_dw))
+
+    def host_io(self):
+        t = self.R.torch
+        self.h_in = [(self.x, t.from_numpy(self.h_x).pin_memory()), (self.gz, t.from_numpy(self.h_gz).pin_memory())]
+        outs = (self.z, self.gx, self.gw_dw, self.gb_dw, self.gw_dn, self.gb_dn)
+        self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in outs]
+
+    def value(self, ms):
+        return self.flops / (ms * 1e-3) / 1e12
+
+    def roofline(self, ops_ms, peaks, sms):
+        alu = alu_peak(peaks, sms)
+        a = 2 * conv_flops(self.dw) / (ops_ms["dw_bwd"] * 1e-3) / 1e12
+        return {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": a, "peak": alu, "unit": "TFLOP/s",
+                "frac": a / alu, "traffic": None,
+                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                "ms_per_launch": ops_ms["dw_bwd"]}
+
+
+def make_workload(name):
+    if name == "dw7":
+        return ConvWorkload("dw7", conv_cfg(7, 256, 128, 512, 256, 7, 1, 3, 256, 4), gen_dw7, "GB/s",
+                            "depthwise 7x7 conv fwd+bwd, x (7,256,128,512) fp32, 4 W-shards of width 128")
+    if name == "dense5x5":
+        return ConvWorkload("dense5x5", conv_cfg(7, 128, 128, 1024, 128, 5, 1, 2, 1, 4), gen_dense5x5, "TFLOP/s",
+                            "dense 5x5 conv 128->128 fwd+bwd, x (7,128,128,1024) fp32 (3xTF32 tensor cores), "
+                            "4 W-shards of width 256")
+    if name == "block":
+        return BlockWorkload()
+    if name == "dwdown":
+        return DwDownWorkload()
+    raise ValueError(name)
+
+
+WORKLOADS = ["dw7", "dense5x5", "block", "dwdown"]
 
 
 # ---------------------------------------------------------------------------
@@ -167,7 +433,6 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def traffic_for(kernel: str, src_file: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -178,14 +443,19 @@ def traffic_for(kernel: str, src_file: str):
     return d["bytes_per_launch"] if d.get("source_sha") == h else None
 
 
-def cpu_oracle_sample(wl, max_seconds=20.0):
+def oracle_depthwise_sample(channels, images=1, max_seconds=20.0):
     """The oracle as it stands on this host's cores, on a bounded sample of the
-    workload (one image, all channels: 1/N of the batch), repeated while time
-    remains.  Returns (GB/s of algorithmic bytes, threads, description)."""
+    depthwise workload: `images` image(s) x `channels` channels of the
+    (7,256,128,512) batch, forward + backward, repeated while time remains.
+    Returns (GB/s of algorithmic bytes, threads, description, seconds per rep)."""
     import oracle
+    from spatially_sharded_cnn_gb300 import synth
     orc = oracle.load()
-    x, w, b, gy = wl.inputs_small
-    cfg = dict(wl.cfg, N=1)
+    cfg = conv_cfg(images, channels, 128, 512, channels, 7, 1, 3, channels, 4)
+    x = synth.normal((images, channels, 128, 512), 1.0, 0, 1)
+    w = synth.trunc_normal((channels, 1, 7, 7), 0.02, 0, 2)
+    b = np.zeros((channels,), np.float32)
+    gy = synth.normal((images, channels, 128, 512), 1.0, 0, 4)
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -197,48 +467,30 @@ def cpu_oracle_sample(wl, max_seconds=20.0):
         if time.perf_counter() - t0 > max_seconds / 2 or reps >= 4:
             break
     dt = (time.perf_counter() - t0) / reps
-    sample_bytes = wl.bytes / wl.cfg["N"]
-    return sample_bytes / dt / 1e9, orc.num_threads(), f"1 of {wl.cfg['N']} images, all channels, fwd+bwd, {reps} rep(s)"
+    sample_bytes = 5 * 4 * images * channels * 128 * 512
+    return (sample_bytes / dt / 1e9, orc.num_threads(),
+            f"{images} image(s) x {channels} of 256 channels of the (7,256,128,512) batch, fwd+bwd, {reps} rep(s)", dt)
 
 
-def run_reference(args, wl):
-    """Reference arm: the CPU oracle timed on the host cores, on the same config
-    and metric, each step a bounded sample (1 image x 16 channels)."""
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+def run_reference(args):
+    """Reference arm: the CPU oracle timed on the host cores on the depthwise
+    workload's config and metric, each step a bounded sample (1 image x 16 channels)."""
+    if int(os.environ.get("RANK", "0")) != 0:
         return 0
-    import oracle
-    orc = oracle.load()
-    from spatially_sharded_cnn_gb300 import synth
-    c = wl.cfg
-    Cs = 16
-    cfg = dict(c, N=1, C_in=Cs, C_out=Cs, groups=Cs)
-    x = synth.normal((1, Cs, c["H"], c["W"]), 1.0, 0, 1)
-    w = synth.trunc_normal((Cs, 1, wl.K, wl.K), 0.02, 0, 2)
-    b = np.zeros((Cs,), np.float32)
-    gy = synth.normal((1, Cs, c["H"], c["W"]), 1.0, 0, 4)
-
-    def step():
-        orc.conv2d_fwd(cfg, x, w, b)
-        orc.conv2d_bwd_input(cfg, w, gy)
-        orc.conv2d_bwd_weight(cfg, x, gy)
-        orc.conv2d_bwd_bias(cfg, gy)
-
+    wl = make_workload("dw7")
     for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
+        oracle_depthwise_sample(16, max_seconds=0.0)
+    steps, cores = [], 1
     for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
-    sample_bytes = 5 * 4 * Cs * c["H"] * c["W"]
-    v = sample_bytes / dt / 1e9
-    sample = f"1 image x {Cs} of {c['C_in']} channels per step ({Cs * c['H'] * c['W']} elements)"
+        _, cores, _, dt = oracle_depthwise_sample(16, max_seconds=0.0)
+        steps.append(dt)
+    dt = float(np.mean(steps)) if steps else float("nan")
+    v = 5 * 4 * 16 * 128 * 512 / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": wl.describe(),
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
-                             "sample": sample},
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl.describe(),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "1 image x 16 of 256 channels of the (7,256,128,512) batch per step"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -252,12 +504,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dw7")
+    ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
-        return run_reference(args, wl)
+        return run_reference(args)
+    wl = make_workload(args.workload)
 
     import torch
     import torch.distributed as dist
@@ -274,28 +526,14 @@ def main():
     from spatially_sharded_cnn_gb300 import hc
 
     peaks = load_peaks()
-    x, w, b, gy = wl.inputs()
-    wl.inputs_small = (np.ascontiguousarray(x[:1]), w, b, np.ascontiguousarray(gy[:1]))
     dev = torch.device("cuda", torch.cuda.current_device())
-    xd, wd, bd, gyd = (torch.from_numpy(a).to(dev) for a in (x, w, b, gy))
-    yd = torch.empty_like(xd)
-    gxd = torch.empty_like(xd)
-    gwd = torch.empty_like(wd)
-    gbd = torch.empty_like(bd)
-    d = hc.desc(wl.cfg)
-    st, ws_bytes = hc.hc_conv2d_workspace_size(d, 1)
-    hc.check(st, "workspace")
-    st, ws_fwd = hc.hc_conv2d_workspace_size(d, 0)
-    hc.check(st, "workspace")
-    ws_bytes = max(ws_bytes, ws_fwd)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    R = Runner(hc, torch, dev, stream)
+    wl.setup(R)
 
-    def fwd():
-        hc.check(hc.hc_conv2d_fwd(d, xd, wd, bd, yd, ws, ws_bytes, stream), "fwd")
-
-    def bwd():
-        hc.check(hc.hc_conv2d_bwd(d, xd, wd, gyd, gxd, gwd, gbd, None, None, ws, ws_bytes, stream), "bwd")
+    def step():
+        wl.fwd()
+        wl.bwd()
 
     def barrier():
         if world > 1:
@@ -303,67 +541,51 @@ def main():
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        fwd()
-        bwd()
+        step()
     hc.check(hc.hc_sync_check(stream), "warmup")
 
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    marks = []
+    R.mark = marks
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     n0 = hc.hc_launch_count()
     start.record(stream)
-    for k in range(K):
-        ev[k][0].record(stream)
-        fwd()
-        ev[k][1].record(stream)
-        bwd()
-        ev[k][2].record(stream)
+    for _ in range(K):
+        step()
     end.record(stream)
     barrier()
+    R.mark = None
     launches = hc.hc_launch_count() - n0
     clk = clocks.stop()
     hc.check(hc.hc_sync_check(stream), "timed region")
     elapsed_ms = start.elapsed_time(end)
-    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    ops = {}
+    for name, e0, e1 in marks:
+        ops.setdefault(name, []).append(e0.elapsed_time(e1))
+    ops_ms = {k: float(np.mean(v)) for k, v in ops.items()}
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     ms_step = elapsed_ms / K
-    dense = isinstance(wl, DenseWorkload)
-    if dense:
-        value = world * wl.flops / (ms_step * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    else:
-        value = world * wl.bytes / (ms_step * 1e-3) / 1e9
-        unit = "GB/s"
+    value = world * wl.value(ms_step)
 
     # end to end: host buffers, copies inside the timed region
-    xh = torch.from_numpy(x).pin_memory()
-    gyh = torch.from_numpy(gy).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    gxh = torch.empty_like(xh).pin_memory()
-    gwh = torch.empty_like(wd, device="cpu").pin_memory()
-    gbh = torch.empty_like(bd, device="cpu").pin_memory()
+    wl.host_io()
     E2 = max(1, args.e2e_steps)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E2):
-        xd.copy_(xh, non_blocking=True)
-        gyd.copy_(gyh, non_blocking=True)
-        fwd()
-        bwd()
-        yh.copy_(yd, non_blocking=True)
-        gxh.copy_(gxd, non_blocking=True)
-        gwh.copy_(gwd, non_blocking=True)
-        gbh.copy_(gbd, non_blocking=True)
+        for d_t, h_t in wl.h_in:
+            d_t.copy_(h_t, non_blocking=True)
+        step()
+        for d_t, h_t in wl.h_out:
+            h_t.copy_(d_t, non_blocking=True)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / E2
@@ -371,48 +593,24 @@ def main():
         t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    h2d = (xh.numel() + gyh.numel()) * 4
-    d2h = (yh.numel() + gxh.numel() + gwh.numel() + gbh.numel()) * 4
+    h2d = sum(h.numel() * 4 for _, h in wl.h_in)
+    d2h = sum(h.numel() * 4 for _, h in wl.h_out)
 
-    # roofline of the dominant kernel (the fused depthwise backward, one launch
-    # per hc_conv2d_bwd call plus two tiny fixed-order reductions)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    e2e_value = world * (wl.flops / 1e12 if dense else wl.bytes / 1e9) / (e2e_ms * 1e-3)
-    alu_peak = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-    bwd_tflops = wl.flops_bwd / (bwd_ms * 1e-3) / 1e12
-    bwd_gbs = wl.bytes_bwd / (bwd_ms * 1e-3) / 1e9
-    if dense:
-        # forward call = operand preparation + one tensor-core GEMM pass; the peak is the
-        # measured bf16 dense rate x the nominal tf32/bf16 ratio (1.1 / 2.25), / 3 for 3xTF32
-        tf32_peak = peaks["bf16"] * (1.1 / 2.25)
-        fwd_tflops = wl.flops_pass / (fwd_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "tc_conv_kernel (forward call incl. operand prep)",
-                "achieved": fwd_tflops, "peak": tf32_peak / 3, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)",
-                "frac": fwd_tflops / (tf32_peak / 3), "traffic": None,
-                "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
-                "ms_per_launch": fwd_ms}
-    else:
-        roof = {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": bwd_tflops, "peak": alu_peak,
-                "unit": "TFLOP/s", "frac": bwd_tflops / alu_peak,
-                "traffic": traffic_for("dw_bwd_kernel<7>", os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc",
-                                                                        "dw.cu")),
-                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
-                "hbm": {"achieved": bwd_gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": bwd_gbs / peaks["hbm"],
-                        "peak_source": peaks["src"]},
-            "ms_per_launch": bwd_ms}
+    roof = wl.roofline(ops_ms, peaks, sms)
     if world > 1:
         dist.barrier()
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+        line = {"metric": METRIC, "value": value, "unit": wl.unit, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": wl.describe(),
-                "hbm_frac": None if dense else value / world / peaks["hbm"],
-                "phases_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
-                "e2e": {"value": e2e_value, "unit": unit,
-                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "hbm_frac": value / world / peaks["hbm"] if wl.unit == "GB/s" else None,
+                "ops_ms": ops_ms,
+                "e2e": {"value": world * wl.value(e2e_ms), "unit": wl.unit, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
-        if world == 1 and not args.no_cpu_baseline and not dense:
-            v, cores, sample = cpu_oracle_sample(wl)
+        if world == 1 and not args.no_cpu_baseline and args.workload == "dw7":
+            v, cores, sample, _ = oracle_depthwise_sample(256)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -189,6 +189,10 @@ hc_status hc_gelu_fwd(long long n, const float* x, float* y, void* stream);
 /* GELU backward: gx = gy * (Phi(x) + x * exp(-x^2 / 2) / sqrt(2 pi)). */
 hc_status hc_gelu_bwd(long long n, const float* x, const float* gy, float* gx, void* stream);
 
+/* y += x over n elements: joins the residual's gradient (the block output's
+ * gradient itself) with the gradient that comes back through the branch. */
+hc_status hc_add_inplace(long long n, float* y, const float* x, void* stream);
+
 /* Layer scale and residual: out = res + gamma[c] * branch. */
 hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
                                      const float* gamma, float* out, void* stream);

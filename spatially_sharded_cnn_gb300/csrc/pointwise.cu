@@ -220,6 +220,23 @@ __global__ void ls_reduce_kernel(const float* __restrict__ part, float* __restri
     gg[c] = t;
 }
 
+// y += x
+__global__ void add_inplace_kernel(float* __restrict__ y, const float* __restrict__ x, long long n) {
+    const long long n4 = n / 4;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
+        float4 a = reinterpret_cast<float4*>(y)[q];
+        const float4 b = __ldg(reinterpret_cast<const float4*>(x) + q);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+        reinterpret_cast<float4*>(y)[q] = a;
+    }
+    for (long long q = n4 * 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n;
+         q += (long long)gridDim.x * blockDim.x)
+        y[q] += __ldg(x + q);
+}
+
 constexpr int LS_CHUNKS = 16;
 
 bool al16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
@@ -300,6 +317,12 @@ hc_status hc_gelu_fwd(long long n, const float* x, float* y, void* stream) {
 hc_status hc_gelu_bwd(long long n, const float* x, const float* gy, float* gx, void* stream) {
     if (n <= 0 || !x || !gy || !gx || !al16(x) || !al16(gy) || !al16(gx)) return HC_ERR_INVALID_ARG;
     gelu_bwd_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(x, gy, gx, n);
+    return launched();
+}
+
+hc_status hc_add_inplace(long long n, float* y, const float* x, void* stream) {
+    if (n <= 0 || !x || !y || !al16(x) || !al16(y)) return HC_ERR_INVALID_ARG;
+    add_inplace_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(y, x, n);
     return launched();
 }
 

@@ -503,7 +503,7 @@ __global__ void prep_split_kernel(const float* __restrict__ x, float* __restrict
 // column.  One block per input row: the row is staged in shared memory once
 // and the four shifted rows are written with 16-byte stores.
 __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                  long long rows, int W, int Wc) {
+                                  long long rows, int W, int Wc, int copies) {
     extern __shared__ float rowbuf[];  // [W + 8]: 4 zeros, the row, 4 zeros
     const long long row = blockIdx.x;
     const float* src = x + row * W;
@@ -513,7 +513,7 @@ __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict
     }
     __syncthreads();
     const int v4 = Wc / 4;
-    for (int q = threadIdx.x; q < 4 * v4; q += blockDim.x) {
+    for (int q = threadIdx.x; q < copies * v4; q += blockDim.x) {
         const int j = q / v4, i0 = (q - j * v4) * 4;
         // element i of copy j is x[i - j] = rowbuf[i - j + 4]
         float4 h, l;
@@ -724,6 +724,8 @@ bool is_s2d(const hc_conv_desc* d) {
     return d->groups == 1 && d->stride >= 2 && d->kh == d->stride && d->kw == d->stride && d->padding == 0;
 }
 int s2d_kp(const hc_conv_desc* d) { return (d->stride * d->stride * d->C_in + 127) / 128 * 128; }
+// Shifted copies the weight gradient reads: a 1-wide kernel never shifts.
+int shift_copies(const hc_conv_desc* d) { return d->kw == 1 ? 1 : 4; }
 
 }  // namespace
 
@@ -770,7 +772,7 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     const size_t ng = (size_t)d->N * d->C_out * p.Ho * p.Wo;
     const size_t wsz = (size_t)d->C_out * KK * d->C_in;
     if (pass == 0) return 2 * al256(4 * nx) + 2 * al256(4 * wsz);
-    const size_t nsh = 4 * (size_t)d->N * d->C_in * d->H * (d->W + 4);
+    const size_t nsh = (size_t)shift_copies(d) * d->N * d->C_in * d->H * (d->W + 4);
     const int J = tc_wgrad_splits(d, p);
     const size_t part = al256(4 * (size_t)p.S * J * wsz);
     return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
@@ -958,8 +960,8 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     if (is_s2d(d)) return s2d_bwd(d, p, x, w, gy, gx, gwp, want_w, ws, st);
     const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
     const size_t ng = (size_t)d->N * Co * p.Ho * p.Wo, wsz = (size_t)Co * KK * Ci;
-    const int Wc = d->W + 4;
-    const size_t nsh = 4 * (size_t)d->N * Ci * d->H * Wc;
+    const int Wc = d->W + 4, copies = shift_copies(d);
+    const size_t nsh = (size_t)copies * d->N * Ci * d->H * Wc;
     char* q = (char*)ws;
     float* gh = (float*)q;
     q += al256(4 * ng);
@@ -1015,7 +1017,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         if ((s = launched())) return s;
         const long long rows = (long long)d->N * Ci * d->H;
         if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, d->W, Wc);
+        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, d->W, Wc, copies);
         if ((s = launched())) return s;
         TcParams tp{};
         tp.mode = 1;
@@ -1037,8 +1039,8 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.part = part;
         CUtensorMap mah, mal, mbh, mbl;
         if ((s = nchw_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (s = nchw_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_BN)) ||
-            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_BN)))
+            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_BN, copies)) ||
+            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_BN, copies)))
             return s;
         if ((s = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return s;
         const long long total = (long long)p.S * wsz;

@@ -80,10 +80,11 @@ _lib.hc_pointwise_workspace_size.argtypes = [_I, _I, _L, C.POINTER(C.c_size_t)]
 _lib.hc_layernorm_c_fwd.argtypes = [_I, _I, _L, _P, _P, _P, _F, _P, _P, _P, _P]
 _lib.hc_layernorm_c_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_gelu_fwd.argtypes = [_L, _P, _P, _P]
+_lib.hc_add_inplace.argtypes = [_L, _P, _P, _P]
 _lib.hc_gelu_bwd.argtypes = [_L, _P, _P, _P, _P]
 _lib.hc_layerscale_residual_fwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P]
 _lib.hc_layerscale_residual_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
-for _n in ("hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
+for _n in ("hc_add_inplace", "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
            "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd"):
     getattr(_lib, _n).restype = C.c_int
 _lib.hc_sync_check.argtypes = [_P]
@@ -100,7 +101,7 @@ EXPORTS = [
     "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
     "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
-    "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd",
+    "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace",
 ]
 
 
@@ -177,6 +178,10 @@ def hc_layernorm_c_bwd(N, C_, HW, x, gamma, mean, rstd, gy, gx, ggamma=None, gbe
                        stream=None) -> int:
     return _lib.hc_layernorm_c_bwd(int(N), int(C_), int(HW), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(gy),
                                    _ptr(gx), _ptr(ggamma), _ptr(gbeta), _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def hc_add_inplace(n, y, x, stream=None) -> int:
+    return _lib.hc_add_inplace(int(n), _ptr(y), _ptr(x), _stream(stream))
 
 
 def hc_gelu_fwd(n, x, y, stream=None) -> int:

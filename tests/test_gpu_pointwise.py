@@ -83,3 +83,14 @@ def test_layerscale_residual(hc, orc, shape):
     _, gbrr, ggr = orc.layerscale_residual_bwd(br, gamma, gy)
     assert R.normwise(gbr.numpy(), gbrr) <= 1e-5
     assert R.normwise(gg.numpy(), ggr) <= 1e-4
+
+
+@pytest.mark.parametrize("n", [1 << 16, 4097])
+def test_add_inplace(hc, n):
+    a = synth.normal((n,), 1.0, 8, 1)
+    b = synth.normal((n,), 1.0, 8, 2)
+    y = R.Guarded((n,))
+    y.view.copy_(torch.from_numpy(a))
+    hc.check(hc.hc_add_inplace(n, y.view, R.dev(b)))
+    hc.check(hc.hc_sync_check())
+    assert np.array_equal(y.numpy(), (a + b).astype(np.float32))
