@@ -208,6 +208,15 @@ hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* br
  * error, or HC_OK. */
 hc_status hc_sync_check(void* stream);
 
+/* Self-test of failure detection.  Launches one kernel that waits on an
+ * mbarrier nothing ever arrives on; after wait_us microseconds (1 .. 2e6) of
+ * the GPU's global timer it gives up, records HC_ERR_TIMEOUT in the device
+ * status word -- the same path every pipelined kernel of the library takes
+ * when a wait runs out -- and returns, leaving the context usable.  The next
+ * hc_sync_check on `stream` then returns HC_ERR_TIMEOUT (and clears it).
+ * Returns HC_ERR_INVALID_ARG for an out-of-range wait_us. */
+hc_status hc_selftest_timeout(int wait_us, void* stream);
+
 /* Static English text for a status code. */
 const char* hc_status_string(hc_status s);
 

@@ -257,6 +257,10 @@ hc_status hc_sync_check(void* stream) {
     return a ? a : b;
 }
 
+hc_status hc_selftest_timeout(int wait_us, void* stream) {
+    return launch_selftest_timeout(wait_us, (cudaStream_t)stream);
+}
+
 const char* hc_status_string(hc_status s) {
     switch (s) {
         case HC_OK: return "ok";

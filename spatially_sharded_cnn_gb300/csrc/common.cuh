@@ -44,6 +44,7 @@ hc_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const
 // stream has been synchronised.
 hc_status dw_take_status();
 hc_status tc_take_status();
+hc_status launch_selftest_timeout(int wait_us, cudaStream_t st);
 
 // ---- kernel launchers (one translation unit each) -------------------------
 hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* x, float* x_ext, cudaStream_t st);

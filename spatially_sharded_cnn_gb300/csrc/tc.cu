@@ -531,46 +531,89 @@ __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict
 // Space-to-depth for a k = stride = s convolution without padding (each output
 // pixel reads one s x s block): channel k = (u*s + v)*C + c of output pixel
 // (ho, wo) is x[c][ho*s + u][wo*s + v]; channels k >= s*s*C are zero.
-//   NHWC form [N][Ho][Wo][Kp] (the forward's B operand), tf32 hi / lo.
+//   NHWC form [N][Ho][Wo][Kp] (the forward's B operand), tf32 hi / lo.  Block
+//   (32 output columns, 32 channels, (n, ho)): for each kernel row u the 32
+//   input rows are staged in shared memory (coalesced reads), then written as
+//   32 consecutive channels per (wo, v) (coalesced writes).
 __global__ void prep_s2d_nhwc_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                     int C, int H, int W, int s, int Kp, long long total) {
+                                     int C, int H, int W, int s, int Kp) {
+    __shared__ float t[32][4 * 32 + 1];
     const int Ho = H / s, Wo = W / s;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
-         q += (long long)gridDim.x * blockDim.x) {
-        const int k = (int)(q % Kp);
-        const long long pix = q / Kp;
-        const int wo = (int)(pix % Wo);
-        const long long r2 = pix / Wo;
-        const int ho = (int)(r2 % Ho), n = (int)(r2 / Ho);
-        float v = 0.0f;
-        if (k < s * s * C) {
-            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
-            v = __ldg(x + (((long long)n * C + c) * H + ho * s + uu) * W + wo * s + vv);
+    const int wo0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    const int n = blockIdx.z / Ho, ho = blockIdx.z % Ho;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int cols = 32 * s;
+    for (int u = 0; u < s; u++) {
+        for (int i = ty; i < 32; i += blockDim.y) {
+            const int c = c0 + i;
+            for (int col = tx; col < cols; col += 32) {
+                const int w = wo0 * s + col;
+                t[i][col] = (c < C && w < W) ? __ldg(x + (((long long)n * C + c) * H + ho * s + u) * W + w) : 0.0f;
+            }
         }
-        const float h = tf32_rna(v);
-        hi[q] = h;
-        lo[q] = tf32_rna(v - h);
+        __syncthreads();
+        for (int i = ty; i < 32; i += blockDim.y) {
+            const int wo = wo0 + i, c = c0 + tx;
+            if (wo < Wo && c < C) {
+                for (int v = 0; v < s; v++) {
+                    const float val = t[tx][i * s + v];
+                    const float h = tf32_rna(val);
+                    const long long o = (((long long)n * Ho + ho) * Wo + wo) * Kp + (u * s + v) * C + c;
+                    hi[o] = h;
+                    lo[o] = tf32_rna(val - h);
+                }
+            }
+        }
+        __syncthreads();
     }
 }
-//   planar form [N][Kp][Ho][Wo] (the weight gradient's B operand: pixels contiguous).
-__global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                       int C, int H, int W, int s, int Kp, long long total) {
-    const int Ho = H / s, Wo = W / s;
+// Zero the channel tail [k0, Kp) of every pixel of an NHWC hi / lo pair.
+__global__ void zero_tail_kernel(float* __restrict__ hi, float* __restrict__ lo, long long pixels, int k0, int Kp) {
+    const int tail = Kp - k0;
+    const long long total = pixels * tail;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
          q += (long long)gridDim.x * blockDim.x) {
-        const int wo = (int)(q % Wo);
-        const long long r1 = q / Wo;
-        const int ho = (int)(r1 % Ho);
-        const long long r2 = r1 / Ho;
-        const int k = (int)(r2 % Kp), n = (int)(r2 / Kp);
-        float v = 0.0f;
-        if (k < s * s * C) {
-            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
-            v = __ldg(x + (((long long)n * C + c) * H + ho * s + uu) * W + wo * s + vv);
+        const long long o = (q / tail) * Kp + k0 + q % tail;
+        hi[o] = 0.0f;
+        lo[o] = 0.0f;
+    }
+}
+//   planar form [N][Kp][Ho][Wo] (the weight gradient's B operand: pixels
+//   contiguous).  One block per input row (n, c, h = ho*s + u): the row is
+//   staged once and written as s output rows, one per v.
+__global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                       int C, int H, int W, int s, int Kp) {
+    extern __shared__ float row[];
+    const int Ho = H / s, Wo = W / s;
+    const long long rid = blockIdx.x;  // (n * C + c) * H + h
+    const int h = (int)(rid % H);
+    const long long nc = rid / H;
+    const int c = (int)(nc % C), n = (int)(nc / C);
+    const int ho = h / s, u = h - ho * s;
+    const float* src = x + rid * W;
+    for (int i = threadIdx.x; i < W; i += blockDim.x) row[i] = __ldg(src + i);
+    __syncthreads();
+    for (int v = 0; v < s; v++) {
+        const long long o = (((long long)n * Kp + (u * s + v) * C + c) * Ho + ho) * Wo;
+        for (int wo = threadIdx.x; wo < Wo; wo += blockDim.x) {
+            const float val = row[wo * s + v];
+            const float hv = tf32_rna(val);
+            hi[o + wo] = hv;
+            lo[o + wo] = tf32_rna(val - hv);
         }
-        const float h = tf32_rna(v);
-        hi[q] = h;
-        lo[q] = tf32_rna(v - h);
+    }
+}
+// Zero the padding channels [k0, Kp) of a planar hi / lo pair ([N][Kp][HWo]).
+__global__ void zero_planar_kernel(float* __restrict__ hi, float* __restrict__ lo, int N, int k0, int Kp,
+                                   long long HWo) {
+    const long long per = (long long)(Kp - k0) * HWo;
+    const long long total = (long long)N * per;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long n = q / per, r = q % per;
+        const long long o = (n * Kp + k0) * HWo + r;
+        hi[o] = 0.0f;
+        lo[o] = 0.0f;
     }
 }
 // Weights in space-to-depth order: forward A[co][k] = w[co][c][u][v];
@@ -733,7 +776,7 @@ int shift_copies(const hc_conv_desc* d) { return d->kw == 1 ? 1 : 4; }
 bool tc_supported(const hc_conv_desc* d, const Plan& p) {
     if (is_s2d(d)) {
         const int s = d->stride;
-        return d->C_out % BM == 0 && d->H % s == 0 && d->W % s == 0 && pick_bn(p.Wl / s) != 0 &&
+        return s <= 4 && d->C_out % BM == 0 && d->H % s == 0 && d->W % s == 0 && pick_bn(p.Wl / s) != 0 &&
                (p.Wl / s) % 32 == 0 && p.Wo == d->W / s && p.Ho == d->H / s;
     }
     if (d->groups != 1 || d->stride != 1 || d->kh != d->kw || d->padding != (d->kh - 1) / 2 || d->kh % 2 == 0)
@@ -790,10 +833,16 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     float* ah = (float*)q;
     q += al256(4 * wsz);
     float* al = (float*)q;
-    prep_s2d_nhwc_kernel<<<cdiv((long long)ns, 256) < 152u * 64 ? cdiv((long long)ns, 256) : 152u * 64, 256, 0, st>>>(
-        x, xh, xl, d->C_in, d->H, d->W, s, Kp, (long long)ns);
+    if (s > 4) return HC_ERR_UNSUPPORTED;
+    prep_s2d_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(d->C_in, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(
+        x, xh, xl, d->C_in, d->H, d->W, s, Kp);
     hc_status e = launched();
     if (e) return e;
+    if (Kp > s * s * d->C_in) {
+        const long long pixels = (long long)d->N * p.Ho * p.Wo;
+        zero_tail_kernel<<<152 * 16, 256, 0, st>>>(xh, xl, pixels, s * s * d->C_in, Kp);
+        if ((e = launched())) return e;
+    }
     prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, d->C_in, s, Kp, 0);
     if ((e = launched())) return e;
     const int BN = pick_bn(p.Wl / s);
@@ -877,9 +926,14 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     if (want_w) {  // G[co][(u,v,c)] = sum over a shard's pixels of gy[co][px] s2d[(u,v,c)][px]
         prep_split_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, (long long)ng / 4);
         if ((e = launched())) return e;
-        prep_s2d_planar_kernel<<<cdiv((long long)ns, 256) < 152u * 64 ? cdiv((long long)ns, 256) : 152u * 64, 256, 0,
-                                 st>>>(x, sh, sl, Ci, d->H, d->W, s, Kp, (long long)ns);
+        const long long rows = (long long)d->N * Ci * d->H;
+        if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+        prep_s2d_planar_kernel<<<(unsigned)rows, 256, sizeof(float) * d->W, st>>>(x, sh, sl, Ci, d->H, d->W, s, Kp);
         if ((e = launched())) return e;
+        if (Kp > s * s * Ci) {
+            zero_planar_kernel<<<152 * 16, 256, 0, st>>>(sh, sl, d->N, s * s * Ci, Kp, (long long)p.Ho * p.Wo);
+            if ((e = launched())) return e;
+        }
         TcParams tp{};
         tp.mode = 1;
         tp.Co = Co;
@@ -1048,6 +1102,33 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         if ((s = launched())) return s;
     }
     return HC_OK;
+}
+
+namespace {
+// Self-test of the timeout path: wait on an mbarrier that nothing arrives on,
+// for at most wait_ns of the global timer, then record HC_ERR_TIMEOUT exactly
+// as a pipeline kernel that gave up would, and return.
+__global__ void selftest_timeout_kernel(long long wait_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t0));
+    while (!mbar_try(&bar, 0)) {
+        asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+        if ((long long)(t - t0) > wait_ns) {
+            atomicCAS(&g_tc_status, 0, (int)HC_ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+}  // namespace
+
+hc_status launch_selftest_timeout(int wait_us, cudaStream_t st) {
+    if (wait_us < 1 || wait_us > 2000000) return HC_ERR_INVALID_ARG;
+    selftest_timeout_kernel<<<1, 32, 0, st>>>((long long)wait_us * 1000);
+    return launched();
 }
 
 hc_status tc_take_status() {

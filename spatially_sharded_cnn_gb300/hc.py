@@ -88,6 +88,8 @@ for _n in ("hc_add_inplace", "hc_pointwise_workspace_size", "hc_layernorm_c_fwd"
            "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd"):
     getattr(_lib, _n).restype = C.c_int
 _lib.hc_sync_check.argtypes = [_P]
+_lib.hc_selftest_timeout.argtypes = [C.c_int, _P]
+_lib.hc_selftest_timeout.restype = C.c_int
 _lib.hc_status_string.argtypes = [C.c_int]
 _lib.hc_status_string.restype = C.c_char_p
 _lib.hc_launch_count.restype = C.c_ulonglong
@@ -101,7 +103,7 @@ EXPORTS = [
     "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
     "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
-    "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace",
+    "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
 ]
 
 
@@ -200,6 +202,10 @@ def hc_layerscale_residual_fwd(N, C_, HW, res, branch, gamma, out, stream=None) 
 def hc_layerscale_residual_bwd(N, C_, HW, branch, gamma, gy, gbranch, ggamma, ws, ws_bytes, stream=None) -> int:
     return _lib.hc_layerscale_residual_bwd(int(N), int(C_), int(HW), _ptr(branch), _ptr(gamma), _ptr(gy),
                                            _ptr(gbranch), _ptr(ggamma), _ptr(ws), int(ws_bytes), _stream(stream))
+
+
+def hc_selftest_timeout(wait_us, stream=None) -> int:
+    return _lib.hc_selftest_timeout(int(wait_us), _stream(stream))
 
 
 def hc_sync_check(stream=None) -> int:
