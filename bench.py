@@ -183,21 +183,21 @@ class ConvWorkload:
                 "ms_per_launch": bms}
 
 
-def gen_dw7(seed=0):
+def gen_dw7(N=7, seed=0):
     from spatially_sharded_cnn_gb300 import synth
-    x = synth.normal((7, 256, 128, 512), 1.0, seed, 1)
+    x = synth.normal((N, 256, 128, 512), 1.0, seed, 1)
     w = synth.trunc_normal((256, 1, 7, 7), 0.02, seed, 2)
     b = np.zeros((256,), np.float32)
-    gy = synth.normal((7, 256, 128, 512), 1.0, seed, 4)
+    gy = synth.normal((N, 256, 128, 512), 1.0, seed, 4)
     return x, w, b, gy
 
 
-def gen_dense5x5(seed=0):
+def gen_dense5x5(N=7, seed=0):
     from spatially_sharded_cnn_gb300 import synth
-    x = synth.normal((7, 128, 128, 1024), 1.0, seed, 1)
+    x = synth.normal((N, 128, 128, 1024), 1.0, seed, 1)
     w = synth.kaiming_normal((128, 128, 5, 5), 128 * 25, seed, 2)
     b = synth.normal((128,), 0.01, seed, 3)
-    gy = synth.normal((7, 128, 128, 1024), 1.0, seed, 4)
+    gy = synth.normal((N, 128, 128, 1024), 1.0, seed, 4)
     return x, w, b, gy
 
 
@@ -364,14 +364,16 @@ class DwDownWorkload:
                 "ms_per_launch": ops_ms["dw_bwd"]}
 
 
-def make_workload(name):
+def make_workload(name, batch=None):
+    """batch overrides N of the single-conv workloads (smaller cases for profiling)."""
+    N = batch or 7
     if name == "dw7":
-        return ConvWorkload("dw7", conv_cfg(7, 256, 128, 512, 256, 7, 1, 3, 256, 4), gen_dw7, "GB/s",
-                            "depthwise 7x7 conv fwd+bwd, x (7,256,128,512) fp32, 4 W-shards of width 128")
+        return ConvWorkload("dw7", conv_cfg(N, 256, 128, 512, 256, 7, 1, 3, 256, 4), lambda: gen_dw7(N), "GB/s",
+                            f"depthwise 7x7 conv fwd+bwd, x ({N},256,128,512) fp32, 4 W-shards of width 128")
     if name == "dense5x5":
-        return ConvWorkload("dense5x5", conv_cfg(7, 128, 128, 1024, 128, 5, 1, 2, 1, 4), gen_dense5x5, "TFLOP/s",
-                            "dense 5x5 conv 128->128 fwd+bwd, x (7,128,128,1024) fp32 (3xTF32 tensor cores), "
-                            "4 W-shards of width 256")
+        return ConvWorkload("dense5x5", conv_cfg(N, 128, 128, 1024, 128, 5, 1, 2, 1, 4), lambda: gen_dense5x5(N),
+                            "TFLOP/s", f"dense 5x5 conv 128->128 fwd+bwd, x ({N},128,128,1024) fp32 (3xTF32 tensor "
+                            "cores), 4 W-shards of width 256")
     if name == "block":
         return BlockWorkload()
     if name == "dwdown":
@@ -505,11 +507,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
+    ap.add_argument("--batch", type=int, default=None, help="batch size of the dw7 / dense5x5 workloads (default 7)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, args.batch)
 
     import torch
     import torch.distributed as dist
@@ -609,7 +612,7 @@ def main():
                 "e2e": {"value": world * wl.value(e2e_ms), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
-        if world == 1 and not args.no_cpu_baseline and args.workload == "dw7":
+        if world == 1 and not args.no_cpu_baseline and args.workload == "dw7" and not args.batch:
             v, cores, sample, _ = oracle_depthwise_sample(256)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)
