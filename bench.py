@@ -166,7 +166,8 @@ class ConvWorkload:
             a = conv_flops(self.cfg) / (ops_ms["conv_fwd"] * 1e-3) / 1e12
             return {"bound": "tensor", "kernel": "tc_conv_kernel<256> (forward call incl. operand prep)",
                     "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
-                    "traffic": None,
+                    "traffic": traffic_for("tc_conv_kernel<256>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
+                                                                               "csrc", "tc.cu")),
                     "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
                     "ms_per_launch": ops_ms["conv_fwd"]}
         alu = alu_peak(peaks, sms)
