@@ -17,21 +17,25 @@
 // Passes (all share one persistent, warp-specialised kernel):
 //   conv   (forward, and grad_input of a stride-1 conv as the conv of
 //          grad_output with the flipped, transposed kernel):
-//          D[m][px] = sum over taps (u,v) and 32-channel chunks of
+//          D[m][px] = sum over taps (u,v) and BK-channel chunks of
 //          A[m][(u,v,c)] * X[n][h+u-p][w+v-p][c]; A = weights, B = the
 //          activation in NHWC (channels contiguous), one 4-D TMA box per
 //          (tap, chunk).
 //   wgrad  G[co][ci] of one tap = sum over a shard's pixels of
-//          gy[co][px] * x[ci][px + tap]; A = grad_output in NCHW (pixels
-//          contiguous), B = one of four copies of x shifted right by 0..3
-//          columns, so that every tap's column shift starts on a 16-byte
-//          boundary (a TMA box's innermost coordinate must); row shifts and
-//          padding come from the box's coordinates and zero fill.
-// All operands are K-major tiles with the 128-byte swizzle.
+//          gy[co][px] * x[ci][px + tap]; A = grad_output, B = one of four
+//          copies of x shifted right by 0..3 columns, so that every tap's
+//          column shift starts on a 16-byte boundary (a TMA box's innermost
+//          coordinate must); row shifts and padding come from the box's
+//          coordinates and zero fill.  Both are stored row-interleaved,
+//          [N][H][C][W] (pixels contiguous, the channels of one image row
+//          together), so one 128-channel box spans 128 rows of W floats
+//          rather than 128 channel planes.  A unit covers two (tap,
+//          128-channel) slots side by side: N = 256 accumulator columns.
+// All operands are K-major tiles with the 128-byte swizzle (32 tf32 per row).
 //
 // Accuracy: the tensor core's fp32 accumulation loses about one unit in the
 // last place per MMA step, so a long K would lose ~1e-5.  The MMA warp
-// therefore accumulates groups of 8 k-chunks (96 MMAs) in one of two TMEM
+// therefore accumulates groups of 256 k-values (96 MMAs) in one of two TMEM
 // buffers and the epilogue warps add the groups up in fp32 registers.
 //
 // Warp roles (320 threads, one CTA per SM): warp 0 issues TMA loads into an
@@ -47,6 +51,8 @@ namespace {
 
 constexpr int BM = 128;             // accumulator rows (TMEM lanes)
 constexpr int BK = 32;              // tf32 per k-chunk = one 128-byte swizzle row
+constexpr int ROWB = BK * 4;        // bytes per tile row
+constexpr uint32_t SW_ATOM = 8 * ROWB;  // 8-row swizzle atom = stride between 8-row groups
 constexpr int TC_SMEM_RING = 196 * 1024;
 constexpr long long kWait = 4000000000LL;  // clock cycles, about 2 s
 
@@ -180,7 +186,8 @@ struct TcParams {
     float* out;     // NCHW [N][M][Ho][Wo], or with d2s > 0 the image [N][d2s_c][Ho*d2s][Wo*d2s]
     int d2s, d2s_c; // depth-to-space store: row m = (u*d2s + v)*d2s_c + c goes to pixel (ho*d2s+u, wo*d2s+v)
     // wgrad mode
-    int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // row_chunks = own_w / 32
+    int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // row_chunks = own_w / BK
+    int slots;      // taps * nblocks: (tap, 128-channel block) pairs; a unit covers two slots
     long long shard_chunks;                               // N * Ho * row_chunks
     float* part;    // [S][J][taps][Co][Ci]
 };
@@ -206,10 +213,9 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int t, int BN) {
     } else {
         u.m0 = (t % p.mblocks) * BM;
         int rest = t / p.mblocks;
-        u.ci0 = (rest % p.nblocks) * BN;
-        rest /= p.nblocks;
-        u.tap = rest % p.taps;
-        rest /= p.taps;
+        const int pairs = (p.slots + 1) / 2;
+        u.tap = rest % pairs;  // slot pair: slots 2*tap and 2*tap + 1
+        rest /= pairs;
         u.j = rest % p.J;
         u.r = rest / p.J;
         u.c_begin = p.shard_chunks * u.j / p.J;
@@ -239,11 +245,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    const __grid_constant__ CUtensorMap bmap_hi, const __grid_constant__ CUtensorMap bmap_lo,
                    TcParams p) {
     extern __shared__ __align__(1024) unsigned char dsmem[];
-    unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle needs 1 KB
+    unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle atoms need 1 KB
     __shared__ Smem sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr uint32_t a_bytes = BM * 128;            // 128 rows x 32 tf32
-    constexpr uint32_t b_bytes = BN * 128;
+    constexpr uint32_t a_bytes = BM * ROWB;           // 128 rows x BK tf32
+    constexpr uint32_t b_bytes = BN * ROWB;
     constexpr uint32_t stage_bytes = 2 * a_bytes + 2 * b_bytes;
     volatile int* abort_flag = &sh.abort_flag;
 
@@ -276,7 +282,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (it >= p.stages && !mbar_wait(&sh.empty[s], (unsigned)(((it / p.stages) - 1) & 1), abort_flag))
                     break;
                 unsigned char* st = ring + (size_t)s * stage_bytes;
-                mbar_expect_tx(&sh.full[s], stage_bytes);
+                const bool second = p.mode == 0 || 2 * u.tap + 1 < p.slots;  // wgrad: last pair may be half
+                mbar_expect_tx(&sh.full[s], second ? stage_bytes : stage_bytes - b_bytes);
                 if (p.mode == 0) {
                     const int cpt = p.Kc / BK;
                     const int tap = (int)(c / cpt), cb = (int)(c % cpt);
@@ -288,19 +295,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tma_4d(st + 2 * a_bytes, &bmap_hi, cb * BK, wx, hy, u.n, &sh.full[s]);
                     tma_4d(st + 2 * a_bytes + b_bytes, &bmap_lo, cb * BK, wx, hy, u.n, &sh.full[s]);
                 } else {
-                    // pixel chunk c of shard r: (n, ho, 32-column piece); the tap's column
-                    // shift s = v - pad is read from the copy shifted right by jc = (-s) mod 4
-                    const int wc = (int)(c % p.row_chunks);
-                    const long long rest = c / p.row_chunks;
-                    const int ho = (int)(rest % p.Ho), n = (int)(rest / p.Ho);
+                    // pixel chunk c of shard r: (n, BK-column piece, ho), rows fastest so the
+                    // taps of one column strip reuse its rows while they are still in L2; the
+                    // tap's column shift s = v - pad is read from the copy shifted right by
+                    // jc = (-s) mod 4
+                    const int ho = (int)(c % p.Ho);
+                    const long long rest = c / p.Ho;
+                    const int wc = (int)(rest % p.row_chunks), n = (int)(rest / p.row_chunks);
                     const int w = u.r * p.own_w + wc * BK;
-                    const int uu = u.tap / p.kw, sft = u.tap % p.kw - p.pad;
-                    const int jc = ((-sft) % 4 + 4) % 4;
-                    tma_4d(st, &amap_hi, w, ho, u.m0, n, &sh.full[s]);
-                    tma_4d(st + a_bytes, &amap_lo, w, ho, u.m0, n, &sh.full[s]);
-                    tma_5d(st + 2 * a_bytes, &bmap_hi, w + sft + jc, ho + uu - p.pad, u.ci0, n, jc, &sh.full[s]);
-                    tma_5d(st + 2 * a_bytes + b_bytes, &bmap_lo, w + sft + jc, ho + uu - p.pad, u.ci0, n, jc,
-                           &sh.full[s]);
+                    tma_4d(st, &amap_hi, w, u.m0, ho, n, &sh.full[s]);
+                    tma_4d(st + a_bytes, &amap_lo, w, u.m0, ho, n, &sh.full[s]);
+                    // B = two 128-row halves, one per slot (tap, 128-channel block)
+                    for (int h = 0; h < 2; h++) {
+                        const int slot = 2 * u.tap + h;
+                        if (slot >= p.slots) break;
+                        const int tap = slot / p.nblocks, ci0 = (slot % p.nblocks) * 128;
+                        const int uu = tap / p.kw, sft = tap % p.kw - p.pad;
+                        const int jc = ((-sft) % 4 + 4) % 4;
+                        const uint32_t off = 2 * a_bytes + (uint32_t)h * (b_bytes / 2);
+                        tma_5d(st + off, &bmap_hi, w + sft + jc, ci0, ho + uu - p.pad, n, jc, &sh.full[s]);
+                        tma_5d(st + off + b_bytes, &bmap_lo, w + sft + jc, ci0, ho + uu - p.pad, n, jc, &sh.full[s]);
+                    }
                 }
             }
         }
@@ -339,8 +354,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     unsigned char *ahi = st, *alo = st + a_bytes, *bhi = st + 2 * a_bytes, *blo = bhi + b_bytes;
 #pragma unroll
                     for (int k = 0; k < BK / 8; k++) {  // 8 tf32 = 32 bytes along the swizzled row
-                        const uint64_t dah = sdesc(ahi + 32 * k, 16, 1024), dal = sdesc(alo + 32 * k, 16, 1024);
-                        const uint64_t dbh = sdesc(bhi + 32 * k, 16, 1024), dbl = sdesc(blo + 32 * k, 16, 1024);
+                        const uint64_t dah = sdesc(ahi + 32 * k, 16, SW_ATOM), dal = sdesc(alo + 32 * k, 16, SW_ATOM);
+                        const uint64_t dbh = sdesc(bhi + 32 * k, 16, SW_ATOM), dbl = sdesc(blo + 32 * k, 16, SW_ATOM);
                         tc_mma(d, dal, dbh, idesc, first ? 0u : 1u);
                         tc_mma(d, dah, dbl, idesc, 1u);
                         tc_mma(d, dah, dbh, idesc, 1u);
@@ -408,12 +423,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     *reinterpret_cast<float4*>(dst + k) =
                         make_float4(acc[k] + bv, acc[k + 1] + bv, acc[k + 2] + bv, acc[k + 3] + bv);
             } else {
-                const int co = u.m0 + row;
-                float* dst = p.part + ((((long long)u.r * p.J + u.j) * p.taps + u.tap) * p.Co + co) * p.Ci + u.ci0 +
-                             half * HC;
+                // column half = slot 2*pair + half (HC = 128 columns = one slot)
+                const int slot = 2 * u.tap + half;
+                if (slot < p.slots) {
+                    const int tap = slot / p.nblocks, ci0 = (slot % p.nblocks) * 128;
+                    const int co = u.m0 + row;
+                    float* dst =
+                        p.part + ((((long long)u.r * p.J + u.j) * p.taps + tap) * p.Co + co) * p.Ci + ci0;
 #pragma unroll
-                for (int k = 0; k < HC; k += 4)
-                    *reinterpret_cast<float4*>(dst + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+                    for (int k = 0; k < HC; k += 4)
+                        *reinterpret_cast<float4*>(dst + k) = make_float4(acc[k], acc[k + 1], acc[k + 2], acc[k + 3]);
+                }
             }
         }
     }
@@ -483,30 +503,42 @@ __global__ void prep_weight_kernel(const float* __restrict__ w, float* __restric
 }
 
 // NCHW -> NCHW tf32 hi / lo (the grad_output operand of the weight gradient).
-__global__ void prep_split_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                  long long n4) {
+// tf32 hi / lo split of an NCHW tensor, stored row-interleaved as [N][H][C][W]:
+// the C rows of one image row sit together, so a TMA box of many channels x a
+// few pixels covers a few hundred KB instead of one page per channel plane.
+__global__ void prep_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
+                                       int C, int H, int W, long long n4) {
+    const int W4 = W / 4;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
+        const long long row = q / W4;  // (n * C + c) * H + h
+        const int h = (int)(row % H);
+        const long long nc = row / H;
+        const int c = (int)(nc % C);
+        const long long n = nc / C;
+        const long long o = ((n * H + h) * C + c) * W4 + (q - row * W4);
         const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
-        float4 h, l;
-        h.x = tf32_rna(v.x); l.x = tf32_rna(v.x - h.x);
-        h.y = tf32_rna(v.y); l.y = tf32_rna(v.y - h.y);
-        h.z = tf32_rna(v.z); l.z = tf32_rna(v.z - h.z);
-        h.w = tf32_rna(v.w); l.w = tf32_rna(v.w - h.w);
-        reinterpret_cast<float4*>(hi)[q] = h;
-        reinterpret_cast<float4*>(lo)[q] = l;
+        float4 hv, l;
+        hv.x = tf32_rna(v.x); l.x = tf32_rna(v.x - hv.x);
+        hv.y = tf32_rna(v.y); l.y = tf32_rna(v.y - hv.y);
+        hv.z = tf32_rna(v.z); l.z = tf32_rna(v.z - hv.z);
+        hv.w = tf32_rna(v.w); l.w = tf32_rna(v.w - hv.w);
+        reinterpret_cast<float4*>(hi)[o] = hv;
+        reinterpret_cast<float4*>(lo)[o] = l;
     }
 }
 
-// Column-shifted tf32 hi / lo copies of x for the weight gradient:
-// c[j][n][c][h][i] = x[n][c][h][i - j] (zero outside [0, W)), j = 0..3, i < Wc = W + 4.
+// Column-shifted tf32 hi / lo copies of x for the weight gradient, row-interleaved:
+// c[j][n][h][c][i] = x[n][c][h][i - j] (zero outside [0, W)), j = 0..3, i < Wc = W + 4.
 // A tap's column shift s is then read from copy (-s) mod 4 at a 16-byte-aligned
 // column.  One block per input row: the row is staged in shared memory once
 // and the four shifted rows are written with 16-byte stores.
 __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                  long long rows, int W, int Wc, int copies) {
+                                  long long rows, int C, int H, int W, int Wc, int copies) {
     extern __shared__ float rowbuf[];  // [W + 8]: 4 zeros, the row, 4 zeros
-    const long long row = blockIdx.x;
+    const long long row = blockIdx.x;  // (n * C + c) * H + h
     const float* src = x + row * W;
+    const long long nc = row / H;
+    const long long orow = (nc / C * H + row % H) * C + nc % C;  // (n * H + h) * C + c
     for (int i = threadIdx.x; i < W + 8; i += blockDim.x) {
         const int c = i - 4;
         rowbuf[i] = (c >= 0 && c < W) ? __ldg(src + c) : 0.0f;
@@ -522,7 +554,7 @@ __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict
         h.y = tf32_rna(b); l.y = tf32_rna(b - h.y);
         h.z = tf32_rna(c); l.z = tf32_rna(c - h.z);
         h.w = tf32_rna(d); l.w = tf32_rna(d - h.w);
-        const long long o = ((long long)j * rows + row) * Wc + i0;
+        const long long o = ((long long)j * rows + orow) * Wc + i0;
         *reinterpret_cast<float4*>(hi + o) = h;
         *reinterpret_cast<float4*>(lo + o) = l;
     }
@@ -578,8 +610,8 @@ __global__ void zero_tail_kernel(float* __restrict__ hi, float* __restrict__ lo,
         lo[o] = 0.0f;
     }
 }
-//   planar form [N][Kp][Ho][Wo] (the weight gradient's B operand: pixels
-//   contiguous).  One block per input row (n, c, h = ho*s + u): the row is
+//   row-interleaved planar form [N][Ho][Kp][Wo] (the weight gradient's B
+//   operand: pixels contiguous).  One block per input row (n, c, h = ho*s + u): the row is
 //   staged once and written as s output rows, one per v.
 __global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
                                        int C, int H, int W, int s, int Kp) {
@@ -593,8 +625,8 @@ __global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __res
     const float* src = x + rid * W;
     for (int i = threadIdx.x; i < W; i += blockDim.x) row[i] = __ldg(src + i);
     __syncthreads();
-    for (int v = 0; v < s; v++) {
-        const long long o = (((long long)n * Kp + (u * s + v) * C + c) * Ho + ho) * Wo;
+    for (int v = 0; v < s; v++) {  // row-interleaved [N][Ho][Kp][Wo]
+        const long long o = (((long long)n * Ho + ho) * Kp + (u * s + v) * C + c) * Wo;
         for (int wo = threadIdx.x; wo < Wo; wo += blockDim.x) {
             const float val = row[wo * s + v];
             const float hv = tf32_rna(val);
@@ -603,15 +635,15 @@ __global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __res
         }
     }
 }
-// Zero the padding channels [k0, Kp) of a planar hi / lo pair ([N][Kp][HWo]).
-__global__ void zero_planar_kernel(float* __restrict__ hi, float* __restrict__ lo, int N, int k0, int Kp,
-                                   long long HWo) {
-    const long long per = (long long)(Kp - k0) * HWo;
-    const long long total = (long long)N * per;
+// Zero the padding channels [k0, Kp) of a row-interleaved hi / lo pair ([NHo][Kp][Wo]).
+__global__ void zero_planar_kernel(float* __restrict__ hi, float* __restrict__ lo, long long NHo, int k0, int Kp,
+                                   int Wo) {
+    const long long per = (long long)(Kp - k0) * Wo;
+    const long long total = NHo * per;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
          q += (long long)gridDim.x * blockDim.x) {
-        const long long n = q / per, r = q % per;
-        const long long o = (n * Kp + k0) * HWo + r;
+        const long long r = q / per, e = q % per;
+        const long long o = (r * Kp + k0) * Wo + e;
         hi[o] = 0.0f;
         lo[o] = 0.0f;
     }
@@ -708,7 +740,7 @@ hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtens
         cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         attr = true;
     }
-    const int stage_bytes = 2 * BM * 128 + 2 * BN * 128;
+    const int stage_bytes = 2 * BM * ROWB + 2 * BN * ROWB;
     p.stages = TC_SMEM_RING / stage_bytes;
     if (p.stages > 8) p.stages = 8;
     const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
@@ -718,47 +750,50 @@ hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtens
 
 hc_status launch_conv_pass(int BN, const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi,
                            const CUtensorMap& blo, TcParams p, cudaStream_t st) {
-    p.group = 8;
+    p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group
     if (BN == 256) return launch_bn<256>(ahi, alo, bhi, blo, p, st);
     if (BN == 128) return launch_bn<128>(ahi, alo, bhi, blo, p, st);
     return HC_ERR_UNSUPPORTED;
 }
 
-// NHWC activation map for the conv pass: dims (Cp, W, H, N), box (32, BN, 1, 1).
+// NHWC activation map for the conv pass: dims (Cp, W, H, N), box (BK, BN, 1, 1).
 hc_status act_map_conv(CUtensorMap* m, const float* base, int N, int H, int W, int Cp, int BN) {
     const uint64_t dims[4] = {(uint64_t)Cp, (uint64_t)W, (uint64_t)H, (uint64_t)N};
     const uint64_t strides[3] = {(uint64_t)Cp * 4, (uint64_t)W * Cp * 4, (uint64_t)H * W * Cp * 4};
-    const uint32_t box[4] = {32, (uint32_t)BN, 1, 1};
+    const uint32_t box[4] = {BK, (uint32_t)BN, 1, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Weight map: dims (Ktot, Mp), box (32, 128).
+// Weight map: dims (Ktot, Mp), box (BK, 128).
 hc_status weight_map(CUtensorMap* m, const float* base, int Mp, long long ktot) {
     const uint64_t dims[2] = {(uint64_t)ktot, (uint64_t)Mp};
     const uint64_t strides[1] = {(uint64_t)ktot * 4};
-    const uint32_t box[2] = {32, 128};
+    const uint32_t box[2] = {BK, 128};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// NCHW map for K-major weight-gradient tiles (pixels contiguous): dims (W, H, C, N),
-// box (32, 1, rows, 1): smem [rows channels][32 pixels].
-hc_status nchw_map(CUtensorMap* m, const float* base, int N, int C, int H, int W, int rows) {
-    const uint64_t dims[4] = {(uint64_t)W, (uint64_t)H, (uint64_t)C, (uint64_t)N};
-    const uint64_t strides[3] = {(uint64_t)W * 4, (uint64_t)H * W * 4, (uint64_t)C * H * W * 4};
-    const uint32_t box[4] = {32, 1, (uint32_t)rows, 1};
+// Row-interleaved [N][H][C][W] map for K-major weight-gradient tiles (pixels
+// contiguous): dims (W, C, H, N), box (BK, rows, 1, 1): smem [rows channels][BK pixels].
+hc_status rows_map(CUtensorMap* m, const float* base, int N, int C, int H, int W, int rows) {
+    const uint64_t dims[4] = {(uint64_t)W, (uint64_t)C, (uint64_t)H, (uint64_t)N};
+    const uint64_t strides[3] = {(uint64_t)W * 4, (uint64_t)C * W * 4, (uint64_t)H * C * W * 4};
+    const uint32_t box[4] = {BK, (uint32_t)rows, 1, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Column-shifted copies: dims (Wc, H, C, N, copies), box (32, 1, rows, 1, 1).
+// Row-interleaved column-shifted copies [copies][N][H][C][Wc]: dims (Wc, C, H, N,
+// copies), box (BK, rows, 1, 1, 1).
 hc_status shifted_map(CUtensorMap* m, const float* base, int N, int C, int H, int Wc, int rows, int copies = 4) {
-    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)H, (uint64_t)C, (uint64_t)N, (uint64_t)copies};
-    const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)H * Wc * 4, (uint64_t)C * H * Wc * 4,
+    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)C, (uint64_t)H, (uint64_t)N, (uint64_t)copies};
+    const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)C * Wc * 4, (uint64_t)H * C * Wc * 4,
                                  (uint64_t)N * C * H * Wc * 4};
-    const uint32_t box[5] = {32, 1, (uint32_t)rows, 1, 1};
+    const uint32_t box[5] = {BK, (uint32_t)rows, 1, 1, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// weight-gradient tiles: 128 output channels x 128 input channels of one tap
-constexpr int WG_BN = 128;
+// weight-gradient tiles: 128 output channels x two slots of 128 input channels
+// (a slot is one tap x one 128-channel block)
+constexpr int WG_BN = 256;
+constexpr int WG_SLOT = 128;
 
 
 // k = stride = s >= 2 without padding: every output pixel reads its own s x s
@@ -790,20 +825,32 @@ bool tc_supported(const hc_conv_desc* d, const Plan& p) {
 int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
     const bool sd = is_s2d(d);
     const int KK = sd ? 1 : d->kh * d->kw;
-    const int nb = sd ? s2d_kp(d) / WG_BN : d->C_in / WG_BN;
-    const long long units0 = (long long)(d->C_out / BM) * KK * nb * p.S;
-    const long long chunks = (long long)d->N * p.Ho * ((p.Wl / d->stride) / 32);
-    // enough units for about four waves, each unit at least 64 chunks long
-    long long J = (4LL * sm_count_tc() + units0 - 1) / units0;
-    if (J > chunks / 64) J = chunks / 64;
-    if (J < 1) J = 1;
-    return (int)J;
+    const int nb = sd ? s2d_kp(d) / WG_SLOT : d->C_in / WG_SLOT;
+    const long long units0 = (long long)(d->C_out / BM) * ((KK * nb + 1) / 2) * p.S;
+    const long long chunks = (long long)d->N * p.Ho * ((p.Wl / d->stride) / BK);
+    // Units are equally long, so the persistent grid runs ceil(units / SMs) waves.
+    // Take the smallest split that fills every SM and keeps the last wave at least
+    // 95 % full (each unit at least 2048 pixels long); else the best-filled split.
+    const long long P = sm_count_tc();
+    const long long jmax = chunks * BK / 2048 > 1 ? chunks * BK / 2048 : 1;
+    long long best = 1;
+    double best_fill = 0.0;
+    for (long long J = 1; J <= jmax; J++) {
+        const long long units = units0 * J;
+        const double fill = (double)units / (double)(((units + P - 1) / P) * P);
+        if (units >= P && fill >= 0.95) return (int)J;
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            best = J;
+        }
+    }
+    return (int)best;
 }
 
 // Workspace: forward  [x NHWC hi][x NHWC lo][A hi][A lo]
-//            backward [gy NHWC hi][lo][A' hi][lo][gy NCHW hi][lo][x shifted hi][lo][split-K partials]
+//            backward [gy NHWC hi][lo][A' hi][lo][gy NHCW hi][lo][x shifted hi][lo][split-K partials]
 size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
-    if (is_s2d(d)) {  // forward [s2d NHWC hi][lo][A hi][lo]; backward [gy NHWC hi][lo][A' hi][lo][gy NCHW hi][lo][s2d planar hi][lo][partials]
+    if (is_s2d(d)) {  // forward [s2d NHWC hi][lo][A hi][lo]; backward [gy NHWC hi][lo][A' hi][lo][gy NHCW hi][lo][s2d planar hi][lo][partials]
         const size_t npx = (size_t)d->N * p.Ho * p.Wo, kp = s2d_kp(d);
         const size_t ns = npx * kp, ng = npx * d->C_out, wsz = (size_t)d->C_out * kp;
         if (pass == 0) return 2 * al256(4 * ns) + 2 * al256(4 * wsz);
@@ -924,14 +971,15 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         if ((e = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return e;
     }
     if (want_w) {  // G[co][(u,v,c)] = sum over a shard's pixels of gy[co][px] s2d[(u,v,c)][px]
-        prep_split_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, (long long)ng / 4);
+        prep_split_rows_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, Co, p.Ho, p.Wo,
+                                                                              (long long)ng / 4);
         if ((e = launched())) return e;
         const long long rows = (long long)d->N * Ci * d->H;
         if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
         prep_s2d_planar_kernel<<<(unsigned)rows, 256, sizeof(float) * d->W, st>>>(x, sh, sl, Ci, d->H, d->W, s, Kp);
         if ((e = launched())) return e;
         if (Kp > s * s * Ci) {
-            zero_planar_kernel<<<152 * 16, 256, 0, st>>>(sh, sl, d->N, s * s * Ci, Kp, (long long)p.Ho * p.Wo);
+            zero_planar_kernel<<<152 * 16, 256, 0, st>>>(sh, sl, (long long)d->N * p.Ho, s * s * Ci, Kp, p.Wo);
             if ((e = launched())) return e;
         }
         TcParams tp{};
@@ -941,21 +989,22 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         tp.S = p.S;
         tp.J = tc_wgrad_splits(d, p);
         tp.own_w = p.Wl / s;
-        tp.row_chunks = tp.own_w / 32;
+        tp.row_chunks = tp.own_w / BK;
         tp.Ho = p.Ho;
         tp.kh = 1;
         tp.kw = 1;
         tp.pad = 0;
         tp.taps = 1;
         tp.mblocks = Co / BM;
-        tp.nblocks = Kp / WG_BN;
+        tp.nblocks = Kp / WG_SLOT;
+        tp.slots = tp.nblocks;
         tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
-        tp.units = tp.mblocks * tp.nblocks * tp.J * p.S;
+        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
         tp.part = part;
         CUtensorMap mah, mal, mbh, mbl;
-        if ((e = nchw_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (e = nchw_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (e = shifted_map(&mbh, sh, d->N, Kp, p.Ho, p.Wo, WG_BN, 1)) ||
-            (e = shifted_map(&mbl, sl, d->N, Kp, p.Ho, p.Wo, WG_BN, 1)))
+        if ((e = rows_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (e = rows_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (e = shifted_map(&mbh, sh, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)) ||
+            (e = shifted_map(&mbl, sl, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)))
             return e;
         if ((e = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return e;
         const long long total = (long long)p.S * Co * Ci * s * s;
@@ -1067,11 +1116,13 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         if ((s = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return s;
     }
     if (want_w) {
-        prep_split_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, (long long)ng / 4);
+        prep_split_rows_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, Co, p.Ho, p.Wo,
+                                                                              (long long)ng / 4);
         if ((s = launched())) return s;
         const long long rows = (long long)d->N * Ci * d->H;
         if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, d->W, Wc, copies);
+        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
+                                                                                    Wc, copies);
         if ((s = launched())) return s;
         TcParams tp{};
         tp.mode = 1;
@@ -1080,21 +1131,22 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.S = p.S;
         tp.J = tc_wgrad_splits(d, p);
         tp.own_w = p.Wl;
-        tp.row_chunks = p.Wl / 32;
+        tp.row_chunks = p.Wl / BK;
         tp.Ho = p.Ho;
         tp.kh = K;
         tp.kw = K;
         tp.pad = d->padding;
         tp.taps = KK;
         tp.mblocks = Co / BM;
-        tp.nblocks = Ci / WG_BN;
+        tp.nblocks = Ci / WG_SLOT;
+        tp.slots = KK * tp.nblocks;
         tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
-        tp.units = tp.mblocks * tp.nblocks * KK * tp.J * p.S;
+        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
         tp.part = part;
         CUtensorMap mah, mal, mbh, mbl;
-        if ((s = nchw_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (s = nchw_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_BN, copies)) ||
-            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_BN, copies)))
+        if ((s = rows_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (s = rows_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_SLOT, copies)) ||
+            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
             return s;
         if ((s = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return s;
         const long long total = (long long)p.S * wsz;
