@@ -22,33 +22,59 @@ __global__ void sum_rows_kernel(const float* __restrict__ in, float* __restrict_
     }
 }
 
-// Bias-gradient partial sums, stage 1: block (slice, co, r) sums grad_output over
-// its slice of the (n, i) rows and shard r's own output columns, in a fixed
-// order (strided thread sums, then a shuffle tree and the warp sums in order).
-// part[(slice * S + r) * Co + co].
-__global__ void bias_slices_kernel(const float* __restrict__ gy, float* __restrict__ part, int N, int Co, int Ho,
-                                   int Wo, int S, int own_w, int slices) {
-    __shared__ float red[32];
-    const int slice = blockIdx.x, co = blockIdx.y, r = blockIdx.z;
-    const int j0 = r * own_w, j1 = (r == S - 1) ? Wo : j0 + own_w;
-    const int nj = j1 - j0;
-    const long long nrows = (long long)N * Ho;
-    const long long r0 = nrows * slice / slices, r1 = nrows * (slice + 1) / slices;
-    float acc = 0.0f;
-    for (long long row = r0; row < r1; row++) {
-        const int n = (int)(row / Ho), i = (int)(row % Ho);
-        const float* p = gy + (((long long)n * Co + co) * Ho + i) * Wo + j0;
-        for (int j = threadIdx.x; j < nj; j += blockDim.x) acc += __ldg(p + j);
+// Bias-gradient partial sums, stage 1: block (slice, co) streams whole rows
+// (n, i) of its slice of grad_output channel co with 16-byte loads, 1024
+// columns at a time: each thread sums its four columns down the rows, then
+// thread r adds the column sums of shard r (shard of column j = j / own_w, the
+// last shard taking the rest) in column order.  Every sum has a fixed order.
+// part[(slice * S + r) * Co + co].  Needs Wo % 4 == 0, S <= 256, 256 threads.
+__global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict__ gy, float* __restrict__ part, int N,
+                                                        int Co, int Ho, int Wo, int S, int own_w, int slices) {
+    __shared__ float cs[256];
+    const int slice = blockIdx.x, co = blockIdx.y, tid = threadIdx.x;
+    const int nrows = N * Ho;
+    const int r0 = (int)((long long)nrows * slice / slices), r1 = (int)((long long)nrows * (slice + 1) / slices);
+    float total = 0.0f;  // thread r < S: shard r's running sum
+    for (int g0 = 0; g0 < Wo; g0 += 1024) {
+        const int col = g0 + 4 * tid;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (col < Wo) {
+            const float* base = gy + (long long)co * Ho * Wo + col;
+            int row = r0;
+            for (; row + 4 <= r1; row += 4) {  // four loads in flight, added in row order
+                float4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int n = (row + k) / Ho, i = row + k - n * Ho;
+                    v[k] = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    acc.x += v[k].x;
+                    acc.y += v[k].y;
+                    acc.z += v[k].z;
+                    acc.w += v[k].w;
+                }
+            }
+            for (; row < r1; row++) {
+                const int n = row / Ho, i = row - n * Ho;
+                const float4 v = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        }
+        cs[tid] = ((acc.x + acc.y) + acc.z) + acc.w;
+        __syncthreads();
+        if (tid < S) {
+            const int j0 = tid * own_w, j1 = (tid == S - 1) ? Wo : j0 + own_w;
+            const int a = (j0 > g0 ? j0 : g0), b = (j1 < g0 + 1024 ? j1 : g0 + 1024);
+            for (int k = a; k < b; k += 4) total += cs[(k - g0) / 4];
+        }
+        __syncthreads();
     }
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float t = 0.0f;
-        for (int k = 0; k < (int)(blockDim.x >> 5); k++) t += red[k];
-        part[((long long)slice * S + r) * Co + co] = t;
-    }
+    if (tid < S) part[((long long)slice * S + tid) * Co + co] = total;
 }
 
 // Column sums, stage 1: tmp[g][k] = sum over rows r in group g (ascending) of
@@ -87,10 +113,17 @@ size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co;
 
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
                                     float* tmp, cudaStream_t st) {
-    bias_slices_kernel<<<dim3(kBiasSlices, Co, S), 128, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, kBiasSlices);
+    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || (long long)N * Ho > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+    // about eight blocks per SM, at most kBiasSlices slices
+    const long long nrows = (long long)N * Ho;
+    long long slices = (152LL * 8 + Co - 1) / Co;
+    if (slices > kBiasSlices) slices = kBiasSlices;
+    if (slices > nrows) slices = nrows;
+    if (slices < 1) slices = 1;
+    bias_rows_kernel<<<dim3((unsigned)slices, Co), 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, (int)slices);
     hc_status s = launched();
     if (s) return s;
-    return launch_sum_rows(tmp, gbp, kBiasSlices, (long long)S * Co, st);  // slices in order
+    return launch_sum_rows(tmp, gbp, (int)slices, (long long)S * Co, st);  // slices in order
 }
 
 hc_status launch_sum_rows(const float* in, float* out, int rows, long long count, cudaStream_t st) {

@@ -405,14 +405,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             if (!ok) break;
             if (p.mode == 0 && p.d2s) {
+                // row m = (uu*C + c)*sd + vv holds image pixels (ho*sd + uu, (w0 + k)*sd + vv)
                 const int m = u.m0 + row, sd = p.d2s;
-                if (m < sd * sd * p.d2s_c) {
-                    const int tap = m / p.d2s_c, c = m - tap * p.d2s_c, uu = tap / sd, vv = tap - uu * sd;
-                    const int Wimg = p.Wo * sd;
-                    float* dst = p.out + (((long long)u.n * p.d2s_c + c) * p.Ho * sd + u.ho * sd + uu) * Wimg +
-                                 (long long)(u.w0 + half * HC) * sd + vv;
+                const bool valid = m < sd * sd * p.d2s_c;
+                const int uc = m / sd, vv = m - uc * sd, uu = uc / p.d2s_c, c = uc - uu * p.d2s_c;
+                const int Wimg = p.Wo * sd;
+                float* dst = p.out + (((long long)u.n * p.d2s_c + c) * p.Ho * sd + u.ho * sd + uu) * Wimg +
+                             (long long)(u.w0 + half * HC) * sd;
+                if (sd == 2) {
+                    // lanes 2i, 2i+1 hold vv = 0, 1 of one (uu, c) (s*s*C is even, so both or
+                    // neither are valid); per 4 columns each passes the other two values and
+                    // stores 4 consecutive pixels: lane vv=0 pixels 8j..8j+3, vv=1 8j+4..8j+7
+                    const bool odd = vv != 0;
+                    const unsigned mask = __activemask();  // the whole warp unless a wait timed out
 #pragma unroll
-                    for (int k = 0; k < HC; k++) dst[(long long)k * sd] = acc[k];
+                    for (int j = 0; j < HC / 4; j++) {
+                        const float s0 = odd ? acc[4 * j] : acc[4 * j + 2];
+                        const float s1 = odd ? acc[4 * j + 1] : acc[4 * j + 3];
+                        const float r0 = __shfl_xor_sync(mask, s0, 1);
+                        const float r1 = __shfl_xor_sync(mask, s1, 1);
+                        const float4 o = odd ? make_float4(r0, acc[4 * j + 2], r1, acc[4 * j + 3])
+                                             : make_float4(acc[4 * j], r0, acc[4 * j + 1], r1);
+                        if (valid) *reinterpret_cast<float4*>(dst + 8 * j + (odd ? 4 : 0)) = o;
+                    }
+                } else if (valid) {
+#pragma unroll
+                    for (int k = 0; k < HC; k++) dst[(long long)k * sd + vv] = acc[k];
                 }
             } else if (p.mode == 0) {
                 const int m = u.m0 + row;
@@ -452,29 +470,51 @@ __device__ __forceinline__ float tf32_rna(float x) {
 }
 
 // NCHW [N][C][H][W] -> NHWC [N][H][W][Cp] split into tf32 hi / lo (channels
-// C..Cp-1 zero).  32x32 (channel x column) tiles through shared memory so
-// both the reads and the writes are coalesced.
-__global__ void prep_nhwc_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo, int C,
-                                 int H, int W, int Cp) {
-    __shared__ float t[32][33];
-    const int w0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+// C..Cp-1 zero).  Tiles of 64 channels x 32 columns go through shared memory
+// (row pitch 33): 16-byte loads along the rows and 16-byte stores of four
+// channels, both coalesced and free of bank conflicts.  Needs W % 4 == 0 and
+// Cp % 64 == 0; 256 threads.
+__global__ void __launch_bounds__(256) prep_nhwc_kernel(const float* __restrict__ x, float* __restrict__ hi,
+                                                        float* __restrict__ lo, int C, int H, int W, int Cp) {
+    __shared__ float t[64][33];
+    const int w0 = blockIdx.x * 32, c0 = blockIdx.y * 64;
     const int nh = blockIdx.z;  // n * H + h
     const int n = nh / H, h = nh % H;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int c = c0 + i, w = w0 + threadIdx.x;
-        t[i][threadIdx.x] = (c < C && w < W) ? __ldg(x + (((long long)n * C + c) * H + h) * W + w) : 0.0f;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int it = 0; it < 2; it++) {  // 64 channel rows x 8 float4
+        const int cl = tid / 8 + 32 * it, w4 = tid % 8;
+        const int c = c0 + cl, w = w0 + 4 * w4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (c < C && w < W) v = __ldg(reinterpret_cast<const float4*>(x + (((long long)n * C + c) * H + h) * W + w));
+        t[cl][4 * w4] = v.x;
+        t[cl][4 * w4 + 1] = v.y;
+        t[cl][4 * w4 + 2] = v.z;
+        t[cl][4 * w4 + 3] = v.w;
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int w = w0 + i, c = c0 + threadIdx.x;
-        if (w < W && c < Cp) {
-            const float v = t[threadIdx.x][i];
-            const float vh = tf32_rna(v);
-            const long long o = (((long long)n * H + h) * W + w) * Cp + c;
-            hi[o] = vh;
-            lo[o] = tf32_rna(v - vh);
+#pragma unroll
+    for (int it = 0; it < 2; it++) {  // 32 pixels x 16 groups of four channels
+        const int cg = tid % 8 + 8 * it, wl = tid / 8;
+        const int w = w0 + wl;
+        if (w < W) {
+            const float4 v = make_float4(t[4 * cg][wl], t[4 * cg + 1][wl], t[4 * cg + 2][wl], t[4 * cg + 3][wl]);
+            float4 vh, vl;
+            vh.x = tf32_rna(v.x); vl.x = tf32_rna(v.x - vh.x);
+            vh.y = tf32_rna(v.y); vl.y = tf32_rna(v.y - vh.y);
+            vh.z = tf32_rna(v.z); vl.z = tf32_rna(v.z - vh.z);
+            vh.w = tf32_rna(v.w); vl.w = tf32_rna(v.w - vh.w);
+            const long long o = (((long long)n * H + h) * W + w) * Cp + c0 + 4 * cg;
+            *reinterpret_cast<float4*>(hi + o) = vh;
+            *reinterpret_cast<float4*>(lo + o) = vl;
         }
     }
+}
+hc_status launch_prep_nhwc(const float* x, float* hi, float* lo, int N, int C, int H, int W, int Cp,
+                           cudaStream_t st) {
+    if (Cp % 64 || W % 4 || (long long)N * H > 65535) return HC_ERR_UNSUPPORTED;
+    prep_nhwc_kernel<<<dim3(cdiv(W, 32), Cp / 64, N * H), 256, 0, st>>>(x, hi, lo, C, H, W, Cp);
+    return launched();
 }
 
 // Weights as the A operand of the conv pass: A[m][(u*kw+v)*Kc + c], hi / lo.
@@ -599,6 +639,60 @@ __global__ void prep_s2d_nhwc_kernel(const float* __restrict__ x, float* __restr
         __syncthreads();
     }
 }
+// The same for C % 64 == 0, with 16-byte accesses: block (32 output columns,
+// 64 channels, (n, ho)), 256 threads, shared tile [64][32*S + 1].  For each
+// kernel row u the 64 input rows are read as float4 (coalesced), then every
+// (input column, four channels) is written as one float4 to output pixel
+// wo = col / S, channel block v = col % S (128 contiguous bytes per 8 lanes;
+// 8 channel groups x 4 columns per warp hit 32 distinct banks).
+template <int S>
+__global__ void __launch_bounds__(256) prep_s2d_nhwc64_kernel(const float* __restrict__ x, float* __restrict__ hi,
+                                                              float* __restrict__ lo, int C, int H, int W, int Kp) {
+    extern __shared__ float t2[];  // [64][32 * S + 1]
+    constexpr int COLS = 32 * S, PITCH = COLS + 1;
+    const int Ho = H / S, Wo = W / S;
+    const int wo0 = blockIdx.x * 32, c0 = blockIdx.y * 64;
+    const int n = blockIdx.z / Ho, ho = blockIdx.z % Ho;
+    const int tid = threadIdx.x;
+#pragma unroll 1
+    for (int u = 0; u < S; u++) {
+#pragma unroll
+        for (int i = 0; i < 2 * S; i++) {  // 64 rows x 8*S float4
+            const int idx = tid + 256 * i;
+            const int cl = idx / (8 * S), q = idx % (8 * S);
+            const int w = wo0 * S + 4 * q;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (w < W)
+                v = __ldg(reinterpret_cast<const float4*>(x + (((long long)n * C + c0 + cl) * H + ho * S + u) * W + w));
+            float* r = t2 + cl * PITCH + 4 * q;
+            r[0] = v.x;
+            r[1] = v.y;
+            r[2] = v.z;
+            r[3] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2 * S; i++) {  // COLS columns x 16 groups of four channels
+            const int idx = tid + 256 * i;
+            const int cg = idx % 8 + 8 * (idx / (8 * COLS));
+            const int col = (idx / 8) % COLS;
+            const int wo = wo0 + col / S, v = col % S;
+            if (wo < Wo) {
+                const float* r = t2 + 4 * cg * PITCH + col;
+                const float4 a = make_float4(r[0], r[PITCH], r[2 * PITCH], r[3 * PITCH]);
+                float4 vh, vl;
+                vh.x = tf32_rna(a.x); vl.x = tf32_rna(a.x - vh.x);
+                vh.y = tf32_rna(a.y); vl.y = tf32_rna(a.y - vh.y);
+                vh.z = tf32_rna(a.z); vl.z = tf32_rna(a.z - vh.z);
+                vh.w = tf32_rna(a.w); vl.w = tf32_rna(a.w - vh.w);
+                const long long o = (((long long)n * Ho + ho) * Wo + wo) * Kp + (u * S + v) * C + c0 + 4 * cg;
+                *reinterpret_cast<float4*>(hi + o) = vh;
+                *reinterpret_cast<float4*>(lo + o) = vl;
+            }
+        }
+        __syncthreads();
+    }
+}
 // Zero the channel tail [k0, Kp) of every pixel of an NHWC hi / lo pair.
 __global__ void zero_tail_kernel(float* __restrict__ hi, float* __restrict__ lo, long long pixels, int k0, int Kp) {
     const int tail = Kp - k0;
@@ -611,27 +705,44 @@ __global__ void zero_tail_kernel(float* __restrict__ hi, float* __restrict__ lo,
     }
 }
 //   row-interleaved planar form [N][Ho][Kp][Wo] (the weight gradient's B
-//   operand: pixels contiguous).  One block per input row (n, c, h = ho*s + u): the row is
-//   staged once and written as s output rows, one per v.
+//   operand: pixels contiguous).  Each item reads 4*S consecutive columns of one
+//   input row (n, c, h = ho*S + u) as S float4 and writes, for every v, the four
+//   output columns wo = 4j..4j+3 of row (n, ho, (u*S + v)*C + c) as one float4.
+//   Needs Wo % 4 == 0.
+template <int S>
 __global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                       int C, int H, int W, int s, int Kp) {
-    extern __shared__ float row[];
-    const int Ho = H / s, Wo = W / s;
-    const long long rid = blockIdx.x;  // (n * C + c) * H + h
-    const int h = (int)(rid % H);
-    const long long nc = rid / H;
-    const int c = (int)(nc % C), n = (int)(nc / C);
-    const int ho = h / s, u = h - ho * s;
-    const float* src = x + rid * W;
-    for (int i = threadIdx.x; i < W; i += blockDim.x) row[i] = __ldg(src + i);
-    __syncthreads();
-    for (int v = 0; v < s; v++) {  // row-interleaved [N][Ho][Kp][Wo]
-        const long long o = (((long long)n * Ho + ho) * Kp + (u * s + v) * C + c) * Wo;
-        for (int wo = threadIdx.x; wo < Wo; wo += blockDim.x) {
-            const float val = row[wo * s + v];
-            const float hv = tf32_rna(val);
-            hi[o + wo] = hv;
-            lo[o + wo] = tf32_rna(val - hv);
+                                       int C, int H, int W, int Kp, long long items) {
+    const int Ho = H / S, Wo = W / S, J = Wo / 4;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < items;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long rid = q / J;  // (n * C + c) * H + h
+        const int j = (int)(q - rid * J);
+        const int h = (int)(rid % H);
+        const long long nc = rid / H;
+        const int c = (int)(nc % C);
+        const long long n = nc / C;
+        const int ho = h / S, u = h - ho * S;
+        float e[4 * S];
+        const float4* src = reinterpret_cast<const float4*>(x + rid * W + 4LL * j * S);
+#pragma unroll
+        for (int k = 0; k < S; k++) {
+            const float4 a = __ldg(src + k);
+            e[4 * k] = a.x;
+            e[4 * k + 1] = a.y;
+            e[4 * k + 2] = a.z;
+            e[4 * k + 3] = a.w;
+        }
+#pragma unroll
+        for (int v = 0; v < S; v++) {
+            const float4 a = make_float4(e[v], e[S + v], e[2 * S + v], e[3 * S + v]);
+            float4 vh, vl;
+            vh.x = tf32_rna(a.x); vl.x = tf32_rna(a.x - vh.x);
+            vh.y = tf32_rna(a.y); vl.y = tf32_rna(a.y - vh.y);
+            vh.z = tf32_rna(a.z); vl.z = tf32_rna(a.z - vh.z);
+            vh.w = tf32_rna(a.w); vl.w = tf32_rna(a.w - vh.w);
+            const long long o = ((n * Ho + ho) * Kp + (u * S + v) * C + c) * Wo + 4LL * j;
+            *reinterpret_cast<float4*>(hi + o) = vh;
+            *reinterpret_cast<float4*>(lo + o) = vl;
         }
     }
 }
@@ -648,8 +759,10 @@ __global__ void zero_planar_kernel(float* __restrict__ hi, float* __restrict__ l
         lo[o] = 0.0f;
     }
 }
-// Weights in space-to-depth order: forward A[co][k] = w[co][c][u][v];
-// grad_input (transpose) A[k][co] = w[co][c][u][v]; k = (u*s + v)*C + c < s*s*C.
+// Weights in space-to-depth order: forward A[co][k] = w[co][c][u][v] with
+// k = (u*s + v)*C + c; grad_input (transpose) A[m][co] = w[co][c][u][v] with
+// m = (u*C + c)*s + v, so that the s outputs of one (u, c) that interleave along
+// an image row sit in adjacent TMEM lanes.  Rows / columns >= s*s*C are zero.
 __global__ void prep_weight_s2d_kernel(const float* __restrict__ w, float* __restrict__ hi, float* __restrict__ lo,
                                        int Co, int C, int s, int Kp, int transpose) {
     const long long total = (long long)Co * Kp;
@@ -665,7 +778,18 @@ __global__ void prep_weight_s2d_kernel(const float* __restrict__ w, float* __res
         }
         float v = 0.0f;
         if (k < s * s * C) {
-            const int tap = k / C, c = k - tap * C, uu = tap / s, vv = tap - uu * s;
+            int c, uu, vv;
+            if (!transpose) {  // k = (u*s + v)*C + c: the channel order of the space-to-depth copies
+                const int tap = k / C;
+                c = k - tap * C;
+                uu = tap / s;
+                vv = tap - uu * s;
+            } else {  // row k = (u*C + c)*s + v: the s rows of one (u, c) are adjacent
+                const int uc = k / s;
+                vv = k - uc * s;
+                uu = uc / C;
+                c = uc - uu * C;
+            }
             v = __ldg(w + (((long long)co * C + c) * s + uu) * s + vv);
         }
         const float h = tf32_rna(v);
@@ -725,9 +849,14 @@ int sm_count_tc() {
     return n;
 }
 
-int pick_bn(int own_out_w) {
-    if (own_out_w % 256 == 0) return 256;
-    if (own_out_w % 128 == 0) return 128;
+// Accumulator columns of a conv-pass tile: a segment of one output row.  Every
+// output pixel's sum over taps and channel chunks runs in the same order
+// whichever tile holds it, and the boxes' neighbour-column reads at a shard
+// edge are exactly that shard's halo, so a tile may cross shard boundaries;
+// its width is picked from the whole row.
+int pick_bn(int out_w) {
+    if (out_w % 256 == 0) return 256;
+    if (out_w % 128 == 0) return 128;
     return 0;
 }
 
@@ -868,6 +997,46 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
 }
 
+static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, const float* x, float* hi, float* lo,
+                                      int Kp, cudaStream_t st) {
+    const int s = d->stride, C = d->C_in;
+    if ((long long)d->N * p.Ho > 65535) return HC_ERR_UNSUPPORTED;
+    if (C % 64 == 0 && d->W % 4 == 0) {
+        const dim3 grid(cdiv(p.Wo, 32), C / 64, d->N * p.Ho);
+        const size_t smem = sizeof(float) * 64 * (32 * s + 1);
+        if (s == 2)
+            prep_s2d_nhwc64_kernel<2><<<grid, 256, smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else if (s == 3)
+            prep_s2d_nhwc64_kernel<3><<<grid, 256, smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else if (s == 4)
+            prep_s2d_nhwc64_kernel<4><<<grid, 256, smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else
+            return HC_ERR_UNSUPPORTED;
+    } else {
+        prep_s2d_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(C, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(x, hi, lo, C, d->H,
+                                                                                                  d->W, s, Kp);
+    }
+    return launched();
+}
+static hc_status launch_prep_s2d_planar(const hc_conv_desc* d, const Plan& p, const float* x, float* hi, float* lo,
+                                        int Kp, cudaStream_t st) {
+    const int s = d->stride;
+    if (p.Wo % 4) return HC_ERR_UNSUPPORTED;
+    const long long items = (long long)d->N * d->C_in * d->H * (p.Wo / 4);
+    long long blocks = (items + 255) / 256;
+    if (blocks > 152LL * 32) blocks = 152LL * 32;
+    if (blocks < 1) blocks = 1;
+    if (s == 2)
+        prep_s2d_planar_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(x, hi, lo, d->C_in, d->H, d->W, Kp, items);
+    else if (s == 3)
+        prep_s2d_planar_kernel<3><<<(unsigned)blocks, 256, 0, st>>>(x, hi, lo, d->C_in, d->H, d->W, Kp, items);
+    else if (s == 4)
+        prep_s2d_planar_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(x, hi, lo, d->C_in, d->H, d->W, Kp, items);
+    else
+        return HC_ERR_UNSUPPORTED;
+    return launched();
+}
+
 static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                          float* y, void* ws, cudaStream_t st) {
     const int s = d->stride, Co = d->C_out, Kp = s2d_kp(d);
@@ -881,9 +1050,7 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     q += al256(4 * wsz);
     float* al = (float*)q;
     if (s > 4) return HC_ERR_UNSUPPORTED;
-    prep_s2d_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(d->C_in, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(
-        x, xh, xl, d->C_in, d->H, d->W, s, Kp);
-    hc_status e = launched();
+    hc_status e = launch_prep_s2d_nhwc(d, p, x, xh, xl, Kp, st);
     if (e) return e;
     if (Kp > s * s * d->C_in) {
         const long long pixels = (long long)d->N * p.Ho * p.Wo;
@@ -892,7 +1059,7 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     }
     prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, d->C_in, s, Kp, 0);
     if ((e = launched())) return e;
-    const int BN = pick_bn(p.Wl / s);
+    const int BN = pick_bn(p.Wo);
     TcParams tp{};
     tp.mode = 0;
     tp.N = d->N;
@@ -938,12 +1105,10 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     float* sl = (float*)q;
     q += al256(4 * ns);
     float* part = (float*)q;
-    const int BN = pick_bn(p.Wl / s);
+    const int BN = pick_bn(p.Wo);
     hc_status e;
     if (gx) {  // D[(u,v,c)][px] = sum_co w[co][c][u][v] gy[co][px], stored depth-to-space
-        prep_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(Co, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(gy, gh, gl, Co,
-                                                                                                p.Ho, p.Wo, Co);
-        if ((e = launched())) return e;
+        if ((e = launch_prep_nhwc(gy, gh, gl, d->N, Co, p.Ho, p.Wo, Co, st))) return e;
         prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, s, Kp, 1);
         if ((e = launched())) return e;
         TcParams tp{};
@@ -974,10 +1139,7 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         prep_split_rows_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, Co, p.Ho, p.Wo,
                                                                               (long long)ng / 4);
         if ((e = launched())) return e;
-        const long long rows = (long long)d->N * Ci * d->H;
-        if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        prep_s2d_planar_kernel<<<(unsigned)rows, 256, sizeof(float) * d->W, st>>>(x, sh, sl, Ci, d->H, d->W, s, Kp);
-        if ((e = launched())) return e;
+        if ((e = launch_prep_s2d_planar(d, p, x, sh, sl, Kp, st))) return e;
         if (Kp > s * s * Ci) {
             zero_planar_kernel<<<152 * 16, 256, 0, st>>>(sh, sl, (long long)d->N * p.Ho, s * s * Ci, Kp, p.Wo);
             if ((e = launched())) return e;
@@ -1027,13 +1189,11 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     float* ah = (float*)q;
     q += al256(4 * wsz);
     float* al = (float*)q;
-    prep_nhwc_kernel<<<dim3(cdiv(d->W, 32), cdiv(Ci, 32), d->N * d->H), dim3(32, 8), 0, st>>>(x, xh, xl, Ci, d->H,
-                                                                                           d->W, Ci);
-    hc_status s = launched();
+    hc_status s = launch_prep_nhwc(x, xh, xl, d->N, Ci, d->H, d->W, Ci, st);
     if (s) return s;
     prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Co, Ci, 0);
     if ((s = launched())) return s;
-    const int BN = pick_bn(p.Wl);
+    const int BN = pick_bn(p.Wo);
     TcParams tp{};
     tp.mode = 0;
     tp.N = d->N;
@@ -1085,12 +1245,10 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     float* part = (float*)q;
     hc_status s;
     if (gx) {  // grad_input = conv of grad_output with the flipped, transposed kernel
-        prep_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(Co, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(gy, gh, gl, Co,
-                                                                                                p.Ho, p.Wo, Co);
-        if ((s = launched())) return s;
+        if ((s = launch_prep_nhwc(gy, gh, gl, d->N, Co, p.Ho, p.Wo, Co, st))) return s;
         prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Ci, Co, 1);
         if ((s = launched())) return s;
-        const int BN = pick_bn(p.Wl);
+        const int BN = pick_bn(p.Wo);
         TcParams tp{};
         tp.mode = 0;
         tp.N = d->N;
