@@ -574,12 +574,12 @@ __global__ void prep_split_rows_kernel(const float* __restrict__ x, float* __res
 // and the four shifted rows are written with 16-byte stores.
 __global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
                                   long long rows, int C, int H, int W, int Wc, int copies) {
-    extern __shared__ float rowbuf[];  // [W + 8]: 4 zeros, the row, 4 zeros
+    extern __shared__ float rowbuf[];  // [Wc + 4]: 4 zeros, the row, zeros
     const long long row = blockIdx.x;  // (n * C + c) * H + h
     const float* src = x + row * W;
     const long long nc = row / H;
     const long long orow = (nc / C * H + row % H) * C + nc % C;  // (n * H + h) * C + c
-    for (int i = threadIdx.x; i < W + 8; i += blockDim.x) {
+    for (int i = threadIdx.x; i < Wc + 4; i += blockDim.x) {
         const int c = i - 4;
         rowbuf[i] = (c >= 0 && c < W) ? __ldg(src + c) : 0.0f;
     }
@@ -1279,8 +1279,8 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         if ((s = launched())) return s;
         const long long rows = (long long)d->N * Ci * d->H;
         if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (d->W + 8), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
-                                                                                    Wc, copies);
+        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (Wc + 4), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
+                                                                                  Wc, copies);
         if ((s = launched())) return s;
         TcParams tp{};
         tp.mode = 1;

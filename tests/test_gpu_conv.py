@@ -91,6 +91,14 @@ CASES = {
     # strided k = stride convs through space-to-depth (stem- and downsample-like)
     "tc_stem4x4s4": lambda: tc_strided_case(2, 3, 12, 512, 128, 4, 1),
     "tc_down2x2s2_S2": lambda: tc_strided_case(1, 128, 6, 512, 256, 2, 2),
+    # s = 3 with a zero channel tail (Kp 640 > 576) and the scalar depth-to-space store
+    "tc_down3x3s3_C64_S2": lambda: tc_strided_case(1, 64, 6, 768, 128, 3, 2),
+    # C % 64 != 0: the generic space-to-depth prep; 256-wide tiles over 128-wide shards
+    "tc_down2x2s2_C96_S4": lambda: tc_strided_case(1, 96, 4, 1024, 128, 2, 4),
+    # 256-wide conv tiles across 128-wide shards, the halo read inside a tile
+    "tc_5x5_S4_tiles_cross_shards": lambda: tc_case(1, 128, 5, 512, 128, 5, 4),
+    # 2048 columns: the bias partials walk two 1024-column groups, 8 shards
+    "tc_3x3_wide_S8": lambda: tc_case(1, 128, 2, 2048, 128, 3, 8),
 }
 
 
@@ -131,7 +139,8 @@ def test_parity_depthwise_explicit(hc, orc, name):
 
 
 @pytest.mark.parametrize("name", ["tc_5x5_S2", "tc_3x3_two_mblocks", "tc_1x1", "tc_5x5_ragged_two_tiles",
-                                  "tc_stem4x4s4", "tc_down2x2s2_S2"])
+                                  "tc_stem4x4s4", "tc_down2x2s2_S2", "tc_down3x3s3_C64_S2", "tc_down2x2s2_C96_S4",
+                                  "tc_5x5_S4_tiles_cross_shards", "tc_3x3_wide_S8"])
 def test_parity_tensor_cores_explicit(hc, orc, name):
     cfg = CASES[name]()[0]
     assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, hc.HC_ALGO_TC_3XTF32)
