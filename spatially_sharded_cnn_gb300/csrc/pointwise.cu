@@ -12,7 +12,10 @@ namespace hc {
 namespace {
 
 constexpr int LN_PIX = 32;       // pixels per LayerNorm block
-constexpr int LN_THREADS = 256;  // 8 channel groups x 32 pixels
+constexpr int LN_PITCH = 33;     // shared-tile row pitch: rows (channels) and columns (pixels) both
+                                 // hit 32 distinct banks
+constexpr int LN_THREADS = 512;  // 16 channel groups x 32 pixels
+constexpr int LN_G = LN_THREADS / 32;
 
 // LayerNorm over C at every (n, pixel): mean, biased variance (two passes over
 // the staged tile), y = (x - mean) * rstd * gamma[c] + beta[c].
@@ -21,47 +24,47 @@ __global__ void __launch_bounds__(LN_THREADS) ln_fwd_kernel(const float* __restr
                                                             float* __restrict__ y, float* __restrict__ mean,
                                                             float* __restrict__ rstd, int C, long long HW,
                                                             long long blocks_per_image) {
-    extern __shared__ float tile[];  // [C][LN_PIX]
-    __shared__ float red[8][LN_PIX];
+    extern __shared__ float tile[];  // [C][LN_PITCH]
+    __shared__ float red[LN_G][LN_PIX];
     __shared__ float stat[2][LN_PIX];
     const long long b = blockIdx.x;
     const int n = (int)(b / blocks_per_image);
     const long long p0 = (b % blocks_per_image) * LN_PIX;
-    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;  // 8 groups of channels
+    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;  // LN_G groups of channels
     const long long p = p0 + px;
     const bool valid = p < HW;
     const float* xb = x + (long long)n * C * HW;
-    for (int c = g; c < C; c += 8) tile[c * LN_PIX + px] = valid ? __ldg(xb + (long long)c * HW + p) : 0.0f;
+    for (int c = g; c < C; c += LN_G) tile[c * LN_PITCH + px] = valid ? __ldg(xb + (long long)c * HW + p) : 0.0f;
     // mean
     float s = 0.0f;
-    for (int c = g; c < C; c += 8) s += tile[c * LN_PIX + px];
+    for (int c = g; c < C; c += LN_G) s += tile[c * LN_PITCH + px];
     red[g][px] = s;
     __syncthreads();
     if (g == 0) {
         float t = 0.0f;
-        for (int k = 0; k < 8; k++) t += red[k][px];
+        for (int k = 0; k < LN_G; k++) t += red[k][px];
         stat[0][px] = t / C;
     }
     __syncthreads();
     const float mu = stat[0][px];
     float v = 0.0f;
-    for (int c = g; c < C; c += 8) {
-        const float d = tile[c * LN_PIX + px] - mu;
+    for (int c = g; c < C; c += LN_G) {
+        const float d = tile[c * LN_PITCH + px] - mu;
         v = fmaf(d, d, v);
     }
     red[g][px] = v;
     __syncthreads();
     if (g == 0) {
         float t = 0.0f;
-        for (int k = 0; k < 8; k++) t += red[k][px];
+        for (int k = 0; k < LN_G; k++) t += red[k][px];
         stat[1][px] = rsqrtf(t / C + eps);
     }
     __syncthreads();
     const float rs = stat[1][px];
     if (valid) {
         float* yb = y + (long long)n * C * HW;
-        for (int c = g; c < C; c += 8)
-            yb[(long long)c * HW + p] = (tile[c * LN_PIX + px] - mu) * rs * __ldg(gamma + c) + __ldg(beta + c);
+        for (int c = g; c < C; c += LN_G)
+            yb[(long long)c * HW + p] = (tile[c * LN_PITCH + px] - mu) * rs * __ldg(gamma + c) + __ldg(beta + c);
         if (g == 0) {
             if (mean) mean[(long long)n * HW + p] = mu;
             if (rstd) rstd[(long long)n * HW + p] = rs;
@@ -78,10 +81,10 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
                                                             const float* __restrict__ gy, float* __restrict__ gx,
                                                             float* __restrict__ part, int C, long long HW,
                                                             long long blocks_per_image) {
-    extern __shared__ float sm[];  // xhat [C][LN_PIX], gy [C][LN_PIX]
+    extern __shared__ float sm[];  // xhat [C][LN_PITCH], gy [C][LN_PITCH]
     float* th = sm;
-    float* tg = sm + C * LN_PIX;
-    __shared__ float red[2][8][LN_PIX];
+    float* tg = sm + C * LN_PITCH;
+    __shared__ float red[2][LN_G][LN_PIX];
     __shared__ float stat[2][LN_PIX];
     const long long b = blockIdx.x;
     const int n = (int)(b / blocks_per_image);
@@ -94,11 +97,11 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
     const float* xb = x + (long long)n * C * HW;
     const float* gb = gy + (long long)n * C * HW;
     float s1 = 0.0f, s2 = 0.0f;
-    for (int c = g; c < C; c += 8) {
+    for (int c = g; c < C; c += LN_G) {
         const float xh = valid ? (__ldg(xb + (long long)c * HW + p) - mu) * rs : 0.0f;
         const float gv = valid ? __ldg(gb + (long long)c * HW + p) : 0.0f;
-        th[c * LN_PIX + px] = xh;
-        tg[c * LN_PIX + px] = gv;
+        th[c * LN_PITCH + px] = xh;
+        tg[c * LN_PITCH + px] = gv;
         const float gg = gv * __ldg(gamma + c);
         s1 += gg;
         s2 = fmaf(gg, xh, s2);
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
     __syncthreads();
     if (g == 0) {
         float a = 0.0f, c2 = 0.0f;
-        for (int k = 0; k < 8; k++) {
+        for (int k = 0; k < LN_G; k++) {
             a += red[0][k][px];
             c2 += red[1][k][px];
         }
@@ -119,9 +122,9 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
     const float mg = stat[0][px], mgx = stat[1][px];
     if (valid) {
         float* gxb = gx + (long long)n * C * HW;
-        for (int c = g; c < C; c += 8) {
-            const float xh = th[c * LN_PIX + px];
-            const float gg = tg[c * LN_PIX + px] * __ldg(gamma + c);
+        for (int c = g; c < C; c += LN_G) {
+            const float xh = th[c * LN_PITCH + px];
+            const float gg = tg[c * LN_PITCH + px] * __ldg(gamma + c);
             gxb[(long long)c * HW + p] = rs * (gg - mg - xh * mgx);
         }
     }
@@ -131,8 +134,8 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
         for (int c = threadIdx.x; c < C; c += LN_THREADS) {
             float a = 0.0f, bb = 0.0f;
             for (int k = 0; k < LN_PIX; k++) {
-                a = fmaf(tg[c * LN_PIX + k], th[c * LN_PIX + k], a);
-                bb += tg[c * LN_PIX + k];
+                a = fmaf(tg[c * LN_PITCH + k], th[c * LN_PITCH + k], a);
+                bb += tg[c * LN_PITCH + k];
             }
             pb[c] = a;
             pb[C + c] = bb;
@@ -266,7 +269,7 @@ hc_status hc_pointwise_workspace_size(int N, int C, long long HW, size_t* bytes)
 hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const float* gamma, const float* beta,
                              float eps, float* y, float* mean, float* rstd, void* stream) {
     if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !beta || !y || !(eps >= 0.0f)) return HC_ERR_INVALID_ARG;
-    const size_t smem = sizeof(float) * (size_t)C * LN_PIX;
+    const size_t smem = sizeof(float) * (size_t)C * LN_PITCH;
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
     static bool attr = false;
     if (!attr) {
@@ -287,7 +290,7 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     hc_pointwise_workspace_size(N, C, HW, &need);
     const bool want_p = ggamma || gbeta;
     if (want_p && (ws_bytes < need || !ws || !al16(ws))) return HC_ERR_WORKSPACE;
-    const size_t smem = sizeof(float) * (size_t)2 * C * LN_PIX;
+    const size_t smem = sizeof(float) * (size_t)2 * C * LN_PITCH;
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
     static bool attr = false;
     if (!attr) {

@@ -53,7 +53,8 @@ constexpr int BM = 128;             // accumulator rows (TMEM lanes)
 constexpr int BK = 32;              // tf32 per k-chunk = one 128-byte swizzle row
 constexpr int ROWB = BK * 4;        // bytes per tile row
 constexpr uint32_t SW_ATOM = 8 * ROWB;  // 8-row swizzle atom = stride between 8-row groups
-constexpr int TC_SMEM_RING = 196 * 1024;
+constexpr int TC_SMEM_RING = 192 * 1024;
+constexpr int TC_STAGE_OUT = 4096;  // per epilogue warp: a 32 x 32 fp32 output box, 128-byte swizzle
 constexpr long long kWait = 4000000000LL;  // clock cycles, about 2 s
 
 __device__ int g_tc_status;
@@ -115,6 +116,19 @@ __device__ __forceinline__ void tma_5d(void* dst, const CUtensorMap* m, int c0, 
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(su32(bar))
         : "memory");
 }
+// TMA store of a shared-memory box to global memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(su32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// the shared-memory source of every committed store has been read
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 __device__ __forceinline__ void tc_alloc(uint32_t* slot, unsigned cols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(slot)), "r"(cols)
@@ -180,6 +194,7 @@ struct TcParams {
     int stages;     // ring depth
     int chunks;     // k-chunks per unit (conv mode)
     int group;      // k-chunks accumulated in TMEM before the epilogue adds them up in fp32
+    int tma_store;  // conv mode without depth-to-space: store through ymap (TMA boxes)
     // conv mode
     int N, Ho, Wo, M, Kc, kh, kw, pad, tiles_w, mblocks;
     const float* bias;
@@ -243,9 +258,10 @@ template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap amap_hi, const __grid_constant__ CUtensorMap amap_lo,
                    const __grid_constant__ CUtensorMap bmap_hi, const __grid_constant__ CUtensorMap bmap_lo,
-                   TcParams p) {
+                   const __grid_constant__ CUtensorMap ymap, TcParams p) {
     extern __shared__ __align__(1024) unsigned char dsmem[];
     unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle atoms need 1 KB
+    unsigned char* stage_out = ring + TC_SMEM_RING;  // TC_EPI_WARPS output boxes, 1 KB aligned
     __shared__ Smem sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t a_bytes = BM * ROWB;           // 128 rows x BK tf32
@@ -432,6 +448,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < HC; k++) dst[(long long)k * sd + vv] = acc[k];
                 }
+            } else if (p.mode == 0 && p.tma_store) {
+                // 32 columns at a time: the warp's 32 rows x 32 columns go to its staging
+                // box (row = lane, 16-byte chunk j at j ^ (lane & 7): the 128-byte swizzle,
+                // conflict-free per 8 lanes), then one lane stores the box with TMA
+                const float bv = p.bias ? __ldg(p.bias + u.m0 + row) : 0.0f;
+                unsigned char* box = stage_out + ew * TC_STAGE_OUT;
+#pragma unroll
+                for (int k = 0; k < HC / 32; k++) {
+                    if (lane == 0) bulk_wait_read();  // the previous box has left shared memory
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const int c = 32 * k + 4 * j;
+                        *reinterpret_cast<float4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_float4(acc[c] + bv, acc[c + 1] + bv, acc[c + 2] + bv, acc[c + 3] + bv);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&ymap, box, u.w0 + half * HC + 32 * k, u.ho, u.n * p.M + u.m0 + 32 * q);
+                        bulk_commit();
+                    }
+                }
             } else if (p.mode == 0) {
                 const int m = u.m0 + row;
                 const float bv = p.bias ? __ldg(p.bias + m) : 0.0f;
@@ -455,6 +494,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         }
     }
+    if (warp >= 2 && lane == 0 && p.tma_store) bulk_wait_all();  // output boxes written out
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -546,25 +586,32 @@ __global__ void prep_weight_kernel(const float* __restrict__ w, float* __restric
 // tf32 hi / lo split of an NCHW tensor, stored row-interleaved as [N][H][C][W]:
 // the C rows of one image row sit together, so a TMA box of many channels x a
 // few pixels covers a few hundred KB instead of one page per channel plane.
-__global__ void prep_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                       int C, int H, int W, long long n4) {
-    const int W4 = W / 4;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {
-        const long long row = q / W4;  // (n * C + c) * H + h
-        const int h = (int)(row % H);
-        const long long nc = row / H;
-        const int c = (int)(nc % C);
-        const long long n = nc / C;
-        const long long o = ((n * H + h) * C + c) * W4 + (q - row * W4);
-        const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
+// Block (image row n*H + h, 16 channels): 16 input rows of W floats, read and
+// written as contiguous float4 runs.  Needs W % 4 == 0; 256 threads.
+__global__ void __launch_bounds__(256) prep_split_rows_kernel(const float* __restrict__ x, float* __restrict__ hi,
+                                                              float* __restrict__ lo, int C, int H, int W) {
+    const int nh = blockIdx.x, n = nh / H, h = nh - n * H;
+    const int c0 = blockIdx.y * 16, nc = C - c0 < 16 ? C - c0 : 16;
+    const int W4 = W / 4, items = nc * W4;
+    const float4* src = reinterpret_cast<const float4*>(x) + (((long long)n * C + c0) * H + h) * W4;
+    const long long o0 = ((long long)nh * C + c0) * W4;
+    const long long plane4 = (long long)H * W4;
+    for (int i = threadIdx.x; i < items; i += 256) {
+        const int cl = i / W4, j = i - cl * W4;
+        const float4 v = __ldg(src + cl * plane4 + j);
         float4 hv, l;
         hv.x = tf32_rna(v.x); l.x = tf32_rna(v.x - hv.x);
         hv.y = tf32_rna(v.y); l.y = tf32_rna(v.y - hv.y);
         hv.z = tf32_rna(v.z); l.z = tf32_rna(v.z - hv.z);
         hv.w = tf32_rna(v.w); l.w = tf32_rna(v.w - hv.w);
-        reinterpret_cast<float4*>(hi)[o] = hv;
-        reinterpret_cast<float4*>(lo)[o] = l;
+        reinterpret_cast<float4*>(hi)[o0 + i] = hv;
+        reinterpret_cast<float4*>(lo)[o0 + i] = l;
     }
+}
+hc_status launch_split_rows(const float* x, float* hi, float* lo, int N, int C, int H, int W, cudaStream_t st) {
+    if (W % 4 || (long long)N * H > 0x7fffffffLL || (C + 15) / 16 > 65535) return HC_ERR_UNSUPPORTED;
+    prep_split_rows_kernel<<<dim3((unsigned)(N * H), (C + 15) / 16), 256, 0, st>>>(x, hi, lo, C, H, W);
+    return launched();
 }
 
 // Column-shifted tf32 hi / lo copies of x for the weight gradient, row-interleaved:
@@ -693,6 +740,63 @@ __global__ void __launch_bounds__(256) prep_s2d_nhwc64_kernel(const float* __res
         __syncthreads();
     }
 }
+// The same for few input channels (s*s*C <= 512, C % 64 != 0; the stem's C = 3):
+// block (32 output columns, (n, ho)), 256 threads.  The C*S input rows of the
+// block's s x s windows (32*S floats each) are staged in shared memory as
+// float4s; then each warp writes whole output pixels, lane l the channel groups
+// 4l, 4l + 128, ... of Kp, zeros past s*s*C included (512 contiguous bytes per
+// 128 channels, hi and lo).
+template <int S>
+__global__ void __launch_bounds__(256) prep_s2d_nhwc_small_kernel(const float* __restrict__ x, float* __restrict__ hi,
+                                                                  float* __restrict__ lo, int C, int H, int W,
+                                                                  int Kp) {
+    extern __shared__ float t3[];  // [C][S][32*S]
+    constexpr int COLS = 32 * S;
+    const int Ho = H / S, Wo = W / S;
+    const int wo0 = blockIdx.x * 32;
+    const int n = blockIdx.y / Ho, ho = blockIdx.y % Ho;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = C * S * (COLS / 4);
+    for (int i = tid; i < q4; i += 256) {
+        const int r = i / (COLS / 4), q = i - r * (COLS / 4);  // r = c*S + u
+        const int c = r / S, u = r - c * S;
+        const int w = wo0 * S + 4 * q;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (w < W) v = __ldg(reinterpret_cast<const float4*>(x + (((long long)n * C + c) * H + ho * S + u) * W + w));
+        float* d = t3 + r * COLS + 4 * q;
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+    }
+    __syncthreads();
+    const int kreal = S * S * C;
+    for (int pl = warp; pl < 32; pl += 8) {
+        const int wo = wo0 + pl;
+        if (wo >= Wo) break;
+        const long long o = (((long long)n * Ho + ho) * Wo + wo) * Kp;
+        for (int k0 = 4 * lane; k0 < Kp; k0 += 128) {
+            float e[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int kk = k0 + j;
+                float val = 0.0f;
+                if (kk < kreal) {
+                    const int tap = kk / C, c = kk - tap * C, u = tap / S, v = tap - u * S;
+                    val = t3[(c * S + u) * COLS + pl * S + v];
+                }
+                e[j] = val;
+            }
+            float4 vh, vl;
+            vh.x = tf32_rna(e[0]); vl.x = tf32_rna(e[0] - vh.x);
+            vh.y = tf32_rna(e[1]); vl.y = tf32_rna(e[1] - vh.y);
+            vh.z = tf32_rna(e[2]); vl.z = tf32_rna(e[2] - vh.z);
+            vh.w = tf32_rna(e[3]); vl.w = tf32_rna(e[3] - vh.w);
+            *reinterpret_cast<float4*>(hi + o + k0) = vh;
+            *reinterpret_cast<float4*>(lo + o + k0) = vl;
+        }
+    }
+}
 // Zero the channel tail [k0, Kp) of every pixel of an NHWC hi / lo pair.
 __global__ void zero_tail_kernel(float* __restrict__ hi, float* __restrict__ lo, long long pixels, int k0, int Kp) {
     const int tail = Kp - k0;
@@ -744,19 +848,6 @@ __global__ void prep_s2d_planar_kernel(const float* __restrict__ x, float* __res
             *reinterpret_cast<float4*>(hi + o) = vh;
             *reinterpret_cast<float4*>(lo + o) = vl;
         }
-    }
-}
-// Zero the padding channels [k0, Kp) of a row-interleaved hi / lo pair ([NHo][Kp][Wo]).
-__global__ void zero_planar_kernel(float* __restrict__ hi, float* __restrict__ lo, long long NHo, int k0, int Kp,
-                                   int Wo) {
-    const long long per = (long long)(Kp - k0) * Wo;
-    const long long total = NHo * per;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
-         q += (long long)gridDim.x * blockDim.x) {
-        const long long r = q / per, e = q % per;
-        const long long o = (r * Kp + k0) * Wo + e;
-        hi[o] = 0.0f;
-        lo[o] = 0.0f;
     }
 }
 // Weights in space-to-depth order: forward A[co][k] = w[co][c][u][v] with
@@ -862,9 +953,9 @@ int pick_bn(int out_w) {
 
 template <int BN>
 hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi, const CUtensorMap& blo,
-                    TcParams p, cudaStream_t st) {
+                    const CUtensorMap& ymap, TcParams p, cudaStream_t st) {
     static bool attr = false;
-    const int smem = TC_SMEM_RING + 1024;
+    const int smem = TC_SMEM_RING + 1024 + TC_EPI_WARPS * TC_STAGE_OUT;
     if (!attr) {
         cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         attr = true;
@@ -873,15 +964,19 @@ hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtens
     p.stages = TC_SMEM_RING / stage_bytes;
     if (p.stages > 8) p.stages = 8;
     const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
-    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(ahi, alo, bhi, blo, p);
+    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(ahi, alo, bhi, blo, ymap, p);
     return launched();
 }
 
+// ymap: the conv-mode output as a TMA map (out_map); nullptr stores with plain
+// per-thread writes (depth-to-space and weight-gradient passes).
 hc_status launch_conv_pass(int BN, const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi,
-                           const CUtensorMap& blo, TcParams p, cudaStream_t st) {
+                           const CUtensorMap& blo, TcParams p, cudaStream_t st, const CUtensorMap* ymap = nullptr) {
+    p.tma_store = ymap != nullptr;
+    if (!ymap) ymap = &ahi;  // unused
     p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group
-    if (BN == 256) return launch_bn<256>(ahi, alo, bhi, blo, p, st);
-    if (BN == 128) return launch_bn<128>(ahi, alo, bhi, blo, p, st);
+    if (BN == 256) return launch_bn<256>(ahi, alo, bhi, blo, *ymap, p, st);
+    if (BN == 128) return launch_bn<128>(ahi, alo, bhi, blo, *ymap, p, st);
     return HC_ERR_UNSUPPORTED;
 }
 
@@ -898,6 +993,14 @@ hc_status weight_map(CUtensorMap* m, const float* base, int Mp, long long ktot) 
     const uint64_t strides[1] = {(uint64_t)ktot * 4};
     const uint32_t box[2] = {BK, 128};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// NCHW output of a conv pass as TMA store boxes: dims (Wo, Ho, N*M), box (32, 1, 32):
+// 32 output columns of one row for 32 channels.
+hc_status out_map(CUtensorMap* m, float* base, int N, int M, int Ho, int Wo) {
+    const uint64_t dims[3] = {(uint64_t)Wo, (uint64_t)Ho, (uint64_t)N * M};
+    const uint64_t strides[2] = {(uint64_t)Wo * 4, (uint64_t)Ho * Wo * 4};
+    const uint32_t box[3] = {32, 1, 32};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // Row-interleaved [N][H][C][W] map for K-major weight-gradient tiles (pixels
 // contiguous): dims (W, C, H, N), box (BK, rows, 1, 1): smem [rows channels][BK pixels].
@@ -933,6 +1036,8 @@ bool is_s2d(const hc_conv_desc* d) {
 int s2d_kp(const hc_conv_desc* d) { return (d->stride * d->stride * d->C_in + 127) / 128 * 128; }
 // Shifted copies the weight gradient reads: a 1-wide kernel never shifts.
 int shift_copies(const hc_conv_desc* d) { return d->kw == 1 ? 1 : 4; }
+// Row pitch of the shifted copies: a column shift of up to 3 needs 4 spare columns.
+int shift_pitch(const hc_conv_desc* d) { return d->kw == 1 ? d->W : d->W + 4; }
 
 }  // namespace
 
@@ -991,7 +1096,7 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     const size_t ng = (size_t)d->N * d->C_out * p.Ho * p.Wo;
     const size_t wsz = (size_t)d->C_out * KK * d->C_in;
     if (pass == 0) return 2 * al256(4 * nx) + 2 * al256(4 * wsz);
-    const size_t nsh = (size_t)shift_copies(d) * d->N * d->C_in * d->H * (d->W + 4);
+    const size_t nsh = (size_t)shift_copies(d) * d->N * d->C_in * d->H * shift_pitch(d);
     const int J = tc_wgrad_splits(d, p);
     const size_t part = al256(4 * (size_t)p.S * J * wsz);
     return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
@@ -1001,6 +1106,19 @@ static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, cons
                                       int Kp, cudaStream_t st) {
     const int s = d->stride, C = d->C_in;
     if ((long long)d->N * p.Ho > 65535) return HC_ERR_UNSUPPORTED;
+    const size_t small_smem = sizeof(float) * C * s * 32 * s;
+    if (C % 64 && s * s * C <= 512 && small_smem <= 48 * 1024 && d->W % 4 == 0) {  // writes the zero tail too
+        const dim3 grid(cdiv(p.Wo, 32), d->N * p.Ho);
+        if (s == 2)
+            prep_s2d_nhwc_small_kernel<2><<<grid, 256, small_smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else if (s == 3)
+            prep_s2d_nhwc_small_kernel<3><<<grid, 256, small_smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else if (s == 4)
+            prep_s2d_nhwc_small_kernel<4><<<grid, 256, small_smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
+        else
+            return HC_ERR_UNSUPPORTED;
+        return launched();
+    }
     if (C % 64 == 0 && d->W % 4 == 0) {
         const dim3 grid(cdiv(p.Wo, 32), C / 64, d->N * p.Ho);
         const size_t smem = sizeof(float) * 64 * (32 * s + 1);
@@ -1016,6 +1134,11 @@ static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, cons
         prep_s2d_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(C, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(x, hi, lo, C, d->H,
                                                                                                   d->W, s, Kp);
     }
+    hc_status e = launched();
+    if (e || Kp == s * s * C) return e;
+    // the channel tail is a K range of the forward GEMM: it must hold zeros
+    const long long pixels = (long long)d->N * p.Ho * p.Wo;
+    zero_tail_kernel<<<152 * 16, 256, 0, st>>>(hi, lo, pixels, s * s * C, Kp);
     return launched();
 }
 static hc_status launch_prep_s2d_planar(const hc_conv_desc* d, const Plan& p, const float* x, float* hi, float* lo,
@@ -1052,11 +1175,6 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     if (s > 4) return HC_ERR_UNSUPPORTED;
     hc_status e = launch_prep_s2d_nhwc(d, p, x, xh, xl, Kp, st);
     if (e) return e;
-    if (Kp > s * s * d->C_in) {
-        const long long pixels = (long long)d->N * p.Ho * p.Wo;
-        zero_tail_kernel<<<152 * 16, 256, 0, st>>>(xh, xl, pixels, s * s * d->C_in, Kp);
-        if ((e = launched())) return e;
-    }
     prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, d->C_in, s, Kp, 0);
     if ((e = launched())) return e;
     const int BN = pick_bn(p.Wo);
@@ -1076,11 +1194,12 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
     tp.bias = b;
     tp.out = y;
-    CUtensorMap mah, mal, mbh, mbl;
+    CUtensorMap mah, mal, mbh, mbl, my;
     if ((e = weight_map(&mah, ah, Co, Kp)) || (e = weight_map(&mal, al, Co, Kp)) ||
-        (e = act_map_conv(&mbh, xh, d->N, p.Ho, p.Wo, Kp, BN)) || (e = act_map_conv(&mbl, xl, d->N, p.Ho, p.Wo, Kp, BN)))
+        (e = act_map_conv(&mbh, xh, d->N, p.Ho, p.Wo, Kp, BN)) || (e = act_map_conv(&mbl, xl, d->N, p.Ho, p.Wo, Kp, BN)) ||
+        (e = out_map(&my, y, d->N, Co, p.Ho, p.Wo)))
         return e;
-    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st);
+    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my);
 }
 
 static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
@@ -1136,14 +1255,10 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         if ((e = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return e;
     }
     if (want_w) {  // G[co][(u,v,c)] = sum over a shard's pixels of gy[co][px] s2d[(u,v,c)][px]
-        prep_split_rows_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, Co, p.Ho, p.Wo,
-                                                                              (long long)ng / 4);
-        if ((e = launched())) return e;
+        if ((e = launch_split_rows(gy, gch, gcl, d->N, Co, p.Ho, p.Wo, st))) return e;
+        // channels k >= s*s*C of the planar copy are left unwritten: they are B rows,
+        // i.e. accumulator columns of their own, which the reduction never reads
         if ((e = launch_prep_s2d_planar(d, p, x, sh, sl, Kp, st))) return e;
-        if (Kp > s * s * Ci) {
-            zero_planar_kernel<<<152 * 16, 256, 0, st>>>(sh, sl, (long long)d->N * p.Ho, s * s * Ci, Kp, p.Wo);
-            if ((e = launched())) return e;
-        }
         TcParams tp{};
         tp.mode = 1;
         tp.Co = Co;
@@ -1210,12 +1325,12 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
     tp.bias = b;
     tp.out = y;
-    CUtensorMap mah, mal, mbh, mbl;
+    CUtensorMap mah, mal, mbh, mbl, my;
     if ((s = weight_map(&mah, ah, Co, (long long)KK * Ci)) || (s = weight_map(&mal, al, Co, (long long)KK * Ci)) ||
         (s = act_map_conv(&mbh, xh, d->N, d->H, d->W, Ci, BN)) ||
-        (s = act_map_conv(&mbl, xl, d->N, d->H, d->W, Ci, BN)))
+        (s = act_map_conv(&mbl, xl, d->N, d->H, d->W, Ci, BN)) || (s = out_map(&my, y, d->N, Co, p.Ho, p.Wo)))
         return s;
-    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st);
+    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my);
 }
 
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
@@ -1223,7 +1338,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     if (is_s2d(d)) return s2d_bwd(d, p, x, w, gy, gx, gwp, want_w, ws, st);
     const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
     const size_t ng = (size_t)d->N * Co * p.Ho * p.Wo, wsz = (size_t)Co * KK * Ci;
-    const int Wc = d->W + 4, copies = shift_copies(d);
+    const int Wc = shift_pitch(d), copies = shift_copies(d);
     const size_t nsh = (size_t)copies * d->N * Ci * d->H * Wc;
     char* q = (char*)ws;
     float* gh = (float*)q;
@@ -1265,23 +1380,25 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.units = tp.mblocks * d->N * d->H * tp.tiles_w;
         tp.bias = nullptr;
         tp.out = gx;
-        CUtensorMap mah, mal, mbh, mbl;
+        CUtensorMap mah, mal, mbh, mbl, my;
         if ((s = weight_map(&mah, ah, Ci, (long long)KK * Co)) ||
             (s = weight_map(&mal, al, Ci, (long long)KK * Co)) ||
             (s = act_map_conv(&mbh, gh, d->N, p.Ho, p.Wo, Co, BN)) ||
-            (s = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)))
+            (s = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)) || (s = out_map(&my, gx, d->N, Ci, d->H, d->W)))
             return s;
-        if ((s = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return s;
+        if ((s = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my))) return s;
     }
     if (want_w) {
-        prep_split_rows_kernel<<<cdiv((long long)ng / 4, 256), 256, 0, st>>>(gy, gch, gcl, Co, p.Ho, p.Wo,
-                                                                              (long long)ng / 4);
-        if ((s = launched())) return s;
+        if ((s = launch_split_rows(gy, gch, gcl, d->N, Co, p.Ho, p.Wo, st))) return s;
         const long long rows = (long long)d->N * Ci * d->H;
         if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (Wc + 4), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
-                                                                                  Wc, copies);
-        if ((s = launched())) return s;
+        if (copies == 1) {  // a 1-wide kernel never shifts: the plain row-interleaved hi / lo split
+            if ((s = launch_split_rows(x, sh, sl, d->N, Ci, d->H, d->W, st))) return s;
+        } else {
+            prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (Wc + 4), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
+                                                                                      Wc, copies);
+            if ((s = launched())) return s;
+        }
         TcParams tp{};
         tp.mode = 1;
         tp.Co = Co;
