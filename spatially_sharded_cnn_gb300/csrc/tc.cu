@@ -55,6 +55,11 @@ constexpr int ROWB = BK * 4;        // bytes per tile row
 constexpr uint32_t SW_ATOM = 8 * ROWB;  // 8-row swizzle atom = stride between 8-row groups
 constexpr int TC_SMEM_RING = 192 * 1024;
 constexpr int TC_STAGE_OUT = 4096;  // per epilogue warp: a 32 x 32 fp32 output box, 128-byte swizzle
+// weight-gradient tiles: 128 output channels x two slots of 128 input channels
+// (a slot is one tap x one 128-channel block)
+constexpr int WG_BN = 256;
+constexpr int WG_SLOT = 128;
+constexpr uint32_t WG_SLOT_BYTES = WG_SLOT * 128;  // one slot's hi (or lo) tile: 128 rows x 32 tf32
 constexpr long long kWait = 4000000000LL;  // clock cycles, about 2 s
 
 __device__ int g_tc_status;
@@ -94,18 +99,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, volatile
     }
     return true;
 }
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint64_t* bar) {
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::
             "r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(su32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-        "[%6];\n" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(su32(bar))
         : "memory");
 }
 __device__ __forceinline__ void tma_5d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, int c4,
@@ -256,8 +254,7 @@ constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 // row segment in conv mode, input channels in wgrad mode).
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_conv_kernel(const __grid_constant__ CUtensorMap amap_hi, const __grid_constant__ CUtensorMap amap_lo,
-                   const __grid_constant__ CUtensorMap bmap_hi, const __grid_constant__ CUtensorMap bmap_lo,
+    tc_conv_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap ymap, TcParams p) {
     extern __shared__ __align__(1024) unsigned char dsmem[];
     unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle atoms need 1 KB
@@ -305,11 +302,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int tap = (int)(c / cpt), cb = (int)(c % cpt);
                     const int uu = tap / p.kw, vv = tap % p.kw;
                     const int ka = tap * p.Kc + cb * BK;
-                    tma_2d(st, &amap_hi, ka, u.m0, &sh.full[s]);
-                    tma_2d(st + a_bytes, &amap_lo, ka, u.m0, &sh.full[s]);
+                    tma_3d(st, &amap, ka, u.m0, 0, &sh.full[s]);  // [hi][lo] x 128 rows
                     const int wx = u.w0 + vv - p.pad, hy = u.ho + uu - p.pad;
-                    tma_4d(st + 2 * a_bytes, &bmap_hi, cb * BK, wx, hy, u.n, &sh.full[s]);
-                    tma_4d(st + 2 * a_bytes + b_bytes, &bmap_lo, cb * BK, wx, hy, u.n, &sh.full[s]);
+                    tma_5d(st + 2 * a_bytes, &bmap, cb * BK, wx, hy, u.n, 0, &sh.full[s]);  // [hi][lo] x BN rows
                 } else {
                     // pixel chunk c of shard r: (n, BK-column piece, ho), rows fastest so the
                     // taps of one column strip reuse its rows while they are still in L2; the
@@ -319,18 +314,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const long long rest = c / p.Ho;
                     const int wc = (int)(rest % p.row_chunks), n = (int)(rest / p.row_chunks);
                     const int w = u.r * p.own_w + wc * BK;
-                    tma_4d(st, &amap_hi, w, u.m0, ho, n, &sh.full[s]);
-                    tma_4d(st + a_bytes, &amap_lo, w, u.m0, ho, n, &sh.full[s]);
-                    // B = two 128-row halves, one per slot (tap, 128-channel block)
+                    tma_5d(st, &amap, w, u.m0, ho, n, 0, &sh.full[s]);  // [hi][lo] x 128 rows
+                    // B = the hi rows of both slots, then their lo rows (one N = 256 operand
+                    // pair); a slot is (tap, 128-channel block); the copy index jc and the
+                    // image index share one box dimension (jc * N + n), hi / lo is the last
                     for (int h = 0; h < 2; h++) {
                         const int slot = 2 * u.tap + h;
                         if (slot >= p.slots) break;
                         const int tap = slot / p.nblocks, ci0 = (slot % p.nblocks) * 128;
                         const int uu = tap / p.kw, sft = tap % p.kw - p.pad;
                         const int jc = ((-sft) % 4 + 4) % 4;
-                        const uint32_t off = 2 * a_bytes + (uint32_t)h * (b_bytes / 2);
-                        tma_5d(st + off, &bmap_hi, w + sft + jc, ci0, ho + uu - p.pad, n, jc, &sh.full[s]);
-                        tma_5d(st + off + b_bytes, &bmap_lo, w + sft + jc, ci0, ho + uu - p.pad, n, jc, &sh.full[s]);
+                        unsigned char* dst = st + 2 * a_bytes + (uint32_t)h * WG_SLOT_BYTES;
+                        tma_5d(dst, &bmap, w + sft + jc, ci0, ho + uu - p.pad, jc * p.N + n, 0, &sh.full[s]);
+                        tma_5d(dst + b_bytes, &bmap, w + sft + jc, ci0, ho + uu - p.pad, jc * p.N + n, 1, &sh.full[s]);
                     }
                 }
             }
@@ -952,8 +948,8 @@ int pick_bn(int out_w) {
 }
 
 template <int BN>
-hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi, const CUtensorMap& blo,
-                    const CUtensorMap& ymap, TcParams p, cudaStream_t st) {
+hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap, TcParams p,
+                    cudaStream_t st) {
     static bool attr = false;
     const int smem = TC_SMEM_RING + 1024 + TC_EPI_WARPS * TC_STAGE_OUT;
     if (!attr) {
@@ -964,35 +960,48 @@ hc_status launch_bn(const CUtensorMap& ahi, const CUtensorMap& alo, const CUtens
     p.stages = TC_SMEM_RING / stage_bytes;
     if (p.stages > 8) p.stages = 8;
     const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
-    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(ahi, alo, bhi, blo, ymap, p);
+    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
     return launched();
 }
 
 // ymap: the conv-mode output as a TMA map (out_map); nullptr stores with plain
 // per-thread writes (depth-to-space and weight-gradient passes).
-hc_status launch_conv_pass(int BN, const CUtensorMap& ahi, const CUtensorMap& alo, const CUtensorMap& bhi,
-                           const CUtensorMap& blo, TcParams p, cudaStream_t st, const CUtensorMap* ymap = nullptr) {
+hc_status launch_conv_pass(int BN, const CUtensorMap& amap, const CUtensorMap& bmap, TcParams p, cudaStream_t st,
+                           const CUtensorMap* ymap = nullptr) {
     p.tma_store = ymap != nullptr;
-    if (!ymap) ymap = &ahi;  // unused
+    if (!ymap) ymap = &amap;  // unused
     p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group
-    if (BN == 256) return launch_bn<256>(ahi, alo, bhi, blo, *ymap, p, st);
-    if (BN == 128) return launch_bn<128>(ahi, alo, bhi, blo, *ymap, p, st);
+    if (BN == 256) return launch_bn<256>(amap, bmap, *ymap, p, st);
+    if (BN == 128) return launch_bn<128>(amap, bmap, *ymap, p, st);
     return HC_ERR_UNSUPPORTED;
 }
 
-// NHWC activation map for the conv pass: dims (Cp, W, H, N), box (BK, BN, 1, 1).
-hc_status act_map_conv(CUtensorMap* m, const float* base, int N, int H, int W, int Cp, int BN) {
-    const uint64_t dims[4] = {(uint64_t)Cp, (uint64_t)W, (uint64_t)H, (uint64_t)N};
-    const uint64_t strides[3] = {(uint64_t)Cp * 4, (uint64_t)W * Cp * 4, (uint64_t)H * W * Cp * 4};
-    const uint32_t box[4] = {BK, (uint32_t)BN, 1, 1};
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+// Every operand map covers a tf32 hi / lo pair (two equal arrays, lo - hi bytes
+// apart) as its outermost dimension, so one box brings [hi][lo]: few large boxes
+// keep the TMA unit's per-box cost low.
+static hc_status pair_stride(const float* hi, const float* lo, uint64_t* stride) {
+    const long long d = (const char*)lo - (const char*)hi;
+    if (d <= 0 || d % 16) return HC_ERR_INVALID_ARG;
+    *stride = (uint64_t)d;
+    return HC_OK;
 }
-// Weight map: dims (Ktot, Mp), box (BK, 128).
-hc_status weight_map(CUtensorMap* m, const float* base, int Mp, long long ktot) {
-    const uint64_t dims[2] = {(uint64_t)ktot, (uint64_t)Mp};
-    const uint64_t strides[1] = {(uint64_t)ktot * 4};
-    const uint32_t box[2] = {BK, 128};
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+// NHWC activation map for the conv pass: dims (Cp, W, H, N, 2), box (BK, BN, 1, 1, 2).
+hc_status act_map_conv(CUtensorMap* m, const float* hi, const float* lo, int N, int H, int W, int Cp, int BN) {
+    uint64_t ps;
+    if (hc_status e = pair_stride(hi, lo, &ps)) return e;
+    const uint64_t dims[5] = {(uint64_t)Cp, (uint64_t)W, (uint64_t)H, (uint64_t)N, 2};
+    const uint64_t strides[4] = {(uint64_t)Cp * 4, (uint64_t)W * Cp * 4, (uint64_t)H * W * Cp * 4, ps};
+    const uint32_t box[5] = {BK, (uint32_t)BN, 1, 1, 2};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, hi, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Weight map: dims (Ktot, Mp, 2), box (BK, 128, 2).
+hc_status weight_map(CUtensorMap* m, const float* hi, const float* lo, int Mp, long long ktot) {
+    uint64_t ps;
+    if (hc_status e = pair_stride(hi, lo, &ps)) return e;
+    const uint64_t dims[3] = {(uint64_t)ktot, (uint64_t)Mp, 2};
+    const uint64_t strides[2] = {(uint64_t)ktot * 4, ps};
+    const uint32_t box[3] = {BK, 128, 2};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, hi, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // NCHW output of a conv pass as TMA store boxes: dims (Wo, Ho, N*M), box (32, 1, 32):
 // 32 output columns of one row for 32 channels.
@@ -1003,29 +1012,31 @@ hc_status out_map(CUtensorMap* m, float* base, int N, int M, int Ho, int Wo) {
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // Row-interleaved [N][H][C][W] map for K-major weight-gradient tiles (pixels
-// contiguous): dims (W, C, H, N), box (BK, rows, 1, 1): smem [rows channels][BK pixels].
-hc_status rows_map(CUtensorMap* m, const float* base, int N, int C, int H, int W, int rows) {
-    const uint64_t dims[4] = {(uint64_t)W, (uint64_t)C, (uint64_t)H, (uint64_t)N};
-    const uint64_t strides[3] = {(uint64_t)W * 4, (uint64_t)C * W * 4, (uint64_t)H * C * W * 4};
-    const uint32_t box[4] = {BK, (uint32_t)rows, 1, 1};
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+// contiguous): dims (W, C, H, N, 2), box (BK, rows, 1, 1, 2): smem [hi][lo] x
+// [rows channels][BK pixels].
+hc_status rows_map(CUtensorMap* m, const float* hi, const float* lo, int N, int C, int H, int W, int rows) {
+    uint64_t ps;
+    if (hc_status e = pair_stride(hi, lo, &ps)) return e;
+    const uint64_t dims[5] = {(uint64_t)W, (uint64_t)C, (uint64_t)H, (uint64_t)N, 2};
+    const uint64_t strides[4] = {(uint64_t)W * 4, (uint64_t)C * W * 4, (uint64_t)H * C * W * 4, ps};
+    const uint32_t box[5] = {BK, (uint32_t)rows, 1, 1, 2};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, hi, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Row-interleaved column-shifted copies [copies][N][H][C][Wc]: dims (Wc, C, H, N,
-// copies), box (BK, rows, 1, 1, 1).
-hc_status shifted_map(CUtensorMap* m, const float* base, int N, int C, int H, int Wc, int rows, int copies = 4) {
-    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)C, (uint64_t)H, (uint64_t)N, (uint64_t)copies};
-    const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)C * Wc * 4, (uint64_t)H * C * Wc * 4,
-                                 (uint64_t)N * C * H * Wc * 4};
+// Row-interleaved column-shifted copies [copies][N][H][C][Wc]: dims (Wc, C, H,
+// copies * N, 2) (copy j of image n at j * N + n), box (BK, rows, 1, 1, 1): hi
+// (coordinate 0) and lo (1) are loaded apart, into the hi and lo halves of B.
+hc_status shifted_map(CUtensorMap* m, const float* hi, const float* lo, int N, int C, int H, int Wc, int rows,
+                      int copies) {
+    uint64_t ps;
+    if (hc_status e = pair_stride(hi, lo, &ps)) return e;
+    const uint64_t dims[5] = {(uint64_t)Wc, (uint64_t)C, (uint64_t)H, (uint64_t)copies * N, 2};
+    const uint64_t strides[4] = {(uint64_t)Wc * 4, (uint64_t)C * Wc * 4, (uint64_t)H * C * Wc * 4, ps};
     const uint32_t box[5] = {BK, (uint32_t)rows, 1, 1, 1};
-    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, hi, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// weight-gradient tiles: 128 output channels x two slots of 128 input channels
-// (a slot is one tap x one 128-channel block)
-constexpr int WG_BN = 256;
-constexpr int WG_SLOT = 128;
 
 
 // k = stride = s >= 2 without padding: every output pixel reads its own s x s
@@ -1194,12 +1205,11 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
     tp.bias = b;
     tp.out = y;
-    CUtensorMap mah, mal, mbh, mbl, my;
-    if ((e = weight_map(&mah, ah, Co, Kp)) || (e = weight_map(&mal, al, Co, Kp)) ||
-        (e = act_map_conv(&mbh, xh, d->N, p.Ho, p.Wo, Kp, BN)) || (e = act_map_conv(&mbl, xl, d->N, p.Ho, p.Wo, Kp, BN)) ||
+    CUtensorMap ma, mb, my;
+    if ((e = weight_map(&ma, ah, al, Co, Kp)) || (e = act_map_conv(&mb, xh, xl, d->N, p.Ho, p.Wo, Kp, BN)) ||
         (e = out_map(&my, y, d->N, Co, p.Ho, p.Wo)))
         return e;
-    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my);
+    return launch_conv_pass(BN, ma, mb, tp, st, &my);
 }
 
 static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
@@ -1247,12 +1257,10 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         tp.out = gx;
         tp.d2s = s;
         tp.d2s_c = Ci;
-        CUtensorMap mah, mal, mbh, mbl;
-        if ((e = weight_map(&mah, ah, Kp, Co)) || (e = weight_map(&mal, al, Kp, Co)) ||
-            (e = act_map_conv(&mbh, gh, d->N, p.Ho, p.Wo, Co, BN)) ||
-            (e = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)))
+        CUtensorMap ma, mb;
+        if ((e = weight_map(&ma, ah, al, Kp, Co)) || (e = act_map_conv(&mb, gh, gl, d->N, p.Ho, p.Wo, Co, BN)))
             return e;
-        if ((e = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st))) return e;
+        if ((e = launch_conv_pass(BN, ma, mb, tp, st))) return e;
     }
     if (want_w) {  // G[co][(u,v,c)] = sum over a shard's pixels of gy[co][px] s2d[(u,v,c)][px]
         if ((e = launch_split_rows(gy, gch, gcl, d->N, Co, p.Ho, p.Wo, st))) return e;
@@ -1278,12 +1286,12 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
         tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
         tp.part = part;
-        CUtensorMap mah, mal, mbh, mbl;
-        if ((e = rows_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (e = rows_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (e = shifted_map(&mbh, sh, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)) ||
-            (e = shifted_map(&mbl, sl, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)))
+        tp.N = d->N;
+        CUtensorMap ma, mb;
+        if ((e = rows_map(&ma, gch, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (e = shifted_map(&mb, sh, sl, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)))
             return e;
-        if ((e = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return e;
+        if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
         const long long total = (long long)p.S * Co * Ci * s * s;
         wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, Co, Ci, s, Kp);
         if ((e = launched())) return e;
@@ -1325,12 +1333,11 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     tp.units = tp.mblocks * d->N * p.Ho * tp.tiles_w;
     tp.bias = b;
     tp.out = y;
-    CUtensorMap mah, mal, mbh, mbl, my;
-    if ((s = weight_map(&mah, ah, Co, (long long)KK * Ci)) || (s = weight_map(&mal, al, Co, (long long)KK * Ci)) ||
-        (s = act_map_conv(&mbh, xh, d->N, d->H, d->W, Ci, BN)) ||
-        (s = act_map_conv(&mbl, xl, d->N, d->H, d->W, Ci, BN)) || (s = out_map(&my, y, d->N, Co, p.Ho, p.Wo)))
+    CUtensorMap ma, mb, my;
+    if ((s = weight_map(&ma, ah, al, Co, (long long)KK * Ci)) || (s = act_map_conv(&mb, xh, xl, d->N, d->H, d->W, Ci, BN)) ||
+        (s = out_map(&my, y, d->N, Co, p.Ho, p.Wo)))
         return s;
-    return launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my);
+    return launch_conv_pass(BN, ma, mb, tp, st, &my);
 }
 
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
@@ -1380,13 +1387,11 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.units = tp.mblocks * d->N * d->H * tp.tiles_w;
         tp.bias = nullptr;
         tp.out = gx;
-        CUtensorMap mah, mal, mbh, mbl, my;
-        if ((s = weight_map(&mah, ah, Ci, (long long)KK * Co)) ||
-            (s = weight_map(&mal, al, Ci, (long long)KK * Co)) ||
-            (s = act_map_conv(&mbh, gh, d->N, p.Ho, p.Wo, Co, BN)) ||
-            (s = act_map_conv(&mbl, gl, d->N, p.Ho, p.Wo, Co, BN)) || (s = out_map(&my, gx, d->N, Ci, d->H, d->W)))
+        CUtensorMap ma, mb, my;
+        if ((s = weight_map(&ma, ah, al, Ci, (long long)KK * Co)) ||
+            (s = act_map_conv(&mb, gh, gl, d->N, p.Ho, p.Wo, Co, BN)) || (s = out_map(&my, gx, d->N, Ci, d->H, d->W)))
             return s;
-        if ((s = launch_conv_pass(BN, mah, mal, mbh, mbl, tp, st, &my))) return s;
+        if ((s = launch_conv_pass(BN, ma, mb, tp, st, &my))) return s;
     }
     if (want_w) {
         if ((s = launch_split_rows(gy, gch, gcl, d->N, Co, p.Ho, p.Wo, st))) return s;
@@ -1418,12 +1423,12 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
         tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
         tp.part = part;
-        CUtensorMap mah, mal, mbh, mbl;
-        if ((s = rows_map(&mah, gch, d->N, Co, p.Ho, p.Wo, BM)) || (s = rows_map(&mal, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (s = shifted_map(&mbh, sh, d->N, Ci, d->H, Wc, WG_SLOT, copies)) ||
-            (s = shifted_map(&mbl, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
+        tp.N = d->N;
+        CUtensorMap ma, mb;
+        if ((s = rows_map(&ma, gch, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
+            (s = shifted_map(&mb, sh, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
             return s;
-        if ((s = launch_conv_pass(WG_BN, mah, mal, mbh, mbl, tp, st))) return s;
+        if ((s = launch_conv_pass(WG_BN, ma, mb, tp, st))) return s;
         const long long total = (long long)p.S * wsz;
         wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, KK, Co, Ci);
         if ((s = launched())) return s;
