@@ -81,6 +81,23 @@ def bwd(cfg, x, w, gy, algo=None, partials=True):
     return out
 
 
+def bwd_subset(cfg, x, w, gy, want, algo=None):
+    """Backward with only the outputs named in `want` (subset of gx, gw, gb,
+    gw_partials, gb_partials); the others are passed as NULL."""
+    d = hc.desc(cfg)
+    S = cfg["num_shards"]
+    wshape = (cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"])
+    shapes = dict(gx=x.shape, gw=wshape, gb=(cfg["C_out"],), gw_partials=(S,) + wshape,
+                  gb_partials=(S, cfg["C_out"]))
+    bufs = {k: Guarded(shapes[k]) for k in want}
+    ws, nb = workspace(d, 1, algo)
+    view = lambda k: bufs[k].view if k in bufs else None
+    hc.check(hc.hc_conv2d_bwd(d, dev(x), dev(w), dev(gy), view("gx"), view("gw"), view("gb"), view("gw_partials"),
+                              view("gb_partials"), ws, nb, algo=algo), "bwd subset")
+    hc.check(hc.hc_sync_check(), "bwd subset sync")
+    return {k: v.numpy() for k, v in bufs.items()}
+
+
 def normwise(got, ref):
     """max |got - ref| / max |ref| (normwise maximum relative error)."""
     ref = np.asarray(ref, np.float64)

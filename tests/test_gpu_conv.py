@@ -147,6 +147,24 @@ def test_parity_tensor_cores_explicit(hc, orc, name):
     check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_TC_3XTF32)
 
 
+@pytest.mark.parametrize("want", [("gx",), ("gw",), ("gb",), ("gw", "gb"), ("gw_partials", "gb_partials"),
+                                  ("gx", "gb_partials")])
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "tc_5x5_S2", "tc_down2x2s2_S2"])
+def test_backward_output_subsets(hc, orc, name, want):
+    """Outputs passed as NULL are skipped; the requested ones still match the oracle."""
+    cfg, x, w, b, gy = CASES[name]()
+    out = R.bwd_subset(cfg, x, w, gy, want)
+    refs = dict(gx=lambda: orc.conv2d_bwd_input(cfg, w, gy), gw=lambda: orc.conv2d_bwd_weight(cfg, x, gy),
+                gb=lambda: orc.conv2d_bwd_bias(cfg, gy))
+    if "gw_partials" in want or "gb_partials" in want:
+        _, gwp_ref, gbp_ref = orc.sharded_bwd(cfg, x, w, gy)
+        refs["gw_partials"] = lambda: gwp_ref
+        refs["gb_partials"] = lambda: gbp_ref
+    for k in want:
+        tol = TOL_FWD if k == "gx" else TOL_W
+        assert R.normwise(out[k], refs[k]()) <= tol, (k, R.normwise(out[k], refs[k]()))
+
+
 @pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2"])
 def test_deterministic(hc, name):
     cfg, x, w, b, gy = CASES[name]()
