@@ -133,7 +133,8 @@ class ConvWorkload:
         c = self.cfg
         return {"workload": self.desc, "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [c["kh"], c["kw"]],
                 "padding": c["padding"], "groups": c["groups"], "num_shards": c["num_shards"],
-                "l2": "inputs (470 MB each) larger than L2; no flush"}
+                "l2": "inputs (470 MB each) larger than L2; no flush" if self.name != "config1" else
+                      "inputs L2-resident (8 KB); launch-latency bound, no flush"}
 
     def setup(self, R):
         self.R = R
@@ -151,6 +152,15 @@ class ConvWorkload:
     def bwd(self):
         self.R.op("conv_bwd", lambda: self.R.conv_bwd(self.d, self.x, self.w, self.gy, self.gx, self.gw, self.gb))
 
+    def make_graph(self):
+        """Capture this workload's fwd + bwd step as one CUDA graph; returns (handle, kernels in it)."""
+        R = self.R
+        n0 = R.hc.hc_launch_count()
+        st, g = R.hc.hc_conv2d_step_graph_create(self.d, self.x, self.w, self.b, self.y, self.gy, self.gx, self.gw,
+                                                 self.gb, R.ws, R.ws_bytes, R.ws, R.ws_bytes)
+        R.hc.check(st, "graph create")
+        return g, R.hc.hc_launch_count() - n0
+
     def host_io(self):
         t = self.R.torch
         x, w, b, gy = self.host
@@ -161,6 +171,28 @@ class ConvWorkload:
         return self.flops / (ms * 1e-3) / 1e12 if self.dense else self.bytes / (ms * 1e-3) / 1e9
 
     def roofline(self, ops_ms, peaks, sms):
+        if self.name == "config1":  # a few kernels of microseconds: launch latency, not a unit, bounds it
+            alu = alu_peak(peaks, sms)
+            ms = sum(ops_ms.values())
+            a = self.flops / (ms * 1e-3) / 1e12
+            return {"bound": "alu", "kernel": "direct conv kernels (launch-latency bound)", "achieved": a, "peak": alu,
+                    "unit": "TFLOP/s", "frac": a / alu, "traffic": None,
+                    "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                    "ms_per_launch": ms}
+        if "conv_fwd" not in ops_ms:  # graph replay: one timed op, the whole step
+            ms = ops_ms["step_graph"]
+            if self.dense:
+                peak, a = tc_peak(peaks), self.flops / (ms * 1e-3) / 1e12
+                return {"bound": "tensor", "kernel": "whole fwd+bwd step (graph replay)", "achieved": a, "peak": peak,
+                        "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak, "traffic": None,
+                        "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3",
+                        "ms_per_launch": ms}
+            alu = alu_peak(peaks, sms)
+            a = 3 * conv_flops(self.cfg) / (ms * 1e-3) / 1e12
+            return {"bound": "alu", "kernel": "whole fwd+bwd step (graph replay)", "achieved": a, "peak": alu,
+                    "unit": "TFLOP/s", "frac": a / alu, "traffic": None,
+                    "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                    "ms_per_launch": ms}
         if self.dense:
             peak = tc_peak(peaks)
             a = conv_flops(self.cfg) / (ops_ms["conv_fwd"] * 1e-3) / 1e12
@@ -190,6 +222,16 @@ def gen_dw7(N=7, seed=0):
     w = synth.trunc_normal((256, 1, 7, 7), 0.02, seed, 2)
     b = np.zeros((256,), np.float32)
     gy = synth.normal((N, 256, 128, 512), 1.0, seed, 4)
+    return x, w, b, gy
+
+
+def gen_config1(seed=0):
+    """The small dense case: x U[-1,1], w N(0,0.1), b N(0,0.1), gy N(0,1)."""
+    from spatially_sharded_cnn_gb300 import synth
+    x = synth.uniform((1, 4, 16, 32), -1.0, 1.0, seed, 1)
+    w = synth.normal((4, 4, 5, 5), 0.1, seed, 2)
+    b = synth.normal((4,), 0.1, seed, 3)
+    gy = synth.normal((1, 4, 16, 32), 1.0, seed, 4)
     return x, w, b, gy
 
 
@@ -375,6 +417,9 @@ def make_workload(name, batch=None):
         return ConvWorkload("dense5x5", conv_cfg(N, 128, 128, 1024, 128, 5, 1, 2, 1, 4), lambda: gen_dense5x5(N),
                             "TFLOP/s", f"dense 5x5 conv 128->128 fwd+bwd, x ({N},128,128,1024) fp32 (3xTF32 tensor "
                             "cores), 4 W-shards of width 256")
+    if name == "config1":
+        return ConvWorkload("config1", conv_cfg(1, 4, 16, 32, 4, 5, 1, 2, 1, 4), gen_config1, "TFLOP/s",
+                            "dense 5x5 conv 4->4 fwd+bwd, x (1,4,16,32) fp32, 4 W-shards of width 8")
     if name == "block":
         return BlockWorkload()
     if name == "dwdown":
@@ -382,7 +427,7 @@ def make_workload(name, batch=None):
     raise ValueError(name)
 
 
-WORKLOADS = ["dw7", "dense5x5", "block", "dwdown"]
+WORKLOADS = ["dw7", "dense5x5", "block", "dwdown", "config1"]
 
 
 # ---------------------------------------------------------------------------
@@ -508,6 +553,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each fwd+bwd step from one captured CUDA graph (single-conv workloads)")
     ap.add_argument("--batch", type=int, default=None, help="batch size of the dw7 / dense5x5 workloads (default 7)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -535,7 +582,16 @@ def main():
     R = Runner(hc, torch, dev, stream)
     wl.setup(R)
 
+    graph, graph_kernels = None, 0
+    if args.graph:
+        if not hasattr(wl, "make_graph"):
+            raise SystemExit("--graph applies to the single-conv workloads")
+        graph, graph_kernels = wl.make_graph()
+
     def step():
+        if graph is not None:
+            R.op("step_graph", lambda: hc.check(hc.hc_step_graph_launch(graph, stream), "graph launch"))
+            return
         wl.fwd()
         wl.bwd()
 
@@ -563,7 +619,7 @@ def main():
     end.record(stream)
     barrier()
     R.mark = None
-    launches = hc.hc_launch_count() - n0
+    launches = hc.hc_launch_count() - n0 + K * graph_kernels  # a replay runs the captured kernels
     clk = clocks.stop()
     hc.check(hc.hc_sync_check(stream), "timed region")
     elapsed_ms = start.elapsed_time(end)
@@ -613,6 +669,8 @@ def main():
                 "e2e": {"value": world * wl.value(e2e_ms), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
+        if graph is not None:
+            line["config"]["cuda_graph"] = f"each step one graph replay of {graph_kernels} kernels"
         if world == 1 and not args.no_cpu_baseline and args.workload == "dw7" and not args.batch:
             v, cores, sample, _ = oracle_depthwise_sample(256)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}

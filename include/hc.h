@@ -203,6 +203,27 @@ hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* br
                                      const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
                                      void* stream);
 
+/* One training step of a convolution -- hc_conv2d_fwd then hc_conv2d_bwd with
+ * the automatic algorithm, every argument as in those calls -- captured into a
+ * CUDA graph that replays with one launch (LibreYOLO documentation, page "Grafy
+ * CUDA": a graph records a fixed kernel sequence and the addresses it uses;
+ * replay must match eager execution bit for bit, which it does here since every
+ * kernel is deterministic).  For small problems the step costs its launch
+ * latency; the graph removes most of it.  The graph is bound to the pointers
+ * given here: replays read the inputs' current contents and overwrite the
+ * outputs.  gx, gw, gb may be NULL as in hc_conv2d_bwd (no partial outputs).
+ * Capture runs on a private stream and launches nothing.  *out receives a handle
+ * owned by the caller (hc_step_graph_destroy); on any error *out is NULL and the
+ * status is the failing call's. */
+typedef struct hc_step_graph_s* hc_step_graph;
+hc_status hc_conv2d_step_graph_create(const hc_conv_desc* d, const float* x, const float* w, const float* bias,
+                                      float* y, const float* gy, float* gx, float* gw, float* gb, void* ws_fwd,
+                                      size_t ws_fwd_bytes, void* ws_bwd, size_t ws_bwd_bytes, hc_step_graph* out);
+/* Replays the step on `stream` (asynchronous; HC_ERR_CUDA if the launch fails). */
+hc_status hc_step_graph_launch(hc_step_graph g, void* stream);
+/* Releases the graph (NULL is a no-op). */
+hc_status hc_step_graph_destroy(hc_step_graph g);
+
 /* Synchronises `stream`, then returns (and clears) the first error a kernel
  * recorded in the device status word, HC_ERR_CUDA for an asynchronous CUDA
  * error, or HC_OK. */

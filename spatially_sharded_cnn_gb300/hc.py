@@ -87,6 +87,13 @@ _lib.hc_layerscale_residual_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, 
 for _n in ("hc_add_inplace", "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
            "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd"):
     getattr(_lib, _n).restype = C.c_int
+_lib.hc_conv2d_step_graph_create.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t,
+                                             C.POINTER(C.c_void_p)]
+_lib.hc_conv2d_step_graph_create.restype = C.c_int
+_lib.hc_step_graph_launch.argtypes = [C.c_void_p, _P]
+_lib.hc_step_graph_launch.restype = C.c_int
+_lib.hc_step_graph_destroy.argtypes = [C.c_void_p]
+_lib.hc_step_graph_destroy.restype = C.c_int
 _lib.hc_sync_check.argtypes = [_P]
 _lib.hc_selftest_timeout.argtypes = [C.c_int, _P]
 _lib.hc_selftest_timeout.restype = C.c_int
@@ -104,6 +111,7 @@ EXPORTS = [
     "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
+    "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy",
 ]
 
 
@@ -159,6 +167,23 @@ def hc_conv2d_bwd_depthwise_noalloc(d, x, w, gy, gx, gw, gb, gw_partials=None, g
     """Depthwise backward with library-owned scratch: no workspace argument."""
     return _lib.hc_conv2d_bwd_depthwise_noalloc(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw),
                                                 _ptr(gb), _ptr(gw_partials), _ptr(gb_partials), _stream(stream))
+
+
+def hc_conv2d_step_graph_create(d, x, w, bias, y, gy, gx, gw, gb, ws_fwd, ws_fwd_bytes, ws_bwd, ws_bwd_bytes):
+    """Returns (status, handle): one fwd + bwd step captured as a CUDA graph."""
+    h = C.c_void_p(None)
+    st = _lib.hc_conv2d_step_graph_create(C.byref(d), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), _ptr(gy), _ptr(gx),
+                                          _ptr(gw), _ptr(gb), _ptr(ws_fwd), int(ws_fwd_bytes), _ptr(ws_bwd),
+                                          int(ws_bwd_bytes), C.byref(h))
+    return st, h
+
+
+def hc_step_graph_launch(h, stream=None) -> int:
+    return _lib.hc_step_graph_launch(h, _stream(stream))
+
+
+def hc_step_graph_destroy(h) -> int:
+    return _lib.hc_step_graph_destroy(h)
 
 
 def hc_halo_gather(d, x, x_ext, stream=None) -> int:
