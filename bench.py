@@ -249,9 +249,10 @@ class BlockWorkload:
 
     unit = "TFLOP/s"
 
-    def __init__(self):
+    def __init__(self, drop_path=0.0):
         N, S = 7, 8
         self.N, self.S = N, S
+        self.drop_path, self.steps_drawn = float(drop_path), 0
         self.stem = conv_cfg(N, 3, 512, 4096, 256, 4, 4, 0, 1, S)
         self.dw = conv_cfg(N, 256, 128, 1024, 256, 7, 1, 3, 256, S)
         self.pw1 = conv_cfg(N, 256, 128, 1024, 1024, 1, 1, 0, 1, S)
@@ -265,7 +266,8 @@ class BlockWorkload:
     def describe(self):
         return {"workload": "ConvNeXt-XL stage-1 block fwd+bwd on the stem output of a (7,3,512,4096) U[0,1] image: "
                             "4x4/s4 stem 3->256, depthwise 7x7, LayerNorm(C), 1x1 256->1024, GELU, 1x1 1024->256, "
-                            "layer scale 1e-6 + residual; fp32; 8 W-shards",
+                            "layer scale 1e-6 + residual" + (f", DropPath {self.drop_path}" if self.drop_path else "") +
+                            "; fp32; 8 W-shards",
                 "shape": [7, 3, 512, 4096], "num_shards": 8, "l2": "activations (0.9-3.8 GB) larger than L2; no flush"}
 
     def setup(self, R):
@@ -283,6 +285,7 @@ class BlockWorkload:
         self.b256, self.b1024 = t.zeros(256, device=R.dev), t.zeros(1024, device=R.dev)
         self.ln_g, self.ln_b = t.ones(256, device=R.dev), t.zeros(256, device=R.dev)
         self.ls_g = t.full((256,), 1e-6, device=R.dev)
+        self.mask = t.empty(N, device=R.dev) if self.drop_path else None
         a256, a1024 = (N, 256, 128, 1024), (N, 1024, 128, 1024)
         self.s, self.dwo, self.ln, self.b2, self.out = (R.empty(a256) for _ in range(5))
         self.mean, self.rstd = R.empty((N, HW)), R.empty((N, HW))
@@ -308,13 +311,17 @@ class BlockWorkload:
         R.op("pw1_fwd", lambda: R.conv_fwd(self.d["pw1"], self.ln, self.w1, self.b1024, self.h))
         R.op("gelu_fwd", lambda: hc.check(hc.hc_gelu_fwd(N * 1024 * HW, self.h, self.a, R.stream)))
         R.op("pw2_fwd", lambda: R.conv_fwd(self.d["pw2"], self.a, self.w2, self.b256, self.b2))
-        R.op("ls_fwd", lambda: hc.check(hc.hc_layerscale_residual_fwd(N, 256, HW, self.s, self.b2, self.ls_g, self.out,
-                                                                      R.stream)))
+        if self.drop_path:  # a fresh per-sample draw each step: offset = samples drawn so far
+            R.op("drop_path_mask", lambda: hc.check(hc.hc_drop_path_mask(N, self.drop_path, 2024, self.steps_drawn * N,
+                                                                         self.mask, R.stream)))
+            self.steps_drawn += 1
+        R.op("ls_fwd", lambda: hc.check(hc.hc_layerscale_droppath_fwd(N, 256, HW, self.s, self.b2, self.ls_g, self.mask,
+                                                                      self.out, R.stream)))
 
     def bwd(self):
         R, hc, N, HW = self.R, self.R.hc, self.N, self.HW
-        R.op("ls_bwd", lambda: hc.check(hc.hc_layerscale_residual_bwd(N, 256, HW, self.b2, self.ls_g, self.gy,
-                                                                      self.g_b2, self.g_ls, R.ws, R.ws_bytes,
+        R.op("ls_bwd", lambda: hc.check(hc.hc_layerscale_droppath_bwd(N, 256, HW, self.b2, self.ls_g, self.mask,
+                                                                      self.gy, self.g_b2, self.g_ls, R.ws, R.ws_bytes,
                                                                       R.stream)))
         R.op("pw2_bwd", lambda: R.conv_bwd(self.d["pw2"], self.a, self.w2, self.g_b2, self.g_a, self.gw2, self.gb2))
         R.op("gelu_bwd", lambda: hc.check(hc.hc_gelu_bwd(N * 1024 * HW, self.h, self.g_a, self.g_a, R.stream)))
@@ -339,7 +346,7 @@ class BlockWorkload:
     def roofline(self, ops_ms, peaks, sms):
         peak = tc_peak(peaks)
         a = conv_flops(self.pw1) / (ops_ms["pw1_fwd"] * 1e-3) / 1e12
-        return {"bound": "tensor", "kernel": "tc_conv_kernel<128> (1x1 256->1024 forward call incl. operand prep)",
+        return {"bound": "tensor", "kernel": "tc_conv_kernel<256> (1x1 256->1024 forward call incl. operand prep)",
                 "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
                 "traffic": None,
                 "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
@@ -407,7 +414,7 @@ class DwDownWorkload:
                 "ms_per_launch": ops_ms["dw_bwd"]}
 
 
-def make_workload(name, batch=None):
+def make_workload(name, batch=None, drop_path=0.0):
     """batch overrides N of the single-conv workloads (smaller cases for profiling)."""
     N = batch or 7
     if name == "dw7":
@@ -421,7 +428,7 @@ def make_workload(name, batch=None):
         return ConvWorkload("config1", conv_cfg(1, 4, 16, 32, 4, 5, 1, 2, 1, 4), gen_config1, "TFLOP/s",
                             "dense 5x5 conv 4->4 fwd+bwd, x (1,4,16,32) fp32, 4 W-shards of width 8")
     if name == "block":
-        return BlockWorkload()
+        return BlockWorkload(drop_path)
     if name == "dwdown":
         return DwDownWorkload()
     raise ValueError(name)
@@ -553,6 +560,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
+    ap.add_argument("--drop-path", type=float, default=0.0,
+                    help="block workload: DropPath probability (per-sample, shard-consistent draw each step)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each fwd+bwd step from one captured CUDA graph (single-conv workloads)")
     ap.add_argument("--batch", type=int, default=None, help="batch size of the dw7 / dense5x5 workloads (default 7)")
@@ -560,7 +569,7 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
-    wl = make_workload(args.workload, args.batch)
+    wl = make_workload(args.workload, args.batch, args.drop_path)
 
     import torch
     import torch.distributed as dist

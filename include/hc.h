@@ -203,6 +203,28 @@ hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* br
                                      const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
                                      void* stream);
 
+/* DropPath (stochastic depth) keep mask with a shard-consistent draw (NVIDIA
+ * blog design section: ConvNeXt-XL's DropPath Bernoulli draw must agree across
+ * devices; kwkr.cn 3.1 and 6.1: a distributed DropPath layer keeps the RNG
+ * consistent, every DropPath layer uses the same seed).
+ *   mask[n] = 1 / (1 - drop_prob) if sample n keeps its branch, else 0,
+ * for n in [0, N).  The draw for sample n is output number offset + n of a
+ * SplitMix64 generator seeded with `seed` (Steele, Lea, Flood 2014), kept iff
+ * its top 24 bits are >= floor(drop_prob * 2^24): it depends on (seed, offset,
+ * n) only, so any shard or device holding sample n -- or a slice of the batch
+ * called with offset + its first sample -- draws the same value.
+ *   mask  out [N] device fp32.  drop_prob in [0, 1), else HC_ERR_INVALID_ARG. */
+hc_status hc_drop_path_mask(int N, float drop_prob, unsigned long long seed, unsigned long long offset, float* mask,
+                            void* stream);
+/* hc_layerscale_residual_fwd / _bwd with a per-sample DropPath mask (from
+ * hc_drop_path_mask; NULL = keep all): out = res + mask[n] * gamma[c] * branch;
+ * backward gbranch = mask[n] * gamma[c] * gy, ggamma[c] = sum mask[n] * branch * gy. */
+hc_status hc_layerscale_droppath_fwd(int N, int C, long long HW, const float* res, const float* branch,
+                                     const float* gamma, const float* mask, float* out, void* stream);
+hc_status hc_layerscale_droppath_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
+                                     const float* mask, const float* gy, float* gbranch, float* ggamma, void* ws,
+                                     size_t ws_bytes, void* stream);
+
 /* One training step of a convolution -- hc_conv2d_fwd then hc_conv2d_bwd with
  * the automatic algorithm, every argument as in those calls -- captured into a
  * CUDA graph that replays with one launch (LibreYOLO documentation, page "Grafy

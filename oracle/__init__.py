@@ -107,9 +107,16 @@ class Oracle:
         L.or_gelu_bwd.argtypes = [I64, _D, _D, _D]
         L.or_layerscale_residual_fwd.argtypes = [C.c_int, C.c_int, I64, _D, _D, _D, _D]
         L.or_layerscale_residual_bwd.argtypes = [C.c_int, C.c_int, I64, _D, _D, _D, _D, _D, _D]
+        L.or_layerscale_droppath_fwd.argtypes = [C.c_int, C.c_int, I64, _D, _D, _D, _D, _D]
+        L.or_layerscale_droppath_bwd.argtypes = [C.c_int, C.c_int, I64, _D, _D, _D, _D, _D, _D, _D]
         for n in ("or_layernorm_c_fwd", "or_layernorm_c_bwd", "or_gelu_fwd", "or_gelu_bwd",
-                  "or_layerscale_residual_fwd", "or_layerscale_residual_bwd"):
+                  "or_layerscale_residual_fwd", "or_layerscale_residual_bwd", "or_layerscale_droppath_fwd",
+                  "or_layerscale_droppath_bwd"):
             getattr(L, n).restype = None
+        L.or_splitmix64.argtypes = [C.c_uint64, C.c_uint64]
+        L.or_splitmix64.restype = C.c_uint64
+        L.or_drop_path_mask.argtypes = [C.c_int, C.c_float, C.c_uint64, C.c_uint64, _F]
+        L.or_drop_path_mask.restype = C.c_int
 
     # -- sizes -------------------------------------------------------------
     def num_threads(self) -> int:
@@ -257,6 +264,38 @@ class Oracle:
         gg = np.empty(Cc)
         self.lib.or_layerscale_residual_bwd(N, Cc, HW, _d(branch), _d(np.ascontiguousarray(gamma, np.float64)),
                                             _d(gy), _d(gres), _d(gbr), _d(gg))
+        return gres, gbr, gg
+
+
+    # -- DropPath ------------------------------------------------------------
+    def splitmix64(self, seed, i) -> int:
+        return int(self.lib.or_splitmix64(seed, i))
+
+    def drop_path_mask(self, N, p, seed, offset=0):
+        mask = np.empty(N, np.float32)
+        if self.lib.or_drop_path_mask(N, float(p), seed, offset, _f(mask)):
+            raise ValueError("drop probability must be in [0, 1)")
+        return mask
+
+    def layerscale_droppath_fwd(self, res, branch, gamma, mask):
+        res = np.ascontiguousarray(res, np.float64)
+        branch = np.ascontiguousarray(branch, np.float64)
+        N, Cc = res.shape[:2]
+        HW = int(np.prod(res.shape[2:]))
+        out = np.empty_like(res)
+        self.lib.or_layerscale_droppath_fwd(N, Cc, HW, _d(res), _d(branch), _d(np.ascontiguousarray(gamma, np.float64)),
+                                            _d(np.ascontiguousarray(mask, np.float64)), _d(out))
+        return out
+
+    def layerscale_droppath_bwd(self, branch, gamma, mask, gy):
+        branch = np.ascontiguousarray(branch, np.float64)
+        gy = np.ascontiguousarray(gy, np.float64)
+        N, Cc = branch.shape[:2]
+        HW = int(np.prod(branch.shape[2:]))
+        gres, gbr, gg = np.empty_like(gy), np.empty_like(gy), np.empty(Cc)
+        self.lib.or_layerscale_droppath_bwd(N, Cc, HW, _d(branch), _d(np.ascontiguousarray(gamma, np.float64)),
+                                            _d(np.ascontiguousarray(mask, np.float64)), _d(gy), _d(gres), _d(gbr),
+                                            _d(gg))
         return gres, gbr, gg
 
 

@@ -559,3 +559,63 @@ void or_layerscale_residual_bwd(int N, int C, int64_t HW, const double* branch, 
                 ggamma[c] += branch[o] * gy[o];
             }
 }
+
+/* DropPath (stochastic depth) with a shard-consistent draw.  [NV] design
+ * section: ConvNeXt-XL's DropPath draws a per-sample Bernoulli (aten.bernoulli)
+ * that every device must reproduce; [KW] section 3.1 (a distributed DropPath
+ * layer keeps the RNG consistent) and section 6.1 (every DropPath layer on every
+ * device uses the same seed).
+ * Reading: sample n keeps its residual branch with probability 1 - p, a kept
+ * branch is scaled by 1 / (1 - p) (stochastic-depth scaling), and the draw for
+ * sample n is output number offset + n of a SplitMix64 generator seeded with
+ * `seed`: it depends on (seed, offset, n) only, so any device holding sample n
+ * draws the same value.  Keep iff the top 24 bits u of that output satisfy
+ * u >= floor(p * 2^24) (an integer decision, the same on every side).
+ * SplitMix64: G. L. Steele, D. Lea, C. H. Flood, "Fast splittable pseudorandom
+ * number generators", OOPSLA 2014, with the finaliser of S. Vigna's
+ * public-domain splitmix64.c: output i of the generator seeded with s mixes
+ * s + (i + 1) * 0x9E3779B97F4A7C15. */
+uint64_t or_splitmix64(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+int or_drop_path_mask(int N, float p, uint64_t seed, uint64_t offset, float* mask) {
+    if (N < 0 || !(p >= 0.0f) || !(p < 1.0f)) return 1;
+    const uint32_t t = (uint32_t)floor((double)p * 16777216.0);
+    const float scale = 1.0f / (1.0f - p);
+    for (int n = 0; n < N; n++) {
+        const uint32_t u = (uint32_t)(or_splitmix64(seed, offset + (uint64_t)n) >> 40);
+        mask[n] = u >= t ? scale : 0.0f;
+    }
+    return 0;
+}
+
+/* Layer scale, DropPath and residual: out = res + mask[n] * gamma[c] * branch. */
+void or_layerscale_droppath_fwd(int N, int C, int64_t HW, const double* res, const double* branch,
+                                const double* gamma, const double* mask, double* out) {
+    for (int n = 0; n < N; n++)
+        for (int c = 0; c < C; c++)
+            for (int64_t q = 0; q < HW; q++) {
+                const int64_t o = ((int64_t)n * C + c) * HW + q;
+                out[o] = res[o] + mask[n] * gamma[c] * branch[o];
+            }
+}
+
+/* Backward: gres = gy, gbranch = mask[n] * gamma[c] * gy,
+ * ggamma[c] = sum over (n, q) of mask[n] * branch * gy. */
+void or_layerscale_droppath_bwd(int N, int C, int64_t HW, const double* branch, const double* gamma,
+                                const double* mask, const double* gy, double* gres, double* gbranch,
+                                double* ggamma) {
+    for (int c = 0; c < C; c++) ggamma[c] = 0.0;
+    for (int n = 0; n < N; n++)
+        for (int c = 0; c < C; c++)
+            for (int64_t q = 0; q < HW; q++) {
+                const int64_t o = ((int64_t)n * C + c) * HW + q;
+                if (gres) gres[o] = gy[o];
+                gbranch[o] = mask[n] * gamma[c] * gy[o];
+                ggamma[c] += mask[n] * branch[o] * gy[o];
+            }
+}

@@ -176,25 +176,51 @@ __global__ void gelu_bwd_kernel(const float* __restrict__ x, const float* __rest
 }
 
 // out = res + gamma[c] * branch; one block per (n, c) plane chunk.
+// DropPath keep mask with a draw that depends only on (seed, offset, n): the
+// value for sample n is output number offset + n of a SplitMix64 generator
+// seeded with `seed` (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", 2014; finaliser constants of Vigna's public splitmix64),
+// so every shard, or device, holding sample n draws the same bits.  Keep iff
+// the output's top 24 bits are >= t = floor(p * 2^24); a kept sample's branch
+// is scaled by 1 / (1 - p).
+__device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed, unsigned long long i) {
+    unsigned long long z = seed + (i + 1ULL) * 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+__global__ void drop_path_mask_kernel(int N, unsigned t, float scale, unsigned long long seed,
+                                      unsigned long long offset, float* __restrict__ mask) {
+    for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
+        const unsigned u = (unsigned)(splitmix64_at(seed, offset + (unsigned long long)n) >> 40);
+        mask[n] = u >= t ? scale : 0.0f;
+    }
+}
+
+// Layer scale (+ DropPath) + residual: out = res + mask[n] * gamma[c] * branch,
+// mask NULL meaning 1.  Block = (plane n*C + c, chunk of its pixels).
 __global__ void ls_fwd_kernel(const float* __restrict__ res, const float* __restrict__ br,
-                              const float* __restrict__ gamma, float* __restrict__ out, int C, long long HW,
-                              int chunks) {
+                              const float* __restrict__ gamma, const float* __restrict__ mask,
+                              float* __restrict__ out, int C, long long HW, int chunks) {
     const long long plane = blockIdx.x / chunks;
     const int chunk = blockIdx.x % chunks;
-    const float gm = __ldg(gamma + plane % C);
+    const float gm = __ldg(gamma + plane % C) * (mask ? __ldg(mask + plane / C) : 1.0f);
     const long long b0 = HW * chunk / chunks, b1 = HW * (chunk + 1) / chunks;
     const long long off = plane * HW;
     for (long long q = b0 + threadIdx.x; q < b1; q += blockDim.x) out[off + q] = fmaf(gm, __ldg(br + off + q), __ldg(res + off + q));
 }
 
 // gbranch = gamma[c] * gy; partial ggamma of this chunk = sum branch * gy (fixed order).
+// Backward: gbranch = mask[n] * gamma[c] * gy; part[plane][chunk] = mask[n] *
+// (sum over the chunk of branch * gy), summed over (n, chunk) by ls_reduce_kernel.
 __global__ void ls_bwd_kernel(const float* __restrict__ br, const float* __restrict__ gamma,
-                              const float* __restrict__ gy, float* __restrict__ gbr, float* __restrict__ part, int C,
-                              long long HW, int chunks) {
+                              const float* __restrict__ mask, const float* __restrict__ gy, float* __restrict__ gbr,
+                              float* __restrict__ part, int C, long long HW, int chunks) {
     __shared__ float red[32];
     const long long plane = blockIdx.x / chunks;
     const int chunk = blockIdx.x % chunks;
-    const float gm = __ldg(gamma + plane % C);
+    const float m = mask ? __ldg(mask + plane / C) : 1.0f;
+    const float gm = __ldg(gamma + plane % C) * m;
     const long long b0 = HW * chunk / chunks, b1 = HW * (chunk + 1) / chunks;
     const long long off = plane * HW;
     float acc = 0.0f;
@@ -209,7 +235,7 @@ __global__ void ls_bwd_kernel(const float* __restrict__ br, const float* __restr
     if (threadIdx.x == 0) {
         float t = 0.0f;
         for (int k = 0; k < (int)(blockDim.x >> 5); k++) t += red[k];
-        part[blockIdx.x] = t;  // [plane][chunk]
+        part[blockIdx.x] = m * t;  // [plane][chunk]
     }
 }
 
@@ -329,29 +355,46 @@ hc_status hc_add_inplace(long long n, float* y, const float* x, void* stream) {
     return launched();
 }
 
-hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
-                                     const float* gamma, float* out, void* stream) {
-    if (N <= 0 || C <= 0 || HW <= 0 || !res || !branch || !gamma || !out) return HC_ERR_INVALID_ARG;
-    ls_fwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, (cudaStream_t)stream>>>(res, branch, gamma, out,
-                                                                                            C, HW, LS_CHUNKS);
+hc_status hc_drop_path_mask(int N, float drop_prob, unsigned long long seed, unsigned long long offset, float* mask,
+                            void* stream) {
+    if (N <= 0 || !mask || !(drop_prob >= 0.0f) || !(drop_prob < 1.0f)) return HC_ERR_INVALID_ARG;
+    const unsigned t = (unsigned)floor((double)drop_prob * 16777216.0);
+    const float scale = 1.0f / (1.0f - drop_prob);
+    drop_path_mask_kernel<<<(N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024, 256, 0, (cudaStream_t)stream>>>(
+        N, t, scale, seed, offset, mask);
     return launched();
 }
-
-hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
-                                     const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
-                                     void* stream) {
+hc_status hc_layerscale_droppath_fwd(int N, int C, long long HW, const float* res, const float* branch,
+                                     const float* gamma, const float* mask, float* out, void* stream) {
+    if (N <= 0 || C <= 0 || HW <= 0 || !res || !branch || !gamma || !out) return HC_ERR_INVALID_ARG;
+    ls_fwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, (cudaStream_t)stream>>>(res, branch, gamma, mask,
+                                                                                            out, C, HW, LS_CHUNKS);
+    return launched();
+}
+hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
+                                     const float* gamma, float* out, void* stream) {
+    return hc_layerscale_droppath_fwd(N, C, HW, res, branch, gamma, nullptr, out, stream);
+}
+hc_status hc_layerscale_droppath_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
+                                     const float* mask, const float* gy, float* gbranch, float* ggamma, void* ws,
+                                     size_t ws_bytes, void* stream) {
     if (N <= 0 || C <= 0 || HW <= 0 || !branch || !gamma || !gy || !ggamma) return HC_ERR_INVALID_ARG;
     size_t need = 0;
     hc_pointwise_workspace_size(N, C, HW, &need);
     if (ws_bytes < need || !ws || !al16(ws)) return HC_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
     float* part = (float*)ws;
-    ls_bwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, st>>>(branch, gamma, gy, gbranch, part, C, HW,
-                                                                          LS_CHUNKS);
+    ls_bwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, st>>>(branch, gamma, mask, gy, gbranch, part, C,
+                                                                          HW, LS_CHUNKS);
     hc_status s = launched();
     if (s) return s;
     ls_reduce_kernel<<<(C + 127) / 128, 128, 0, st>>>(part, ggamma, N, C, LS_CHUNKS);
     return launched();
+}
+hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
+                                     const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,
+                                     void* stream) {
+    return hc_layerscale_droppath_bwd(N, C, HW, branch, gamma, nullptr, gy, gbranch, ggamma, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -87,6 +87,12 @@ _lib.hc_layerscale_residual_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, 
 for _n in ("hc_add_inplace", "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
            "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd"):
     getattr(_lib, _n).restype = C.c_int
+_lib.hc_drop_path_mask.argtypes = [_I, _F, C.c_ulonglong, C.c_ulonglong, _P, _P]
+_lib.hc_drop_path_mask.restype = C.c_int
+_lib.hc_layerscale_droppath_fwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P]
+_lib.hc_layerscale_droppath_fwd.restype = C.c_int
+_lib.hc_layerscale_droppath_bwd.argtypes = [_I, _I, _L, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
+_lib.hc_layerscale_droppath_bwd.restype = C.c_int
 _lib.hc_conv2d_step_graph_create.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t,
                                              C.POINTER(C.c_void_p)]
 _lib.hc_conv2d_step_graph_create.restype = C.c_int
@@ -111,7 +117,8 @@ EXPORTS = [
     "hc_sync_check", "hc_status_string", "hc_launch_count", "hc_conv2d_bwd_depthwise_noalloc",
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
-    "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy",
+    "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
+    "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd",
 ]
 
 
@@ -184,6 +191,20 @@ def hc_step_graph_launch(h, stream=None) -> int:
 
 def hc_step_graph_destroy(h) -> int:
     return _lib.hc_step_graph_destroy(h)
+
+
+def hc_drop_path_mask(N, drop_prob, seed, offset, mask, stream=None) -> int:
+    return _lib.hc_drop_path_mask(int(N), float(drop_prob), int(seed), int(offset), _ptr(mask), _stream(stream))
+
+
+def hc_layerscale_droppath_fwd(N, C_, HW, res, branch, gamma, mask, out, stream=None) -> int:
+    return _lib.hc_layerscale_droppath_fwd(int(N), int(C_), int(HW), _ptr(res), _ptr(branch), _ptr(gamma), _ptr(mask),
+                                           _ptr(out), _stream(stream))
+
+
+def hc_layerscale_droppath_bwd(N, C_, HW, branch, gamma, mask, gy, gbranch, ggamma, ws, ws_bytes, stream=None) -> int:
+    return _lib.hc_layerscale_droppath_bwd(int(N), int(C_), int(HW), _ptr(branch), _ptr(gamma), _ptr(mask), _ptr(gy),
+                                           _ptr(gbranch), _ptr(ggamma), _ptr(ws), int(ws_bytes), _stream(stream))
 
 
 def hc_halo_gather(d, x, x_ext, stream=None) -> int:

@@ -17,7 +17,13 @@ What pins what:
                            one for every shard count;
   * LayerNorm / GELU / layer scale -- torch fp64 functions and autograd, closed
                            forms (mean 0, variance 1, GELU(0) = 0, GELU'(0) = 1/2,
-                           Phi(1)), central finite differences.
+                           Phi(1)), central finite differences;
+  * DropPath mask         -- the published first outputs of SplitMix64
+                           (tests/golden/splitmix64.json), the keep decision on
+                           those bits, p = 0, the Bernoulli rate within 5 sigma,
+                           unbiased scaling, slices drawn with an offset;
+  * layer scale + DropPath -- the unmasked op (all-ones mask), dropped samples,
+                           torch autograd.
 """
 from __future__ import annotations
 
@@ -365,8 +371,57 @@ def pin_layerscale(orc):
     assert np.abs(gg - gt.grad.numpy()).max() <= 1e-13
 
 
+def pin_splitmix64_published(orc):
+    g = json.load(open(os.path.join(os.path.dirname(GOLDEN), "splitmix64.json")))
+    for i, hx in enumerate(g["outputs_hex"]):
+        assert orc.splitmix64(g["seed"], i) == int(hx, 16), (i, hex(orc.splitmix64(g["seed"], i)))
+
+
+def pin_drop_path_mask(orc):
+    # the keep decision on the published first output of seed 0: top 24 bits 0xe220a8
+    u0 = int(json.load(open(os.path.join(os.path.dirname(GOLDEN), "splitmix64.json")))["outputs_hex"][0], 16) >> 40
+    p_keep = math.floor(u0 / 2 ** 24 * 100) / 100          # largest p (2 decimals) that still keeps sample 0
+    assert orc.drop_path_mask(1, p_keep, 0, 0)[0] == np.float32(1.0) / (np.float32(1.0) - np.float32(p_keep))
+    assert orc.drop_path_mask(1, p_keep + 0.01, 0, 0)[0] == 0.0
+    assert np.all(orc.drop_path_mask(1000, 0.0, 7, 3) == 1.0)          # p = 0 keeps every sample, scale 1
+    p = 0.3
+    m = orc.drop_path_mask(400_000, p, 12345, 0)
+    scale = np.float32(1.0) / (np.float32(1.0) - np.float32(p))
+    assert set(np.unique(m).tolist()) <= {0.0, float(scale)}
+    kept = float(np.mean(m > 0))
+    sd = math.sqrt(p * (1 - p) / m.size)
+    assert abs(kept - (1 - p)) <= 5 * sd, kept                        # Bernoulli(1 - p) within 5 sigma
+    assert abs(float(np.mean(m, dtype=np.float64)) - 1.0) <= 5 * sd / (1 - p) + 1e-6   # unbiased scaling
+    # shard consistency: a slice of the batch drawn with offset = its first sample matches
+    for k, n in ((0, 10), (17, 100), (399_000, 1000)):
+        assert np.array_equal(orc.drop_path_mask(n, p, 12345, k), m[k:k + n]), k
+    assert not np.array_equal(orc.drop_path_mask(1000, p, 12346, 0), m[:1000])
+
+
+def pin_layerscale_droppath(orc):
+    res = synth.normal((4, 6, 3, 4), 1.0, 5, 1).astype(np.float64)
+    br = synth.normal(res.shape, 1.0, 5, 2).astype(np.float64)
+    gamma = synth.normal((6,), 1e-2, 5, 3).astype(np.float64)
+    gy = synth.normal(res.shape, 1.0, 5, 4).astype(np.float64)
+    ones = np.ones(4)
+    assert np.array_equal(orc.layerscale_droppath_fwd(res, br, gamma, ones), orc.layerscale_residual_fwd(res, br, gamma))
+    for a, b in zip(orc.layerscale_droppath_bwd(br, gamma, ones, gy), orc.layerscale_residual_bwd(br, gamma, gy)):
+        assert np.array_equal(a, b)
+    mask = np.array([0.0, 1.25, 0.0, 1.25])
+    out = orc.layerscale_droppath_fwd(res, br, gamma, mask)
+    assert np.array_equal(out[0], res[0]) and np.array_equal(out[2], res[2])   # a dropped sample passes res through
+    rt, bt, gt = (_t(a).requires_grad_() for a in (res, br, gamma))
+    (rt + _t(mask)[:, None, None, None] * gt[None, :, None, None] * bt).backward(_t(gy))
+    gres, gbr, gg = orc.layerscale_droppath_bwd(br, gamma, mask, gy)
+    assert np.array_equal(gres, gy)
+    assert np.abs(gbr - bt.grad.numpy()).max() <= 1e-15
+    assert np.all(gbr[0] == 0) and np.all(gbr[2] == 0)
+    assert np.abs(gg - gt.grad.numpy()).max() <= 1e-13
+
+
 ALL_PINS = [
     pin_out_size, pin_fwd_vs_torch, pin_fwd_vs_scipy, pin_fwd_1x1_is_matmul, pin_fwd_delta_kernel,
     pin_bwd_vs_autograd, pin_bwd_jacobian, pin_adjoint, pin_point_evaluators, pin_shard_plan_pages,
     pin_shard_plan_cover, pin_halo_extend, pin_sharded_equals_unsharded, pin_layernorm, pin_gelu, pin_layerscale,
+    pin_splitmix64_published, pin_drop_path_mask, pin_layerscale_droppath,
 ]

@@ -94,3 +94,63 @@ def test_add_inplace(hc, n):
     hc.check(hc.hc_add_inplace(n, y.view, R.dev(b)))
     hc.check(hc.hc_sync_check())
     assert np.array_equal(y.numpy(), (a + b).astype(np.float32))
+
+
+@pytest.mark.parametrize("N,p,seed,offset", [(7, 0.1, 0, 0), (4096, 0.3, 12345, 0), (100_003, 0.5, 2 ** 63 + 5, 77),
+                                             (33, 0.0, 9, 1), (1, 0.999, 3, 2 ** 40)])
+def test_drop_path_mask_bitexact(hc, orc, N, p, seed, offset):
+    """The device draw equals the oracle's SplitMix64 draw bit for bit."""
+    m = R.Guarded((N,))
+    hc.check(hc.hc_drop_path_mask(N, p, seed, offset, m.view))
+    hc.check(hc.hc_sync_check())
+    assert np.array_equal(m.numpy(), orc.drop_path_mask(N, p, seed, offset))
+
+
+def test_drop_path_mask_shard_consistent(hc, orc):
+    """A slice of the batch drawn with offset = its first sample (what a device or
+    shard holding those samples would call) equals that slice of the full draw."""
+    N, p, seed = 1000, 0.25, 31337
+    full = R.Guarded((N,))
+    hc.check(hc.hc_drop_path_mask(N, p, seed, 0, full.view))
+    parts = []
+    for a, b in ((0, 250), (250, 500), (500, 1000)):
+        g = R.Guarded((b - a,))
+        hc.check(hc.hc_drop_path_mask(b - a, p, seed, a, g.view))
+        parts.append(g)
+    hc.check(hc.hc_sync_check())
+    assert np.array_equal(np.concatenate([g.numpy() for g in parts]), full.numpy())
+    st = hc.hc_drop_path_mask(N, 1.0, seed, 0, full.view)
+    assert st == hc.HC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape", [(8, 64, 9, 17), (3, 256, 4, 128)])
+def test_layerscale_droppath(hc, orc, shape):
+    N, C, H, W = shape
+    HW = H * W
+    res = synth.normal(shape, 1.0, 9, 1)
+    br = synth.normal(shape, 1.0, 9, 2)
+    gamma = synth.normal((C,), 1e-1, 9, 3)
+    gy = synth.normal(shape, 1.0, 9, 4)
+    mask = R.dev(orc.drop_path_mask(N, 0.4, 2024, 0))
+    hmask = mask.cpu().numpy()
+    assert 0 < np.count_nonzero(hmask) < N   # both kept and dropped samples
+    out = R.Guarded(shape)
+    hc.check(hc.hc_layerscale_droppath_fwd(N, C, HW, R.dev(res), R.dev(br), R.dev(gamma), mask, out.view))
+    gbr, gg = R.Guarded(shape), R.Guarded((C,))
+    ws, nb = _ws(hc, N, C, HW)
+    hc.check(hc.hc_layerscale_droppath_bwd(N, C, HW, R.dev(br), R.dev(gamma), mask, R.dev(gy), gbr.view, gg.view,
+                                           ws, nb))
+    hc.check(hc.hc_sync_check())
+    o = out.numpy()
+    assert R.normwise(o, orc.layerscale_droppath_fwd(res, br, gamma, hmask)) <= 1e-5
+    for n in np.flatnonzero(hmask == 0):
+        assert np.array_equal(o[n], res[n]) and np.all(gbr.numpy()[n] == 0)
+    _, gbrr, ggr = orc.layerscale_droppath_bwd(br, gamma, hmask, gy)
+    assert R.normwise(gbr.numpy(), gbrr) <= 1e-5
+    assert R.normwise(gg.numpy(), ggr) <= 1e-4
+    # no mask: bit-identical to the plain layer scale
+    o1, o2 = R.Guarded(shape), R.Guarded(shape)
+    hc.check(hc.hc_layerscale_droppath_fwd(N, C, HW, R.dev(res), R.dev(br), R.dev(gamma), None, o1.view))
+    hc.check(hc.hc_layerscale_residual_fwd(N, C, HW, R.dev(res), R.dev(br), R.dev(gamma), o2.view))
+    hc.check(hc.hc_sync_check())
+    assert np.array_equal(o1.numpy(), o2.numpy())

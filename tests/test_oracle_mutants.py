@@ -33,6 +33,13 @@ MUTANTS = [
     ("gelu_missing_sqrt2", "void or_gelu_fwd(", "erf(x[i] / sqrt(2.0))", "erf(x[i])"),
     ("gelu_bwd_drops_density_term", "void or_gelu_bwd(", "(Phi + x[i] * phi)", "(Phi)"),
     ("layerscale_bwd_wrong_gamma_grad", "void or_layerscale_residual_bwd(", "ggamma[c] += branch[o] * gy[o];", "ggamma[c] += gy[o];"),
+    ("splitmix_wrong_final_shift", "uint64_t or_splitmix64(", "return z ^ (z >> 31);", "return z ^ (z >> 30);"),
+    ("splitmix_counter_off_by_one", "uint64_t or_splitmix64(", "(i + 1) *", "i *"),
+    ("drop_path_inverted_keep", "int or_drop_path_mask(", "u >= t ? scale : 0.0f", "u < t ? scale : 0.0f"),
+    ("drop_path_unscaled", "int or_drop_path_mask(", "const float scale = 1.0f / (1.0f - p);", "const float scale = 1.0f;"),
+    ("drop_path_low_bits", "int or_drop_path_mask(", "offset + (uint64_t)n) >> 40)", "offset + (uint64_t)n) & 0xFFFFFF)"),
+    ("droppath_fwd_ignores_mask", "void or_layerscale_droppath_fwd(", "res[o] + mask[n] * gamma[c] * branch[o]", "res[o] + gamma[c] * branch[o]"),
+    ("droppath_bwd_gamma_grad_ignores_mask", "void or_layerscale_droppath_bwd(", "ggamma[c] += mask[n] * branch[o] * gy[o];", "ggamma[c] += branch[o] * gy[o];"),
 ]
 
 
