@@ -39,7 +39,8 @@ def compile_oracle(src: str = SRC, out: str = LIB, openmp: bool = True) -> str:
 
 class Desc(C.Structure):
     _fields_ = [(n, C.c_int) for n in
-                ("N", "C_in", "H", "W", "C_out", "kh", "kw", "stride", "padding", "groups", "num_shards")]
+                ("N", "C_in", "H", "W", "C_out", "kh", "kw", "stride", "padding", "groups", "num_shards",
+                 "num_shards_h")]
 
 
 class Extent(C.Structure):
@@ -48,7 +49,7 @@ class Extent(C.Structure):
 
 
 def make_desc(cfg: dict) -> Desc:
-    return Desc(*(int(cfg[k]) for k, _ in Desc._fields_))
+    return Desc(*(int(cfg.get(k, 1) if k == "num_shards_h" else cfg[k]) for k, _ in Desc._fields_))
 
 
 _F = C.POINTER(C.c_float)
@@ -87,6 +88,7 @@ class Oracle:
             "or_conv2d_bwd_weight": [P, _F, _F, _D],
             "or_conv2d_bwd_bias": [P, _F, _D],
             "or_shard_plan": [P, C.POINTER(Extent), C.POINTER(C.c_int), C.POINTER(C.c_int)],
+            "or_shard_plan_h": [P, C.POINTER(Extent)],
             "or_halo_extend": [P, C.c_int, _F, _F],
             "or_sharded_fwd": [P, _F, _F, _F, _D],
             "or_sharded_bwd": [P, _F, _F, _F, _D, _D, _D],
@@ -96,7 +98,7 @@ class Oracle:
             fn.restype = C.c_int
         L.or_conv2d_fwd_at.argtypes = [P, _F, _F, _F] + [C.c_int] * 4
         L.or_conv2d_gx_at.argtypes = [P, _F, _F] + [C.c_int] * 4
-        L.or_conv2d_gw_at.argtypes = [P, _F, _F] + [C.c_int] * 6
+        L.or_conv2d_gw_at.argtypes = [P, _F, _F] + [C.c_int] * 8
         L.or_conv2d_gb_at.argtypes = [P, _F] + [C.c_int] * 3
         for n in ("or_conv2d_fwd_at", "or_conv2d_gx_at", "or_conv2d_gw_at", "or_conv2d_gb_at"):
             getattr(L, n).restype = C.c_double
@@ -164,8 +166,9 @@ class Oracle:
     def gx_at(self, cfg, w, gy, n, ci, h, c):
         return self.lib.or_conv2d_gx_at(C.byref(make_desc(cfg)), _f(w), _f(gy), n, ci, h, c)
 
-    def gw_at(self, cfg, x, gy, co, cl, u, v, j0, j1):
-        return self.lib.or_conv2d_gw_at(C.byref(make_desc(cfg)), _f(x), _f(gy), co, cl, u, v, j0, j1)
+    def gw_at(self, cfg, x, gy, co, cl, u, v, j0, j1, i0=0, i1=1 << 30):
+        """grad_weight[co, cl, u, v] restricted to output columns [j0, j1) and rows [i0, i1)."""
+        return self.lib.or_conv2d_gw_at(C.byref(make_desc(cfg)), _f(x), _f(gy), co, cl, u, v, j0, j1, i0, i1)
 
     def gb_at(self, cfg, gy, co, j0, j1):
         return self.lib.or_conv2d_gb_at(C.byref(make_desc(cfg)), _f(gy), co, j0, j1)
@@ -181,13 +184,26 @@ class Oracle:
         rows = [tuple(getattr(e, f) for f, _ in Extent._fields_) for e in ext]
         return 0, rows, Ho.value, Wo.value
 
-    def halo_extend(self, cfg, r, x):
+    def shard_plan_h(self, cfg):
+        """Row-shard extents (num_shards_h of them, or one covering every row)."""
+        Sh = max(1, int(cfg.get("num_shards_h", 1)))
+        ext = (Extent * Sh)()
+        rc = self.lib.or_shard_plan_h(C.byref(make_desc(cfg)), ext)
+        if rc:
+            return rc, None
+        return 0, [tuple(getattr(e, f) for f, _ in Extent._fields_) for e in ext]
+
+    def halo_extend(self, cfg, q, x):
+        """Extended tile of grid shard q = a * num_shards + b: [N][C][He][We]."""
         rc, plan, _, _ = self.shard_plan(cfg)
         assert rc == 0, rc
-        e = plan[r]
+        rc, plan_h = self.shard_plan_h(cfg)
+        assert rc == 0, rc
+        e, f = plan[q % cfg["num_shards"]], plan_h[q // cfg["num_shards"]]
         We = e[2] + (e[1] - e[0]) + e[3]
-        xe = np.empty((cfg["N"], cfg["C_in"], cfg["H"], We), np.float32)
-        rc = self.lib.or_halo_extend(C.byref(make_desc(cfg)), r, _f(x), _f(xe))
+        He = f[2] + (f[1] - f[0]) + f[3]
+        xe = np.empty((cfg["N"], cfg["C_in"], He, We), np.float32)
+        rc = self.lib.or_halo_extend(C.byref(make_desc(cfg)), q, _f(x), _f(xe))
         assert rc == 0, rc
         return xe
 
@@ -199,7 +215,7 @@ class Oracle:
         return y
 
     def sharded_bwd(self, cfg, x, w, gy):
-        S = cfg["num_shards"]
+        S = cfg["num_shards"] * max(1, int(cfg.get("num_shards_h", 1)))
         gx = np.empty((cfg["N"], cfg["C_in"], cfg["H"], cfg["W"]), np.float64)
         gwp = np.empty((S, cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"]), np.float64)
         gbp = np.empty((S, cfg["C_out"]), np.float64)

@@ -55,6 +55,7 @@
 
 typedef struct {
     int N, C_in, H, W, C_out, kh, kw, stride, padding, groups, num_shards;
+    int num_shards_h; /* row shards (Shard(2)); 0 or 1: none */
 } or_desc;
 
 /* Per-shard extent: input columns [in_begin, in_end), halo widths, and the
@@ -261,14 +262,14 @@ double or_conv2d_gx_at(const or_desc* d, const float* w, const float* gy, int n,
 /* gw[co,ci',u,v] restricted to output columns [j_begin, j_end): with a
  * shard's owned columns this is that shard's _Partial value. */
 double or_conv2d_gw_at(const or_desc* d, const float* x, const float* gy, int co, int cl, int u, int v,
-                       int j_begin, int j_end) {
+                       int j_begin, int j_end, int i_begin, int i_end) {
     const int Ho = or_out_size(d->H, d->kh, d->stride, d->padding);
     const int Wo = or_out_size(d->W, d->kw, d->stride, d->padding);
     const int Cgi = d->C_in / d->groups, Cgo = d->C_out / d->groups;
     const int ci = (co / Cgo) * Cgi + cl, s = d->stride, p = d->padding;
     double acc = 0.0;
     for (int n = 0; n < d->N; n++)
-        for (int i = 0; i < Ho; i++) {
+        for (int i = i_begin; i < i_end && i < Ho; i++) {
             const int h = i * s - p + u;
             if (h < 0 || h >= d->H) continue;
             for (int j = j_begin; j < j_end && j < Wo; j++) {
@@ -303,146 +304,188 @@ double or_conv2d_gb_at(const or_desc* d, const float* gy, int co, int j_begin, i
  * outputs read.  Returns 0, or 2 when the layout is not supported (W not
  * divisible by the shard count, Wl not divisible by the stride, stride not
  * dividing the padding, or a halo wider than a neighbouring shard). */
-int or_shard_plan(const or_desc* d, or_extent* ext, int* Ho_out, int* Wo_out) {
-    if (!desc_ok(d) || d->num_shards <= 0) return 1;
-    const int S = d->num_shards, s = d->stride, p = d->padding;
-    const int Ho = or_out_size(d->H, d->kh, s, p), Wo = or_out_size(d->W, d->kw, s, p);
-    if (Ho <= 0 || Wo <= 0) return 1;
-    if (d->W % S) return 2;
-    const int Wl = d->W / S;
-    if (Wl % s || p % s) return 2;
+static int plan_1d(int in, int k, int s, int p, int S, int out, or_extent* ext) {
+    if (in % S) return 2;
+    const int L = in / S;
+    if (L % s || p % s) return 2;
     for (int r = 0; r < S; r++) {
         or_extent e;
-        e.in_begin = r * Wl;
-        e.in_end = (r + 1) * Wl;
-        e.out_begin = r * Wl / s;
-        e.out_end = (r == S - 1) ? Wo : (r + 1) * Wl / s;
-        if (e.out_end > Wo) e.out_end = Wo;
+        e.in_begin = r * L;
+        e.in_end = (r + 1) * L;
+        e.out_begin = r * L / s;
+        e.out_end = (r == S - 1) ? out : (r + 1) * L / s;
+        if (e.out_end > out) e.out_end = out;
         if (e.out_begin > e.out_end) e.out_begin = e.out_end;
         e.halo_left = 0;
         e.halo_right = 0;
         if (e.out_end > e.out_begin) {
-            const int first = e.out_begin * s - p;                 /* first column read */
-            const int last = (e.out_end - 1) * s - p + d->kw - 1;  /* last column read  */
+            const int first = e.out_begin * s - p;                /* first index read */
+            const int last = (e.out_end - 1) * s - p + k - 1;     /* last index read  */
             e.halo_left = first < e.in_begin ? e.in_begin - first : 0;
             e.halo_right = last >= e.in_end ? last - e.in_end + 1 : 0;
         }
-        if (e.halo_left > Wl || e.halo_right > Wl) return 2;
+        if (e.halo_left > L || e.halo_right > L) return 2;
         ext[r] = e;
     }
+    return 0;
+}
+
+static int shards_h(const or_desc* d) { return d->num_shards_h > 1 ? d->num_shards_h : 1; }
+
+int or_shard_plan(const or_desc* d, or_extent* ext, int* Ho_out, int* Wo_out) {
+    if (!desc_ok(d) || d->num_shards <= 0) return 1;
+    const int s = d->stride, p = d->padding;
+    const int Ho = or_out_size(d->H, d->kh, s, p), Wo = or_out_size(d->W, d->kw, s, p);
+    if (Ho <= 0 || Wo <= 0) return 1;
+    const int rc = plan_1d(d->W, d->kw, s, p, d->num_shards, Wo, ext);
+    if (rc) return rc;
     if (Ho_out) *Ho_out = Ho;
     if (Wo_out) *Wo_out = Wo;
     return 0;
 }
 
-/* Halo exchange + concat for shard r ([KW] 2.2 steps 1-2): the extended tile
- * [N][C][H][halo_left + Wl + halo_right] holds the left neighbour's last
- * halo_left columns, the shard's own block and the right neighbour's first
- * halo_right columns; columns outside the image are zero. */
-int or_halo_extend(const or_desc* d, int r, const float* x, float* x_ext) {
-    or_extent ext[1024];
-    if (d->num_shards > 1024) return 1;
-    int rc = or_shard_plan(d, ext, NULL, NULL);
+/* Row shards (the pages' Shard(2) variant: [KW] 5.2 switches the sharded
+ * dimension to the height at very high resolution): the same rule as the
+ * column plan, applied to H with the kernel height.  With num_shards_h <= 1
+ * there are no row neighbours: one extent covers every row with no halo rows
+ * (the local conv's padding supplies the image edges) and no row crop. */
+int or_shard_plan_h(const or_desc* d, or_extent* ext) {
+    if (!desc_ok(d)) return 1;
+    const int s = d->stride, p = d->padding;
+    const int Ho = or_out_size(d->H, d->kh, s, p);
+    if (Ho <= 0) return 1;
+    if (shards_h(d) == 1) {
+        or_extent e = {0, d->H, 0, 0, 0, Ho};
+        ext[0] = e;
+        return 0;
+    }
+    return plan_1d(d->H, d->kh, s, p, shards_h(d), Ho, ext);
+}
+
+/* Halo exchange + concat for shard q = a * S + b of the row x column shard
+ * grid ([KW] 2.2 steps 1-2, applied to rows and columns): the extended tile
+ * [N][C][top + Hl + bottom][left + Wl + right] holds the shard's block and the
+ * halo rows and columns around it read from the neighbouring shards; positions
+ * outside the image are zero. */
+int or_halo_extend(const or_desc* d, int q, const float* x, float* x_ext) {
+    or_extent ew[1024], eh[1024];
+    if (d->num_shards > 1024 || shards_h(d) > 1024) return 1;
+    int rc = or_shard_plan(d, ew, NULL, NULL);
+    if (!rc) rc = or_shard_plan_h(d, eh);
     if (rc) return rc;
-    const or_extent e = ext[r];
+    const or_extent e = ew[q % d->num_shards], f = eh[q / d->num_shards];
     const int We = e.halo_left + (e.in_end - e.in_begin) + e.halo_right;
+    const int He = f.halo_left + (f.in_end - f.in_begin) + f.halo_right;
     for (int n = 0; n < d->N; n++)
         for (int c = 0; c < d->C_in; c++)
-            for (int h = 0; h < d->H; h++)
+            for (int r = 0; r < He; r++)
                 for (int t = 0; t < We; t++) {
-                    const int col = e.in_begin - e.halo_left + t;
-                    X4(x_ext, d->C_in, d->H, We, n, c, h, t) =
-                        (col >= 0 && col < d->W) ? X4(x, d->C_in, d->H, d->W, n, c, h, col) : 0.0f;
+                    const int row = f.in_begin - f.halo_left + r, col = e.in_begin - e.halo_left + t;
+                    X4(x_ext, d->C_in, He, We, n, c, r, t) =
+                        (row >= 0 && row < d->H && col >= 0 && col < d->W) ? X4(x, d->C_in, d->H, d->W, n, c, row, col)
+                                                                           : 0.0f;
                 }
     return 0;
 }
 
-/* Forward, shard by shard: exchange + concat, local conv with padding in both
- * H and W on the extended tile, crop to the owned output columns. */
+/* Forward, shard by shard over the row x column grid: exchange + concat, local
+ * conv with padding in both H and W on the extended tile, crop to the owned
+ * output rows and columns. */
 int or_sharded_fwd(const or_desc* d, const float* x, const float* w, const float* b, double* y) {
-    or_extent ext[1024];
+    or_extent ew[1024], eh[1024];
     int Ho, Wo;
-    if (d->num_shards > 1024) return 1;
-    int rc = or_shard_plan(d, ext, &Ho, &Wo);
+    if (d->num_shards > 1024 || shards_h(d) > 1024) return 1;
+    int rc = or_shard_plan(d, ew, &Ho, &Wo);
+    if (!rc) rc = or_shard_plan_h(d, eh);
     if (rc) return rc;
-    const int s = d->stride, p = d->padding;
-    for (int r = 0; r < d->num_shards; r++) {
-        const or_extent e = ext[r];
-        if (e.out_end <= e.out_begin) continue;
+    const int s = d->stride, p = d->padding, S = d->num_shards;
+    for (int q = 0; q < shards_h(d) * S; q++) {
+        const or_extent e = ew[q % S], f = eh[q / S];
+        if (e.out_end <= e.out_begin || f.out_end <= f.out_begin) continue;
         const int We = e.halo_left + (e.in_end - e.in_begin) + e.halo_right;
-        float* xe = (float*)malloc(sizeof(float) * (size_t)d->N * d->C_in * d->H * We);
-        or_halo_extend(d, r, x, xe);
+        const int He = f.halo_left + (f.in_end - f.in_begin) + f.halo_right;
+        float* xe = (float*)malloc(sizeof(float) * (size_t)d->N * d->C_in * He * We);
+        or_halo_extend(d, q, x, xe);
         or_desc ld = *d;
         ld.W = We;
-        const int Wloc = or_out_size(We, d->kw, s, p);
-        double* yl = (double*)malloc(sizeof(double) * (size_t)d->N * d->C_out * Ho * (Wloc > 0 ? Wloc : 1));
+        ld.H = He;
+        const int Wloc = or_out_size(We, d->kw, s, p), Hloc = or_out_size(He, d->kh, s, p);
+        double* yl = (double*)malloc(sizeof(double) * (size_t)d->N * d->C_out * Hloc * Wloc);
         or_conv2d_fwd(&ld, xe, w, b, yl);
         /* Crop: owned output column out_begin + t reads extended-tile columns
          * from (out_begin*s - p) - (in_begin - halo_left) on; with padding p
-         * applied to the tile that is local output column t + crop. */
+         * applied to the tile that is local output column t + crop (rows alike). */
         const int crop = ((e.out_begin * s - p) - (e.in_begin - e.halo_left) + p) / s;
+        const int crop_h = ((f.out_begin * s - p) - (f.in_begin - f.halo_left) + p) / s;
         for (int n = 0; n < d->N; n++)
             for (int co = 0; co < d->C_out; co++)
-                for (int i = 0; i < Ho; i++)
+                for (int i = 0; i < f.out_end - f.out_begin; i++)
                     for (int t = 0; t < e.out_end - e.out_begin; t++)
-                        X4(y, d->C_out, Ho, Wo, n, co, i, e.out_begin + t) = X4(yl, d->C_out, Ho, Wloc, n, co, i, t + crop);
+                        X4(y, d->C_out, Ho, Wo, n, co, f.out_begin + i, e.out_begin + t) =
+                            X4(yl, d->C_out, Hloc, Wloc, n, co, i + crop_h, t + crop);
         free(yl);
         free(xe);
     }
     return 0;
 }
 
-/* Backward, shard by shard: zero-pad the shard's grad_output to the local
- * conv's output width (undoing the crop), local grad_input / grad_weight /
- * grad_bias on the extended tile, then send the halo columns of the local
- * grad_input back to the shards that own them (accumulate into gx).
- * gw_part is [S][C_out][C_in/groups][kh][kw], gb_part is [S][C_out]; either
- * may be NULL.  gx (NULL allowed) is [N][C_in][H][W]. */
+/* Backward, shard by shard over the row x column grid: zero-pad the shard's
+ * grad_output to the local conv's output size (undoing the crop), local
+ * grad_input / grad_weight / grad_bias on the extended tile, then send the halo
+ * rows and columns of the local grad_input back to the shards that own them
+ * (accumulate into gx).  gw_part is [Sh*S][C_out][C_in/groups][kh][kw] and
+ * gb_part is [Sh*S][C_out], shard q = a * S + b; either may be NULL.  gx (NULL
+ * allowed) is [N][C_in][H][W]. */
 int or_sharded_bwd(const or_desc* d, const float* x, const float* w, const float* gy,
                    double* gx, double* gw_part, double* gb_part) {
-    or_extent ext[1024];
+    or_extent ew[1024], eh[1024];
     int Ho, Wo;
-    if (d->num_shards > 1024) return 1;
-    int rc = or_shard_plan(d, ext, &Ho, &Wo);
+    if (d->num_shards > 1024 || shards_h(d) > 1024) return 1;
+    int rc = or_shard_plan(d, ew, &Ho, &Wo);
+    if (!rc) rc = or_shard_plan_h(d, eh);
     if (rc) return rc;
-    const int s = d->stride, p = d->padding;
+    const int s = d->stride, p = d->padding, S = d->num_shards;
     const size_t wsz = (size_t)d->C_out * (d->C_in / d->groups) * d->kh * d->kw;
     if (gx) memset(gx, 0, sizeof(double) * (size_t)d->N * d->C_in * d->H * d->W);
-    for (int r = 0; r < d->num_shards; r++) {
-        const or_extent e = ext[r];
-        if (e.out_end <= e.out_begin) {
-            if (gw_part) memset(gw_part + r * wsz, 0, sizeof(double) * wsz);
-            if (gb_part) memset(gb_part + (size_t)r * d->C_out, 0, sizeof(double) * d->C_out);
+    for (int q = 0; q < shards_h(d) * S; q++) {
+        const or_extent e = ew[q % S], f = eh[q / S];
+        if (e.out_end <= e.out_begin || f.out_end <= f.out_begin) {
+            if (gw_part) memset(gw_part + q * wsz, 0, sizeof(double) * wsz);
+            if (gb_part) memset(gb_part + (size_t)q * d->C_out, 0, sizeof(double) * d->C_out);
             continue;
         }
         const int We = e.halo_left + (e.in_end - e.in_begin) + e.halo_right;
-        float* xe = (float*)malloc(sizeof(float) * (size_t)d->N * d->C_in * d->H * We);
-        or_halo_extend(d, r, x, xe);
+        const int He = f.halo_left + (f.in_end - f.in_begin) + f.halo_right;
+        float* xe = (float*)malloc(sizeof(float) * (size_t)d->N * d->C_in * He * We);
+        or_halo_extend(d, q, x, xe);
         or_desc ld = *d;
         ld.W = We;
-        const int Wloc = or_out_size(We, d->kw, s, p);
+        ld.H = He;
+        const int Wloc = or_out_size(We, d->kw, s, p), Hloc = or_out_size(He, d->kh, s, p);
         const int crop = ((e.out_begin * s - p) - (e.in_begin - e.halo_left) + p) / s;
-        float* gyl = (float*)calloc((size_t)d->N * d->C_out * Ho * Wloc, sizeof(float));
+        const int crop_h = ((f.out_begin * s - p) - (f.in_begin - f.halo_left) + p) / s;
+        float* gyl = (float*)calloc((size_t)d->N * d->C_out * Hloc * Wloc, sizeof(float));
         for (int n = 0; n < d->N; n++)
             for (int co = 0; co < d->C_out; co++)
-                for (int i = 0; i < Ho; i++)
+                for (int i = 0; i < f.out_end - f.out_begin; i++)
                     for (int t = 0; t < e.out_end - e.out_begin; t++)
-                        X4(gyl, d->C_out, Ho, Wloc, n, co, i, t + crop) = X4(gy, d->C_out, Ho, Wo, n, co, i, e.out_begin + t);
+                        X4(gyl, d->C_out, Hloc, Wloc, n, co, i + crop_h, t + crop) =
+                            X4(gy, d->C_out, Ho, Wo, n, co, f.out_begin + i, e.out_begin + t);
         if (gx) {
-            double* gxe = (double*)malloc(sizeof(double) * (size_t)d->N * d->C_in * d->H * We);
+            double* gxe = (double*)malloc(sizeof(double) * (size_t)d->N * d->C_in * He * We);
             or_conv2d_bwd_input(&ld, w, gyl, gxe);
             for (int n = 0; n < d->N; n++)
                 for (int c = 0; c < d->C_in; c++)
-                    for (int h = 0; h < d->H; h++)
+                    for (int r = 0; r < He; r++)
                         for (int t = 0; t < We; t++) {
-                            const int col = e.in_begin - e.halo_left + t;
-                            if (col >= 0 && col < d->W)
-                                X4(gx, d->C_in, d->H, d->W, n, c, h, col) += X4(gxe, d->C_in, d->H, We, n, c, h, t);
+                            const int row = f.in_begin - f.halo_left + r, col = e.in_begin - e.halo_left + t;
+                            if (row >= 0 && row < d->H && col >= 0 && col < d->W)
+                                X4(gx, d->C_in, d->H, d->W, n, c, row, col) += X4(gxe, d->C_in, He, We, n, c, r, t);
                         }
             free(gxe);
         }
-        if (gw_part) or_conv2d_bwd_weight(&ld, xe, gyl, gw_part + r * wsz);
-        if (gb_part) or_conv2d_bwd_bias(&ld, gyl, gb_part + (size_t)r * d->C_out);
+        if (gw_part) or_conv2d_bwd_weight(&ld, xe, gyl, gw_part + q * wsz);
+        if (gb_part) or_conv2d_bwd_bias(&ld, gyl, gb_part + (size_t)q * d->C_out);
         free(gyl);
         free(xe);
     }

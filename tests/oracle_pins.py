@@ -257,15 +257,42 @@ def pin_shard_plan_cover(orc):
 
 def pin_halo_extend(orc):
     for cfg in (cfg_of(2, 3, 4, 16, 3, 5, 1, 2, 1, 4), cfg_of(1, 2, 3, 24, 2, 7, 1, 3, 2, 4),
-                cfg_of(1, 2, 3, 16, 2, 2, 2, 0, 1, 2)):
+                cfg_of(1, 2, 3, 16, 2, 2, 2, 0, 1, 2), dict(cfg_of(1, 2, 8, 16, 2, 3, 1, 1, 1, 2), num_shards_h=2),
+                dict(cfg_of(2, 1, 12, 8, 1, 5, 1, 2, 1, 1), num_shards_h=3)):
         x, _, _, _ = rand_case(cfg, 8)
         rc, plan, _, _ = orc.shard_plan(cfg)
+        rc2, plan_h = orc.shard_plan_h(cfg)
+        assert rc == 0 and rc2 == 0
         P = 8
-        xp = np.pad(x, ((0, 0), (0, 0), (0, 0), (P, P)))
-        for r, e in enumerate(plan):
-            xe = orc.halo_extend(cfg, r, x)
-            ref = xp[:, :, :, P + e[0] - e[2]: P + e[1] + e[3]]
-            assert np.array_equal(xe, ref), (cfg, r)
+        xp = np.pad(x, ((0, 0), (0, 0), (P, P), (P, P)))   # zeros past every image edge
+        for q in range(len(plan_h) * len(plan)):
+            e, f = plan[q % len(plan)], plan_h[q // len(plan)]
+            xe = orc.halo_extend(cfg, q, x)
+            ref = xp[:, :, P + f[0] - f[2]: P + f[1] + f[3], P + e[0] - e[2]: P + e[1] + e[3]]
+            assert np.array_equal(xe, ref), (cfg, q)
+
+
+def pin_shard_plan_rows(orc):
+    # The row plan follows the column rule on H: owned output rows partition
+    # [0, Hout); halos are exactly the rows read outside the shard.
+    for H, Sh, k, s, p in itertools.product((8, 12, 16), (1, 2, 4), (1, 2, 3, 5), (1, 2), (0, 1, 2)):
+        cfg = dict(cfg_of(1, 1, H, 8, 1, k, s, p, 1, 1), num_shards_h=Sh)
+        rc, plan = orc.shard_plan_h(cfg)
+        Hl = H // Sh
+        Ho = (H + 2 * p - k) // s + 1
+        if Sh == 1:   # no row neighbours: every row, no halo rows (padding supplies the edges)
+            assert rc == 0 and plan == [(0, H, 0, 0, 0, Ho)], (H, k, s, p)
+            continue
+        if H % Sh or Hl % s or p % s:
+            assert rc != 0, (H, Sh, k, s, p)
+            continue
+        if rc:
+            continue    # a halo wider than a neighbouring shard
+        assert [i for f in plan for i in range(f[4], f[5])] == list(range(Ho)), (H, Sh, k, s, p)
+        for f in plan:
+            if f[5] > f[4]:
+                rows = [i * s - p + u for i in range(f[4], f[5]) for u in range(k)]
+                assert f[0] - f[2] == min(min(rows), f[0]) and f[1] + f[3] == max(max(rows) + 1, f[1])
 
 
 SHARD_CASES = [
@@ -285,24 +312,28 @@ def pin_sharded_equals_unsharded(orc):
         gx = orc.conv2d_bwd_input(base, w, gy)
         gw = orc.conv2d_bwd_weight(base, x, gy)
         gb = orc.conv2d_bwd_bias(base, gy)
-        tried = 0
-        for S in range(1, base["W"] + 1):
-            cfg = dict(base, num_shards=S)
+        tried = tried_h = 0
+        for S, Sh in itertools.product(range(1, base["W"] + 1), (1, 2, 3)):
+            cfg = dict(base, num_shards=S, num_shards_h=Sh)
             rc, plan, _, _ = orc.shard_plan(cfg)
-            if rc:
+            rc2, plan_h = orc.shard_plan_h(cfg)
+            if rc or rc2:
                 continue
             tried += 1
+            tried_h += Sh > 1
             ys = orc.sharded_fwd(cfg, x, w, b)
-            assert np.abs(ys - y).max() <= 1e-12, (base, S)
+            assert np.abs(ys - y).max() <= 1e-12, (base, S, Sh)
             gxs, gwp, gbp = orc.sharded_bwd(cfg, x, w, gy)
-            assert np.abs(gxs - gx).max() <= 1e-12, (base, S)
-            assert np.abs(gwp.sum(0) - gw).max() <= 1e-12 * max(1, np.abs(gw).max()), (base, S)
-            assert np.abs(gbp.sum(0) - gb).max() <= 1e-12 * max(1, np.abs(gb).max()), (base, S)
-            # each partial is the gradient restricted to the shard's own output columns
-            for r, e in enumerate(plan):
+            assert np.abs(gxs - gx).max() <= 1e-12, (base, S, Sh)
+            assert np.abs(gwp.sum(0) - gw).max() <= 1e-12 * max(1, np.abs(gw).max()), (base, S, Sh)
+            assert np.abs(gbp.sum(0) - gb).max() <= 1e-12 * max(1, np.abs(gb).max()), (base, S, Sh)
+            # each partial is the gradient restricted to the shard's own output rows and columns
+            for q in range(len(plan_h) * len(plan)):
+                e, f = plan[q % len(plan)], plan_h[q // len(plan)]
                 co, cl, u, v = 0, 0, base["kh"] - 1, 0
-                assert abs(gwp[r, co, cl, u, v] - orc.gw_at(base, x, gy, co, cl, u, v, e[4], e[5])) <= 1e-12
-        assert tried >= 2, base
+                ref = orc.gw_at(base, x, gy, co, cl, u, v, e[4], e[5], f[4], f[5])
+                assert abs(gwp[q, co, cl, u, v] - ref) <= 1e-12, (base, S, Sh, q)
+        assert tried >= 2 and (tried_h >= 1 or (base["H"] % 2 and base["H"] % 3)), base
 
 
 def pin_layernorm(orc):
@@ -422,6 +453,6 @@ def pin_layerscale_droppath(orc):
 ALL_PINS = [
     pin_out_size, pin_fwd_vs_torch, pin_fwd_vs_scipy, pin_fwd_1x1_is_matmul, pin_fwd_delta_kernel,
     pin_bwd_vs_autograd, pin_bwd_jacobian, pin_adjoint, pin_point_evaluators, pin_shard_plan_pages,
-    pin_shard_plan_cover, pin_halo_extend, pin_sharded_equals_unsharded, pin_layernorm, pin_gelu, pin_layerscale,
+    pin_shard_plan_cover, pin_shard_plan_rows, pin_halo_extend, pin_sharded_equals_unsharded, pin_layernorm, pin_gelu, pin_layerscale,
     pin_splitmix64_published, pin_drop_path_mask, pin_layerscale_droppath,
 ]

@@ -23,11 +23,15 @@ MUTANTS = [
     ("bwd_bias_drops_last_row", "int or_conv2d_bwd_bias(", "for (int i = 0; i < Ho; i++)", "for (int i = 0; i < Ho - 1; i++)"),
     ("gx_at_ignores_stride", "double or_conv2d_gx_at(", "if (ti < 0 || ti % s) continue;", "if (ti < 0) continue;"),
     ("gw_at_extra_column", "double or_conv2d_gw_at(", "j < j_end && j < Wo", "j <= j_end && j < Wo"),
-    ("plan_right_halo_short", "int or_shard_plan(", "last - e.in_end + 1", "last - e.in_end"),
-    ("plan_owned_cols_shifted", "int or_shard_plan(", "e.out_begin = r * Wl / s;", "e.out_begin = r * Wl / s + (r > 0);"),
-    ("halo_drops_first_column", "int or_halo_extend(", "(col >= 0 && col < d->W)", "(col > 0 && col < d->W)"),
+    ("plan_right_halo_short", "static int plan_1d(", "last - e.in_end + 1", "last - e.in_end"),
+    ("plan_owned_cols_shifted", "static int plan_1d(", "e.out_begin = r * L / s;", "e.out_begin = r * L / s + (r > 0);"),
+    ("halo_drops_first_column", "int or_halo_extend(", "col >= 0 && col < d->W)", "col > 0 && col < d->W)"),
+    ("halo_drops_first_row", "int or_halo_extend(", "(row >= 0 && row < d->H", "(row > 0 && row < d->H"),
+    ("row_plan_ignores_kernel_height", "int or_shard_plan_h(", "plan_1d(d->H, d->kh,", "plan_1d(d->H, d->kh - 1,"),
+    ("sharded_fwd_no_row_crop", "int or_sharded_fwd(", "i + crop_h, t + crop", "i, t + crop"),
     ("sharded_fwd_no_crop", "int or_sharded_fwd(", "+ p) / s;", "+ 0) / s;"),
-    ("sharded_bwd_keeps_halo_grads", "int or_sharded_bwd(", "if (col >= 0 && col < d->W)", "if (col >= e.in_begin && col < e.in_end)"),
+    ("sharded_bwd_keeps_halo_grads", "int or_sharded_bwd(", "col >= 0 && col < d->W)", "col >= e.in_begin && col < e.in_end)"),
+    ("sharded_bwd_keeps_halo_row_grads", "int or_sharded_bwd(", "if (row >= 0 && row < d->H &&", "if (row >= f.in_begin && row < f.in_end &&"),
     ("ln_unbiased_variance", "void or_layernorm_c_fwd(", "var /= C;", "var /= (C - 1);"),
     ("ln_bwd_drops_mean_term", "void or_layernorm_c_bwd(", "gx[o] = rs * (gy[o] * gamma[c] - mg - xh * mgx);", "gx[o] = rs * (gy[o] * gamma[c] - xh * mgx);"),
     ("gelu_missing_sqrt2", "void or_gelu_fwd(", "erf(x[i] / sqrt(2.0))", "erf(x[i])"),
