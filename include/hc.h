@@ -47,9 +47,17 @@ typedef enum {
 
 /* The convolution (input, weight, bias, stride, padding, groups -- the
  * arguments of the _conv_forward override, kwkr.cn section 3.2) plus the
- * number of W shards.  Square stride and padding; no dilation. */
+ * number of W shards and, optionally, of H shards.  Square stride and padding;
+ * no dilation.
+ *   num_shards    W blocks (Shard(3)), >= 1.
+ *   num_shards_h  H blocks (Shard(2), kwkr.cn 5.2: the sharded dimension
+ *                 switches to the height at very high resolution); 0 or 1 for
+ *                 none.  With both, the shards form a row x column grid and
+ *                 shard q = a * num_shards + b holds row block a and column
+ *                 block b. */
 typedef struct {
     int N, C_in, H, W, C_out, kh, kw, stride, padding, groups, num_shards;
+    int num_shards_h;
 } hc_conv_desc;
 
 /* One shard of the plan: input columns [in_begin, in_end) (its Shard(3)
@@ -81,6 +89,14 @@ typedef enum {
  * when W % num_shards, Wl % stride or padding % stride is non-zero, or when a
  * halo is wider than Wl (a halo may only come from the adjacent shards). */
 hc_status hc_shard_plan(const hc_conv_desc* d, hc_shard_extent* ext, int* H_out, int* W_out);
+
+/* The row plan: the same rule on H with the kernel height (in_* / out_* are
+ * rows, halo_left / halo_right the halo rows above / below the block).  With
+ * num_shards_h <= 1 it is one extent of every row with no halo rows (no row
+ * neighbours; the padding supplies the image edges).
+ *   ext   out: max(1, num_shards_h) entries.
+ * HC_ERR_UNSUPPORTED as for hc_shard_plan, on H. */
+hc_status hc_shard_plan_rows(const hc_conv_desc* d, hc_shard_extent* ext);
 
 /* Workspace bytes that hc_conv2d_fwd (pass 0) or hc_conv2d_bwd (pass 1) needs
  * for this desc with HC_ALGO_AUTO (use hc_conv2d_workspace_size_algo for a
@@ -114,8 +130,11 @@ hc_status hc_conv2d_fwd_algo(const hc_conv_desc* d, const float* x, const float*
  *   gx         out [N][C_in][H][W], or NULL to skip
  *   gw         out [C_out][C_in/groups][kh][kw], or NULL to skip
  *   gb         out [C_out], or NULL to skip
- *   gw_partials out [num_shards][C_out][C_in/groups][kh][kw], or NULL
- *   gb_partials out [num_shards][C_out], or NULL
+ *   gw_partials out [Q][C_out][C_in/groups][kh][kw], or NULL
+ *   gb_partials out [Q][C_out], or NULL
+ *     Q = num_shards * max(1, num_shards_h), shard q = a * num_shards + b owning
+ *     output rows of row block a and columns of column block b; the full
+ *     gradients are the sums over q in increasing order.
  *   ws, ws_bytes: workspace of at least hc_conv2d_workspace_size(d, 1) bytes. */
 hc_status hc_conv2d_bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
                         float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes, void* stream);
@@ -124,10 +143,13 @@ hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float*
                              void* stream, hc_algo algo);
 
 /* Halo exchange + concat made explicit (kwkr.cn 2.2 steps 1-2): for every
- * shard r, x_ext[r] = [left halo | own block | right halo] of x, zeros past
- * the image edge.  x_ext is [num_shards][N][C_in][H][We] with
- * We = max over shards of halo_left + Wl + halo_right; a shard with narrower
- * halos leaves its unused trailing columns zero.  A pure copy (bit-exact). */
+ * shard q of the row x column grid, x_ext[q] is its block of x with the halo
+ * rows above / below (hc_shard_plan_rows) and halo columns left / right
+ * (hc_shard_plan) around it, zeros past the image edge.  x_ext is
+ * [Q][N][C_in][He][We], Q = num_shards * max(1, num_shards_h),
+ * We = max over column shards of halo_left + Wl + halo_right and He the same
+ * over row shards (H when there is one row shard); a shard with narrower halos
+ * leaves its unused trailing rows / columns zero.  A pure copy (bit-exact). */
 hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream);
 
 /* Depthwise backward that allocates nothing.  The pages have no counterpart:

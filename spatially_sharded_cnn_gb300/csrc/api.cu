@@ -17,7 +17,7 @@ static bool desc_valid(const hc_conv_desc* d) {
     if (!d) return false;
     if (d->N <= 0 || d->C_in <= 0 || d->H <= 0 || d->W <= 0 || d->C_out <= 0) return false;
     if (d->kh <= 0 || d->kw <= 0 || d->stride <= 0 || d->padding < 0 || d->groups <= 0) return false;
-    if (d->num_shards <= 0) return false;
+    if (d->num_shards <= 0 || d->num_shards_h < 0) return false;
     if (d->C_in % d->groups || d->C_out % d->groups) return false;
     if (out_size(d->H, d->kh, d->stride, d->padding) <= 0) return false;
     if (out_size(d->W, d->kw, d->stride, d->padding) <= 0) return false;
@@ -26,41 +26,60 @@ static bool desc_valid(const hc_conv_desc* d) {
     return elems < 1.0e12;
 }
 
-// Shard(3) plan.  Shard r owns input block [r*Wl, (r+1)*Wl) and output
-// columns [r*Wl/s, (r+1)*Wl/s) (the last shard up to W_out); its halos are
-// the columns outside its block that those outputs read.
-hc_status make_plan(const hc_conv_desc* d, Plan* p) {
-    if (!desc_valid(d)) return HC_ERR_INVALID_ARG;
-    const int S = d->num_shards, s = d->stride, pad = d->padding;
+// One dimension of the plan (Shard(3) on W, Shard(2) on H).  Block r owns
+// input [r*L, (r+1)*L) and outputs [r*L/s, (r+1)*L/s) (the last block up to
+// `out`); its halos are the positions outside its block that those outputs read.
+static hc_status plan_1d(int in, int k, int s, int pad, int S, int out, hc_shard_extent* ext, int* widest) {
     if (S > kMaxShards) return HC_ERR_UNSUPPORTED;
-    if (d->W % S) return HC_ERR_UNSUPPORTED;
-    const int Wl = d->W / S;
-    if (Wl % s || pad % s) return HC_ERR_UNSUPPORTED;
-    p->S = S;
-    p->Wl = Wl;
-    p->Ho = out_size(d->H, d->kh, s, pad);
-    p->Wo = out_size(d->W, d->kw, s, pad);
-    p->We = 0;
+    if (in % S) return HC_ERR_UNSUPPORTED;
+    const int L = in / S;
+    if (L % s || pad % s) return HC_ERR_UNSUPPORTED;
+    *widest = 0;
     for (int r = 0; r < S; r++) {
         hc_shard_extent e;
-        e.in_begin = r * Wl;
-        e.in_end = (r + 1) * Wl;
-        e.out_begin = r * (Wl / s);
-        e.out_end = (r == S - 1) ? p->Wo : (r + 1) * (Wl / s);
-        if (e.out_end > p->Wo) e.out_end = p->Wo;
+        e.in_begin = r * L;
+        e.in_end = (r + 1) * L;
+        e.out_begin = r * (L / s);
+        e.out_end = (r == S - 1) ? out : (r + 1) * (L / s);
+        if (e.out_end > out) e.out_end = out;
         if (e.out_begin > e.out_end) e.out_begin = e.out_end;
         e.halo_left = e.halo_right = 0;
         if (e.out_end > e.out_begin) {
             const int lo = e.out_begin * s - pad;
-            const int hi = (e.out_end - 1) * s - pad + d->kw;  // one past the last column read
+            const int hi = (e.out_end - 1) * s - pad + k;  // one past the last position read
             if (lo < e.in_begin) e.halo_left = e.in_begin - lo;
             if (hi > e.in_end) e.halo_right = hi - e.in_end;
         }
-        if (e.halo_left > Wl || e.halo_right > Wl) return HC_ERR_UNSUPPORTED;
-        const int we = e.halo_left + Wl + e.halo_right;
-        if (we > p->We) p->We = we;
-        p->ext[r] = e;
+        if (e.halo_left > L || e.halo_right > L) return HC_ERR_UNSUPPORTED;
+        const int we = e.halo_left + L + e.halo_right;
+        if (we > *widest) *widest = we;
+        ext[r] = e;
     }
+    return HC_OK;
+}
+
+hc_status make_plan(const hc_conv_desc* d, Plan* p) {
+    if (!desc_valid(d)) return HC_ERR_INVALID_ARG;
+    const int S = d->num_shards, s = d->stride, pad = d->padding;
+    p->S = S;
+    p->Wl = d->W / S;
+    p->Ho = out_size(d->H, d->kh, s, pad);
+    p->Wo = out_size(d->W, d->kw, s, pad);
+    hc_status st = plan_1d(d->W, d->kw, s, pad, S, p->Wo, p->ext, &p->We);
+    if (st) return st;
+    p->Sh = d->num_shards_h > 1 ? d->num_shards_h : 1;
+    if (p->Sh == 1) {  // no row neighbours: every row, no halo rows, no row crop
+        p->ext_h[0] = hc_shard_extent{0, d->H, 0, 0, 0, p->Ho};
+        p->Hl = d->H;
+        p->Hlo = p->Ho;
+        p->He = d->H;
+    } else {
+        if ((st = plan_1d(d->H, d->kh, s, pad, p->Sh, p->Ho, p->ext_h, &p->He))) return st;
+        p->Hl = d->H / p->Sh;
+        p->Hlo = p->Hl / s;
+    }
+    if ((long long)p->Sh * S > kMaxShards) return HC_ERR_UNSUPPORTED;
+    p->Q = p->Sh * S;
     return HC_OK;
 }
 
@@ -92,9 +111,9 @@ static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
 //   DEPTHWISE: [gw partials S*C*K*K][gb partials S*C][tile partials]
 //   TC_3XTF32: [gw partials][gb partials][NHWC hi/lo copies, weights hi/lo, split-K partials]
 static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
-    size_t b = round256(sizeof(float) * p.S * wsize(d)) + round256(sizeof(float) * p.S * d->C_out);
+    size_t b = round256(sizeof(float) * p.Q * wsize(d)) + round256(sizeof(float) * p.Q * d->C_out);
     if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
-    if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.S)) + tc_ws_bytes(d, p, 1);
+    if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + tc_ws_bytes(d, p, 1);
     return b;
 }
 
@@ -150,9 +169,9 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     cudaStream_t s = (cudaStream_t)stream;
     char* wsp = (char*)ws;
     float* gwp = (float*)wsp;
-    wsp += round256(sizeof(float) * p.S * wsize(d));
+    wsp += round256(sizeof(float) * p.Q * wsize(d));
     float* gbp = (float*)wsp;
-    wsp += round256(sizeof(float) * p.S * d->C_out);
+    wsp += round256(sizeof(float) * p.Q * d->C_out);
     if (gwp_out) gwp = gwp_out;
     if (gbp_out) gbp = gbp_out;
     const bool want_w = gw || gwp_out;
@@ -163,10 +182,11 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
             break;
         case HC_ALGO_TC_3XTF32: {
             float* btmp = (float*)wsp;
-            wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.S));
+            wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q));
             if ((gx || want_w) && (st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s))) return st;
             if (want_b)
-                st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl / d->stride, btmp, s);
+                st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl / d->stride, p.Sh, p.Hlo,
+                                               btmp, s);
             break;
         }
         case HC_ALGO_DIRECT:
@@ -178,8 +198,8 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     }
     if (st) return st;
     // _Partial -> full: sum the shards' partials in shard order.
-    if (gw && (st = launch_sum_rows(gwp, gw, p.S, (long long)wsize(d), s))) return st;
-    if (gb && (st = launch_sum_rows(gbp, gb, p.S, d->C_out, s))) return st;
+    if (gw && (st = launch_sum_rows(gwp, gw, p.Q, (long long)wsize(d), s))) return st;
+    if (gb && (st = launch_sum_rows(gbp, gb, p.Q, d->C_out, s))) return st;
     return HC_OK;
 }
 
@@ -197,6 +217,15 @@ hc_status hc_shard_plan(const hc_conv_desc* d, hc_shard_extent* ext, int* H_out,
     memcpy(ext, p.ext, sizeof(hc_shard_extent) * p.S);
     if (H_out) *H_out = p.Ho;
     if (W_out) *W_out = p.Wo;
+    return HC_OK;
+}
+
+hc_status hc_shard_plan_rows(const hc_conv_desc* d, hc_shard_extent* ext) {
+    if (!d || !ext) return HC_ERR_INVALID_ARG;
+    static thread_local Plan p;
+    hc_status st = make_plan(d, &p);
+    if (st) return st;
+    memcpy(ext, p.ext_h, sizeof(hc_shard_extent) * p.Sh);
     return HC_OK;
 }
 
@@ -243,7 +272,7 @@ hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, vo
     hc_status st = make_plan(d, &p);
     if (st) return st;
     if (!x || !x_ext) return HC_ERR_INVALID_ARG;
-    if (p.S > kMaxKernelShards) return HC_ERR_UNSUPPORTED;
+    if (p.S > kMaxKernelShards || p.Sh > kMaxKernelShards) return HC_ERR_UNSUPPORTED;
     return launch_halo_gather(d, p, x, x_ext, (cudaStream_t)stream);
 }
 

@@ -14,12 +14,18 @@ namespace hc {
 constexpr int kMaxShards = 1024;     // host-side plan
 constexpr int kMaxKernelShards = 64; // shards a kernel takes per-shard tables for
 
-// Host-side shard plan (see hc_shard_plan): uniform block width Wl; the
-// per-shard halo widths and owned output columns.
+// Host-side shard plan (see hc_shard_plan / hc_shard_plan_rows): uniform
+// block width Wl (and height Hl); the per-shard halo widths and owned output
+// columns (rows).  Shard q = a * S + b of the Sh x S grid holds row block a and
+// column block b; Q = Sh * S partials.
 struct Plan {
     int S = 0, Wl = 0, Ho = 0, Wo = 0;
     int We = 0;  // widest extended tile: max_r(halo_left + Wl + halo_right)
+    int Sh = 1, Hl = 0, Hlo = 0;  // row shards, rows per row block, owned output rows per row block
+    int He = 0;                   // tallest extended tile (H with one row shard)
+    int Q = 0;                    // Sh * S
     hc_shard_extent ext[kMaxShards];
+    hc_shard_extent ext_h[kMaxShards];
 };
 
 hc_status make_plan(const hc_conv_desc* d, Plan* p);
@@ -83,8 +89,10 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 // using tmp[bias_grad_ws_floats(Co, S)].
 constexpr int kBiasSlices = 64;
 size_t bias_grad_ws_floats(int Co, int S);
+// gbp [Sh*S][Co]: row shard a owns output rows [a*own_h, (a+1)*own_h) (the last
+// up to Ho), column shard b columns [b*own_w, (b+1)*own_w) (the last up to Wo)
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
-                                    float* tmp, cudaStream_t st);
+                                    int Sh, int own_h, float* tmp, cudaStream_t st);
 
 // out[k] = sum over rows r (ascending, in groups of kColumnGroup) of in[r * stride + k];
 // tmp holds column_sum_tmp_floats(rows, count) floats.

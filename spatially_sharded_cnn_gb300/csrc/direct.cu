@@ -7,7 +7,8 @@
 // an output column owned by shard r reads its halo columns directly from the
 // neighbouring shards' blocks of x (zeros past the image edge); the weight and
 // bias gradients are produced per shard (_Partial) over the shard's own output
-// columns and summed afterwards in shard order.
+// rows and columns (row x column shard grid) and summed afterwards in shard
+// order.
 #include "common.cuh"
 
 namespace hc {
@@ -106,51 +107,68 @@ __device__ float block_sum(float v, float* red) {
 
 // One block per (weight element, shard): the shard's _Partial gradient
 //   gw_part[r, co, ci', u, v] = sum_{n, i, j in own(r)} gy[n,co,i,j] * x[n,ci,i*s-p+u,j*s-p+v]
+// Grid shard q = a * S + b: output rows [a*own_h, ...) (the last row shard up to
+// Ho) and columns [b*own_w, ...) (the last column shard up to Wo).
+struct ShardBox {
+    int S, Sh, own_w, own_h;
+    __device__ __forceinline__ void of(int q, const ConvDims& D, int& i0, int& i1, int& j0, int& j1) const {
+        const int a = q / S, b = q - a * S;
+        i0 = a * own_h;
+        i1 = (a == Sh - 1) ? D.Ho : i0 + own_h;
+        j0 = b * own_w;
+        j1 = (b == S - 1) ? D.Wo : j0 + own_w;
+        if (i1 < i0) i1 = i0;
+        if (j1 < j0) j1 = j0;
+    }
+};
+
+// gw_part[q, co, ci', u, v] = sum_{n, i, j owned by q} gy[n,co,i,j] * x[n,ci,i*s-p+u,j*s-p+v]
 __global__ void direct_gw_partial_kernel(const float* __restrict__ x, const float* __restrict__ gy,
-                                         float* __restrict__ gw_part, ConvDims D, long long wsz, int S, int own_w,
-                                         int last_end) {
+                                         float* __restrict__ gw_part, ConvDims D, long long wsz, ShardBox sb) {
     __shared__ float red[32];
     const long long k = blockIdx.x;
-    const int r = blockIdx.y;
+    const int q = blockIdx.y;
     const int v = (int)(k % D.kw);
     const int u = (int)((k / D.kw) % D.kh);
     const int cl = (int)((k / ((long long)D.kw * D.kh)) % D.Cgi);
     const int co = (int)(k / ((long long)D.kw * D.kh * D.Cgi));
     const int ci = (co / D.Cgo) * D.Cgi + cl;
-    const int j0 = r * own_w, j1 = (r == S - 1) ? last_end : j0 + own_w;
-    const int nj = j1 > j0 ? j1 - j0 : 0;
-    const long long terms = (long long)D.N * D.Ho * nj;
+    int i0, i1, j0, j1;
+    sb.of(q, D, i0, i1, j0, j1);
+    const int nj = j1 - j0, ni = i1 - i0;
+    const long long terms = (long long)D.N * ni * nj;
     float acc = 0.0f;
-    for (long long q = threadIdx.x; q < terms; q += blockDim.x) {
-        const int j = j0 + (int)(q % nj);
-        const int i = (int)((q / nj) % D.Ho);
-        const int n = (int)(q / ((long long)nj * D.Ho));
+    for (long long t = threadIdx.x; t < terms; t += blockDim.x) {
+        const int j = j0 + (int)(t % nj);
+        const int i = i0 + (int)((t / nj) % ni);
+        const int n = (int)(t / ((long long)nj * ni));
         const int h = i * D.s - D.p + u, c = j * D.s - D.p + v;
         if (h < 0 || h >= D.H || c < 0 || c >= D.W) continue;
         acc = fmaf(__ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j),
                    __ldg(x + (((long long)n * D.Ci + ci) * D.H + h) * D.W + c), acc);
     }
     const float t = block_sum(acc, red);
-    if (threadIdx.x == 0) gw_part[(long long)r * wsz + k] = t;
+    if (threadIdx.x == 0) gw_part[(long long)q * wsz + k] = t;
 }
 
-// gb_part[r, co] = sum_{n, i, j in own(r)} gy[n,co,i,j]
+// gb_part[q, co] = sum_{n, i, j owned by q} gy[n,co,i,j]
 __global__ void direct_gb_partial_kernel(const float* __restrict__ gy, float* __restrict__ gb_part, ConvDims D,
-                                         int S, int own_w, int last_end) {
+                                         ShardBox sb) {
     __shared__ float red[32];
-    const int co = blockIdx.x, r = blockIdx.y;
-    const int j0 = r * own_w, j1 = (r == S - 1) ? last_end : j0 + own_w;
-    const int nj = j1 > j0 ? j1 - j0 : 0;
-    const long long terms = (long long)D.N * D.Ho * nj;
+    const int co = blockIdx.x, q = blockIdx.y;
+    int i0, i1, j0, j1;
+    sb.of(q, D, i0, i1, j0, j1);
+    const int nj = j1 - j0, ni = i1 - i0;
+    const long long terms = (long long)D.N * ni * nj;
     float acc = 0.0f;
-    for (long long q = threadIdx.x; q < terms; q += blockDim.x) {
-        const int j = j0 + (int)(q % nj);
-        const int i = (int)((q / nj) % D.Ho);
-        const int n = (int)(q / ((long long)nj * D.Ho));
+    for (long long t = threadIdx.x; t < terms; t += blockDim.x) {
+        const int j = j0 + (int)(t % nj);
+        const int i = i0 + (int)((t / nj) % ni);
+        const int n = (int)(t / ((long long)nj * ni));
         acc += __ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j);
     }
     const float t = block_sum(acc, red);
-    if (threadIdx.x == 0) gb_part[(long long)r * D.Co + co] = t;
+    if (threadIdx.x == 0) gb_part[(long long)q * D.Co + co] = t;
 }
 
 }  // namespace
@@ -173,16 +191,16 @@ hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const flo
                                  float* gw_part, float* gb_part, cudaStream_t st) {
     const ConvDims D = dims_of(d, p);
     const long long wsz = (long long)D.Co * D.Cgi * D.kh * D.kw;
-    const int own_w = p.Wl / d->stride;
+    const ShardBox sb{p.S, p.Sh, p.Wl / d->stride, p.Hlo};
+    if (p.Q > 65535) return HC_ERR_UNSUPPORTED;
     if (gw_part) {
         if (wsz > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        direct_gw_partial_kernel<<<dim3((unsigned)wsz, p.S), 256, 0, st>>>(x, gy, gw_part, D, wsz, p.S, own_w,
-                                                                           p.Wo);
+        direct_gw_partial_kernel<<<dim3((unsigned)wsz, p.Q), 256, 0, st>>>(x, gy, gw_part, D, wsz, sb);
         hc_status s = launched();
         if (s) return s;
     }
     if (gb_part) {
-        direct_gb_partial_kernel<<<dim3(D.Co, p.S), 256, 0, st>>>(gy, gb_part, D, p.S, own_w, p.Wo);
+        direct_gb_partial_kernel<<<dim3(D.Co, p.Q), 256, 0, st>>>(gy, gb_part, D, sb);
         return launched();
     }
     return HC_OK;

@@ -306,9 +306,12 @@ struct BwdArgs {
     float* tile_part;
     int tiles_per_shard;
     int want_wb;
+    int S, Sh, hlo;  // column shards, row shards, rows per row shard (a multiple of TH when Sh > 1)
 };
 
-template <int K>
+// ROWS: row shards present (a.Sh > 1); a separate instantiation so that the
+// one-row-shard kernel carries none of their bookkeeping.
+template <int K, bool ROWS>
 __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
     dw_bwd_kernel(const __grid_constant__ CUtensorMap gymap, const __grid_constant__ CUtensorMap xmap, BwdArgs a,
                   Sched sc) {
@@ -419,9 +422,10 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
                 }
                 correlate_4x4<K>(xs, row0, lane, g, gw);
             }
-            // flush at the end of a (c, column tile) run
+            // flush at the end of a (c, column tile) run; with row shards, at the end of
+            // each row shard of each image (its partial belongs to that grid shard)
             const bool last_tile = t == ntiles - 1;
-            if (last_tile && (!has_next || cn != c || ctn != ct)) {
+            if (ROWS ? ((t + 1) * TH) % a.hlo == 0 : (last_tile && (!has_next || cn != c || ctn != ct))) {
 #pragma unroll
                 for (int u = 0; u < K; u++)
 #pragma unroll
@@ -443,7 +447,8 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
 #pragma unroll
                     for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + tid];
                     const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
-                    float* slot = a.tile_part + (((long long)r * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
+                    const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
+                    float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
                     for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + tid] = m == run_n0 ? tot : 0.0f;
                 }
                 run_n0 = -1;
@@ -538,15 +543,19 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
         sizeof(float) * (2 * NSTAGE * G::TILE + 2 * WSLOT + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(dw_bwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    BwdArgs a{w, gx, tile_part, tps, want_wb ? 1 : 0};
-    dw_bwd_kernel<K><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+    BwdArgs a{w, gx, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
+    if (p.Sh > 1)
+        dw_bwd_kernel<K, true><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+    else
+        dw_bwd_kernel<K, false><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
     s = launched();
     if (s || !want_wb) return s;
-    const long long total = (long long)p.S * d->C_in * (K * K + 1);
-    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, p.S, d->C_in,
+    const long long total = (long long)p.Q * d->C_in * (K * K + 1);
+    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, p.Q, d->C_in,
                                                                              tps * d->N, K * K);
     return launched();
 }
@@ -555,14 +564,17 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
 
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
+    // row shards: the backward splits its weight-gradient runs at row-shard ends,
+    // which must fall on the 64-row tile boundaries
     return d->groups == d->C_in && d->C_out == d->C_in && d->kh == d->kw && (K == 3 || K == 5 || K == 7) &&
            d->stride == 1 && d->padding == (K - 1) / 2 && p.Wl % TW == 0 &&
+           (p.Sh == 1 || p.Hlo % Geo<3, BWD_WARPS>::TH == 0) &&
            (long long)d->N * d->C_in * (d->W / TW) < (1LL << 31);
 }
 
 size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
-    return (size_t)p.S * d->C_in * (p.Wl / TW) * d->N * (K * K + 1);
+    return (size_t)p.Q * d->C_in * (p.Wl / TW) * d->N * (K * K + 1);
 }
 
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,

@@ -68,8 +68,8 @@ extern "C" hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, cons
 
     // scratch layout: [shard gw partials][shard gb partials][tile partials]
     const size_t kk = (size_t)d->kh * d->kw;
-    const size_t gwp_bytes = round_up256(sizeof(float) * p.S * d->C_out * kk);
-    const size_t gbp_bytes = round_up256(sizeof(float) * p.S * d->C_out);
+    const size_t gwp_bytes = round_up256(sizeof(float) * p.Q * d->C_out * kk);
+    const size_t gbp_bytes = round_up256(sizeof(float) * p.Q * d->C_out);
     const size_t tile_bytes = round_up256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
     if (gwp_bytes + gbp_bytes + tile_bytes > kNoAllocScratchBytes) return HC_ERR_WORKSPACE;
 
@@ -83,7 +83,7 @@ extern "C" hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, cons
     cudaStream_t cs = (cudaStream_t)stream;
     const bool want_wb = gw || gb || gw_partials || gb_partials;
     if ((st = launch_depthwise_bwd(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_wb, cs))) return st;
-    if (gw && (st = launch_sum_rows(gwp, gw, p.S, (long long)(d->C_out * kk), cs))) return st;
-    if (gb && (st = launch_sum_rows(gbp, gb, p.S, d->C_out, cs))) return st;
+    if (gw && (st = launch_sum_rows(gwp, gw, p.Q, (long long)(d->C_out * kk), cs))) return st;
+    if (gb && (st = launch_sum_rows(gbp, gb, p.Q, d->C_out, cs))) return st;
     return HC_OK;
 }

@@ -22,19 +22,23 @@ __global__ void sum_rows_kernel(const float* __restrict__ in, float* __restrict_
     }
 }
 
-// Bias-gradient partial sums, stage 1: block (slice, co) streams whole rows
-// (n, i) of its slice of grad_output channel co with 16-byte loads, 1024
-// columns at a time: each thread sums its four columns down the rows, then
-// thread r adds the column sums of shard r (shard of column j = j / own_w, the
-// last shard taking the rest) in column order.  Every sum has a fixed order.
-// part[(slice * S + r) * Co + co].  Needs Wo % 4 == 0, S <= 256, 256 threads.
+// Bias-gradient partial sums, stage 1: block (row shard a, slice, co) streams
+// whole output rows (n, i), i among row shard a's rows, of its slice of
+// grad_output channel co with 16-byte loads, 1024 columns at a time: each thread
+// sums its four columns down the rows, then thread b adds the column sums of
+// column shard b (shard of column j = j / own_w, the last shard taking the
+// rest) in column order.  Every sum has a fixed order.
+// part[(slice * Sh * S + a * S + b) * Co + co].  Needs Wo % 4 == 0, S <= 256,
+// 256 threads.
 __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict__ gy, float* __restrict__ part, int N,
-                                                        int Co, int Ho, int Wo, int S, int own_w, int slices) {
+                                                        int Co, int Ho, int Wo, int S, int own_w, int Sh, int own_h,
+                                                        int slices) {
     __shared__ float cs[256];
-    const int slice = blockIdx.x, co = blockIdx.y, tid = threadIdx.x;
-    const int nrows = N * Ho;
+    const int a = blockIdx.x / slices, slice = blockIdx.x - a * slices, co = blockIdx.y, tid = threadIdx.x;
+    const int i0 = a * own_h, i1 = (a == Sh - 1) ? Ho : i0 + own_h, rows_a = i1 - i0;
+    const int nrows = N * rows_a;
     const int r0 = (int)((long long)nrows * slice / slices), r1 = (int)((long long)nrows * (slice + 1) / slices);
-    float total = 0.0f;  // thread r < S: shard r's running sum
+    float total = 0.0f;  // thread b < S: column shard b's running sum
     for (int g0 = 0; g0 < Wo; g0 += 1024) {
         const int col = g0 + 4 * tid;
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -45,7 +49,7 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
                 float4 v[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const int n = (row + k) / Ho, i = row + k - n * Ho;
+                    const int n = (row + k) / rows_a, i = i0 + row + k - n * rows_a;
                     v[k] = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
                 }
 #pragma unroll
@@ -57,7 +61,7 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
                 }
             }
             for (; row < r1; row++) {
-                const int n = row / Ho, i = row - n * Ho;
+                const int n = row / rows_a, i = i0 + row - n * rows_a;
                 const float4 v = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
                 acc.x += v.x;
                 acc.y += v.y;
@@ -69,12 +73,12 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
         __syncthreads();
         if (tid < S) {
             const int j0 = tid * own_w, j1 = (tid == S - 1) ? Wo : j0 + own_w;
-            const int a = (j0 > g0 ? j0 : g0), b = (j1 < g0 + 1024 ? j1 : g0 + 1024);
-            for (int k = a; k < b; k += 4) total += cs[(k - g0) / 4];
+            const int lo = (j0 > g0 ? j0 : g0), hi = (j1 < g0 + 1024 ? j1 : g0 + 1024);
+            for (int k = lo; k < hi; k += 4) total += cs[(k - g0) / 4];
         }
         __syncthreads();
     }
-    if (tid < S) part[((long long)slice * S + tid) * Co + co] = total;
+    if (tid < S) part[((long long)slice * Sh * S + (long long)a * S + tid) * Co + co] = total;
 }
 
 // Column sums, stage 1: tmp[g][k] = sum over rows r in group g (ascending) of
@@ -112,18 +116,21 @@ hc_status launch_column_sum(const float* in, float* out, int rows, int count, lo
 size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co; }
 
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
-                                    float* tmp, cudaStream_t st) {
-    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || (long long)N * Ho > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-    // about eight blocks per SM, at most kBiasSlices slices
-    const long long nrows = (long long)N * Ho;
-    long long slices = (152LL * 8 + Co - 1) / Co;
+                                    int Sh, int own_h, float* tmp, cudaStream_t st) {
+    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || Sh < 1 || (long long)N * Ho > 0x7fffffffLL)
+        return HC_ERR_UNSUPPORTED;
+    // about eight blocks per SM, at most kBiasSlices slices per row shard
+    const long long rows_min = (long long)N * (Sh > 1 ? own_h : Ho);
+    long long slices = (152LL * 8 + (long long)Co * Sh - 1) / ((long long)Co * Sh);
     if (slices > kBiasSlices) slices = kBiasSlices;
-    if (slices > nrows) slices = nrows;
+    if (slices > rows_min) slices = rows_min;
     if (slices < 1) slices = 1;
-    bias_rows_kernel<<<dim3((unsigned)slices, Co), 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, (int)slices);
+    if ((long long)slices * Sh > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+    bias_rows_kernel<<<dim3((unsigned)(slices * Sh), Co), 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h,
+                                                                          (int)slices);
     hc_status s = launched();
     if (s) return s;
-    return launch_sum_rows(tmp, gbp, (int)slices, (long long)S * Co, st);  // slices in order
+    return launch_sum_rows(tmp, gbp, (int)slices, (long long)Sh * S * Co, st);  // slices in order
 }
 
 hc_status launch_sum_rows(const float* in, float* out, int rows, long long count, cudaStream_t st) {

@@ -199,9 +199,10 @@ struct TcParams {
     float* out;     // NCHW [N][M][Ho][Wo], or with d2s > 0 the image [N][d2s_c][Ho*d2s][Wo*d2s]
     int d2s, d2s_c; // depth-to-space store: row m = (u*d2s + v)*d2s_c + c goes to pixel (ho*d2s+u, wo*d2s+v)
     // wgrad mode
-    int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // row_chunks = own_w / BK
+    int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // S: grid shards Sh*Sw; row_chunks = own_w / BK
+    int Sw, own_h;  // column shards; owned output rows per row shard (shard q = a*Sw + b)
     int slots;      // taps * nblocks: (tap, 128-channel block) pairs; a unit covers two slots
-    long long shard_chunks;                               // N * Ho * row_chunks
+    long long shard_chunks;                               // N * own_h * row_chunks
     float* part;    // [S][J][taps][Co][Ci]
 };
 
@@ -310,10 +311,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // taps of one column strip reuse its rows while they are still in L2; the
                     // tap's column shift s = v - pad is read from the copy shifted right by
                     // jc = (-s) mod 4
-                    const int ho = (int)(c % p.Ho);
-                    const long long rest = c / p.Ho;
+                    const int qa = u.r / p.Sw, qb = u.r - qa * p.Sw;  // row and column shard
+                    const int ho = qa * p.own_h + (int)(c % p.own_h);
+                    const long long rest = c / p.own_h;
                     const int wc = (int)(rest % p.row_chunks), n = (int)(rest / p.row_chunks);
-                    const int w = u.r * p.own_w + wc * BK;
+                    const int w = qb * p.own_w + wc * BK;
                     tma_5d(st, &amap, w, u.m0, ho, n, 0, &sh.full[s]);  // [hi][lo] x 128 rows
                     // B = the hi rows of both slots, then their lo rows (one N = 256 operand
                     // pair); a slot is (tap, 128-channel block); the copy index jc and the
@@ -1071,8 +1073,8 @@ int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
     const bool sd = is_s2d(d);
     const int KK = sd ? 1 : d->kh * d->kw;
     const int nb = sd ? s2d_kp(d) / WG_SLOT : d->C_in / WG_SLOT;
-    const long long units0 = (long long)(d->C_out / BM) * ((KK * nb + 1) / 2) * p.S;
-    const long long chunks = (long long)d->N * p.Ho * ((p.Wl / d->stride) / BK);
+    const long long units0 = (long long)(d->C_out / BM) * ((KK * nb + 1) / 2) * p.Q;
+    const long long chunks = (long long)d->N * p.Hlo * ((p.Wl / d->stride) / BK);
     // Units are equally long, so the persistent grid runs ceil(units / SMs) waves.
     // Take the smallest split that fills every SM and keeps the last wave at least
     // 95 % full (each unit at least 2048 pixels long); else the best-filled split.
@@ -1099,7 +1101,7 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
         const size_t npx = (size_t)d->N * p.Ho * p.Wo, kp = s2d_kp(d);
         const size_t ns = npx * kp, ng = npx * d->C_out, wsz = (size_t)d->C_out * kp;
         if (pass == 0) return 2 * al256(4 * ns) + 2 * al256(4 * wsz);
-        const size_t part = al256(4 * (size_t)p.S * tc_wgrad_splits(d, p) * wsz);
+        const size_t part = al256(4 * (size_t)p.Q * tc_wgrad_splits(d, p) * wsz);
         return 4 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ns) + part;
     }
     const int KK = d->kh * d->kw;
@@ -1109,7 +1111,7 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     if (pass == 0) return 2 * al256(4 * nx) + 2 * al256(4 * wsz);
     const size_t nsh = (size_t)shift_copies(d) * d->N * d->C_in * d->H * shift_pitch(d);
     const int J = tc_wgrad_splits(d, p);
-    const size_t part = al256(4 * (size_t)p.S * J * wsz);
+    const size_t part = al256(4 * (size_t)p.Q * J * wsz);
     return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
 }
 
@@ -1271,7 +1273,9 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         tp.mode = 1;
         tp.Co = Co;
         tp.Ci = Kp;
-        tp.S = p.S;
+        tp.S = p.Q;
+        tp.Sw = p.S;
+        tp.own_h = p.Hlo;
         tp.J = tc_wgrad_splits(d, p);
         tp.own_w = p.Wl / s;
         tp.row_chunks = tp.own_w / BK;
@@ -1283,8 +1287,8 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
         tp.mblocks = Co / BM;
         tp.nblocks = Kp / WG_SLOT;
         tp.slots = tp.nblocks;
-        tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
-        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
+        tp.shard_chunks = (long long)d->N * p.Hlo * tp.row_chunks;
+        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.Q;
         tp.part = part;
         tp.N = d->N;
         CUtensorMap ma, mb;
@@ -1292,8 +1296,8 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
             (e = shifted_map(&mb, sh, sl, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)))
             return e;
         if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
-        const long long total = (long long)p.S * Co * Ci * s * s;
-        wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, Co, Ci, s, Kp);
+        const long long total = (long long)p.Q * Co * Ci * s * s;
+        wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, Co, Ci, s, Kp);
         if ((e = launched())) return e;
     }
     return HC_OK;
@@ -1408,7 +1412,9 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.mode = 1;
         tp.Co = Co;
         tp.Ci = Ci;
-        tp.S = p.S;
+        tp.S = p.Q;
+        tp.Sw = p.S;
+        tp.own_h = p.Hlo;
         tp.J = tc_wgrad_splits(d, p);
         tp.own_w = p.Wl;
         tp.row_chunks = p.Wl / BK;
@@ -1420,8 +1426,8 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.mblocks = Co / BM;
         tp.nblocks = Ci / WG_SLOT;
         tp.slots = KK * tp.nblocks;
-        tp.shard_chunks = (long long)d->N * p.Ho * tp.row_chunks;
-        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.S;
+        tp.shard_chunks = (long long)d->N * p.Hlo * tp.row_chunks;
+        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.Q;
         tp.part = part;
         tp.N = d->N;
         CUtensorMap ma, mb;
@@ -1429,8 +1435,8 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
             (s = shifted_map(&mb, sh, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
             return s;
         if ((s = launch_conv_pass(WG_BN, ma, mb, tp, st))) return s;
-        const long long total = (long long)p.S * wsz;
-        wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.S, tp.J, KK, Co, Ci);
+        const long long total = (long long)p.Q * wsz;
+        wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, KK, Co, Ci);
         if ((s = launched())) return s;
     }
     return HC_OK;

@@ -27,7 +27,8 @@ HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32 = range(4)
 
 class hc_conv_desc(C.Structure):
     _fields_ = [(n, C.c_int) for n in
-                ("N", "C_in", "H", "W", "C_out", "kh", "kw", "stride", "padding", "groups", "num_shards")]
+                ("N", "C_in", "H", "W", "C_out", "kh", "kw", "stride", "padding", "groups", "num_shards",
+                 "num_shards_h")]
 
 
 class hc_shard_extent(C.Structure):
@@ -42,8 +43,8 @@ class HcError(RuntimeError):
 
 
 def desc(cfg: dict) -> hc_conv_desc:
-    """hc_conv_desc from a dict with the field names of the C struct."""
-    return hc_conv_desc(*(int(cfg[k]) for k, _ in hc_conv_desc._fields_))
+    """hc_conv_desc from a dict with the field names of the C struct (num_shards_h defaults to 1)."""
+    return hc_conv_desc(*(int(cfg.get(k, 1) if k == "num_shards_h" else cfg[k]) for k, _ in hc_conv_desc._fields_))
 
 
 def _ptr(t):
@@ -65,6 +66,7 @@ def _stream(s):
 _P = C.c_void_p
 _D = C.POINTER(hc_conv_desc)
 _lib.hc_shard_plan.argtypes = [_D, C.POINTER(hc_shard_extent), C.POINTER(C.c_int), C.POINTER(C.c_int)]
+_lib.hc_shard_plan_rows.argtypes = [_D, C.POINTER(hc_shard_extent)]
 _lib.hc_conv2d_workspace_size.argtypes = [_D, C.c_int, C.POINTER(C.c_size_t)]
 _lib.hc_conv2d_workspace_size_algo.argtypes = [_D, C.c_int, C.c_int, C.POINTER(C.c_size_t)]
 _lib.hc_conv2d_select.argtypes = [_D, C.c_int, C.POINTER(C.c_int)]
@@ -106,7 +108,8 @@ _lib.hc_selftest_timeout.restype = C.c_int
 _lib.hc_status_string.argtypes = [C.c_int]
 _lib.hc_status_string.restype = C.c_char_p
 _lib.hc_launch_count.restype = C.c_ulonglong
-for _n in ("hc_shard_plan", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo", "hc_conv2d_select",
+for _n in ("hc_shard_plan", "hc_shard_plan_rows", "hc_conv2d_workspace_size", "hc_conv2d_workspace_size_algo",
+           "hc_conv2d_select",
            "hc_conv2d_fwd", "hc_conv2d_fwd_algo", "hc_conv2d_bwd", "hc_conv2d_bwd_algo", "hc_halo_gather",
            "hc_sync_check"):
     getattr(_lib, _n).restype = C.c_int
@@ -118,7 +121,7 @@ EXPORTS = [
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
-    "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd",
+    "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows",
 ]
 
 
@@ -134,6 +137,16 @@ def hc_shard_plan(d: hc_conv_desc):
     if st:
         return st, None, None, None
     return st, [tuple(getattr(e, f) for f, _ in hc_shard_extent._fields_) for e in ext[:d.num_shards]], ho.value, wo.value
+
+
+def hc_shard_plan_rows(d: hc_conv_desc):
+    """Returns (status, [row extent tuples])."""
+    Sh = max(1, d.num_shards_h)
+    ext = (hc_shard_extent * Sh)()
+    st = _lib.hc_shard_plan_rows(C.byref(d), ext)
+    if st:
+        return st, None
+    return st, [tuple(getattr(e, f) for f, _ in hc_shard_extent._fields_) for e in ext]
 
 
 def hc_conv2d_workspace_size(d: hc_conv_desc, pass_: int, algo: int | None = None):

@@ -61,9 +61,14 @@ def fwd(cfg, x, w, b, algo=None):
     return y.numpy()
 
 
+def num_partials(cfg):
+    """Grid shards Q = num_shards * num_shards_h (the partial count)."""
+    return cfg["num_shards"] * max(1, int(cfg.get("num_shards_h", 1)))
+
+
 def bwd(cfg, x, w, gy, algo=None, partials=True):
     d = hc.desc(cfg)
-    S = cfg["num_shards"]
+    S = num_partials(cfg)
     wshape = (cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"])
     gx = Guarded(x.shape)
     gw = Guarded(wshape)
@@ -85,7 +90,7 @@ def bwd_subset(cfg, x, w, gy, want, algo=None):
     """Backward with only the outputs named in `want` (subset of gx, gw, gb,
     gw_partials, gb_partials); the others are passed as NULL."""
     d = hc.desc(cfg)
-    S = cfg["num_shards"]
+    S = num_partials(cfg)
     wshape = (cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"])
     shapes = dict(gx=x.shape, gw=wshape, gb=(cfg["C_out"],), gw_partials=(S,) + wshape,
                   gb_partials=(S, cfg["C_out"]))

@@ -64,6 +64,20 @@ def test_plan_matches_oracle(hc, orc):
         assert ext == plan and (Ho, Wo) == (oHo, oWo), cfg
 
 
+def test_row_plan_matches_oracle(hc, orc):
+    for H, Sh, k, s, p in itertools.product((8, 12, 16, 24), (0, 1, 2, 3, 4), (1, 2, 3, 5), (1, 2), (0, 1, 2)):
+        cfg = dict(P.cfg_of(1, 2, H, 16, 2, k, s, p, 1, 2), num_shards_h=Sh)
+        if H + 2 * p < k:
+            continue
+        st, ext = hc.hc_shard_plan_rows(hc.desc(cfg))
+        rc, plan = orc.shard_plan_h(cfg)
+        rcw = orc.shard_plan(cfg)[0]
+        if rc or rcw:
+            assert st == hc.HC_ERR_UNSUPPORTED, (cfg, st, rc, rcw)
+            continue
+        assert st == hc.HC_OK and ext == plan, (cfg, ext, plan)
+
+
 def test_plan_pages_example(hc):
     # (7,3,512,2048) over 4 shards -> 4 blocks of 512 columns; 5x5/p2/s1 -> 2-column halos
     st, ext, Ho, Wo = hc.hc_shard_plan(hc.desc(P.cfg_of(7, 3, 512, 2048, 3, 5, 1, 2, 1, 4)))

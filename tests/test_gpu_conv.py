@@ -99,7 +99,18 @@ CASES = {
     "tc_5x5_S4_tiles_cross_shards": lambda: tc_case(1, 128, 5, 512, 128, 5, 4),
     # 2048 columns: the bias partials walk two 1024-column groups, 8 shards
     "tc_3x3_wide_S8": lambda: tc_case(1, 128, 2, 2048, 128, 3, 8),
+    # row x column shard grids (Shard(2) and Shard(3) together)
+    "tc_5x5_grid_2x2": lambda: _rows(tc_case(1, 128, 8, 256, 128, 5, 2), 2),
+    "tc_down2x2s2_grid_2x2": lambda: _rows(tc_strided_case(1, 128, 8, 512, 256, 2, 2), 2),
+    "dw7_grid_2x2": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 2),          # 64-row shards: depthwise
+    "dw7_grid_4x2_direct": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 4),   # 32-row shards: direct
+    "grouped_strided_grid_3x2": lambda: _rows(generic_case(P.cfg_of(2, 6, 12, 16, 4, 3, 2, 2, 2, 2)), 3),
 }
+
+
+def _rows(case, Sh):
+    cfg, *rest = case
+    return (dict(cfg, num_shards_h=Sh), *rest)
 
 
 def check_case(hc, orc, cfg, x, w, b, gy, algo=None):
@@ -128,6 +139,16 @@ def test_parity_auto(hc, orc, name):
 @pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "stem4x4s4"])
 def test_parity_direct(hc, orc, name):
     check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_DIRECT)
+
+
+def test_grid_family_choice(hc):
+    """Row shards keep the depthwise kernels when each row shard is whole 64-row
+    tiles, and fall back to the direct kernels otherwise."""
+    sel = lambda n: hc.hc_conv2d_select(hc.desc(CASES[n]()[0]), 1)
+    assert sel("dw7_grid_2x2") == (0, hc.HC_ALGO_DEPTHWISE)
+    assert sel("dw7_grid_4x2_direct") == (0, hc.HC_ALGO_DIRECT)
+    assert sel("tc_5x5_grid_2x2") == (0, hc.HC_ALGO_TC_3XTF32)
+    assert sel("tc_down2x2s2_grid_2x2") == (0, hc.HC_ALGO_TC_3XTF32)
 
 
 @pytest.mark.parametrize("name", ["dw7_ragged_S4", "dw5_S2", "dw3_S4"])
@@ -176,21 +197,27 @@ def test_deterministic(hc, name):
 
 
 @pytest.mark.parametrize("cfg", [P.cfg_of(2, 3, 5, 32, 3, 5, 1, 2, 1, 4), P.cfg_of(1, 2, 4, 48, 2, 7, 1, 3, 2, 4),
-                                 P.cfg_of(1, 2, 3, 16, 2, 3, 2, 2, 1, 2), P.cfg_of(1, 2, 3, 16, 2, 2, 2, 0, 1, 8)])
+                                 P.cfg_of(1, 2, 3, 16, 2, 3, 2, 2, 1, 2), P.cfg_of(1, 2, 3, 16, 2, 2, 2, 0, 1, 8),
+                                 dict(P.cfg_of(2, 3, 12, 32, 3, 5, 1, 2, 1, 4), num_shards_h=3),
+                                 dict(P.cfg_of(1, 2, 16, 16, 2, 3, 2, 2, 1, 2), num_shards_h=2)])
 def test_halo_gather_bit_exact(hc, orc, cfg):
     x = synth.normal((cfg["N"], cfg["C_in"], cfg["H"], cfg["W"]), 1.0, 3, 1)
     d = hc.desc(cfg)
     st, plan, _, _ = hc.hc_shard_plan(d)
+    st2, plan_h = hc.hc_shard_plan_rows(d)
+    assert st == 0 and st2 == 0
     We = max(e[2] + (e[1] - e[0]) + e[3] for e in plan)
-    xe = R.Guarded((cfg["num_shards"], cfg["N"], cfg["C_in"], cfg["H"], We))
+    He = max(f[2] + (f[1] - f[0]) + f[3] for f in plan_h)
+    Q = len(plan) * len(plan_h)
+    xe = R.Guarded((Q, cfg["N"], cfg["C_in"], He, We))
     hc.check(hc.hc_halo_gather(d, R.dev(x), xe.view), "halo")
     hc.check(hc.hc_sync_check(), "halo sync")
     got = xe.numpy()
-    for r, e in enumerate(plan):
-        ref = orc.halo_extend(cfg, r, x)
-        wr = ref.shape[-1]
-        assert np.array_equal(got[r, ..., :wr], ref), r
-        assert np.all(got[r, ..., wr:] == 0)
+    for q in range(Q):
+        ref = orc.halo_extend(cfg, q, x)
+        hr, wr = ref.shape[-2:]
+        assert np.array_equal(got[q, :, :, :hr, :wr], ref), q
+        assert np.all(got[q, :, :, hr:, :] == 0) and np.all(got[q, :, :, :, wr:] == 0)
 
 
 @pytest.mark.parametrize("K,S,groups", [(7, 4, "dw"), (5, 4, "dw"), (3, 2, "dw"), (5, 4, "dense"), (3, 2, "dense")])
