@@ -133,6 +133,7 @@ class ConvWorkload:
         c = self.cfg
         return {"workload": self.desc, "shape": [c["N"], c["C_in"], c["H"], c["W"]], "kernel": [c["kh"], c["kw"]],
                 "padding": c["padding"], "groups": c["groups"], "num_shards": c["num_shards"],
+                "num_shards_h": c.get("num_shards_h", 1),
                 "l2": "inputs (470 MB each) larger than L2; no flush" if self.name != "config1" else
                       "inputs L2-resident (8 KB); launch-latency bound, no flush"}
 
@@ -414,9 +415,20 @@ class DwDownWorkload:
                 "ms_per_launch": ops_ms["dw_bwd"]}
 
 
-def make_workload(name, batch=None, drop_path=0.0):
-    """batch overrides N of the single-conv workloads (smaller cases for profiling)."""
+def make_workload(name, batch=None, drop_path=0.0, shards_h=1):
+    """batch overrides N of the single-conv workloads (smaller cases for profiling);
+    shards_h > 1 also splits their rows (a row x column shard grid)."""
     N = batch or 7
+    wl = _make_workload(name, N, drop_path)
+    if shards_h > 1:
+        if not isinstance(wl, ConvWorkload):
+            raise SystemExit("--shards-h applies to the single-conv workloads")
+        wl.cfg = dict(wl.cfg, num_shards_h=shards_h)
+        wl.desc += f", {shards_h} H-shards (a {shards_h} x {wl.cfg['num_shards']} shard grid)"
+    return wl
+
+
+def _make_workload(name, N, drop_path):
     if name == "dw7":
         return ConvWorkload("dw7", conv_cfg(N, 256, 128, 512, 256, 7, 1, 3, 256, 4), lambda: gen_dw7(N), "GB/s",
                             f"depthwise 7x7 conv fwd+bwd, x ({N},256,128,512) fp32, 4 W-shards of width 128")
@@ -560,6 +572,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
+    ap.add_argument("--shards-h", type=int, default=1,
+                    help="single-conv workloads: also split the rows into this many shards")
     ap.add_argument("--drop-path", type=float, default=0.0,
                     help="block workload: DropPath probability (per-sample, shard-consistent draw each step)")
     ap.add_argument("--graph", action="store_true",
@@ -569,7 +583,7 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
-    wl = make_workload(args.workload, args.batch, args.drop_path)
+    wl = make_workload(args.workload, args.batch, args.drop_path, args.shards_h)
 
     import torch
     import torch.distributed as dist

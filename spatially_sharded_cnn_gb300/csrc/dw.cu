@@ -330,13 +330,38 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
     const int jobs = (i1 - i0) * ntiles;
     const bool want_wb = a.want_wb != 0;
 
+    // Job q -> (item, row tile t).  Items run (c, column tile, n), n fastest; a
+    // run is this CTA's items of one (c, column tile).  Without row shards the
+    // jobs go item by item, tile by tile.  With row shards a run's jobs go row
+    // shard by row shard, each over all the run's images, so the weight
+    // gradient of one (run, row shard) accumulates in registers and is flushed
+    // once; seg_end marks the last job of such a segment.
+    auto job = [&](int q, int& item, int& t, bool& seg_end) {
+        if (!ROWS) {
+            item = i0 + q / ntiles;
+            t = q - (item - i0) * ntiles;
+            seg_end = false;
+            return;
+        }
+        const int g = (i0 + q / ntiles) / sc.N;
+        const int rs = i0 > g * sc.N ? i0 : g * sc.N, re = i1 < (g + 1) * sc.N ? i1 : (g + 1) * sc.N;
+        const int R = re - rs, tpr = ntiles / a.Sh;
+        const int jr = q - (rs - i0) * ntiles;
+        const int seg = jr / (R * tpr), rest = jr - seg * R * tpr;
+        item = rs + rest / tpr;
+        t = seg * tpr + rest % tpr;
+        seg_end = rest == R * tpr - 1;
+    };
+
     auto issue = [&](int q) {
-        int n, c, ct;
-        sc.decode(i0 + q / ntiles, n, c, ct);
+        int n, c, ct, item, t;
+        bool se;
+        job(q, item, t, se);
+        sc.decode(item, n, c, ct);
         uint64_t* bar = full + (q % NSTAGE);
         float* st = tiles + (q % NSTAGE) * 2 * G::TILE;
         mbar_expect_tx(bar, want_wb ? 2 * G::BYTES : G::BYTES);
-        const int x0 = ct * TW - 4, y0 = (q % ntiles) * TH - P, z = n * sc.C + c;
+        const int x0 = ct * TW - 4, y0 = t * TH - P, z = n * sc.C + c;
         tma_load_3d(st, &gymap, x0, y0, z, bar);
         if (want_wb) tma_load_3d(st + G::TILE, &xmap, x0, y0, z, bar);
     };
@@ -363,13 +388,19 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
     int cur_c = -1;
     int run_n0 = -1;  // first image of the current (c, column tile) run
     for (int q = 0; q < jobs; q++) {
-        const int t = q % ntiles;
-        int n, c, ct;
-        sc.decode(i0 + q / ntiles, n, c, ct);
+        int n, c, ct, item, t;
+        bool seg_end;
+        job(q, item, t, seg_end);
+        sc.decode(item, n, c, ct);
         if (run_n0 < 0) run_n0 = n;
         const bool has_next = q + 1 < jobs;
         int nn = 0, cn = c, ctn = ct;
-        if (has_next) sc.decode(i0 + (q + 1) / ntiles, nn, cn, ctn);
+        if (has_next) {
+            int item2, t2;
+            bool se2;
+            job(q + 1, item2, t2, se2);
+            sc.decode(item2, nn, cn, ctn);
+        }
         if (has_next && tid < KK) cp_async4(wsm + ((q + 1) & 1) * WSLOT + tid, a.w + cn * KK + tid);
         if (c != cur_c) {
             const float* ws = wsm + (q & 1) * WSLOT;
@@ -423,9 +454,9 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
                 correlate_4x4<K>(xs, row0, lane, g, gw);
             }
             // flush at the end of a (c, column tile) run; with row shards, at the end of
-            // each row shard of each image (its partial belongs to that grid shard)
+            // each row-shard segment of the run (its partial belongs to that grid shard)
             const bool last_tile = t == ntiles - 1;
-            if (ROWS ? ((t + 1) * TH) % a.hlo == 0 : (last_tile && (!has_next || cn != c || ctn != ct))) {
+            if (ROWS ? seg_end : (last_tile && (!has_next || cn != c || ctn != ct))) {
 #pragma unroll
                 for (int u = 0; u < K; u++)
 #pragma unroll
