@@ -72,7 +72,19 @@ typedef enum {
     HC_ALGO_AUTO = 0,
     HC_ALGO_DIRECT = 1,       /* plain direct convolution, any groups / stride  */
     HC_ALGO_DEPTHWISE = 2,    /* groups == C, odd k, stride 1, padding (k-1)/2  */
-    HC_ALGO_TC_3XTF32 = 3     /* groups == 1: tcgen05 implicit GEMM, 3xTF32     */
+    HC_ALGO_TC_3XTF32 = 3,    /* groups == 1: tcgen05 implicit GEMM, 3xTF32     */
+    HC_ALGO_TC_BF16X6 = 4     /* groups 1, padding 0, C_out a multiple of 128,
+                                 W_out % 8 == 0, W / num_shards / stride a
+                                 multiple of 32, and either
+                                 1x1 / stride 1 with C_in a multiple of 128 and
+                                 H*W a multiple of 128, or
+                                 k = stride <= 4 (space-to-depth) with
+                                 stride^2 * C_in a multiple of 8 and W_out a
+                                 multiple of 128:
+                                 tcgen05 GEMM on three bf16 pieces per operand
+                                 (a = a0 + a1 + a2, six products a_i*b_j with
+                                 i + j <= 2, fp32 accumulation), operands in
+                                 NCHW order with no transposed copies           */
 } hc_algo;
 
 /* Shard(3) plan (NVIDIA blog, design section; kwkr.cn 2.1 and 2.2).

@@ -96,12 +96,14 @@ static bool algo_supported(const hc_conv_desc* d, const Plan& p, hc_algo a) {
         case HC_ALGO_DIRECT: return true;
         case HC_ALGO_DEPTHWISE: return depthwise_supported(d, p);
         case HC_ALGO_TC_3XTF32: return tc_supported(d, p);
+        case HC_ALGO_TC_BF16X6: return bf16_supported(d, p);
         default: return false;
     }
 }
 
 static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
     if (depthwise_supported(d, p)) return HC_ALGO_DEPTHWISE;
+    if (bf16_supported(d, p)) return HC_ALGO_TC_BF16X6;
     if (tc_supported(d, p)) return HC_ALGO_TC_3XTF32;
     return HC_ALGO_DIRECT;
 }
@@ -109,16 +111,21 @@ static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
 // Workspace layout of the backward pass (bytes, each piece 256-aligned):
 //   DIRECT:    [gw partials S*wsize][gb partials S*C_out]
 //   DEPTHWISE: [gw partials S*C*K*K][gb partials S*C][tile partials]
-//   TC_3XTF32: [gw partials][gb partials][NHWC hi/lo copies, weights hi/lo, split-K partials]
+//   TC_3XTF32: [gw partials][gb partials][bias scratch][NHWC hi/lo copies, weights hi/lo, split-K partials]
+//   TC_BF16X6: [gw partials][gb partials][bias scratch][bf16 pieces of gy, w^T, x; split-K partials]
 static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
     size_t b = round256(sizeof(float) * p.Q * wsize(d)) + round256(sizeof(float) * p.Q * d->C_out);
     if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
     if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + tc_ws_bytes(d, p, 1);
+    if (a == HC_ALGO_TC_BF16X6)
+        b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + bf16_ws_bytes(d, p, 1);
     return b;
 }
 
 static size_t fwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
-    return a == HC_ALGO_TC_3XTF32 ? tc_ws_bytes(d, p, 0) : 0;
+    if (a == HC_ALGO_TC_3XTF32) return tc_ws_bytes(d, p, 0);
+    if (a == HC_ALGO_TC_BF16X6) return bf16_ws_bytes(d, p, 0);
+    return 0;
 }
 
 static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* bytes) {
@@ -146,6 +153,7 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
     cudaStream_t s = (cudaStream_t)stream;
     switch (a) {
         case HC_ALGO_TC_3XTF32: return launch_tc_fwd(d, p, x, w, b, y, ws, s);
+        case HC_ALGO_TC_BF16X6: return launch_bf16_fwd(d, p, x, w, b, y, ws, s);
         case HC_ALGO_DEPTHWISE: return launch_depthwise_fwd(d, p, x, w, b, y, s);
         case HC_ALGO_DIRECT: return launch_direct_fwd(d, p, x, w, b, y, s);
         default: return HC_ERR_UNSUPPORTED;
@@ -180,10 +188,15 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
         case HC_ALGO_DEPTHWISE:
             st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s);
             break;
-        case HC_ALGO_TC_3XTF32: {
+        case HC_ALGO_TC_3XTF32:
+        case HC_ALGO_TC_BF16X6: {
             float* btmp = (float*)wsp;
             wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q));
-            if ((gx || want_w) && (st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s))) return st;
+            if (gx || want_w) {
+                st = a == HC_ALGO_TC_BF16X6 ? launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s)
+                                            : launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
+                if (st) return st;
+            }
             if (want_b)
                 st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl / d->stride, p.Sh, p.Hlo,
                                                btmp, s);

@@ -85,6 +85,15 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
                         float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st);
 
+// 1x1 conv (stride 1, padding 0, groups 1) on tcgen05 with three bf16 pieces per
+// operand (six products, fp32 accuracy); C_in and C_out multiples of 128
+bool bf16_supported(const hc_conv_desc* d, const Plan& p);
+size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
+hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                          float* y, void* ws, cudaStream_t st);
+hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
+                          float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st);
+
 // Per-shard bias-gradient partials gbp[S][Co] in two fixed-order stages,
 // using tmp[bias_grad_ws_floats(Co, S)].
 constexpr int kBiasSlices = 64;

@@ -33,6 +33,16 @@
 //          128-channel) slots side by side: N = 256 accumulator columns.
 // All operands are K-major tiles with the 128-byte swizzle (32 tf32 per row).
 //
+// 1x1 convolutions (stride 1, no padding) take a second operand format: every
+// value is split into three bf16 pieces, a = a0 + a1 + a2 with a0 = bf16(a),
+// a1 = bf16(a - a0), a2 = bf16(a - a0 - a1) (both differences are exact in
+// fp32), and each product is taken as the six terms a_i*b_j with i + j <= 2
+// (the dropped terms are below 2^-24 of |a*b|).  Six bf16 MMAs cost the tensor
+// time of three tf32 ones, and 16-bit operands may be MN-major, so the pieces
+// keep the NCHW order of the tensors they come from: the conv passes read
+// pixels as MN-major B tiles, the weight gradient reads them as K-major tiles,
+// and no pass needs a transposed copy.
+//
 // Accuracy: the tensor core's fp32 accumulation loses about one unit in the
 // last place per MMA step, so a long K would lose ~1e-5.  The MMA warp
 // therefore accumulates groups of 256 k-values (96 MMAs) in one of two TMEM
@@ -45,6 +55,8 @@
 // bounded: on timeout the CTA records HC_ERR_TIMEOUT, drains its outstanding
 // copies and MMAs, frees its tensor memory and exits.
 #include "common.cuh"
+
+#include <cuda_bf16.h>
 
 namespace hc {
 namespace {
@@ -60,6 +72,8 @@ constexpr int TC_STAGE_OUT = 4096;  // per epilogue warp: a 32 x 32 fp32 output 
 constexpr int WG_BN = 256;
 constexpr int WG_SLOT = 128;
 constexpr uint32_t WG_SLOT_BYTES = WG_SLOT * 128;  // one slot's hi (or lo) tile: 128 rows x 32 tf32
+constexpr int BKH = 32;             // bf16 pieces: k-values per chunk (channels in conv mode, pixels in wgrad mode)
+constexpr int TC_SMEM_MAX = TC_SMEM_RING + 1024 + 8 * TC_STAGE_OUT;  // dynamic shared memory of every launch at most
 constexpr long long kWait = 4000000000LL;  // clock cycles, about 2 s
 
 __device__ int g_tc_status;
@@ -151,6 +165,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 with bf16 A and B, one CTA.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -170,18 +193,28 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start,
 // leading and stride byte offsets in 16-byte units, version 1 at bit 46,
 // layout type 2 = SWIZZLE_128B at bits 61-63).
-__device__ __forceinline__ uint64_t sdesc(const void* p, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+// Other layout types: 4 = SWIZZLE_64B.  K-major swizzled tiles: LBO unused,
+// SBO = the stride of 8-row groups; MN-major tiles: LBO = the stride of the
+// 64-element (128-byte) MN blocks, SBO = the stride of 8-row K groups.
+__device__ __forceinline__ uint64_t sdesc(const void* p, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                          uint32_t layout = 2) {
     uint64_t d = 0;
     d |= (uint64_t)((su32(p) >> 4) & 0x3FFF);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)layout << 61;
     return d;
 }
 // Instruction descriptor, kind::tf32: D fp32, A and B tf32, majors, N, M.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, int a_mn_major, int b_mn_major) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, majors, N, M.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -193,11 +226,13 @@ struct TcParams {
     int chunks;     // k-chunks per unit (conv mode)
     int group;      // k-chunks accumulated in TMEM before the epilogue adds them up in fp32
     int tma_store;  // conv mode without depth-to-space: store through ymap (TMA boxes)
+    int fmt;        // operands: 0 tf32 [hi][lo] pairs, 1 three bf16 pieces (1x1 convolutions)
+    int stage_bytes, a_piece, b_piece;  // bf16 pieces: ring stage, one piece of the A / B tile
     // conv mode
     int N, Ho, Wo, M, Kc, kh, kw, pad, tiles_w, mblocks;
     const float* bias;
     float* out;     // NCHW [N][M][Ho][Wo], or with d2s > 0 the image [N][d2s_c][Ho*d2s][Wo*d2s]
-    int d2s, d2s_c; // depth-to-space store: row m = (u*d2s + v)*d2s_c + c goes to pixel (ho*d2s+u, wo*d2s+v)
+    int d2s, d2s_c; // depth-to-space store: row m = (u*d2s_c + c)*d2s + v goes to pixel (ho*d2s+u, wo*d2s+v)
     // wgrad mode
     int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // S: grid shards Sh*Sw; row_chunks = own_w / BK
     int Sw, own_h;  // column shards; owned output rows per row shard (shard q = a*Sw + b)
@@ -259,7 +294,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    const __grid_constant__ CUtensorMap ymap, TcParams p) {
     extern __shared__ __align__(1024) unsigned char dsmem[];
     unsigned char* ring = (unsigned char*)(((uintptr_t)dsmem + 1023) & ~(uintptr_t)1023);  // 128-byte swizzle atoms need 1 KB
-    unsigned char* stage_out = ring + TC_SMEM_RING;  // TC_EPI_WARPS output boxes, 1 KB aligned
+    // TC_EPI_WARPS output boxes, 1 KB aligned, after a conv-mode ring of at most TC_SMEM_RING
+    // bytes (a weight-gradient ring, which stores no boxes, may extend over them)
+    unsigned char* stage_out = ring + TC_SMEM_RING;
     __shared__ Smem sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t a_bytes = BM * ROWB;           // 128 rows x BK tf32
@@ -295,6 +332,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int s = (int)(it % p.stages);
                 if (it >= p.stages && !mbar_wait(&sh.empty[s], (unsigned)(((it / p.stages) - 1) & 1), abort_flag))
                     break;
+                if (p.fmt == 1) {
+                    // bf16 pieces: one box brings all three pieces of a tile
+                    unsigned char* st = ring + (size_t)s * p.stage_bytes;
+                    unsigned char* bdst = st + 3 * p.a_piece;
+                    mbar_expect_tx(&sh.full[s], (unsigned)p.stage_bytes);
+                    if (p.mode == 0) {
+                        // A: weights [3][M][K], 128 rows x 32 k; B: activation [3][N][K][Ho*Wo],
+                        // BN pixels x 32 channels (the tile starts on a 64-pixel block)
+                        tma_3d(st, &amap, (int)c * BKH, u.m0, 0, &sh.full[s]);
+                        tma_5d(bdst, &bmap, 0, (int)c * BKH, (u.ho * p.Wo + u.w0) / 64, u.n, 0, &sh.full[s]);
+                    } else {
+                        // pixel chunk c of shard r, along the row: (n, ho, 32-pixel piece), the
+                        // piece fastest, so a box row (64 bytes) and its neighbour in the same
+                        // 128-byte line are read one after the other (a 1x1 kernel has no taps
+                        // that would reuse rows).  A = grad_output [3][N][Co][H][W], 128
+                        // channels x 32 pixels; B = x, the 256 channels of the slot pair (past
+                        // C_in the box reads zeros)
+                        const int qa = u.r / p.Sw, qb = u.r - qa * p.Sw;
+                        const int wc = (int)(c % p.row_chunks);
+                        const long long rest = c / p.row_chunks;
+                        const int ho = qa * p.own_h + (int)(rest % p.own_h), n = (int)(rest / p.own_h);
+                        const int w = qb * p.own_w + wc * BKH;
+                        tma_5d(st, &amap, w, ho, u.m0, n, 0, &sh.full[s]);
+                        tma_5d(bdst, &bmap, w, ho, 2 * u.tap * WG_SLOT, n, 0, &sh.full[s]);
+                    }
+                    continue;
+                }
                 unsigned char* st = ring + (size_t)s * stage_bytes;
                 const bool second = p.mode == 0 || 2 * u.tap + 1 < p.slots;  // wgrad: last pair may be half
                 mbar_expect_tx(&sh.full[s], second ? stage_bytes : stage_bytes - b_bytes);
@@ -341,7 +405,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = idesc_tf32(BM, BN, 0, 0);
+        const uint32_t idesc = p.fmt == 1 ? idesc_bf16(BM, BN, 0, p.mode == 0 ? 1 : 0) : idesc_tf32(BM, BN, 0, 0);
         long long it = 0;
         long long g = 0;  // group counter = TMEM buffer position
         bool ok = true;
@@ -364,6 +428,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (p.fmt == 1) {
+                        // A: K-major, 64-byte swizzle, 8-row groups 512 B apart (both modes).  B:
+                        // conv mode MN-major, 128-byte swizzle, 64-pixel blocks BKH rows apart and
+                        // 8-channel groups 1 KB apart; wgrad mode K-major like A.  Products a_i*b_j
+                        // with i + j <= 2, the small ones first
+                        // (offsets are added to the descriptors' start field, in 16-byte units)
+                        constexpr int kPa[6] = {1, 2, 0, 1, 0, 0}, kPb[6] = {1, 0, 2, 0, 1, 0};
+                        unsigned char* st = ring + (size_t)s * p.stage_bytes;
+                        const uint64_t a0 = sdesc(st, 16, 512, 4);
+                        const uint64_t b0 = p.mode == 0 ? sdesc(st + 3 * p.a_piece, BKH * 128, 1024, 2)
+                                                        : sdesc(st + 3 * p.a_piece, 16, 512, 4);
+                        const uint32_t ap = (uint32_t)p.a_piece >> 4, bp = (uint32_t)p.b_piece >> 4;
+                        const uint32_t bk = p.mode == 0 ? 2048 >> 4 : 32 >> 4;
+#pragma unroll
+                        for (int k = 0; k < BKH / 16; k++) {  // 16 bf16 per MMA
+#pragma unroll
+                            for (int t = 0; t < 6; t++) {
+                                tc_mma_bf16(d, a0 + kPa[t] * ap + 2 * k, b0 + kPb[t] * bp + k * bk, idesc,
+                                            first ? 0u : 1u);
+                                first = false;
+                            }
+                        }
+                        tc_commit(&sh.empty[s]);
+                        continue;
+                    }
                     unsigned char* st = ring + (size_t)s * stage_bytes;
                     unsigned char *ahi = st, *alo = st + a_bytes, *bhi = st + 2 * a_bytes, *blo = bhi + b_bytes;
 #pragma unroll
@@ -927,6 +1016,117 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __res
     }
 }
 
+// fp32 -> three bf16 pieces, piece k of value i at out[k * ps + i]:
+// p0 = bf16(v), p1 = bf16(v - p0), p2 = bf16(v - p0 - p1); the two differences
+// are exact in fp32, and the pieces carry 24 bits of v's significand.
+__device__ __forceinline__ void split3(float v, __nv_bfloat16& p0, __nv_bfloat16& p1, __nv_bfloat16& p2) {
+    p0 = __float2bfloat16_rn(v);
+    const float r = v - __bfloat162float(p0);
+    p1 = __float2bfloat16_rn(r);
+    p2 = __float2bfloat16_rn(r - __bfloat162float(p1));
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+// Elementwise over n4 float4s (the layout is kept); ps4 = piece stride / 4.
+__global__ void __launch_bounds__(256) prep_pieces_kernel(const float4* __restrict__ x, uint2* __restrict__ out,
+                                                          long long n4, long long ps4) {
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += (long long)gridDim.x * 256) {
+        const float4 v = __ldg(x + i);
+        __nv_bfloat16 a[4], b[4], c[4];
+        split3(v.x, a[0], b[0], c[0]);
+        split3(v.y, a[1], b[1], c[1]);
+        split3(v.z, a[2], b[2], c[2]);
+        split3(v.w, a[3], b[3], c[3]);
+        out[i] = make_uint2(pack2(a[0], a[1]), pack2(a[2], a[3]));
+        out[ps4 + i] = make_uint2(pack2(b[0], b[1]), pack2(b[2], b[3]));
+        out[2 * ps4 + i] = make_uint2(pack2(c[0], c[1]), pack2(c[2], c[3]));
+    }
+}
+// Transposed pieces of a small R x C matrix: out[k * ps + c * R + r] = piece k of w[r * C + c].
+__global__ void prep_pieces_t_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ out, int R, int C,
+                                     long long ps) {
+    const long long i = blockIdx.x * 256LL + threadIdx.x;
+    if (i >= (long long)R * C) return;
+    const int c = (int)(i / R), r = (int)(i % R);
+    __nv_bfloat16 a, b, e;
+    split3(__ldg(w + (long long)r * C + c), a, b, e);
+    out[i] = a;
+    out[ps + i] = b;
+    out[2 * ps + i] = e;
+}
+
+// Space-to-depth pieces: x [N][C][H][W] -> [3][N][K][Ho][Wo] with K = S*S*C and
+// channel k = (u*S + v)*C + c holding x[n][c][ho*S + u][wo*S + v].  Each item
+// reads 4*S consecutive columns of one input row (n, c, h = ho*S + u) and
+// writes, for every v, output columns 4j..4j+3 of channel (u*S + v)*C + c.
+// Needs Wo % 4 == 0; ps4 = piece stride / 4.
+template <int S>
+__global__ void prep_s2d_pieces_kernel(const float* __restrict__ x, uint2* __restrict__ out, int C, int H, int W,
+                                       long long items, long long ps4) {
+    const int Ho = H / S, Wo = W / S, J = Wo / 4, K = S * S * C;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < items;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long rid = q / J;  // (n * C + c) * H + h
+        const int j = (int)(q - rid * J);
+        const int h = (int)(rid % H);
+        const long long nc = rid / H;
+        const int c = (int)(nc % C);
+        const long long n = nc / C;
+        const int ho = h / S, u = h - ho * S;
+        float e[4 * S];
+        const float4* src = reinterpret_cast<const float4*>(x + rid * W + 4LL * j * S);
+#pragma unroll
+        for (int k = 0; k < S; k++) {
+            const float4 a = __ldg(src + k);
+            e[4 * k] = a.x;
+            e[4 * k + 1] = a.y;
+            e[4 * k + 2] = a.z;
+            e[4 * k + 3] = a.w;
+        }
+#pragma unroll
+        for (int v = 0; v < S; v++) {
+            __nv_bfloat16 a[4], b[4], g[4];
+#pragma unroll
+            for (int t = 0; t < 4; t++) split3(e[t * S + v], a[t], b[t], g[t]);
+            const long long o4 = (((n * K + (u * S + v) * C + c) * Ho + ho) * Wo + 4LL * j) / 4;
+            out[o4] = make_uint2(pack2(a[0], a[1]), pack2(a[2], a[3]));
+            out[ps4 + o4] = make_uint2(pack2(b[0], b[1]), pack2(b[2], b[3]));
+            out[2 * ps4 + o4] = make_uint2(pack2(g[0], g[1]), pack2(g[2], g[3]));
+        }
+    }
+}
+// Weight pieces in space-to-depth order, K = s*s*C: forward A[co][k] = w[co][c][u][v]
+// with k = (u*s + v)*C + c ([Co][K]); grad_input A[m][co] = w[co][c][u][v] with
+// m = (u*C + c)*s + v ([K][Co]), the row order of the depth-to-space store.
+__global__ void prep_weight_s2d_pieces_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ out, int Co,
+                                              int C, int s, int transpose, long long ps) {
+    const int K = s * s * C;
+    const long long q = blockIdx.x * 256LL + threadIdx.x;
+    if (q >= (long long)Co * K) return;
+    int co, k, c, uu, vv;
+    if (!transpose) {
+        co = (int)(q / K);
+        k = (int)(q % K);
+        const int tap = k / C;
+        c = k - tap * C;
+        uu = tap / s;
+        vv = tap - uu * s;
+    } else {
+        k = (int)(q / Co);
+        co = (int)(q % Co);
+        const int uc = k / s;
+        vv = k - uc * s;
+        uu = uc / C;
+        c = uc - uu * C;
+    }
+    __nv_bfloat16 a, b, g;
+    split3(__ldg(w + (((long long)co * C + c) * s + uu) * s + vv), a, b, g);
+    out[q] = a;
+    out[ps + q] = b;
+    out[2 * ps + q] = g;
+}
+
 int sm_count_tc() {
     static int n = 0;
     if (!n) {
@@ -953,14 +1153,28 @@ template <int BN>
 hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap, TcParams p,
                     cudaStream_t st) {
     static bool attr = false;
-    const int smem = TC_SMEM_RING + 1024 + TC_EPI_WARPS * TC_STAGE_OUT;
     if (!attr) {
-        cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX);
         attr = true;
     }
-    const int stage_bytes = 2 * BM * ROWB + 2 * BN * ROWB;
-    p.stages = TC_SMEM_RING / stage_bytes;
-    if (p.stages > 8) p.stages = 8;
+    int smem;
+    if (p.fmt == 1) {
+        // three pieces of A (128 x BKH) and B (BN x BKH) per stage; as many stages as
+        // fit before the output boxes (conv mode: 2 for BN = 256) or in the whole
+        // buffer (weight gradient: 3)
+        p.a_piece = BM * BKH * 2;
+        p.b_piece = BN * BKH * 2;
+        p.stage_bytes = 3 * (p.a_piece + p.b_piece);
+        p.stages = (p.tma_store ? TC_SMEM_RING : TC_SMEM_MAX - 1024) / p.stage_bytes;
+        if (p.stages > 8) p.stages = 8;
+        if (p.stages < 2) return HC_ERR_UNSUPPORTED;
+        smem = p.tma_store ? TC_SMEM_MAX : p.stages * p.stage_bytes + 1024;
+    } else {
+        const int stage_bytes = 2 * BM * ROWB + 2 * BN * ROWB;
+        p.stages = TC_SMEM_RING / stage_bytes;
+        if (p.stages > 8) p.stages = 8;
+        smem = TC_SMEM_MAX;
+    }
     const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
     tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
     return launched();
@@ -972,7 +1186,7 @@ hc_status launch_conv_pass(int BN, const CUtensorMap& amap, const CUtensorMap& b
                            const CUtensorMap* ymap = nullptr) {
     p.tma_store = ymap != nullptr;
     if (!ymap) ymap = &amap;  // unused
-    p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group
+    p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group (BKH == BK)
     if (BN == 256) return launch_bn<256>(amap, bmap, *ymap, p, st);
     if (BN == 128) return launch_bn<128>(amap, bmap, *ymap, p, st);
     return HC_ERR_UNSUPPORTED;
@@ -1037,7 +1251,49 @@ hc_status shifted_map(CUtensorMap* m, const float* hi, const float* lo, int N, i
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, hi, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// bf16 piece arrays: the three pieces of one tensor ps elements apart (the
+// outermost map dimension), so one box brings all three.
+// Weight pieces [3][M][K], K-major tiles of 128 rows x 32 k: dims (K, M, 3),
+// box (32, 128, 3), 64-byte swizzle.
+hc_status pieces_weight_map(CUtensorMap* m, const void* base, int M, int K, long long ps) {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)M, 3};
+    const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)ps * 2};
+    const uint32_t box[3] = {BKH, 128, 3};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+// Activation pieces [3][N][C][P] (P pixels of an image, contiguous) as MN-major
+// tiles of BN pixels x 32 channels: dims (64, C, P / 64, N, 3).  The 64-pixel
+// block is a dimension of its own (stride 128 B) placed after the channel, so
+// a box lands as [piece][pixel block][channel][64 pixels]: per pixel block, 32
+// rows of 128 bytes with the 128-byte swizzle, the MN-major tile layout.
+hc_status pieces_mn_map(CUtensorMap* m, const void* base, int N, int C, long long P, int BN, long long ps) {
+    const uint64_t dims[5] = {64, (uint64_t)C, (uint64_t)(P / 64), (uint64_t)N, 3};
+    const uint64_t strides[4] = {(uint64_t)P * 2, 128, (uint64_t)C * P * 2, (uint64_t)ps * 2};
+    const uint32_t box[5] = {64, BKH, (uint32_t)(BN / 64), 1, 3};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Pieces [3][N][C][H][W] as K-major tiles of `rows` channels x 32 pixels of one
+// image row: dims (W, H, C, N, 3), box (32, 1, rows, 1, 3), 64-byte swizzle.
+hc_status pieces_rows_map(CUtensorMap* m, const void* base, int N, int C, int H, int W, int rows, long long ps) {
+    const uint64_t dims[5] = {(uint64_t)W, (uint64_t)H, (uint64_t)C, (uint64_t)N, 3};
+    const uint64_t strides[4] = {(uint64_t)W * 2, (uint64_t)H * W * 2, (uint64_t)C * H * W * 2, (uint64_t)ps * 2};
+    const uint32_t box[5] = {BKH, 1, (uint32_t)rows, 1, 3};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+// piece stride: the element count rounded up to 128 (256 bytes)
+long long piece_stride(long long n) { return (n + 127) / 128 * 128; }
+
+hc_status launch_prep_pieces(const float* x, void* out, long long n, long long ps, cudaStream_t st) {
+    if (n % 4 || ps % 4) return HC_ERR_UNSUPPORTED;
+    long long blocks = (n / 4 + 255) / 256;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    if (blocks < 1) blocks = 1;
+    prep_pieces_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(x),
+                                                         reinterpret_cast<uint2*>(out), n / 4, ps / 4);
+    return launched();
+}
 
 
 
@@ -1438,6 +1694,230 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         const long long total = (long long)p.Q * wsz;
         wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, KK, Co, Ci);
         if ((s = launched())) return s;
+    }
+    return HC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Convolutions on bf16 pieces: 1x1 (stride 1, no padding) and k = stride = s
+// (no padding) as a 1x1 conv of the space-to-depth image.  The pieces keep
+// NCHW order -- of x, or of the space-to-depth image [N][s*s*C][Ho][Wo] --
+// and of grad_output.  A 1x1 conv pass treats the H*W pixels of an image as
+// one flat row (Ho = 1, Wo = H*W); a space-to-depth pass tiles output rows and
+// stores grad_input depth-to-space.  K past the last channel reads as zeros
+// (TMA fill), so no padded copies are written.  The weight gradient walks a
+// shard's own columns as in the tf32 pass.
+namespace {
+struct Bf16View {
+    bool s2d;
+    int s, K;     // stride; GEMM depth of the forward pass (C_in, or s*s*C_in)
+    long long P;  // pixels of one output image
+};
+Bf16View bf16_view(const hc_conv_desc* d, const Plan& p) {
+    Bf16View v;
+    v.s2d = is_s2d(d);
+    v.s = d->stride;
+    v.K = v.s2d ? v.s * v.s * d->C_in : d->C_in;
+    v.P = (long long)p.Ho * p.Wo;
+    return v;
+}
+}  // namespace
+
+bool bf16_supported(const hc_conv_desc* d, const Plan& p) {
+    if (d->C_out % BM) return false;  // M blocks of the forward pass
+    const Bf16View v = bf16_view(d, p);
+    if (v.s2d) {
+        // row tiles of 128 / 256 output columns; 4*s input columns per prep item
+        if (v.s > 4 || d->H % v.s || d->W % v.s || p.Ho != d->H / v.s || p.Wo != d->W / v.s) return false;
+        if (!pick_bn(p.Wo) || v.K % 8) return false;
+    } else {
+        if (d->groups != 1 || d->kh != 1 || d->kw != 1 || d->stride != 1 || d->padding != 0) return false;
+        if (d->C_in % BM || v.P % 128) return false;  // grad_input M blocks; flat tiles of 128 / 256 pixels
+    }
+    // weight-gradient chunks of 32 pixels inside a shard's columns; 16-byte rows
+    if ((p.Wl / v.s) % BKH || p.Wo % 8) return false;
+    return (long long)d->N * v.K * v.P < (1LL << 36) && (long long)d->N * d->C_out * v.P < (1LL << 36);
+}
+
+// Workspace: forward  [x pieces][w pieces]
+//            backward [gy pieces][w^T pieces][x pieces][split-K partials]
+size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
+    const Bf16View v = bf16_view(d, p);
+    const size_t psx = piece_stride((long long)d->N * v.K * v.P), psg = piece_stride((long long)d->N * d->C_out * v.P);
+    const size_t psw = piece_stride((long long)d->C_out * v.K);
+    if (pass == 0) return al256(6 * psx) + al256(6 * psw);
+    const int Kp = v.s2d ? s2d_kp(d) : d->C_in;  // partial row pitch: whole 128-column slots
+    const size_t part = al256(4 * (size_t)p.Q * tc_wgrad_splits(d, p) * d->C_out * Kp);
+    return al256(6 * psg) + al256(6 * psw) + al256(6 * psx) + part;
+}
+
+static hc_status prep_x_pieces(const hc_conv_desc* d, const Plan& p, const Bf16View& v, const float* x, void* out,
+                               long long ps, cudaStream_t st) {
+    if (!v.s2d) return launch_prep_pieces(x, out, (long long)d->N * d->C_in * v.P, ps, st);
+    const long long items = (long long)d->N * d->C_in * d->H * (p.Wo / 4);
+    long long blocks = (items + 255) / 256;
+    if (blocks > 152LL * 32) blocks = 152LL * 32;
+    if (blocks < 1) blocks = 1;
+    uint2* o = reinterpret_cast<uint2*>(out);
+    if (v.s == 2)
+        prep_s2d_pieces_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(x, o, d->C_in, d->H, d->W, items, ps / 4);
+    else if (v.s == 3)
+        prep_s2d_pieces_kernel<3><<<(unsigned)blocks, 256, 0, st>>>(x, o, d->C_in, d->H, d->W, items, ps / 4);
+    else if (v.s == 4)
+        prep_s2d_pieces_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(x, o, d->C_in, d->H, d->W, items, ps / 4);
+    else
+        return HC_ERR_UNSUPPORTED;
+    return launched();
+}
+
+// The conv-pass tiling: flat rows of BN pixels (1x1) or BN-column segments of
+// output rows (space-to-depth).
+static void bf16_tiles(const Plan& p, const Bf16View& v, TcParams& tp, int* BN) {
+    if (v.s2d) {
+        *BN = pick_bn(p.Wo);
+        tp.Ho = p.Ho;
+        tp.Wo = p.Wo;
+    } else {
+        *BN = v.P % 256 == 0 ? 256 : 128;
+        tp.Ho = 1;
+        tp.Wo = (int)v.P;
+    }
+    tp.tiles_w = tp.Wo / *BN;
+}
+
+hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
+                          float* y, void* ws, cudaStream_t st) {
+    const Bf16View v = bf16_view(d, p);
+    const int Co = d->C_out;
+    const long long wsz = (long long)Co * v.K;
+    const long long psx = piece_stride((long long)d->N * v.K * v.P), psw = piece_stride(wsz);
+    char* q = (char*)ws;
+    void* xp = q;
+    q += al256(6 * psx);
+    void* ap = q;
+    hc_status e;
+    if ((e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
+    if (v.s2d) {
+        prep_weight_s2d_pieces_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, v.s, 0,
+                                                                      psw);
+        e = launched();
+    } else {
+        e = launch_prep_pieces(w, ap, wsz, psw, st);
+    }
+    if (e) return e;
+    TcParams tp{};
+    int BN;
+    bf16_tiles(p, v, tp, &BN);
+    tp.mode = 0;
+    tp.fmt = 1;
+    tp.N = d->N;
+    tp.M = Co;
+    tp.Kc = v.K;
+    tp.kh = 1;
+    tp.kw = 1;
+    tp.pad = 0;
+    tp.mblocks = Co / BM;
+    tp.chunks = (v.K + BKH - 1) / BKH;
+    tp.units = tp.mblocks * d->N * tp.Ho * tp.tiles_w;
+    tp.bias = b;
+    tp.out = y;
+    CUtensorMap ma, mb, my;
+    if ((e = pieces_weight_map(&ma, ap, Co, v.K, psw)) || (e = pieces_mn_map(&mb, xp, d->N, v.K, v.P, BN, psx)) ||
+        (e = out_map(&my, y, d->N, Co, tp.Ho, tp.Wo)))
+        return e;
+    return launch_conv_pass(BN, ma, mb, tp, st, &my);
+}
+
+hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
+                          float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+    const Bf16View v = bf16_view(d, p);
+    const int Co = d->C_out;
+    const long long wsz = (long long)Co * v.K;
+    const long long psx = piece_stride((long long)d->N * v.K * v.P);
+    const long long psg = piece_stride((long long)d->N * Co * v.P), psw = piece_stride(wsz);
+    char* q = (char*)ws;
+    void* gp = q;
+    q += al256(6 * psg);
+    void* ap = q;
+    q += al256(6 * psw);
+    void* xp = q;
+    q += al256(6 * psx);
+    float* part = (float*)q;
+    hc_status e;
+    // grad_output's pieces serve both passes
+    if ((e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st))) return e;
+    if (gx) {  // D[m][px] = sum_co w^T[m][co] gy[co][px], m = ci (1x1) or (u*C + c)*s + v (depth-to-space)
+        if (v.s2d)
+            prep_weight_s2d_pieces_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, v.s,
+                                                                          1, psw);
+        else
+            prep_pieces_t_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, psw);
+        if ((e = launched())) return e;
+        TcParams tp{};
+        int BN;
+        bf16_tiles(p, v, tp, &BN);
+        tp.mode = 0;
+        tp.fmt = 1;
+        tp.N = d->N;
+        tp.M = v.K;
+        tp.Kc = Co;
+        tp.kh = 1;
+        tp.kw = 1;
+        tp.pad = 0;
+        tp.mblocks = (v.K + BM - 1) / BM;
+        tp.chunks = Co / BKH;
+        tp.units = tp.mblocks * d->N * tp.Ho * tp.tiles_w;
+        tp.bias = nullptr;
+        tp.out = gx;
+        CUtensorMap ma, mb, my;
+        if ((e = pieces_weight_map(&ma, ap, v.K, Co, psw)) || (e = pieces_mn_map(&mb, gp, d->N, Co, v.P, BN, psg)))
+            return e;
+        if (v.s2d) {
+            tp.d2s = v.s;
+            tp.d2s_c = d->C_in;
+            if ((e = launch_conv_pass(BN, ma, mb, tp, st))) return e;
+        } else {
+            if ((e = out_map(&my, gx, d->N, v.K, 1, (int)v.P))) return e;
+            if ((e = launch_conv_pass(BN, ma, mb, tp, st, &my))) return e;
+        }
+    }
+    if (want_w) {  // G[co][k] = sum over a shard's pixels of gy[co][px] x'[k][px]
+        if ((e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
+        const int Kp = v.s2d ? s2d_kp(d) : d->C_in;
+        TcParams tp{};
+        tp.mode = 1;
+        tp.fmt = 1;
+        tp.Co = Co;
+        tp.Ci = Kp;
+        tp.S = p.Q;
+        tp.Sw = p.S;
+        tp.own_h = p.Hlo;
+        tp.J = tc_wgrad_splits(d, p);
+        tp.own_w = p.Wl / v.s;
+        tp.row_chunks = tp.own_w / BKH;
+        tp.Ho = p.Ho;
+        tp.kh = 1;
+        tp.kw = 1;
+        tp.pad = 0;
+        tp.taps = 1;
+        tp.mblocks = Co / BM;
+        tp.nblocks = Kp / WG_SLOT;
+        tp.slots = tp.nblocks;
+        tp.shard_chunks = (long long)d->N * p.Hlo * tp.row_chunks;
+        tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.Q;
+        tp.part = part;
+        tp.N = d->N;
+        CUtensorMap ma, mb;
+        if ((e = pieces_rows_map(&ma, gp, d->N, Co, p.Ho, p.Wo, BM, psg)) ||
+            (e = pieces_rows_map(&mb, xp, d->N, v.K, p.Ho, p.Wo, WG_BN, psx)))
+            return e;
+        if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
+        const long long total = (long long)p.Q * wsz;
+        if (v.s2d)
+            wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, Co, d->C_in, v.s, Kp);
+        else
+            wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, 1, Co, d->C_in);
+        if ((e = launched())) return e;
     }
     return HC_OK;
 }

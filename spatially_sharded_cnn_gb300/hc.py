@@ -22,7 +22,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_TIMEOUT = range(6)
-HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32 = range(4)
+HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32, HC_ALGO_TC_BF16X6 = range(5)
 
 
 class hc_conv_desc(C.Structure):

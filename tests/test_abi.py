@@ -120,3 +120,26 @@ def test_algorithm_choice(hc):
     # depthwise tiles are 128 columns inside a shard: 64-column shards fall back
     odd = hc.desc(P.cfg_of(1, 8, 16, 256, 8, 7, 1, 3, 8, 4))
     assert hc.hc_conv2d_select(odd, 0) == (0, hc.HC_ALGO_DIRECT)
+
+
+def test_pointwise_algorithm_choice(hc):
+    """1x1 convs with 128-multiple channels go to the bf16-piece GEMM; its
+    operand copies take 6 bytes per element against 8 for tf32 hi / lo."""
+    for ci, co in ((256, 1024), (1024, 256)):
+        d = hc.desc(P.cfg_of(7, ci, 128, 1024, co, 1, 1, 0, 1, 8))
+        assert hc.hc_conv2d_select(d, 0) == (0, hc.HC_ALGO_TC_BF16X6)
+        assert hc.hc_conv2d_select(d, 1) == (0, hc.HC_ALGO_TC_BF16X6)
+        st6, b6 = hc.hc_conv2d_workspace_size(d, 0, hc.HC_ALGO_TC_BF16X6)
+        st3, b3 = hc.hc_conv2d_workspace_size(d, 0, hc.HC_ALGO_TC_3XTF32)
+        assert st6 == 0 and st3 == 0 and b6 < b3
+        assert b6 >= 6 * 7 * ci * 128 * 1024
+    # the block's stem (4x4/s4, 3 -> 256) and a 2x2/s2 downsample: space-to-depth GEMMs
+    for cfg in (P.cfg_of(7, 3, 512, 4096, 256, 4, 4, 0, 1, 8), P.cfg_of(7, 256, 128, 2048, 512, 2, 2, 0, 1, 8)):
+        assert hc.hc_conv2d_select(hc.desc(cfg), 1) == (0, hc.HC_ALGO_TC_BF16X6)
+    # not a 1x1 / stride-1 / unpadded conv, or shard columns not whole 32-pixel chunks
+    for cfg in (P.cfg_of(1, 128, 8, 256, 128, 3, 1, 1, 1, 2), P.cfg_of(1, 128, 8, 256, 128, 1, 1, 0, 1, 16),
+                P.cfg_of(1, 96, 8, 256, 128, 1, 1, 0, 1, 2), P.cfg_of(1, 128, 8, 256, 96, 2, 2, 0, 1, 2),
+                P.cfg_of(1, 128, 8, 256, 128, 2, 2, 1, 1, 2), P.cfg_of(1, 3, 8, 256, 128, 2, 2, 0, 1, 2)):
+        d = hc.desc(cfg)
+        assert hc.hc_conv2d_workspace_size(d, 0, hc.HC_ALGO_TC_BF16X6)[0] == hc.HC_ERR_UNSUPPORTED, cfg
+        assert hc.hc_conv2d_select(d, 0)[1] != hc.HC_ALGO_TC_BF16X6

@@ -87,6 +87,13 @@ CASES = {
     "tc_5x5_S2": lambda: tc_case(1, 128, 6, 256, 128, 5, 2),
     "tc_3x3_two_mblocks": lambda: tc_case(1, 128, 5, 256, 256, 3, 1),
     "tc_1x1": lambda: tc_case(2, 256, 4, 128, 128, 1, 1),
+    # 1x1 convs on three bf16 pieces: half slot pair (C_in 128), 128-pixel tiles
+    # (H*W = 384) with a half pair (C_in 384), the block's 256->1024 and 1024->256
+    # shapes at 8 shards, a 2 x 4 grid
+    "pw_128to256_S4_half_pair": lambda: tc_case(2, 128, 4, 256, 256, 1, 4),
+    "pw_384to128_tiles128": lambda: tc_case(1, 384, 3, 128, 128, 1, 2),
+    "pw_256to1024_S8": lambda: tc_case(1, 256, 2, 1024, 1024, 1, 8),
+    "pw_1024to256_S8": lambda: tc_case(1, 1024, 2, 1024, 256, 1, 8),
     "tc_5x5_ragged_two_tiles": lambda: tc_case(1, 128, 7, 512, 128, 5, 1),
     # strided k = stride convs through space-to-depth (stem- and downsample-like)
     "tc_stem4x4s4": lambda: tc_strided_case(2, 3, 12, 512, 128, 4, 1),
@@ -102,6 +109,7 @@ CASES = {
     # row x column shard grids (Shard(2) and Shard(3) together)
     "tc_5x5_grid_2x2": lambda: _rows(tc_case(1, 128, 8, 256, 128, 5, 2), 2),
     "tc_down2x2s2_grid_2x2": lambda: _rows(tc_strided_case(1, 128, 8, 512, 256, 2, 2), 2),
+    "pw_grid_2x4": lambda: _rows(tc_case(1, 256, 8, 256, 128, 1, 4), 2),
     "dw7_grid_2x2": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 2),          # 64-row shards: depthwise
     "dw7_grid_4x2_direct": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 4),   # 32-row shards: direct
     "grouped_strided_grid_3x2": lambda: _rows(generic_case(P.cfg_of(2, 6, 12, 16, 4, 3, 2, 2, 2, 2)), 3),
@@ -148,7 +156,8 @@ def test_grid_family_choice(hc):
     assert sel("dw7_grid_2x2") == (0, hc.HC_ALGO_DEPTHWISE)
     assert sel("dw7_grid_4x2_direct") == (0, hc.HC_ALGO_DIRECT)
     assert sel("tc_5x5_grid_2x2") == (0, hc.HC_ALGO_TC_3XTF32)
-    assert sel("tc_down2x2s2_grid_2x2") == (0, hc.HC_ALGO_TC_3XTF32)
+    assert sel("tc_down2x2s2_grid_2x2") == (0, hc.HC_ALGO_TC_BF16X6)
+    assert sel("pw_grid_2x4") == (0, hc.HC_ALGO_TC_BF16X6)
 
 
 @pytest.mark.parametrize("name", ["dw7_ragged_S4", "dw5_S2", "dw3_S4"])
@@ -164,8 +173,92 @@ def test_parity_depthwise_explicit(hc, orc, name):
                                   "tc_5x5_S4_tiles_cross_shards", "tc_3x3_wide_S8"])
 def test_parity_tensor_cores_explicit(hc, orc, name):
     cfg = CASES[name]()[0]
-    assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, hc.HC_ALGO_TC_3XTF32)
+    auto = hc.HC_ALGO_TC_BF16X6 if name in BF16_CASES else hc.HC_ALGO_TC_3XTF32
+    assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, auto)
     check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_TC_3XTF32)
+
+
+# 1x1 convs and k = stride convs (space-to-depth) with 128-multiple output
+# channels take the bf16-piece GEMM
+BF16_CASES = ["tc_1x1", "pw_128to256_S4_half_pair", "pw_384to128_tiles128", "pw_256to1024_S8", "pw_1024to256_S8",
+              "pw_grid_2x4", "tc_stem4x4s4", "tc_down2x2s2_S2", "tc_down3x3s3_C64_S2", "tc_down2x2s2_C96_S4",
+              "tc_down2x2s2_grid_2x2"]
+
+
+@pytest.mark.parametrize("name", BF16_CASES)
+def test_parity_bf16x6_explicit(hc, orc, name):
+    cfg = CASES[name]()[0]
+    assert hc.hc_conv2d_select(hc.desc(cfg), 0) == (0, hc.HC_ALGO_TC_BF16X6)
+    assert hc.hc_conv2d_select(hc.desc(cfg), 1) == (0, hc.HC_ALGO_TC_BF16X6)
+    check_case(hc, orc, *CASES[name](), algo=hc.HC_ALGO_TC_BF16X6)
+
+
+def test_bf16x6_space_to_depth_moves_bit_exact(hc):
+    """A 2x2/s2 conv whose weights pick one input tap per output channel:
+    y[co] = x[c][2ho + u][2wo + v] exactly, and grad_input puts each grad_output
+    value back at that tap (zeros elsewhere), for 20-bit significands."""
+    N, C, H, W, Co, s = 1, 64, 8, 512, 128, 2
+    cfg = P.cfg_of(N, C, H, W, Co, s, s, 0, 1, 2)
+    pick = [(co % C, co // C, 1 - co // C) for co in range(Co)]  # (c, u, v)
+    w = np.zeros((Co, C, s, s), np.float32)
+    for co, (c, u, v) in enumerate(pick):
+        w[co, c, u, v] = 1.0
+    x = synth.dyadic((N, C, H, W), 20, 1, 9, 1)
+    gy = synth.dyadic((N, Co, H // s, W // s), 20, 1, 9, 2)
+    algo = hc.HC_ALGO_TC_BF16X6
+    y = R.fwd(cfg, x, w, None, algo)
+    want = np.stack([x[:, c, u::s, v::s] for c, u, v in pick], axis=1)
+    assert np.array_equal(y, want)
+    gx = R.bwd_subset(cfg, x, w, gy, ("gx",), algo)["gx"]
+    want = np.zeros_like(x)
+    for co, (c, u, v) in enumerate(pick):
+        want[:, c, u::s, v::s] = gy[:, co]
+    assert np.array_equal(gx, want)
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_bf16x6_permutation_bit_exact(hc, S):
+    """A 1x1 conv whose weight is a permutation matrix moves values: y = x[perm]
+    and grad_input = grad_output[perm^-1], exactly, for values with 20-bit
+    significands -- so all three bf16 pieces reach the output, every channel and
+    pixel lands where the tile layouts say, and nothing else is added."""
+    N, C, H, W = 2, 256, 2, 256
+    cfg = P.cfg_of(N, C, H, W, C, 1, 1, 0, 1, S)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(C)
+    w = np.zeros((C, C, 1, 1), np.float32)
+    w[np.arange(C), perm, 0, 0] = 1.0
+    x = synth.dyadic((N, C, H, W), 20, 1, 6, 1)
+    gy = synth.dyadic((N, C, H, W), 20, 1, 6, 2)
+    algo = hc.HC_ALGO_TC_BF16X6
+    y = R.fwd(cfg, x, w, None, algo)
+    assert np.array_equal(y, x[:, perm])
+    out = R.bwd_subset(cfg, x, w, gy, ("gx",), algo)
+    inv = np.argsort(perm)
+    assert np.array_equal(out["gx"], gy[:, inv])
+
+
+@pytest.mark.parametrize("cfg", [P.cfg_of(2, 256, 4, 256, 256, 1, 1, 0, 1, 4),
+                                 P.cfg_of(2, 128, 8, 512, 128, 2, 2, 0, 1, 2),
+                                 P.cfg_of(1, 3, 16, 512, 128, 4, 4, 0, 1, 1)])
+def test_bf16x6_dyadic_exact(hc, orc, cfg):
+    """Multiples of 1/4 in [-4, 4]: every piece split and every fp32 sum of the
+    GEMMs is exact, so forward, grad_input, grad_weight and their per-shard
+    partials equal the oracle bit for bit (1x1, 2x2/s2, and a 4x4/s4 stem whose
+    48-deep K ends inside a 32-chunk)."""
+    Ho, Wo = R.out_hw(cfg)
+    x = synth.dyadic((cfg["N"], cfg["C_in"], cfg["H"], cfg["W"]), 2, 4, 8, 1)
+    w = synth.dyadic((cfg["C_out"], cfg["C_in"], cfg["kh"], cfg["kw"]), 2, 4, 8, 2)
+    b = synth.dyadic((cfg["C_out"],), 2, 4, 8, 3)
+    gy = synth.dyadic((cfg["N"], cfg["C_out"], Ho, Wo), 2, 4, 8, 4)
+    algo = hc.HC_ALGO_TC_BF16X6
+    assert hc.hc_conv2d_select(hc.desc(cfg), 1) == (0, algo)
+    assert np.array_equal(R.fwd(cfg, x, w, b, algo), orc.conv2d_fwd(cfg, x, w, b))
+    out = R.bwd(cfg, x, w, gy, algo)
+    assert np.array_equal(out["gx"], orc.conv2d_bwd_input(cfg, w, gy))
+    assert np.array_equal(out["gw"], orc.conv2d_bwd_weight(cfg, x, gy))
+    _, gwp_ref, _ = orc.sharded_bwd(cfg, x, w, gy)
+    assert np.array_equal(out["gw_partials"], gwp_ref.astype(np.float32))
 
 
 @pytest.mark.parametrize("want", [("gx",), ("gw",), ("gb",), ("gw", "gb"), ("gw_partials", "gb_partials"),
@@ -186,7 +279,8 @@ def test_backward_output_subsets(hc, orc, name, want):
         assert R.normwise(out[k], refs[k]()) <= tol, (k, R.normwise(out[k], refs[k]()))
 
 
-@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2"])
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2",
+                                  "pw_128to256_S4_half_pair"])
 def test_deterministic(hc, name):
     cfg, x, w, b, gy = CASES[name]()
     y1, y2 = R.fwd(cfg, x, w, b), R.fwd(cfg, x, w, b)
