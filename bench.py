@@ -81,13 +81,15 @@ def alu_peak(peaks, sms):
 
 
 class Runner:
-    """Device state shared by the workloads: the C ABI, a stream, one workspace,
-    and per-op CUDA events for the op breakdown."""
+    """Device state shared by the workloads: the C ABI, a stream, a workspace
+    shared by the backward passes and the pointwise ops, each conv's forward
+    workspace, and per-op CUDA events for the op breakdown."""
 
     def __init__(self, hc, torch, dev, stream):
         self.hc, self.torch, self.dev, self.stream = hc, torch, dev, stream
         self.ws = None
         self.ws_bytes = 0
+        self.fws = {}  # each conv's own forward workspace, kept for its backward pass
         self.mark = None  # when set: list collecting (name, start event, end event)
 
     def empty(self, shape):
@@ -112,18 +114,24 @@ class Runner:
         self.mark.append((name, e0, e1))
 
     def conv_fwd(self, d, x, w, b, y):
-        self.hc.check(self.hc.hc_conv2d_fwd(d, x, w, b, y, self.ws, self.ws_bytes, self.stream), "fwd")
+        fws, fnb = self.fws[id(d)]
+        self.hc.check(self.hc.hc_conv2d_fwd(d, x, w, b, y, fws, fnb, self.stream), "fwd")
 
     def conv_bwd(self, d, x, w, gy, gx, gw, gb):
-        self.hc.check(self.hc.hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, self.stream),
-                      "bwd")
+        # reads x's operand copy from the forward workspace (where the algorithm keeps one)
+        fws, fnb = self.fws[id(d)]
+        self.hc.check(self.hc.hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, fws,
+                                                  fnb, self.stream), "bwd")
 
     def conv_ws(self, d):
+        """Allocates the conv's forward workspace; returns the bytes its backward
+        pass needs from the shared workspace."""
         st, a = self.hc.hc_conv2d_workspace_size(d, 0)
         self.hc.check(st, "ws")
-        st, b = self.hc.hc_conv2d_workspace_size(d, 1)
+        st, b = self.hc.hc_conv2d_workspace_size(d, 2)
         self.hc.check(st, "ws")
-        return max(a, b, 16)
+        self.fws[id(d)] = (self.torch.empty(max(a, 16) // 4 + 64, dtype=self.torch.float32, device=self.dev), a)
+        return max(b, 16)
 
 
 class ConvWorkload:
@@ -164,8 +172,9 @@ class ConvWorkload:
         """Capture this workload's fwd + bwd step as one CUDA graph; returns (handle, kernels in it)."""
         R = self.R
         n0 = R.hc.hc_launch_count()
+        fws, fnb = R.fws[id(self.d)]
         st, g = R.hc.hc_conv2d_step_graph_create(self.d, self.x, self.w, self.b, self.y, self.gy, self.gx, self.gw,
-                                                 self.gb, R.ws, R.ws_bytes, R.ws, R.ws_bytes)
+                                                 self.gb, fws, fnb, R.ws, R.ws_bytes)
         R.hc.check(st, "graph create")
         return g, R.hc.hc_launch_count() - n0
 
@@ -257,8 +266,8 @@ class BlockWorkload:
 
     unit = "TFLOP/s"
 
-    def __init__(self, drop_path=0.0):
-        N, S = 7, 8
+    def __init__(self, drop_path=0.0, N=7):
+        S = 8
         self.N, self.S = N, S
         self.drop_path, self.steps_drawn = float(drop_path), 0
         self.stem = conv_cfg(N, 3, 512, 4096, 256, 4, 4, 0, 1, S)
@@ -275,8 +284,9 @@ class BlockWorkload:
         return {"workload": "ConvNeXt-XL stage-1 block fwd+bwd on the stem output of a (7,3,512,4096) U[0,1] image: "
                             "4x4/s4 stem 3->256, depthwise 7x7, LayerNorm(C), 1x1 256->1024, GELU, 1x1 1024->256, "
                             "layer scale 1e-6 + residual" + (f", DropPath {self.drop_path}" if self.drop_path else "") +
-                            "; fp32; 8 W-shards",
-                "shape": [7, 3, 512, 4096], "num_shards": 8, "l2": "activations (0.9-3.8 GB) larger than L2; no flush"}
+                            f"; fp32; 8 W-shards" + (f"; batch {self.N}" if self.N != 7 else ""),
+                "shape": [self.N, 3, 512, 4096], "num_shards": 8,
+                "l2": "activations (0.13-0.54 GB per image) larger than L2; no flush"}
 
     def setup(self, R):
         from spatially_sharded_cnn_gb300 import synth
@@ -367,22 +377,24 @@ class DwDownWorkload:
 
     unit = "TFLOP/s"
 
-    def __init__(self):
-        self.dw = conv_cfg(7, 256, 128, 2048, 256, 7, 1, 3, 256, 8)
-        self.down = conv_cfg(7, 256, 128, 2048, 512, 2, 2, 0, 1, 8)
+    def __init__(self, N=7):
+        self.N = N
+        self.dw = conv_cfg(N, 256, 128, 2048, 256, 7, 1, 3, 256, 8)
+        self.down = conv_cfg(N, 256, 128, 2048, 512, 2, 2, 0, 1, 8)
         self.flops = 3 * (conv_flops(self.dw) + conv_flops(self.down))
 
     def describe(self):
         return {"workload": "depthwise 7x7 (p3, groups=C) then 2x2/s2 downsample 256->512 fwd+bwd on x "
-                            "(7,256,128,2048) fp32, 8 W-shards of width 256",
-                "shape": [7, 256, 128, 2048], "num_shards": 8, "l2": "activations (1.9 GB) larger than L2; no flush"}
+                            f"({self.N},256,128,2048) fp32, 8 W-shards of width 256",
+                "shape": [self.N, 256, 128, 2048], "num_shards": 8,
+                "l2": "activations (0.27 GB per image) larger than L2; no flush"}
 
     def setup(self, R):
         from spatially_sharded_cnn_gb300 import synth
         self.R = R
         hc, t = R.hc, R.torch
-        self.h_x = synth.normal((7, 256, 128, 2048), 1.0, 0, 1)
-        self.h_gz = synth.normal((7, 512, 64, 1024), 1.0, 0, 9)
+        self.h_x = synth.normal((self.N, 256, 128, 2048), 1.0, 0, 1)
+        self.h_gz = synth.normal((self.N, 512, 64, 1024), 1.0, 0, 9)
         self.x, self.gz = R.upload(self.h_x), R.upload(self.h_gz)
         self.w_dw = R.upload(synth.trunc_normal((256, 1, 7, 7), 0.02, 0, 2))
         self.w_dn = R.upload(synth.trunc_normal((512, 256, 2, 2), 0.02, 0, 3))
@@ -424,7 +436,7 @@ class DwDownWorkload:
 
 
 def make_workload(name, batch=None, drop_path=0.0, shards_h=1):
-    """batch overrides N of the single-conv workloads (smaller cases for profiling);
+    """batch overrides N of every workload but config1 (smaller cases for profiling);
     shards_h > 1 also splits their rows (a row x column shard grid)."""
     N = batch or 7
     wl = _make_workload(name, N, drop_path)
@@ -448,9 +460,9 @@ def _make_workload(name, N, drop_path):
         return ConvWorkload("config1", conv_cfg(1, 4, 16, 32, 4, 5, 1, 2, 1, 4), gen_config1, "TFLOP/s",
                             "dense 5x5 conv 4->4 fwd+bwd, x (1,4,16,32) fp32, 4 W-shards of width 8")
     if name == "block":
-        return BlockWorkload(drop_path)
+        return BlockWorkload(drop_path, N)
     if name == "dwdown":
-        return DwDownWorkload()
+        return DwDownWorkload(N)
     raise ValueError(name)
 
 
@@ -586,7 +598,7 @@ def main():
                     help="block workload: DropPath probability (per-sample, shard-consistent draw each step)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each fwd+bwd step from one captured CUDA graph (single-conv workloads)")
-    ap.add_argument("--batch", type=int, default=None, help="batch size of the dw7 / dense5x5 workloads (default 7)")
+    ap.add_argument("--batch", type=int, default=None, help="batch size of every workload but config1 (default 7)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

@@ -110,9 +110,10 @@ hc_status hc_shard_plan(const hc_conv_desc* d, hc_shard_extent* ext, int* H_out,
  * HC_ERR_UNSUPPORTED as for hc_shard_plan, on H. */
 hc_status hc_shard_plan_rows(const hc_conv_desc* d, hc_shard_extent* ext);
 
-/* Workspace bytes that hc_conv2d_fwd (pass 0) or hc_conv2d_bwd (pass 1) needs
- * for this desc with HC_ALGO_AUTO (use hc_conv2d_workspace_size_algo for a
- * fixed algorithm).  Zero is a valid answer; ws may then be NULL. */
+/* Workspace bytes that hc_conv2d_fwd (pass 0), hc_conv2d_bwd (pass 1) or
+ * hc_conv2d_bwd_reuse (pass 2) needs for this desc with HC_ALGO_AUTO (use
+ * hc_conv2d_workspace_size_algo for a fixed algorithm).  Zero is a valid
+ * answer; ws may then be NULL. */
 hc_status hc_conv2d_workspace_size(const hc_conv_desc* d, int pass, size_t* bytes);
 hc_status hc_conv2d_workspace_size_algo(const hc_conv_desc* d, int pass, hc_algo algo, size_t* bytes);
 
@@ -153,6 +154,24 @@ hc_status hc_conv2d_bwd(const hc_conv_desc* d, const float* x, const float* w, c
 hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
                              float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
                              void* stream, hc_algo algo);
+
+/* Backward pass that reuses the forward pass's operand copy of x instead of
+ * rebuilding it (the way a training step keeps forward state for its
+ * backward pass).  With HC_ALGO_TC_BF16X6 the forward workspace begins with
+ * the bf16 pieces of x (or of its space-to-depth image), which the weight
+ * gradient reads; the other algorithms keep nothing between the passes, and
+ * for them the call is hc_conv2d_bwd_algo (fwd_ws is not read).
+ *   fwd_ws, fwd_ws_bytes: the workspace of the last hc_conv2d_fwd(_algo) call
+ *     with this desc, this x and the same algorithm, not written since; at
+ *     least hc_conv2d_workspace_size(d, 0) bytes, 256-byte aligned
+ *     (HC_ERR_INVALID_ARG if NULL or misaligned, HC_ERR_WORKSPACE if too
+ *     small, for HC_ALGO_TC_BF16X6).
+ *   ws, ws_bytes: at least hc_conv2d_workspace_size(d, 2) bytes.
+ * Every other argument as for hc_conv2d_bwd; the results are bit-identical to
+ * hc_conv2d_bwd's. */
+hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                              float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws,
+                              size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo);
 
 /* Halo exchange + concat made explicit (kwkr.cn 2.2 steps 1-2): for every
  * shard q of the row x column grid, x_ext[q] is its block of x with the halo
@@ -259,8 +278,12 @@ hc_status hc_layerscale_droppath_bwd(int N, int C, long long HW, const float* br
                                      const float* mask, const float* gy, float* gbranch, float* ggamma, void* ws,
                                      size_t ws_bytes, void* stream);
 
-/* One training step of a convolution -- hc_conv2d_fwd then hc_conv2d_bwd with
- * the automatic algorithm, every argument as in those calls -- captured into a
+/* One training step of a convolution -- hc_conv2d_fwd then, when ws_fwd and
+ * ws_bwd do not overlap, hc_conv2d_bwd_reuse (reading x's operand copy from
+ * ws_fwd; ws_bwd needs hc_conv2d_workspace_size(d, 2) bytes), else
+ * hc_conv2d_bwd (pass-1 bytes), with the automatic algorithm and every
+ * argument as in those calls; either way the results equal hc_conv2d_fwd +
+ * hc_conv2d_bwd -- captured into a
  * CUDA graph that replays with one launch (LibreYOLO documentation, page "Grafy
  * CUDA": a graph records a fixed kernel sequence and the addresses it uses;
  * replay must match eager execution bit for bit, which it does here since every

@@ -113,12 +113,13 @@ static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
 //   DEPTHWISE: [gw partials S*C*K*K][gb partials S*C][tile partials]
 //   TC_3XTF32: [gw partials][gb partials][bias scratch][NHWC hi/lo copies, weights hi/lo, split-K partials]
 //   TC_BF16X6: [gw partials][gb partials][bias scratch][bf16 pieces of gy, w^T, x; split-K partials]
-static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
+// reuse: the backward pass that takes x's operand copy from the forward workspace
+static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a, bool reuse = false) {
     size_t b = round256(sizeof(float) * p.Q * wsize(d)) + round256(sizeof(float) * p.Q * d->C_out);
     if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
     if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + tc_ws_bytes(d, p, 1);
     if (a == HC_ALGO_TC_BF16X6)
-        b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + bf16_ws_bytes(d, p, 1);
+        b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + bf16_ws_bytes(d, p, reuse ? 2 : 1);
     return b;
 }
 
@@ -129,13 +130,13 @@ static size_t fwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a) {
 }
 
 static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* bytes) {
-    if (!bytes || (pass != 0 && pass != 1)) return HC_ERR_INVALID_ARG;
+    if (!bytes || pass < 0 || pass > 2) return HC_ERR_INVALID_ARG;
     Plan p;
     hc_status st = make_plan(d, &p);
     if (st) return st;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
     if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
-    *bytes = pass == 0 ? fwd_ws_bytes(d, p, a) : bwd_ws_bytes(d, p, a);
+    *bytes = pass == 0 ? fwd_ws_bytes(d, p, a) : bwd_ws_bytes(d, p, a, pass == 2);
     return HC_OK;
 }
 
@@ -160,9 +161,11 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
     }
 }
 
+// fwd_ws (reuse only): the forward workspace of this desc and x, whose operand
+// copy of x the backward pass reads instead of rebuilding it
 static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
                      float* gb, float* gwp_out, float* gbp_out, void* ws, size_t ws_bytes, void* stream,
-                     hc_algo a) {
+                     hc_algo a, bool reuse = false, const void* fwd_ws = nullptr, size_t fwd_ws_bytes_given = 0) {
     static thread_local Plan p;
     hc_status st = make_plan(d, &p);
     if (st) return st;
@@ -172,7 +175,12 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
         if (q && !aligned16(q)) return HC_ERR_INVALID_ARG;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
     if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
-    const size_t need = bwd_ws_bytes(d, p, a);
+    reuse = reuse && a == HC_ALGO_TC_BF16X6;  // the other families keep nothing between the passes
+    if (reuse) {
+        if (!fwd_ws || ((uintptr_t)fwd_ws & 255)) return HC_ERR_INVALID_ARG;
+        if (fwd_ws_bytes_given < fwd_ws_bytes(d, p, a)) return HC_ERR_WORKSPACE;
+    }
+    const size_t need = bwd_ws_bytes(d, p, a, reuse);
     if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char* wsp = (char*)ws;
@@ -193,8 +201,9 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
             float* btmp = (float*)wsp;
             wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q));
             if (gx || want_w) {
-                st = a == HC_ALGO_TC_BF16X6 ? launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s)
-                                            : launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
+                st = a == HC_ALGO_TC_BF16X6
+                         ? launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, reuse ? fwd_ws : nullptr, s)
+                         : launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
                 if (st) return st;
             }
             if (want_b)
@@ -278,6 +287,13 @@ hc_status hc_conv2d_bwd_algo(const hc_conv_desc* d, const float* x, const float*
                              float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
                              void* stream, hc_algo algo) {
     return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo);
+}
+
+hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                              float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws,
+                              size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo) {
+    return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo, true, fwd_ws,
+               fwd_ws_bytes);
 }
 
 hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream) {

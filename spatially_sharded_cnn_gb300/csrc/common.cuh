@@ -87,12 +87,15 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 
 // 1x1 conv (stride 1, padding 0, groups 1) on tcgen05 with three bf16 pieces per
 // operand (six products, fp32 accuracy); C_in and C_out multiples of 128
+// (and k = stride convs as 1x1 convs of the space-to-depth image)
 bool bf16_supported(const hc_conv_desc* d, const Plan& p);
+// pass 2: the backward pass that takes x's pieces from the forward workspace
 size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
 hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                           float* y, void* ws, cudaStream_t st);
+// fwd_ws: the workspace of the forward pass on this desc and x, or NULL to split x here
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                          float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st);
+                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, cudaStream_t st);
 
 // Per-shard bias-gradient partials gbp[S][Co] in two fixed-order stages,
 // using tmp[bias_grad_ws_floats(Co, S)].

@@ -35,8 +35,16 @@ extern "C" hc_status hc_conv2d_step_graph_create(const hc_conv_desc* d, const fl
         cudaStreamDestroy(s);
         return HC_ERR_CUDA;
     }
+    // with separate workspaces the backward pass reads x's operand copy from the
+    // forward one where the algorithm keeps one (the results equal
+    // hc_conv2d_bwd's bit for bit); a shared buffer would be overwritten first
+    const char *f0 = (const char*)ws_fwd, *b0 = (const char*)ws_bwd;
+    const bool apart = !f0 || !b0 || f0 + ws_fwd_bytes <= b0 || b0 + ws_bwd_bytes <= f0;
     hc_status st = hc_conv2d_fwd(d, x, w, bias, y, ws_fwd, ws_fwd_bytes, (void*)s);
-    if (st == HC_OK) st = hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, nullptr, nullptr, ws_bwd, ws_bwd_bytes, (void*)s);
+    if (st == HC_OK)
+        st = apart ? hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, nullptr, nullptr, ws_bwd, ws_bwd_bytes, ws_fwd,
+                                         ws_fwd_bytes, (void*)s, HC_ALGO_AUTO)
+                   : hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, nullptr, nullptr, ws_bwd, ws_bwd_bytes, (void*)s);
     cudaGraph_t g = nullptr;
     const cudaError_t e = cudaStreamEndCapture(s, &g);
     cudaStreamDestroy(s);

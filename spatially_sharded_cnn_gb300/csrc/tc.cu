@@ -288,7 +288,9 @@ constexpr int TC_THREADS = 32 * (2 + TC_EPI_WARPS);
 
 // One persistent CTA per SM.  BN = accumulator columns (pixels of an output
 // row segment in conv mode, input channels in wgrad mode).
-template <int BN>
+// FMT: operand format (p.fmt), a template parameter so that each format's
+// instantiation carries only its own producer and MMA code.
+template <int BN, int FMT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_conv_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap ymap, TcParams p) {
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int s = (int)(it % p.stages);
                 if (it >= p.stages && !mbar_wait(&sh.empty[s], (unsigned)(((it / p.stages) - 1) & 1), abort_flag))
                     break;
-                if (p.fmt == 1) {
+                if (FMT == 1) {
                     // bf16 pieces: one box brings all three pieces of a tile
                     unsigned char* st = ring + (size_t)s * p.stage_bytes;
                     unsigned char* bdst = st + 3 * p.a_piece;
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = p.fmt == 1 ? idesc_bf16(BM, BN, 0, p.mode == 0 ? 1 : 0) : idesc_tf32(BM, BN, 0, 0);
+        const uint32_t idesc = FMT == 1 ? idesc_bf16(BM, BN, 0, p.mode == 0 ? 1 : 0) : idesc_tf32(BM, BN, 0, 0);
         long long it = 0;
         long long g = 0;  // group counter = TMEM buffer position
         bool ok = true;
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    if (p.fmt == 1) {
+                    if (FMT == 1) {
                         // A: K-major, 64-byte swizzle, 8-row groups 512 B apart (both modes).  B:
                         // conv mode MN-major, 128-byte swizzle, 64-pixel blocks BKH rows apart and
                         // 8-channel groups 1 KB apart; wgrad mode K-major like A.  Products a_i*b_j
@@ -1149,12 +1151,12 @@ int pick_bn(int out_w) {
     return 0;
 }
 
-template <int BN>
+template <int BN, int FMT>
 hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap, TcParams p,
                     cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(tc_conv_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX);
+        cudaFuncSetAttribute(tc_conv_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX);
         attr = true;
     }
     int smem;
@@ -1176,7 +1178,7 @@ hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUte
         smem = TC_SMEM_MAX;
     }
     const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
-    tc_conv_kernel<BN><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
+    tc_conv_kernel<BN, FMT><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
     return launched();
 }
 
@@ -1187,8 +1189,13 @@ hc_status launch_conv_pass(int BN, const CUtensorMap& amap, const CUtensorMap& b
     p.tma_store = ymap != nullptr;
     if (!ymap) ymap = &amap;  // unused
     p.group = 256 / BK;  // 256 k-values (96 MMAs) per TMEM accumulation group (BKH == BK)
-    if (BN == 256) return launch_bn<256>(amap, bmap, *ymap, p, st);
-    if (BN == 128) return launch_bn<128>(amap, bmap, *ymap, p, st);
+    if (p.fmt == 1) {
+        if (BN == 256) return launch_bn<256, 1>(amap, bmap, *ymap, p, st);
+        if (BN == 128) return launch_bn<128, 1>(amap, bmap, *ymap, p, st);
+    } else {
+        if (BN == 256) return launch_bn<256, 0>(amap, bmap, *ymap, p, st);
+        if (BN == 128) return launch_bn<128, 0>(amap, bmap, *ymap, p, st);
+    }
     return HC_ERR_UNSUPPORTED;
 }
 
@@ -1740,7 +1747,8 @@ bool bf16_supported(const hc_conv_desc* d, const Plan& p) {
 }
 
 // Workspace: forward  [x pieces][w pieces]
-//            backward [gy pieces][w^T pieces][x pieces][split-K partials]
+//            backward [gy pieces][w^T pieces][split-K partials][x pieces]; pass 2
+//            (x's pieces taken from the forward workspace) stops before x pieces
 size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     const Bf16View v = bf16_view(d, p);
     const size_t psx = piece_stride((long long)d->N * v.K * v.P), psg = piece_stride((long long)d->N * d->C_out * v.P);
@@ -1748,7 +1756,7 @@ size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     if (pass == 0) return al256(6 * psx) + al256(6 * psw);
     const int Kp = v.s2d ? s2d_kp(d) : d->C_in;  // partial row pitch: whole 128-column slots
     const size_t part = al256(4 * (size_t)p.Q * tc_wgrad_splits(d, p) * d->C_out * Kp);
-    return al256(6 * psg) + al256(6 * psw) + al256(6 * psx) + part;
+    return al256(6 * psg) + al256(6 * psw) + part + (pass == 2 ? 0 : al256(6 * psx));
 }
 
 static hc_status prep_x_pieces(const hc_conv_desc* d, const Plan& p, const Bf16View& v, const float* x, void* out,
@@ -1829,20 +1837,22 @@ hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, 
 }
 
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                          float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, cudaStream_t st) {
     const Bf16View v = bf16_view(d, p);
     const int Co = d->C_out;
     const long long wsz = (long long)Co * v.K;
     const long long psx = piece_stride((long long)d->N * v.K * v.P);
     const long long psg = piece_stride((long long)d->N * Co * v.P), psw = piece_stride(wsz);
+    const int Kp = v.s2d ? s2d_kp(d) : d->C_in;  // partial row pitch: whole 128-column slots
     char* q = (char*)ws;
     void* gp = q;
     q += al256(6 * psg);
     void* ap = q;
     q += al256(6 * psw);
-    void* xp = q;
-    q += al256(6 * psx);
     float* part = (float*)q;
+    q += al256(4 * (size_t)p.Q * tc_wgrad_splits(d, p) * Co * Kp);
+    // x's pieces: from the forward workspace (its first region) or built here
+    void* xp = fwd_ws ? const_cast<void*>(fwd_ws) : (void*)q;
     hc_status e;
     // grad_output's pieces serve both passes
     if ((e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st))) return e;
@@ -1882,8 +1892,7 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
         }
     }
     if (want_w) {  // G[co][k] = sum over a shard's pixels of gy[co][px] x'[k][px]
-        if ((e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
-        const int Kp = v.s2d ? s2d_kp(d) : d->C_in;
+        if (!fwd_ws && (e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
         TcParams tp{};
         tp.mode = 1;
         tp.fmt = 1;

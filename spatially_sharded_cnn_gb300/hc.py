@@ -74,6 +74,7 @@ _lib.hc_conv2d_fwd.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_conv2d_fwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_conv2d_bwd.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
+_lib.hc_conv2d_bwd_reuse.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_halo_gather.argtypes = [_D, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.restype = C.c_int
@@ -121,7 +122,7 @@ EXPORTS = [
     "hc_pointwise_workspace_size", "hc_layernorm_c_fwd", "hc_layernorm_c_bwd", "hc_gelu_fwd", "hc_gelu_bwd",
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
-    "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows",
+    "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
 ]
 
 
@@ -180,6 +181,14 @@ def hc_conv2d_bwd(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None, w
     if algo is None:
         return _lib.hc_conv2d_bwd(*args)
     return _lib.hc_conv2d_bwd_algo(*args, int(algo))
+
+
+def hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None, ws=None, ws_bytes=0,
+                        fwd_ws=None, fwd_ws_bytes=0, stream=None, algo=None) -> int:
+    """Backward pass reading x's operand copy from the forward workspace fwd_ws."""
+    return _lib.hc_conv2d_bwd_reuse(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw), _ptr(gb),
+                                    _ptr(gw_partials), _ptr(gb_partials), _ptr(ws), int(ws_bytes), _ptr(fwd_ws),
+                                    int(fwd_ws_bytes), _stream(stream), int(algo or HC_ALGO_AUTO))
 
 
 def hc_conv2d_bwd_depthwise_noalloc(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None,

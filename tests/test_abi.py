@@ -122,6 +122,28 @@ def test_algorithm_choice(hc):
     assert hc.hc_conv2d_select(odd, 0) == (0, hc.HC_ALGO_DIRECT)
 
 
+def test_bwd_reuse_arguments(hc):
+    """The reusing backward pass checks the forward workspace it is handed and
+    needs a smaller workspace of its own (no copy of x) for the bf16-piece GEMM;
+    other algorithms keep nothing, so their pass-2 size is the pass-1 size."""
+    pw = hc.desc(P.cfg_of(2, 256, 8, 256, 256, 1, 1, 0, 1, 2))
+    bf = hc.HC_ALGO_TC_BF16X6
+    st1, b1 = hc.hc_conv2d_workspace_size(pw, 1, bf)
+    st2, b2 = hc.hc_conv2d_workspace_size(pw, 2, bf)
+    st0, b0 = hc.hc_conv2d_workspace_size(pw, 0, bf)
+    assert st0 == st1 == st2 == 0 and b2 < b1 and b1 - b2 >= 6 * 2 * 256 * 8 * 256
+    assert hc.hc_conv2d_workspace_size(pw, 3, bf)[0] == hc.HC_ERR_INVALID_ARG
+    dense = hc.desc(P.cfg_of(1, 128, 8, 256, 128, 5, 1, 2, 1, 2))
+    assert hc.hc_conv2d_workspace_size(dense, 2)[1] == hc.hc_conv2d_workspace_size(dense, 1)[1]
+    call = lambda fws, fnb: hc.hc_conv2d_bwd_reuse(pw, 256, 256, 256, 256, 256, 256, None, None, 256, b2, fws, fnb,
+                                                   algo=bf)
+    assert call(None, b0) == hc.HC_ERR_INVALID_ARG      # no forward workspace
+    assert call(256 + 128, b0) == hc.HC_ERR_INVALID_ARG  # not 256-byte aligned
+    assert call(256, b0 - 1) == hc.HC_ERR_WORKSPACE     # too small
+    assert hc.hc_conv2d_bwd_reuse(pw, 256, 256, 256, 256, 256, 256, None, None, 256, b2 - 1, 256, b0,
+                                  algo=bf) == hc.HC_ERR_WORKSPACE
+
+
 def test_pointwise_algorithm_choice(hc):
     """1x1 convs with 128-multiple channels go to the bf16-piece GEMM; its
     operand copies take 6 bytes per element against 8 for tf32 hi / lo."""

@@ -279,6 +279,34 @@ def test_backward_output_subsets(hc, orc, name, want):
         assert R.normwise(out[k], refs[k]()) <= tol, (k, R.normwise(out[k], refs[k]()))
 
 
+@pytest.mark.parametrize("name", ["tc_1x1", "pw_128to256_S4_half_pair", "pw_grid_2x4", "tc_down2x2s2_S2",
+                                  "tc_stem4x4s4", "tc_5x5_S2", "dw7_ragged_S4"])
+def test_bwd_reuse_bit_identical(hc, name):
+    """hc_conv2d_bwd_reuse, reading x's operand copy from the forward workspace
+    (bf16 pieces; other families keep nothing), gives hc_conv2d_bwd's results
+    bit for bit, including the per-shard partials."""
+    cfg, x, w, b, gy = CASES[name]()
+    ref = R.bwd(cfg, x, w, gy)
+    d = hc.desc(cfg)
+    Ho, Wo = R.out_hw(cfg)
+    xd, wd, bd, gyd = R.dev(x), R.dev(w), R.dev(b), R.dev(gy)
+    y = torch.empty((cfg["N"], cfg["C_out"], Ho, Wo), device="cuda")
+    wsf, nbf = R.workspace(d, 0)
+    wsb, nbb = R.workspace(d, 2)
+    Q = R.num_partials(cfg)
+    gx = R.Guarded(x.shape)
+    gw = R.Guarded(w.shape)
+    gb = R.Guarded((cfg["C_out"],))
+    gwp = R.Guarded((Q,) + w.shape)
+    gbp = R.Guarded((Q, cfg["C_out"]))
+    hc.check(hc.hc_conv2d_fwd(d, xd, wd, bd, y, wsf, nbf), "fwd")
+    hc.check(hc.hc_conv2d_bwd_reuse(d, xd, wd, gyd, gx.view, gw.view, gb.view, gwp.view, gbp.view, wsb, nbb, wsf, nbf),
+             "bwd reuse")
+    hc.check(hc.hc_sync_check(), "sync")
+    for k, g in (("gx", gx), ("gw", gw), ("gb", gb), ("gw_partials", gwp), ("gb_partials", gbp)):
+        assert np.array_equal(g.numpy(), ref[k]), k
+
+
 @pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2",
                                   "pw_128to256_S4_half_pair"])
 def test_deterministic(hc, name):

@@ -31,7 +31,8 @@ def _eager(hc, cfg, x, w, b, gy):
     return y, out["gx"], out["gw"], out["gb"]
 
 
-@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "tc_5x5_S2", "tc_down2x2s2_S2", "stem4x4s4"])
+@pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "tc_5x5_S2", "tc_down2x2s2_S2", "stem4x4s4",
+                                  "tc_1x1"])
 def test_step_graph_bitwise(hc, orc, name):
     cfg, x, w, b, gy = CASES[name]()
     d = hc.desc(cfg)
@@ -64,6 +65,33 @@ def test_step_graph_bitwise(hc, orc, name):
         for got, want in zip((y, gx, gw, gb), ref):
             assert np.array_equal(got.cpu().numpy(), want)
         assert R.normwise(y.cpu().numpy(), orc.conv2d_fwd(cfg, x2, w, b)) <= 1e-5
+    finally:
+        hc.check(hc.hc_step_graph_destroy(g), "graph destroy")
+
+
+@pytest.mark.parametrize("name", ["tc_1x1", "tc_down2x2s2_S2"])
+def test_step_graph_shared_workspace(hc, orc, name):
+    """One buffer as both workspaces: the backward pass may not read x's operand
+    copy from the forward workspace (it overwrites it), so the graph runs the
+    plain backward pass -- same results."""
+    cfg, x, w, b, gy = CASES[name]()
+    d = hc.desc(cfg)
+    Ho, Wo = R.out_hw(cfg)
+    wshape = (cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"])
+    xd, wd, bd, gyd = R.dev(x), R.dev(w), R.dev(b), R.dev(gy)
+    y = torch.empty((cfg["N"], cfg["C_out"], Ho, Wo), device="cuda")
+    gx = torch.empty(x.shape, device="cuda")
+    gw = torch.empty(wshape, device="cuda")
+    gb = torch.empty((cfg["C_out"],), device="cuda")
+    nb = max(R.workspace(d, 0)[1], R.workspace(d, 1)[1])
+    ws = torch.empty(nb // 4 + 64, device="cuda")
+    st, g = hc.hc_conv2d_step_graph_create(d, xd, wd, bd, y, gyd, gx, gw, gb, ws, nb, ws, nb)
+    hc.check(st, "graph create")
+    try:
+        hc.check(hc.hc_step_graph_launch(g), "graph launch")
+        hc.check(hc.hc_sync_check(), "graph sync")
+        for got, want in zip((y, gx, gw, gb), _eager(hc, cfg, x, w, b, gy)):
+            assert np.array_equal(got.cpu().numpy(), want)
     finally:
         hc.check(hc.hc_step_graph_destroy(g), "graph destroy")
 
