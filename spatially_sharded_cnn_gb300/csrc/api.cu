@@ -200,13 +200,18 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
         case HC_ALGO_TC_BF16X6: {
             float* btmp = (float*)wsp;
             wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q));
+            bool bias_done = false;
             if (gx || want_w) {
-                st = a == HC_ALGO_TC_BF16X6
-                         ? launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, reuse ? fwd_ws : nullptr, s)
-                         : launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
+                if (a == HC_ALGO_TC_BF16X6) {  // the bias partials come with grad_output's pieces
+                    st = launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, reuse ? fwd_ws : nullptr,
+                                         want_b ? gbp : nullptr, btmp, s);
+                    bias_done = true;
+                } else {
+                    st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
+                }
                 if (st) return st;
             }
-            if (want_b)
+            if (want_b && !bias_done)
                 st = launch_bias_grad_partials(gy, gbp, d->N, d->C_out, p.Ho, p.Wo, p.S, p.Wl / d->stride, p.Sh, p.Hlo,
                                                btmp, s);
             break;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,6 +53,31 @@ hc_status dw_take_status();
 hc_status tc_take_status();
 hc_status launch_selftest_timeout(int wait_us, cudaStream_t st);
 
+// fp32 -> three bf16 pieces, the operand format of HC_ALGO_TC_BF16X6:
+// p0 = bf16(v), p1 = bf16(v - p0), p2 = bf16(v - p0 - p1); the two differences
+// are exact in fp32, and the pieces carry 24 bits of v's significand.
+__device__ __forceinline__ void split3(float v, __nv_bfloat16& p0, __nv_bfloat16& p1, __nv_bfloat16& p2) {
+    p0 = __float2bfloat16_rn(v);
+    const float r = v - __bfloat162float(p0);
+    p1 = __float2bfloat16_rn(r);
+    p2 = __float2bfloat16_rn(r - __bfloat162float(p1));
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+// The pieces of four consecutive values (float4 number i): out[k * ps4 + i] holds
+// piece k of all four.
+__device__ __forceinline__ void store_pieces4(float4 v, uint2* out, long long i, long long ps4) {
+    __nv_bfloat16 a[4], b[4], c[4];
+    split3(v.x, a[0], b[0], c[0]);
+    split3(v.y, a[1], b[1], c[1]);
+    split3(v.z, a[2], b[2], c[2]);
+    split3(v.w, a[3], b[3], c[3]);
+    out[i] = make_uint2(pack2(a[0], a[1]), pack2(a[2], a[3]));
+    out[ps4 + i] = make_uint2(pack2(b[0], b[1]), pack2(b[2], b[3]));
+    out[2 * ps4 + i] = make_uint2(pack2(c[0], c[1]), pack2(c[2], c[3]));
+}
+
 // ---- kernel launchers (one translation unit each) -------------------------
 hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* x, float* x_ext, cudaStream_t st);
 
@@ -94,8 +120,10 @@ size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
 hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                           float* y, void* ws, cudaStream_t st);
 // fwd_ws: the workspace of the forward pass on this desc and x, or NULL to split x here
+// gbp (optional): also the bias-gradient partials, with tmp[bias_grad_ws_floats]
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, cudaStream_t st);
+                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, float* gbp,
+                          float* btmp, cudaStream_t st);
 
 // Per-shard bias-gradient partials gbp[S][Co] in two fixed-order stages,
 // using tmp[bias_grad_ws_floats(Co, S)].
@@ -103,8 +131,11 @@ constexpr int kBiasSlices = 64;
 size_t bias_grad_ws_floats(int Co, int S);
 // gbp [Sh*S][Co]: row shard a owns output rows [a*own_h, (a+1)*own_h) (the last
 // up to Ho), column shard b columns [b*own_w, (b+1)*own_w) (the last up to Wo)
+// pieces (optional): also writes the bf16 pieces of gy there (piece k of element
+// e at pieces[k * ps + e], ps a multiple of 4) while reading it -- the same sums
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
-                                    int Sh, int own_h, float* tmp, cudaStream_t st);
+                                    int Sh, int own_h, float* tmp, cudaStream_t st, void* pieces = nullptr,
+                                    long long ps = 0);
 
 // out[k] = sum over rows r (ascending, in groups of kColumnGroup) of in[r * stride + k];
 // tmp holds column_sum_tmp_floats(rows, count) floats.

@@ -29,10 +29,12 @@ __global__ void sum_rows_kernel(const float* __restrict__ in, float* __restrict_
 // column shard b (shard of column j = j / own_w, the last shard taking the
 // rest) in column order.  Every sum has a fixed order.
 // part[(slice * Sh * S + a * S + b) * Co + co].  Needs Wo % 4 == 0, S <= 256,
-// 256 threads.
+// 256 threads.  PIECES: every float4 read also goes out as bf16 pieces
+// (store_pieces4 at its own index), so one pass over grad_output serves both.
+template <bool PIECES>
 __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict__ gy, float* __restrict__ part, int N,
                                                         int Co, int Ho, int Wo, int S, int own_w, int Sh, int own_h,
-                                                        int slices) {
+                                                        int slices, uint2* __restrict__ pieces, long long ps4) {
     __shared__ float cs[256];
     const int a = blockIdx.x / slices, slice = blockIdx.x - a * slices, co = blockIdx.y, tid = threadIdx.x;
     const int i0 = a * own_h, i1 = (a == Sh - 1) ? Ho : i0 + own_h, rows_a = i1 - i0;
@@ -43,14 +45,19 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
         const int col = g0 + 4 * tid;
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (col < Wo) {
-            const float* base = gy + (long long)co * Ho * Wo + col;
             int row = r0;
             for (; row + 4 <= r1; row += 4) {  // four loads in flight, added in row order
                 float4 v[4];
+                long long e[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const int n = (row + k) / rows_a, i = i0 + row + k - n * rows_a;
-                    v[k] = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
+                    e[k] = (long long)co * Ho * Wo + col + ((long long)n * Co * Ho + i) * Wo;
+                    v[k] = __ldg(reinterpret_cast<const float4*>(gy + e[k]));
+                }
+                if (PIECES) {
+#pragma unroll
+                    for (int k = 0; k < 4; k++) store_pieces4(v[k], pieces, e[k] / 4, ps4);
                 }
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
@@ -62,7 +69,9 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
             }
             for (; row < r1; row++) {
                 const int n = row / rows_a, i = i0 + row - n * rows_a;
-                const float4 v = __ldg(reinterpret_cast<const float4*>(base + ((long long)n * Co * Ho + i) * Wo));
+                const long long e = (long long)co * Ho * Wo + col + ((long long)n * Co * Ho + i) * Wo;
+                const float4 v = __ldg(reinterpret_cast<const float4*>(gy + e));
+                if (PIECES) store_pieces4(v, pieces, e / 4, ps4);
                 acc.x += v.x;
                 acc.y += v.y;
                 acc.z += v.z;
@@ -116,8 +125,8 @@ hc_status launch_column_sum(const float* in, float* out, int rows, int count, lo
 size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co; }
 
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
-                                    int Sh, int own_h, float* tmp, cudaStream_t st) {
-    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || Sh < 1 || (long long)N * Ho > 0x7fffffffLL)
+                                    int Sh, int own_h, float* tmp, cudaStream_t st, void* pieces, long long ps) {
+    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || Sh < 1 || (long long)N * Ho > 0x7fffffffLL || ps % 4)
         return HC_ERR_UNSUPPORTED;
     // about eight blocks per SM, at most kBiasSlices slices per row shard
     const long long rows_min = (long long)N * (Sh > 1 ? own_h : Ho);
@@ -126,8 +135,13 @@ hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, 
     if (slices > rows_min) slices = rows_min;
     if (slices < 1) slices = 1;
     if ((long long)slices * Sh > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-    bias_rows_kernel<<<dim3((unsigned)(slices * Sh), Co), 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h,
-                                                                          (int)slices);
+    const dim3 grid((unsigned)(slices * Sh), Co);
+    if (pieces)
+        bias_rows_kernel<true><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
+                                                     reinterpret_cast<uint2*>(pieces), ps / 4);
+    else
+        bias_rows_kernel<false><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
+                                                      nullptr, 0);
     hc_status s = launched();
     if (s) return s;
     return launch_sum_rows(tmp, gbp, (int)slices, (long long)Sh * S * Co, st);  // slices in order

@@ -56,8 +56,6 @@
 // copies and MMAs, frees its tensor memory and exits.
 #include "common.cuh"
 
-#include <cuda_bf16.h>
-
 namespace hc {
 namespace {
 
@@ -1018,31 +1016,13 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __res
     }
 }
 
-// fp32 -> three bf16 pieces, piece k of value i at out[k * ps + i]:
-// p0 = bf16(v), p1 = bf16(v - p0), p2 = bf16(v - p0 - p1); the two differences
-// are exact in fp32, and the pieces carry 24 bits of v's significand.
-__device__ __forceinline__ void split3(float v, __nv_bfloat16& p0, __nv_bfloat16& p1, __nv_bfloat16& p2) {
-    p0 = __float2bfloat16_rn(v);
-    const float r = v - __bfloat162float(p0);
-    p1 = __float2bfloat16_rn(r);
-    p2 = __float2bfloat16_rn(r - __bfloat162float(p1));
-}
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
-// Elementwise over n4 float4s (the layout is kept); ps4 = piece stride / 4.
+// fp32 -> three bf16 pieces (split3, common.cuh), piece k of value i at
+// out[k * ps + i].  Elementwise over n4 float4s (the layout is kept); ps4 =
+// piece stride / 4.
 __global__ void __launch_bounds__(256) prep_pieces_kernel(const float4* __restrict__ x, uint2* __restrict__ out,
                                                           long long n4, long long ps4) {
     for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += (long long)gridDim.x * 256) {
-        const float4 v = __ldg(x + i);
-        __nv_bfloat16 a[4], b[4], c[4];
-        split3(v.x, a[0], b[0], c[0]);
-        split3(v.y, a[1], b[1], c[1]);
-        split3(v.z, a[2], b[2], c[2]);
-        split3(v.w, a[3], b[3], c[3]);
-        out[i] = make_uint2(pack2(a[0], a[1]), pack2(a[2], a[3]));
-        out[ps4 + i] = make_uint2(pack2(b[0], b[1]), pack2(b[2], b[3]));
-        out[2 * ps4 + i] = make_uint2(pack2(c[0], c[1]), pack2(c[2], c[3]));
+        store_pieces4(__ldg(x + i), out, i, ps4);
     }
 }
 // Transposed pieces of a small R x C matrix: out[k * ps + c * R + r] = piece k of w[r * C + c].
@@ -1778,6 +1758,14 @@ static hc_status prep_x_pieces(const hc_conv_desc* d, const Plan& p, const Bf16V
     return launched();
 }
 
+// Output stores of a bf16 conv pass: a short K (under 16 chunks) leaves the
+// 128 KB output tile of a unit a large share of the copy traffic, and the TMA
+// store boxes win; a long K gains more from the third ring stage that plain
+// per-thread stores leave room for (measured on the block's 1x1 and stem convs).
+static const CUtensorMap* bf16_store_map(const TcParams& tp, const CUtensorMap* my) {
+    return tp.chunks < 16 ? my : nullptr;
+}
+
 // The conv-pass tiling: flat rows of BN pixels (1x1) or BN-column segments of
 // output rows (space-to-depth).
 static void bf16_tiles(const Plan& p, const Bf16View& v, TcParams& tp, int* BN) {
@@ -1833,11 +1821,12 @@ hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, 
     if ((e = pieces_weight_map(&ma, ap, Co, v.K, psw)) || (e = pieces_mn_map(&mb, xp, d->N, v.K, v.P, BN, psx)) ||
         (e = out_map(&my, y, d->N, Co, tp.Ho, tp.Wo)))
         return e;
-    return launch_conv_pass(BN, ma, mb, tp, st, &my);
+    return launch_conv_pass(BN, ma, mb, tp, st, bf16_store_map(tp, &my));
 }
 
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, cudaStream_t st) {
+                          float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, float* gbp,
+                          float* btmp, cudaStream_t st) {
     const Bf16View v = bf16_view(d, p);
     const int Co = d->C_out;
     const long long wsz = (long long)Co * v.K;
@@ -1854,8 +1843,14 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
     // x's pieces: from the forward workspace (its first region) or built here
     void* xp = fwd_ws ? const_cast<void*>(fwd_ws) : (void*)q;
     hc_status e;
-    // grad_output's pieces serve both passes
-    if ((e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st))) return e;
+    // grad_output's pieces serve both passes; the bias-gradient partials, when
+    // asked for, are summed in the same read of grad_output
+    if (gbp)
+        e = launch_bias_grad_partials(gy, gbp, d->N, Co, p.Ho, p.Wo, p.S, p.Wl / v.s, p.Sh, p.Hlo, btmp, st, gp,
+                                      psg);
+    else
+        e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st);
+    if (e) return e;
     if (gx) {  // D[m][px] = sum_co w^T[m][co] gy[co][px], m = ci (1x1) or (u*C + c)*s + v (depth-to-space)
         if (v.s2d)
             prep_weight_s2d_pieces_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, v.s,
@@ -1888,7 +1883,7 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
             if ((e = launch_conv_pass(BN, ma, mb, tp, st))) return e;
         } else {
             if ((e = out_map(&my, gx, d->N, v.K, 1, (int)v.P))) return e;
-            if ((e = launch_conv_pass(BN, ma, mb, tp, st, &my))) return e;
+            if ((e = launch_conv_pass(BN, ma, mb, tp, st, bf16_store_map(tp, &my)))) return e;
         }
     }
     if (want_w) {  // G[co][k] = sum over a shard's pixels of gy[co][px] x'[k][px]
