@@ -213,10 +213,10 @@ class ConvWorkload:
         if self.dense:
             peak = tc_peak(peaks)
             a = conv_flops(self.cfg) / (ops_ms["conv_fwd"] * 1e-3) / 1e12
-            return {"bound": "tensor", "kernel": "tc_conv_kernel<256> (forward call incl. operand prep)",
+            return {"bound": "tensor", "kernel": "tc_conv_kernel<256, 0> (3xTF32; forward call incl. operand prep)",
                     "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
-                    "traffic": traffic_for("tc_conv_kernel<256>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
-                                                                               "csrc", "tc.cu")),
+                    "traffic": traffic_for("tc_conv_kernel<256, 0>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
+                                                                                  "csrc", "tc.cu")),
                     "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
                     "ms_per_launch": ops_ms["conv_fwd"]}
         alu = alu_peak(peaks, sms)
@@ -365,9 +365,11 @@ class BlockWorkload:
         peak = bf16x6_peak(peaks)
         a = conv_flops(self.pw1) / (ops_ms["pw1_fwd"] * 1e-3) / 1e12
         return {"bound": "tensor",
-                "kernel": "tc_conv_kernel<256> on bf16 pieces (1x1 256->1024 forward call incl. operand prep)",
+                "kernel": "tc_conv_kernel<256, 1> on bf16 pieces (1x1 256->1024 forward call incl. operand prep)",
                 "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, six bf16 products)",
-                "frac": a / peak, "traffic": None,
+                "frac": a / peak,
+                "traffic": traffic_for("tc_conv_kernel<256, 1>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
+                                                                              "csrc", "tc.cu")),
                 "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s / 6 (bf16 products per fp32 product)",
                 "ms_per_launch": ops_ms["pw1_fwd"]}
 
