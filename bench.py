@@ -17,7 +17,8 @@ Workloads (--workload):
             U[0,1] image, 8 W-shards: 4x4/s4 stem 3->256, depthwise 7x7,
             LayerNorm over C, 1x1 256->1024, GELU, 1x1 1024->256, layer scale
             1e-6 + residual; forward + backward; TFLOP/s of the conv FLOPs
-            (stem and 1x1 convs on the bf16-piece tensor-core GEMM).
+            (stem and 1x1 convs on the bf16-piece tensor-core GEMM; the GELU
+            folded into the 1x1 convs' operand splits, forward and backward).
   dwdown    depthwise 7x7 then 2x2/s2 downsample 256->512 on x
             (7,256,128,2048), 8 W-shards; forward + backward; TFLOP/s.
 All inputs are larger than the 129 MB L2, so no flush is needed between steps.
@@ -122,6 +123,25 @@ class Runner:
         fws, fnb = self.fws[id(d)]
         self.hc.check(self.hc.hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, fws,
                                                   fnb, self.stream), "bwd")
+
+    def conv_fwd_gelu(self, d, x, w, b, y):
+        """The conv of GELU(x), GELU applied as x's operand pieces are made."""
+        fws, fnb = self.fws[id(d)]
+        self.hc.check(self.hc.hc_conv2d_fwd_act(d, x, w, b, y, fws, fnb, self.stream, act=self.hc.HC_ACT_GELU_INPUT),
+                      "fwd gelu")
+
+    def conv_bwd_gelu(self, d, x, w, gy, gx, gw, gb):
+        """Backward of conv_fwd_gelu: gx is the gradient with respect to GELU(x)."""
+        fws, fnb = self.fws[id(d)]
+        self.hc.check(self.hc.hc_conv2d_bwd_act(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, fws, fnb,
+                                                self.stream, act=self.hc.HC_ACT_GELU_INPUT), "bwd gelu in")
+
+    def conv_bwd_gelu_out(self, d, x, w, gy, y_pre, gx, gw, gb):
+        """Backward of a conv whose output y_pre feeds a GELU; gy is the gradient of GELU(y_pre)."""
+        fws, fnb = self.fws[id(d)]
+        self.hc.check(self.hc.hc_conv2d_bwd_act(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, fws, fnb,
+                                                self.stream, act=self.hc.HC_ACT_GELU_OUTPUT, y_pre=y_pre),
+                      "bwd gelu out")
 
     def conv_ws(self, d):
         """Allocates the conv's forward workspace; returns the bytes its backward
@@ -307,7 +327,7 @@ class BlockWorkload:
         a256, a1024 = (N, 256, 128, 1024), (N, 1024, 128, 1024)
         self.s, self.dwo, self.ln, self.b2, self.out = (R.empty(a256) for _ in range(5))
         self.mean, self.rstd = R.empty((N, HW)), R.empty((N, HW))
-        self.h, self.a = R.empty(a1024), R.empty(a1024)
+        self.h = R.empty(a1024)  # the 1x1 256->1024 output; GELU(h) is never stored
         self.g_b2, self.g_l, self.g_d, self.g_s = (R.empty(a256) for _ in range(4))
         self.g_a = R.empty(a1024)
         self.gw_stem, self.gb_stem = t.empty_like(self.w_stem), t.empty(256, device=R.dev)
@@ -327,8 +347,8 @@ class BlockWorkload:
         R.op("ln_fwd", lambda: hc.check(hc.hc_layernorm_c_fwd(N, 256, HW, self.dwo, self.ln_g, self.ln_b, 1e-6, self.ln,
                                                               self.mean, self.rstd, R.stream)))
         R.op("pw1_fwd", lambda: R.conv_fwd(self.d["pw1"], self.ln, self.w1, self.b1024, self.h))
-        R.op("gelu_fwd", lambda: hc.check(hc.hc_gelu_fwd(N * 1024 * HW, self.h, self.a, R.stream)))
-        R.op("pw2_fwd", lambda: R.conv_fwd(self.d["pw2"], self.a, self.w2, self.b256, self.b2))
+        # GELU goes into the 1x1 1024->256's operand split (hc_conv2d_fwd_act)
+        R.op("gelu_pw2_fwd", lambda: R.conv_fwd_gelu(self.d["pw2"], self.h, self.w2, self.b256, self.b2))
         if self.drop_path:  # a fresh per-sample draw each step: offset = samples drawn so far
             R.op("drop_path_mask", lambda: hc.check(hc.hc_drop_path_mask(N, self.drop_path, 2024, self.steps_drawn * N,
                                                                          self.mask, R.stream)))
@@ -341,9 +361,12 @@ class BlockWorkload:
         R.op("ls_bwd", lambda: hc.check(hc.hc_layerscale_droppath_bwd(N, 256, HW, self.b2, self.ls_g, self.mask,
                                                                       self.gy, self.g_b2, self.g_ls, R.ws, R.ws_bytes,
                                                                       R.stream)))
-        R.op("pw2_bwd", lambda: R.conv_bwd(self.d["pw2"], self.a, self.w2, self.g_b2, self.g_a, self.gw2, self.gb2))
-        R.op("gelu_bwd", lambda: hc.check(hc.hc_gelu_bwd(N * 1024 * HW, self.h, self.g_a, self.g_a, R.stream)))
-        R.op("pw1_bwd", lambda: R.conv_bwd(self.d["pw1"], self.ln, self.w1, self.g_a, self.g_l, self.gw1, self.gb1))
+        # the 1x1 1024->256's grad_input is the gradient with respect to GELU(h); the
+        # 1x1 256->1024's backward runs on it times GELU'(h), formed as it is read
+        R.op("pw2_bwd", lambda: R.conv_bwd_gelu(self.d["pw2"], self.h, self.w2, self.g_b2, self.g_a, self.gw2,
+                                                self.gb2))
+        R.op("gelu_pw1_bwd", lambda: R.conv_bwd_gelu_out(self.d["pw1"], self.ln, self.w1, self.g_a, self.h, self.g_l,
+                                                         self.gw1, self.gb1))
         R.op("ln_bwd", lambda: hc.check(hc.hc_layernorm_c_bwd(N, 256, HW, self.dwo, self.ln_g, self.mean, self.rstd,
                                                               self.g_l, self.g_d, self.g_lng, self.g_lnb, R.ws,
                                                               R.ws_bytes, R.stream)))

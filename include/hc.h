@@ -173,6 +173,49 @@ hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float
                               float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws,
                               size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo);
 
+/* A GELU (exact form, hc_gelu_fwd) next to a convolution, folded into the
+ * passes that read the tensor it touches -- the MLP pattern 1x1 -> GELU -> 1x1
+ * of a ConvNeXt block, with h the first conv's output:
+ *   second conv:  hc_conv2d_fwd_act(..., x = h, HC_ACT_GELU_INPUT) and
+ *                 hc_conv2d_bwd_act(..., HC_ACT_GELU_INPUT), whose grad_input is
+ *                 the gradient with respect to GELU(h);
+ *   first conv:   hc_conv2d_fwd (its output is h) and hc_conv2d_bwd_act(...,
+ *                 gy = that gradient, HC_ACT_GELU_OUTPUT, y_pre = h), which runs on
+ *                 gy * GELU'(h), the gradient with respect to h.
+ * GELU(h) and the separate GELU backward pass are never materialised. */
+typedef enum {
+    HC_ACT_NONE = 0,
+    HC_ACT_GELU_INPUT = 1,  /* the conv's input is GELU(x) */
+    HC_ACT_GELU_OUTPUT = 2  /* the conv's output y feeds GELU(y) */
+} hc_act;
+
+/* Forward pass with a GELU: HC_ACT_GELU_INPUT gives y = conv(GELU(x)) + bias,
+ * GELU(x) going straight into the operand pieces as x is read;
+ * HC_ACT_GELU_OUTPUT and HC_ACT_NONE give the plain conv (the output is the
+ * pre-activation).  GELU needs HC_ALGO_TC_BF16X6 (or HC_ALGO_AUTO picking it)
+ * and a 1x1 stride-1 conv, else HC_ERR_UNSUPPORTED.  Arguments and workspace as
+ * for hc_conv2d_fwd. */
+hc_status hc_conv2d_fwd_act(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                            void* ws, size_t ws_bytes, void* stream, hc_algo algo, hc_act act);
+
+/* Backward pass with a GELU:
+ *   HC_ACT_GELU_INPUT: the backward of hc_conv2d_fwd_act(HC_ACT_GELU_INPUT): gw,
+ *     gb of the conv on GELU(x); gx = the gradient with respect to the conv's
+ *     input GELU(x) (GELU'(x) is left to the consumer: the first conv's
+ *     HC_ACT_GELU_OUTPUT backward, or hc_gelu_bwd).  y_pre is not read.
+ *   HC_ACT_GELU_OUTPUT: gy is the gradient with respect to GELU(y_pre), y_pre
+ *     ([N][C_out][H_out][W_out]) the conv's output; the pass runs on
+ *     gy * GELU'(y_pre), formed as gy is read, and gx, gw, gb, partials are the
+ *     conv's gradients for it (HC_ERR_INVALID_ARG if y_pre is NULL).
+ * fwd_ws: the workspace of this conv's forward call (hc_conv2d_fwd_act with the
+ * same desc, x and act, or hc_conv2d_fwd for HC_ACT_GELU_OUTPUT), read as by
+ * hc_conv2d_bwd_reuse (ws then needs pass-2 bytes), or NULL (pass-1 bytes).
+ * Same support rule as hc_conv2d_fwd_act. */
+hc_status hc_conv2d_bwd_act(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                            float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
+                            const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo, hc_act act,
+                            const float* y_pre);
+
 /* Halo exchange + concat made explicit (kwkr.cn 2.2 steps 1-2): for every
  * shard q of the row x column grid, x_ext[q] is its block of x with the halo
  * rows above / below (hc_shard_plan_rows) and halo columns left / right

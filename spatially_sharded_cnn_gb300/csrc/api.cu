@@ -140,21 +140,29 @@ static hc_status ws_size(const hc_conv_desc* d, int pass, hc_algo a, size_t* byt
     return HC_OK;
 }
 
+// act: a GELU on the conv's input (HC_ACT_GELU_INPUT) or output
+// (HC_ACT_GELU_OUTPUT), folded into the bf16-piece 1x1 convs' operand splits
+static bool act_supported(const hc_conv_desc* d, hc_algo a, hc_act act) {
+    if (act == HC_ACT_NONE) return true;
+    return (act == HC_ACT_GELU_INPUT || act == HC_ACT_GELU_OUTPUT) && a == HC_ALGO_TC_BF16X6 && d->kh == 1 &&
+           d->kw == 1 && d->stride == 1;
+}
+
 static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, const float* b, float* y, void* ws,
-                     size_t ws_bytes, void* stream, hc_algo a) {
+                     size_t ws_bytes, void* stream, hc_algo a, hc_act act = HC_ACT_NONE) {
     static thread_local Plan p;
     hc_status st = make_plan(d, &p);
     if (st) return st;
     if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y) || (b && !aligned16(b)))
         return HC_ERR_INVALID_ARG;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
-    if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
+    if (!algo_supported(d, p, a) || !act_supported(d, a, act)) return HC_ERR_UNSUPPORTED;
     const size_t need = fwd_ws_bytes(d, p, a);
     if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     switch (a) {
         case HC_ALGO_TC_3XTF32: return launch_tc_fwd(d, p, x, w, b, y, ws, s);
-        case HC_ALGO_TC_BF16X6: return launch_bf16_fwd(d, p, x, w, b, y, ws, s);
+        case HC_ALGO_TC_BF16X6: return launch_bf16_fwd(d, p, x, w, b, y, ws, s, act == HC_ACT_GELU_INPUT);
         case HC_ALGO_DEPTHWISE: return launch_depthwise_fwd(d, p, x, w, b, y, s);
         case HC_ALGO_DIRECT: return launch_direct_fwd(d, p, x, w, b, y, s);
         default: return HC_ERR_UNSUPPORTED;
@@ -165,7 +173,8 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
 // copy of x the backward pass reads instead of rebuilding it
 static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
                      float* gb, float* gwp_out, float* gbp_out, void* ws, size_t ws_bytes, void* stream,
-                     hc_algo a, bool reuse = false, const void* fwd_ws = nullptr, size_t fwd_ws_bytes_given = 0) {
+                     hc_algo a, bool reuse = false, const void* fwd_ws = nullptr, size_t fwd_ws_bytes_given = 0,
+                     hc_act act = HC_ACT_NONE, const float* y_pre = nullptr) {
     static thread_local Plan p;
     hc_status st = make_plan(d, &p);
     if (st) return st;
@@ -174,7 +183,8 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
                           (const void*)gbp_out})
         if (q && !aligned16(q)) return HC_ERR_INVALID_ARG;
     if (a == HC_ALGO_AUTO) a = pick(d, p);
-    if (!algo_supported(d, p, a)) return HC_ERR_UNSUPPORTED;
+    if (!algo_supported(d, p, a) || !act_supported(d, a, act)) return HC_ERR_UNSUPPORTED;
+    if (act == HC_ACT_GELU_OUTPUT && (!y_pre || !aligned16(y_pre))) return HC_ERR_INVALID_ARG;
     reuse = reuse && a == HC_ALGO_TC_BF16X6;  // the other families keep nothing between the passes
     if (reuse) {
         if (!fwd_ws || ((uintptr_t)fwd_ws & 255)) return HC_ERR_INVALID_ARG;
@@ -201,10 +211,12 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
             float* btmp = (float*)wsp;
             wsp += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q));
             bool bias_done = false;
-            if (gx || want_w) {
+            // (a GELU on the output changes grad_output itself: the bias then comes from its split too)
+            if (gx || want_w || (want_b && act == HC_ACT_GELU_OUTPUT)) {
                 if (a == HC_ALGO_TC_BF16X6) {  // the bias partials come with grad_output's pieces
                     st = launch_bf16_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, reuse ? fwd_ws : nullptr,
-                                         want_b ? gbp : nullptr, btmp, s);
+                                         want_b ? gbp : nullptr, btmp, s, act == HC_ACT_GELU_INPUT,
+                                         act == HC_ACT_GELU_OUTPUT ? y_pre : nullptr);
                     bias_done = true;
                 } else {
                     st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
@@ -299,6 +311,19 @@ hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float
                               size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo) {
     return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo, true, fwd_ws,
                fwd_ws_bytes);
+}
+
+hc_status hc_conv2d_fwd_act(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,
+                            void* ws, size_t ws_bytes, void* stream, hc_algo algo, hc_act act) {
+    return fwd(d, x, w, bias, y, ws, ws_bytes, stream, algo, act);
+}
+
+hc_status hc_conv2d_bwd_act(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx,
+                            float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws, size_t ws_bytes,
+                            const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo, hc_act act,
+                            const float* y_pre) {
+    return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo, fwd_ws != nullptr,
+               fwd_ws, fwd_ws_bytes, act, y_pre);
 }
 
 hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream) {

@@ -53,6 +53,13 @@ hc_status dw_take_status();
 hc_status tc_take_status();
 hc_status launch_selftest_timeout(int wait_us, cudaStream_t st);
 
+// GELU, exact form: x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2.
+__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+// d/dx GELU = Phi(x) + x * exp(-x^2 / 2) / sqrt(2 pi)
+__device__ __forceinline__ float gelu_d(float v) {
+    return 0.5f * (1.0f + erff(v * 0.70710678118654752f)) + v * 0.39894228040143268f * expf(-0.5f * v * v);
+}
+
 // fp32 -> three bf16 pieces, the operand format of HC_ALGO_TC_BF16X6:
 // p0 = bf16(v), p1 = bf16(v - p0), p2 = bf16(v - p0 - p1); the two differences
 // are exact in fp32, and the pieces carry 24 bits of v's significand.
@@ -117,13 +124,17 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 bool bf16_supported(const hc_conv_desc* d, const Plan& p);
 // pass 2: the backward pass that takes x's pieces from the forward workspace
 size_t bf16_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
+// gelu_in: the conv's input is GELU(x) (1x1 only): both passes split GELU(x), and
+// grad_input is the gradient with respect to GELU(x)
 hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
-                          float* y, void* ws, cudaStream_t st);
+                          float* y, void* ws, cudaStream_t st, bool gelu_in = false);
 // fwd_ws: the workspace of the forward pass on this desc and x, or NULL to split x here
 // gbp (optional): also the bias-gradient partials, with tmp[bias_grad_ws_floats]
+// gelu_y (1x1 only): the conv's output y feeds a GELU and gy is the gradient of
+// GELU(y): the pass runs on gy * GELU'(gelu_y)
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
                           float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, float* gbp,
-                          float* btmp, cudaStream_t st);
+                          float* btmp, cudaStream_t st, bool gelu_in = false, const float* gelu_y = nullptr);
 
 // Per-shard bias-gradient partials gbp[S][Co] in two fixed-order stages,
 // using tmp[bias_grad_ws_floats(Co, S)].
@@ -132,10 +143,11 @@ size_t bias_grad_ws_floats(int Co, int S);
 // gbp [Sh*S][Co]: row shard a owns output rows [a*own_h, (a+1)*own_h) (the last
 // up to Ho), column shard b columns [b*own_w, (b+1)*own_w) (the last up to Wo)
 // pieces (optional): also writes the bf16 pieces of gy there (piece k of element
-// e at pieces[k * ps + e], ps a multiple of 4) while reading it -- the same sums
+// e at pieces[k * ps + e], ps a multiple of 4) while reading it -- the same sums.
+// gelu_y (with pieces): the gradient summed and split is gy * GELU'(gelu_y).
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
                                     int Sh, int own_h, float* tmp, cudaStream_t st, void* pieces = nullptr,
-                                    long long ps = 0);
+                                    long long ps = 0, const float* gelu_y = nullptr);
 
 // out[k] = sum over rows r (ascending, in groups of kColumnGroup) of in[r * stride + k];
 // tmp holds column_sum_tmp_floats(rows, count) floats.

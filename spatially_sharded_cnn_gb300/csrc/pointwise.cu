@@ -143,13 +143,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
     }
 }
 
-// GELU, exact form: x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2.
-__device__ __forceinline__ float gelu_f(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
-// d/dx GELU = Phi(x) + x * exp(-x^2 / 2) / sqrt(2 pi)
-__device__ __forceinline__ float gelu_d(float v) {
-    return 0.5f * (1.0f + erff(v * 0.70710678118654752f)) + v * 0.39894228040143268f * expf(-0.5f * v * v);
-}
-
+// GELU and its derivative: gelu_f / gelu_d (common.cuh).
 __global__ void gelu_fwd_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
     const long long n4 = n / 4;
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < n4; q += (long long)gridDim.x * blockDim.x) {

@@ -31,10 +31,12 @@ __global__ void sum_rows_kernel(const float* __restrict__ in, float* __restrict_
 // part[(slice * Sh * S + a * S + b) * Co + co].  Needs Wo % 4 == 0, S <= 256,
 // 256 threads.  PIECES: every float4 read also goes out as bf16 pieces
 // (store_pieces4 at its own index), so one pass over grad_output serves both.
-template <bool PIECES>
+// GELU_D: the gradient read is gy * GELU'(hy) (hy: the pre-activation, gy's layout).
+template <bool PIECES, bool GELU_D>
 __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict__ gy, float* __restrict__ part, int N,
                                                         int Co, int Ho, int Wo, int S, int own_w, int Sh, int own_h,
-                                                        int slices, uint2* __restrict__ pieces, long long ps4) {
+                                                        int slices, uint2* __restrict__ pieces, long long ps4,
+                                                        const float* __restrict__ hy) {
     __shared__ float cs[256];
     const int a = blockIdx.x / slices, slice = blockIdx.x - a * slices, co = blockIdx.y, tid = threadIdx.x;
     const int i0 = a * own_h, i1 = (a == Sh - 1) ? Ho : i0 + own_h, rows_a = i1 - i0;
@@ -55,6 +57,15 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
                     e[k] = (long long)co * Ho * Wo + col + ((long long)n * Co * Ho + i) * Wo;
                     v[k] = __ldg(reinterpret_cast<const float4*>(gy + e[k]));
                 }
+                if (GELU_D) {
+                    float4 h[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) h[k] = __ldg(reinterpret_cast<const float4*>(hy + e[k]));
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        v[k] = make_float4(v[k].x * gelu_d(h[k].x), v[k].y * gelu_d(h[k].y), v[k].z * gelu_d(h[k].z),
+                                           v[k].w * gelu_d(h[k].w));
+                }
                 if (PIECES) {
 #pragma unroll
                     for (int k = 0; k < 4; k++) store_pieces4(v[k], pieces, e[k] / 4, ps4);
@@ -70,7 +81,11 @@ __global__ void __launch_bounds__(256) bias_rows_kernel(const float* __restrict_
             for (; row < r1; row++) {
                 const int n = row / rows_a, i = i0 + row - n * rows_a;
                 const long long e = (long long)co * Ho * Wo + col + ((long long)n * Co * Ho + i) * Wo;
-                const float4 v = __ldg(reinterpret_cast<const float4*>(gy + e));
+                float4 v = __ldg(reinterpret_cast<const float4*>(gy + e));
+                if (GELU_D) {
+                    const float4 h = __ldg(reinterpret_cast<const float4*>(hy + e));
+                    v = make_float4(v.x * gelu_d(h.x), v.y * gelu_d(h.y), v.z * gelu_d(h.z), v.w * gelu_d(h.w));
+                }
                 if (PIECES) store_pieces4(v, pieces, e / 4, ps4);
                 acc.x += v.x;
                 acc.y += v.y;
@@ -124,24 +139,60 @@ hc_status launch_column_sum(const float* in, float* out, int rows, int count, lo
 
 size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co; }
 
+// Blocks of a bias row kernel variant resident on the whole GPU at once (one
+// wave): 0 sums only, 1 with pieces, 2 with pieces of gy * GELU'(y).
+static long long bias_wave(int variant) {
+    static long long cap[3] = {0, 0, 0};
+    if (!cap[variant]) {
+        int dev = 0, sms = 0, per = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (variant == 2)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<true, true>, 256, 0);
+        else if (variant == 1)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<true, false>, 256, 0);
+        else
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<false, false>, 256, 0);
+        cudaGetLastError();
+        cap[variant] = (long long)(sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+    }
+    return cap[variant];
+}
+
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
-                                    int Sh, int own_h, float* tmp, cudaStream_t st, void* pieces, long long ps) {
-    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || Sh < 1 || (long long)N * Ho > 0x7fffffffLL || ps % 4)
+                                    int Sh, int own_h, float* tmp, cudaStream_t st, void* pieces, long long ps,
+                                    const float* gelu_y) {
+    if (Wo % 4 || own_w % 4 || S > 256 || Co > 65535 || Sh < 1 || (long long)N * Ho > 0x7fffffffLL || ps % 4 ||
+        (gelu_y && !pieces))
         return HC_ERR_UNSUPPORTED;
-    // about eight blocks per SM, at most kBiasSlices slices per row shard
+    // about eight blocks per SM, at most kBiasSlices slices per row shard; then the
+    // first slice count (upwards) whose last wave of resident blocks is >= 90 % full
     const long long rows_min = (long long)N * (Sh > 1 ? own_h : Ho);
+    long long smax = rows_min < kBiasSlices ? rows_min : kBiasSlices;
+    if (smax < 1) smax = 1;
     long long slices = (152LL * 8 + (long long)Co * Sh - 1) / ((long long)Co * Sh);
-    if (slices > kBiasSlices) slices = kBiasSlices;
-    if (slices > rows_min) slices = rows_min;
+    if (slices > smax) slices = smax;
     if (slices < 1) slices = 1;
+    const long long cap = bias_wave(gelu_y ? 2 : pieces ? 1 : 0);
+    for (long long t = slices; t <= smax; t++) {
+        const long long blocks = t * Sh * Co, waves = (blocks + cap - 1) / cap;
+        if (blocks >= 0.9 * (double)(waves * cap)) {
+            slices = t;
+            break;
+        }
+    }
     if ((long long)slices * Sh > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)(slices * Sh), Co);
-    if (pieces)
-        bias_rows_kernel<true><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
-                                                     reinterpret_cast<uint2*>(pieces), ps / 4);
+    uint2* pc = reinterpret_cast<uint2*>(pieces);
+    if (gelu_y)
+        bias_rows_kernel<true, true><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
+                                                           pc, ps / 4, gelu_y);
+    else if (pieces)
+        bias_rows_kernel<true, false><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
+                                                            pc, ps / 4, nullptr);
     else
-        bias_rows_kernel<false><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h, (int)slices,
-                                                      nullptr, 0);
+        bias_rows_kernel<false, false><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h,
+                                                             (int)slices, nullptr, 0, nullptr);
     hc_status s = launched();
     if (s) return s;
     return launch_sum_rows(tmp, gbp, (int)slices, (long long)Sh * S * Co, st);  // slices in order

@@ -1018,11 +1018,19 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __res
 
 // fp32 -> three bf16 pieces (split3, common.cuh), piece k of value i at
 // out[k * ps + i].  Elementwise over n4 float4s (the layout is kept); ps4 =
-// piece stride / 4.
-__global__ void __launch_bounds__(256) prep_pieces_kernel(const float4* __restrict__ x, uint2* __restrict__ out,
-                                                          long long n4, long long ps4) {
+// piece stride / 4.  MODE 1: the pieces of GELU(x); MODE 2: of x * GELU'(y)
+// (gelu_f / gelu_d, common.cuh).
+template <int MODE>
+__global__ void __launch_bounds__(256) prep_pieces_kernel(const float4* __restrict__ x, const float4* __restrict__ y,
+                                                          uint2* __restrict__ out, long long n4, long long ps4) {
     for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += (long long)gridDim.x * 256) {
-        store_pieces4(__ldg(x + i), out, i, ps4);
+        float4 v = __ldg(x + i);
+        if (MODE == 1) v = make_float4(gelu_f(v.x), gelu_f(v.y), gelu_f(v.z), gelu_f(v.w));
+        if (MODE == 2) {
+            const float4 h = __ldg(y + i);
+            v = make_float4(v.x * gelu_d(h.x), v.y * gelu_d(h.y), v.z * gelu_d(h.z), v.w * gelu_d(h.w));
+        }
+        store_pieces4(v, out, i, ps4);
     }
 }
 // Transposed pieces of a small R x C matrix: out[k * ps + c * R + r] = piece k of w[r * C + c].
@@ -1272,13 +1280,22 @@ size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 // piece stride: the element count rounded up to 128 (256 bytes)
 long long piece_stride(long long n) { return (n + 127) / 128 * 128; }
 
-hc_status launch_prep_pieces(const float* x, void* out, long long n, long long ps, cudaStream_t st) {
+// gelu: split GELU(x); gelu_y: split x * GELU'(gelu_y) (same layout as x)
+hc_status launch_prep_pieces(const float* x, void* out, long long n, long long ps, cudaStream_t st,
+                             bool gelu = false, const float* gelu_y = nullptr) {
     if (n % 4 || ps % 4) return HC_ERR_UNSUPPORTED;
     long long blocks = (n / 4 + 255) / 256;
     if (blocks > 152LL * 16) blocks = 152LL * 16;
     if (blocks < 1) blocks = 1;
-    prep_pieces_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(x),
-                                                         reinterpret_cast<uint2*>(out), n / 4, ps / 4);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* y4 = reinterpret_cast<const float4*>(gelu_y);
+    uint2* o = reinterpret_cast<uint2*>(out);
+    if (gelu_y)
+        prep_pieces_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(x4, y4, o, n / 4, ps / 4);
+    else if (gelu)
+        prep_pieces_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(x4, nullptr, o, n / 4, ps / 4);
+    else
+        prep_pieces_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(x4, nullptr, o, n / 4, ps / 4);
     return launched();
 }
 
@@ -1782,8 +1799,9 @@ static void bf16_tiles(const Plan& p, const Bf16View& v, TcParams& tp, int* BN) 
 }
 
 hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
-                          float* y, void* ws, cudaStream_t st) {
+                          float* y, void* ws, cudaStream_t st, bool gelu_in) {
     const Bf16View v = bf16_view(d, p);
+    if (gelu_in && v.s2d) return HC_ERR_UNSUPPORTED;
     const int Co = d->C_out;
     const long long wsz = (long long)Co * v.K;
     const long long psx = piece_stride((long long)d->N * v.K * v.P), psw = piece_stride(wsz);
@@ -1792,7 +1810,9 @@ hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, 
     q += al256(6 * psx);
     void* ap = q;
     hc_status e;
-    if ((e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
+    if ((e = gelu_in ? launch_prep_pieces(x, xp, (long long)d->N * d->C_in * v.P, psx, st, true)
+                     : prep_x_pieces(d, p, v, x, xp, psx, st)))
+        return e;
     if (v.s2d) {
         prep_weight_s2d_pieces_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, v.s, 0,
                                                                       psw);
@@ -1826,8 +1846,9 @@ hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, 
 
 hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
                           float* gx, float* gwp, bool want_w, void* ws, const void* fwd_ws, float* gbp,
-                          float* btmp, cudaStream_t st) {
+                          float* btmp, cudaStream_t st, bool gelu_in, const float* gelu_y) {
     const Bf16View v = bf16_view(d, p);
+    if ((gelu_in || gelu_y) && v.s2d) return HC_ERR_UNSUPPORTED;
     const int Co = d->C_out;
     const long long wsz = (long long)Co * v.K;
     const long long psx = piece_stride((long long)d->N * v.K * v.P);
@@ -1844,12 +1865,13 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
     void* xp = fwd_ws ? const_cast<void*>(fwd_ws) : (void*)q;
     hc_status e;
     // grad_output's pieces serve both passes; the bias-gradient partials, when
-    // asked for, are summed in the same read of grad_output
+    // asked for, are summed in the same read of grad_output.  With gelu_y the
+    // output gradient is gy * GELU'(gelu_y), formed as gy is read.
     if (gbp)
         e = launch_bias_grad_partials(gy, gbp, d->N, Co, p.Ho, p.Wo, p.S, p.Wl / v.s, p.Sh, p.Hlo, btmp, st, gp,
-                                      psg);
+                                      psg, gelu_y);
     else
-        e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st);
+        e = launch_prep_pieces(gy, gp, (long long)d->N * Co * v.P, psg, st, false, gelu_y);
     if (e) return e;
     if (gx) {  // D[m][px] = sum_co w^T[m][co] gy[co][px], m = ci (1x1) or (u*C + c)*s + v (depth-to-space)
         if (v.s2d)
@@ -1887,7 +1909,9 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
         }
     }
     if (want_w) {  // G[co][k] = sum over a shard's pixels of gy[co][px] x'[k][px]
-        if (!fwd_ws && (e = prep_x_pieces(d, p, v, x, xp, psx, st))) return e;
+        if (!fwd_ws && (e = gelu_in ? launch_prep_pieces(x, xp, (long long)d->N * d->C_in * v.P, psx, st, true)
+                                    : prep_x_pieces(d, p, v, x, xp, psx, st)))
+            return e;
         TcParams tp{};
         tp.mode = 1;
         tp.fmt = 1;

@@ -23,6 +23,7 @@ _lib = C.CDLL(LIB_PATH)
 
 HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_TIMEOUT = range(6)
 HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32, HC_ALGO_TC_BF16X6 = range(5)
+HC_ACT_NONE, HC_ACT_GELU_INPUT, HC_ACT_GELU_OUTPUT = range(3)
 
 
 class hc_conv_desc(C.Structure):
@@ -75,6 +76,9 @@ _lib.hc_conv2d_fwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_
 _lib.hc_conv2d_bwd.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_conv2d_bwd_reuse.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, C.c_int]
+_lib.hc_conv2d_fwd_act.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int, C.c_int]
+_lib.hc_conv2d_bwd_act.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, C.c_int,
+                                   C.c_int, _P]
 _lib.hc_halo_gather.argtypes = [_D, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.hc_conv2d_bwd_depthwise_noalloc.restype = C.c_int
@@ -123,6 +127,7 @@ EXPORTS = [
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
     "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
+    "hc_conv2d_fwd_act", "hc_conv2d_bwd_act",
 ]
 
 
@@ -189,6 +194,22 @@ def hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=N
     return _lib.hc_conv2d_bwd_reuse(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw), _ptr(gb),
                                     _ptr(gw_partials), _ptr(gb_partials), _ptr(ws), int(ws_bytes), _ptr(fwd_ws),
                                     int(fwd_ws_bytes), _stream(stream), int(algo or HC_ALGO_AUTO))
+
+
+def hc_conv2d_fwd_act(d, x, w, b, y, ws=None, ws_bytes=0, stream=None, algo=None, act=HC_ACT_NONE) -> int:
+    """Forward pass on act(x) (HC_ACT_GELU_INPUT: conv of GELU(x))."""
+    return _lib.hc_conv2d_fwd_act(C.byref(d), _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws), int(ws_bytes),
+                                  _stream(stream), int(algo or HC_ALGO_AUTO), int(act))
+
+
+def hc_conv2d_bwd_act(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None, ws=None, ws_bytes=0,
+                      fwd_ws=None, fwd_ws_bytes=0, stream=None, algo=None, act=HC_ACT_NONE, y_pre=None) -> int:
+    """Backward pass with a GELU on the input (gx w.r.t. GELU(x)) or on the output
+    (gy w.r.t. GELU(y_pre); the pass runs on gy * GELU'(y_pre))."""
+    return _lib.hc_conv2d_bwd_act(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw), _ptr(gb),
+                                  _ptr(gw_partials), _ptr(gb_partials), _ptr(ws), int(ws_bytes), _ptr(fwd_ws),
+                                  int(fwd_ws_bytes), _stream(stream), int(algo or HC_ALGO_AUTO), int(act),
+                                  _ptr(y_pre))
 
 
 def hc_conv2d_bwd_depthwise_noalloc(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=None,

@@ -144,6 +144,27 @@ def test_bwd_reuse_arguments(hc):
                                   algo=bf) == hc.HC_ERR_WORKSPACE
 
 
+def test_gelu_input_support(hc):
+    """A folded GELU is a bf16-piece 1x1 feature: other algorithms, kernels and
+    strides refuse it before launching anything."""
+    act = hc.HC_ACT_GELU_INPUT
+    pw = hc.desc(P.cfg_of(1, 256, 8, 256, 256, 1, 1, 0, 1, 2))
+    _, nb = hc.hc_conv2d_workspace_size(pw, 0, hc.HC_ALGO_TC_3XTF32)
+    assert hc.hc_conv2d_fwd_act(pw, 256, 256, None, 256, 256, nb, algo=hc.HC_ALGO_TC_3XTF32,
+                                act=act) == hc.HC_ERR_UNSUPPORTED
+    for cfg in (P.cfg_of(1, 128, 8, 256, 128, 5, 1, 2, 1, 2), P.cfg_of(1, 128, 8, 256, 128, 2, 2, 0, 1, 2)):
+        d = hc.desc(cfg)
+        _, nb = hc.hc_conv2d_workspace_size(d, 0)
+        assert hc.hc_conv2d_fwd_act(d, 256, 256, None, 256, 256, nb, act=act) == hc.HC_ERR_UNSUPPORTED, cfg
+        _, nb1 = hc.hc_conv2d_workspace_size(d, 1)
+        assert hc.hc_conv2d_bwd_act(d, 256, 256, 256, 256, 256, 256, None, None, 256, nb1,
+                                    act=act) == hc.HC_ERR_UNSUPPORTED, cfg
+    # a GELU on the output needs its pre-activation
+    _, nb1 = hc.hc_conv2d_workspace_size(pw, 1)
+    assert hc.hc_conv2d_bwd_act(pw, 256, 256, 256, 256, 256, 256, None, None, 256, nb1,
+                                act=hc.HC_ACT_GELU_OUTPUT) == hc.HC_ERR_INVALID_ARG
+
+
 def test_pointwise_algorithm_choice(hc):
     """1x1 convs with 128-multiple channels go to the bf16-piece GEMM; its
     operand copies take 6 bytes per element against 8 for tf32 hi / lo."""

@@ -307,6 +307,112 @@ def test_bwd_reuse_bit_identical(hc, name):
         assert np.array_equal(g.numpy(), ref[k]), k
 
 
+def _bwd_act(hc, cfg, xd, wd, gyd, act, y_pre=None, fwd_ws=None, want=("gx", "gw", "gb", "gw_partials",
+                                                                          "gb_partials")):
+    d = hc.desc(cfg)
+    Q = R.num_partials(cfg)
+    wshape = (cfg["C_out"], cfg["C_in"], 1, 1)
+    shapes = dict(gx=tuple(xd.shape), gw=wshape, gb=(cfg["C_out"],), gw_partials=(Q,) + wshape,
+                  gb_partials=(Q, cfg["C_out"]))
+    o = {k: R.Guarded(shapes[k]) for k in want}
+    ws, nb = R.workspace(d, 2 if fwd_ws else 1)
+    fws, fnb = fwd_ws if fwd_ws else (None, 0)
+    v = lambda k: o[k].view if k in o else None
+    hc.check(hc.hc_conv2d_bwd_act(d, xd, wd, gyd, v("gx"), v("gw"), v("gb"), v("gw_partials"), v("gb_partials"), ws,
+                                  nb, fws, fnb, algo=hc.HC_ALGO_TC_BF16X6, act=act, y_pre=y_pre), "bwd act")
+    hc.check(hc.hc_sync_check(), "sync")
+    return {k: g.numpy() for k, g in o.items()}
+
+
+@pytest.mark.parametrize("name", ["pw_128to256_S4_half_pair", "pw_1024to256_S8", "pw_grid_2x4"])
+def test_gelu_input_fusion(hc, orc, name):
+    """HC_ACT_GELU_INPUT: the conv of GELU(x) against the oracle's GELU followed by
+    its convolution; grad_input is the gradient with respect to GELU(x); the
+    backward pass taking GELU(x)'s pieces from the forward workspace equals the
+    one that splits them itself, bit for bit."""
+    cfg, x, w, b, gy = CASES[name]()
+    x = (2.0 * x).astype(np.float32)  # spread the pre-activations over GELU's curved part
+    d = hc.desc(cfg)
+    act = hc.HC_ACT_GELU_INPUT
+    xd, wd, bd, gyd = R.dev(x), R.dev(w), R.dev(b), R.dev(gy)
+    y = R.Guarded(gy.shape)
+    wsf, nbf = R.workspace(d, 0)
+    hc.check(hc.hc_conv2d_fwd_act(d, xd, wd, bd, y.view, wsf, nbf, algo=hc.HC_ALGO_TC_BF16X6, act=act), "fwd act")
+    a = orc.gelu_fwd(x).astype(np.float32)
+    assert R.normwise(y.numpy(), orc.conv2d_fwd(cfg, a, w, b)) <= TOL_FWD
+    out = _bwd_act(hc, cfg, xd, wd, gyd, act, fwd_ws=(wsf, nbf))
+    own = _bwd_act(hc, cfg, xd, wd, gyd, act)
+    for k in out:
+        assert np.array_equal(out[k], own[k]), k
+    assert R.normwise(out["gx"], orc.conv2d_bwd_input(cfg, w, gy)) <= TOL_FWD
+    assert R.normwise(out["gw"], orc.conv2d_bwd_weight(cfg, a, gy)) <= TOL_W
+    assert R.normwise(out["gb"], orc.conv2d_bwd_bias(cfg, gy)) <= TOL_W
+    _, gwp_ref, gbp_ref = orc.sharded_bwd(cfg, a, w, gy)
+    assert R.normwise(out["gw_partials"], gwp_ref) <= TOL_W
+    assert R.normwise(out["gb_partials"], gbp_ref) <= TOL_W
+
+
+@pytest.mark.parametrize("name", ["pw_128to256_S4_half_pair", "pw_256to1024_S8", "pw_grid_2x4"])
+def test_gelu_output_fusion(hc, orc, name):
+    """HC_ACT_GELU_OUTPUT: gy is the gradient of GELU(y_pre); every gradient is the
+    conv's for gy * GELU'(y_pre) (oracle: its GELU backward, then its conv
+    backward), with and without the forward workspace, and with gb alone."""
+    cfg, x, w, b, gy = CASES[name]()
+    y_pre = synth.normal(gy.shape, 2.0, 11, 1)
+    xd, wd, gyd, yd = R.dev(x), R.dev(w), R.dev(gy), R.dev(y_pre)
+    d = hc.desc(cfg)
+    act = hc.HC_ACT_GELU_OUTPUT
+    y = torch.empty(gy.shape, device="cuda")
+    wsf, nbf = R.workspace(d, 0)
+    hc.check(hc.hc_conv2d_fwd_act(d, xd, wd, None, y, wsf, nbf, algo=hc.HC_ALGO_TC_BF16X6, act=act), "fwd")
+    out = _bwd_act(hc, cfg, xd, wd, gyd, act, y_pre=yd, fwd_ws=(wsf, nbf))
+    own = _bwd_act(hc, cfg, xd, wd, gyd, act, y_pre=yd)
+    for k in out:
+        assert np.array_equal(out[k], own[k]), k
+    g = orc.gelu_bwd(y_pre, gy).astype(np.float32)
+    assert R.normwise(out["gx"], orc.conv2d_bwd_input(cfg, w, g)) <= TOL_FWD
+    assert R.normwise(out["gw"], orc.conv2d_bwd_weight(cfg, x, g)) <= TOL_W
+    assert R.normwise(out["gb"], orc.conv2d_bwd_bias(cfg, g)) <= TOL_W
+    _, gwp_ref, gbp_ref = orc.sharded_bwd(cfg, x, w, g)
+    assert R.normwise(out["gw_partials"], gwp_ref) <= TOL_W
+    assert R.normwise(out["gb_partials"], gbp_ref) <= TOL_W
+    only_b = _bwd_act(hc, cfg, xd, wd, gyd, act, y_pre=yd, want=("gb",))
+    assert np.array_equal(only_b["gb"], out["gb"])
+
+
+def test_gelu_mlp_chain(hc, orc):
+    """1x1 -> GELU -> 1x1 with the GELU folded into both convs (h = conv1(x),
+    out = conv2(GELU(h)); backward: conv2 with HC_ACT_GELU_INPUT, conv1 with
+    HC_ACT_GELU_OUTPUT on h) against the oracle's unfused chain."""
+    c1 = P.cfg_of(1, 128, 2, 256, 256, 1, 1, 0, 1, 2)
+    c2 = P.cfg_of(1, 256, 2, 256, 128, 1, 1, 0, 1, 2)
+    x = synth.normal((1, 128, 2, 256), 1.0, 12, 1)
+    w1 = synth.normal((256, 128, 1, 1), 0.15, 12, 2)
+    w2 = synth.normal((128, 256, 1, 1), 0.1, 12, 3)
+    b1, b2 = synth.normal((256,), 0.1, 12, 4), synth.normal((128,), 0.1, 12, 5)
+    gout = synth.normal((1, 128, 2, 256), 1.0, 12, 6)
+    d1, d2 = hc.desc(c1), hc.desc(c2)
+    bf, gi, go = hc.HC_ALGO_TC_BF16X6, hc.HC_ACT_GELU_INPUT, hc.HC_ACT_GELU_OUTPUT
+    xd, w1d, w2d, b1d, b2d, god = (R.dev(a) for a in (x, w1, w2, b1, b2, gout))
+    h = torch.empty((1, 256, 2, 256), device="cuda")
+    out = torch.empty((1, 128, 2, 256), device="cuda")
+    ws1, n1 = R.workspace(d1, 0)
+    ws2, n2 = R.workspace(d2, 0)
+    hc.check(hc.hc_conv2d_fwd_act(d1, xd, w1d, b1d, h, ws1, n1, algo=bf, act=go), "fwd 1")
+    hc.check(hc.hc_conv2d_fwd_act(d2, h, w2d, b2d, out, ws2, n2, algo=bf, act=gi), "fwd 2")
+    g2 = _bwd_act(hc, c2, h, w2d, god, gi, fwd_ws=(ws2, n2))
+    g1 = _bwd_act(hc, c1, xd, w1d, R.dev(g2["gx"]), go, y_pre=h, fwd_ws=(ws1, n1))
+    h_ref = orc.conv2d_fwd(c1, x, w1, b1)
+    a_ref = orc.gelu_fwd(h_ref).astype(np.float32)
+    assert R.normwise(out.cpu().numpy(), orc.conv2d_fwd(c2, a_ref, w2, b2)) <= TOL_FWD
+    ga_ref = orc.conv2d_bwd_input(c2, w2, gout)
+    gh_ref = orc.gelu_bwd(h_ref, ga_ref).astype(np.float32)
+    assert R.normwise(g1["gx"], orc.conv2d_bwd_input(c1, w1, gh_ref)) <= TOL_FWD
+    assert R.normwise(g1["gw"], orc.conv2d_bwd_weight(c1, x, gh_ref)) <= TOL_W
+    assert R.normwise(g1["gb"], orc.conv2d_bwd_bias(c1, gh_ref)) <= TOL_W
+    assert R.normwise(g2["gw"], orc.conv2d_bwd_weight(c2, a_ref, gout)) <= TOL_W
+
+
 @pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "grouped_strided", "tc_5x5_S2",
                                   "pw_128to256_S4_half_pair"])
 def test_deterministic(hc, name):
