@@ -95,6 +95,11 @@ CASES = {
     "pw_256to1024_S8": lambda: tc_case(1, 256, 2, 1024, 1024, 1, 8),
     "pw_1024to256_S8": lambda: tc_case(1, 1024, 2, 1024, 256, 1, 8),
     "tc_5x5_ragged_two_tiles": lambda: tc_case(1, 128, 7, 512, 128, 5, 1),
+    # weight-gradient slot pairs: 7 kernel rows (a single in every column), and
+    # C_in = 256 (channel-block pairs of one tap)
+    "tc_7x7_S2": lambda: tc_case(1, 128, 9, 256, 128, 7, 2),
+    "tc_3x3_Cin256_S2": lambda: tc_case(1, 256, 6, 256, 128, 3, 2),
+    "tc_1x1_Cin384_S2": lambda: tc_case(1, 384, 3, 256, 128, 1, 2),  # 3 channel blocks: a pair and a single
     # strided k = stride convs through space-to-depth (stem- and downsample-like)
     "tc_stem4x4s4": lambda: tc_strided_case(2, 3, 12, 512, 128, 4, 1),
     "tc_down2x2s2_S2": lambda: tc_strided_case(1, 128, 6, 512, 256, 2, 2),
@@ -170,7 +175,8 @@ def test_parity_depthwise_explicit(hc, orc, name):
 
 @pytest.mark.parametrize("name", ["tc_5x5_S2", "tc_3x3_two_mblocks", "tc_1x1", "tc_5x5_ragged_two_tiles",
                                   "tc_stem4x4s4", "tc_down2x2s2_S2", "tc_down3x3s3_C64_S2", "tc_down2x2s2_C96_S4",
-                                  "tc_5x5_S4_tiles_cross_shards", "tc_3x3_wide_S8"])
+                                  "tc_5x5_S4_tiles_cross_shards", "tc_3x3_wide_S8", "tc_7x7_S2", "tc_3x3_Cin256_S2",
+                                  "tc_1x1_Cin384_S2"])
 def test_parity_tensor_cores_explicit(hc, orc, name):
     cfg = CASES[name]()[0]
     auto = hc.HC_ALGO_TC_BF16X6 if name in BF16_CASES else hc.HC_ALGO_TC_3XTF32
@@ -182,7 +188,7 @@ def test_parity_tensor_cores_explicit(hc, orc, name):
 # channels take the bf16-piece GEMM
 BF16_CASES = ["tc_1x1", "pw_128to256_S4_half_pair", "pw_384to128_tiles128", "pw_256to1024_S8", "pw_1024to256_S8",
               "pw_grid_2x4", "tc_stem4x4s4", "tc_down2x2s2_S2", "tc_down3x3s3_C64_S2", "tc_down2x2s2_C96_S4",
-              "tc_down2x2s2_grid_2x2"]
+              "tc_down2x2s2_grid_2x2", "tc_1x1_Cin384_S2"]
 
 
 @pytest.mark.parametrize("name", BF16_CASES)
