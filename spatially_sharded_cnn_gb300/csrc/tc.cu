@@ -235,6 +235,8 @@ struct TcParams {
     int Co, Ci, S, J, own_w, nblocks, taps, row_chunks;  // S: grid shards Sh*Sw; row_chunks = own_w / BK
     int Sw, own_h;  // column shards; owned output rows per row shard (shard q = a*Sw + b)
     int slots;      // taps * nblocks: (tap, 128-channel block) pairs; a unit covers two slots
+    int kvalid;     // bf16 weight gradient: input channels that exist (the slots' columns past them
+                    // are not computed: the reduction never reads them)
     long long shard_chunks;                               // N * own_h * row_chunks
     float* part;    // [S][J][taps][Co][Ci]
 };
@@ -405,12 +407,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = FMT == 1 ? idesc_bf16(BM, BN, 0, p.mode == 0 ? 1 : 0) : idesc_tf32(BM, BN, 0, 0);
         long long it = 0;
         long long g = 0;  // group counter = TMEM buffer position
         bool ok = true;
         for (int t = blockIdx.x; t < p.units && ok && !*abort_flag; t += gridDim.x) {
             const Unit u = decode(p, t, BN);
+            uint32_t idesc = idesc_tf32(BM, BN, 0, 0);
+            if (FMT == 1) {
+                // a bf16 weight-gradient pair without a second slot: N = its real channels
+                // (rounded up to 16), e.g. 48 for a 4x4/s4 conv over 3 channels
+                int ncol = BN;
+                if (p.mode == 1 && 2 * u.tap + 1 >= p.slots) {
+                    const int kv = p.kvalid - 2 * u.tap * WG_SLOT;
+                    ncol = kv >= WG_SLOT ? WG_SLOT : (kv + 15) / 16 * 16;
+                }
+                idesc = idesc_bf16(BM, ncol, 0, p.mode == 0 ? 1 : 0);
+            }
             for (long long c0 = u.c_begin; c0 < u.c_end && ok; c0 += p.group, g++) {
                 const int b = (int)(g & 1);
                 if (g >= 2 && !mbar_wait(&sh.buf_empty[b], (unsigned)(((g >> 1) - 1) & 1), abort_flag)) {
@@ -1931,6 +1943,7 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
         tp.mblocks = Co / BM;
         tp.nblocks = Kp / WG_SLOT;
         tp.slots = tp.nblocks;
+        tp.kvalid = v.K;
         tp.shard_chunks = (long long)d->N * p.Hlo * tp.row_chunks;
         tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.Q;
         tp.part = part;
