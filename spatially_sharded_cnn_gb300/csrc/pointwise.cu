@@ -143,6 +143,71 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
     }
 }
 
+// The same two passes with C = VPT * LN_G known at compile time: every thread
+// holds its VPT channels of one pixel in registers (VPT independent loads in
+// flight, no shared-memory tile); sums run in the same channel order as
+// ln_fwd_kernel's.  (C = 256: 0.44 -> 0.31 ms on a 940 MB tensor.  The same
+// change to the backward pass did not speed it up.)
+template <int VPT>
+__global__ void __launch_bounds__(LN_THREADS) ln_fwd_reg_kernel(const float* __restrict__ x,
+                                                                const float* __restrict__ gamma,
+                                                                const float* __restrict__ beta, float eps,
+                                                                float* __restrict__ y, float* __restrict__ mean,
+                                                                float* __restrict__ rstd, long long HW,
+                                                                long long blocks_per_image) {
+    constexpr int C = VPT * LN_G;
+    __shared__ float red[LN_G][LN_PIX];
+    __shared__ float stat[2][LN_PIX];
+    const long long b = blockIdx.x;
+    const int n = (int)(b / blocks_per_image);
+    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;
+    const long long p = (b % blocks_per_image) * LN_PIX + px;
+    const bool valid = p < HW;
+    const float* xb = x + (long long)n * C * HW + p;
+    float v[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; k++) v[k] = valid ? __ldg(xb + (long long)(g + k * LN_G) * HW) : 0.0f;
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; k++) s += v[k];
+    red[g][px] = s;
+    __syncthreads();
+    if (g == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < LN_G; k++) t += red[k][px];
+        stat[0][px] = t / C;
+    }
+    __syncthreads();
+    const float mu = stat[0][px];
+    float var = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+        const float d = v[k] - mu;
+        var = fmaf(d, d, var);
+    }
+    red[g][px] = var;
+    __syncthreads();
+    if (g == 0) {
+        float t = 0.0f;
+        for (int k = 0; k < LN_G; k++) t += red[k][px];
+        stat[1][px] = rsqrtf(t / C + eps);
+    }
+    __syncthreads();
+    const float rs = stat[1][px];
+    if (valid) {
+        float* yb = y + (long long)n * C * HW + p;
+#pragma unroll
+        for (int k = 0; k < VPT; k++) {
+            const int c = g + k * LN_G;
+            yb[(long long)c * HW] = (v[k] - mu) * rs * __ldg(gamma + c) + __ldg(beta + c);
+        }
+        if (g == 0) {
+            if (mean) mean[(long long)n * HW + p] = mu;
+            if (rstd) rstd[(long long)n * HW + p] = rs;
+        }
+    }
+}
+
 // GELU and its derivative: gelu_f / gelu_d (common.cuh).
 __global__ void gelu_fwd_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
     const long long n4 = n / 4;
@@ -297,8 +362,12 @@ hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const f
         attr = true;
     }
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
-    ln_fwd_kernel<<<(unsigned)(N * bpi), LN_THREADS, smem, (cudaStream_t)stream>>>(x, gamma, beta, eps, y, mean, rstd, C,
-                                                                                 HW, bpi);
+    if (C == 16 * LN_G)
+        ln_fwd_reg_kernel<16><<<(unsigned)(N * bpi), LN_THREADS, 0, (cudaStream_t)stream>>>(x, gamma, beta, eps, y,
+                                                                                          mean, rstd, HW, bpi);
+    else
+        ln_fwd_kernel<<<(unsigned)(N * bpi), LN_THREADS, smem, (cudaStream_t)stream>>>(x, gamma, beta, eps, y, mean,
+                                                                                     rstd, C, HW, bpi);
     return launched();
 }
 
