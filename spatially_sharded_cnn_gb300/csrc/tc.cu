@@ -989,42 +989,33 @@ __global__ void prep_weight_s2d_kernel(const float* __restrict__ w, float* __res
 }
 // Weight-gradient partials in space-to-depth order back to [S][Co][C][s][s]:
 // gwp[r][co][c][u][v] = sum_j part[r][j][co][(u*s + v)*C + c] (j ascending).
-__global__ void wgrad_reduce_s2d_kernel(const float* __restrict__ part, float* __restrict__ gwp, int S, int J, int Co,
+// One block per (r, co) row: threads walk k (coalesced reads), writes scatter.
+__global__ void wgrad_reduce_s2d_kernel(const float* __restrict__ part, float* __restrict__ gwp, int J, int Co,
                                         int C, int s, int Kp) {
-    const long long per = (long long)Co * C * s * s;
-    const long long total = (long long)S * per;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
-         q += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(q / per);
-        long long rem = q % per;
-        const int vv = (int)(rem % s);
-        rem /= s;
-        const int uu = (int)(rem % s);
-        rem /= s;
-        const int c = (int)(rem % C), co = (int)(rem / C);
-        const int k = (uu * s + vv) * C + c;
-        const float* src = part + ((long long)r * J * Co + co) * Kp + k;
+    const int r = blockIdx.x / Co, co = blockIdx.x - r * Co, K = s * s * C;
+    const float* src = part + ((long long)r * J * Co + co) * Kp;
+    float* dst = gwp + (long long)blockIdx.x * K;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
         float t = 0.0f;
-        for (int j = 0; j < J; j++) t += src[(long long)j * Co * Kp];
-        gwp[q] = t;
+        for (int j = 0; j < J; j++) t += src[(long long)j * Co * Kp + k];
+        const int tap = k / C, c = k - tap * C;  // tap = u*s + v
+        dst[c * s * s + tap] = t;
     }
 }
 
-// Weight-gradient partials: gwp[r][co][ci][tap] = sum_j part[r][j][tap][co][ci] (j ascending).
-__global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ gwp, int S, int J, int taps,
+// Weight-gradient partials: gwp[r][co][ci][tap] = sum_j part[r][j][tap][co][ci]
+// (j ascending).  One block per (r, co) row: threads walk ci (coalesced reads).
+__global__ void wgrad_reduce_kernel(const float* __restrict__ part, float* __restrict__ gwp, int J, int taps,
                                     int Co, int Ci) {
+    const int r = blockIdx.x / Co, co = blockIdx.x - r * Co;
     const long long per = (long long)taps * Co * Ci;
-    const long long total = (long long)S * per;
-    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
-         q += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(q / per);
-        const long long rem = q % per;  // ((co * Ci) + ci) * taps + tap
-        const int tap = (int)(rem % taps);
-        const long long coci = rem / taps;
-        const float* src = part + ((long long)r * J * taps + tap) * Co * Ci + coci;
-        float s = 0.0f;
-        for (int j = 0; j < J; j++) s += src[(long long)j * per];
-        gwp[q] = s;
+    float* dst = gwp + (long long)blockIdx.x * Ci * taps;
+    for (int q = threadIdx.x; q < taps * Ci; q += blockDim.x) {
+        const int tap = q / Ci, ci = q - tap * Ci;
+        const float* src = part + (long long)r * J * per + ((long long)tap * Co + co) * Ci + ci;
+        float t = 0.0f;
+        for (int j = 0; j < J; j++) t += src[(long long)j * per];
+        dst[ci * taps + tap] = t;
     }
 }
 
@@ -1568,8 +1559,7 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
             (e = shifted_map(&mb, sh, sl, d->N, Kp, p.Ho, p.Wo, WG_SLOT, 1)))
             return e;
         if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
-        const long long total = (long long)p.Q * Co * Ci * s * s;
-        wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, Co, Ci, s, Kp);
+        wgrad_reduce_s2d_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, Co, Ci, s, Kp);
         if ((e = launched())) return e;
     }
     return HC_OK;
@@ -1707,8 +1697,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
             (s = shifted_map(&mb, sh, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
             return s;
         if ((s = launch_conv_pass(WG_BN, ma, mb, tp, st))) return s;
-        const long long total = (long long)p.Q * wsz;
-        wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, KK, Co, Ci);
+        wgrad_reduce_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, KK, Co, Ci);
         if ((s = launched())) return s;
     }
     return HC_OK;
@@ -1953,11 +1942,10 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
             (e = pieces_rows_map(&mb, xp, d->N, v.K, p.Ho, p.Wo, WG_BN, psx)))
             return e;
         if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
-        const long long total = (long long)p.Q * wsz;
         if (v.s2d)
-            wgrad_reduce_s2d_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, Co, d->C_in, v.s, Kp);
+            wgrad_reduce_s2d_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, Co, d->C_in, v.s, Kp);
         else
-            wgrad_reduce_kernel<<<cdiv(total, 256), 256, 0, st>>>(part, gwp, p.Q, tp.J, 1, Co, d->C_in);
+            wgrad_reduce_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, 1, Co, d->C_in);
         if ((e = launched())) return e;
     }
     return HC_OK;
