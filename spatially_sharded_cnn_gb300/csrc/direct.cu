@@ -91,6 +91,64 @@ __global__ void direct_gx_kernel(const float* __restrict__ w, const float* __res
     }
 }
 
+// Small problems (a few thousand outputs would leave most SMs idle, each thread
+// running a long serial chain): one warp per output element, its lanes taking
+// every 32nd term of the sum; a fixed butterfly adds the lanes' sums.
+__global__ void direct_fwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                       const float* __restrict__ b, float* __restrict__ y, ConvDims D) {
+    const long long total = (long long)D.N * D.Co * D.Ho * D.Wo;
+    const int lane = threadIdx.x & 31, KK = D.kh * D.kw, R = D.Cgi * KK;
+    const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long q = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; q < total; q += warps) {
+        const int j = (int)(q % D.Wo);
+        const int i = (int)((q / D.Wo) % D.Ho);
+        const int co = (int)((q / ((long long)D.Wo * D.Ho)) % D.Co);
+        const int n = (int)(q / ((long long)D.Wo * D.Ho * D.Co));
+        const int ci0 = (co / D.Cgo) * D.Cgi;
+        float acc = 0.0f;
+        for (int r = lane; r < R; r += 32) {  // r = (ci', u, v)
+            const int cl = r / KK, uv = r - cl * KK, u = uv / D.kw, v = uv - u * D.kw;
+            const int h = i * D.s - D.p + u, c = j * D.s - D.p + v;
+            if (h >= 0 && h < D.H && c >= 0 && c < D.W)
+                acc = fmaf(__ldg(w + ((long long)co * D.Cgi + cl) * KK + uv),
+                           __ldg(x + (((long long)n * D.Ci + ci0 + cl) * D.H + h) * D.W + c), acc);
+        }
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) y[q] = acc + (b ? __ldg(b + co) : 0.0f);
+    }
+}
+
+// direct_gx_kernel's sum with a warp per grad_input element (small problems).
+__global__ void direct_gx_warp_kernel(const float* __restrict__ w, const float* __restrict__ gy,
+                                      float* __restrict__ gx, ConvDims D) {
+    const long long total = (long long)D.N * D.Ci * D.H * D.W;
+    const int lane = threadIdx.x & 31, KK = D.kh * D.kw, R = D.Cgo * KK;
+    const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long q = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; q < total; q += warps) {
+        const int c = (int)(q % D.W);
+        const int h = (int)((q / D.W) % D.H);
+        const int ci = (int)((q / ((long long)D.W * D.H)) % D.Ci);
+        const int n = (int)(q / ((long long)D.W * D.H * D.Ci));
+        const int g = ci / D.Cgi, cl = ci % D.Cgi;
+        float acc = 0.0f;
+        for (int r = lane; r < R; r += 32) {  // r = (co in the group, u, v)
+            const int col = r / KK, uv = r - col * KK, u = uv / D.kw, v = uv - u * D.kw;
+            const int co = g * D.Cgo + col;
+            const int ti = h + D.p - u, tj = c + D.p - v;
+            if (ti < 0 || tj < 0 || ti % D.s || tj % D.s) continue;
+            const int i = ti / D.s, j = tj / D.s;
+            if (i >= D.Ho || j >= D.Wo) continue;
+            acc = fmaf(__ldg(w + ((long long)co * D.Cgi + cl) * KK + uv),
+                       __ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j), acc);
+        }
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) gx[q] = acc;
+    }
+}
+
+// Outputs below which a warp per output is used: about four 256-thread blocks per SM.
+constexpr long long kWarpPerOutput = 152LL * 4 * 256;
+
 // Fixed-order block reduction: warp shuffle tree, then warp 0 adds the
 // per-warp sums in warp order.  Result valid in thread 0.
 __device__ float block_sum(float v, float* red) {
@@ -176,14 +234,22 @@ __global__ void direct_gb_partial_kernel(const float* __restrict__ gy, float* __
 hc_status launch_direct_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                             float* y, cudaStream_t st) {
     const ConvDims D = dims_of(d, p);
-    direct_fwd_kernel<<<grid_for((long long)D.N * D.Co * D.Ho * D.Wo, 256), 256, 0, st>>>(x, w, b, y, D);
+    const long long total = (long long)D.N * D.Co * D.Ho * D.Wo;
+    if (total < kWarpPerOutput)
+        direct_fwd_warp_kernel<<<grid_for(total * 32, 256), 256, 0, st>>>(x, w, b, y, D);
+    else
+        direct_fwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(x, w, b, y, D);
     return launched();
 }
 
 hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w, const float* gy, float* gx,
                            cudaStream_t st) {
     const ConvDims D = dims_of(d, p);
-    direct_gx_kernel<<<grid_for((long long)D.N * D.Ci * D.H * D.W, 256), 256, 0, st>>>(w, gy, gx, D);
+    const long long total = (long long)D.N * D.Ci * D.H * D.W;
+    if (total < kWarpPerOutput)
+        direct_gx_warp_kernel<<<grid_for(total * 32, 256), 256, 0, st>>>(w, gy, gx, D);
+    else
+        direct_gx_kernel<<<grid_for(total, 256), 256, 0, st>>>(w, gy, gx, D);
     return launched();
 }
 
