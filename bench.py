@@ -77,6 +77,24 @@ def bf16x6_peak(peaks):
     return peaks["bf16"] / 6
 
 
+def op_rooflines(ops_ms, work, peaks, sms):
+    """Per-op rates against each op's own bound.  work: op -> (bound, amount)
+    with bound "tensor" (fp32 FLOPs on the bf16-piece GEMM), "alu" (FP32 FLOPs)
+    or "hbm" (algorithmic bytes); ops without an entry are left out."""
+    out = {}
+    for op, ms in ops_ms.items():
+        if op not in work or ms <= 0:
+            continue
+        bound, amount = work[op]
+        if bound == "hbm":
+            a, peak, unit = amount / (ms * 1e-3) / 1e9, peaks["hbm"], "GB/s"
+        else:
+            a = amount / (ms * 1e-3) / 1e12
+            peak, unit = (bf16x6_peak(peaks), "TFLOP/s") if bound == "tensor" else (alu_peak(peaks, sms), "TFLOP/s")
+        out[op] = {"bound": bound, "achieved": a, "unit": unit, "peak": peak, "frac": a / peak}
+    return out
+
+
 def alu_peak(peaks, sms):
     return sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
 
@@ -384,6 +402,18 @@ class BlockWorkload:
     def value(self, ms):
         return self.flops / (ms * 1e-3) / 1e12
 
+    def op_work(self):
+        """Each op's bound and algorithmic work: conv FLOPs (tensor: the bf16-piece
+        GEMMs; alu: the depthwise stencil) or HBM bytes of the pointwise ops
+        (E = elements of a 256-channel activation)."""
+        E = self.N * 256 * self.HW
+        st, dw, p1, p2 = (conv_flops(c) for c in (self.stem, self.dw, self.pw1, self.pw2))
+        return {"stem_fwd": ("tensor", st), "dw_fwd": ("alu", dw), "pw1_fwd": ("tensor", p1),
+                "gelu_pw2_fwd": ("tensor", p2), "pw2_bwd": ("tensor", 2 * p2), "gelu_pw1_bwd": ("tensor", 2 * p1),
+                "dw_bwd": ("alu", 2 * dw), "stem_bwd": ("tensor", st),
+                "ln_fwd": ("hbm", 8 * E + 8 * self.N * self.HW), "ln_bwd": ("hbm", 12 * E + 8 * self.N * self.HW),
+                "ls_fwd": ("hbm", 12 * E), "ls_bwd": ("hbm", 12 * E), "residual_add": ("hbm", 12 * E)}
+
     def roofline(self, ops_ms, peaks, sms):
         peak = bf16x6_peak(peaks)
         a = conv_flops(self.pw1) / (ops_ms["pw1_fwd"] * 1e-3) / 1e12
@@ -450,6 +480,13 @@ class DwDownWorkload:
 
     def value(self, ms):
         return self.flops / (ms * 1e-3) / 1e12
+
+    def op_work(self):
+        """Each op's bound and FLOPs: the depthwise stencil on the FP32 ALU, the
+        downsample on the bf16-piece GEMM (backward: grad_input and grad_weight)."""
+        dw, dn = conv_flops(self.dw), conv_flops(self.down)
+        return {"dw_fwd": ("alu", dw), "dw_bwd": ("alu", 2 * dw), "down_fwd": ("tensor", dn),
+                "down_bwd": ("tensor", 2 * dn)}
 
     def roofline(self, ops_ms, peaks, sms):
         alu = alu_peak(peaks, sms)
@@ -745,6 +782,7 @@ def main():
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roof = wl.roofline(ops_ms, peaks, sms)
+    op_roofs = op_rooflines(ops_ms, wl.op_work(), peaks, sms) if hasattr(wl, "op_work") else None
     if world > 1:
         dist.barrier()
     if rank == 0:
@@ -758,6 +796,8 @@ def main():
                         "copies": "every step: inputs in from pinned host memory, all outputs out; the copy-in of "
                                   "step k+1 overlaps the copy-out of step k"},
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
+        if op_roofs:
+            line["ops_roofline"] = op_roofs
         if graph is not None:
             line["config"]["cuda_graph"] = f"each step one graph replay of {graph_kernels} kernels"
         if world == 1 and not args.no_cpu_baseline and args.workload == "dw7" and not args.batch:
