@@ -17,10 +17,12 @@
 // TMA (a 3-D box of rows h0-P .. h0+TH+P-1 and columns c0-4 .. c0+131 of one
 // plane; the box start is 16-byte aligned and out-of-image parts are
 // zero-filled by the copy engine) into a three-stage ring of shared-memory
-// buffers guarded by mbarriers; the next job's weights are fetched one job
-// ahead through shared memory.  Every barrier wait is bounded: a CTA that
-// gives up records HC_ERR_TIMEOUT in a status word (read by hc_sync_check),
-// waits for its own copies still in flight, and returns.
+// buffers guarded by mbarriers.  In the forward pass the warps run through the
+// jobs independently and the last warp done with a stage refills it; the
+// backward pass fetches the next job's weights one job ahead through shared
+// memory and refills after a CTA barrier.  Every barrier wait is bounded: a
+// CTA that gives up records HC_ERR_TIMEOUT in a status word (read by
+// hc_sync_check), waits for its own copies still in flight, and returns.
 //
 // Each thread computes an 8-row x 4-column block: per input row it reads 12
 // floats (three 16-byte shared loads) and issues up to 7 * 4 * K FMAs with the
@@ -207,6 +209,11 @@ struct Sched {
 };
 
 // ---- forward ----------------------------------------------------------------
+// Warps run through the CTA's jobs independently: a warp waits for its job's
+// stage to fill, computes, and counts itself done with the stage; the last
+// warp done refills the stage with the job NSTAGE ahead, so no job ends in a
+// CTA-wide barrier.  A warp that changes channel reads the K*K weights straight
+// from global memory (L1 / L2 hits after the first warp).
 template <int K>
 __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
     dw_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ w,
@@ -214,10 +221,12 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
     using G = Geo<K, FWD_WARPS>;
     constexpr int P = G::P, TH = G::TH, KK = K * K;
     extern __shared__ __align__(1024) float smem[];
-    float* tiles = smem;                              // [NSTAGE][TILE]
-    float* wsm = smem + NSTAGE * G::TILE;             // [2][WSLOT]
-    uint64_t* full = reinterpret_cast<uint64_t*>(wsm + 2 * WSLOT);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* tiles = smem;                                               // [NSTAGE][TILE]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NSTAGE * G::TILE);
+    int* done = reinterpret_cast<int*>(full + NSTAGE);                 // [NSTAGE] warps finished with the stage
+    int* issued = done + NSTAGE;                                       // jobs whose copies have been issued
+    int* failed = issued + 1;                                          // a warp gave up waiting
+    const int tid = threadIdx.x, lane = tid & 31;
     int i0, i1;
     sc.range(i0, i1);
     if (i0 >= i1) return;
@@ -232,59 +241,61 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
         tma_load_3d(tiles + (q % NSTAGE) * G::TILE, &xmap, ct * TW - 4, (q % ntiles) * TH - P, n * sc.C + c, bar);
     };
     if (tid == 0) {
-        for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
+        for (int s = 0; s < NSTAGE; s++) {
+            mbar_init(full + s, 1);
+            done[s] = 0;
+        }
+        *failed = 0;
         fence_barrier_init();
-    }
-    {
-        int n, c, ct;
-        sc.decode(i0, n, c, ct);
-        if (tid < KK) wsm[tid] = __ldg(w + c * KK + tid);
-        if (tid == KK) wsm[KK] = bias ? __ldg(bias + c) : 0.0f;
+        const int first = jobs < NSTAGE ? jobs : NSTAGE;
+        for (int j = 0; j < first; j++) issue(j);
+        *issued = first;
     }
     __syncthreads();
-    if (tid == 0)
-        for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
 
+    const int warp = tid >> 5;
     float wt[K][K];
     float bv = 0.0f;
     int cur_c = -1;
     for (int q = 0; q < jobs; q++) {
-        const int t = q % ntiles;
+        const int t = q % ntiles, s = q % NSTAGE;
         int n, c, ct;
         sc.decode(i0 + q / ntiles, n, c, ct);
-        const bool has_next = q + 1 < jobs;
-        if (has_next && tid <= KK) {  // next job's weights, straight into shared memory
-            int nn, cn, ctn;
-            sc.decode(i0 + (q + 1) / ntiles, nn, cn, ctn);
-            float* dst = wsm + ((q + 1) & 1) * WSLOT + tid;
-            if (tid < KK)
-                cp_async4(dst, w + cn * KK + tid);
-            else if (bias)
-                cp_async4(dst, bias + cn);
-            else
-                *dst = 0.0f;
-        }
         if (c != cur_c) {
-            const float* ws = wsm + (q & 1) * WSLOT;
 #pragma unroll
             for (int u = 0; u < K; u++)
 #pragma unroll
-                for (int v = 0; v < K; v++) wt[u][v] = ws[u * K + v];
-            bv = ws[KK];
+                for (int v = 0; v < K; v++) wt[u][v] = __ldg(w + c * KK + u * K + v);
+            bv = bias ? __ldg(bias + c) : 0.0f;
             cur_c = c;
         }
-        const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
-        if (__syncthreads_or(!ok)) {
-            give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
-            return;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(full + s, (unsigned)((q / NSTAGE) & 1)));
+        if (!ok) {
+            if (lane == 0) {
+                atomicCAS(&g_dw_status, 0, (int)HC_ERR_TIMEOUT);
+                *reinterpret_cast<volatile int*>(failed) = 1;
+            }
+            break;
         }
-        const float* sm = tiles + (q % NSTAGE) * G::TILE;
+        const float* sm = tiles + s * G::TILE;
         float acc[8][4];
 #pragma unroll
         for (int r = 0; r < 8; r++)
 #pragma unroll
             for (int jj = 0; jj < 4; jj++) acc[r][jj] = bv;
         stencil_8x4<K>(sm, warp * 8, lane, wt, acc);
+        __syncwarp();  // the warp's reads of the stage are done
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(done + s, 1) == FWD_WARPS - 1) {  // the last warp out refills the stage
+                done[s] = 0;
+                __threadfence_block();
+                if (q + NSTAGE < jobs) {
+                    issue(q + NSTAGE);
+                    atomicAdd(issued, 1);
+                }
+            }
+        }
         float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
 #pragma unroll
         for (int r = 0; r < 8; r++) {
@@ -293,9 +304,14 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
                 *reinterpret_cast<float4*>(yp + (long long)h * sc.W) =
                     make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
-        cp_async_wait_all();
-        __syncthreads();  // this job's buffer is free again; the next weights are in place
-        if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
+    }
+    // A warp that gave up: wait (bounded) for the copies still in flight, so
+    // none lands after the CTA is gone.  At most NSTAGE jobs are outstanding.
+    __syncthreads();
+    if (tid == 0 && *failed) {
+        const int last = *issued;
+        for (int j = last - NSTAGE > 0 ? last - NSTAGE : 0; j < last; j++)
+            mbar_wait(full + (j % NSTAGE), (unsigned)((j / NSTAGE) & 1));
     }
 }
 
@@ -549,7 +565,7 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
     if (s) return s;
     int grid;
     const Sched sc = sched_of(d, &grid, 1, FWD_CTAS);  // horizontal neighbours back to back: their halos hit L2
-    const size_t smem = sizeof(float) * (NSTAGE * G::TILE + 2 * WSLOT) + NSTAGE * sizeof(uint64_t);
+    const size_t smem = sizeof(float) * NSTAGE * G::TILE + NSTAGE * sizeof(uint64_t) + (NSTAGE + 2) * sizeof(int);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(dw_fwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
