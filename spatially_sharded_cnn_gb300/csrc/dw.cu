@@ -47,7 +47,7 @@ constexpr int TW = 128;        // tile width (columns)
 constexpr int SMW = TW + 8;    // staged row: 4 halo columns on each side
 constexpr int FWD_WARPS = 8;   // forward: 64-row tiles, two CTAs per SM
 constexpr int FWD_CTAS = 2;
-constexpr int BWD_WARPS = 8;   // backward: 64-row tiles, one CTA per SM
+constexpr int BWD_WARPS = 8;   // backward: 64-row tiles, one CTA per SM, 8 grad_input + 8 weight-gradient warps
 constexpr int NSTAGE = 3;      // depth of the shared-memory ring
 constexpr int WSLOT = 64;      // floats per weight slot (K*K weights + bias)
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
@@ -328,15 +328,14 @@ struct BwdArgs {
 // ROWS: row shards present (a.Sh > 1); a separate instantiation so that the
 // one-row-shard kernel carries none of their bookkeeping.
 template <int K, bool ROWS>
-__global__ void __launch_bounds__(BWD_WARPS * 32, 1)
+__global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     dw_bwd_kernel(const __grid_constant__ CUtensorMap gymap, const __grid_constant__ CUtensorMap xmap, BwdArgs a,
                   Sched sc) {
     using G = Geo<K, BWD_WARPS>;
     constexpr int P = G::P, TH = G::TH, KK = K * K;
     extern __shared__ __align__(1024) float smem[];
     float* tiles = smem;                              // [NSTAGE][gy, x][TILE]
-    float* wsm = smem + 2 * NSTAGE * G::TILE;         // [2][WSLOT]
-    float* red = wsm + 2 * WSLOT;                     // [BWD_WARPS][KK + 1]
+    float* red = smem + 2 * NSTAGE * G::TILE;         // [BWD_WARPS][KK + 1]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + BWD_WARPS * WSLOT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int i0, i1;
@@ -385,125 +384,140 @@ __global__ void __launch_bounds__(BWD_WARPS * 32, 1)
         for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
         fence_barrier_init();
     }
-    {
-        int n, c, ct;
-        sc.decode(i0, n, c, ct);
-        if (tid < KK) wsm[tid] = __ldg(a.w + c * KK + tid);
-    }
     __syncthreads();
     if (tid == 0)
         for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
 
-    float wf[K][K];  // flipped kernel
-    float gw[K][K];  // weight-gradient accumulators of the current run
-    float gbs = 0.0f;
-#pragma unroll
-    for (int u = 0; u < K; u++)
-#pragma unroll
-        for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
-    int cur_c = -1;
-    int run_n0 = -1;  // first image of the current (c, column tile) run
-    for (int q = 0; q < jobs; q++) {
-        int n, c, ct, item, t;
-        bool seg_end;
-        job(q, item, t, seg_end);
-        sc.decode(item, n, c, ct);
-        if (run_n0 < 0) run_n0 = n;
-        const bool has_next = q + 1 < jobs;
-        int nn = 0, cn = c, ctn = ct;
-        if (has_next) {
-            int item2, t2;
-            bool se2;
-            job(q + 1, item2, t2, se2);
-            sc.decode(item2, nn, cn, ctn);
-        }
-        if (has_next && tid < KK) cp_async4(wsm + ((q + 1) & 1) * WSLOT + tid, a.w + cn * KK + tid);
-        if (c != cur_c) {
-            const float* ws = wsm + (q & 1) * WSLOT;
-#pragma unroll
-            for (int u = 0; u < K; u++)
-#pragma unroll
-                for (int v = 0; v < K; v++) wf[u][v] = ws[(K - 1 - u) * K + (K - 1 - v)];
-            cur_c = c;
-        }
-        const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
-        if (__syncthreads_or(!ok)) {
-            give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
-            return;
-        }
-        const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
-        const float* xs = gys + G::TILE;
-        if (a.gx) {  // phase A, in two 4-row halves (keeps the unrolled body small)
-            float* gp = a.gx + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                const int row0 = warp * 8 + 4 * half;
-                float acc[4][4];
-#pragma unroll
-                for (int r = 0; r < 4; r++)
-#pragma unroll
-                    for (int jj = 0; jj < 4; jj++) acc[r][jj] = 0.0f;
-                stencil_4x4<K>(gys, row0, lane, wf, acc);
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const int h = t * TH + row0 + r;
-                    if (h < sc.H)
-                        *reinterpret_cast<float4*>(gp + (long long)h * sc.W) =
-                            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-                }
+    // The ring, shared by both roles: every warp waits for job q's stage, does
+    // its role's work on it, and the stage is refilled after a CTA barrier.
+    // work(q, n, c, ct, t, flush): flush = the last job of a weight-gradient run
+    // (segment).  Returns false when a wait timed out.
+    auto ring = [&](auto&& on_channel, auto&& work) {
+        int cur_c = -1;
+        for (int q = 0; q < jobs; q++) {
+            int n, c, ct, item, t;
+            bool seg_end;
+            job(q, item, t, seg_end);
+            sc.decode(item, n, c, ct);
+            int nn = 0, cn = c, ctn = ct;
+            const bool has_next = q + 1 < jobs;
+            if (has_next) {
+                int item2, t2;
+                bool se2;
+                job(q + 1, item2, t2, se2);
+                sc.decode(item2, nn, cn, ctn);
             }
-        }
-        if (want_wb) {  // phase B, in two 4-row halves
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                const int row0 = warp * 8 + 4 * half;
-                float g[4][4];
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const float4 v4 = *reinterpret_cast<const float4*>(gys + (P + row0 + r) * SMW + 4 + 4 * lane);
-                    g[r][0] = v4.x;
-                    g[r][1] = v4.y;
-                    g[r][2] = v4.z;
-                    g[r][3] = v4.w;
-                    gbs += (v4.x + v4.y) + (v4.z + v4.w);
-                }
-                correlate_4x4<K>(xs, row0, lane, g, gw);
+            if (c != cur_c) {
+                on_channel(c);
+                cur_c = c;
             }
-            // flush at the end of a (c, column tile) run; with row shards, at the end of
-            // each row-shard segment of the run (its partial belongs to that grid shard)
+            const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
+            if (__syncthreads_or(!ok)) {
+                give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
+                return;
+            }
             const bool last_tile = t == ntiles - 1;
-            if (ROWS ? seg_end : (last_tile && (!has_next || cn != c || ctn != ct))) {
+            const bool flush = ROWS ? seg_end : (last_tile && (!has_next || cn != c || ctn != ct));
+            work(q, n, c, ct, t, flush);
+            __syncthreads();  // every warp is done with this stage
+            if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
+        }
+    };
+
+    if (warp < BWD_WARPS) {
+        // grad_input warps: the flipped stencil on grad_output, 8 rows each in two 4-row halves
+        float wf[K][K];
+        ring(
+            [&](int c) {
 #pragma unroll
                 for (int u = 0; u < K; u++)
 #pragma unroll
-                    for (int v = 0; v < K; v++) {
-                        float s = gw[u][v];
+                    for (int v = 0; v < K; v++) wf[u][v] = __ldg(a.w + c * KK + (K - 1 - u) * K + (K - 1 - v));
+            },
+            [&](int q, int n, int c, int ct, int t, bool) {
+                if (!a.gx) return;
+                const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
+                float* gp = a.gx + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+#pragma unroll 1
+                for (int half = 0; half < 2; half++) {
+                    const int row0 = warp * 8 + 4 * half;
+                    float acc[4][4];
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                        if (lane == 0) red[warp * WSLOT + u * K + v] = s;
-                        gw[u][v] = 0.0f;
+                    for (int r = 0; r < 4; r++)
+#pragma unroll
+                        for (int jj = 0; jj < 4; jj++) acc[r][jj] = 0.0f;
+                    stencil_4x4<K>(gys, row0, lane, wf, acc);
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int h = t * TH + row0 + r;
+                        if (h < sc.H)
+                            *reinterpret_cast<float4*>(gp + (long long)h * sc.W) =
+                                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
                     }
-                float s = gbs;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) red[warp * WSLOT + KK] = s;
-                gbs = 0.0f;
-                __syncthreads();
-                if (tid <= KK) {
-                    float tot = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + tid];
-                    const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
-                    const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
-                    float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
-                    for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + tid] = m == run_n0 ? tot : 0.0f;
                 }
-                run_n0 = -1;
-            }
-        }
-        cp_async_wait_all();
-        __syncthreads();
-        if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
+            });
+    } else {
+        // weight / bias gradient warps: the correlation of the same rows with x,
+        // accumulated in registers over a run and flushed at its end
+        const int wg = warp - BWD_WARPS, wtid = tid - BWD_WARPS * 32;
+        float gw[K][K];
+        float gbs = 0.0f;
+#pragma unroll
+        for (int u = 0; u < K; u++)
+#pragma unroll
+            for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
+        int run_n0 = -1;  // first image of the current (c, column tile) run
+        ring([](int) {},
+             [&](int q, int n, int c, int ct, int t, bool flush) {
+                 if (!want_wb) return;
+                 if (run_n0 < 0) run_n0 = n;
+                 const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
+                 const float* xs = gys + G::TILE;
+#pragma unroll 1
+                 for (int half = 0; half < 2; half++) {
+                     const int row0 = wg * 8 + 4 * half;
+                     float g[4][4];
+#pragma unroll
+                     for (int r = 0; r < 4; r++) {
+                         const float4 v4 = *reinterpret_cast<const float4*>(gys + (P + row0 + r) * SMW + 4 + 4 * lane);
+                         g[r][0] = v4.x;
+                         g[r][1] = v4.y;
+                         g[r][2] = v4.z;
+                         g[r][3] = v4.w;
+                         gbs += (v4.x + v4.y) + (v4.z + v4.w);
+                     }
+                     correlate_4x4<K>(xs, row0, lane, g, gw);
+                 }
+                 // flush at the end of a (c, column tile) run; with row shards, at the end
+                 // of each row-shard segment of the run (its partial belongs to that grid shard)
+                 if (!flush) return;
+#pragma unroll
+                 for (int u = 0; u < K; u++)
+#pragma unroll
+                     for (int v = 0; v < K; v++) {
+                         float s = gw[u][v];
+#pragma unroll
+                         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                         if (lane == 0) red[wg * WSLOT + u * K + v] = s;
+                         gw[u][v] = 0.0f;
+                     }
+                 float s = gbs;
+#pragma unroll
+                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                 if (lane == 0) red[wg * WSLOT + KK] = s;
+                 gbs = 0.0f;
+                 asm volatile("bar.sync 1, %0;\n" ::"n"(BWD_WARPS * 32) : "memory");  // the weight-gradient warps
+                 if (wtid <= KK) {
+                     float tot = 0.0f;
+#pragma unroll
+                     for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + wtid];
+                     const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
+                     const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
+                     float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
+                     for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + wtid] = m == run_n0 ? tot : 0.0f;
+                 }
+                 run_n0 = -1;
+             });
     }
 }
 
@@ -586,8 +600,7 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     int grid;
     const Sched sc = sched_of(d, &grid, 0, 1);  // runs of one (c, column tile): gw stays in registers
     const int tps = p.Wl / TW;
-    const size_t smem =
-        sizeof(float) * (2 * NSTAGE * G::TILE + 2 * WSLOT + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
+    const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(dw_bwd_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -596,9 +609,9 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     }
     BwdArgs a{w, gx, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
     if (p.Sh > 1)
-        dw_bwd_kernel<K, true><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+        dw_bwd_kernel<K, true><<<grid, 2 * BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
     else
-        dw_bwd_kernel<K, false><<<grid, BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+        dw_bwd_kernel<K, false><<<grid, 2 * BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
     s = launched();
     if (s || !want_wb) return s;
     const long long total = (long long)p.Q * d->C_in * (K * K + 1);
