@@ -146,8 +146,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_bwd_kernel(const float* __restr
 // The same two passes with C = VPT * LN_G known at compile time: every thread
 // holds its VPT channels of one pixel in registers (VPT independent loads in
 // flight, no shared-memory tile); sums run in the same channel order as
-// ln_fwd_kernel's.  (C = 256: 0.44 -> 0.31 ms on a 940 MB tensor.  The same
-// change to the backward pass did not speed it up.)
+// ln_fwd_kernel's.  (C = 256: 0.44 -> 0.31 ms on a 940 MB tensor.)
 template <int VPT>
 __global__ void __launch_bounds__(LN_THREADS) ln_fwd_reg_kernel(const float* __restrict__ x,
                                                                 const float* __restrict__ gamma,
@@ -206,6 +205,97 @@ __global__ void __launch_bounds__(LN_THREADS) ln_fwd_reg_kernel(const float* __r
             if (rstd) rstd[(long long)n * HW + p] = rs;
         }
     }
+}
+
+// The backward with C = VPT * LN_G known at compile time, persistent: block b
+// takes the 32-pixel groups b, b + gridDim.x, ... in that order (two blocks per
+// SM).  Each thread holds its VPT channels of one pixel (x and grad_output: all
+// 2 * VPT loads in flight, no shared-memory tile).  The ggamma / gbeta sums of a
+// group reduce each channel over the warp's 32 pixels with a fixed shuffle tree
+// -- four halving steps (lane bits 4..1) leave lane L one channel,
+// (L >> 1) & 15, summed over 16 lanes, and the last step adds lane L ^ 1 --
+// and accumulate across the block's groups in one register; the block writes
+// one partial row at the end (even lanes the gy * xhat sums, odd lanes the gy
+// sums).
+template <int VPT>
+__global__ void __launch_bounds__(LN_THREADS, 2) ln_bwd_reg_kernel(const float* __restrict__ x,
+                                                                   const float* __restrict__ gamma,
+                                                                   const float* __restrict__ mean,
+                                                                   const float* __restrict__ rstd,
+                                                                   const float* __restrict__ gy, float* __restrict__ gx,
+                                                                   float* __restrict__ part, int HW,
+                                                                   int blocks_per_image, int groups) {
+    static_assert(VPT == 16, "the shuffle tree takes 16 channels per thread");
+    constexpr int C = VPT * LN_G;
+    __shared__ float red[2][LN_G][LN_PIX];
+    __shared__ float stat[2][LN_PIX];
+    const int px = threadIdx.x % LN_PIX, g = threadIdx.x / LN_PIX;
+    const int lane = px;  // a warp is one channel group's 32 pixels
+    float acc = 0.0f;     // this lane's channel sum over the block's groups
+    for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+        const int n = grp / blocks_per_image;
+        const int p = (grp - n * blocks_per_image) * LN_PIX + px;
+        const bool valid = p < HW;
+        const size_t img = (size_t)n * C * HW;  // C * HW < 2^31: offsets inside an image are 32-bit
+        const int off = g * HW + p;
+        float xh[VPT], gv[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; k++) {
+            xh[k] = valid ? __ldg(x + img + off + k * LN_G * HW) : 0.0f;
+            gv[k] = valid ? __ldg(gy + img + off + k * LN_G * HW) : 0.0f;
+        }
+        const float mu = valid ? __ldg(mean + (size_t)n * HW + p) : 0.0f;
+        const float rs = valid ? __ldg(rstd + (size_t)n * HW + p) : 0.0f;
+        float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; k++) {
+            xh[k] = valid ? (xh[k] - mu) * rs : 0.0f;
+            const float gg = gv[k] * __ldg(gamma + g + k * LN_G);
+            s1 += gg;
+            s2 = fmaf(gg, xh[k], s2);
+        }
+        red[0][g][px] = s1;
+        red[1][g][px] = s2;
+        __syncthreads();
+        if (g == 0) {
+            float a = 0.0f, c2 = 0.0f;
+            for (int k = 0; k < LN_G; k++) {
+                a += red[0][k][px];
+                c2 += red[1][k][px];
+            }
+            stat[0][px] = a / C;
+            stat[1][px] = c2 / C;
+        }
+        __syncthreads();  // (the next group writes red only after every thread has read stat)
+        const float mg = stat[0][px], mgx = stat[1][px];
+        if (valid) {
+#pragma unroll
+            for (int k = 0; k < VPT; k++) {
+                const float gg = gv[k] * __ldg(gamma + g + k * LN_G);
+                gx[img + off + k * LN_G * HW] = rs * (gg - mg - xh[k] * mgx);
+            }
+        }
+        if (part) {
+#pragma unroll
+            for (int k = 0; k < VPT; k++) xh[k] *= gv[k];  // gy * xhat (zero for pixels past HW)
+#pragma unroll
+            for (int lvl = 0; lvl < 4; lvl++) {
+                const int sh = 16 >> lvl, half = 8 >> lvl;
+                const bool up = (lane & sh) != 0;
+#pragma unroll
+                for (int j = 0; j < half; j++) {
+                    const float sa = up ? xh[j] : xh[j + half], ka = up ? xh[j + half] : xh[j];
+                    const float sb = up ? gv[j] : gv[j + half], kb = up ? gv[j + half] : gv[j];
+                    xh[j] = ka + __shfl_xor_sync(0xffffffffu, sa, sh);
+                    gv[j] = kb + __shfl_xor_sync(0xffffffffu, sb, sh);
+                }
+            }
+            const float ta = xh[0] + __shfl_xor_sync(0xffffffffu, xh[0], 1);
+            const float tb = gv[0] + __shfl_xor_sync(0xffffffffu, gv[0], 1);
+            acc += (lane & 1) ? tb : ta;
+        }
+    }
+    if (part) part[blockIdx.x * 2 * C + (lane & 1) * C + g + ((lane >> 1) & 15) * LN_G] = acc;
 }
 
 // GELU and its derivative: gelu_f / gelu_d (common.cuh).
@@ -334,6 +424,19 @@ unsigned grid_elems(long long n) {
     return (unsigned)(b < 1 ? 1 : (b > 152LL * 32 ? 152LL * 32 : b));
 }
 
+int sm_count_pw() {
+    static int n[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!n[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev] = v > 0 ? v : 1;
+    }
+    return n[dev];
+}
+
 }  // namespace
 }  // namespace hc
 
@@ -390,13 +493,22 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
     const long long blocks = N * bpi;
     float* part = want_p ? (float*)ws : nullptr;
-    ln_bwd_kernel<<<(unsigned)blocks, LN_THREADS, smem, st>>>(x, gamma, mean, rstd, gy, gx, part, C, HW, bpi);
+    long long rows = blocks;  // partial rows: one per block
+    if (C == 16 * LN_G && (long long)C * HW < (1LL << 31) && blocks < (1LL << 31)) {
+        // persistent, two blocks per SM, one partial row per block
+        const long long g = 2LL * sm_count_pw();
+        rows = blocks < g ? blocks : g;
+        ln_bwd_reg_kernel<16><<<(unsigned)rows, LN_THREADS, 0, st>>>(x, gamma, mean, rstd, gy, gx, part, (int)HW,
+                                                                    (int)bpi, (int)blocks);
+    } else {
+        ln_bwd_kernel<<<(unsigned)blocks, LN_THREADS, smem, st>>>(x, gamma, mean, rstd, gy, gx, part, C, HW, bpi);
+    }
     hc_status s = launched();
     if (s || !want_p) return s;
-    // part is [blocks][2][C]: summed over blocks in block order
+    // part is [rows][2][C]: summed over rows in row order
     float* tmp = part + (size_t)blocks * 2 * C;
-    if (ggamma && (s = launch_column_sum(part, ggamma, (int)blocks, C, 2 * (long long)C, tmp, st))) return s;
-    if (gbeta && (s = launch_column_sum(part + C, gbeta, (int)blocks, C, 2 * (long long)C, tmp, st))) return s;
+    if (ggamma && (s = launch_column_sum(part, ggamma, (int)rows, C, 2 * (long long)C, tmp, st))) return s;
+    if (gbeta && (s = launch_column_sum(part + C, gbeta, (int)rows, C, 2 * (long long)C, tmp, st))) return s;
     return HC_OK;
 }
 
