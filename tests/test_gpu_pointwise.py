@@ -26,7 +26,10 @@ def _ws(hc, N, C, HW):
     return torch.empty(nb // 4 + 64, device="cuda"), nb
 
 
-@pytest.mark.parametrize("shape", [(2, 256, 37, 29), (1, 96, 8, 64), (3, 32, 1, 5)])
+# C = 256 runs the persistent register kernel: (2, 256, 128, 160) gives 1280
+# 32-pixel groups, several per block; (1, 256, 97, 113) a ragged last group
+@pytest.mark.parametrize("shape", [(2, 256, 37, 29), (1, 96, 8, 64), (3, 32, 1, 5), (2, 256, 128, 160),
+                                   (1, 256, 97, 113)])
 def test_layernorm(hc, orc, shape):
     N, C, H, W = shape
     HW = H * W
@@ -51,6 +54,12 @@ def test_layernorm(hc, orc, shape):
     assert R.normwise(gx.numpy(), gxr) <= 1e-5
     assert R.normwise(gg.numpy(), ggr) <= 1e-4
     assert R.normwise(gb.numpy(), gbr) <= 1e-4
+    # a second call gives the same bits (fixed summation order)
+    gx2, gg2, gb2 = R.Guarded(shape), R.Guarded((C,)), R.Guarded((C,))
+    hc.check(hc.hc_layernorm_c_bwd(N, C, HW, xd, gd, mean.view, rstd.view, gyd, gx2.view, gg2.view, gb2.view, ws, nb))
+    hc.check(hc.hc_sync_check())
+    for a, b in ((gx, gx2), (gg, gg2), (gb, gb2)):
+        assert np.array_equal(a.numpy(), b.numpy())
 
 
 @pytest.mark.parametrize("n", [4096 * 3 + 3, 7, 1 << 20])
