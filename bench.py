@@ -142,6 +142,11 @@ class Runner:
         self.hc.check(self.hc.hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, None, None, self.ws, self.ws_bytes, fws,
                                                   fnb, self.stream), "bwd")
 
+    def conv_bwd_residual(self, d, x, w, gy, res, gx, gw, gb):
+        """Backward whose grad_input also receives res, the gradient along a skip connection."""
+        self.hc.check(self.hc.hc_conv2d_bwd_residual(d, x, w, gy, res, gx, gw, gb, ws=self.ws, ws_bytes=self.ws_bytes,
+                                                     stream=self.stream), "bwd residual")
+
     def conv_fwd_gelu(self, d, x, w, b, y):
         """The conv of GELU(x), GELU applied as x's operand pieces are made."""
         fws, fnb = self.fws[id(d)]
@@ -388,8 +393,9 @@ class BlockWorkload:
         R.op("ln_bwd", lambda: hc.check(hc.hc_layernorm_c_bwd(N, 256, HW, self.dwo, self.ln_g, self.mean, self.rstd,
                                                               self.g_l, self.g_d, self.g_lng, self.g_lnb, R.ws,
                                                               R.ws_bytes, R.stream)))
-        R.op("dw_bwd", lambda: R.conv_bwd(self.d["dw"], self.s, self.w_dw, self.g_d, self.g_s, self.gw_dw, self.gb_dw))
-        R.op("residual_add", lambda: hc.check(hc.hc_add_inplace(N * 256 * HW, self.g_s, self.gy, R.stream)))
+        # the depthwise conv's grad_input plus the residual's gradient gy, added in its epilogue
+        R.op("dw_bwd", lambda: R.conv_bwd_residual(self.d["dw"], self.s, self.w_dw, self.g_d, self.gy, self.g_s,
+                                                   self.gw_dw, self.gb_dw))
         R.op("stem_bwd", lambda: R.conv_bwd(self.d["stem"], self.img, self.w_stem, self.g_s, None, self.gw_stem,
                                             self.gb_stem))
 
@@ -412,7 +418,7 @@ class BlockWorkload:
                 "gelu_pw2_fwd": ("tensor", p2), "pw2_bwd": ("tensor", 2 * p2), "gelu_pw1_bwd": ("tensor", 2 * p1),
                 "dw_bwd": ("alu", 2 * dw), "stem_bwd": ("tensor", st),
                 "ln_fwd": ("hbm", 8 * E + 8 * self.N * self.HW), "ln_bwd": ("hbm", 12 * E + 8 * self.N * self.HW),
-                "ls_fwd": ("hbm", 12 * E), "ls_bwd": ("hbm", 12 * E), "residual_add": ("hbm", 12 * E)}
+                "ls_fwd": ("hbm", 12 * E), "ls_bwd": ("hbm", 12 * E)}
 
     def roofline(self, ops_ms, peaks, sms):
         peak = bf16x6_peak(peaks)

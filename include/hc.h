@@ -173,6 +173,22 @@ hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float
                               float* gw, float* gb, float* gw_partials, float* gb_partials, void* ws,
                               size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo);
 
+/* Backward pass of a convolution on the branch of a residual block (the
+ * ConvNeXt-XL blocks the pages train, NVIDIA blog design section: out = x +
+ * branch(x)): grad_input also receives the gradient that reaches x along the
+ * skip connection.
+ *   residual: that gradient, same shape and layout as x (device, 16-byte
+ *     aligned); it must not overlap gx (HC_ERR_INVALID_ARG if NULL,
+ *     misaligned or equal to gx).
+ *   gx: required (not NULL); receives grad_input + residual.
+ * The depthwise family adds the residual in its grad_input epilogue (one more
+ * read, no extra pass over gx); the other families run their backward pass and
+ * then add it (hc_add_inplace).  Every other argument, the workspace and the
+ * errors as for hc_conv2d_bwd_algo; gw, gb and the partials are unchanged. */
+hc_status hc_conv2d_bwd_residual(const hc_conv_desc* d, const float* x, const float* w, const float* gy,
+                                 const float* residual, float* gx, float* gw, float* gb, float* gw_partials,
+                                 float* gb_partials, void* ws, size_t ws_bytes, void* stream, hc_algo algo);
+
 /* A GELU (exact form, hc_gelu_fwd) next to a convolution, folded into the
  * passes that read the tensor it touches -- the MLP pattern 1x1 -> GELU -> 1x1
  * of a ConvNeXt block, with h the first conv's output:

@@ -174,7 +174,7 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
 static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, const float* gy, float* gx, float* gw,
                      float* gb, float* gwp_out, float* gbp_out, void* ws, size_t ws_bytes, void* stream,
                      hc_algo a, bool reuse = false, const void* fwd_ws = nullptr, size_t fwd_ws_bytes_given = 0,
-                     hc_act act = HC_ACT_NONE, const float* y_pre = nullptr) {
+                     hc_act act = HC_ACT_NONE, const float* y_pre = nullptr, const float* residual = nullptr) {
     static thread_local Plan p;
     hc_status st = make_plan(d, &p);
     if (st) return st;
@@ -203,8 +203,9 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     const bool want_w = gw || gwp_out;
     const bool want_b = gb || gbp_out;
     switch (a) {
-        case HC_ALGO_DEPTHWISE:
-            st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s);
+        case HC_ALGO_DEPTHWISE:  // a residual gradient goes into the grad_input epilogue
+            st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s, residual);
+            residual = nullptr;
             break;
         case HC_ALGO_TC_3XTF32:
         case HC_ALGO_TC_BF16X6: {
@@ -236,6 +237,7 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
         default: return HC_ERR_UNSUPPORTED;
     }
     if (st) return st;
+    if (residual && (st = hc_add_inplace((long long)d->N * d->C_in * d->H * d->W, gx, residual, stream))) return st;
     // _Partial -> full: sum the shards' partials in shard order.
     if (gw && (st = launch_sum_rows(gwp, gw, p.Q, (long long)wsize(d), s))) return st;
     if (gb && (st = launch_sum_rows(gbp, gb, p.Q, d->C_out, s))) return st;
@@ -311,6 +313,14 @@ hc_status hc_conv2d_bwd_reuse(const hc_conv_desc* d, const float* x, const float
                               size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes, void* stream, hc_algo algo) {
     return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo, true, fwd_ws,
                fwd_ws_bytes);
+}
+
+hc_status hc_conv2d_bwd_residual(const hc_conv_desc* d, const float* x, const float* w, const float* gy,
+                                 const float* residual, float* gx, float* gw, float* gb, float* gw_partials,
+                                 float* gb_partials, void* ws, size_t ws_bytes, void* stream, hc_algo algo) {
+    if (!residual || !gx || ((uintptr_t)residual & 15u) || residual == gx) return HC_ERR_INVALID_ARG;
+    return bwd(d, x, w, gy, gx, gw, gb, gw_partials, gb_partials, ws, ws_bytes, stream, algo, false, nullptr, 0,
+               HC_ACT_NONE, nullptr, residual);
 }
 
 hc_status hc_conv2d_fwd_act(const hc_conv_desc* d, const float* x, const float* w, const float* bias, float* y,

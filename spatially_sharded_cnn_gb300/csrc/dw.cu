@@ -101,11 +101,6 @@ __device__ __forceinline__ void tma_load_3d(float* dst, const CUtensorMap* map, 
         : "memory");
 }
 
-// 4-byte asynchronous global -> shared copy (weights of the next job).
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // A CTA that timed out: record it, then let thread 0 wait (bounded) for the
 // copies it issued and nobody consumed, so none lands after the CTA is gone.
@@ -319,15 +314,17 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
 struct BwdArgs {
     const float* w;
     float* gx;
+    const float* gres;  // nullable: added to grad_input (a residual branch's gradient), same layout as gx
     float* tile_part;
     int tiles_per_shard;
     int want_wb;
     int S, Sh, hlo;  // column shards, row shards, rows per row shard (a multiple of TH when Sh > 1)
 };
 
-// ROWS: row shards present (a.Sh > 1); a separate instantiation so that the
-// one-row-shard kernel carries none of their bookkeeping.
-template <int K, bool ROWS>
+// ROWS: row shards present (a.Sh > 1); RES: a residual gradient is added to
+// grad_input (a.gres).  Separate instantiations, so that the plain kernel
+// carries none of their bookkeeping.
+template <int K, bool ROWS, bool RES>
 __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     dw_bwd_kernel(const __grid_constant__ CUtensorMap gymap, const __grid_constant__ CUtensorMap xmap, BwdArgs a,
                   Sched sc) {
@@ -437,10 +434,19 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             [&](int q, int n, int c, int ct, int t, bool) {
                 if (!a.gx) return;
                 const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
-                float* gp = a.gx + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+                const long long off = ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+                float* gp = a.gx + off;
 #pragma unroll 1
                 for (int half = 0; half < 2; half++) {
                     const int row0 = warp * 8 + 4 * half;
+                    // the residual rows, loaded before the stencil so their latency is hidden
+                    float4 res[4];
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const int h = t * TH + row0 + r;
+                        res[r] = RES && h < sc.H ? __ldg(reinterpret_cast<const float4*>(a.gres + off + (long long)h * sc.W))
+                                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
                     float acc[4][4];
 #pragma unroll
                     for (int r = 0; r < 4; r++)
@@ -452,7 +458,9 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                         const int h = t * TH + row0 + r;
                         if (h < sc.H)
                             *reinterpret_cast<float4*>(gp + (long long)h * sc.W) =
-                                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+                                RES ? make_float4(acc[r][0] + res[r].x, acc[r][1] + res[r].y, acc[r][2] + res[r].z,
+                                                  acc[r][3] + res[r].w)
+                                    : make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
                     }
                 }
             });
@@ -591,7 +599,7 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
 
 template <int K>
 hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy, float* gx,
-                float* tile_part, float* gwp, float* gbp, bool want_wb, cudaStream_t st) {
+                const float* gres, float* tile_part, float* gwp, float* gbp, bool want_wb, cudaStream_t st) {
     using G = Geo<K, BWD_WARPS>;
     if (!gx && !want_wb) return HC_OK;
     CUtensorMap gm, xm;
@@ -603,15 +611,24 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(dw_bwd_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(dw_bwd_kernel<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(dw_bwd_kernel<K, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    BwdArgs a{w, gx, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
-    if (p.Sh > 1)
-        dw_bwd_kernel<K, true><<<grid, 2 * BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
-    else
-        dw_bwd_kernel<K, false><<<grid, 2 * BWD_WARPS * 32, smem, st>>>(gm, xm, a, sc);
+    BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
+    const dim3 grd(grid), blk(2 * BWD_WARPS * 32);
+    if (a.gres) {
+        if (p.Sh > 1)
+            dw_bwd_kernel<K, true, true><<<grd, blk, smem, st>>>(gm, xm, a, sc);
+        else
+            dw_bwd_kernel<K, false, true><<<grd, blk, smem, st>>>(gm, xm, a, sc);
+    } else if (p.Sh > 1) {
+        dw_bwd_kernel<K, true, false><<<grd, blk, smem, st>>>(gm, xm, a, sc);
+    } else {
+        dw_bwd_kernel<K, false, false><<<grd, blk, smem, st>>>(gm, xm, a, sc);
+    }
     s = launched();
     if (s || !want_wb) return s;
     const long long total = (long long)p.Q * d->C_in * (K * K + 1);
@@ -650,11 +667,11 @@ hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float
 
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
-                               bool want_weight_grads, cudaStream_t st) {
+                               bool want_weight_grads, cudaStream_t st, const float* gres) {
     switch (d->kh) {
-        case 3: return bwd_k<3>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
-        case 5: return bwd_k<5>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
-        case 7: return bwd_k<7>(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_weight_grads, st);
+        case 3: return bwd_k<3>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
+        case 5: return bwd_k<5>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
+        case 7: return bwd_k<7>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
     }
     return HC_ERR_UNSUPPORTED;
 }

@@ -76,6 +76,7 @@ _lib.hc_conv2d_fwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_
 _lib.hc_conv2d_bwd.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
 _lib.hc_conv2d_bwd_algo.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_conv2d_bwd_reuse.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, C.c_int]
+_lib.hc_conv2d_bwd_residual.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int]
 _lib.hc_conv2d_fwd_act.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_int, C.c_int]
 _lib.hc_conv2d_bwd_act.argtypes = [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, C.c_int,
                                    C.c_int, _P]
@@ -127,7 +128,7 @@ EXPORTS = [
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
     "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
-    "hc_conv2d_fwd_act", "hc_conv2d_bwd_act",
+    "hc_conv2d_fwd_act", "hc_conv2d_bwd_act", "hc_conv2d_bwd_residual",
 ]
 
 
@@ -194,6 +195,14 @@ def hc_conv2d_bwd_reuse(d, x, w, gy, gx, gw, gb, gw_partials=None, gb_partials=N
     return _lib.hc_conv2d_bwd_reuse(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(gx), _ptr(gw), _ptr(gb),
                                     _ptr(gw_partials), _ptr(gb_partials), _ptr(ws), int(ws_bytes), _ptr(fwd_ws),
                                     int(fwd_ws_bytes), _stream(stream), int(algo or HC_ALGO_AUTO))
+
+
+def hc_conv2d_bwd_residual(d, x, w, gy, residual, gx, gw, gb, gw_partials=None, gb_partials=None, ws=None,
+                           ws_bytes=0, stream=None, algo=None) -> int:
+    """Backward pass whose grad_input also receives a residual gradient: gx = grad_input + residual."""
+    return _lib.hc_conv2d_bwd_residual(C.byref(d), _ptr(x), _ptr(w), _ptr(gy), _ptr(residual), _ptr(gx), _ptr(gw),
+                                       _ptr(gb), _ptr(gw_partials), _ptr(gb_partials), _ptr(ws), int(ws_bytes),
+                                       _stream(stream), int(algo or HC_ALGO_AUTO))
 
 
 def hc_conv2d_fwd_act(d, x, w, b, y, ws=None, ws_bytes=0, stream=None, algo=None, act=HC_ACT_NONE) -> int:

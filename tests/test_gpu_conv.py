@@ -542,3 +542,33 @@ def test_config3_full_size_sampled(hc, orc):
             ref.append(orc.gw_at(cfg, x, gy, co, ci, u, v, r * 256, (r + 1) * 256))
     assert R.normwise(np.array(got), np.array(ref)) <= TOL_W
     assert np.abs(out["gw_partials"].astype(np.float64).sum(0) - out["gw"]).max() <= 1e-5 * np.abs(out["gw"]).max()
+
+
+@pytest.mark.parametrize("name,family", [("dw7_ragged_S4", "DEPTHWISE"), ("dw5_S2", "DEPTHWISE"),
+                                         ("dw7_grid_2x2", "DEPTHWISE"), ("tc_5x5_S2", "TC_3XTF32"),
+                                         ("tc_down2x2s2_S2", "TC_BF16X6"), ("config1_dense5x5", "DIRECT")])
+def test_bwd_residual(hc, orc, name, family):
+    """hc_conv2d_bwd_residual: grad_input plus the gradient reaching x along a
+    skip connection, against the oracle's grad_input plus that gradient; the
+    parameter gradients equal hc_conv2d_bwd's bit for bit.  Aliasing the
+    residual with gx, or passing no gx, is refused."""
+    cfg, x, w, b, gy = CASES[name]()
+    algo = getattr(hc, "HC_ALGO_" + family)
+    d = hc.desc(cfg)
+    res = synth.normal(x.shape, 1.0, 17, 1)
+    wshape = (cfg["C_out"], cfg["C_in"] // cfg["groups"], cfg["kh"], cfg["kw"])
+    gx, gw, gb = R.Guarded(x.shape), R.Guarded(wshape), R.Guarded((cfg["C_out"],))
+    ws, nb = R.workspace(d, 1, algo)
+    xd, wd, gyd, rd = R.dev(x), R.dev(w), R.dev(gy), R.dev(res)
+    hc.check(hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, rd, gx.view, gw.view, gb.view, ws=ws, ws_bytes=nb, algo=algo),
+             "bwd residual")
+    hc.check(hc.hc_sync_check(), "bwd residual sync")
+    ref = orc.conv2d_bwd_input(cfg, w, gy) + res.astype(np.float64)
+    assert R.normwise(gx.numpy(), ref) <= TOL_FWD
+    plain = R.bwd(cfg, x, w, gy, algo, partials=False)
+    assert np.array_equal(gw.numpy(), plain["gw"]) and np.array_equal(gb.numpy(), plain["gb"])
+    assert np.array_equal(rd.cpu().numpy(), res)  # the residual is only read
+    assert hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, gx.view, gx.view, gw.view, gb.view, ws=ws, ws_bytes=nb,
+                                     algo=algo) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, rd, None, gw.view, gb.view, ws=ws, ws_bytes=nb,
+                                     algo=algo) == hc.HC_ERR_INVALID_ARG
