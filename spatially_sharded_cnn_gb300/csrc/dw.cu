@@ -18,24 +18,27 @@
 // plane; the box start is 16-byte aligned and out-of-image parts are
 // zero-filled by the copy engine) into a three-stage ring of shared-memory
 // buffers guarded by mbarriers.  In the forward pass the warps run through the
-// jobs independently and the last warp done with a stage refills it; the
-// backward pass fetches the next job's weights one job ahead through shared
-// memory and refills after a CTA barrier.  Every barrier wait is bounded: a
-// CTA that gives up records HC_ERR_TIMEOUT in a status word (read by
-// hc_sync_check), waits for its own copies still in flight, and returns.
+// jobs independently and the last warp done with a stage refills it; in the
+// backward pass a CTA barrier ends each job and thread 0 then refills the
+// stage.  A warp that changes channel reads the weights from global memory.
+// Every barrier wait is bounded: a CTA that gives up records HC_ERR_TIMEOUT in
+// a status word (read by hc_sync_check), waits for its own copies still in
+// flight, and returns.
 //
 // Each thread computes an 8-row x 4-column block: per input row it reads 12
 // floats (three 16-byte shared loads) and issues up to 7 * 4 * K FMAs with the
 // plane's K*K weights in registers.
 //
-// Backward (one kernel, every warp runs both phases on its own block):
-//   phase A  grad_input = the same stencil over the grad_output tile with the
-//            kernel flipped (gx[h][c] = sum_{u,v} w[K-1-u][K-1-v] gy[h+u-P][c+v-P]);
-//   phase B  weight / bias gradients of the block's own grad_output elements,
-//            gw[u][v] += gy[h][c] * x[h+u-P][c+v-P], accumulated in registers over
-//            all consecutive items of the same (c, column tile) and then reduced
-//            across the CTA (warp shuffles, then the per-warp sums in warp
-//            order) into one partial per run.
+// Backward (one kernel, 16 warps on one ring; both roles cover the same 8-row
+// blocks of each staged tile):
+//   warps 0-7   grad_input = the same stencil over the grad_output tile with the
+//               kernel flipped (gx[h][c] = sum_{u,v} w[K-1-u][K-1-v] gy[h+u-P][c+v-P]),
+//               plus, in a separate instantiation, a residual gradient;
+//   warps 8-15  weight / bias gradients of the block's own grad_output elements,
+//               gw[u][v] += gy[h][c] * x[h+u-P][c+v-P], accumulated in registers over
+//               all consecutive items of the same (c, column tile) and then reduced
+//               across these warps (warp shuffles, then the per-warp sums in warp
+//               order) into one partial per run.
 // dw_shard_partials_kernel then sums the partials of each (shard, c) in a
 // fixed order: the per-shard _Partial gradients.
 #include "common.cuh"
@@ -49,7 +52,7 @@ constexpr int FWD_WARPS = 8;   // forward: 64-row tiles, two CTAs per SM
 constexpr int FWD_CTAS = 2;
 constexpr int BWD_WARPS = 8;   // backward: 64-row tiles, one CTA per SM, 8 grad_input + 8 weight-gradient warps
 constexpr int NSTAGE = 3;      // depth of the shared-memory ring
-constexpr int WSLOT = 64;      // floats per weight slot (K*K weights + bias)
+constexpr int WSLOT = 64;      // floats per warp in the weight-gradient reduction buffer (K*K + bias)
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 
 __device__ int g_dw_status;
