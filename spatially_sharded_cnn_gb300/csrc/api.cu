@@ -203,9 +203,11 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     const bool want_w = gw || gwp_out;
     const bool want_b = gb || gbp_out;
     switch (a) {
-        case HC_ALGO_DEPTHWISE:  // a residual gradient goes into the grad_input epilogue
-            st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s, residual);
+        case HC_ALGO_DEPTHWISE:  // a residual gradient goes into the grad_input epilogue; the shard
+                                 // partials' kernel also writes the full gradients
+            st = launch_depthwise_bwd(d, p, x, w, gy, gx, (float*)wsp, gwp, gbp, want_w || want_b, s, residual, gw, gb);
             residual = nullptr;
+            gw = gb = nullptr;
             break;
         case HC_ALGO_TC_3XTF32:
         case HC_ALGO_TC_BF16X6: {

@@ -103,10 +103,12 @@ size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p);
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* b, float* y, cudaStream_t st);
 // tile partials go to ws; then reduced to shard partials gwp / gbp ([S][C][K*K], [S][C])
-// gres (nullable, only with gx): added to grad_input in its epilogue (a residual gradient)
+// gres (nullable, only with gx): added to grad_input in its epilogue (a residual gradient);
+// gw / gb (nullable): the full gradients, the shard partials summed in shard order
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
-                               bool want_weight_grads, cudaStream_t st, const float* gres = nullptr);
+                               bool want_weight_grads, cudaStream_t st, const float* gres = nullptr,
+                               float* gw = nullptr, float* gb = nullptr);
 
 // dense conv on tcgen05 (3xTF32 implicit GEMM): groups 1, stride 1, odd k,
 // padding (k-1)/2, C_in and C_out multiples of 128

@@ -533,21 +533,35 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
 }
 
 // Shard partials: gwp[r][c][k] = sum over (tile tt, image n) of the partials,
-// tt then n ascending; gbp[r][c] likewise from the last slot.
+// tt then n ascending; gbp[r][c] likewise from the last slot.  One thread per
+// (c, k) walks the shards in order and also writes the full gradients
+// gw[c][k] / gb[c] (either may be null): the shard partials added from shard 0
+// up, the order hc_conv2d_bwd's shard sum uses.
 __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, float* __restrict__ gwp,
-                                         float* __restrict__ gbp, int S, int C, int rows, int KK) {
-    const long long total = (long long)S * C * (KK + 1);
+                                         float* __restrict__ gbp, float* __restrict__ gw, float* __restrict__ gb,
+                                         int Q, int C, int rows, int KK) {
+    const long long total = (long long)C * (KK + 1);
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
          q += (long long)gridDim.x * blockDim.x) {
         const int k = (int)(q % (KK + 1));
-        const long long rc = q / (KK + 1);  // r * C + c
-        const float* src = tile_part + rc * rows * (KK + 1) + k;
-        float s = 0.0f;
-        for (int m = 0; m < rows; m++) s += src[(long long)m * (KK + 1)];
+        const int c = (int)(q / (KK + 1));
+        float tot = 0.0f;
+        for (int r = 0; r < Q; r++) {
+            const long long rc = (long long)r * C + c;
+            const float* src = tile_part + rc * rows * (KK + 1) + k;
+            float s = 0.0f;
+            for (int m = 0; m < rows; m++) s += src[(long long)m * (KK + 1)];
+            if (k < KK) {
+                if (gwp) gwp[rc * KK + k] = s;
+            } else if (gbp) {
+                gbp[rc] = s;
+            }
+            tot += s;
+        }
         if (k < KK) {
-            if (gwp) gwp[rc * KK + k] = s;
-        } else if (gbp) {
-            gbp[rc] = s;
+            if (gw) gw[(long long)c * KK + k] = tot;
+        } else if (gb) {
+            gb[c] = tot;
         }
     }
 }
@@ -602,7 +616,8 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
 
 template <int K>
 hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy, float* gx,
-                const float* gres, float* tile_part, float* gwp, float* gbp, bool want_wb, cudaStream_t st) {
+                const float* gres, float* tile_part, float* gwp, float* gbp, float* gw, float* gb, bool want_wb,
+                cudaStream_t st) {
     using G = Geo<K, BWD_WARPS>;
     if (!gx && !want_wb) return HC_OK;
     CUtensorMap gm, xm;
@@ -634,9 +649,9 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     }
     s = launched();
     if (s || !want_wb) return s;
-    const long long total = (long long)p.Q * d->C_in * (K * K + 1);
-    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, p.Q, d->C_in,
-                                                                             tps * d->N, K * K);
+    const long long total = (long long)d->C_in * (K * K + 1);
+    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, gw, gb, p.Q,
+                                                                             d->C_in, tps * d->N, K * K);
     return launched();
 }
 
@@ -670,11 +685,11 @@ hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float
 
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
-                               bool want_weight_grads, cudaStream_t st, const float* gres) {
+                               bool want_weight_grads, cudaStream_t st, const float* gres, float* gw, float* gb) {
     switch (d->kh) {
-        case 3: return bwd_k<3>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
-        case 5: return bwd_k<5>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
-        case 7: return bwd_k<7>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, want_weight_grads, st);
+        case 3: return bwd_k<3>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
+        case 5: return bwd_k<5>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
+        case 7: return bwd_k<7>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
     }
     return HC_ERR_UNSUPPORTED;
 }

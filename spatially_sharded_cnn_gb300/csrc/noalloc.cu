@@ -82,8 +82,5 @@ extern "C" hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, cons
 
     cudaStream_t cs = (cudaStream_t)stream;
     const bool want_wb = gw || gb || gw_partials || gb_partials;
-    if ((st = launch_depthwise_bwd(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_wb, cs))) return st;
-    if (gw && (st = launch_sum_rows(gwp, gw, p.Q, (long long)(d->C_out * kk), cs))) return st;
-    if (gb && (st = launch_sum_rows(gbp, gb, p.Q, d->C_out, cs))) return st;
-    return HC_OK;
+    return launch_depthwise_bwd(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_wb, cs, nullptr, gw, gb);
 }
