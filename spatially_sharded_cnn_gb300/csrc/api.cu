@@ -231,10 +231,11 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
                                                btmp, s);
             break;
         }
-        case HC_ALGO_DIRECT:
+        case HC_ALGO_DIRECT:  // the partials' kernel also writes the full gradients
             if (gx && (st = launch_direct_gx(d, p, w, gy, gx, s))) return st;
             if (want_w || want_b)
-                st = launch_direct_partials(d, p, x, gy, want_w ? gwp : nullptr, want_b ? gbp : nullptr, s);
+                st = launch_direct_partials(d, p, x, gy, want_w ? gwp : nullptr, want_b ? gbp : nullptr, s, gw, gb);
+            gw = gb = nullptr;
             break;
         default: return HC_ERR_UNSUPPORTED;
     }

@@ -93,9 +93,11 @@ hc_status launch_direct_fwd(const hc_conv_desc* d, const Plan& p, const float* x
                             float* y, cudaStream_t st);
 hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w, const float* gy, float* gx,
                            cudaStream_t st);
-// per-shard partials gw_part [S][C_out][C_in/g][kh][kw], gb_part [S][C_out] (either may be null)
+// per-shard partials gw_part [S][C_out][C_in/g][kh][kw], gb_part [S][C_out] (either may be null), and
+// with gw / gb (nullable) the full gradients, the partials summed in shard order
 hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
-                                 float* gw_part, float* gb_part, cudaStream_t st);
+                                 float* gw_part, float* gb_part, cudaStream_t st, float* gw = nullptr,
+                                 float* gb = nullptr);
 
 // depthwise K x K, stride 1, padding (K-1)/2, 128-column tiles inside a shard
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p);

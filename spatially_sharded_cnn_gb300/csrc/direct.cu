@@ -180,53 +180,57 @@ struct ShardBox {
     }
 };
 
-// gw_part[q, co, ci', u, v] = sum_{n, i, j owned by q} gy[n,co,i,j] * x[n,ci,i*s-p+u,j*s-p+v]
-__global__ void direct_gw_partial_kernel(const float* __restrict__ x, const float* __restrict__ gy,
-                                         float* __restrict__ gw_part, ConvDims D, long long wsz, ShardBox sb) {
+// One block per weight element (blocks [0, nw)) or output channel (blocks
+// [nw, nw + nb)), walking the grid shards q = 0 .. Q-1 in order:
+//   gw_part[q, co, ci', u, v] = sum_{n, i, j owned by q} gy[n,co,i,j] * x[n,ci,i*s-p+u,j*s-p+v]
+//   gb_part[q, co]            = sum_{n, i, j owned by q} gy[n,co,i,j]
+// and, when gw / gb are given, the full gradient: the shard partials added from
+// q = 0 up (the order of the library's shard sum).
+__global__ void direct_partials_kernel(const float* __restrict__ x, const float* __restrict__ gy,
+                                       float* __restrict__ gw_part, float* __restrict__ gb_part,
+                                       float* __restrict__ gw, float* __restrict__ gb, ConvDims D, long long wsz,
+                                       long long nw, int Q, ShardBox sb) {
     __shared__ float red[32];
-    const long long k = blockIdx.x;
-    const int q = blockIdx.y;
+    const bool weight = blockIdx.x < nw;
+    const long long k = weight ? (long long)blockIdx.x : 0;
     const int v = (int)(k % D.kw);
     const int u = (int)((k / D.kw) % D.kh);
     const int cl = (int)((k / ((long long)D.kw * D.kh)) % D.Cgi);
-    const int co = (int)(k / ((long long)D.kw * D.kh * D.Cgi));
+    const int co = weight ? (int)(k / ((long long)D.kw * D.kh * D.Cgi)) : (int)(blockIdx.x - nw);
     const int ci = (co / D.Cgo) * D.Cgi + cl;
-    int i0, i1, j0, j1;
-    sb.of(q, D, i0, i1, j0, j1);
-    const int nj = j1 - j0, ni = i1 - i0;
-    const long long terms = (long long)D.N * ni * nj;
-    float acc = 0.0f;
-    for (long long t = threadIdx.x; t < terms; t += blockDim.x) {
-        const int j = j0 + (int)(t % nj);
-        const int i = i0 + (int)((t / nj) % ni);
-        const int n = (int)(t / ((long long)nj * ni));
-        const int h = i * D.s - D.p + u, c = j * D.s - D.p + v;
-        if (h < 0 || h >= D.H || c < 0 || c >= D.W) continue;
-        acc = fmaf(__ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j),
-                   __ldg(x + (((long long)n * D.Ci + ci) * D.H + h) * D.W + c), acc);
+    float total = 0.0f;
+    for (int q = 0; q < Q; q++) {
+        int i0, i1, j0, j1;
+        sb.of(q, D, i0, i1, j0, j1);
+        const int nj = j1 - j0, ni = i1 - i0;
+        const long long terms = (long long)D.N * ni * nj;
+        float acc = 0.0f;
+        for (long long t = threadIdx.x; t < terms; t += blockDim.x) {
+            const int j = j0 + (int)(t % nj);
+            const int i = i0 + (int)((t / nj) % ni);
+            const int n = (int)(t / ((long long)nj * ni));
+            const float g = __ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j);
+            if (!weight) {
+                acc += g;
+                continue;
+            }
+            const int h = i * D.s - D.p + u, c = j * D.s - D.p + v;
+            if (h < 0 || h >= D.H || c < 0 || c >= D.W) continue;
+            acc = fmaf(g, __ldg(x + (((long long)n * D.Ci + ci) * D.H + h) * D.W + c), acc);
+        }
+        const float t = block_sum(acc, red);
+        if (threadIdx.x == 0) {
+            if (weight)
+                gw_part[(long long)q * wsz + k] = t;
+            else
+                gb_part[(long long)q * D.Co + co] = t;
+            total += t;
+        }
     }
-    const float t = block_sum(acc, red);
-    if (threadIdx.x == 0) gw_part[(long long)q * wsz + k] = t;
-}
-
-// gb_part[q, co] = sum_{n, i, j owned by q} gy[n,co,i,j]
-__global__ void direct_gb_partial_kernel(const float* __restrict__ gy, float* __restrict__ gb_part, ConvDims D,
-                                         ShardBox sb) {
-    __shared__ float red[32];
-    const int co = blockIdx.x, q = blockIdx.y;
-    int i0, i1, j0, j1;
-    sb.of(q, D, i0, i1, j0, j1);
-    const int nj = j1 - j0, ni = i1 - i0;
-    const long long terms = (long long)D.N * ni * nj;
-    float acc = 0.0f;
-    for (long long t = threadIdx.x; t < terms; t += blockDim.x) {
-        const int j = j0 + (int)(t % nj);
-        const int i = i0 + (int)((t / nj) % ni);
-        const int n = (int)(t / ((long long)nj * ni));
-        acc += __ldg(gy + (((long long)n * D.Co + co) * D.Ho + i) * D.Wo + j);
+    if (threadIdx.x == 0) {
+        if (weight && gw) gw[k] = total;
+        if (!weight && gb) gb[co] = total;
     }
-    const float t = block_sum(acc, red);
-    if (threadIdx.x == 0) gb_part[(long long)q * D.Co + co] = t;
 }
 
 }  // namespace
@@ -254,22 +258,16 @@ hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w,
 }
 
 hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
-                                 float* gw_part, float* gb_part, cudaStream_t st) {
+                                 float* gw_part, float* gb_part, cudaStream_t st, float* gw, float* gb) {
     const ConvDims D = dims_of(d, p);
     const long long wsz = (long long)D.Co * D.Cgi * D.kh * D.kw;
     const ShardBox sb{p.S, p.Sh, p.Wl / d->stride, p.Hlo};
-    if (p.Q > 65535) return HC_ERR_UNSUPPORTED;
-    if (gw_part) {
-        if (wsz > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        direct_gw_partial_kernel<<<dim3((unsigned)wsz, p.Q), 256, 0, st>>>(x, gy, gw_part, D, wsz, sb);
-        hc_status s = launched();
-        if (s) return s;
-    }
-    if (gb_part) {
-        direct_gb_partial_kernel<<<dim3(D.Co, p.Q), 256, 0, st>>>(gy, gb_part, D, sb);
-        return launched();
-    }
-    return HC_OK;
+    const long long nw = gw_part ? wsz : 0, nb = gb_part ? D.Co : 0;
+    if (nw + nb == 0) return HC_OK;
+    if (nw + nb > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+    direct_partials_kernel<<<(unsigned)(nw + nb), 256, 0, st>>>(x, gy, gw_part, gb_part, gw_part ? gw : nullptr,
+                                                               gb_part ? gb : nullptr, D, wsz, nw, p.Q, sb);
+    return launched();
 }
 
 }  // namespace hc
