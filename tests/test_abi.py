@@ -108,6 +108,18 @@ def test_argument_errors_before_launch(hc):
     st, nb = hc.hc_conv2d_workspace_size(d, 1)
     assert st == 0 and nb > 0
     assert hc.hc_conv2d_bwd(d, 256, 256, 256, 256, 256, 256, None, None, 256, nb - 1) == hc.HC_ERR_WORKSPACE
+    # maximum sizes: 10^12 elements and more are refused, as are more than 1024 shards
+    huge = hc.desc(P.cfg_of(1000, 1000, 1000, 1024, 4, 3, 1, 1, 1, 4))
+    assert hc.hc_conv2d_fwd(huge, 256, 256, None, 256) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_shard_plan(huge)[0] == hc.HC_ERR_INVALID_ARG
+    many = hc.desc(P.cfg_of(1, 1, 4, 4096, 1, 1, 1, 0, 1, 2048))
+    assert hc.hc_shard_plan(many)[0] == hc.HC_ERR_UNSUPPORTED
+    # the residual backward: a residual is required, 16-byte aligned and not gx itself; gx is required
+    args = (d, 256, 256, 256)
+    assert hc.hc_conv2d_bwd_residual(*args, None, 512, 256, 256, ws=256, ws_bytes=nb) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_conv2d_bwd_residual(*args, 512, 512, 256, 256, ws=256, ws_bytes=nb) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_conv2d_bwd_residual(*args, 520, 512, 256, 256, ws=256, ws_bytes=nb) == hc.HC_ERR_INVALID_ARG
+    assert hc.hc_conv2d_bwd_residual(*args, 512, None, 256, 256, ws=256, ws_bytes=nb) == hc.HC_ERR_INVALID_ARG
 
 
 def test_algorithm_choice(hc):
