@@ -8,6 +8,20 @@ namespace hc {
 
 std::atomic<unsigned long long> g_launches{0};
 
+int device_sm_count() {
+    static std::atomic<int> n[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (!v) {
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (v <= 0) v = 1;
+        n[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
 static int out_size(int in, int k, int s, int p) {
     const int span = in + 2 * p - k;
     return span < 0 ? 0 : span / s + 1;

@@ -41,6 +41,9 @@ inline hc_status launched() {
 
 inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+int device_sm_count();
+
 // TMA descriptor for a tensor of `rank` dims (dims[0] innermost), strides in
 // bytes for dims 1..rank-1, zero fill out of bounds.
 hc_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,

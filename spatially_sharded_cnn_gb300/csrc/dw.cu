@@ -566,18 +566,6 @@ __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, fl
     }
 }
 
-int sm_count() {
-    static int n[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!n[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n[dev] = v > 0 ? v : 1;
-    }
-    return n[dev];
-}
 
 // Tensor map of an NCHW fp32 tensor viewed as [N*C][H][W], box = one staged tile.
 template <int K, int WARPS>
@@ -591,7 +579,7 @@ hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d) {
 Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm) {
     Sched sc{d->N, d->C_in, d->H, d->W, d->W / TW, 0, tile_fastest};
     sc.items = d->N * d->C_in * sc.col_tiles;
-    const int g = sm_count() * ctas_per_sm;
+    const int g = device_sm_count() * ctas_per_sm;
     *grid = g < sc.items ? g : sc.items;
     return sc;
 }

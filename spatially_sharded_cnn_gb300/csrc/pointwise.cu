@@ -424,18 +424,6 @@ unsigned grid_elems(long long n) {
     return (unsigned)(b < 1 ? 1 : (b > 152LL * 32 ? 152LL * 32 : b));
 }
 
-int sm_count_pw() {
-    static int n[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!n[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n[dev] = v > 0 ? v : 1;
-    }
-    return n[dev];
-}
 
 }  // namespace
 }  // namespace hc
@@ -496,7 +484,7 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     long long rows = blocks;  // partial rows: one per block
     if (C == 16 * LN_G && (long long)C * HW < (1LL << 31) && blocks < (1LL << 31)) {
         // persistent, two blocks per SM, one partial row per block
-        const long long g = 2LL * sm_count_pw();
+        const long long g = 2LL * device_sm_count();
         rows = blocks < g ? blocks : g;
         ln_bwd_reg_kernel<16><<<(unsigned)rows, LN_THREADS, 0, st>>>(x, gamma, mean, rstd, gy, gx, part, (int)HW,
                                                                     (int)bpi, (int)blocks);

@@ -1120,16 +1120,6 @@ __global__ void prep_weight_s2d_pieces_kernel(const float* __restrict__ w, __nv_
     out[2 * ps + q] = g;
 }
 
-int sm_count_tc() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n = v > 0 ? v : 1;
-    }
-    return n;
-}
 
 // Accumulator columns of a conv-pass tile: a segment of one output row.  Every
 // output pixel's sum over taps and channel chunks runs in the same order
@@ -1168,7 +1158,7 @@ hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUte
         if (p.stages > 8) p.stages = 8;
         smem = TC_SMEM_MAX;
     }
-    const int grid = p.units < sm_count_tc() ? p.units : sm_count_tc();
+    const int grid = p.units < device_sm_count() ? p.units : device_sm_count();
     tc_conv_kernel<BN, FMT><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
     return launched();
 }
@@ -1341,7 +1331,7 @@ int tc_wgrad_splits(const hc_conv_desc* d, const Plan& p) {
     // Units are equally long, so the persistent grid runs ceil(units / SMs) waves.
     // Take the smallest split that fills every SM and keeps the last wave at least
     // 95 % full (each unit at least 2048 pixels long); else the best-filled split.
-    const long long P = sm_count_tc();
+    const long long P = device_sm_count();
     const long long jmax = chunks * BK / 2048 > 1 ? chunks * BK / 2048 : 1;
     long long best = 1;
     double best_fill = 0.0;
