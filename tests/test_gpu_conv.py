@@ -545,7 +545,8 @@ def test_config3_full_size_sampled(hc, orc):
 
 
 @pytest.mark.parametrize("name,family", [("dw7_ragged_S4", "DEPTHWISE"), ("dw5_S2", "DEPTHWISE"),
-                                         ("dw7_grid_2x2", "DEPTHWISE"), ("tc_5x5_S2", "TC_3XTF32"),
+                                         ("dw3_S4", "DEPTHWISE"), ("dw7_grid_2x2", "DEPTHWISE"),
+                                         ("tc_5x5_S2", "TC_3XTF32"),
                                          ("tc_down2x2s2_S2", "TC_BF16X6"), ("config1_dense5x5", "DIRECT")])
 def test_bwd_residual(hc, orc, name, family):
     """hc_conv2d_bwd_residual: grad_input plus the gradient reaching x along a
@@ -568,6 +569,12 @@ def test_bwd_residual(hc, orc, name, family):
     plain = R.bwd(cfg, x, w, gy, algo, partials=False)
     assert np.array_equal(gw.numpy(), plain["gw"]) and np.array_equal(gb.numpy(), plain["gb"])
     assert np.array_equal(rd.cpu().numpy(), res)  # the residual is only read
+    # grad_input alone (no parameter gradients): the same values
+    gx_only = R.Guarded(x.shape)
+    hc.check(hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, rd, gx_only.view, None, None, ws=ws, ws_bytes=nb, algo=algo),
+             "bwd residual gx only")
+    hc.check(hc.hc_sync_check(), "bwd residual gx only sync")
+    assert np.array_equal(gx_only.numpy(), gx.numpy())
     assert hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, gx.view, gx.view, gw.view, gb.view, ws=ws, ws_bytes=nb,
                                      algo=algo) == hc.HC_ERR_INVALID_ARG
     assert hc.hc_conv2d_bwd_residual(d, xd, wd, gyd, rd, None, gw.view, gb.view, ws=ws, ws_bytes=nb,
