@@ -44,6 +44,20 @@ inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) /
 // Streaming multiprocessors of the current device (looked up once per device).
 int device_sm_count();
 
+// Runs `set` (e.g. cudaFuncSetAttribute calls) once for each device the
+// library launches on: kernel attributes belong to a device, so a process that
+// runs the library on several GPUs needs them set on each.  `done` holds one
+// bit per device, set after `set` has run.
+template <typename F>
+inline void once_per_device(std::atomic<unsigned long long>& done, F&& set) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return;
+    set();
+    done.fetch_or(bit, std::memory_order_release);
+}
+
 // TMA descriptor for a tensor of `rank` dims (dims[0] innermost), strides in
 // bytes for dims 1..rank-1, zero fill out of bounds.
 hc_status make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,

@@ -593,11 +593,10 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
     int grid;
     const Sched sc = sched_of(d, &grid, 1, FWD_CTAS);  // horizontal neighbours back to back: their halos hit L2
     const size_t smem = sizeof(float) * NSTAGE * G::TILE + NSTAGE * sizeof(uint64_t) + (NSTAGE + 2) * sizeof(int);
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    once_per_device(attr, [&] {
         cudaFuncSetAttribute(dw_fwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    });
     dw_fwd_kernel<K><<<grid, FWD_WARPS * 32, smem, st>>>(xm, w, b, y, sc);
     return launched();
 }
@@ -615,14 +614,13 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     const Sched sc = sched_of(d, &grid, 0, 1);  // runs of one (c, column tile): gw stays in registers
     const int tps = p.Wl / TW;
     const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    once_per_device(attr, [&] {
         cudaFuncSetAttribute(dw_bwd_kernel<K, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(dw_bwd_kernel<K, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(dw_bwd_kernel<K, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(dw_bwd_kernel<K, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    });
     BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
     const dim3 grd(grid), blk(2 * BWD_WARPS * 32);
     if (a.gres) {

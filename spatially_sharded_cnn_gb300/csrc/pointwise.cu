@@ -447,11 +447,10 @@ hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const f
     if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !beta || !y || !(eps >= 0.0f)) return HC_ERR_INVALID_ARG;
     const size_t smem = sizeof(float) * (size_t)C * LN_PITCH;
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    once_per_device(attr, [&] {
         cudaFuncSetAttribute(ln_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
+    });
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
     if (C == 16 * LN_G)
         ln_fwd_reg_kernel<16><<<(unsigned)(N * bpi), LN_THREADS, 0, (cudaStream_t)stream>>>(x, gamma, beta, eps, y,
@@ -472,11 +471,10 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     if (want_p && (ws_bytes < need || !ws || !al16(ws))) return HC_ERR_WORKSPACE;
     const size_t smem = sizeof(float) * (size_t)2 * C * LN_PITCH;
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    once_per_device(attr, [&] {
         cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
+    });
     cudaStream_t st = (cudaStream_t)stream;
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
     const long long blocks = N * bpi;

@@ -144,10 +144,12 @@ size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co;
 // Blocks of a bias row kernel variant resident on the whole GPU at once (one
 // wave): 0 sums only, 1 with pieces, 2 with pieces of gy * GELU'(y).
 static long long bias_wave(int variant) {
-    static long long cap[3] = {0, 0, 0};
+    static long long caps[64][3];  // per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    long long* cap = caps[dev & 63];
     if (!cap[variant]) {
-        int dev = 0, sms = 0, per = 0;
-        cudaGetDevice(&dev);
+        int sms = 0, per = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (variant == 2)
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<true, true>, 256, 0);

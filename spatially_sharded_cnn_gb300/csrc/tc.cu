@@ -1135,11 +1135,10 @@ int pick_bn(int out_w) {
 template <int BN, int FMT>
 hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap, TcParams p,
                     cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr{0};
+    once_per_device(attr, [&] {
         cudaFuncSetAttribute(tc_conv_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX);
-        attr = true;
-    }
+    });
     int smem;
     if (p.fmt == 1) {
         // three pieces of A (128 x BKH) and B (BN x BKH) per stage; as many stages as
