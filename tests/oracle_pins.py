@@ -333,6 +333,9 @@ def pin_sharded_equals_unsharded(orc):
                 co, cl, u, v = 0, 0, base["kh"] - 1, 0
                 ref = orc.gw_at(base, x, gy, co, cl, u, v, e[4], e[5], f[4], f[5])
                 assert abs(gwp[q, co, cl, u, v] - ref) <= 1e-12, (base, S, Sh, q)
+                if Sh == 1:  # the bias evaluator restricts columns only: each column shard's own partial
+                    for co in range(base["C_out"]):
+                        assert abs(gbp[q, co] - orc.gb_at(base, gy, co, e[4], e[5])) <= 1e-12, (base, S, q, co)
         assert tried >= 2 and (tried_h >= 1 or (base["H"] % 2 and base["H"] % 3)), base
 
 

@@ -23,6 +23,8 @@ MUTANTS = [
     ("bwd_bias_drops_last_row", "int or_conv2d_bwd_bias(", "for (int i = 0; i < Ho; i++)", "for (int i = 0; i < Ho - 1; i++)"),
     ("gx_at_ignores_stride", "double or_conv2d_gx_at(", "if (ti < 0 || ti % s) continue;", "if (ti < 0) continue;"),
     ("gw_at_extra_column", "double or_conv2d_gw_at(", "j < j_end && j < Wo", "j <= j_end && j < Wo"),
+    ("gb_at_extra_column", "double or_conv2d_gb_at(", "j < j_end && j < Wo", "j <= j_end && j < Wo"),
+    ("gb_at_skips_first_column", "double or_conv2d_gb_at(", "for (int j = j_begin;", "for (int j = j_begin + 1;"),
     ("plan_right_halo_short", "static int plan_1d(", "last - e.in_end + 1", "last - e.in_end"),
     ("plan_owned_cols_shifted", "static int plan_1d(", "e.out_begin = r * L / s;", "e.out_begin = r * L / s + (r > 0);"),
     ("halo_drops_first_column", "int or_halo_extend(", "col >= 0 && col < d->W)", "col > 0 && col < d->W)"),
