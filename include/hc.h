@@ -258,9 +258,11 @@ hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, vo
  *   - Sizes whose scratch would exceed 16 MiB are rejected with
  *     HC_ERR_WORKSPACE before anything is launched; so are descs the depthwise
  *     kernels do not cover (HC_ERR_UNSUPPORTED).
- *   - The first call on a device looks up that device's address of the array
- *     (once per device, with that device current); make that first call
- *     before any stream capture.
+ *   - A call looks up the current device's address of the array (with that
+ *     device current) unless its stream is being captured; a call into a
+ *     capturing stream reuses the address of the device's last lookup, so make
+ *     one call on the device before any stream capture (a capture with no
+ *     earlier call returns HC_ERR_UNSUPPORTED).
  *   - All calls share the one array and it keeps the last call's contents;
  *     every scratch value a call reads is written earlier in the same call, so
  *     nothing needs clearing, but calls that overlap on the GPU (different
@@ -381,6 +383,25 @@ const char* hc_status_string(hc_status s);
 
 /* Number of kernels this library has launched since it was loaded. */
 unsigned long long hc_launch_count(void);
+
+/* Per-kernel device timing (a measurement aid; the pages have no counterpart).
+ * hc_trace_enable(1): from then on every launcher records a CUDA event on its
+ * stream before its first kernel and one after every kernel, so each kernel's
+ * device time is the interval between the event before it and its own on the
+ * same stream.  Launches into a stream that is being captured are not traced.
+ * hc_trace_enable(0) stops recording.  While off, the cost is one atomic load
+ * per launch; while on, one event record per launch.
+ * hc_trace_collect: waits for the recorded events, adds the intervals up per
+ * kernel name into out[0 .. *n_entries) (caller-owned host memory; names that
+ * do not fit in max_entries are dropped) and clears the record.  Returns
+ * HC_ERR_CUDA if an event could not be read (its interval is left out). */
+typedef struct {
+    char name[48];
+    int launches;
+    double total_ms;
+} hc_trace_entry;
+hc_status hc_trace_enable(int on);
+hc_status hc_trace_collect(hc_trace_entry* out, int max_entries, int* n_entries);
 
 #ifdef __cplusplus
 }

@@ -9,15 +9,15 @@ namespace hc {
 std::atomic<unsigned long long> g_launches{0};
 
 int device_sm_count() {
-    static std::atomic<int> n[64];
+    static std::atomic<int> n[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    int v = n[dev].load(std::memory_order_relaxed);
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    int v = cached ? n[dev].load(std::memory_order_relaxed) : 0;
     if (!v) {
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        if (v <= 0) v = 1;
-        n[dev].store(v, std::memory_order_relaxed);
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) cudaGetLastError();
+        if (v <= 0) return 1;
+        if (cached) n[dev].store(v, std::memory_order_relaxed);
     }
     return v;
 }
@@ -174,6 +174,7 @@ static hc_status fwd(const hc_conv_desc* d, const float* x, const float* w, cons
     const size_t need = fwd_ws_bytes(d, p, a);
     if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
+    traced_begin(s);
     switch (a) {
         case HC_ALGO_TC_3XTF32: return launch_tc_fwd(d, p, x, w, b, y, ws, s);
         case HC_ALGO_TC_BF16X6: return launch_bf16_fwd(d, p, x, w, b, y, ws, s, act == HC_ACT_GELU_INPUT);
@@ -207,6 +208,7 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     const size_t need = bwd_ws_bytes(d, p, a, reuse);
     if (ws_bytes < need || (need && !ws) || ((uintptr_t)ws & 255)) return HC_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
+    traced_begin(s);
     char* wsp = (char*)ws;
     float* gwp = (float*)wsp;
     wsp += round256(sizeof(float) * p.Q * wsize(d));
@@ -359,6 +361,7 @@ hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, vo
     if (st) return st;
     if (!x || !x_ext) return HC_ERR_INVALID_ARG;
     if (p.S > kMaxKernelShards || p.Sh > kMaxKernelShards) return HC_ERR_UNSUPPORTED;
+    traced_begin((cudaStream_t)stream);
     return launch_halo_gather(d, p, x, x_ext, (cudaStream_t)stream);
 }
 
@@ -373,6 +376,7 @@ hc_status hc_sync_check(void* stream) {
 }
 
 hc_status hc_selftest_timeout(int wait_us, void* stream) {
+    traced_begin((cudaStream_t)stream);
     return launch_selftest_timeout(wait_us, (cudaStream_t)stream);
 }
 

@@ -34,9 +34,23 @@ hc_status make_plan(const hc_conv_desc* d, Plan* p);
 // Count of kernel launches issued by the library.
 extern std::atomic<unsigned long long> g_launches;
 
-inline hc_status launched() {
+// Per-kernel timing (trace.cu): trace_begin(st) at the start of a launcher,
+// trace_launch(name, st) after each of its launches.  Both return at once
+// while tracing is off.
+extern std::atomic<int> g_trace_on;
+void trace_begin(cudaStream_t st);
+void trace_launch(const char* name, cudaStream_t st);
+inline void traced_begin(cudaStream_t st) {
+    if (g_trace_on.load(std::memory_order_relaxed)) trace_begin(st);
+}
+
+// After a launch: counts it, records its trace event, and returns HC_ERR_CUDA
+// if the launch failed.
+inline hc_status launched(const char* name, cudaStream_t st) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaPeekAtLastError() == cudaSuccess ? HC_OK : (cudaGetLastError(), HC_ERR_CUDA);
+    const hc_status s = cudaPeekAtLastError() == cudaSuccess ? HC_OK : (cudaGetLastError(), HC_ERR_CUDA);
+    if (s == HC_OK && g_trace_on.load(std::memory_order_relaxed)) trace_launch(name, st);
+    return s;
 }
 
 inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
@@ -44,18 +58,31 @@ inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) /
 // Streaming multiprocessors of the current device (looked up once per device).
 int device_sm_count();
 
+// Per-device caches (kernel attributes, SM counts, wave sizes, the no-alloc
+// scratch address) hold kMaxDevices entries; a device ordinal at or beyond it
+// is served without caching (the value is looked up on every call).
+constexpr int kMaxDevices = 64;
+
 // Runs `set` (e.g. cudaFuncSetAttribute calls) once for each device the
 // library launches on: kernel attributes belong to a device, so a process that
-// runs the library on several GPUs needs them set on each.  `done` holds one
-// bit per device, set after `set` has run.
+// runs the library on several GPUs needs them set on each.  `set` returns true
+// when every call it made succeeded; only then is the device's bit in `done`
+// set, so a failed attempt (for example inside a strict stream capture) is
+// retried on the next call, and its error is cleared.
 template <typename F>
 inline void once_per_device(std::atomic<unsigned long long>& done, F&& set) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const unsigned long long bit = 1ull << (dev & 63);
+    if (dev < 0 || dev >= kMaxDevices) {
+        if (!set()) cudaGetLastError();
+        return;
+    }
+    const unsigned long long bit = 1ull << dev;
     if (done.load(std::memory_order_acquire) & bit) return;
-    set();
-    done.fetch_or(bit, std::memory_order_release);
+    if (set())
+        done.fetch_or(bit, std::memory_order_release);
+    else
+        cudaGetLastError();
 }
 
 // TMA descriptor for a tensor of `rank` dims (dims[0] innermost), strides in

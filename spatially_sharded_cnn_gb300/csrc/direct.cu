@@ -243,7 +243,7 @@ hc_status launch_direct_fwd(const hc_conv_desc* d, const Plan& p, const float* x
         direct_fwd_warp_kernel<<<grid_for(total * 32, 256), 256, 0, st>>>(x, w, b, y, D);
     else
         direct_fwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(x, w, b, y, D);
-    return launched();
+    return launched("direct_fwd_kernel", st);
 }
 
 hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w, const float* gy, float* gx,
@@ -254,7 +254,7 @@ hc_status launch_direct_gx(const hc_conv_desc* d, const Plan& p, const float* w,
         direct_gx_warp_kernel<<<grid_for(total * 32, 256), 256, 0, st>>>(w, gy, gx, D);
     else
         direct_gx_kernel<<<grid_for(total, 256), 256, 0, st>>>(w, gy, gx, D);
-    return launched();
+    return launched("direct_gx_kernel", st);
 }
 
 hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
@@ -267,7 +267,7 @@ hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const flo
     if (nw + nb > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
     direct_partials_kernel<<<(unsigned)(nw + nb), 256, 0, st>>>(x, gy, gw_part, gb_part, gw_part ? gw : nullptr,
                                                                gb_part ? gb : nullptr, D, wsz, nw, p.Q, sb);
-    return launched();
+    return launched("direct_partials_kernel", st);
 }
 
 }  // namespace hc

@@ -59,7 +59,7 @@ hc_status launch_halo_gather(const hc_conv_desc* d, const Plan& p, const float* 
     const unsigned grid = (unsigned)(blocks < 152LL * 64 ? blocks : 152LL * 64);
     halo_gather_kernel<<<grid, threads, 0, st>>>(x, x_ext, planes, d->H, d->W, p.Hl, p.Wl, p.He, p.We, p.S, total,
                                                  tab);
-    return launched();
+    return launched("halo_gather_kernel", st);
 }
 
 }  // namespace hc

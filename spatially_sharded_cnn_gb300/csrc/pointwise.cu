@@ -444,12 +444,13 @@ hc_status hc_pointwise_workspace_size(int N, int C, long long HW, size_t* bytes)
 
 hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const float* gamma, const float* beta,
                              float eps, float* y, float* mean, float* rstd, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !beta || !y || !(eps >= 0.0f)) return HC_ERR_INVALID_ARG;
     const size_t smem = sizeof(float) * (size_t)C * LN_PITCH;
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
-        cudaFuncSetAttribute(ln_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        return cudaFuncSetAttribute(ln_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) == cudaSuccess;
     });
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
     if (C == 16 * LN_G)
@@ -458,12 +459,13 @@ hc_status hc_layernorm_c_fwd(int N, int C, long long HW, const float* x, const f
     else
         ln_fwd_kernel<<<(unsigned)(N * bpi), LN_THREADS, smem, (cudaStream_t)stream>>>(x, gamma, beta, eps, y, mean,
                                                                                      rstd, C, HW, bpi);
-    return launched();
+    return launched("ln_fwd_kernel", (cudaStream_t)stream);
 }
 
 hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const float* gamma, const float* mean,
                              const float* rstd, const float* gy, float* gx, float* ggamma, float* gbeta, void* ws,
                              size_t ws_bytes, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (N <= 0 || C <= 0 || HW <= 0 || !x || !gamma || !mean || !rstd || !gy || !gx) return HC_ERR_INVALID_ARG;
     size_t need = 0;
     hc_pointwise_workspace_size(N, C, HW, &need);
@@ -473,7 +475,7 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     if (smem > 200 * 1024) return HC_ERR_UNSUPPORTED;
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
-        cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        return cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) == cudaSuccess;
     });
     cudaStream_t st = (cudaStream_t)stream;
     const long long bpi = (HW + LN_PIX - 1) / LN_PIX;
@@ -489,7 +491,7 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
     } else {
         ln_bwd_kernel<<<(unsigned)blocks, LN_THREADS, smem, st>>>(x, gamma, mean, rstd, gy, gx, part, C, HW, bpi);
     }
-    hc_status s = launched();
+    hc_status s = launched("ln_bwd_kernel", st);
     if (s || !want_p) return s;
     // part is [rows][2][C]: summed over rows in row order
     float* tmp = part + (size_t)blocks * 2 * C;
@@ -499,38 +501,43 @@ hc_status hc_layernorm_c_bwd(int N, int C, long long HW, const float* x, const f
 }
 
 hc_status hc_gelu_fwd(long long n, const float* x, float* y, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (n <= 0 || !x || !y || !al16(x) || !al16(y)) return HC_ERR_INVALID_ARG;
     gelu_fwd_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(x, y, n);
-    return launched();
+    return launched("gelu_fwd_kernel", (cudaStream_t)stream);
 }
 
 hc_status hc_gelu_bwd(long long n, const float* x, const float* gy, float* gx, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (n <= 0 || !x || !gy || !gx || !al16(x) || !al16(gy) || !al16(gx)) return HC_ERR_INVALID_ARG;
     gelu_bwd_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(x, gy, gx, n);
-    return launched();
+    return launched("gelu_bwd_kernel", (cudaStream_t)stream);
 }
 
 hc_status hc_add_inplace(long long n, float* y, const float* x, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (n <= 0 || !x || !y || !al16(x) || !al16(y)) return HC_ERR_INVALID_ARG;
     add_inplace_kernel<<<grid_elems(n), 256, 0, (cudaStream_t)stream>>>(y, x, n);
-    return launched();
+    return launched("add_inplace_kernel", (cudaStream_t)stream);
 }
 
 hc_status hc_drop_path_mask(int N, float drop_prob, unsigned long long seed, unsigned long long offset, float* mask,
                             void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (N <= 0 || !mask || !(drop_prob >= 0.0f) || !(drop_prob < 1.0f)) return HC_ERR_INVALID_ARG;
     const unsigned t = (unsigned)floor((double)drop_prob * 16777216.0);
     const float scale = 1.0f / (1.0f - drop_prob);
     drop_path_mask_kernel<<<(N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024, 256, 0, (cudaStream_t)stream>>>(
         N, t, scale, seed, offset, mask);
-    return launched();
+    return launched("drop_path_mask_kernel", (cudaStream_t)stream);
 }
 hc_status hc_layerscale_droppath_fwd(int N, int C, long long HW, const float* res, const float* branch,
                                      const float* gamma, const float* mask, float* out, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (N <= 0 || C <= 0 || HW <= 0 || !res || !branch || !gamma || !out) return HC_ERR_INVALID_ARG;
     ls_fwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, (cudaStream_t)stream>>>(res, branch, gamma, mask,
                                                                                             out, C, HW, LS_CHUNKS);
-    return launched();
+    return launched("ls_fwd_kernel", (cudaStream_t)stream);
 }
 hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* res, const float* branch,
                                      const float* gamma, float* out, void* stream) {
@@ -539,6 +546,7 @@ hc_status hc_layerscale_residual_fwd(int N, int C, long long HW, const float* re
 hc_status hc_layerscale_droppath_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
                                      const float* mask, const float* gy, float* gbranch, float* ggamma, void* ws,
                                      size_t ws_bytes, void* stream) {
+    traced_begin((cudaStream_t)stream);
     if (N <= 0 || C <= 0 || HW <= 0 || !branch || !gamma || !gy || !ggamma) return HC_ERR_INVALID_ARG;
     size_t need = 0;
     hc_pointwise_workspace_size(N, C, HW, &need);
@@ -547,10 +555,10 @@ hc_status hc_layerscale_droppath_bwd(int N, int C, long long HW, const float* br
     float* part = (float*)ws;
     ls_bwd_kernel<<<(unsigned)((long long)N * C * LS_CHUNKS), 256, 0, st>>>(branch, gamma, mask, gy, gbranch, part, C,
                                                                           HW, LS_CHUNKS);
-    hc_status s = launched();
+    hc_status s = launched("ls_bwd_kernel", st);
     if (s) return s;
     ls_reduce_kernel<<<(C + 127) / 128, 128, 0, st>>>(part, ggamma, N, C, LS_CHUNKS);
-    return launched();
+    return launched("ls_reduce_kernel", st);
 }
 hc_status hc_layerscale_residual_bwd(int N, int C, long long HW, const float* branch, const float* gamma,
                                      const float* gy, float* gbranch, float* ggamma, void* ws, size_t ws_bytes,

@@ -134,7 +134,7 @@ hc_status launch_column_sum(const float* in, float* out, int rows, int count, lo
     long long blocks = (total + 255) / 256;
     if (blocks > 152LL * 16) blocks = 152LL * 16;
     column_group_kernel<<<(unsigned)blocks, 256, 0, st>>>(in, tmp, rows, count, stride, kColumnGroup);
-    hc_status s = launched();
+    hc_status s = launched("column_group_kernel", st);
     if (s) return s;
     return launch_sum_rows(tmp, out, (rows + kColumnGroup - 1) / kColumnGroup, count, st);
 }
@@ -144,11 +144,12 @@ size_t bias_grad_ws_floats(int Co, int S) { return (size_t)kBiasSlices * S * Co;
 // Blocks of a bias row kernel variant resident on the whole GPU at once (one
 // wave): 0 sums only, 1 with pieces, 2 with pieces of gy * GELU'(y).
 static long long bias_wave(int variant) {
-    static long long caps[64][3];  // per device
+    static std::atomic<long long> caps[kMaxDevices][3];  // per device; host threads may call at once
     int dev = 0;
     cudaGetDevice(&dev);
-    long long* cap = caps[dev & 63];
-    if (!cap[variant]) {
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    long long v = cached ? caps[dev][variant].load(std::memory_order_relaxed) : 0;
+    if (!v) {
         int sms = 0, per = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (variant == 2)
@@ -158,9 +159,10 @@ static long long bias_wave(int variant) {
         else
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<false, false>, 256, 0);
         cudaGetLastError();
-        cap[variant] = (long long)(sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+        v = (long long)(sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+        if (cached) caps[dev][variant].store(v, std::memory_order_relaxed);
     }
-    return cap[variant];
+    return v;
 }
 
 hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, int Ho, int Wo, int S, int own_w,
@@ -197,7 +199,7 @@ hc_status launch_bias_grad_partials(const float* gy, float* gbp, int N, int Co, 
     else
         bias_rows_kernel<false, false><<<grid, 256, 0, st>>>(gy, tmp, N, Co, Ho, Wo, S, own_w, Sh, own_h,
                                                              (int)slices, nullptr, 0, nullptr);
-    hc_status s = launched();
+    hc_status s = launched("bias_rows_kernel", st);
     if (s) return s;
     return launch_sum_rows(tmp, gbp, (int)slices, (long long)Sh * S * Co, st);  // slices in order
 }
@@ -208,7 +210,7 @@ hc_status launch_sum_rows(const float* in, float* out, int rows, long long count
     if (blocks > 152LL * 16) blocks = 152LL * 16;
     if (blocks < 1) blocks = 1;
     sum_rows_kernel<<<(unsigned)blocks, threads, 0, st>>>(in, out, rows, count);
-    return launched();
+    return launched("sum_rows_kernel", st);
 }
 
 }  // namespace hc

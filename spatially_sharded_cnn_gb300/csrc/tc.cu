@@ -653,7 +653,7 @@ hc_status launch_prep_nhwc(const float* x, float* hi, float* lo, int N, int C, i
                            cudaStream_t st) {
     if (Cp % 64 || W % 4 || (long long)N * H > 65535) return HC_ERR_UNSUPPORTED;
     prep_nhwc_kernel<<<dim3(cdiv(W, 32), Cp / 64, N * H), 256, 0, st>>>(x, hi, lo, C, H, W, Cp);
-    return launched();
+    return launched("prep_nhwc_kernel", st);
 }
 
 // Weights as the A operand of the conv pass: A[m][(u*kw+v)*Kc + c], hi / lo.
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(256) prep_split_rows_kernel(const float* __res
 hc_status launch_split_rows(const float* x, float* hi, float* lo, int N, int C, int H, int W, cudaStream_t st) {
     if (W % 4 || (long long)N * H > 0x7fffffffLL || (C + 15) / 16 > 65535) return HC_ERR_UNSUPPORTED;
     prep_split_rows_kernel<<<dim3((unsigned)(N * H), (C + 15) / 16), 256, 0, st>>>(x, hi, lo, C, H, W);
-    return launched();
+    return launched("prep_split_rows_kernel", st);
 }
 
 // Column-shifted tf32 hi / lo copies of x for the weight gradient, row-interleaved:
@@ -1132,12 +1132,19 @@ int pick_bn(int out_w) {
     return 0;
 }
 
+// Trace name of a tc_conv_kernel launch: operand format and pass.
+const char* tc_pass_name(const TcParams& p) {
+    if (p.fmt == 1) return p.mode == 1 ? "tc_conv_kernel bf16x6 weight-gradient pass" : "tc_conv_kernel bf16x6 conv pass";
+    return p.mode == 1 ? "tc_conv_kernel 3xTF32 weight-gradient pass" : "tc_conv_kernel 3xTF32 conv pass";
+}
+
 template <int BN, int FMT>
 hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& ymap, TcParams p,
                     cudaStream_t st) {
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
-        cudaFuncSetAttribute(tc_conv_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_MAX);
+        return cudaFuncSetAttribute(tc_conv_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    TC_SMEM_MAX) == cudaSuccess;
     });
     int smem;
     if (p.fmt == 1) {
@@ -1159,7 +1166,7 @@ hc_status launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const CUte
     }
     const int grid = p.units < device_sm_count() ? p.units : device_sm_count();
     tc_conv_kernel<BN, FMT><<<grid, TC_THREADS, smem, st>>>(amap, bmap, ymap, p);
-    return launched();
+    return launched(tc_pass_name(p), st);
 }
 
 // ymap: the conv-mode output as a TMA map (out_map); nullptr stores with plain
@@ -1288,7 +1295,7 @@ hc_status launch_prep_pieces(const float* x, void* out, long long n, long long p
         prep_pieces_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(x4, nullptr, o, n / 4, ps / 4);
     else
         prep_pieces_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(x4, nullptr, o, n / 4, ps / 4);
-    return launched();
+    return launched("prep_pieces_kernel", st);
 }
 
 
@@ -1382,7 +1389,7 @@ static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, cons
             prep_s2d_nhwc_small_kernel<4><<<grid, 256, small_smem, st>>>(x, hi, lo, C, d->H, d->W, Kp);
         else
             return HC_ERR_UNSUPPORTED;
-        return launched();
+        return launched("prep_s2d_nhwc_small_kernel", st);
     }
     if (C % 64 == 0 && d->W % 4 == 0) {
         const dim3 grid(cdiv(p.Wo, 32), C / 64, d->N * p.Ho);
@@ -1399,12 +1406,12 @@ static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, cons
         prep_s2d_nhwc_kernel<<<dim3(cdiv(p.Wo, 32), cdiv(C, 32), d->N * p.Ho), dim3(32, 8), 0, st>>>(x, hi, lo, C, d->H,
                                                                                                   d->W, s, Kp);
     }
-    hc_status e = launched();
+    hc_status e = launched("prep_s2d_nhwc_kernel", st);
     if (e || Kp == s * s * C) return e;
     // the channel tail is a K range of the forward GEMM: it must hold zeros
     const long long pixels = (long long)d->N * p.Ho * p.Wo;
     zero_tail_kernel<<<152 * 16, 256, 0, st>>>(hi, lo, pixels, s * s * C, Kp);
-    return launched();
+    return launched("zero_tail_kernel", st);
 }
 static hc_status launch_prep_s2d_planar(const hc_conv_desc* d, const Plan& p, const float* x, float* hi, float* lo,
                                         int Kp, cudaStream_t st) {
@@ -1422,7 +1429,7 @@ static hc_status launch_prep_s2d_planar(const hc_conv_desc* d, const Plan& p, co
         prep_s2d_planar_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(x, hi, lo, d->C_in, d->H, d->W, Kp, items);
     else
         return HC_ERR_UNSUPPORTED;
-    return launched();
+    return launched("prep_s2d_planar_kernel", st);
 }
 
 static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
@@ -1441,7 +1448,7 @@ static hc_status s2d_fwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     hc_status e = launch_prep_s2d_nhwc(d, p, x, xh, xl, Kp, st);
     if (e) return e;
     prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, d->C_in, s, Kp, 0);
-    if ((e = launched())) return e;
+    if ((e = launched("prep_weight_s2d_kernel", st))) return e;
     const int BN = pick_bn(p.Wo);
     TcParams tp{};
     tp.mode = 0;
@@ -1493,7 +1500,7 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
     if (gx) {  // D[(u,v,c)][px] = sum_co w[co][c][u][v] gy[co][px], stored depth-to-space
         if ((e = launch_prep_nhwc(gy, gh, gl, d->N, Co, p.Ho, p.Wo, Co, st))) return e;
         prep_weight_s2d_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, s, Kp, 1);
-        if ((e = launched())) return e;
+        if ((e = launched("prep_weight_s2d_kernel", st))) return e;
         TcParams tp{};
         tp.mode = 0;
         tp.N = d->N;
@@ -1549,7 +1556,7 @@ static hc_status s2d_bwd(const hc_conv_desc* d, const Plan& p, const float* x, c
             return e;
         if ((e = launch_conv_pass(WG_BN, ma, mb, tp, st))) return e;
         wgrad_reduce_s2d_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, Co, Ci, s, Kp);
-        if ((e = launched())) return e;
+        if ((e = launched("wgrad_reduce_s2d_kernel", st))) return e;
     }
     return HC_OK;
 }
@@ -1570,7 +1577,7 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     hc_status s = launch_prep_nhwc(x, xh, xl, d->N, Ci, d->H, d->W, Ci, st);
     if (s) return s;
     prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Co, Ci, 0);
-    if ((s = launched())) return s;
+    if ((s = launched("prep_weight_kernel", st))) return s;
     const int BN = pick_bn(p.Wo);
     TcParams tp{};
     tp.mode = 0;
@@ -1624,7 +1631,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     if (gx) {  // grad_input = conv of grad_output with the flipped, transposed kernel
         if ((s = launch_prep_nhwc(gy, gh, gl, d->N, Co, p.Ho, p.Wo, Co, st))) return s;
         prep_weight_kernel<<<cdiv((long long)wsz, 256), 256, 0, st>>>(w, ah, al, Co, Ci, K, K, Ci, Co, 1);
-        if ((s = launched())) return s;
+        if ((s = launched("prep_weight_kernel", st))) return s;
         const int BN = pick_bn(p.Wo);
         TcParams tp{};
         tp.mode = 0;
@@ -1657,7 +1664,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         } else {
             prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (Wc + 4), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
                                                                                       Wc, copies);
-            if ((s = launched())) return s;
+            if ((s = launched("prep_shift_kernel", st))) return s;
         }
         TcParams tp{};
         tp.mode = 1;
@@ -1687,7 +1694,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
             return s;
         if ((s = launch_conv_pass(WG_BN, ma, mb, tp, st))) return s;
         wgrad_reduce_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, KK, Co, Ci);
-        if ((s = launched())) return s;
+        if ((s = launched("wgrad_reduce_kernel", st))) return s;
     }
     return HC_OK;
 }
@@ -1762,7 +1769,7 @@ static hc_status prep_x_pieces(const hc_conv_desc* d, const Plan& p, const Bf16V
         prep_s2d_pieces_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(x, o, d->C_in, d->H, d->W, items, ps / 4);
     else
         return HC_ERR_UNSUPPORTED;
-    return launched();
+    return launched("prep_s2d_pieces_kernel", st);
 }
 
 // Output stores of a bf16 conv pass: a short K (under 16 chunks) leaves the
@@ -1806,7 +1813,7 @@ hc_status launch_bf16_fwd(const hc_conv_desc* d, const Plan& p, const float* x, 
     if (v.s2d) {
         prep_weight_s2d_pieces_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, v.s, 0,
                                                                       psw);
-        e = launched();
+        e = launched("prep_weight_s2d_pieces_kernel", st);
     } else {
         e = launch_prep_pieces(w, ap, wsz, psw, st);
     }
@@ -1869,7 +1876,7 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
                                                                           1, psw);
         else
             prep_pieces_t_kernel<<<cdiv(wsz, 256), 256, 0, st>>>(w, (__nv_bfloat16*)ap, Co, d->C_in, psw);
-        if ((e = launched())) return e;
+        if ((e = launched("prep_pieces_t_kernel", st))) return e;
         TcParams tp{};
         int BN;
         bf16_tiles(p, v, tp, &BN);
@@ -1935,7 +1942,7 @@ hc_status launch_bf16_bwd(const hc_conv_desc* d, const Plan& p, const float* x, 
             wgrad_reduce_s2d_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, Co, d->C_in, v.s, Kp);
         else
             wgrad_reduce_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, 1, Co, d->C_in);
-        if ((e = launched())) return e;
+        if ((e = launched("wgrad_reduce_kernel", st))) return e;
     }
     return HC_OK;
 }
@@ -1964,7 +1971,7 @@ __global__ void selftest_timeout_kernel(long long wait_ns) {
 hc_status launch_selftest_timeout(int wait_us, cudaStream_t st) {
     if (wait_us < 1 || wait_us > 2000000) return HC_ERR_INVALID_ARG;
     selftest_timeout_kernel<<<1, 32, 0, st>>>((long long)wait_us * 1000);
-    return launched();
+    return launched("selftest_timeout_kernel", st);
 }
 
 hc_status tc_take_status() {

@@ -128,7 +128,7 @@ EXPORTS = [
     "hc_layerscale_residual_fwd", "hc_layerscale_residual_bwd", "hc_add_inplace", "hc_selftest_timeout",
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
     "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
-    "hc_conv2d_fwd_act", "hc_conv2d_bwd_act", "hc_conv2d_bwd_residual",
+    "hc_conv2d_fwd_act", "hc_conv2d_bwd_act", "hc_conv2d_bwd_residual", "hc_trace_enable", "hc_trace_collect",
 ]
 
 
@@ -312,6 +312,28 @@ def hc_sync_check(stream=None) -> int:
 
 def hc_launch_count() -> int:
     return int(_lib.hc_launch_count())
+
+
+class hc_trace_entry(C.Structure):
+    _fields_ = [("name", C.c_char * 48), ("launches", C.c_int), ("total_ms", C.c_double)]
+
+
+_lib.hc_trace_enable.argtypes = [C.c_int]
+_lib.hc_trace_enable.restype = C.c_int
+_lib.hc_trace_collect.argtypes = [C.POINTER(hc_trace_entry), C.c_int, C.POINTER(C.c_int)]
+_lib.hc_trace_collect.restype = C.c_int
+
+
+def hc_trace_enable(on: bool) -> int:
+    return _lib.hc_trace_enable(1 if on else 0)
+
+
+def hc_trace_collect(max_entries: int = 256):
+    """(status, {kernel name: (launches, total device ms)}) since the last collect."""
+    arr = (hc_trace_entry * max_entries)()
+    n = C.c_int(0)
+    st = _lib.hc_trace_collect(arr, max_entries, C.byref(n))
+    return st, {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(n.value)}
 
 
 def check(status: int, what: str = "hc call") -> None:

@@ -43,6 +43,19 @@ def test_every_declared_symbol_is_exported(hc):
     assert set(hc.EXPORTS) <= set(names)
 
 
+def test_trace_without_launches(hc):
+    """The per-kernel trace API on the host: enabling, collecting with nothing
+    recorded, and argument errors."""
+    assert hc.hc_trace_enable(True) == hc.HC_OK
+    assert hc.hc_trace_enable(False) == hc.HC_OK
+    st, table = hc.hc_trace_collect()
+    assert table == {}
+    import ctypes as C
+    n = C.c_int(7)
+    assert hc._lib.hc_trace_collect(None, 4, C.byref(n)) == hc.HC_ERR_INVALID_ARG
+    assert hc._lib.hc_trace_collect(None, 0, None) == hc.HC_ERR_INVALID_ARG
+
+
 def test_status_strings(hc):
     for s in range(6):
         assert hc.hc_status_string(s) and hc.hc_status_string(s) != "unknown status"
