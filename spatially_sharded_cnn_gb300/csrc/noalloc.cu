@@ -4,9 +4,12 @@
 // The scratch that hc_conv2d_bwd keeps in the caller's workspace lives here in
 // one statically sized device array instead.  Host code may not hand the
 // array's name to a kernel (on the host it is only a stand-in for the device
-// symbol), so each device's real address is looked up once with
+// symbol), so the device's real address is looked up with
 // cudaGetSymbolAddress, with that device current, and that address is what
-// the kernels receive.
+// the kernels receive.  It is looked up again on every call made outside a
+// stream capture (so an address from before a device reset is never reused);
+// a call into a capturing stream uses the address of the device's last such
+// lookup.
 #include <mutex>
 
 #include "common.cuh"
@@ -17,7 +20,6 @@ namespace {
 // 16 MiB: enough for the depthwise scratch of e.g. 8 shards x 256 channels x
 // 2 column tiles x 7 images of 7x7 partials (5.7 MB) with room to spare.
 constexpr size_t kNoAllocScratchBytes = 16u << 20;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -26,24 +28,33 @@ void* g_scratch_addr[kMaxDevices];  // per device, filled on first use
 
 size_t round_up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Device address of the scratch array on the current device (looked up once).
-hc_status scratch_on_current_device(void** out) {
+// Device address of the scratch array on the current device: looked up now
+// unless `st` is capturing, then the device's last looked-up address.
+hc_status scratch_on_current_device(cudaStream_t st, void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return HC_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return HC_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return HC_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (cs != cudaStreamCaptureStatusNone) {  // no lookup inside a capture
+        if (!cached || !g_scratch_addr[dev]) return HC_ERR_UNSUPPORTED;
+        *out = g_scratch_addr[dev];
+        return HC_OK;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return HC_ERR_CUDA;
+    }
+    if (cached) g_scratch_addr[dev] = p;
+    *out = p;
     return HC_OK;
 }
 
@@ -74,13 +85,14 @@ extern "C" hc_status hc_conv2d_bwd_depthwise_noalloc(const hc_conv_desc* d, cons
     if (gwp_bytes + gbp_bytes + tile_bytes > kNoAllocScratchBytes) return HC_ERR_WORKSPACE;
 
     void* base = nullptr;
-    if ((st = scratch_on_current_device(&base))) return st;
+    if ((st = scratch_on_current_device((cudaStream_t)stream, &base))) return st;
     char* s = (char*)base;
     float* gwp = gw_partials ? gw_partials : (float*)s;
     float* gbp = gb_partials ? gb_partials : (float*)(s + gwp_bytes);
     float* tile_part = (float*)(s + gwp_bytes + gbp_bytes);
 
     cudaStream_t cs = (cudaStream_t)stream;
+    traced_begin(cs);
     const bool want_wb = gw || gb || gw_partials || gb_partials;
     return launch_depthwise_bwd(d, p, x, w, gy, gx, tile_part, gwp, gbp, want_wb, cs, nullptr, gw, gb);
 }

@@ -5,8 +5,10 @@ Some callers may not allocate device memory when they call the backward pass
 allocate after start-up), so they cannot hand hc_conv2d_bwd a workspace.
 hc_conv2d_bwd_depthwise_noalloc keeps that scratch in a library-owned static
 device array instead.  This test checks, through the C ABI, that two calls in a
-row give the same results as the workspace-taking entry point (within the
-tolerances the other GPU tests use), and that sizes beyond the array are
+row give bit-for-bit the results of the workspace-taking entry point (same
+kernels, same sums in the same order), that they match the oracle within the
+tolerances the other GPU tests use -- including a case whose scratch reaches
+past the middle of the 16 MiB array -- and that sizes beyond the array are
 refused.  The file is named so that pytest collects it last.
 """
 import numpy as np
@@ -46,10 +48,26 @@ def _outputs(cfg, S):
                 gb=R.Guarded((cfg["C_out"],)), gwp=R.Guarded((S,) + wshape), gbp=R.Guarded((S, cfg["C_out"])))
 
 
-@pytest.mark.parametrize("shape", [(2, 4, 70, 512, 4), (1, 8, 40, 512, 2)], ids=["ragged_S4", "two_tiles_S2"])
-def test_noalloc_matches_workspace_entry_point(hc, shape):
+def _scratch_bytes(N, C, W, S):
+    """The entry point's scratch for a depthwise 7x7 desc: shard partials of the
+    weight and bias gradients, then per-(shard, channel, 128-column tile, image)
+    partials of 49 + 1 floats, each region rounded up to 256 bytes."""
+    r = lambda b: (b + 255) // 256 * 256
+    return r(4 * S * C * 49) + r(4 * S * C) + r(4 * S * C * (W // S // 128) * N * 50)
+
+
+# (N, C, H, W, S): a ragged row tile over 4 shards; two column tiles per shard; and
+# 12 images x 256 channels x 8 tiles per shard x 2 shards, whose 9.9 MB of scratch
+# runs past the first 8 MiB of the array
+SHAPES = [(2, 4, 70, 512, 4), (1, 8, 40, 512, 2), (12, 256, 8, 2048, 2)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=["ragged_S4", "two_tiles_S2", "scratch_past_8MiB"])
+def test_noalloc_matches_workspace_entry_point_and_oracle(hc, orc, shape):
     N, C, H, W, S = shape
     cfg, x, w, gy = _case(N, C, H, W, S, seed=11)
+    if shape == SHAPES[2]:
+        assert _scratch_bytes(N, C, W, S) > (8 << 20)
     d = hc.desc(cfg)
     xd, wd, gyd = R.dev(x), R.dev(w), R.dev(gy)
     ref = _outputs(cfg, S)
@@ -58,21 +76,29 @@ def test_noalloc_matches_workspace_entry_point(hc, shape):
                               ref["gbp"].view, ws, nb, algo=hc.HC_ALGO_DEPTHWISE), "workspace bwd")
     hc.check(hc.hc_sync_check(), "workspace bwd sync")
     want = {k: v.numpy() for k, v in ref.items()}
+    # the oracle: unsharded gradients and the sharded method's per-shard partials
+    o_gx = orc.conv2d_bwd_input(cfg, w, gy)
+    o_gw = orc.conv2d_bwd_weight(cfg, x, gy)
+    o_gb = orc.conv2d_bwd_bias(cfg, gy)
+    _, o_gwp, o_gbp = orc.sharded_bwd(cfg, x, w, gy)
+    oracle_ref = dict(gx=o_gx, gw=o_gw, gb=o_gb, gwp=o_gwp, gbp=o_gbp)
     for call in range(2):  # the shared scratch keeps the previous call's contents
         got = _outputs(cfg, S)
         hc.check(hc.hc_conv2d_bwd_depthwise_noalloc(d, xd, wd, gyd, got["gx"].view, got["gw"].view, got["gb"].view,
                                                      got["gwp"].view, got["gbp"].view), f"noalloc call {call}")
         hc.check(hc.hc_sync_check(), f"noalloc sync {call}")
         g = {k: v.numpy() for k, v in got.items()}
-        assert R.normwise(g["gx"], want["gx"]) <= TOL_GX
+        for k in want:
+            assert np.array_equal(g[k], want[k]), (call, k)  # same kernels and sums: bit-identical
+        assert R.normwise(g["gx"], oracle_ref["gx"]) <= TOL_GX, call
         for k in ("gw", "gb", "gwp", "gbp"):
-            assert R.normwise(g[k], want[k]) <= TOL_W, (call, k)
+            assert R.normwise(g[k], oracle_ref[k]) <= TOL_W, (call, k)
     # weight gradients only (grad_input skipped, partials kept in the scratch)
     got = _outputs(cfg, S)
     hc.check(hc.hc_conv2d_bwd_depthwise_noalloc(d, xd, wd, gyd, None, got["gw"].view, got["gb"].view), "noalloc w")
     hc.check(hc.hc_sync_check(), "noalloc w sync")
-    assert R.normwise(got["gw"].numpy(), want["gw"]) <= TOL_W
-    assert R.normwise(got["gb"].numpy(), want["gb"]) <= TOL_W
+    assert np.array_equal(got["gw"].numpy(), want["gw"])
+    assert np.array_equal(got["gb"].numpy(), want["gb"])
 
 
 def test_noalloc_refuses_oversized_and_unsupported(hc):
