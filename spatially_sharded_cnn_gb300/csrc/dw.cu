@@ -200,6 +200,24 @@ struct Sched {
             c = rest / col_tiles;
         }
     }
+    // the item after (n, c, ct) in this order, without divisions
+    __device__ __forceinline__ void next(int& n, int& c, int& ct) const {
+        if (tile_fastest) {
+            if (++ct == col_tiles) {
+                ct = 0;
+                if (++n == N) {
+                    n = 0;
+                    ++c;
+                }
+            }
+        } else if (++n == N) {
+            n = 0;
+            if (++ct == col_tiles) {
+                ct = 0;
+                ++c;
+            }
+        }
+    }
     __device__ __forceinline__ void range(int& i0, int& i1) const {
         i0 = (int)((long long)blockIdx.x * items / gridDim.x);
         i1 = (int)((long long)(blockIdx.x + 1) * items / gridDim.x);
@@ -255,10 +273,11 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
     float wt[K][K];
     float bv = 0.0f;
     int cur_c = -1;
+    // this warp's job: item (n, c, ct) and row tile t, advanced one job at a time
+    int n, c, ct, t = 0, s = 0;
+    unsigned ph = 0;  // phase of stage s's barrier this job waits for
+    sc.decode(i0, n, c, ct);
     for (int q = 0; q < jobs; q++) {
-        const int t = q % ntiles, s = q % NSTAGE;
-        int n, c, ct;
-        sc.decode(i0 + q / ntiles, n, c, ct);
         if (c != cur_c) {
 #pragma unroll
             for (int u = 0; u < K; u++)
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
             bv = bias ? __ldg(bias + c) : 0.0f;
             cur_c = c;
         }
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(full + s, (unsigned)((q / NSTAGE) & 1)));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(full + s, ph));
         if (!ok) {
             if (lane == 0) {
                 atomicCAS(&g_dw_status, 0, (int)HC_ERR_TIMEOUT);
@@ -301,6 +320,14 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
             if (h < sc.H)
                 *reinterpret_cast<float4*>(yp + (long long)h * sc.W) =
                     make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        }
+        if (++s == NSTAGE) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (++t == ntiles) {
+            t = 0;
+            sc.next(n, c, ct);
         }
     }
     // A warp that gave up: wait (bounded) for the copies still in flight, so
@@ -368,11 +395,23 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         seg_end = rest == R * tpr - 1;
     };
 
+    // Thread 0 issues the jobs in order; without row shards its cursor (in_, ic,
+    // ict, it) advances one job at a time (no divisions).
+    int in_ = 0, ic = 0, ict = 0, it = 0;
+    if (!ROWS) sc.decode(i0, in_, ic, ict);
     auto issue = [&](int q) {
         int n, c, ct, item, t;
-        bool se;
-        job(q, item, t, se);
-        sc.decode(item, n, c, ct);
+        if (ROWS) {
+            bool se;
+            job(q, item, t, se);
+            sc.decode(item, n, c, ct);
+        } else {
+            n = in_, c = ic, ct = ict, t = it;
+            if (++it == ntiles) {
+                it = 0;
+                sc.next(in_, ic, ict);
+            }
+        }
         uint64_t* bar = full + (q % NSTAGE);
         float* st = tiles + (q % NSTAGE) * 2 * G::TILE;
         mbar_expect_tx(bar, want_wb ? 2 * G::BYTES : G::BYTES);
@@ -390,37 +429,45 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
 
     // The ring, shared by both roles: every warp waits for job q's stage, does
     // its role's work on it, and the stage is refilled after a CTA barrier.
-    // work(q, n, c, ct, t, flush): flush = the last job of a weight-gradient run
-    // (segment).  Returns false when a wait timed out.
+    // work(s, n, c, ct, t, flush): s = the job's stage; flush = the last job of a
+    // weight-gradient run (segment).  Returns false when a wait timed out.
     auto ring = [&](auto&& on_channel, auto&& work) {
         int cur_c = -1;
+        // without row shards: job q's item (n, c, ct) and row tile t, advanced one job at a time
+        int n, c, ct, t = 0, s = 0;
+        unsigned ph = 0;  // phase of stage s's barrier this job waits for
+        if (!ROWS) sc.decode(i0, n, c, ct);
         for (int q = 0; q < jobs; q++) {
-            int n, c, ct, item, t;
-            bool seg_end;
-            job(q, item, t, seg_end);
-            sc.decode(item, n, c, ct);
-            int nn = 0, cn = c, ctn = ct;
-            const bool has_next = q + 1 < jobs;
-            if (has_next) {
-                int item2, t2;
-                bool se2;
-                job(q + 1, item2, t2, se2);
-                sc.decode(item2, nn, cn, ctn);
+            bool flush;
+            if (ROWS) {
+                int item;
+                job(q, item, t, flush);  // the last job of a (run, row shard) segment
+                sc.decode(item, n, c, ct);
+            } else {
+                // the last job of a run: its last row tile, and the next job (if any)
+                // is another (c, column tile) -- with n fastest, exactly when n = N - 1
+                flush = t == ntiles - 1 && (q + 1 == jobs || n == sc.N - 1);
             }
             if (c != cur_c) {
                 on_channel(c);
                 cur_c = c;
             }
-            const bool ok = mbar_wait(full + (q % NSTAGE), (unsigned)((q / NSTAGE) & 1));
+            const bool ok = mbar_wait(full + s, ph);
             if (__syncthreads_or(!ok)) {
                 give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
                 return;
             }
-            const bool last_tile = t == ntiles - 1;
-            const bool flush = ROWS ? seg_end : (last_tile && (!has_next || cn != c || ctn != ct));
-            work(q, n, c, ct, t, flush);
+            work(s, n, c, ct, t, flush);
             __syncthreads();  // every warp is done with this stage
             if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
+            if (++s == NSTAGE) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (!ROWS && ++t == ntiles) {
+                t = 0;
+                sc.next(n, c, ct);
+            }
         }
     };
 
@@ -434,9 +481,9 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
 #pragma unroll
                     for (int v = 0; v < K; v++) wf[u][v] = __ldg(a.w + c * KK + (K - 1 - u) * K + (K - 1 - v));
             },
-            [&](int q, int n, int c, int ct, int t, bool) {
+            [&](int s, int n, int c, int ct, int t, bool) {
                 if (!a.gx) return;
-                const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
+                const float* gys = tiles + s * 2 * G::TILE;
                 const long long off = ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
                 float* gp = a.gx + off;
 #pragma unroll 1
@@ -479,10 +526,10 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
         int run_n0 = -1;  // first image of the current (c, column tile) run
         ring([](int) {},
-             [&](int q, int n, int c, int ct, int t, bool flush) {
+             [&](int s, int n, int c, int ct, int t, bool flush) {
                  if (!want_wb) return;
                  if (run_n0 < 0) run_n0 = n;
-                 const float* gys = tiles + (q % NSTAGE) * 2 * G::TILE;
+                 const float* gys = tiles + s * 2 * G::TILE;
                  const float* xs = gys + G::TILE;
 #pragma unroll 1
                  for (int half = 0; half < 2; half++) {
@@ -506,16 +553,16 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                  for (int u = 0; u < K; u++)
 #pragma unroll
                      for (int v = 0; v < K; v++) {
-                         float s = gw[u][v];
+                         float sum = gw[u][v];
 #pragma unroll
-                         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                         if (lane == 0) red[wg * WSLOT + u * K + v] = s;
+                         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                         if (lane == 0) red[wg * WSLOT + u * K + v] = sum;
                          gw[u][v] = 0.0f;
                      }
-                 float s = gbs;
+                 float sum = gbs;
 #pragma unroll
-                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                 if (lane == 0) red[wg * WSLOT + KK] = s;
+                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                 if (lane == 0) red[wg * WSLOT + KK] = sum;
                  gbs = 0.0f;
                  asm volatile("bar.sync 1, %0;\n" ::"n"(BWD_WARPS * 32) : "memory");  // the weight-gradient warps
                  if (wtid <= KK) {
@@ -595,10 +642,11 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
     const size_t smem = sizeof(float) * NSTAGE * G::TILE + NSTAGE * sizeof(uint64_t) + (NSTAGE + 2) * sizeof(int);
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
-        cudaFuncSetAttribute(dw_fwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return cudaFuncSetAttribute(dw_fwd_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+               cudaSuccess;
     });
     dw_fwd_kernel<K><<<grid, FWD_WARPS * 32, smem, st>>>(xm, w, b, y, sc);
-    return launched();
+    return launched("dw_fwd_kernel", st);
 }
 
 template <int K>
@@ -616,10 +664,11 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
-        cudaFuncSetAttribute(dw_bwd_kernel<K, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(dw_bwd_kernel<K, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(dw_bwd_kernel<K, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(dw_bwd_kernel<K, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        return cudaFuncSetAttribute(dw_bwd_kernel<K, false, false>, A, (int)smem) == cudaSuccess &&
+               cudaFuncSetAttribute(dw_bwd_kernel<K, true, false>, A, (int)smem) == cudaSuccess &&
+               cudaFuncSetAttribute(dw_bwd_kernel<K, false, true>, A, (int)smem) == cudaSuccess &&
+               cudaFuncSetAttribute(dw_bwd_kernel<K, true, true>, A, (int)smem) == cudaSuccess;
     });
     BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
     const dim3 grd(grid), blk(2 * BWD_WARPS * 32);
@@ -633,12 +682,12 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     } else {
         dw_bwd_kernel<K, false, false><<<grd, blk, smem, st>>>(gm, xm, a, sc);
     }
-    s = launched();
+    s = launched("dw_bwd_kernel", st);
     if (s || !want_wb) return s;
     const long long total = (long long)d->C_in * (K * K + 1);
     dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, gw, gb, p.Q,
                                                                              d->C_in, tps * d->N, K * K);
-    return launched();
+    return launched("dw_shard_partials_kernel", st);
 }
 
 }  // namespace
