@@ -99,6 +99,63 @@ def alu_peak(peaks, sms):
     return sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
 
 
+# Source file of each traced kernel (a DRAM-traffic record applies only to the source it was taken on).
+KERNEL_SRC = {"dw_": "dw.cu", "tc_conv_kernel": "tc.cu", "ln_": "pointwise.cu", "ls_": "pointwise.cu",
+              "bias_rows": "reduce.cu", "direct_": "direct.cu"}
+
+
+def kernel_src(name):
+    for pre, f in KERNEL_SRC.items():
+        if name.startswith(pre):
+            return os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc", f)
+    return None
+
+
+def kernel_table(trace, steps):
+    """Traced kernels: launches per step, device ms per launch and share of the traced time."""
+    tot = sum(ms for _, ms in trace.values()) or 1.0
+    return {k: {"launches_per_step": n / steps, "ms_per_launch": ms / n, "ms_per_step": ms / steps,
+                "share": ms / tot}
+            for k, (n, ms) in sorted(trace.items(), key=lambda kv: -kv[1][1])}
+
+
+def peak_of(bound, peaks, sms):
+    if bound == "alu":
+        return alu_peak(peaks, sms), "TFLOP/s", \
+            f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz"
+    if bound == "tensor_tf32":
+        return tc_peak(peaks), "TFLOP/s (fp32-equivalent, 3xTF32)", \
+            f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (nominal tf32/bf16) / 3 (3xTF32 passes)"
+    if bound == "tensor":
+        return bf16x6_peak(peaks), "TFLOP/s (fp32-equivalent, six bf16 products)", \
+            f"measured bf16 {peaks['bf16']:.0f} TFLOP/s / 6 (bf16 products per fp32 product)"
+    return peaks["hbm"], "GB/s", f"{peaks['src']} HBM copy bandwidth"
+
+
+def kernel_rooflines(table, work, peaks, sms):
+    """Each traced kernel with a work entry, against its own bound; the dominant
+    one (largest device time per step) is the line's roofline."""
+    out = {}
+    for k, row in table.items():
+        if k not in work:
+            continue
+        bound, amount, nbytes = work[k]
+        t = row["ms_per_step"] * 1e-3
+        peak, unit, src = peak_of(bound, peaks, sms)
+        a = amount / t / (1e9 if bound == "hbm" else 1e12)
+        r = {"bound": bound if bound in ("alu", "hbm") else "tensor", "kernel": k, "achieved": a, "peak": peak,
+             "unit": unit, "frac": a / peak, "peak_source": src, "ms_per_launch": row["ms_per_launch"],
+             "launches_per_step": row["launches_per_step"], "share": row["share"]}
+        if nbytes:
+            gbs = nbytes / t / 1e9
+            r["hbm"] = {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                        "peak_source": peaks["src"]}
+        src_file = kernel_src(k)
+        r["traffic"] = traffic_for(k, src_file) if src_file else None
+        out[k] = r
+    return out
+
+
 class Runner:
     """Device state shared by the workloads: the C ABI, a stream, a workspace
     shared by the backward passes and the pointwise ops, each conv's forward
@@ -224,8 +281,45 @@ class ConvWorkload:
     def host_io(self):
         t = self.R.torch
         x, w, b, gy = self.host
-        self.h_in = [(self.x, t.from_numpy(x).pin_memory()), (self.gy, t.from_numpy(gy).pin_memory())]
+        self.h_in = [(d, t.from_numpy(h).pin_memory()) for d, h in ((self.x, x), (self.w, w), (self.b, b), (self.gy, gy))]
         self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in (self.y, self.gx, self.gw, self.gb)]
+
+    def kernel_work(self):
+        """Algorithmic work per step of each compute kernel, by trace name:
+        (bound, amount, HBM bytes or None)."""
+        F = conv_flops(self.cfg)
+        if self.name == "dw7":
+            return {"dw_fwd_kernel": ("alu", F, 8 * self.E), "dw_bwd_kernel": ("alu", 2 * F, 12 * self.E)}
+        if self.name == "dense5x5":
+            return {"tc_conv_kernel 3xTF32 conv pass": ("tensor_tf32", 2 * F, None),
+                    "tc_conv_kernel 3xTF32 weight-gradient pass": ("tensor_tf32", F, None)}
+        return {}
+
+    def oracle_sample(self, orc):
+        """One bounded sample of this workload for the oracle, fwd + bwd: config1
+        whole; the others one image and a band of rows (the same kernel, channels
+        and width).  Returns (run: the oracle calls on inputs made here, units of
+        the metric one run does, description)."""
+        from spatially_sharded_cnn_gb300 import synth
+        c = dict(self.cfg)
+        c.pop("num_shards_h", None)
+        if self.name != "config1":
+            c["N"], c["H"] = 1, (32 if self.name == "dw7" else 4)
+        x = synth.normal((c["N"], c["C_in"], c["H"], c["W"]), 1.0, 0, 1)
+        w = synth.normal((c["C_out"], c["C_in"] // c["groups"], c["kh"], c["kw"]), 0.02, 0, 2)
+        b = synth.normal((c["C_out"],), 0.01, 0, 3)
+        Ho = (c["H"] + 2 * c["padding"] - c["kh"]) // c["stride"] + 1
+        Wo = (c["W"] + 2 * c["padding"] - c["kw"]) // c["stride"] + 1
+        gy = synth.normal((c["N"], c["C_out"], Ho, Wo), 1.0, 0, 4)
+
+        def run():
+            orc.conv2d_fwd(c, x, w, b)
+            orc.conv2d_bwd_input(c, w, gy)
+            orc.conv2d_bwd_weight(c, x, gy)
+            orc.conv2d_bwd_bias(c, gy)
+        units = 5 * 4 * x.size / 1e9 if not self.dense else 3 * conv_flops(c) / 1e12
+        return run, units, (f"{c['N']} image(s) x {c['H']} of {self.cfg['H']} rows of the {self.desc.split(', x ')[0]} "
+                       f"workload (shape {[c['N'], c['C_in'], c['H'], c['W']]}), fwd+bwd")
 
     def value(self, ms):
         return self.flops / (ms * 1e-3) / 1e12 if self.dense else self.bytes / (ms * 1e-3) / 1e9
@@ -253,27 +347,7 @@ class ConvWorkload:
                     "unit": "TFLOP/s", "frac": a / alu, "traffic": None,
                     "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                     "ms_per_launch": ms}
-        if self.dense:
-            peak = tc_peak(peaks)
-            a = conv_flops(self.cfg) / (ops_ms["conv_fwd"] * 1e-3) / 1e12
-            return {"bound": "tensor", "kernel": "tc_conv_kernel<256, 0> (3xTF32; forward call incl. operand prep)",
-                    "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, 3xTF32)", "frac": a / peak,
-                    "traffic": traffic_for("tc_conv_kernel<256, 0>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
-                                                                                  "csrc", "tc.cu")),
-                    "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s x 1.1/2.25 (tf32) / 3 (3xTF32 passes)",
-                    "ms_per_launch": ops_ms["conv_fwd"]}
-        alu = alu_peak(peaks, sms)
-        bms = ops_ms["conv_bwd"]
-        a = 2 * conv_flops(self.cfg) / (bms * 1e-3) / 1e12
-        gbs = 3 * 4 * self.E / (bms * 1e-3) / 1e9
-        return {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": a, "peak": alu, "unit": "TFLOP/s",
-                "frac": a / alu,
-                "traffic": traffic_for("dw_bwd_kernel<7>", os.path.join(ROOT, "spatially_sharded_cnn_gb300", "csrc",
-                                                                        "dw.cu")),
-                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
-                "hbm": {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                        "peak_source": peaks["src"]},
-                "ms_per_launch": bms}
+        return None  # the dominant traced kernel's roofline (kernel_roofline) applies
 
 
 def gen_dw7(N=7, seed=0):
@@ -401,9 +475,72 @@ class BlockWorkload:
 
     def host_io(self):
         t = self.R.torch
-        self.h_in = [(self.img, t.from_numpy(self.h_img).pin_memory()), (self.gy, t.from_numpy(self.h_gy).pin_memory())]
+        ins = (self.img, self.gy, self.w_stem, self.w_dw, self.w1, self.w2, self.b256, self.b1024, self.ln_g, self.ln_b,
+               self.ls_g)
+        self.h_in = [(d, d.cpu().pin_memory()) for d in ins]
         outs = (self.out, self.gw_stem, self.gb_stem, self.gw_dw, self.gw1, self.gw2, self.g_lng, self.g_lnb, self.g_ls)
         self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in outs]
+
+    def kernel_work(self):
+        """Algorithmic work per step of the compute kernels, by trace name: the
+        bf16-piece GEMM passes (stem, 1x1 256->1024, 1x1 1024->256: forward and
+        grad_input conv passes, weight-gradient passes) and the depthwise stencil."""
+        st, dw, p1, p2 = (conv_flops(c) for c in (self.stem, self.dw, self.pw1, self.pw2))
+        E = self.N * 256 * self.HW
+        return {"tc_conv_kernel bf16x6 conv pass": ("tensor", st + 2 * p1 + 2 * p2, None),
+                "tc_conv_kernel bf16x6 weight-gradient pass": ("tensor", st + p1 + p2, None),
+                "dw_fwd_kernel": ("alu", dw, 8 * E), "dw_bwd_kernel": ("alu", 2 * dw, 16 * E)}
+
+    def oracle_sample(self, orc):
+        """The block's chain for the oracle, forward and backward, on one image
+        and a band of 8 of its 512 input rows (2 rows of the stem output)."""
+        from spatially_sharded_cnn_gb300 import synth
+        f32 = lambda a: np.ascontiguousarray(a, np.float32)
+        img = synth.uniform((1, 3, 8, 4096), 0.0, 1.0, 0, 1)
+        cs = dict(self.stem, N=1, H=8)
+        cd = dict(self.dw, N=1, H=2)
+        c1 = dict(self.pw1, N=1, H=2)
+        c2 = dict(self.pw2, N=1, H=2)
+        for c in (cs, cd, c1, c2):
+            c.pop("num_shards_h", None)
+        ws = synth.trunc_normal((256, 3, 4, 4), 0.02, 0, 2)
+        wd = synth.trunc_normal((256, 1, 7, 7), 0.02, 0, 3)
+        w1 = synth.trunc_normal((1024, 256, 1, 1), 0.02, 0, 4)
+        w2 = synth.trunc_normal((256, 1024, 1, 1), 0.02, 0, 5)
+        z256, z1024 = np.zeros(256, np.float32), np.zeros(1024, np.float32)
+        g, bt, ls = np.ones(256), np.zeros(256), np.full(256, 1e-6)
+        gy = synth.normal((1, 256, 2, 1024), 1.0, 0, 9)
+        flops = sum(conv_flops(c) for c in (cs, cd, c1, c2)) + conv_flops(cs) + 2 * sum(conv_flops(c) for c in (cd, c1, c2))
+        return lambda: self._oracle_chain(orc, img, ws, wd, w1, w2, z256, z1024, g, bt, ls, gy, cs, cd, c1, c2), \
+            flops / 1e12, ("the block's chain (stem, depthwise, LayerNorm, 1x1, GELU, 1x1, layer scale + residual), "
+                           "fwd+bwd, on 1 image x 8 of 512 input rows of the (7,3,512,4096) batch")
+
+    @staticmethod
+    def _oracle_chain(orc, img, ws, wd, w1, w2, z256, z1024, g, bt, ls, gy, cs, cd, c1, c2):
+        f32 = lambda a: np.ascontiguousarray(a, np.float32)
+        s = f32(orc.conv2d_fwd(cs, img, ws, z256))
+        d = f32(orc.conv2d_fwd(cd, s, wd, z256))
+        ln, _, _ = orc.layernorm_c_fwd(d, g, bt, 1e-6)
+        h = orc.conv2d_fwd(c1, f32(ln), w1, z1024)
+        a = f32(orc.gelu_fwd(h))
+        b2 = orc.conv2d_fwd(c2, a, w2, z256)
+        orc.layerscale_residual_fwd(s, b2, ls)
+        _, g_b2, _ = orc.layerscale_residual_bwd(b2, ls, gy)
+        g_b2 = f32(g_b2)
+        g_a = f32(orc.conv2d_bwd_input(c2, w2, g_b2))
+        orc.conv2d_bwd_weight(c2, a, g_b2)
+        orc.conv2d_bwd_bias(c2, g_b2)
+        g_h = f32(orc.gelu_bwd(h, g_a))
+        g_l = orc.conv2d_bwd_input(c1, w1, g_h)
+        orc.conv2d_bwd_weight(c1, f32(ln), g_h)
+        orc.conv2d_bwd_bias(c1, g_h)
+        g_d, _, _ = orc.layernorm_c_bwd(d, g, g_l, 1e-6)
+        g_d = f32(g_d)
+        g_s = f32(orc.conv2d_bwd_input(cd, wd, g_d) + gy)
+        orc.conv2d_bwd_weight(cd, s, g_d)
+        orc.conv2d_bwd_bias(cd, g_d)
+        orc.conv2d_bwd_weight(cs, img, g_s)
+        orc.conv2d_bwd_bias(cs, g_s)
 
     def value(self, ms):
         return self.flops / (ms * 1e-3) / 1e12
@@ -421,16 +558,7 @@ class BlockWorkload:
                 "ls_fwd": ("hbm", 12 * E), "ls_bwd": ("hbm", 12 * E)}
 
     def roofline(self, ops_ms, peaks, sms):
-        peak = bf16x6_peak(peaks)
-        a = conv_flops(self.pw1) / (ops_ms["pw1_fwd"] * 1e-3) / 1e12
-        return {"bound": "tensor",
-                "kernel": "tc_conv_kernel<256, 1> on bf16 pieces (1x1 256->1024 forward call incl. operand prep)",
-                "achieved": a, "peak": peak, "unit": "TFLOP/s (fp32-equivalent, six bf16 products)",
-                "frac": a / peak,
-                "traffic": traffic_for("tc_conv_kernel<256, 1>", os.path.join(ROOT, "spatially_sharded_cnn_gb300",
-                                                                              "csrc", "tc.cu")),
-                "peak_source": f"measured bf16 {peaks['bf16']:.0f} TFLOP/s / 6 (bf16 products per fp32 product)",
-                "ms_per_launch": ops_ms["pw1_fwd"]}
+        return None  # the dominant traced kernel's roofline applies
 
 
 class DwDownWorkload:
@@ -480,9 +608,43 @@ class DwDownWorkload:
 
     def host_io(self):
         t = self.R.torch
-        self.h_in = [(self.x, t.from_numpy(self.h_x).pin_memory()), (self.gz, t.from_numpy(self.h_gz).pin_memory())]
+        ins = (self.x, self.gz, self.w_dw, self.w_dn, self.b256, self.b512)
+        self.h_in = [(d, d.cpu().pin_memory()) for d in ins]
         outs = (self.z, self.gx, self.gw_dw, self.gb_dw, self.gw_dn, self.gb_dn)
         self.h_out = [(o, t.empty_like(o, device="cpu").pin_memory()) for o in outs]
+
+    def kernel_work(self):
+        """Algorithmic work per step by trace name: the depthwise stencil (FP32
+        ALU) and the downsample's bf16-piece GEMM passes."""
+        dw, dn = conv_flops(self.dw), conv_flops(self.down)
+        E = self.N * 256 * 128 * 2048
+        return {"dw_fwd_kernel": ("alu", dw, 8 * E), "dw_bwd_kernel": ("alu", 2 * dw, 12 * E),
+                "tc_conv_kernel bf16x6 conv pass": ("tensor", 2 * dn, None),
+                "tc_conv_kernel bf16x6 weight-gradient pass": ("tensor", dn, None)}
+
+    def oracle_sample(self, orc):
+        """Depthwise then downsample for the oracle, forward and backward, on one
+        image and 4 of its 128 rows."""
+        from spatially_sharded_cnn_gb300 import synth
+        f32 = lambda a: np.ascontiguousarray(a, np.float32)
+        cd, cn = dict(self.dw, N=1, H=4), dict(self.down, N=1, H=4)
+        x = synth.normal((1, 256, 4, 2048), 1.0, 0, 1)
+        wd = synth.trunc_normal((256, 1, 7, 7), 0.02, 0, 2)
+        wn = synth.trunc_normal((512, 256, 2, 2), 0.02, 0, 3)
+        z = np.zeros(512, np.float32)
+        gz = synth.normal((1, 512, 2, 1024), 1.0, 0, 9)
+
+        def run():
+            d = f32(orc.conv2d_fwd(cd, x, wd, z[:256]))
+            orc.conv2d_fwd(cn, d, wn, z)
+            gd = f32(orc.conv2d_bwd_input(cn, wn, gz))
+            orc.conv2d_bwd_weight(cn, d, gz)
+            orc.conv2d_bwd_bias(cn, gz)
+            orc.conv2d_bwd_input(cd, wd, gd)
+            orc.conv2d_bwd_weight(cd, x, gd)
+            orc.conv2d_bwd_bias(cd, gd)
+        return run, 3 * (conv_flops(cd) + conv_flops(cn)) / 1e12, \
+            "depthwise 7x7 + 2x2/s2 downsample, fwd+bwd, on 1 image x 4 of 128 rows of the (7,256,128,2048) batch"
 
     def value(self, ms):
         return self.flops / (ms * 1e-3) / 1e12
@@ -495,12 +657,7 @@ class DwDownWorkload:
                 "down_bwd": ("tensor", 2 * dn)}
 
     def roofline(self, ops_ms, peaks, sms):
-        alu = alu_peak(peaks, sms)
-        a = 2 * conv_flops(self.dw) / (ops_ms["dw_bwd"] * 1e-3) / 1e12
-        return {"bound": "alu", "kernel": "dw_bwd_kernel<7>", "achieved": a, "peak": alu, "unit": "TFLOP/s",
-                "frac": a / alu, "traffic": None,
-                "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
-                "ms_per_launch": ops_ms["dw_bwd"]}
+        return None  # the dominant traced kernel's roofline applies
 
 
 def make_workload(name, batch=None, drop_path=0.0, shards_h=1):
@@ -598,55 +755,112 @@ def traffic_for(kernel: str, src_file: str):
     return d["bytes_per_launch"] if d.get("source_sha") == h else None
 
 
-def oracle_depthwise_sample(channels, images=1, max_seconds=20.0):
-    """The oracle as it stands on this host's cores, on a bounded sample of the
-    depthwise workload: `images` image(s) x `channels` channels of the
-    (7,256,128,512) batch, forward + backward, repeated while time remains.
-    Returns (GB/s of algorithmic bytes, threads, description, seconds per rep)."""
+def oracle_sample(wl, max_seconds=20.0, reps_max=4):
+    """The oracle as it stands, on this host's cores, on a bounded sample of the
+    workload (its oracle_sample: one image and a band of rows; config1 whole),
+    forward + backward, repeated while time remains (inputs made outside the
+    timing).  Returns (the metric's rate on the sample, threads, description,
+    seconds per repetition)."""
     import oracle
-    from spatially_sharded_cnn_gb300 import synth
     orc = oracle.load()
-    cfg = conv_cfg(images, channels, 128, 512, channels, 7, 1, 3, channels, 4)
-    x = synth.normal((images, channels, 128, 512), 1.0, 0, 1)
-    w = synth.trunc_normal((channels, 1, 7, 7), 0.02, 0, 2)
-    b = np.zeros((channels,), np.float32)
-    gy = synth.normal((images, channels, 128, 512), 1.0, 0, 4)
+    run, units, desc = wl.oracle_sample(orc)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        orc.conv2d_fwd(cfg, x, w, b)
-        orc.conv2d_bwd_input(cfg, w, gy)
-        orc.conv2d_bwd_weight(cfg, x, gy)
-        orc.conv2d_bwd_bias(cfg, gy)
+        run()
         reps += 1
-        if time.perf_counter() - t0 > max_seconds / 2 or reps >= 4:
+        if time.perf_counter() - t0 > max_seconds / 2 or reps >= reps_max:
             break
     dt = (time.perf_counter() - t0) / reps
-    sample_bytes = 5 * 4 * images * channels * 128 * 512
-    return (sample_bytes / dt / 1e9, orc.num_threads(),
-            f"{images} image(s) x {channels} of 256 channels of the (7,256,128,512) batch, fwd+bwd, {reps} rep(s)", dt)
+    return units / dt, orc.num_threads(), f"{desc}, {reps} rep(s)", dt
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle timed on the host cores on the depthwise
-    workload's config and metric, each step a bounded sample (1 image x 16 channels)."""
+    """Reference arm: the CPU oracle timed on the host cores on the chosen
+    workload's config and metric, each step one bounded sample of it."""
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
-    wl = make_workload("dw7")
+    import oracle
+    wl = make_workload(args.workload, args.batch, args.drop_path, args.shards_h)
+    orc = oracle.load()
+    run, units, desc = wl.oracle_sample(orc)
     for _ in range(args.warmup):
-        oracle_depthwise_sample(16, max_seconds=0.0)
-    steps, cores = [], 1
+        run()
+    steps = []
     for _ in range(args.steps):
-        _, cores, _, dt = oracle_depthwise_sample(16, max_seconds=0.0)
-        steps.append(dt)
+        t0 = time.perf_counter()
+        run()
+        steps.append(time.perf_counter() - t0)
     dt = float(np.mean(steps)) if steps else float("nan")
-    v = 5 * 4 * 16 * 128 * 512 / dt / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+    v = units / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": wl.unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl.describe(),
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": "1 image x 16 of 256 channels of the (7,256,128,512) batch per step"},
-            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": v, "unit": wl.unit, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": desc + " per step"},
+            "e2e": {"value": v, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_peaks(args):
+    """--workload peaks: the measured ceilings the rooflines are read against.
+    FP32 FMA loops (two loop-invariant operands, packed f32x2 pairs, three
+    distinct registers), the depthwise stencil and weight-gradient correlation
+    with their tiles in shared memory, and tcgen05 MMA loops (kind::tf32,
+    kind::f16 bf16) -- each the best of 5 CUDA-event timed launches after one
+    warm-up, with the SM clock sampled meanwhile."""
+    import ctypes as C
+    import torch
+    from spatially_sharded_cnn_gb300 import build
+    build.build()
+    lib = C.CDLL(build.PEAKS_LIB)
+    lib.hcp_out_floats.restype = C.c_longlong
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty(int(lib.hcp_out_floats()), device=dev)
+    src = torch.rand(64, device=dev) * 0.5 + 0.25
+    w = torch.randn(128 * 49, device=dev) * 0.02
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    P = lambda t: C.c_void_p(t.data_ptr())
+    S = C.c_void_p(st.cuda_stream)
+
+    def best(launch):
+        fl = C.c_double(0)
+        assert launch(C.byref(fl)) == 0
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            assert launch(C.byref(fl)) == 0
+            e1.record(st)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return fl.value / (min(ms) * 1e-3) / 1e12, min(ms)
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    res = {}
+    for kind, name in ((0, "ffma_two_invariant_operands"), (1, "ffma2_packed_pairs"), (2, "ffma_three_registers")):
+        tf, ms = best(lambda fl: lib.hcp_fp32_loop(kind, 4000, 8, P(out), P(src), S, fl))
+        res[name] = {"tflops": tf, "ms": ms}
+    for kind, name in ((0, "depthwise7x7_stencil_smem"), (1, "depthwise7x7_weight_correlation_smem")):
+        tf, ms = best(lambda fl: lib.hcp_stencil(kind, 1000, P(w), P(out), S, fl))
+        res[name] = {"tflops": tf, "ms": ms}
+    for kind, name in ((0, "tcgen05_tf32_m128n256k8"), (1, "tcgen05_bf16_m128n256k16")):
+        tf, ms = best(lambda fl: lib.hcp_mma(kind, 20000, C.cast(P(status), C.POINTER(C.c_int)), S, fl))
+        res[name] = {"tflops": tf, "ms": ms}
+    clk = clocks.stop()
+    if int(status.item()):
+        raise SystemExit("an MMA loop CTA gave up waiting for its MMAs")
+    peaks = load_peaks()
+    line = {"workload": "peaks", "sms": sms, "unit": "TFLOP/s", "results": res,
+            "fp32_derived_peak": alu_peak(peaks, sms), "clocks": clk,
+            "note": "FP32 derived peak = SMs x 128 lanes x 2 x max SM clock; tensor rates per MMA loop of one CTA "
+                    "per SM (M 128, N 256, operands zero, from shared memory)"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -659,7 +873,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=WORKLOADS, default="dw7")
+    ap.add_argument("--workload", choices=WORKLOADS + ["peaks"], default="dw7")
     ap.add_argument("--shards-h", type=int, default=1,
                     help="single-conv workloads: also split the rows into this many shards")
     ap.add_argument("--drop-path", type=float, default=0.0,
@@ -669,6 +883,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="batch size of every workload but config1 (default 7)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.workload == "peaks":
+        return run_peaks(args)
     if args.impl == "reference":
         return run_reference(args)
     wl = make_workload(args.workload, args.batch, args.drop_path, args.shards_h)
@@ -724,12 +940,22 @@ def main():
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     n0 = hc.hc_launch_count()
+    trace = graph is None and args.workload != "config1"  # config1's few-microsecond kernels: no per-launch events
+    if trace:
+        hc.hc_trace_collect()  # drop anything recorded before
+        hc.hc_trace_enable(True)
     start.record(stream)
     for _ in range(K):
         step()
     end.record(stream)
     barrier()
     R.mark = None
+    ktable = None
+    if trace:
+        hc.hc_trace_enable(False)
+        st_tr, tr = hc.hc_trace_collect()
+        hc.check(st_tr, "trace collect")
+        ktable = kernel_table(tr, K)
     launches = hc.hc_launch_count() - n0 + K * graph_kernels  # a replay runs the captured kernels
     clk = clocks.stop()
     hc.check(hc.hc_sync_check(stream), "timed region")
@@ -805,6 +1031,11 @@ def main():
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roof = wl.roofline(ops_ms, peaks, sms)
+    k_roofs = None
+    if ktable is not None and hasattr(wl, "kernel_work"):
+        k_roofs = kernel_rooflines(ktable, wl.kernel_work(), peaks, sms)
+        if roof is None and k_roofs:  # the dominant kernel: the largest device time per step
+            roof = dict(max(k_roofs.values(), key=lambda r: r["ms_per_launch"] * r["launches_per_step"]))
     op_roofs = op_rooflines(ops_ms, wl.op_work(), peaks, sms) if hasattr(wl, "op_work") else None
     if world > 1:
         dist.barrier()
@@ -822,11 +1053,17 @@ def main():
                 "gpu_launches": launches, "roofline": roof, "clocks": clk}
         if op_roofs:
             line["ops_roofline"] = op_roofs
+        if ktable is not None:
+            line["kernels"] = ktable
+            line["kernels_note"] = ("device time per kernel from CUDA events the library records on the launch "
+                                    "stream around every launch (hc_trace_enable) during the timed region")
+        if k_roofs:
+            line["kernels_roofline"] = k_roofs
         if graph is not None:
             line["config"]["cuda_graph"] = f"each step one graph replay of {graph_kernels} kernels"
-        if world == 1 and not args.no_cpu_baseline and args.workload == "dw7" and not args.batch:
-            v, cores, sample, _ = oracle_depthwise_sample(256)
-            line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, sample, _ = oracle_sample(wl, max_seconds=20.0)
+            line["cpu_baseline"] = {"value": v, "unit": wl.unit, "cores": cores, "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
