@@ -242,6 +242,80 @@ hc_status hc_conv2d_bwd_act(const hc_conv_desc* d, const float* x, const float* 
  * leaves its unused trailing rows / columns zero.  A pure copy (bit-exact). */
 hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, void* stream);
 
+/* ---- One rank of a multi-device Shard(3) layout ----------------------------
+ * The pages' design puts each column block on its own device, which receives
+ * its halo columns from the neighbouring devices (NVIDIA blog, design section
+ * and Figure 1; kwkr.cn 2.2: halo exchange, concat, local conv, crop) and may
+ * compute the region away from the block edges while the halo is in flight
+ * (kwkr.cn 5.2).  A rank keeps its block of Wl = W / num_shards columns in the
+ * halo-padded layout x_pad [N][C][H][Wl + 2 * HC_HALO_COLS]: its own columns at
+ * [HC_HALO_COLS, HC_HALO_COLS + Wl), the HC_HALO_COLS columns left of them
+ * holding the left neighbour's last columns and those right of them the right
+ * neighbour's first columns (zeros past the image edge), so the pages' concat
+ * is the layout itself.  A halo exchange moves HC_HALO_COLS columns each way:
+ * hc_halo_pack on the sender, the caller's transport (NCCL send / recv, a peer
+ * copy), hc_halo_unpack on the receiver.  Every call takes the GLOBAL desc d
+ * (W the full width, num_shards the number of ranks); the work is one block's.
+ * Tensors: fp32, device memory, 16-byte aligned; x_pad rows are Wl + 8 floats. */
+#define HC_HALO_COLS 4
+
+/* Column tiles of one rank's block that a call computes (128-column tiles,
+ * T = Wl / 128 of them). */
+typedef enum {
+    HC_TILES_ALL = 0,       /* every tile                                          */
+    HC_TILES_INTERIOR = 1,  /* tiles 1 .. T-2: they read no halo column            */
+    HC_TILES_EDGE = 2       /* tiles 0 and T-1: they read the halo columns         */
+} hc_tiles;
+
+/* x_pad's own columns from the rank's block x_local [N][C][H][Wl]; both margins
+ * zeroed.  HC_ERR_INVALID_ARG for null or misaligned pointers or Wl % 4 != 0. */
+hc_status hc_halo_pad(const hc_conv_desc* d, const float* x_local, float* x_pad, void* stream);
+
+/* The HC_HALO_COLS edge columns of x_pad's own block that a neighbour needs,
+ * packed as buf [N*C*H][HC_HALO_COLS]: side 0 the first ones (the left
+ * neighbour's right margin), side 1 the last ones (the right neighbour's left
+ * margin).  A pure copy. */
+hc_status hc_halo_pack(const hc_conv_desc* d, const float* x_pad, int side, float* buf, void* stream);
+
+/* A packed halo (hc_halo_pack of the neighbour) into x_pad's margin: side 0
+ * the left margin, side 1 the right one; buf NULL writes zeros (the image
+ * edge).  A pure copy. */
+hc_status hc_halo_unpack(const hc_conv_desc* d, const float* buf, int side, float* x_pad, void* stream);
+
+/* Forward of one rank: y [N][C][H][Wl], its block's output columns, from x_pad
+ * whose margins hold the exchanged halo.  tiles selects the column tiles: an
+ * HC_TILES_INTERIOR call reads only the block's own columns, so it may run
+ * while the halo is in flight, and an HC_TILES_EDGE call after it completes
+ * the output (bit-identical to one HC_TILES_ALL call).  Depthwise
+ * convolutions (groups = C_in = C_out, K in {3, 5, 7}, stride 1, padding
+ * (K-1)/2 <= HC_HALO_COLS) with Wl a multiple of 128 and no row shards;
+ * HC_ERR_UNSUPPORTED otherwise. */
+hc_status hc_conv2d_fwd_rank(const hc_conv_desc* d, const float* x_pad, const float* w, const float* bias, float* y,
+                             hc_tiles tiles, void* stream);
+
+/* Workspace bytes of hc_conv2d_bwd_rank (the per-tile weight-gradient partials). */
+hc_status hc_conv2d_workspace_size_rank(const hc_conv_desc* d, size_t* bytes);
+
+/* Backward of one rank (the pages' backward on one device): gy_pad is
+ * grad_output in the halo-padded layout, its margins exchanged like x's (the
+ * zero-pad + exchange of grad_output, kwkr.cn 2.2).  Outputs (each nullable):
+ * gx [N][C][H][Wl] the block's grad_input; gw_part [C][1][K][K] and gb_part
+ * [C] this rank's _Partial grad_weight / grad_bias, which summed over the
+ * ranks in rank order (hc_sum_partials) give the full gradients.  An
+ * HC_TILES_INTERIOR call followed by an HC_TILES_EDGE call on the same
+ * workspace computes what one HC_TILES_ALL call does (grad_input
+ * bit-identical; the weight gradient's tile sums may split differently across
+ * blocks, within rounding); the call covering the edge tiles (ALL or EDGE) also
+ * reduces the partials.  Same support as hc_conv2d_fwd_rank. */
+hc_status hc_conv2d_bwd_rank(const hc_conv_desc* d, const float* x_pad, const float* w, const float* gy_pad,
+                             float* gx, float* gw_part, float* gb_part, void* ws, size_t ws_bytes, hc_tiles tiles,
+                             void* stream);
+
+/* out[k] = sum_{r < count} parts[r * n + k] with r ascending: the ranks'
+ * gathered _Partial gradients summed in rank order, the deterministic form of
+ * the pages' all-reduce (NVIDIA blog, design section). */
+hc_status hc_sum_partials(const float* parts, int count, long long n, float* out, void* stream);
+
 /* Depthwise backward that allocates nothing.  The pages have no counterpart:
  * this entry point exists for callers that may not allocate device memory at
  * the point of the call -- for example code running under another framework's

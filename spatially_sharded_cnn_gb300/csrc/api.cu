@@ -263,6 +263,29 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     return HC_OK;
 }
 
+// ---- one rank of a multi-device layout ------------------------------------
+// The rank-local desc: one column block of the global desc, no shards of its
+// own.  Returns HC_ERR_UNSUPPORTED unless the depthwise kernels cover it and
+// its halo fits the HC_HALO_COLS margins.
+static hc_status rank_local(const hc_conv_desc* d, hc_conv_desc* loc, Plan* p) {
+    hc_status st = make_plan(d, p);  // validates the global split
+    if (st) return st;
+    if (p->Sh > 1 || d->stride != 1 || d->padding > kHaloCols) return HC_ERR_UNSUPPORTED;
+    *loc = *d;
+    loc->W = d->W / d->num_shards;
+    loc->num_shards = 1;
+    loc->num_shards_h = 1;
+    if ((st = make_plan(loc, p))) return st;
+    return depthwise_supported(loc, *p) ? HC_OK : HC_ERR_UNSUPPORTED;
+}
+
+static hc_status halo_layout_args(const hc_conv_desc* d, int* Wl) {
+    if (!d || d->N <= 0 || d->C_in <= 0 || d->H <= 0 || d->W <= 0 || d->num_shards <= 0 || d->W % d->num_shards)
+        return HC_ERR_INVALID_ARG;
+    *Wl = d->W / d->num_shards;
+    return *Wl % 4 ? HC_ERR_INVALID_ARG : HC_OK;
+}
+
 }  // namespace hc
 
 using namespace hc;
@@ -363,6 +386,95 @@ hc_status hc_halo_gather(const hc_conv_desc* d, const float* x, float* x_ext, vo
     if (p.S > kMaxKernelShards || p.Sh > kMaxKernelShards) return HC_ERR_UNSUPPORTED;
     traced_begin((cudaStream_t)stream);
     return launch_halo_gather(d, p, x, x_ext, (cudaStream_t)stream);
+}
+
+
+hc_status hc_halo_pad(const hc_conv_desc* d, const float* x_local, float* x_pad, void* stream) {
+    int Wl;
+    hc_status st = halo_layout_args(d, &Wl);
+    if (st) return st;
+    if (!x_local || !x_pad || !aligned16(x_local) || !aligned16(x_pad)) return HC_ERR_INVALID_ARG;
+    traced_begin((cudaStream_t)stream);
+    return launch_halo_pad(d, Wl, x_local, x_pad, (cudaStream_t)stream);
+}
+
+hc_status hc_halo_pack(const hc_conv_desc* d, const float* x_pad, int side, float* buf, void* stream) {
+    int Wl;
+    hc_status st = halo_layout_args(d, &Wl);
+    if (st) return st;
+    if (!x_pad || !buf || (side != 0 && side != 1) || !aligned16(x_pad) || !aligned16(buf) || Wl < kHaloCols)
+        return HC_ERR_INVALID_ARG;
+    traced_begin((cudaStream_t)stream);
+    return launch_halo_pack(d, Wl, x_pad, side, buf, (cudaStream_t)stream);
+}
+
+hc_status hc_halo_unpack(const hc_conv_desc* d, const float* buf, int side, float* x_pad, void* stream) {
+    int Wl;
+    hc_status st = halo_layout_args(d, &Wl);
+    if (st) return st;
+    if (!x_pad || (side != 0 && side != 1) || !aligned16(x_pad) || (buf && !aligned16(buf)))
+        return HC_ERR_INVALID_ARG;
+    traced_begin((cudaStream_t)stream);
+    return launch_halo_unpack(d, Wl, buf, side, x_pad, (cudaStream_t)stream);
+}
+
+hc_status hc_conv2d_fwd_rank(const hc_conv_desc* d, const float* x_pad, const float* w, const float* bias, float* y,
+                             hc_tiles tiles, void* stream) {
+    static thread_local Plan p;
+    hc_conv_desc loc;
+    hc_status st = rank_local(d, &loc, &p);
+    if (st) return st;
+    if (!x_pad || !w || !y || !aligned16(x_pad) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        tiles < HC_TILES_ALL || tiles > HC_TILES_EDGE)
+        return HC_ERR_INVALID_ARG;
+    DwLayout lay;
+    lay.pitch = loc.W + 2 * kHaloCols;
+    lay.xo = kHaloCols;
+    lay.tiles = tiles;
+    traced_begin((cudaStream_t)stream);
+    return launch_depthwise_fwd(&loc, p, x_pad, w, bias, y, (cudaStream_t)stream, lay);
+}
+
+hc_status hc_conv2d_workspace_size_rank(const hc_conv_desc* d, size_t* bytes) {
+    if (!bytes) return HC_ERR_INVALID_ARG;
+    static thread_local Plan p;
+    hc_conv_desc loc;
+    hc_status st = rank_local(d, &loc, &p);
+    if (st) return st;
+    *bytes = sizeof(float) * depthwise_bwd_ws_floats(&loc, p);
+    return HC_OK;
+}
+
+hc_status hc_conv2d_bwd_rank(const hc_conv_desc* d, const float* x_pad, const float* w, const float* gy_pad,
+                             float* gx, float* gw_part, float* gb_part, void* ws, size_t ws_bytes, hc_tiles tiles,
+                             void* stream) {
+    static thread_local Plan p;
+    hc_conv_desc loc;
+    hc_status st = rank_local(d, &loc, &p);
+    if (st) return st;
+    if (!x_pad || !w || !gy_pad || !aligned16(x_pad) || !aligned16(w) || !aligned16(gy_pad) ||
+        tiles < HC_TILES_ALL || tiles > HC_TILES_EDGE)
+        return HC_ERR_INVALID_ARG;
+    for (const void* q : {(const void*)gx, (const void*)gw_part, (const void*)gb_part})
+        if (q && !aligned16(q)) return HC_ERR_INVALID_ARG;
+    const bool want_wb = gw_part || gb_part;
+    const size_t need = sizeof(float) * depthwise_bwd_ws_floats(&loc, p);
+    if (want_wb && (ws_bytes < need || !ws || ((uintptr_t)ws & 15))) return HC_ERR_WORKSPACE;
+    DwLayout lay;
+    lay.pitch = loc.W + 2 * kHaloCols;
+    lay.xo = kHaloCols;
+    lay.tiles = tiles;
+    lay.partials = tiles != HC_TILES_INTERIOR;
+    traced_begin((cudaStream_t)stream);
+    // one shard: its partials are the rank's _Partial gradients
+    return launch_depthwise_bwd(&loc, p, x_pad, w, gy_pad, gx, (float*)ws, gw_part, gb_part, want_wb,
+                                (cudaStream_t)stream, nullptr, nullptr, nullptr, lay);
+}
+
+hc_status hc_sum_partials(const float* parts, int count, long long n, float* out, void* stream) {
+    if (!parts || !out || count <= 0 || n <= 0) return HC_ERR_INVALID_ARG;
+    traced_begin((cudaStream_t)stream);
+    return launch_sum_rows(parts, out, count, n, (cudaStream_t)stream);
 }
 
 hc_status hc_sync_check(void* stream) {

@@ -146,15 +146,31 @@ hc_status launch_direct_partials(const hc_conv_desc* d, const Plan& p, const flo
 // depthwise K x K, stride 1, padding (K-1)/2, 128-column tiles inside a shard
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p);
 size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p);
+// Where a depthwise launch reads x (and grad_output) and which column tiles it
+// covers.  pitch: floats per row of those tensors (0: W), xo: the column of a
+// row where the block's column 0 sits (the halo-padded layout of one rank:
+// pitch W + 2 * kHaloCols, xo = kHaloCols).  tiles: HC_TILES_ALL, _INTERIOR
+// (column tiles 1 .. T-2, which read no margin column) or _EDGE (0 and T-1).
+// partials (backward): reduce the tile partials to shard partials after the
+// launch (the last launch of a split backward).
+constexpr int kHaloCols = 4;
+struct DwLayout {
+    int pitch = 0, xo = 0, tiles = HC_TILES_ALL;
+    bool partials = true;
+};
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
-                               const float* b, float* y, cudaStream_t st);
+                               const float* b, float* y, cudaStream_t st, const DwLayout& lay = DwLayout());
 // tile partials go to ws; then reduced to shard partials gwp / gbp ([S][C][K*K], [S][C])
 // gres (nullable, only with gx): added to grad_input in its epilogue (a residual gradient);
 // gw / gb (nullable): the full gradients, the shard partials summed in shard order
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
                                bool want_weight_grads, cudaStream_t st, const float* gres = nullptr,
-                               float* gw = nullptr, float* gb = nullptr);
+                               float* gw = nullptr, float* gb = nullptr, const DwLayout& lay = DwLayout());
+// the halo-padded layout of one rank (hc_halo_pad / _pack / _unpack)
+hc_status launch_halo_pad(const hc_conv_desc* d, int Wl, const float* x, float* xp, cudaStream_t st);
+hc_status launch_halo_pack(const hc_conv_desc* d, int Wl, const float* xp, int side, float* buf, cudaStream_t st);
+hc_status launch_halo_unpack(const hc_conv_desc* d, int Wl, const float* buf, int side, float* xp, cudaStream_t st);
 
 // dense conv on tcgen05 (3xTF32 implicit GEMM): groups 1, stride 1, odd k,
 // padding (k-1)/2, C_in and C_out multiples of 128

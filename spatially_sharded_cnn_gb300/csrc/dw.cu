@@ -187,6 +187,13 @@ __device__ __forceinline__ void correlate_4x4(const float* sm, int row0, int lan
 struct Sched {
     int N, C, H, W, col_tiles, items;
     int tile_fastest;  // 1: items ordered (c, n, column tile); 0: (c, column tile, n)
+    // The column tiles the items cover: tile k (0 <= k < col_tiles) is column tile
+    // ct_base + k * ct_step of the output (all of them: 0, 1; a rank's interior or
+    // edge tiles: see the rank entry points).  xo: the column of the x (and
+    // grad_output) tensor maps where the block's column 0 sits (4 in the
+    // halo-padded layout, else 0).
+    int ct_base, ct_step, xo;
+    __device__ __forceinline__ int col(int k) const { return ct_base + k * ct_step; }
     __device__ __forceinline__ void decode(int item, int& n, int& c, int& ct) const {
         if (tile_fastest) {
             ct = item % col_tiles;
@@ -254,7 +261,8 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
         sc.decode(i0 + q / ntiles, n, c, ct);
         uint64_t* bar = full + (q % NSTAGE);
         mbar_expect_tx(bar, G::BYTES);
-        tma_load_3d(tiles + (q % NSTAGE) * G::TILE, &xmap, ct * TW - 4, (q % ntiles) * TH - P, n * sc.C + c, bar);
+        tma_load_3d(tiles + (q % NSTAGE) * G::TILE, &xmap, sc.xo + sc.col(ct) * TW - 4, (q % ntiles) * TH - P,
+                    n * sc.C + c, bar);
     };
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; s++) {
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
                 }
             }
         }
-        float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+        float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + sc.col(ct) * TW + 4 * lane;
 #pragma unroll
         for (int r = 0; r < 8; r++) {
             const int h = t * TH + warp * 8 + r;
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         uint64_t* bar = full + (q % NSTAGE);
         float* st = tiles + (q % NSTAGE) * 2 * G::TILE;
         mbar_expect_tx(bar, want_wb ? 2 * G::BYTES : G::BYTES);
-        const int x0 = ct * TW - 4, y0 = t * TH - P, z = n * sc.C + c;
+        const int x0 = sc.xo + sc.col(ct) * TW - 4, y0 = t * TH - P, z = n * sc.C + c;
         tma_load_3d(st, &gymap, x0, y0, z, bar);
         if (want_wb) tma_load_3d(st + G::TILE, &xmap, x0, y0, z, bar);
     };
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             [&](int s, int n, int c, int ct, int t, bool) {
                 if (!a.gx) return;
                 const float* gys = tiles + s * 2 * G::TILE;
-                const long long off = ((long long)(n * sc.C + c) * sc.H) * sc.W + ct * TW + 4 * lane;
+                const long long off = ((long long)(n * sc.C + c) * sc.H) * sc.W + sc.col(ct) * TW + 4 * lane;
                 float* gp = a.gx + off;
 #pragma unroll 1
                 for (int half = 0; half < 2; half++) {
@@ -569,7 +577,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                      float tot = 0.0f;
 #pragma unroll
                      for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + wtid];
-                     const int r = ct / a.tiles_per_shard, tt = ct - r * a.tiles_per_shard;
+                     const int r = sc.col(ct) / a.tiles_per_shard, tt = sc.col(ct) - r * a.tiles_per_shard;
                      const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
                      float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
                      for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + wtid] = m == run_n0 ? tot : 0.0f;
@@ -614,17 +622,27 @@ __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, fl
 }
 
 
-// Tensor map of an NCHW fp32 tensor viewed as [N*C][H][W], box = one staged tile.
+// Tensor map of an NCHW fp32 tensor viewed as [N*C][H][pitch] (pitch 0: W),
+// box = one staged tile.
 template <int K, int WARPS>
-hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d) {
-    const uint64_t dims[3] = {(uint64_t)d->W, (uint64_t)d->H, (uint64_t)d->N * d->C_in};
-    const uint64_t strides[2] = {(uint64_t)d->W * 4, (uint64_t)d->H * d->W * 4};
+hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d, int pitch) {
+    const uint64_t wp = pitch > 0 ? (uint64_t)pitch : (uint64_t)d->W;
+    const uint64_t dims[3] = {wp, (uint64_t)d->H, (uint64_t)d->N * d->C_in};
+    const uint64_t strides[2] = {wp * 4, (uint64_t)d->H * wp * 4};
     const uint32_t box[3] = {(uint32_t)SMW, (uint32_t)Geo<K, WARPS>::R, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm) {
-    Sched sc{d->N, d->C_in, d->H, d->W, d->W / TW, 0, tile_fastest};
+Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm, const DwLayout& lay) {
+    const int T = d->W / TW;
+    Sched sc{d->N, d->C_in, d->H, d->W, T, 0, tile_fastest, 0, 1, lay.xo};
+    if (lay.tiles == HC_TILES_INTERIOR) {
+        sc.ct_base = 1;
+        sc.col_tiles = T > 2 ? T - 2 : 0;
+    } else if (lay.tiles == HC_TILES_EDGE) {
+        sc.ct_step = T > 1 ? T - 1 : 1;
+        sc.col_tiles = T > 1 ? 2 : 1;
+    }
     sc.items = d->N * d->C_in * sc.col_tiles;
     const int g = device_sm_count() * ctas_per_sm;
     *grid = g < sc.items ? g : sc.items;
@@ -632,13 +650,15 @@ Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_
 }
 
 template <int K>
-hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const float* b, float* y, cudaStream_t st) {
+hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const float* b, float* y, cudaStream_t st,
+                const DwLayout& lay) {
     using G = Geo<K, FWD_WARPS>;
     CUtensorMap xm;
-    hc_status s = plane_map<K, FWD_WARPS>(&xm, x, d);
+    hc_status s = plane_map<K, FWD_WARPS>(&xm, x, d, lay.pitch);
     if (s) return s;
     int grid;
-    const Sched sc = sched_of(d, &grid, 1, FWD_CTAS);  // horizontal neighbours back to back: their halos hit L2
+    const Sched sc = sched_of(d, &grid, 1, FWD_CTAS, lay);  // horizontal neighbours back to back: their halos hit L2
+    if (sc.items == 0) return HC_OK;
     const size_t smem = sizeof(float) * NSTAGE * G::TILE + NSTAGE * sizeof(uint64_t) + (NSTAGE + 2) * sizeof(int);
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
@@ -652,14 +672,14 @@ hc_status fwd_k(const hc_conv_desc* d, const float* x, const float* w, const flo
 template <int K>
 hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy, float* gx,
                 const float* gres, float* tile_part, float* gwp, float* gbp, float* gw, float* gb, bool want_wb,
-                cudaStream_t st) {
+                cudaStream_t st, const DwLayout& lay) {
     using G = Geo<K, BWD_WARPS>;
     if (!gx && !want_wb) return HC_OK;
     CUtensorMap gm, xm;
-    hc_status s = plane_map<K, BWD_WARPS>(&gm, gy, d);
-    if (s || (s = plane_map<K, BWD_WARPS>(&xm, x, d))) return s;
+    hc_status s = plane_map<K, BWD_WARPS>(&gm, gy, d, lay.pitch);
+    if (s || (s = plane_map<K, BWD_WARPS>(&xm, x, d, lay.pitch))) return s;
     int grid;
-    const Sched sc = sched_of(d, &grid, 0, 1);  // runs of one (c, column tile): gw stays in registers
+    const Sched sc = sched_of(d, &grid, 0, 1, lay);  // runs of one (c, column tile): gw stays in registers
     const int tps = p.Wl / TW;
     const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static std::atomic<unsigned long long> attr{0};
@@ -672,7 +692,9 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     });
     BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
     const dim3 grd(grid), blk(2 * BWD_WARPS * 32);
-    if (a.gres) {
+    if (sc.items == 0) {
+        s = HC_OK;
+    } else if (a.gres) {
         if (p.Sh > 1)
             dw_bwd_kernel<K, true, true><<<grd, blk, smem, st>>>(gm, xm, a, sc);
         else
@@ -682,8 +704,8 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     } else {
         dw_bwd_kernel<K, false, false><<<grd, blk, smem, st>>>(gm, xm, a, sc);
     }
-    s = launched("dw_bwd_kernel", st);
-    if (s || !want_wb) return s;
+    if (sc.items) s = launched("dw_bwd_kernel", st);
+    if (s || !want_wb || !lay.partials) return s;
     const long long total = (long long)d->C_in * (K * K + 1);
     dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, gw, gb, p.Q,
                                                                              d->C_in, tps * d->N, K * K);
@@ -708,23 +730,24 @@ size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p) {
 }
 
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
-                               const float* b, float* y, cudaStream_t st) {
+                               const float* b, float* y, cudaStream_t st, const DwLayout& lay) {
     (void)p;
     switch (d->kh) {
-        case 3: return fwd_k<3>(d, x, w, b, y, st);
-        case 5: return fwd_k<5>(d, x, w, b, y, st);
-        case 7: return fwd_k<7>(d, x, w, b, y, st);
+        case 3: return fwd_k<3>(d, x, w, b, y, st, lay);
+        case 5: return fwd_k<5>(d, x, w, b, y, st, lay);
+        case 7: return fwd_k<7>(d, x, w, b, y, st, lay);
     }
     return HC_ERR_UNSUPPORTED;
 }
 
 hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,
                                const float* gy, float* gx, float* tile_part, float* gwp, float* gbp,
-                               bool want_weight_grads, cudaStream_t st, const float* gres, float* gw, float* gb) {
+                               bool want_weight_grads, cudaStream_t st, const float* gres, float* gw, float* gb,
+                               const DwLayout& lay) {
     switch (d->kh) {
-        case 3: return bwd_k<3>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
-        case 5: return bwd_k<5>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
-        case 7: return bwd_k<7>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st);
+        case 3: return bwd_k<3>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st, lay);
+        case 5: return bwd_k<5>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st, lay);
+        case 7: return bwd_k<7>(d, p, x, w, gy, gx, gres, tile_part, gwp, gbp, gw, gb, want_weight_grads, st, lay);
     }
     return HC_ERR_UNSUPPORTED;
 }

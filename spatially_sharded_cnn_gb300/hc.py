@@ -24,6 +24,8 @@ _lib = C.CDLL(LIB_PATH)
 HC_OK, HC_ERR_INVALID_ARG, HC_ERR_UNSUPPORTED, HC_ERR_WORKSPACE, HC_ERR_CUDA, HC_ERR_TIMEOUT = range(6)
 HC_ALGO_AUTO, HC_ALGO_DIRECT, HC_ALGO_DEPTHWISE, HC_ALGO_TC_3XTF32, HC_ALGO_TC_BF16X6 = range(5)
 HC_ACT_NONE, HC_ACT_GELU_INPUT, HC_ACT_GELU_OUTPUT = range(3)
+HC_TILES_ALL, HC_TILES_INTERIOR, HC_TILES_EDGE = range(3)
+HC_HALO_COLS = 4
 
 
 class hc_conv_desc(C.Structure):
@@ -129,6 +131,8 @@ EXPORTS = [
     "hc_conv2d_step_graph_create", "hc_step_graph_launch", "hc_step_graph_destroy", "hc_drop_path_mask",
     "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
     "hc_conv2d_fwd_act", "hc_conv2d_bwd_act", "hc_conv2d_bwd_residual", "hc_trace_enable", "hc_trace_collect",
+    "hc_halo_pad", "hc_halo_pack", "hc_halo_unpack", "hc_conv2d_fwd_rank", "hc_conv2d_bwd_rank",
+    "hc_conv2d_workspace_size_rank", "hc_sum_partials",
 ]
 
 
@@ -312,6 +316,49 @@ def hc_sync_check(stream=None) -> int:
 
 def hc_launch_count() -> int:
     return int(_lib.hc_launch_count())
+
+
+# ---- one rank of a multi-device layout (halo-padded blocks) -----------------
+for _n, _a in (("hc_halo_pad", [_D, _P, _P, _P]), ("hc_halo_pack", [_D, _P, C.c_int, _P, _P]),
+               ("hc_halo_unpack", [_D, _P, C.c_int, _P, _P]),
+               ("hc_conv2d_fwd_rank", [_D, _P, _P, _P, _P, C.c_int, _P]),
+               ("hc_conv2d_bwd_rank", [_D, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, C.c_int, _P]),
+               ("hc_conv2d_workspace_size_rank", [_D, C.POINTER(C.c_size_t)]),
+               ("hc_sum_partials", [_P, C.c_int, C.c_longlong, _P, _P])):
+    getattr(_lib, _n).argtypes = _a
+    getattr(_lib, _n).restype = C.c_int
+
+
+def hc_halo_pad(d, x_local, x_pad, stream=None) -> int:
+    return _lib.hc_halo_pad(C.byref(d), _ptr(x_local), _ptr(x_pad), _stream(stream))
+
+
+def hc_halo_pack(d, x_pad, side, buf, stream=None) -> int:
+    return _lib.hc_halo_pack(C.byref(d), _ptr(x_pad), int(side), _ptr(buf), _stream(stream))
+
+
+def hc_halo_unpack(d, buf, side, x_pad, stream=None) -> int:
+    return _lib.hc_halo_unpack(C.byref(d), _ptr(buf), int(side), _ptr(x_pad), _stream(stream))
+
+
+def hc_conv2d_fwd_rank(d, x_pad, w, bias, y, tiles=HC_TILES_ALL, stream=None) -> int:
+    return _lib.hc_conv2d_fwd_rank(C.byref(d), _ptr(x_pad), _ptr(w), _ptr(bias), _ptr(y), int(tiles), _stream(stream))
+
+
+def hc_conv2d_workspace_size_rank(d):
+    n = C.c_size_t(0)
+    st = _lib.hc_conv2d_workspace_size_rank(C.byref(d), C.byref(n))
+    return st, n.value
+
+
+def hc_conv2d_bwd_rank(d, x_pad, w, gy_pad, gx, gw_part, gb_part, ws=None, ws_bytes=0, tiles=HC_TILES_ALL,
+                       stream=None) -> int:
+    return _lib.hc_conv2d_bwd_rank(C.byref(d), _ptr(x_pad), _ptr(w), _ptr(gy_pad), _ptr(gx), _ptr(gw_part),
+                                   _ptr(gb_part), _ptr(ws), int(ws_bytes), int(tiles), _stream(stream))
+
+
+def hc_sum_partials(parts, count, n, out, stream=None) -> int:
+    return _lib.hc_sum_partials(_ptr(parts), int(count), int(n), _ptr(out), _stream(stream))
 
 
 class hc_trace_entry(C.Structure):

@@ -206,3 +206,73 @@ def test_halo_fault_is_detected(fault):
     out = _run(P.cfg_of(1, 2, 4, 16, 2, 5, 1, 2, 1), fault=fault)
     # rank 1 dropped (or duplicated) the halo it owes rank 0: rank 0 must notice
     assert out[0][0] == "halo_error", out[0]
+
+
+# ---- the library's rank path (spatially_sharded_cnn_gb300.exchange) on CPU ranks ----
+def _exchange_worker(rank, world, port, cfg, q):
+    """One rank of RankHalo on host tensors: pad, exchange x's and grad_output's
+    margins, then the local conv on the exchanged block (the oracle standing in
+    for the device kernels) and the rank-order reduction of the partials."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=30))
+    try:
+        import oracle
+        from spatially_sharded_cnn_gb300.exchange import HALO, RankHalo, padded_shape
+        orc = oracle.load()
+        cfg = dict(cfg, num_shards=world)
+        x, w, b, gy = P.rand_case(cfg, 91)
+        ex = RankHalo(cfg)
+        Wl = ex.Wl
+        pads = {}
+        for name, t in (("x", x), ("gy", gy)):
+            tp = torch.full(padded_shape(cfg), float("nan"))
+            tp[..., HALO:HALO + Wl] = torch.from_numpy(np.ascontiguousarray(t[..., rank * Wl:(rank + 1) * Wl]))
+            ex.exchange(tp)
+            pads[name] = tp.numpy()
+        p = cfg["padding"]
+        xe = np.ascontiguousarray(pads["x"][..., HALO - p:HALO + Wl + p])
+        # the local conv on the exchanged block (stride 1, "same"): padding p, then the crop
+        lcfg = dict(cfg, W=Wl + 2 * p, num_shards=1)
+        y_own = orc.conv2d_fwd(lcfg, xe, w, b)[..., p:p + Wl]
+        # this rank's _Partial gradients (the sharded oracle's), reduced across the ranks in rank order
+        _, gwp, gbp = orc.sharded_bwd(cfg, x, w, gy)
+        gw = ex.reduce_partials(torch.from_numpy(gwp[rank].astype(np.float32)))
+        gb = ex.reduce_partials(torch.from_numpy(gbp[rank].astype(np.float32)))
+        q.put((rank, "ok", pads["x"], pads["gy"], y_own, gw.numpy(), gb.numpy()))
+    except Exception as ex_:
+        q.put((rank, "error", repr(ex_), None, None, None, None))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_rank_halo_exchange_on_cpu_ranks(orc, world):
+    cfg = P.cfg_of(2, 3, 6, 8 * world, 3, 7, 1, 3, 3)   # depthwise 7x7, 8 columns per rank
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_exchange_worker, args=(r, world, port, cfg, q)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    out = {}
+    for _ in range(world):
+        item = q.get(timeout=60)
+        out[item[0]] = item[1:]
+    for pr in procs:
+        pr.join(timeout=60)
+    assert all(v[0] == "ok" for v in out.values()), out
+    c = dict(cfg, num_shards=world)
+    x, w, b, gy = P.rand_case(c, 91)
+    Wl, p = 8, 3
+    for r in range(world):
+        # the margins: the neighbours' edge columns (zeros past the image edge), bit for bit
+        assert np.array_equal(out[r][1][..., 4 - p:4 + Wl + p], orc.halo_extend(c, r, x)[..., :Wl + 2 * p]), r
+        assert np.array_equal(out[r][2][..., 4 - p:4 + Wl + p], orc.halo_extend(c, r, gy)[..., :Wl + 2 * p]), r
+    y = orc.conv2d_fwd(c, x, w, b)
+    assert np.abs(np.concatenate([out[r][3] for r in range(world)], axis=-1) - y).max() <= 1e-12
+    gw, gb = orc.conv2d_bwd_weight(c, x, gy), orc.conv2d_bwd_bias(c, gy)
+    for r in range(world):  # every rank holds the same reduced gradient
+        assert np.array_equal(out[r][4], out[0][4]) and np.array_equal(out[r][5], out[0][5])
+        assert np.abs(out[r][4] - gw).max() <= 1e-6 * np.abs(gw).max()
+        assert np.abs(out[r][5] - gb).max() <= 1e-6 * np.abs(gb).max()
