@@ -458,6 +458,16 @@ const char* hc_status_string(hc_status s);
 /* Number of kernels this library has launched since it was loaded. */
 unsigned long long hc_launch_count(void);
 
+/* Reproducibility hook (the pages have no counterpart): the number of SMs the
+ * library sizes its persistent grids and split counts for; 0 (the default)
+ * uses the device's.  Results are bit-identical from call to call for a fixed
+ * count; another count partitions the fixed-order sums differently and may
+ * round differently, within the stated tolerances -- this hook lets a test see
+ * both on one GPU.  Process-wide; set it before querying workspace sizes (the
+ * tensor-core weight-gradient split count, hence its workspace, depends on
+ * it).  HC_ERR_INVALID_ARG for a negative count. */
+hc_status hc_set_sm_count(int sms);
+
 /* Per-kernel device timing (a measurement aid; the pages have no counterpart).
  * hc_trace_enable(1): from then on every launcher records a CUDA event on its
  * stream before its first kernel and one after every kernel, so each kernel's

@@ -8,7 +8,11 @@ namespace hc {
 
 std::atomic<unsigned long long> g_launches{0};
 
+std::atomic<int> g_sm_override{0};  // hc_set_sm_count
+
 int device_sm_count() {
+    const int o = g_sm_override.load(std::memory_order_relaxed);
+    if (o > 0) return o;
     static std::atomic<int> n[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -505,5 +509,11 @@ const char* hc_status_string(hc_status s) {
 }
 
 unsigned long long hc_launch_count(void) { return g_launches.load(); }
+
+hc_status hc_set_sm_count(int sms) {
+    if (sms < 0) return HC_ERR_INVALID_ARG;
+    g_sm_override.store(sms, std::memory_order_relaxed);
+    return HC_OK;
+}
 
 }  // extern "C"

@@ -55,8 +55,10 @@ inline hc_status launched(const char* name, cudaStream_t st) {
 
 inline unsigned cdiv(long long a, long long b) { return (unsigned)((a + b - 1) / b); }
 
-// Streaming multiprocessors of the current device (looked up once per device).
+// Streaming multiprocessors of the current device (looked up once per device),
+// or the count hc_set_sm_count imposes.
 int device_sm_count();
+extern std::atomic<int> g_sm_override;
 
 // Per-device caches (kernel attributes, SM counts, wave sizes, the no-alloc
 // scratch address) hold kMaxDevices entries; a device ordinal at or beyond it

@@ -147,11 +147,11 @@ static long long bias_wave(int variant) {
     static std::atomic<long long> caps[kMaxDevices][3];  // per device; host threads may call at once
     int dev = 0;
     cudaGetDevice(&dev);
-    const bool cached = dev >= 0 && dev < kMaxDevices;
+    // an imposed SM count (hc_set_sm_count) is not cached
+    const bool cached = dev >= 0 && dev < kMaxDevices && g_sm_override.load(std::memory_order_relaxed) == 0;
     long long v = cached ? caps[dev][variant].load(std::memory_order_relaxed) : 0;
     if (!v) {
-        int sms = 0, per = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int sms = device_sm_count(), per = 0;
         if (variant == 2)
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, bias_rows_kernel<true, true>, 256, 0);
         else if (variant == 1)

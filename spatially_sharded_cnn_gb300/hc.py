@@ -132,7 +132,7 @@ EXPORTS = [
     "hc_layerscale_droppath_fwd", "hc_layerscale_droppath_bwd", "hc_shard_plan_rows", "hc_conv2d_bwd_reuse",
     "hc_conv2d_fwd_act", "hc_conv2d_bwd_act", "hc_conv2d_bwd_residual", "hc_trace_enable", "hc_trace_collect",
     "hc_halo_pad", "hc_halo_pack", "hc_halo_unpack", "hc_conv2d_fwd_rank", "hc_conv2d_bwd_rank",
-    "hc_conv2d_workspace_size_rank", "hc_sum_partials",
+    "hc_conv2d_workspace_size_rank", "hc_sum_partials", "hc_set_sm_count",
 ]
 
 
@@ -316,6 +316,14 @@ def hc_sync_check(stream=None) -> int:
 
 def hc_launch_count() -> int:
     return int(_lib.hc_launch_count())
+
+
+_lib.hc_set_sm_count.argtypes = [C.c_int]
+_lib.hc_set_sm_count.restype = C.c_int
+
+
+def hc_set_sm_count(sms: int) -> int:
+    return _lib.hc_set_sm_count(int(sms))
 
 
 # ---- one rank of a multi-device layout (halo-padded blocks) -----------------
