@@ -116,10 +116,12 @@ __device__ void give_up(uint64_t* full, int first_unconsumed, int issued) {
 }
 
 // ---- the stencil ------------------------------------------------------------
-// acc[r][jj] += sum_{u,v} wt[u][v] * tile[row0 + r + u][4*lane + jj + v - P + 4]
-template <int K>
+// acc[r][jj] += sum_{u,v} wt[u][v] * tile[row0 + r + u][4*lane + jj + v - P + 4];
+// done(r) runs as soon as output row r has all its terms (after input row r + K - 1),
+// so a row's store issues while the later rows compute.
+template <int K, typename Done>
 __device__ __forceinline__ void stencil_8x4(const float* sm, int row0, int lane, const float (&wt)[K][K],
-                                            float (&acc)[8][4]) {
+                                            float (&acc)[8][4], Done&& done) {
     constexpr int P = (K - 1) / 2;
 #pragma unroll
     for (int i = 0; i < 8 + 2 * P; i++) {
@@ -136,13 +138,15 @@ __device__ __forceinline__ void stencil_8x4(const float* sm, int row0, int lane,
                     for (int v = 0; v < K; v++) acc[r][jj] = fmaf(wt[u][v], xs[jj + v - P + 4], acc[r][jj]);
             }
         }
+        if (i >= K - 1) done(i - (K - 1));
     }
 }
 
-// Half-block forms used by the backward: rows row0 .. row0+3 of the block.
-template <int K>
+// Half-block forms used by the backward: rows row0 .. row0+3 of the block
+// (done(r) as in stencil_8x4).
+template <int K, typename Done>
 __device__ __forceinline__ void stencil_4x4(const float* sm, int row0, int lane, const float (&wt)[K][K],
-                                            float (&acc)[4][4]) {
+                                            float (&acc)[4][4], Done&& done) {
     constexpr int P = (K - 1) / 2;
 #pragma unroll
     for (int i = 0; i < 4 + 2 * P; i++) {
@@ -159,6 +163,7 @@ __device__ __forceinline__ void stencil_4x4(const float* sm, int row0, int lane,
                     for (int v = 0; v < K; v++) acc[r][jj] = fmaf(wt[u][v], xs[jj + v - P + 4], acc[r][jj]);
             }
         }
+        if (i >= K - 1) done(i - (K - 1));
     }
 }
 
@@ -308,7 +313,13 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
         for (int r = 0; r < 8; r++)
 #pragma unroll
             for (int jj = 0; jj < 4; jj++) acc[r][jj] = bv;
-        stencil_8x4<K>(sm, warp * 8, lane, wt, acc);
+        float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + sc.col(ct) * TW + 4 * lane;
+        stencil_8x4<K>(sm, warp * 8, lane, wt, acc, [&](int r) {
+            const int h = t * TH + warp * 8 + r;
+            if (h < sc.H)
+                *reinterpret_cast<float4*>(yp + (long long)h * sc.W) =
+                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        });
         __syncwarp();  // the warp's reads of the stage are done
         if (lane == 0) {
             __threadfence_block();
@@ -320,14 +331,6 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
                     atomicAdd(issued, 1);
                 }
             }
-        }
-        float* yp = y + ((long long)(n * sc.C + c) * sc.H) * sc.W + sc.col(ct) * TW + 4 * lane;
-#pragma unroll
-        for (int r = 0; r < 8; r++) {
-            const int h = t * TH + warp * 8 + r;
-            if (h < sc.H)
-                *reinterpret_cast<float4*>(yp + (long long)h * sc.W) =
-                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
         if (++s == NSTAGE) {
             s = 0;
@@ -510,16 +513,14 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                     for (int r = 0; r < 4; r++)
 #pragma unroll
                         for (int jj = 0; jj < 4; jj++) acc[r][jj] = 0.0f;
-                    stencil_4x4<K>(gys, row0, lane, wf, acc);
-#pragma unroll
-                    for (int r = 0; r < 4; r++) {
+                    stencil_4x4<K>(gys, row0, lane, wf, acc, [&](int r) {
                         const int h = t * TH + row0 + r;
                         if (h < sc.H)
                             *reinterpret_cast<float4*>(gp + (long long)h * sc.W) =
                                 RES ? make_float4(acc[r][0] + res[r].x, acc[r][1] + res[r].y, acc[r][2] + res[r].z,
                                                   acc[r][3] + res[r].w)
                                     : make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-                    }
+                    });
                 }
             });
     } else {
