@@ -191,7 +191,12 @@ __device__ __forceinline__ void correlate_4x4(const float* sm, int row0, int lan
 
 struct Sched {
     int N, C, H, W, col_tiles, items;
-    int tile_fastest;  // 1: items ordered (c, n, column tile); 0: (c, column tile, n)
+    // item order.  1: (c, n, column tile), contiguous ranges per CTA.  0: (c, column
+    // tile, n), contiguous ranges per CTA.  2: CTA b keeps column tile b % col_tiles
+    // and walks (c, n), n fastest; the col_tiles CTAs of a group share one contiguous
+    // (c, n) range, so neighbouring tiles read their common halo strips at about the
+    // same time (L2 hits) while each CTA's runs of one (c, column tile) stay whole.
+    int tile_fastest;
     // The column tiles the items cover: tile k (0 <= k < col_tiles) is column tile
     // ct_base + k * ct_step of the output (all of them: 0, 1; a rank's interior or
     // edge tiles: see the rank entry points).  xo: the column of the x (and
@@ -200,7 +205,11 @@ struct Sched {
     int ct_base, ct_step, xo;
     __device__ __forceinline__ int col(int k) const { return ct_base + k * ct_step; }
     __device__ __forceinline__ void decode(int item, int& n, int& c, int& ct) const {
-        if (tile_fastest) {
+        if (tile_fastest == 2) {
+            n = item % N;
+            c = item / N;
+            ct = blockIdx.x % col_tiles;
+        } else if (tile_fastest) {
             ct = item % col_tiles;
             const int rest = item / col_tiles;
             n = rest % N;
@@ -214,7 +223,12 @@ struct Sched {
     }
     // the item after (n, c, ct) in this order, without divisions
     __device__ __forceinline__ void next(int& n, int& c, int& ct) const {
-        if (tile_fastest) {
+        if (tile_fastest == 2) {
+            if (++n == N) {
+                n = 0;
+                ++c;
+            }
+        } else if (tile_fastest) {
             if (++ct == col_tiles) {
                 ct = 0;
                 if (++n == N) {
@@ -231,6 +245,13 @@ struct Sched {
         }
     }
     __device__ __forceinline__ void range(int& i0, int& i1) const {
+        if (tile_fastest == 2) {  // items here index (c, n) of the CTA's own column tile
+            const int g = blockIdx.x / col_tiles, groups = gridDim.x / col_tiles;
+            const long long per = (long long)N * C;
+            i0 = (int)(g * per / groups);
+            i1 = (int)((g + 1) * per / groups);
+            return;
+        }
         i0 = (int)((long long)blockIdx.x * items / gridDim.x);
         i1 = (int)((long long)(blockIdx.x + 1) * items / gridDim.x);
     }
@@ -647,6 +668,16 @@ Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_
     sc.items = d->N * d->C_in * sc.col_tiles;
     const int g = device_sm_count() * ctas_per_sm;
     *grid = g < sc.items ? g : sc.items;
+    if (tile_fastest == 2) {
+        // one group of col_tiles CTAs per (c, n) range; with more tiles than CTAs,
+        // runs of one (c, column tile) in contiguous ranges instead
+        const int groups = sc.col_tiles ? g / sc.col_tiles : 0;
+        const long long per = (long long)d->N * d->C_in;
+        if (groups >= 1)
+            *grid = (int)((groups < per ? groups : per) * sc.col_tiles);
+        else
+            sc.tile_fastest = 0;
+    }
     return sc;
 }
 
@@ -680,7 +711,8 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     hc_status s = plane_map<K, BWD_WARPS>(&gm, gy, d, lay.pitch);
     if (s || (s = plane_map<K, BWD_WARPS>(&xm, x, d, lay.pitch))) return s;
     int grid;
-    const Sched sc = sched_of(d, &grid, 0, 1, lay);  // runs of one (c, column tile): gw stays in registers
+    // runs of one (c, column tile): gw stays in registers; column tiles side by side in CTA groups
+    const Sched sc = sched_of(d, &grid, 2, 1, lay);
     const int tps = p.Wl / TW;
     const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
     static std::atomic<unsigned long long> attr{0};
