@@ -78,20 +78,24 @@ def bf16x6_peak(peaks):
 
 
 def op_rooflines(ops_ms, work, peaks, sms):
-    """Per-op rates against each op's own bound.  work: op -> (bound, amount)
-    with bound "tensor" (fp32 FLOPs on the bf16-piece GEMM), "alu" (FP32 FLOPs)
-    or "hbm" (algorithmic bytes); ops without an entry are left out."""
+    """Per-op rates against each op's own bound.  work: op -> (bound, amount[,
+    hbm bytes]) with bound "tensor" (fp32 FLOPs on the bf16-piece GEMM), "alu"
+    (FP32 FLOPs) or "hbm" (algorithmic bytes); a compute-bound op may also give
+    its algorithmic HBM bytes, reported beside; ops without an entry are left out."""
     out = {}
     for op, ms in ops_ms.items():
         if op not in work or ms <= 0:
             continue
-        bound, amount = work[op]
+        bound, amount = work[op][:2]
         if bound == "hbm":
             a, peak, unit = amount / (ms * 1e-3) / 1e9, peaks["hbm"], "GB/s"
         else:
             a = amount / (ms * 1e-3) / 1e12
             peak, unit = (bf16x6_peak(peaks), "TFLOP/s") if bound == "tensor" else (alu_peak(peaks, sms), "TFLOP/s")
         out[op] = {"bound": bound, "achieved": a, "unit": unit, "peak": peak, "frac": a / peak}
+        if len(work[op]) > 2 and work[op][2]:
+            hb = work[op][2] / (ms * 1e-3) / 1e9
+            out[op]["hbm"] = {"achieved": hb, "peak": peaks["hbm"], "unit": "GB/s", "frac": hb / peaks["hbm"]}
     return out
 
 
@@ -101,7 +105,7 @@ def alu_peak(peaks, sms):
 
 # Source file of each traced kernel (a DRAM-traffic record applies only to the source it was taken on).
 KERNEL_SRC = {"dw_": "dw.cu", "tc_conv_kernel": "tc.cu", "ln_": "pointwise.cu", "ls_": "pointwise.cu",
-              "bias_rows": "reduce.cu", "direct_": "direct.cu"}
+              "bias_rows": "reduce.cu", "direct_": "direct.cu", "patchify_": "patchify.cu"}
 
 
 def kernel_src(name):
@@ -483,13 +487,20 @@ class BlockWorkload:
 
     def kernel_work(self):
         """Algorithmic work per step of the compute kernels, by trace name: the
-        bf16-piece GEMM passes (stem, 1x1 256->1024, 1x1 1024->256: forward and
-        grad_input conv passes, weight-gradient passes) and the depthwise stencil."""
+        bf16-piece GEMM passes (stem forward; 1x1 256->1024 and 1024->256 forward,
+        grad_input and weight gradient), the depthwise stencil and the stem's
+        weight gradient (FP32 reduction reading the image and grad_output once)."""
         st, dw, p1, p2 = (conv_flops(c) for c in (self.stem, self.dw, self.pw1, self.pw2))
         E = self.N * 256 * self.HW
         return {"tc_conv_kernel bf16x6 conv pass": ("tensor", st + 2 * p1 + 2 * p2, None),
-                "tc_conv_kernel bf16x6 weight-gradient pass": ("tensor", st + p1 + p2, None),
-                "dw_fwd_kernel": ("alu", dw, 8 * E), "dw_bwd_kernel": ("alu", 2 * dw, 16 * E)}
+                "tc_conv_kernel bf16x6 weight-gradient pass": ("tensor", p1 + p2, None),
+                "dw_fwd_kernel": ("alu", dw, 8 * E), "dw_bwd_kernel": ("alu", 2 * dw, 16 * E),
+                "patchify_wgrad_kernel": ("alu", st, self.stem_bytes())}
+
+    def stem_bytes(self):
+        """The stem's algorithmic HBM bytes: the image and the 256-channel stem
+        output (written forward, grad_output read backward) once each."""
+        return 4 * (self.N * 3 * 512 * 4096 + self.N * 256 * self.HW)
 
     def oracle_sample(self, orc):
         """The block's chain for the oracle, forward and backward, on one image
@@ -547,13 +558,16 @@ class BlockWorkload:
 
     def op_work(self):
         """Each op's bound and algorithmic work: conv FLOPs (tensor: the bf16-piece
-        GEMMs; alu: the depthwise stencil) or HBM bytes of the pointwise ops
-        (E = elements of a 256-channel activation)."""
+        GEMMs; alu: the depthwise stencil and the stem's weight gradient) or HBM
+        bytes of the stem forward and the pointwise ops (E = elements of a
+        256-channel activation)."""
         E = self.N * 256 * self.HW
         st, dw, p1, p2 = (conv_flops(c) for c in (self.stem, self.dw, self.pw1, self.pw2))
-        return {"stem_fwd": ("tensor", st), "dw_fwd": ("alu", dw), "pw1_fwd": ("tensor", p1),
+        # the stem: forward bound by its output write (48-deep K, 256 wide), backward
+        # (weight and bias gradients only) by the FP32 reduction, HBM bytes beside
+        return {"stem_fwd": ("hbm", self.stem_bytes()), "dw_fwd": ("alu", dw), "pw1_fwd": ("tensor", p1),
                 "gelu_pw2_fwd": ("tensor", p2), "pw2_bwd": ("tensor", 2 * p2), "gelu_pw1_bwd": ("tensor", 2 * p1),
-                "dw_bwd": ("alu", 2 * dw), "stem_bwd": ("tensor", st),
+                "dw_bwd": ("alu", 2 * dw), "stem_bwd": ("alu", st, self.stem_bytes()),
                 "ln_fwd": ("hbm", 8 * E + 8 * self.N * self.HW), "ln_bwd": ("hbm", 12 * E + 8 * self.N * self.HW),
                 "ls_fwd": ("hbm", 12 * E), "ls_bwd": ("hbm", 12 * E)}
 
@@ -850,9 +864,12 @@ def run_peaks(args):
     for kind, name in ((0, "depthwise7x7_stencil_smem"), (1, "depthwise7x7_weight_correlation_smem")):
         tf, ms = best(lambda fl: lib.hcp_stencil(kind, 1000, P(w), P(out), S, fl))
         res[name] = {"tflops": tf, "ms": ms}
-    for kind, name in ((0, "tcgen05_tf32_m128n256k8"), (1, "tcgen05_bf16_m128n256k16")):
+    for kind, name in ((0, "tcgen05_tf32_m128n256k8"), (1, "tcgen05_bf16_m128n256k16"),
+                       (2, "tcgen05_tf32_m128n16k8_2cta_per_sm")):
         tf, ms = best(lambda fl: lib.hcp_mma(kind, 20000, C.cast(P(status), C.POINTER(C.c_int)), S, fl))
         res[name] = {"tflops": tf, "ms": ms}
+        if kind == 2:  # time per MMA per SM: the floor a narrow (N <= 32) MMA pays
+            res[name]["ns_per_mma_per_sm"] = ms * 1e6 / (20000 * 2)
     clk = clocks.stop()
     if int(status.item()):
         raise SystemExit("an MMA loop CTA gave up waiting for its MMAs")
@@ -860,7 +877,8 @@ def run_peaks(args):
     line = {"workload": "peaks", "sms": sms, "unit": "TFLOP/s", "results": res,
             "fp32_derived_peak": alu_peak(peaks, sms), "clocks": clk,
             "note": "FP32 derived peak = SMs x 128 lanes x 2 x max SM clock; tensor rates per MMA loop of one CTA "
-                    "per SM (M 128, N 256, operands zero, from shared memory)"}
+                    "per SM (M 128, N 256, operands zero, from shared memory); the N 16 loop runs two CTAs per SM "
+                    "and gives the tensor pipe's time per narrow MMA"}
     print(json.dumps(line), flush=True)
     return 0
 

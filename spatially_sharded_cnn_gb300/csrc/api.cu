@@ -133,11 +133,17 @@ static hc_algo pick(const hc_conv_desc* d, const Plan& p) {
 //   TC_BF16X6: [gw partials][gb partials][bias scratch][bf16 pieces of gy, w^T, x; split-K partials]
 // reuse: the backward pass that takes x's operand copy from the forward workspace
 static size_t bwd_ws_bytes(const hc_conv_desc* d, const Plan& p, hc_algo a, bool reuse = false) {
-    size_t b = round256(sizeof(float) * p.Q * wsize(d)) + round256(sizeof(float) * p.Q * d->C_out);
+    const size_t base = round256(sizeof(float) * p.Q * wsize(d)) + round256(sizeof(float) * p.Q * d->C_out);
+    size_t b = base;
     if (a == HC_ALGO_DEPTHWISE) b += round256(sizeof(float) * depthwise_bwd_ws_floats(d, p));
     if (a == HC_ALGO_TC_3XTF32) b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + tc_ws_bytes(d, p, 1);
     if (a == HC_ALGO_TC_BF16X6)
         b += round256(sizeof(float) * bias_grad_ws_floats(d->C_out, p.Q)) + bf16_ws_bytes(d, p, reuse ? 2 : 1);
+    // room for the patchify stem's weight-gradient slots (taken without grad_input)
+    if (patchify_wgrad_supported(d, p)) {
+        const size_t pw = base + round256(sizeof(float) * patchify_wgrad_ws_floats(d, p));
+        if (pw > b) b = pw;
+    }
     return b;
 }
 
@@ -201,7 +207,8 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     for (const void* q : {(const void*)gx, (const void*)gw, (const void*)gb, (const void*)gwp_out,
                           (const void*)gbp_out})
         if (q && !aligned16(q)) return HC_ERR_INVALID_ARG;
-    if (a == HC_ALGO_AUTO) a = pick(d, p);
+    const bool auto_algo = a == HC_ALGO_AUTO;
+    if (auto_algo) a = pick(d, p);
     if (!algo_supported(d, p, a) || !act_supported(d, a, act)) return HC_ERR_UNSUPPORTED;
     if (act == HC_ACT_GELU_OUTPUT && (!y_pre || !aligned16(y_pre))) return HC_ERR_INVALID_ARG;
     reuse = reuse && a == HC_ALGO_TC_BF16X6;  // the other families keep nothing between the passes
@@ -222,6 +229,18 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
     if (gbp_out) gbp = gbp_out;
     const bool want_w = gw || gwp_out;
     const bool want_b = gb || gbp_out;
+    // Weight / bias gradients alone of the patchify stem (the image needs no
+    // gradient): the direct FP32 reduction reads x and grad_output once instead
+    // of splitting grad_output into bf16 pieces for a 48-column GEMM.  Taken
+    // when the algorithm was left to the library and the workspace holds its
+    // slot table (its size follows the SM count).
+    if (auto_algo && !gx && act == HC_ACT_NONE && !residual && patchify_wgrad_supported(d, p)) {
+        const size_t used = (size_t)(wsp - (char*)ws);
+        if (used + sizeof(float) * patchify_wgrad_ws_floats(d, p) <= ws_bytes) {
+            if (!want_w && !want_b) return HC_OK;
+            return launch_patchify_wgrad(d, p, x, gy, (float*)wsp, gwp, gbp, gw, gb, s);
+        }
+    }
     switch (a) {
         case HC_ALGO_DEPTHWISE:  // a residual gradient goes into the grad_input epilogue; the shard
                                  // partials' kernel also writes the full gradients
@@ -487,8 +506,8 @@ hc_status hc_sync_check(void* stream) {
         return HC_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return HC_ERR_CUDA;
-    const hc_status a = dw_take_status(), b = tc_take_status();
-    return a ? a : b;
+    const hc_status a = dw_take_status(), b = tc_take_status(), c = pw_take_status();
+    return a ? a : b ? b : c;
 }
 
 hc_status hc_selftest_timeout(int wait_us, void* stream) {

@@ -170,6 +170,21 @@ hc_status launch_depthwise_bwd(const hc_conv_desc* d, const Plan& p, const float
                                bool want_weight_grads, cudaStream_t st, const float* gres = nullptr,
                                float* gw = nullptr, float* gb = nullptr, const DwLayout& lay = DwLayout());
 // the halo-padded layout of one rank (hc_halo_pad / _pack / _unpack)
+// Shard partials of a per-(grid shard, channel) slot table
+// tile_part[Q][C][rows][KK + 1] (KK weight terms + the bias): gwp[q][c][k] /
+// gbp[q][c] = the slots summed in order, gw / gb (nullable) = those summed over
+// q in order.
+hc_status launch_shard_partials(const float* tile_part, float* gwp, float* gbp, float* gw, float* gb, int Q, int C,
+                                int rows, int KK, cudaStream_t st);
+
+// patchify.cu: weight / bias gradient of a 4x4 stride-4 conv with 3 input
+// channels (the ConvNeXt stem) as a direct FP32 reduction, per grid shard.
+bool patchify_wgrad_supported(const hc_conv_desc* d, const Plan& p);
+size_t patchify_wgrad_ws_floats(const hc_conv_desc* d, const Plan& p);
+hc_status launch_patchify_wgrad(const hc_conv_desc* d, const Plan& p, const float* x, const float* gy,
+                                float* tile_part, float* gwp, float* gbp, float* gw, float* gb, cudaStream_t st);
+hc_status pw_take_status();
+
 hc_status launch_halo_pad(const hc_conv_desc* d, int Wl, const float* x, float* xp, cudaStream_t st);
 hc_status launch_halo_pack(const hc_conv_desc* d, int Wl, const float* xp, int side, float* buf, cudaStream_t st);
 hc_status launch_halo_unpack(const hc_conv_desc* d, int Wl, const float* buf, int side, float* xp, cudaStream_t st);

@@ -244,6 +244,16 @@ struct Sched {
             }
         }
     }
+    // This CTA's jobs [j0, j1) when each item is split into `ntiles` row-tile jobs
+    // and the split falls between any two jobs (item = job / ntiles).
+    __device__ __forceinline__ void job_range(int ntiles, long long& j0, long long& j1) const {
+        const bool grouped = tile_fastest == 2;
+        const long long total = (grouped ? (long long)N * C : (long long)items) * ntiles;
+        const int idx = grouped ? (int)blockIdx.x / col_tiles : (int)blockIdx.x;
+        const int parts = grouped ? (int)gridDim.x / col_tiles : (int)gridDim.x;
+        j0 = idx * total / parts;
+        j1 = (idx + 1) * total / parts;
+    }
     __device__ __forceinline__ void range(int& i0, int& i1) const {
         if (tile_fastest == 2) {  // items here index (c, n) of the CTA's own column tile
             const int g = blockIdx.x / col_tiles, groups = gridDim.x / col_tiles;
@@ -397,15 +407,28 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     float* red = smem + 2 * NSTAGE * G::TILE;         // [BWD_WARPS][KK + 1]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + BWD_WARPS * WSLOT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int i0, i1;
-    sc.range(i0, i1);
-    if (i0 >= i1) return;
     const int ntiles = (sc.H + TH - 1) / TH;
-    const int jobs = (i1 - i0) * ntiles;
+    // Without row shards the CTA's jobs are a contiguous run of (item, row tile)
+    // pairs that may start and end inside an item (t0: the first job's row tile);
+    // with row shards whole items.
+    int i0, i1, jobs, t0 = 0;
+    if (ROWS) {
+        sc.range(i0, i1);
+        if (i0 >= i1) return;
+        jobs = (i1 - i0) * ntiles;
+    } else {
+        long long j0, j1;
+        sc.job_range(ntiles, j0, j1);
+        if (j0 >= j1) return;
+        jobs = (int)(j1 - j0);
+        i0 = (int)(j0 / ntiles);
+        t0 = (int)(j0 - (long long)i0 * ntiles);
+        i1 = i0;  // unused without row shards
+    }
     const bool want_wb = a.want_wb != 0;
 
     // Job q -> (item, row tile t).  Items run (c, column tile, n), n fastest; a
-    // run is this CTA's items of one (c, column tile).  Without row shards the
+    // run is this CTA's jobs of one (c, column tile).  Without row shards the
     // jobs go item by item, tile by tile.  With row shards a run's jobs go row
     // shard by row shard, each over all the run's images, so the weight
     // gradient of one (run, row shard) accumulates in registers and is flushed
@@ -429,7 +452,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
 
     // Thread 0 issues the jobs in order; without row shards its cursor (in_, ic,
     // ict, it) advances one job at a time (no divisions).
-    int in_ = 0, ic = 0, ict = 0, it = 0;
+    int in_ = 0, ic = 0, ict = 0, it = t0;
     if (!ROWS) sc.decode(i0, in_, ic, ict);
     auto issue = [&](int q) {
         int n, c, ct, item, t;
@@ -466,7 +489,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     auto ring = [&](auto&& on_channel, auto&& work) {
         int cur_c = -1;
         // without row shards: job q's item (n, c, ct) and row tile t, advanced one job at a time
-        int n, c, ct, t = 0, s = 0;
+        int n, c, ct, t = t0, s = 0;
         unsigned ph = 0;  // phase of stage s's barrier this job waits for
         if (!ROWS) sc.decode(i0, n, c, ct);
         for (int q = 0; q < jobs; q++) {
@@ -476,9 +499,9 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                 job(q, item, t, flush);  // the last job of a (run, row shard) segment
                 sc.decode(item, n, c, ct);
             } else {
-                // the last job of a run: its last row tile, and the next job (if any)
-                // is another (c, column tile) -- with n fastest, exactly when n = N - 1
-                flush = t == ntiles - 1 && (q + 1 == jobs || n == sc.N - 1);
+                // the last job of a run: the CTA's last job, or the last row tile of
+                // image N - 1 (the next job is another (c, column tile))
+                flush = q + 1 == jobs || (t == ntiles - 1 && n == sc.N - 1);
             }
             if (c != cur_c) {
                 on_channel(c);
@@ -554,11 +577,16 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         for (int u = 0; u < K; u++)
 #pragma unroll
             for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
-        int run_n0 = -1;  // first image of the current (c, column tile) run
+        // Partial slots of one (grid shard, c, tile): one per image with row shards,
+        // else one per (image, row tile); a run's total goes to its first slot and
+        // its other slots get zeros, so every slot is written exactly once.
+        const int slots = ROWS ? sc.N : sc.N * ntiles;
+        int run_m0 = -1;  // first slot of the current run
         ring([](int) {},
              [&](int s, int n, int c, int ct, int t, bool flush) {
                  if (!want_wb) return;
-                 if (run_n0 < 0) run_n0 = n;
+                 const int m = ROWS ? n : n * ntiles + t;
+                 if (run_m0 < 0) run_m0 = m;
                  const float* gys = tiles + s * 2 * G::TILE;
                  const float* xs = gys + G::TILE;
 #pragma unroll 1
@@ -601,39 +629,64 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                      for (int k = 0; k < BWD_WARPS; k++) tot += red[k * WSLOT + wtid];
                      const int r = sc.col(ct) / a.tiles_per_shard, tt = sc.col(ct) - r * a.tiles_per_shard;
                      const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
-                     float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * sc.N * (KK + 1);
-                     for (int m = run_n0; m <= n; m++) slot[(long long)m * (KK + 1) + wtid] = m == run_n0 ? tot : 0.0f;
+                     float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * slots * (KK + 1);
+                     for (int k = run_m0; k <= m; k++) slot[(long long)k * (KK + 1) + wtid] = k == run_m0 ? tot : 0.0f;
                  }
-                 run_n0 = -1;
+                 run_m0 = -1;
              });
     }
 }
 
-// Shard partials: gwp[r][c][k] = sum over (tile tt, image n) of the partials,
-// tt then n ascending; gbp[r][c] likewise from the last slot.  One thread per
+// Shard partials: gwp[r][c][k] = sum over shard r's slots of the partials (tile
+// tt, then image n and, without row shards, row tile, ascending); gbp[r][c]
+// likewise from the last entry.  One thread per
 // (c, k) walks the shards in order and also writes the full gradients
 // gw[c][k] / gb[c] (either may be null): the shard partials added from shard 0
 // up, the order hc_conv2d_bwd's shard sum uses.
 __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, float* __restrict__ gwp,
                                          float* __restrict__ gbp, float* __restrict__ gw, float* __restrict__ gb,
                                          int Q, int C, int rows, int KK) {
+    constexpr int B = 16;  // loads in flight per thread
     const long long total = (long long)C * (KK + 1);
     for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
          q += (long long)gridDim.x * blockDim.x) {
         const int k = (int)(q % (KK + 1));
         const int c = (int)(q / (KK + 1));
-        float tot = 0.0f;
-        for (int r = 0; r < Q; r++) {
-            const long long rc = (long long)r * C + c;
-            const float* src = tile_part + rc * rows * (KK + 1) + k;
-            float s = 0.0f;
-            for (int m = 0; m < rows; m++) s += src[(long long)m * (KK + 1)];
-            if (k < KK) {
-                if (gwp) gwp[rc * KK + k] = s;
-            } else if (gbp) {
-                gbp[rc] = s;
+        // the (shard r, slot m) pairs in order, r slowest: loaded B at a time, added one
+        // by one (slots ascending within a shard, shards ascending into the total)
+        const long long all = (long long)Q * rows;
+        float s = 0.0f, tot = 0.0f;
+        int lr = 0, lm = 0, ar = 0, am = 0;  // load and add cursors (shard, slot)
+        for (long long i0 = 0; i0 < all; i0 += B) {
+            float v[B];
+#pragma unroll
+            for (int i = 0; i < B; i++) {
+                v[i] = 0.0f;
+                if (i0 + i < all) {
+                    v[i] = __ldg(tile_part + (((long long)lr * C + c) * rows + lm) * (KK + 1) + k);
+                    if (++lm == rows) {
+                        lm = 0;
+                        ++lr;
+                    }
+                }
             }
-            tot += s;
+#pragma unroll
+            for (int i = 0; i < B; i++) {
+                if (i0 + i >= all) break;
+                s += v[i];
+                if (++am == rows) {  // shard ar complete
+                    const long long rc = (long long)ar * C + c;
+                    if (k < KK) {
+                        if (gwp) gwp[rc * KK + k] = s;
+                    } else if (gbp) {
+                        gbp[rc] = s;
+                    }
+                    tot += s;
+                    s = 0.0f;
+                    am = 0;
+                    ++ar;
+                }
+            }
         }
         if (k < KK) {
             if (gw) gw[(long long)c * KK + k] = tot;
@@ -653,6 +706,13 @@ hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d, in
     const uint64_t strides[2] = {wp * 4, (uint64_t)d->H * wp * 4};
     const uint32_t box[3] = {(uint32_t)SMW, (uint32_t)Geo<K, WARPS>::R, 1};
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Weight-gradient partial slots per (grid shard, channel, column tile) of the
+// backward: one per image with row shards, else one per (image, row tile).
+long long bwd_slots(const hc_conv_desc* d, const Plan& p) {
+    constexpr int TH = Geo<3, BWD_WARPS>::TH;  // the same for every K
+    return p.Sh > 1 ? (long long)d->N : (long long)d->N * ((d->H + TH - 1) / TH);
 }
 
 Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm, const DwLayout& lay) {
@@ -739,13 +799,19 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     }
     if (sc.items) s = launched("dw_bwd_kernel", st);
     if (s || !want_wb || !lay.partials) return s;
-    const long long total = (long long)d->C_in * (K * K + 1);
-    dw_shard_partials_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tile_part, gwp, gbp, gw, gb, p.Q,
-                                                                             d->C_in, tps * d->N, K * K);
-    return launched("dw_shard_partials_kernel", st);
+    return launch_shard_partials(tile_part, gwp, gbp, gw, gb, p.Q, d->C_in, (int)(tps * bwd_slots(d, p)), K * K, st);
 }
 
 }  // namespace
+
+hc_status launch_shard_partials(const float* tile_part, float* gwp, float* gbp, float* gw, float* gb, int Q, int C,
+                                int rows, int KK, cudaStream_t st) {
+    const long long total = (long long)C * (KK + 1);
+    // small blocks: the few thousand threads spread over all the SMs
+    dw_shard_partials_kernel<<<(unsigned)((total + 63) / 64), 64, 0, st>>>(tile_part, gwp, gbp, gw, gb, Q, C, rows,
+                                                                           KK);
+    return launched("dw_shard_partials_kernel", st);
+}
 
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
@@ -759,7 +825,7 @@ bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
 
 size_t depthwise_bwd_ws_floats(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
-    return (size_t)p.Q * d->C_in * (p.Wl / TW) * d->N * (K * K + 1);
+    return (size_t)p.Q * d->C_in * (p.Wl / TW) * bwd_slots(d, p) * (K * K + 1);
 }
 
 hc_status launch_depthwise_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w,

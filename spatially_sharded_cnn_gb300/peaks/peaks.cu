@@ -181,19 +181,20 @@ __host__ __device__ constexpr uint32_t idesc(int kind, int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-constexpr int MMA_M = 128, MMA_N = 256;
+constexpr int MMA_M = 128;
 
-// One CTA per SM; one thread issues `iters` MMAs (M = 128, N = 256, K = 8 tf32
-// or 16 bf16: one 32-byte k-step of 128-byte swizzled operand rows, cycling over
-// the four k-steps of the tiles) accumulating into one TMEM tile, commits them
-// to an mbarrier, and the CTA waits for it (bounded) before freeing the tensor
-// memory.  Operand values do not matter for the rate; the tiles are zero.
-template <int KIND>
-__global__ void __launch_bounds__(128, 1) mma_loop(int iters, int* status) {
+// One thread per CTA issues `iters` MMAs (M = 128, N = MMA_N, K = 8 tf32 or 16
+// bf16: one 32-byte k-step of 128-byte swizzled operand rows, cycling over the
+// four k-steps of the tiles) accumulating into one TMEM tile, commits them to an
+// mbarrier, and the CTA waits for it (bounded) before freeing the tensor memory.
+// Operand values do not matter for the rate; the tiles are zero.
+template <int KIND, int MMA_N>
+__global__ void __launch_bounds__(128) mma_loop(int iters, int* status) {
+    constexpr uint32_t TCOLS = MMA_N < 32 ? 32 : MMA_N;
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     unsigned char* a = base;                       // 128 rows x 128 bytes
-    unsigned char* b = base + MMA_M * 128;         // 256 rows x 128 bytes
+    unsigned char* b = base + MMA_M * 128;         // MMA_N rows x 128 bytes
     uint64_t* bar = (uint64_t*)(b + MMA_N * 128);
     uint32_t* slot = (uint32_t*)(bar + 1);
     for (int i = threadIdx.x; i < (MMA_M + MMA_N) * 128 / 16; i += blockDim.x)
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(128, 1) mma_loop(int iters, int* status) {
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(slot)),
-                     "r"(MMA_N)
+                     "r"(TCOLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(128, 1) mma_loop(int iters, int* status) {
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(MMA_N) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TCOLS) : "memory");
 }
 
 int sm_count() {
@@ -309,20 +310,28 @@ int hcp_stencil(int kind, int jobs, const float* w, float* out, void* stream, do
 }
 
 // kind 0: tcgen05.mma kind::tf32 (M 128, N 256, K 8); kind 1: kind::f16 with
-// bf16 operands (K 16); one CTA per SM, `iters` MMAs each.  status: device int,
-// set to 1 if a CTA gave up waiting for its MMAs.
+// bf16 operands (K 16); one CTA per SM, `iters` MMAs each.  kind 2: kind::tf32
+// with N 16 (the narrowest M 128 shape), two CTAs per SM issuing side by side:
+// the floor of the tensor pipe's time per MMA, which a narrow MMA cannot go
+// below.  status: device int, set to 1 if a CTA gave up waiting for its MMAs.
+// *flops: the FLOPs the MMAs issued (2 M N K each).
 int hcp_mma(int kind, int iters, int* status, void* stream, double* flops) {
     cudaStream_t st = (cudaStream_t)stream;
-    const int smem = (MMA_M + MMA_N) * 128 + 1024 + 64;
     const int sms = sm_count();
+    const int N = kind == 2 ? 16 : 256, ctas = kind == 2 ? 2 * sms : sms;
+    const int smem = (MMA_M + N) * 128 + 1024 + 64;
+    const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (kind == 0) {
-        if (cudaFuncSetAttribute(mma_loop<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) return -2;
-        mma_loop<0><<<sms, 128, smem, st>>>(iters, status);
+        if (cudaFuncSetAttribute(mma_loop<0, 256>, A, smem)) return -2;
+        mma_loop<0, 256><<<ctas, 128, smem, st>>>(iters, status);
+    } else if (kind == 1) {
+        if (cudaFuncSetAttribute(mma_loop<1, 256>, A, smem)) return -2;
+        mma_loop<1, 256><<<ctas, 128, smem, st>>>(iters, status);
     } else {
-        if (cudaFuncSetAttribute(mma_loop<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) return -2;
-        mma_loop<1><<<sms, 128, smem, st>>>(iters, status);
+        if (cudaFuncSetAttribute(mma_loop<0, 16>, A, smem)) return -2;
+        mma_loop<0, 16><<<ctas, 128, smem, st>>>(iters, status);
     }
-    *flops = 2.0 * MMA_M * MMA_N * (kind ? 16 : 8) * (double)iters * sms;
+    *flops = 2.0 * MMA_M * N * (kind == 1 ? 16 : 8) * (double)iters * ctas;
     return (int)cudaGetLastError();
 }
 
