@@ -136,7 +136,7 @@ def peak_of(bound, peaks, sms):
     return peaks["hbm"], "GB/s", f"{peaks['src']} HBM copy bandwidth"
 
 
-def kernel_rooflines(table, work, peaks, sms):
+def kernel_rooflines(table, work, peaks, sms, traffic_key=None):
     """Each traced kernel with a work entry, against its own bound; the dominant
     one (largest device time per step) is the line's roofline."""
     out = {}
@@ -155,7 +155,7 @@ def kernel_rooflines(table, work, peaks, sms):
             r["hbm"] = {"achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
                         "peak_source": peaks["src"]}
         src_file = kernel_src(k)
-        r["traffic"] = traffic_for(k, src_file) if src_file else None
+        r["traffic"] = traffic_for(traffic_key, k, src_file) if src_file and traffic_key else None
         out[k] = r
     return out
 
@@ -295,8 +295,9 @@ class ConvWorkload:
         if self.name == "dw7":
             return {"dw_fwd_kernel": ("alu", F, 8 * self.E), "dw_bwd_kernel": ("alu", 2 * F, 12 * self.E)}
         if self.name == "dense5x5":
+            # conv passes on 3xTF32; the weight gradient on bf16 pieces (six products)
             return {"tc_conv_kernel 3xTF32 conv pass": ("tensor_tf32", 2 * F, None),
-                    "tc_conv_kernel 3xTF32 weight-gradient pass": ("tensor_tf32", F, None)}
+                    "tc_conv_kernel bf16x6 weight-gradient pass": ("tensor", F, None)}
         return {}
 
     def oracle_sample(self, orc):
@@ -757,12 +758,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def traffic_for(kernel: str, src_file: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+def traffic_for(workload: str, kernel: str, src_file: str):
+    """DRAM bytes per launch of `kernel` in the default-size `workload` from a
+    committed ncu summary, if it was taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
+    d = json.load(open(p)).get(workload, {}).get(kernel)
     if not d:
         return None
     h = hashlib.sha256(open(src_file, "rb").read()).hexdigest()[:16]
@@ -1051,7 +1053,9 @@ def main():
     roof = wl.roofline(ops_ms, peaks, sms)
     k_roofs = None
     if ktable is not None and hasattr(wl, "kernel_work"):
-        k_roofs = kernel_rooflines(ktable, wl.kernel_work(), peaks, sms)
+        # DRAM traffic records hold for the default batch of each workload
+        k_roofs = kernel_rooflines(ktable, wl.kernel_work(), peaks, sms,
+                                   args.workload if args.batch in (None, 7) else None)
         if roof is None and k_roofs:  # the dominant kernel: the largest device time per step
             roof = dict(max(k_roofs.values(), key=lambda r: r["ms_per_launch"] * r["launches_per_step"]))
     op_roofs = op_rooflines(ops_ms, wl.op_work(), peaks, sms) if hasattr(wl, "op_work") else None

@@ -72,7 +72,9 @@ typedef enum {
     HC_ALGO_AUTO = 0,
     HC_ALGO_DIRECT = 1,       /* plain direct convolution, any groups / stride  */
     HC_ALGO_DEPTHWISE = 2,    /* groups == C, odd k, stride 1, padding (k-1)/2  */
-    HC_ALGO_TC_3XTF32 = 3,    /* groups == 1: tcgen05 implicit GEMM, 3xTF32     */
+    HC_ALGO_TC_3XTF32 = 3,    /* groups == 1: tcgen05 implicit GEMM; forward and
+                                 grad_input on 3xTF32, the weight gradient (not
+                                 space-to-depth) on three bf16 pieces per operand */
     HC_ALGO_TC_BF16X6 = 4     /* groups 1, padding 0, C_out a multiple of 128,
                                  W_out % 8 == 0, W / num_shards / stride a
                                  multiple of 32, and either

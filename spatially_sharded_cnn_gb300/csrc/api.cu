@@ -101,6 +101,10 @@ hc_status make_plan(const hc_conv_desc* d, Plan* p) {
     return HC_OK;
 }
 
+static bool is_s2d_conv(const hc_conv_desc* d) {
+    return d->groups == 1 && d->stride >= 2 && d->kh == d->stride && d->kw == d->stride && d->padding == 0;
+}
+
 static bool aligned16(const void* q) { return ((uintptr_t)q & 15u) == 0; }
 
 static size_t wsize(const hc_conv_desc* d) {
@@ -261,7 +265,11 @@ static hc_status bwd(const hc_conv_desc* d, const float* x, const float* w, cons
                                          act == HC_ACT_GELU_OUTPUT ? y_pre : nullptr);
                     bias_done = true;
                 } else {
-                    st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s);
+                    // with the weight gradient (not space-to-depth) the bias partials come with
+                    // grad_output's pieces
+                    const bool fused_b = want_b && want_w && !is_s2d_conv(d);
+                    st = launch_tc_bwd(d, p, x, w, gy, gx, gwp, want_w, wsp, s, fused_b ? gbp : nullptr, btmp);
+                    bias_done = fused_b;
                 }
                 if (st) return st;
             }

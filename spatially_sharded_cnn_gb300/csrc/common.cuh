@@ -197,8 +197,11 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass);
 hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* b,
                         float* y, void* ws, cudaStream_t st);
 // grad_input (if gx) and the per-shard weight-gradient partials gwp (if want_w)
+// gbp (nullable, with want_w): the bias-gradient partials, summed in the read of
+// grad_output that splits it into the weight gradient's pieces (btmp: scratch).
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st);
+                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st, float* gbp = nullptr,
+                        float* btmp = nullptr);
 
 // 1x1 conv (stride 1, padding 0, groups 1) on tcgen05 with three bf16 pieces per
 // operand (six products, fp32 accuracy); C_in and C_out multiples of 128

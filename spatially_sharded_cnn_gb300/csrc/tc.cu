@@ -237,6 +237,9 @@ struct TcParams {
     int slots;      // taps * nblocks: (tap, 128-channel block) pairs; a unit covers two slots
     int kvalid;     // bf16 weight gradient: input channels that exist (the slots' columns past them
                     // are not computed: the reduction never reads them)
+    int bmn;        // bf16 weight gradient of a K x K conv: B MN-major from x's pieces in the
+                    // channel-blocked NHWC layout, each slot its own box at the tap's (row, column)
+                    // shift and its own N = 128 MMAs
     long long shard_chunks;                               // N * own_h * row_chunks
     float* part;    // [S][J][taps][Co][Ci]
 };
@@ -338,6 +341,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // bf16 pieces: one box brings all three pieces of a tile
                     unsigned char* st = ring + (size_t)s * p.stage_bytes;
                     unsigned char* bdst = st + 3 * p.a_piece;
+                    if (p.bmn) {
+                        // K x K weight gradient: chunk c of shard r = (n, 32-pixel piece, ho),
+                        // rows fastest, so the kernel rows of one column strip reuse its rows
+                        // while they are in L2.  A = grad_output [3][N][Co][H][W], 128 channels
+                        // x 32 pixels (K-major).  B, per slot: x [N][H][W][C/128][3][128], the
+                        // slot's 128 channels (all three pieces) at 32 pixels of row ho + u - pad
+                        // from column w + v - pad (MN-major; W is not the innermost dimension, so
+                        // any shift is a plain coordinate; rows and columns past the image read
+                        // zeros)
+                        const int qa = u.r / p.Sw, qb = u.r - qa * p.Sw;
+                        const int ho = qa * p.own_h + (int)(c % p.own_h);
+                        const long long rest = c / p.own_h;
+                        const int wc = (int)(rest % p.row_chunks), n = (int)(rest / p.row_chunks);
+                        const int w = qb * p.own_w + wc * BKH;
+                        const int slot_bytes = 3 * (p.b_piece / 2);
+                        const int nsl = 2 * u.tap + 1 < p.slots ? 2 : 1;
+                        mbar_expect_tx(&sh.full[s], (unsigned)(3 * p.a_piece + nsl * slot_bytes));
+                        tma_5d(st, &amap, w, ho, u.m0, n, 0, &sh.full[s]);
+                        for (int h = 0; h < nsl; h++) {
+                            const int slot = 2 * u.tap + h;
+                            const int tap = slot / p.nblocks, cb = slot - tap * p.nblocks;
+                            const int uu = tap / p.kw, vv = tap - uu * p.kw;
+                            tma_5d(bdst + h * slot_bytes, &bmap, 0, w + vv - p.pad, 6 * cb, ho + uu - p.pad, n,
+                                   &sh.full[s]);
+                        }
+                        continue;
+                    }
                     mbar_expect_tx(&sh.full[s], (unsigned)p.stage_bytes);
                     if (p.mode == 0) {
                         // A: weights [3][M][K], 128 rows x 32 k; B: activation [3][N][K][Ho*Wo],
@@ -433,6 +463,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t d = tmem + (uint32_t)(b * 256);
                 const long long c1 = c0 + p.group < u.c_end ? c0 + p.group : u.c_end;
                 bool first = true;
+                bool first_slot[2] = {true, true};
                 for (long long c = c0; c < c1; c++, it++) {
                     const int s = (int)(it % p.stages);
                     if (!mbar_wait(&sh.full[s], (unsigned)((it / p.stages) & 1), abort_flag)) {
@@ -440,6 +471,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (FMT == 1 && p.bmn) {
+                        // A as in the 1x1 weight gradient; B per slot: MN-major, 128-byte swizzle,
+                        // two 64-channel blocks BKH rows apart, 8-pixel groups 1 KB apart, the
+                        // three pieces a third of the slot apart.  Slot h accumulates into TMEM
+                        // columns 128 h .. 128 h + 127 (N = 128).
+                        constexpr int kPa[6] = {1, 2, 0, 1, 0, 0}, kPb[6] = {1, 0, 2, 0, 1, 0};
+                        unsigned char* st = ring + (size_t)s * p.stage_bytes;
+                        const uint64_t a0 = sdesc(st, 16, 512, 4);
+                        const uint32_t ap = (uint32_t)p.a_piece >> 4, pb = (uint32_t)(p.b_piece / 2) >> 4;
+                        const int slot_bytes = 3 * (p.b_piece / 2);
+                        const int nsl = 2 * u.tap + 1 < p.slots ? 2 : 1;
+                        const uint32_t id128 = idesc_bf16(BM, 128, 0, 1);
+#pragma unroll
+                        for (int k = 0; k < BKH / 16; k++) {
+#pragma unroll
+                            for (int t = 0; t < 6; t++) {
+#pragma unroll
+                                for (int h = 0; h < 2; h++) {
+                                    if (h >= nsl) break;
+                                    const uint64_t b0 = sdesc(st + 3 * p.a_piece + h * slot_bytes, BKH * 128, 1024, 2);
+                                    tc_mma_bf16(d + (uint32_t)(128 * h), a0 + kPa[t] * ap + 2 * k,
+                                                b0 + kPb[t] * pb + k * (2048 >> 4), id128, first_slot[h] ? 0u : 1u);
+                                    first_slot[h] = false;
+                                }
+                            }
+                        }
+                        tc_commit(&sh.empty[s]);
+                        continue;
+                    }
                     if (FMT == 1) {
                         // A: K-major, 64-byte swizzle, 8-row groups 512 B apart (both modes).  B:
                         // conv mode MN-major, 128-byte swizzle, 64-pixel blocks BKH rows apart and
@@ -1049,6 +1109,60 @@ __global__ void prep_pieces_t_kernel(const float* __restrict__ w, __nv_bfloat16*
     out[2 * ps + i] = e;
 }
 
+// x [N][C][H][W] -> three bf16 pieces in the channel-blocked NHWC layout
+// [N][H][W][C/128][3][128]: piece k of channel c at pixel (n, h, w) is element
+// (((n*H + h)*W + w)*(C/128) + c/128)*384 + k*128 + c%128 -- the weight
+// gradient's B operand, where a tap's pixel shift is a plain TMA coordinate.
+// A block takes 32 columns of one row (n, h) and walks the 128-channel blocks:
+// 128 rows x 32 floats through shared memory (16-byte loads along the rows,
+// pitch 33: no bank conflicts either way), then each thread splits 16 channels
+// of one pixel and writes 32 contiguous bytes per piece.  Needs C % 128 == 0
+// and W % 4 == 0; 256 threads.
+__global__ void __launch_bounds__(256) prep_pieces_nhwc_kernel(const float* __restrict__ x,
+                                                               __nv_bfloat16* __restrict__ out, int C, int H, int W) {
+    __shared__ float t[128][33];
+    const int tiles = (W + 31) / 32;
+    const long long nh = blockIdx.x / tiles;
+    const int w0 = (int)(blockIdx.x - nh * tiles) * 32;
+    const int n = (int)(nh / H), h = (int)(nh - (long long)n * H);
+    const int tid = threadIdx.x, wl = tid & 31, g = tid >> 5;
+    const int blocks = C / 128;
+    for (int cb = 0; cb < blocks; cb++) {
+#pragma unroll
+        for (int it = 0; it < 4; it++) {  // 128 channel rows x 8 float4
+            const int cl = tid / 8 + 32 * it, w4 = tid % 8;
+            const int c = cb * 128 + cl, w = w0 + 4 * w4;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (w < W) v = __ldg(reinterpret_cast<const float4*>(x + (((long long)n * C + c) * H + h) * W + w));
+            t[cl][4 * w4] = v.x;
+            t[cl][4 * w4 + 1] = v.y;
+            t[cl][4 * w4 + 2] = v.z;
+            t[cl][4 * w4 + 3] = v.w;
+        }
+        __syncthreads();
+        const int w = w0 + wl;
+        if (w < W) {
+            uint32_t q[3][8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                __nv_bfloat16 a[3], b[3];
+                split3(t[16 * g + i][wl], a[0], a[1], a[2]);
+                split3(t[16 * g + i + 1][wl], b[0], b[1], b[2]);
+#pragma unroll
+                for (int k = 0; k < 3; k++) q[k][i / 2] = pack2(a[k], b[k]);
+            }
+            __nv_bfloat16* o = out + ((nh * W + w) * blocks + cb) * 384 + 16 * g;
+#pragma unroll
+            for (int k = 0; k < 3; k++) {
+                uint4* d4 = reinterpret_cast<uint4*>(o + 128 * k);
+                d4[0] = make_uint4(q[k][0], q[k][1], q[k][2], q[k][3]);
+                d4[1] = make_uint4(q[k][4], q[k][5], q[k][6], q[k][7]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // Space-to-depth pieces: x [N][C][H][W] -> [3][N][K][Ho][Wo] with K = S*S*C and
 // channel k = (u*S + v)*C + c holding x[n][c][ho*S + u][wo*S + v].  Each item
 // reads 4*S consecutive columns of one input row (n, c, h = ho*S + u) and
@@ -1275,6 +1389,21 @@ hc_status pieces_rows_map(CUtensorMap* m, const void* base, int N, int C, int H,
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// x pieces in the channel-blocked NHWC layout (prep_pieces_nhwc_kernel) as
+// MN-major B tiles of one slot: dims (64, W, 6 * C/128, H, N) -- the third
+// dimension walks the 64-channel blocks of a pixel, (128-channel block, piece,
+// half) in that order, 128 bytes apart -- and box (64, 32, 6, 1, 1): for one
+// pixel row segment of 32 columns, the slot's 128 channels in all three pieces,
+// landing as [piece][64-channel half][32 pixels][64 channels] with the 128-byte
+// swizzle.
+hc_status pieces_nhwc_map(CUtensorMap* m, const void* base, int N, int C, int H, int W) {
+    const uint64_t pix = (uint64_t)3 * C * 2;  // bytes per pixel
+    const uint64_t dims[5] = {64, (uint64_t)W, (uint64_t)(6 * (C / 128)), (uint64_t)H, (uint64_t)N};
+    const uint64_t strides[4] = {pix, 128, (uint64_t)W * pix, (uint64_t)H * W * pix};
+    const uint32_t box[5] = {64, BKH, 6, 1, 1};
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 // piece stride: the element count rounded up to 128 (256 bytes)
 long long piece_stride(long long n) { return (n + 127) / 128 * 128; }
@@ -1368,10 +1497,10 @@ size_t tc_ws_bytes(const hc_conv_desc* d, const Plan& p, int pass) {
     const size_t ng = (size_t)d->N * d->C_out * p.Ho * p.Wo;
     const size_t wsz = (size_t)d->C_out * KK * d->C_in;
     if (pass == 0) return 2 * al256(4 * nx) + 2 * al256(4 * wsz);
-    const size_t nsh = (size_t)shift_copies(d) * d->N * d->C_in * d->H * shift_pitch(d);
     const int J = tc_wgrad_splits(d, p);
     const size_t part = al256(4 * (size_t)p.Q * J * wsz);
-    return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + 2 * al256(4 * ng) + 2 * al256(4 * nsh) + part;
+    return 2 * al256(4 * ng) + 2 * al256(4 * wsz) + al256(6 * (size_t)piece_stride((long long)ng)) +
+           al256(6 * nx) + part;
 }
 
 static hc_status launch_prep_s2d_nhwc(const hc_conv_desc* d, const Plan& p, const float* x, float* hi, float* lo,
@@ -1603,12 +1732,12 @@ hc_status launch_tc_fwd(const hc_conv_desc* d, const Plan& p, const float* x, co
 }
 
 hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, const float* w, const float* gy,
-                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st) {
+                        float* gx, float* gwp, bool want_w, void* ws, cudaStream_t st, float* gbp, float* btmp) {
     if (is_s2d(d)) return s2d_bwd(d, p, x, w, gy, gx, gwp, want_w, ws, st);
     const int K = d->kh, KK = K * K, Ci = d->C_in, Co = d->C_out;
     const size_t ng = (size_t)d->N * Co * p.Ho * p.Wo, wsz = (size_t)Co * KK * Ci;
-    const int Wc = shift_pitch(d), copies = shift_copies(d);
-    const size_t nsh = (size_t)copies * d->N * Ci * d->H * Wc;
+    const size_t nx = (size_t)d->N * Ci * d->H * d->W;
+    const long long psg = piece_stride((long long)ng);
     char* q = (char*)ws;
     float* gh = (float*)q;
     q += al256(4 * ng);
@@ -1618,14 +1747,10 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
     q += al256(4 * wsz);
     float* al = (float*)q;
     q += al256(4 * wsz);
-    float* gch = (float*)q;
-    q += al256(4 * ng);
-    float* gcl = (float*)q;
-    q += al256(4 * ng);
-    float* sh = (float*)q;
-    q += al256(4 * nsh);
-    float* sl = (float*)q;
-    q += al256(4 * nsh);
+    void* gp = q;  // grad_output's bf16 pieces [3][N][Co][Ho][Wo]
+    q += al256(6 * (size_t)psg);
+    __nv_bfloat16* xp = (__nv_bfloat16*)q;  // x's pieces [N][H][W][C/128][3][128]
+    q += al256(6 * nx);
     float* part = (float*)q;
     hc_status s;
     if (gx) {  // grad_input = conv of grad_output with the flipped, transposed kernel
@@ -1656,18 +1781,25 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         if ((s = launch_conv_pass(BN, ma, mb, tp, st, &my))) return s;
     }
     if (want_w) {
-        if ((s = launch_split_rows(gy, gch, gcl, d->N, Co, p.Ho, p.Wo, st))) return s;
-        const long long rows = (long long)d->N * Ci * d->H;
-        if (rows > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
-        if (copies == 1) {  // a 1-wide kernel never shifts: the plain row-interleaved hi / lo split
-            if ((s = launch_split_rows(x, sh, sl, d->N, Ci, d->H, d->W, st))) return s;
-        } else {
-            prep_shift_kernel<<<(unsigned)rows, 256, sizeof(float) * (Wc + 4), st>>>(x, sh, sl, rows, Ci, d->H, d->W,
-                                                                                      Wc, copies);
-            if ((s = launched("prep_shift_kernel", st))) return s;
-        }
+        // G[co][(tap, ci)] = sum over a shard's pixels of gy[co][px] x[ci][px + tap] on three
+        // bf16 pieces per operand (six products, as the 1x1 convs): 16-bit operands may be
+        // MN-major, so x's pieces stay in one NHWC copy and every tap's row and column shift
+        // is a box coordinate.  The bias-gradient partials, when asked for, come from the
+        // same read of grad_output as its pieces.
+        if (gbp)
+            s = launch_bias_grad_partials(gy, gbp, d->N, Co, p.Ho, p.Wo, p.S, p.Wl, p.Sh, p.Hlo, btmp, st, gp, psg,
+                                          nullptr);
+        else
+            s = launch_prep_pieces(gy, gp, (long long)ng, psg, st);
+        if (s) return s;
+        const long long blocks = (long long)d->N * d->H * ((d->W + 31) / 32);
+        if (blocks > 0x7fffffffLL) return HC_ERR_UNSUPPORTED;
+        prep_pieces_nhwc_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, xp, Ci, d->H, d->W);
+        if ((s = launched("prep_pieces_nhwc_kernel", st))) return s;
         TcParams tp{};
         tp.mode = 1;
+        tp.fmt = 1;
+        tp.bmn = 1;
         tp.Co = Co;
         tp.Ci = Ci;
         tp.S = p.Q;
@@ -1675,7 +1807,7 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.own_h = p.Hlo;
         tp.J = tc_wgrad_splits(d, p);
         tp.own_w = p.Wl;
-        tp.row_chunks = p.Wl / BK;
+        tp.row_chunks = p.Wl / BKH;
         tp.Ho = p.Ho;
         tp.kh = K;
         tp.kw = K;
@@ -1684,13 +1816,14 @@ hc_status launch_tc_bwd(const hc_conv_desc* d, const Plan& p, const float* x, co
         tp.mblocks = Co / BM;
         tp.nblocks = Ci / WG_SLOT;
         tp.slots = KK * tp.nblocks;
+        tp.kvalid = Ci;
         tp.shard_chunks = (long long)d->N * p.Hlo * tp.row_chunks;
         tp.units = tp.mblocks * ((tp.slots + 1) / 2) * tp.J * p.Q;
         tp.part = part;
         tp.N = d->N;
         CUtensorMap ma, mb;
-        if ((s = rows_map(&ma, gch, gcl, d->N, Co, p.Ho, p.Wo, BM)) ||
-            (s = shifted_map(&mb, sh, sl, d->N, Ci, d->H, Wc, WG_SLOT, copies)))
+        if ((s = pieces_rows_map(&ma, gp, d->N, Co, p.Ho, p.Wo, BM, psg)) ||
+            (s = pieces_nhwc_map(&mb, xp, d->N, Ci, d->H, d->W)))
             return s;
         if ((s = launch_conv_pass(WG_BN, ma, mb, tp, st))) return s;
         wgrad_reduce_kernel<<<(unsigned)(p.Q * Co), 256, 0, st>>>(part, gwp, tp.J, KK, Co, Ci);
