@@ -885,6 +885,139 @@ def run_peaks(args):
     return 0
 
 
+def run_exchange(args):
+    """--exchange (N ranks under torchrun): the pages' multi-device form of the
+    depthwise workload.  Rank r holds column block r (N,256,128,512) of an
+    (N,256,128,512*ranks) image in the halo-padded layout, exchanges its edge
+    columns with its neighbours (NCCL on device tensors when every rank has a
+    device of its own; else gloo through host memory -- ranks that share a
+    device run independent kernels, none waits on another) while its interior
+    column tiles run, then its edge tiles; the _Partial weight and bias
+    gradients are gathered and summed in rank order on every rank
+    (spatially_sharded_cnn_gb300.exchange).  Weak scaling: value = the
+    algorithmic bytes of all ranks (20 B per element of a block) / the slowest
+    rank's step time.  --check compares every rank's block with the one-device
+    call on the whole image: forward and grad_input bit for bit, weight and
+    bias gradients within 1e-5 (the rank-order sum splits the partials at other
+    points than the shard-order sum)."""
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world < 2:
+        raise SystemExit("--exchange needs two or more ranks (torchrun)")
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    ndev = torch.cuda.device_count()
+    backend = "nccl" if ndev >= world else "gloo"
+    torch.cuda.set_device(local % ndev)
+    dev = torch.device("cuda", local % ndev)
+    if backend == "nccl":
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        dist.init_process_group("gloo")
+    from spatially_sharded_cnn_gb300 import hc
+    from spatially_sharded_cnn_gb300.exchange import RankConv, padded_shape, HALO
+    N, C, H, Wl, K = (args.batch or 7), 256, 128, 512, 7
+    cfg = dict(N=N, C_in=C, H=H, W=Wl * world, C_out=C, kh=K, kw=K, stride=1, padding=3, groups=C,
+               num_shards=world)
+    d = hc.desc(cfg)
+    conv = RankConv(cfg)
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)  # this rank's block of the synthetic image and of grad_output
+    x_pad = torch.zeros(padded_shape(cfg), device=dev)
+    gy_pad = torch.zeros(padded_shape(cfg), device=dev)
+    x_pad[..., HALO:HALO + Wl] = torch.randn((N, C, H, Wl), generator=g, device=dev)
+    gy_pad[..., HALO:HALO + Wl] = torch.randn((N, C, H, Wl), generator=g, device=dev)
+    gw0 = torch.Generator(device=dev)
+    gw0.manual_seed(7)  # replicated weights: the same on every rank
+    w = torch.randn((C, 1, K, K), generator=gw0, device=dev) * 0.02
+    b = torch.randn((C,), generator=gw0, device=dev) * 0.01
+    y = torch.empty((N, C, H, Wl), device=dev)
+    gx = torch.empty_like(y)
+    gwt, gbt = torch.empty_like(w), torch.empty_like(b)
+    st, nb = hc.hc_conv2d_workspace_size_rank(d)
+    hc.check(st, "rank workspace")
+    ws = torch.empty(nb // 4 + 64, device=dev)
+
+    def step():
+        conv.forward(x_pad, w, b, y, stream)
+        conv.backward(x_pad, w, gy_pad, gx, gwt, gbt, ws, nb, stream)
+
+    def slowest(ms):
+        t = torch.tensor([ms], dtype=torch.float64, device=dev if backend == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    hc.check(hc.hc_sync_check(stream), "warmup")
+    clocks = ClockSampler(local % ndev)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    n0 = hc.hc_launch_count()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    dist.barrier()
+    launches = hc.hc_launch_count() - n0
+    clk = clocks.stop()
+    hc.check(hc.hc_sync_check(stream), "timed region")
+    # the exchange waits on the host (gloo) or in NCCL's streams, so a rank's step is
+    # its wall time; the device events give the same on the NCCL path
+    ms_step = slowest(max(e0.elapsed_time(e1), wall_ms) / args.steps)
+    E = N * C * H * Wl
+    value = world * 20.0 * E / (ms_step * 1e-3) / 1e9
+    check = None
+    if args.check:
+        def gather(t):  # every rank's block, concatenated along W on every rank
+            part = t.contiguous().to("cpu")
+            parts = [torch.empty_like(part) for _ in range(world)]
+            dist.all_gather(parts, part)
+            return torch.cat(parts, dim=3).to(dev)
+        xf, gyf = gather(x_pad[..., HALO:HALO + Wl]), gather(gy_pad[..., HALO:HALO + Wl])
+        yf, gxf = gather(y), gather(gx)
+        y1, gx1 = torch.empty_like(yf), torch.empty_like(gxf)
+        gw1, gb1 = torch.empty_like(w), torch.empty_like(b)
+        st1, nb1 = hc.hc_conv2d_workspace_size(d, 1)
+        hc.check(st1, "workspace")
+        ws1 = torch.empty(nb1 // 4 + 64, device=dev)
+        hc.check(hc.hc_conv2d_fwd(d, xf, w, b, y1, None, 0, stream), "one-device fwd")
+        hc.check(hc.hc_conv2d_bwd(d, xf, w, gyf, gx1, gw1, gb1, None, None, ws1, nb1, stream), "one-device bwd")
+        hc.check(hc.hc_sync_check(stream), "check")
+        nw = lambda a, r: float((a - r).abs().max() / r.abs().max())
+        check = {"y_bit_identical": bool(torch.equal(yf, y1)), "gx_bit_identical": bool(torch.equal(gxf, gx1)),
+                 "gw_normwise": nw(gwt, gw1), "gb_normwise": nw(gbt, gb1)}
+    if rank == 0:
+        peaks = load_peaks()
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": min(world, ndev), "ranks": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"depthwise 7x7 p3 groups=C fwd+bwd, {world} ranks each holding one column "
+                                       f"block ({N},{C},{H},{Wl}) of a ({N},{C},{H},{Wl * world}) image; halo "
+                                       f"exchange over {backend} with the interior tiles during the transfer; "
+                                       "partials gathered and summed in rank order",
+                           "exchange": backend, "shape_per_rank": [N, C, H, Wl],
+                           "l2": "inputs (470 MB each per rank at N = 7) larger than L2; no flush"},
+                "hbm_frac": value / min(world, ndev) / peaks["hbm"], "e2e": None,
+                "e2e_note": "device-resident inputs only in this mode",
+                "gpu_launches": launches, "clocks": clk}
+        if check is not None:
+            line["check"] = check
+        print(json.dumps(line), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -901,12 +1034,19 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="replay each fwd+bwd step from one captured CUDA graph (single-conv workloads)")
     ap.add_argument("--batch", type=int, default=None, help="batch size of every workload but config1 (default 7)")
+    ap.add_argument("--exchange", action="store_true",
+                    help="with N ranks under torchrun: the depthwise workload W-sharded across the ranks, halo "
+                         "exchange and rank-order partial sums (default: N independent replicas)")
+    ap.add_argument("--check", action="store_true",
+                    help="--exchange: compare every rank's block with the one-device call on the whole image")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.workload == "peaks":
         return run_peaks(args)
     if args.impl == "reference":
         return run_reference(args)
+    if args.exchange:
+        return run_exchange(args)
     wl = make_workload(args.workload, args.batch, args.drop_path, args.shards_h)
 
     import torch

@@ -20,7 +20,10 @@ each way:
   column tiles run (hc_conv2d_*_rank, HC_TILES_INTERIOR) while the transfer is
   in flight, the edge tiles after it;
 * host tensors (a gloo group, e.g. CPU ranks): the same messages, packed and
-  unpacked on the host.
+  unpacked on the host;
+* device tensors in a gloo group (ranks that share a device, or a host without
+  NCCL): packed and unpacked by the library, the messages staged through host
+  memory.
 
 The partial gradients are gathered from every rank and summed in rank order
 (hc_sum_partials on the device), so every rank holds the same, deterministic
@@ -59,6 +62,7 @@ class RankHalo:
         self.Wl = cfg["W"] // self.world
         self.rows = cfg["N"] * cfg["C_in"] * cfg["H"]
         self._hc = None
+        self.gloo = dist.get_backend(group) == "gloo"  # device messages go through host memory
 
     # -- peers ------------------------------------------------------------
     def _peer(self, r):
@@ -101,10 +105,16 @@ class RankHalo:
         """Pack this block's edge columns and post the sends to, and receives
         from, both neighbours.  Returns the pending exchange for finish()."""
         ops, recv = [], {}
+        staged = self.gloo and t_pad.is_cuda
+        if staged:
+            stream = self._st(t_pad, stream)
         for side, nb in ((0, self.rank - 1), (1, self.rank + 1)):
             if 0 <= nb < self.world:
                 send = self._pack(t_pad, side, stream)
-                rbuf = torch.empty((self.rows, HALO), dtype=torch.float32, device=t_pad.device)
+                if staged:  # the packed columns to the host (the pack must finish first)
+                    with torch.cuda.stream(stream):
+                        send = send.to("cpu")
+                rbuf = torch.empty((self.rows, HALO), dtype=torch.float32, device="cpu" if staged else t_pad.device)
                 ops.append(dist.P2POp(dist.isend, send, self._peer(nb), self.group))
                 ops.append(dist.P2POp(dist.irecv, rbuf, self._peer(nb), self.group))
                 recv[side] = (send, rbuf)
@@ -118,8 +128,17 @@ class RankHalo:
         works, recv = pending
         for w in works:
             w.wait()
+        staged = self.gloo and t_pad.is_cuda
+        if staged:
+            stream = self._st(t_pad, stream)
         for side in (0, 1):
-            self._unpack(recv[side][1] if side in recv else None, side, t_pad, stream)
+            buf = recv[side][1] if side in recv else None
+            if staged and buf is not None:
+                with torch.cuda.stream(stream):
+                    buf = buf.to(t_pad.device)
+            if staged and buf is None:  # the image edge: zeros into the margin
+                buf = torch.zeros((self.rows, HALO), dtype=torch.float32, device=t_pad.device)
+            self._unpack(buf, side, t_pad, stream)
 
     def exchange(self, t_pad, stream=None):
         self.finish(self.start(t_pad, stream), t_pad, stream)
@@ -129,11 +148,22 @@ class RankHalo:
         """The full gradient from every rank's _Partial one: gathered, then
         summed in rank order (the same sum on every rank); into `out` if given."""
         flat = part.reshape(-1).contiguous()
+        if out is None:
+            out = torch.empty_like(part)
+        if flat.is_cuda and self.gloo:  # gathered through host memory, summed on the device
+            stream = self._st(flat, stream)
+            with torch.cuda.stream(stream):
+                host = flat.to("cpu")
+            g_host = torch.empty((self.world, flat.numel()), dtype=flat.dtype)
+            dist.all_gather(list(g_host.unbind(0)), host, group=self.group)
+            with torch.cuda.stream(stream):
+                gathered = g_host.to(flat.device)
+            hc = self._lib()
+            hc.check(hc.hc_sum_partials(gathered, self.world, flat.numel(), out, stream), "sum partials")
+            return out
         gathered = torch.empty((self.world, flat.numel()), dtype=flat.dtype, device=flat.device)
         dist.all_gather_into_tensor(gathered, flat, group=self.group) if flat.is_cuda else \
             dist.all_gather(list(gathered.unbind(0)), flat, group=self.group)
-        if out is None:
-            out = torch.empty_like(part)
         if flat.is_cuda:
             hc = self._lib()
             hc.check(hc.hc_sum_partials(gathered, self.world, flat.numel(), out, self._st(out, stream)),
