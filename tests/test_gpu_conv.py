@@ -267,6 +267,35 @@ def test_bf16x6_dyadic_exact(hc, orc, cfg):
     assert np.array_equal(out["gw_partials"], gwp_ref.astype(np.float32))
 
 
+@pytest.mark.parametrize("cfg", [P.cfg_of(1, 128, 6, 256, 128, 5, 1, 2, 1, 2),
+                                 P.cfg_of(1, 256, 5, 256, 128, 3, 1, 1, 1, 2),
+                                 P.cfg_of(1, 128, 4, 512, 128, 7, 1, 3, 1, 4),
+                                 dict(P.cfg_of(1, 128, 8, 256, 128, 5, 1, 2, 1, 2), num_shards_h=2)])
+def test_tc_kxk_dyadic_exact(hc, orc, cfg):
+    """K x K convs on the tensor-core path (3xTF32 conv passes, the weight gradient
+    on bf16 pieces with every tap's shift a box coordinate), on multiples of 1/4 in
+    [-4, 4]: every split and every fp32 sum is exact, so forward, grad_input,
+    grad_weight and the per-shard partials equal the oracle bit for bit -- a tap
+    read from a wrong row or column, or a slot written to the wrong tap or channel
+    block, would show (5x5 over 2 shards, 3x3 with two 128-channel blocks, 7x7 over
+    4 shards, a 2 x 2 grid)."""
+    Ho, Wo = R.out_hw(cfg)
+    x = synth.dyadic((cfg["N"], cfg["C_in"], cfg["H"], cfg["W"]), 2, 4, 9, 1)
+    w = synth.dyadic((cfg["C_out"], cfg["C_in"], cfg["kh"], cfg["kw"]), 2, 4, 9, 2)
+    b = synth.dyadic((cfg["C_out"],), 2, 4, 9, 3)
+    gy = synth.dyadic((cfg["N"], cfg["C_out"], Ho, Wo), 2, 4, 9, 4)
+    algo = hc.HC_ALGO_TC_3XTF32
+    assert hc.hc_conv2d_select(hc.desc(cfg), 1) == (0, algo)
+    assert np.array_equal(R.fwd(cfg, x, w, b, algo), orc.conv2d_fwd(cfg, x, w, b))
+    out = R.bwd(cfg, x, w, gy, algo)
+    assert np.array_equal(out["gx"], orc.conv2d_bwd_input(cfg, w, gy))
+    assert np.array_equal(out["gw"], orc.conv2d_bwd_weight(cfg, x, gy))
+    assert np.array_equal(out["gb"], orc.conv2d_bwd_bias(cfg, gy))
+    _, gwp_ref, gbp_ref = orc.sharded_bwd(cfg, x, w, gy)
+    assert np.array_equal(out["gw_partials"], gwp_ref.astype(np.float32))
+    assert np.array_equal(out["gb_partials"], gbp_ref.astype(np.float32))
+
+
 @pytest.mark.parametrize("want", [("gx",), ("gw",), ("gb",), ("gw", "gb"), ("gw_partials", "gb_partials"),
                                   ("gx", "gb_partials")])
 @pytest.mark.parametrize("name", ["config1_dense5x5", "dw7_ragged_S4", "tc_5x5_S2", "tc_down2x2s2_S2"])
