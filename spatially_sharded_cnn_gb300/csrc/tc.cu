@@ -22,26 +22,29 @@
 //          activation in NHWC (channels contiguous), one 4-D TMA box per
 //          (tap, chunk).
 //   wgrad  G[co][ci] of one tap = sum over a shard's pixels of
-//          gy[co][px] * x[ci][px + tap]; A = grad_output, B = one of four
-//          copies of x shifted right by 0..3 columns, so that every tap's
-//          column shift starts on a 16-byte boundary (a TMA box's innermost
-//          coordinate must); row shifts and padding come from the box's
-//          coordinates and zero fill.  Both are stored row-interleaved,
-//          [N][H][C][W] (pixels contiguous, the channels of one image row
-//          together), so one 128-channel box spans 128 rows of W floats
-//          rather than 128 channel planes.  A unit covers two (tap,
-//          128-channel) slots side by side: N = 256 accumulator columns.
-// All operands are K-major tiles with the 128-byte swizzle (32 tf32 per row).
+//          gy[co][px] * x[ci][px + tap], on bf16 pieces (below): A =
+//          grad_output's pieces (pixels contiguous, K-major), B = x's pieces
+//          in a channel-blocked NHWC copy read as MN-major tiles, so a tap's
+//          row and column shift are box coordinates on dimensions that are
+//          not the innermost one (which must start on a 16-byte boundary),
+//          with zero fill past the image.  A unit covers two (tap,
+//          128-channel) slots side by side, each its own box and its own
+//          N = 128 MMAs (256 accumulator columns).  (A space-to-depth conv
+//          on this path keeps a tf32 weight gradient over planar copies.)
+// The tf32 operands are K-major tiles with the 128-byte swizzle (32 tf32 per
+// row): kind::tf32 takes no MN-major operands on this part.
 //
-// 1x1 convolutions (stride 1, no padding) take a second operand format: every
+// 1x1 convolutions (stride 1, no padding), k = stride convs and the weight
+// gradient of K x K convs take a second operand format: every
 // value is split into three bf16 pieces, a = a0 + a1 + a2 with a0 = bf16(a),
 // a1 = bf16(a - a0), a2 = bf16(a - a0 - a1) (both differences are exact in
 // fp32), and each product is taken as the six terms a_i*b_j with i + j <= 2
 // (the dropped terms are below 2^-24 of |a*b|).  Six bf16 MMAs cost the tensor
 // time of three tf32 ones, and 16-bit operands may be MN-major, so the pieces
-// keep the NCHW order of the tensors they come from: the conv passes read
-// pixels as MN-major B tiles, the weight gradient reads them as K-major tiles,
-// and no pass needs a transposed copy.
+// of the 1x1 and space-to-depth convs keep the NCHW order of the tensors they
+// come from: their conv passes read pixels as MN-major B tiles, their weight
+// gradient reads them as K-major tiles, and no pass needs a transposed copy.
+// The K x K weight gradient reads x's pieces from one NHWC copy (above).
 //
 // Accuracy: the tensor core's fp32 accumulation loses about one unit in the
 // last place per MMA step, so a long K would lose ~1e-5.  The MMA warp
@@ -773,39 +776,6 @@ hc_status launch_split_rows(const float* x, float* hi, float* lo, int N, int C, 
     return launched("prep_split_rows_kernel", st);
 }
 
-// Column-shifted tf32 hi / lo copies of x for the weight gradient, row-interleaved:
-// c[j][n][h][c][i] = x[n][c][h][i - j] (zero outside [0, W)), j = 0..3, i < Wc = W + 4.
-// A tap's column shift s is then read from copy (-s) mod 4 at a 16-byte-aligned
-// column.  One block per input row: the row is staged in shared memory once
-// and the four shifted rows are written with 16-byte stores.
-__global__ void prep_shift_kernel(const float* __restrict__ x, float* __restrict__ hi, float* __restrict__ lo,
-                                  long long rows, int C, int H, int W, int Wc, int copies) {
-    extern __shared__ float rowbuf[];  // [Wc + 4]: 4 zeros, the row, zeros
-    const long long row = blockIdx.x;  // (n * C + c) * H + h
-    const float* src = x + row * W;
-    const long long nc = row / H;
-    const long long orow = (nc / C * H + row % H) * C + nc % C;  // (n * H + h) * C + c
-    for (int i = threadIdx.x; i < Wc + 4; i += blockDim.x) {
-        const int c = i - 4;
-        rowbuf[i] = (c >= 0 && c < W) ? __ldg(src + c) : 0.0f;
-    }
-    __syncthreads();
-    const int v4 = Wc / 4;
-    for (int q = threadIdx.x; q < copies * v4; q += blockDim.x) {
-        const int j = q / v4, i0 = (q - j * v4) * 4;
-        // element i of copy j is x[i - j] = rowbuf[i - j + 4]
-        float4 h, l;
-        const float a = rowbuf[i0 - j + 4], b = rowbuf[i0 - j + 5], c = rowbuf[i0 - j + 6], d = rowbuf[i0 - j + 7];
-        h.x = tf32_rna(a); l.x = tf32_rna(a - h.x);
-        h.y = tf32_rna(b); l.y = tf32_rna(b - h.y);
-        h.z = tf32_rna(c); l.z = tf32_rna(c - h.z);
-        h.w = tf32_rna(d); l.w = tf32_rna(d - h.w);
-        const long long o = ((long long)j * rows + orow) * Wc + i0;
-        *reinterpret_cast<float4*>(hi + o) = h;
-        *reinterpret_cast<float4*>(lo + o) = l;
-    }
-}
-
 // Space-to-depth for a k = stride = s convolution without padding (each output
 // pixel reads one s x s block): channel k = (u*s + v)*C + c of output pixel
 // (ho, wo) is x[c][ho*s + u][wo*s + v]; channels k >= s*s*C are zero.
@@ -1435,10 +1405,6 @@ bool is_s2d(const hc_conv_desc* d) {
     return d->groups == 1 && d->stride >= 2 && d->kh == d->stride && d->kw == d->stride && d->padding == 0;
 }
 int s2d_kp(const hc_conv_desc* d) { return (d->stride * d->stride * d->C_in + 127) / 128 * 128; }
-// Shifted copies the weight gradient reads: a 1-wide kernel never shifts.
-int shift_copies(const hc_conv_desc* d) { return d->kw == 1 ? 1 : 4; }
-// Row pitch of the shifted copies: a column shift of up to 3 needs 4 spare columns.
-int shift_pitch(const hc_conv_desc* d) { return d->kw == 1 ? d->W : d->W + 4; }
 
 }  // namespace
 
