@@ -1024,7 +1024,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="end-to-end steps (two buffer sets in turn: more steps amortise the first copy-in and the last copy-out)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=WORKLOADS + ["peaks"], default="dw7")
     ap.add_argument("--shards-h", type=int, default=1,
