@@ -713,6 +713,61 @@ __global__ void dw_shard_partials_kernel(const float* __restrict__ tile_part, fl
 }
 
 
+// The same sums with one lane per shard: lanes r = 0..Q-1 of one (c, k) group
+// (Q divides 32, so a group never straddles a warp) each add their shard's
+// slots in order and write gwp / gbp, then the group's lane 0 gathers the Q
+// shard sums by shuffles and adds them from shard 0 up -- the order of
+// dw_shard_partials_kernel, with Q times the threads in flight.
+__global__ void dw_shard_partials_lanes_kernel(const float* __restrict__ tile_part, float* __restrict__ gwp,
+                                               float* __restrict__ gbp, float* __restrict__ gw,
+                                               float* __restrict__ gb, int Q, int C, int rows, int KK) {
+    constexpr int B = 16;  // loads in flight per thread
+    const long long total = (long long)C * (KK + 1) * Q;
+    const int lane = threadIdx.x & 31;
+    // every lane of a warp runs the same number of iterations (total is a multiple of Q,
+    // and of the whole grid's stride only by chance), so the shuffles see the whole group
+    for (long long base = (long long)blockIdx.x * blockDim.x; base < total; base += (long long)gridDim.x * blockDim.x) {
+        const long long t = base + threadIdx.x;
+        const bool live = t < total;
+        const int r = (int)(t % Q);
+        const long long ck = t / Q;
+        const int k = (int)(ck % (KK + 1));
+        const int c = (int)(ck / (KK + 1));
+        float s = 0.0f;
+        if (live) {
+            const float* src = tile_part + ((long long)r * C + c) * rows * (KK + 1) + k;
+            for (int m0 = 0; m0 < rows; m0 += B) {
+                float v[B];
+#pragma unroll
+                for (int i = 0; i < B; i++) v[i] = m0 + i < rows ? __ldg(src + (long long)(m0 + i) * (KK + 1)) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < B; i++)
+                    if (m0 + i < rows) s += v[i];
+            }
+            const long long rc = (long long)r * C + c;
+            if (k < KK) {
+                if (gwp) gwp[rc * KK + k] = s;
+            } else if (gbp) {
+                gbp[rc] = s;
+            }
+        }
+        // the group's lane 0 adds the shard sums in order
+        float tot = s;
+        const int g0 = lane - r;  // this group's first lane
+        for (int j = 1; j < Q; j++) {
+            const float o = __shfl_sync(0xffffffffu, s, g0 + j);
+            if (r == 0) tot += o;
+        }
+        if (live && r == 0) {
+            if (k < KK) {
+                if (gw) gw[(long long)c * KK + k] = tot;
+            } else if (gb) {
+                gb[c] = tot;
+            }
+        }
+    }
+}
+
 // Tensor map of an NCHW fp32 tensor viewed as [N*C][H][pitch] (pitch 0: W),
 // box = one staged tile.
 template <int K, int WARPS>
@@ -822,6 +877,13 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
 
 hc_status launch_shard_partials(const float* tile_part, float* gwp, float* gbp, float* gw, float* gb, int Q, int C,
                                 int rows, int KK, cudaStream_t st) {
+    if (Q > 1 && 32 % Q == 0) {  // one lane per shard
+        const long long total = (long long)C * (KK + 1) * Q;
+        long long blocks = (total + 127) / 128;
+        if (blocks > 152LL * 16) blocks = 152LL * 16;
+        dw_shard_partials_lanes_kernel<<<(unsigned)blocks, 128, 0, st>>>(tile_part, gwp, gbp, gw, gb, Q, C, rows, KK);
+        return launched("dw_shard_partials_kernel", st);
+    }
     const long long total = (long long)C * (KK + 1);
     // small blocks: the few thousand threads spread over all the SMs
     dw_shard_partials_kernel<<<(unsigned)((total + 63) / 64), 64, 0, st>>>(tile_part, gwp, gbp, gw, gb, Q, C, rows,
