@@ -383,6 +383,47 @@ __global__ void __launch_bounds__(FWD_WARPS * 32, FWD_CTAS)
 }
 
 // ---- backward ---------------------------------------------------------------
+// Job cursor of the backward with row shards.  A CTA's jobs go run by run (a run:
+// its items of one (c, column tile), n fastest), within a run row shard by row
+// shard, within a row shard item by item and, per item, over the row shard's
+// tpr row tiles; the weight gradient of one (run, row shard) is flushed at its
+// last job.  Advanced one job at a time: one decode per run, no per-job division.
+struct RowJobs {
+    int item, seg, tt;  // this job: item, row shard, row tile within the row shard
+    int rs, re;         // this run's items [rs, re)
+    int n, c, ct;       // the item's coordinates
+    int n_rs;           // the image of item rs
+    __device__ __forceinline__ void start(const Sched& sc, int i0, int i1) {
+        rs = i0;
+        const int e = (i0 / sc.N + 1) * sc.N;
+        re = e < i1 ? e : i1;
+        item = rs;
+        seg = tt = 0;
+        sc.decode(rs, n, c, ct);
+        n_rs = n;
+    }
+    __device__ __forceinline__ int t(int tpr) const { return seg * tpr + tt; }
+    __device__ __forceinline__ bool seg_end(int tpr) const { return item == re - 1 && tt == tpr - 1; }
+    __device__ __forceinline__ void advance(const Sched& sc, int Sh, int tpr, int i1) {
+        if (++tt < tpr) return;
+        tt = 0;
+        if (++item < re) {  // the next image of the run (n fastest)
+            ++n;
+            return;
+        }
+        item = rs;
+        n = n_rs;
+        if (++seg < Sh) return;  // the run again, in the next row shard
+        seg = 0;
+        rs = re;  // the next run starts on a run boundary
+        if (rs >= i1) return;  // past the CTA's last job
+        re = rs + sc.N < i1 ? rs + sc.N : i1;
+        item = rs;
+        sc.decode(rs, n, c, ct);
+        n_rs = n;
+    }
+};
+
 struct BwdArgs {
     const float* w;
     float* gx;
@@ -427,39 +468,23 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     }
     const bool want_wb = a.want_wb != 0;
 
-    // Job q -> (item, row tile t).  Items run (c, column tile, n), n fastest; a
-    // run is this CTA's jobs of one (c, column tile).  Without row shards the
-    // jobs go item by item, tile by tile.  With row shards a run's jobs go row
-    // shard by row shard, each over all the run's images, so the weight
-    // gradient of one (run, row shard) accumulates in registers and is flushed
-    // once; seg_end marks the last job of such a segment.
-    auto job = [&](int q, int& item, int& t, bool& seg_end) {
-        if (!ROWS) {
-            item = i0 + q / ntiles;
-            t = q - (item - i0) * ntiles;
-            seg_end = false;
-            return;
-        }
-        const int g = (i0 + q / ntiles) / sc.N;
-        const int rs = i0 > g * sc.N ? i0 : g * sc.N, re = i1 < (g + 1) * sc.N ? i1 : (g + 1) * sc.N;
-        const int R = re - rs, tpr = ntiles / a.Sh;
-        const int jr = q - (rs - i0) * ntiles;
-        const int seg = jr / (R * tpr), rest = jr - seg * R * tpr;
-        item = rs + rest / tpr;
-        t = seg * tpr + rest % tpr;
-        seg_end = rest == R * tpr - 1;
-    };
+    // Jobs: items run (c, column tile, n), n fastest; a run is this CTA's jobs of
+    // one (c, column tile).  Without row shards the jobs go item by item, tile by
+    // tile; with row shards as RowJobs walks them.
+    const int tpr = ntiles / a.Sh;  // row tiles per row shard (row shards only)
 
-    // Thread 0 issues the jobs in order; without row shards its cursor (in_, ic,
-    // ict, it) advances one job at a time (no divisions).
+    // Thread 0 issues the jobs in order; its cursor ((in_, ic, ict, it), or rj with
+    // row shards) advances one job at a time (no divisions).
     int in_ = 0, ic = 0, ict = 0, it = t0;
+    RowJobs rj{};
     if (!ROWS) sc.decode(i0, in_, ic, ict);
+    else rj.start(sc, i0, i1);
     auto issue = [&](int q) {
-        int n, c, ct, item, t;
+        (void)q;
+        int n, c, ct, t;
         if (ROWS) {
-            bool se;
-            job(q, item, t, se);
-            sc.decode(item, n, c, ct);
+            n = rj.n, c = rj.c, ct = rj.ct, t = rj.t(tpr);
+            rj.advance(sc, a.Sh, tpr, i1);
         } else {
             n = in_, c = ic, ct = ict, t = it;
             if (++it == ntiles) {
@@ -491,13 +516,14 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         // without row shards: job q's item (n, c, ct) and row tile t, advanced one job at a time
         int n, c, ct, t = t0, s = 0;
         unsigned ph = 0;  // phase of stage s's barrier this job waits for
+        RowJobs cur{};
         if (!ROWS) sc.decode(i0, n, c, ct);
+        else cur.start(sc, i0, i1);
         for (int q = 0; q < jobs; q++) {
             bool flush;
             if (ROWS) {
-                int item;
-                job(q, item, t, flush);  // the last job of a (run, row shard) segment
-                sc.decode(item, n, c, ct);
+                n = cur.n, c = cur.c, ct = cur.ct, t = cur.t(tpr);
+                flush = cur.seg_end(tpr);  // the last job of a (run, row shard) segment
             } else {
                 // the last job of a run: the CTA's last job, or the last row tile of
                 // image N - 1 (the next job is another (c, column tile))
@@ -519,7 +545,9 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                 s = 0;
                 ph ^= 1u;
             }
-            if (!ROWS && ++t == ntiles) {
+            if (ROWS) {
+                cur.advance(sc, a.Sh, tpr, i1);
+            } else if (++t == ntiles) {
                 t = 0;
                 sc.next(n, c, ct);
             }
