@@ -192,11 +192,14 @@ __device__ __forceinline__ void correlate_4x4(const float* sm, int row0, int lan
 struct Sched {
     int N, C, H, W, col_tiles, items;
     // item order.  1: (c, n, column tile), contiguous ranges per CTA.  0: (c, column
-    // tile, n), contiguous ranges per CTA.  2: CTA b keeps column tile b % col_tiles
-    // and walks (c, n), n fastest; the col_tiles CTAs of a group share one contiguous
-    // (c, n) range, so neighbouring tiles read their common halo strips at about the
-    // same time (L2 hits) while each CTA's runs of one (c, column tile) stay whole.
+    // tile, n), contiguous ranges per CTA.  2: the column tiles in blocks of tb; CTA b
+    // keeps tile b % tb of a block and walks (tile block, c, n), n fastest; the tb CTAs
+    // of a group share one contiguous range of that sequence, so neighbouring tiles
+    // read their common halo strips at about the same time (L2 hits) while each CTA's
+    // runs of one (c, column tile) stay whole.  (tb divides col_tiles and the grid is
+    // a multiple of tb.)
     int tile_fastest;
+    int tb;
     // The column tiles the items cover: tile k (0 <= k < col_tiles) is column tile
     // ct_base + k * ct_step of the output (all of them: 0, 1; a rank's interior or
     // edge tiles: see the rank entry points).  xo: the column of the x (and
@@ -207,8 +210,9 @@ struct Sched {
     __device__ __forceinline__ void decode(int item, int& n, int& c, int& ct) const {
         if (tile_fastest == 2) {
             n = item % N;
-            c = item / N;
-            ct = blockIdx.x % col_tiles;
+            const int rest = item / N;
+            c = rest % C;
+            ct = (rest / C) * tb + (int)blockIdx.x % tb;
         } else if (tile_fastest) {
             ct = item % col_tiles;
             const int rest = item / col_tiles;
@@ -226,7 +230,10 @@ struct Sched {
         if (tile_fastest == 2) {
             if (++n == N) {
                 n = 0;
-                ++c;
+                if (++c == C) {  // the next tile block
+                    c = 0;
+                    ct += tb;
+                }
             }
         } else if (tile_fastest) {
             if (++ct == col_tiles) {
@@ -248,16 +255,16 @@ struct Sched {
     // and the split falls between any two jobs (item = job / ntiles).
     __device__ __forceinline__ void job_range(int ntiles, long long& j0, long long& j1) const {
         const bool grouped = tile_fastest == 2;
-        const long long total = (grouped ? (long long)N * C : (long long)items) * ntiles;
-        const int idx = grouped ? (int)blockIdx.x / col_tiles : (int)blockIdx.x;
-        const int parts = grouped ? (int)gridDim.x / col_tiles : (int)gridDim.x;
+        const long long total = (grouped ? (long long)N * C * (col_tiles / tb) : (long long)items) * ntiles;
+        const int idx = grouped ? (int)blockIdx.x / tb : (int)blockIdx.x;
+        const int parts = grouped ? (int)gridDim.x / tb : (int)gridDim.x;
         j0 = idx * total / parts;
         j1 = (idx + 1) * total / parts;
     }
     __device__ __forceinline__ void range(int& i0, int& i1) const {
-        if (tile_fastest == 2) {  // items here index (c, n) of the CTA's own column tile
-            const int g = blockIdx.x / col_tiles, groups = gridDim.x / col_tiles;
-            const long long per = (long long)N * C;
+        if (tile_fastest == 2) {  // items here index (tile block, c, n) of the CTA's own tile in each block
+            const int g = blockIdx.x / tb, groups = gridDim.x / tb;
+            const long long per = (long long)N * C * (col_tiles / tb);
             i0 = (int)(g * per / groups);
             i1 = (int)((g + 1) * per / groups);
             return;
@@ -576,7 +583,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                         sc.next(n2, c2, ct2);
                     }
                     const int h2 = t2 * TH + warp * 8 + (lane >> 2);
-                    if (c2 < sc.C && h2 < sc.H) {
+                    if (c2 < sc.C && ct2 < sc.col_tiles && h2 < sc.H) {  // not past the CTA's last item
                         const float* pf = a.gres + ((long long)(n2 * sc.C + c2) * sc.H + h2) * sc.W +
                                           sc.col(ct2) * TW + (lane & 3) * 32;
                         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pf));
@@ -816,7 +823,7 @@ long long bwd_slots(const hc_conv_desc* d, const Plan& p) {
 
 Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_sm, const DwLayout& lay) {
     const int T = d->W / TW;
-    Sched sc{d->N, d->C_in, d->H, d->W, T, 0, tile_fastest, 0, 1, lay.xo};
+    Sched sc{d->N, d->C_in, d->H, d->W, T, 0, tile_fastest, 1, 0, 1, lay.xo};
     if (lay.tiles == HC_TILES_INTERIOR) {
         sc.ct_base = 1;
         sc.col_tiles = T > 2 ? T - 2 : 0;
@@ -828,14 +835,31 @@ Sched sched_of(const hc_conv_desc* d, int* grid, int tile_fastest, int ctas_per_
     const int g = device_sm_count() * ctas_per_sm;
     *grid = g < sc.items ? g : sc.items;
     if (tile_fastest == 2) {
-        // one group of col_tiles CTAs per (c, n) range; with more tiles than CTAs,
-        // runs of one (c, column tile) in contiguous ranges instead
-        const int groups = sc.col_tiles ? g / sc.col_tiles : 0;
-        const long long per = (long long)d->N * d->C_in;
-        if (groups >= 1)
-            *grid = (int)((groups < per ? groups : per) * sc.col_tiles);
-        else
+        // groups of tb CTAs: tb the largest divisor of col_tiles whose groups fill at
+        // least 96 % of the CTAs (few block edges, whose halo strips miss L2), else the
+        // divisor that fills the most; with none that fits, runs of one (c, column
+        // tile) in contiguous ranges instead
+        int best = 0, used = 0;
+        for (int t = sc.col_tiles; t >= 1; t--) {
+            if (sc.col_tiles % t) continue;
+            const int u = (g / t) * t;
+            if (u > 0 && (long long)u * 100 >= (long long)g * 96) {
+                best = t;
+                break;
+            }
+            if (u > used) {
+                used = u;
+                best = t;
+            }
+        }
+        if (best > 0) {
+            sc.tb = best;
+            const long long per = (long long)d->N * d->C_in * (sc.col_tiles / best);
+            const int groups = g / best;
+            *grid = (int)((groups < per ? groups : per) * best);
+        } else {
             sc.tile_fastest = 0;
+        }
     }
     return sc;
 }
