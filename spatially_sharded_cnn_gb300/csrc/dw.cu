@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     // tile; with row shards as RowJobs walks them.
     const int tpr = ntiles / a.Sh;  // row tiles per row shard (row shards only)
 
-    // Thread 0 issues the jobs in order; its cursor ((in_, ic, ict, it), or rj with
+    // The issuer thread issues the jobs in order; its cursor ((in_, ic, ict, it), or rj with
     // row shards) advances one job at a time (no divisions).
     int in_ = 0, ic = 0, ict = 0, it = t0;
     RowJobs rj{};
@@ -506,12 +506,15 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         tma_load_3d(st, &gymap, x0, y0, z, bar);
         if (want_wb) tma_load_3d(st + G::TILE, &xmap, x0, y0, z, bar);
     };
-    if (tid == 0) {
+    // the copies are issued by lane 0 of the first weight-gradient warp: the
+    // grad_input role is the longer one, so none of its warps waits on an issue
+    const int issuer = BWD_WARPS * 32;
+    if (tid == issuer) {
         for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
         fence_barrier_init();
     }
     __syncthreads();
-    if (tid == 0)
+    if (tid == issuer)
         for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
 
     // The ring, shared by both roles: every warp waits for job q's stage, does
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             }
             work(s, n, c, ct, t, flush);
             __syncthreads();  // every warp is done with this stage
-            if (tid == 0 && q + NSTAGE < jobs) issue(q + NSTAGE);
+            if (tid == issuer && q + NSTAGE < jobs) issue(q + NSTAGE);
             if (++s == NSTAGE) {
                 s = 0;
                 ph ^= 1u;
