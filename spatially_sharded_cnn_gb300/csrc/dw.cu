@@ -576,22 +576,6 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             },
             [&](int s, int n, int c, int ct, int t, bool) {
                 if (!a.gx) return;
-                if (RES && !ROWS) {
-                    // the next job's residual rows into L2 (one 128-byte line per lane: row
-                    // lane / 4 of this warp's eight, quarter lane % 4 of the 512-byte segment),
-                    // so this job's loads below are L2 hits rather than DRAM misses
-                    int n2 = n, c2 = c, ct2 = ct, t2 = t + 1;
-                    if (t2 == ntiles) {
-                        t2 = 0;
-                        sc.next(n2, c2, ct2);
-                    }
-                    const int h2 = t2 * TH + warp * 8 + (lane >> 2);
-                    if (c2 < sc.C && ct2 < sc.col_tiles && h2 < sc.H) {  // not past the CTA's last item
-                        const float* pf = a.gres + ((long long)(n2 * sc.C + c2) * sc.H + h2) * sc.W +
-                                          sc.col(ct2) * TW + (lane & 3) * 32;
-                        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pf));
-                    }
-                }
                 const float* gys = tiles + s * 2 * G::TILE;
                 const long long off = ((long long)(n * sc.C + c) * sc.H) * sc.W + sc.col(ct) * TW + 4 * lane;
                 float* gp = a.gx + off;
@@ -638,6 +622,23 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
         int run_m0 = -1;  // first slot of the current run
         ring([](int) {},
              [&](int s, int n, int c, int ct, int t, bool flush) {
+                 if (RES && !ROWS && a.gx) {
+                     // the next job's residual rows into L2 for the grad_input warp of the same
+                     // rows (the longer role): one 128-byte line per lane, row lane / 4 of the
+                     // warp's eight, quarter lane % 4 of the 512-byte segment, so that warp's
+                     // residual loads are L2 hits rather than DRAM misses
+                     int n2 = n, c2 = c, ct2 = ct, t2 = t + 1;
+                     if (t2 == ntiles) {
+                         t2 = 0;
+                         sc.next(n2, c2, ct2);
+                     }
+                     const int h2 = t2 * TH + wg * 8 + (lane >> 2);
+                     if (c2 < sc.C && ct2 < sc.col_tiles && h2 < sc.H) {  // not past the CTA's last item
+                         const float* pf = a.gres + ((long long)(n2 * sc.C + c2) * sc.H + h2) * sc.W +
+                                           sc.col(ct2) * TW + (lane & 3) * 32;
+                         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pf));
+                     }
+                 }
                  if (!want_wb) return;
                  const int m = ROWS ? n : n * ntiles + t;
                  if (run_m0 < 0) run_m0 = m;
