@@ -172,21 +172,32 @@ __global__ void __launch_bounds__(PW_WARPS * 32, 1)
                     else
                         gb0 += t;
                 }
+            // the image values of the 4 pixels: per channel, pixel p's four kw columns
+            float4 xv[PW_CI][4];
 #pragma unroll
-            for (int ci = 0; ci < PW_CI; ci++) {
-                const float* xr = xs + (ci * PW_K + kh) * (PW_PX * PW_K) + c4 * 16;
-                float4 xv[4];
+            for (int ci = 0; ci < PW_CI; ci++)
 #pragma unroll
-                for (int p = 0; p < 4; p++) xv[p] = *reinterpret_cast<const float4*>(xr + 4 * p);
+                for (int p = 0; p < 4; p++)
+                    xv[ci][p] = *reinterpret_cast<const float4*>(xs + (ci * PW_K + kh) * (PW_PX * PW_K) + c4 * 16 +
+                                                                 4 * p);
+            // acc[j][ci][kw] += gy[j][p] * x[ci][p][kw], kw in pairs (packed f32x2 FMAs: each
+            // lane one fused multiply-add, the same sums in the same order as scalar FMAs)
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const float g4[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+            for (int j = 0; j < 8; j++) {
+                const float g4[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
 #pragma unroll
-                    for (int p = 0; p < 4; p++) {
-                        acc[j][ci][0] = fmaf(g4[p], xv[p].x, acc[j][ci][0]);
-                        acc[j][ci][1] = fmaf(g4[p], xv[p].y, acc[j][ci][1]);
-                        acc[j][ci][2] = fmaf(g4[p], xv[p].z, acc[j][ci][2]);
-                        acc[j][ci][3] = fmaf(g4[p], xv[p].w, acc[j][ci][3]);
+                for (int p = 0; p < 4; p++) {
+                    const float2 gg = make_float2(g4[p], g4[p]);
+#pragma unroll
+                    for (int ci = 0; ci < PW_CI; ci++) {
+                        const float2 lo = __ffma2_rn(gg, make_float2(xv[ci][p].x, xv[ci][p].y),
+                                                     make_float2(acc[j][ci][0], acc[j][ci][1]));
+                        const float2 hi = __ffma2_rn(gg, make_float2(xv[ci][p].z, xv[ci][p].w),
+                                                     make_float2(acc[j][ci][2], acc[j][ci][3]));
+                        acc[j][ci][0] = lo.x;
+                        acc[j][ci][1] = lo.y;
+                        acc[j][ci][2] = hi.x;
+                        acc[j][ci][3] = hi.y;
                     }
                 }
             }
