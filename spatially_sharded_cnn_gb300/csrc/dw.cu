@@ -16,11 +16,11 @@
 // Kernels are persistent (a fixed number of CTAs per SM).  One thread streams the tiles in with
 // TMA (a 3-D box of rows h0-P .. h0+TH+P-1 and columns c0-4 .. c0+131 of one
 // plane; the box start is 16-byte aligned and out-of-image parts are
-// zero-filled by the copy engine) into a three-stage ring of shared-memory
-// buffers guarded by mbarriers.  In the forward pass the warps run through the
-// jobs independently and the last warp done with a stage refills it; in the
-// backward pass a CTA barrier ends each job and thread 0 then refills the
-// stage.  A warp that changes channel reads the weights from global memory.
+// zero-filled by the copy engine) into a ring of shared-memory buffers guarded
+// by mbarriers (three stages forward, two backward).  In the forward pass the
+// warps run through the jobs independently and the last warp done with a stage
+// refills it; in the backward pass a CTA barrier ends each job and one thread
+// then refills the stage.  A warp that changes channel reads the weights from global memory.
 // Every barrier wait is bounded: a CTA that gives up records HC_ERR_TIMEOUT in
 // a status word (read by hc_sync_check), waits for its own copies still in
 // flight, and returns.
@@ -29,12 +29,13 @@
 // floats (three 16-byte shared loads) and issues up to 7 * 4 * K FMAs with the
 // plane's K*K weights in registers.
 //
-// Backward (one kernel, 16 warps on one ring; both roles cover the same 8-row
-// blocks of each staged tile):
-//   warps 0-7   grad_input = the same stencil over the grad_output tile with the
+// Backward (one kernel, two 8-warp CTAs per SM, 32-row jobs, each CTA on its own
+// ring, so one CTA's warps keep the SM busy while the other's wait at their
+// per-job barrier; both roles cover the same 8-row blocks of each staged tile):
+//   warps 0-3   grad_input = the same stencil over the grad_output tile with the
 //               kernel flipped (gx[h][c] = sum_{u,v} w[K-1-u][K-1-v] gy[h+u-P][c+v-P]),
 //               plus, in a separate instantiation, a residual gradient;
-//   warps 8-15  weight / bias gradients of the block's own grad_output elements,
+//   warps 4-7   weight / bias gradients of the block's own grad_output elements,
 //               gw[u][v] += gy[h][c] * x[h+u-P][c+v-P], accumulated in registers over
 //               all consecutive items of the same (c, column tile) and then reduced
 //               across these warps (warp shuffles, then the per-warp sums in warp
@@ -50,8 +51,10 @@ constexpr int TW = 128;        // tile width (columns)
 constexpr int SMW = TW + 8;    // staged row: 4 halo columns on each side
 constexpr int FWD_WARPS = 8;   // forward: 64-row tiles, two CTAs per SM
 constexpr int FWD_CTAS = 2;
-constexpr int BWD_WARPS = 8;   // backward: 64-row tiles, one CTA per SM, 8 grad_input + 8 weight-gradient warps
-constexpr int NSTAGE = 3;      // depth of the shared-memory ring
+constexpr int BWD_WARPS = 4;   // backward: 32-row tiles, two CTAs per SM, 4 grad_input + 4 weight-gradient warps each
+constexpr int BWD_CTAS = 2;
+constexpr int BWD_NSTAGE = 2;  // depth of the backward's ring (two 41.5 KB stages: three would not fit twice per SM)
+constexpr int NSTAGE = 3;      // depth of the forward's ring
 constexpr int WSLOT = 64;      // floats per warp in the weight-gradient reduction buffer (K*K + bias)
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 
@@ -107,11 +110,12 @@ __device__ __forceinline__ void tma_load_3d(float* dst, const CUtensorMap* map, 
 
 // A CTA that timed out: record it, then let thread 0 wait (bounded) for the
 // copies it issued and nobody consumed, so none lands after the CTA is gone.
+template <int NST>
 __device__ void give_up(uint64_t* full, int first_unconsumed, int issued) {
     if (threadIdx.x == 0) {
         atomicCAS(&g_dw_status, 0, (int)HC_ERR_TIMEOUT);
         for (int j = first_unconsumed; j < issued; j++)
-            mbar_wait(full + (j % NSTAGE), (unsigned)((j / NSTAGE) & 1));
+            mbar_wait(full + (j % NST), (unsigned)((j / NST) & 1));
     }
 }
 
@@ -445,14 +449,14 @@ struct BwdArgs {
 // grad_input (a.gres).  Separate instantiations, so that the plain kernel
 // carries none of their bookkeeping.
 template <int K, bool ROWS, bool RES>
-__global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
+__global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
     dw_bwd_kernel(const __grid_constant__ CUtensorMap gymap, const __grid_constant__ CUtensorMap xmap, BwdArgs a,
                   Sched sc) {
     using G = Geo<K, BWD_WARPS>;
     constexpr int P = G::P, TH = G::TH, KK = K * K;
     extern __shared__ __align__(1024) float smem[];
-    float* tiles = smem;                              // [NSTAGE][gy, x][TILE]
-    float* red = smem + 2 * NSTAGE * G::TILE;         // [BWD_WARPS][KK + 1]
+    float* tiles = smem;                              // [BWD_NSTAGE][gy, x][TILE]
+    float* red = smem + 2 * BWD_NSTAGE * G::TILE;         // [BWD_WARPS][KK + 1]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + BWD_WARPS * WSLOT);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = (sc.H + TH - 1) / TH;
@@ -499,8 +503,8 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
                 sc.next(in_, ic, ict);
             }
         }
-        uint64_t* bar = full + (q % NSTAGE);
-        float* st = tiles + (q % NSTAGE) * 2 * G::TILE;
+        uint64_t* bar = full + (q % BWD_NSTAGE);
+        float* st = tiles + (q % BWD_NSTAGE) * 2 * G::TILE;
         mbar_expect_tx(bar, want_wb ? 2 * G::BYTES : G::BYTES);
         const int x0 = sc.xo + sc.col(ct) * TW - 4, y0 = t * TH - P, z = n * sc.C + c;
         tma_load_3d(st, &gymap, x0, y0, z, bar);
@@ -510,12 +514,12 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
     // grad_input role is the longer one, so none of its warps waits on an issue
     const int issuer = BWD_WARPS * 32;
     if (tid == issuer) {
-        for (int s = 0; s < NSTAGE; s++) mbar_init(full + s, 1);
+        for (int s = 0; s < BWD_NSTAGE; s++) mbar_init(full + s, 1);
         fence_barrier_init();
     }
     __syncthreads();
     if (tid == issuer)
-        for (int j = 0; j < NSTAGE && j < jobs; j++) issue(j);
+        for (int j = 0; j < BWD_NSTAGE && j < jobs; j++) issue(j);
 
     // The ring, shared by both roles: every warp waits for job q's stage, does
     // its role's work on it, and the stage is refilled after a CTA barrier.
@@ -545,13 +549,13 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, 1)
             }
             const bool ok = mbar_wait(full + s, ph);
             if (__syncthreads_or(!ok)) {
-                give_up(full, q, q + NSTAGE < jobs ? q + NSTAGE : jobs);
+                give_up<BWD_NSTAGE>(full, q, q + BWD_NSTAGE < jobs ? q + BWD_NSTAGE : jobs);
                 return;
             }
             work(s, n, c, ct, t, flush);
             __syncthreads();  // every warp is done with this stage
-            if (tid == issuer && q + NSTAGE < jobs) issue(q + NSTAGE);
-            if (++s == NSTAGE) {
+            if (tid == issuer && q + BWD_NSTAGE < jobs) issue(q + BWD_NSTAGE);
+            if (++s == BWD_NSTAGE) {
                 s = 0;
                 ph ^= 1u;
             }
@@ -899,9 +903,9 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     if (s || (s = plane_map<K, BWD_WARPS>(&xm, x, d, lay.pitch))) return s;
     int grid;
     // runs of one (c, column tile): gw stays in registers; column tiles side by side in CTA groups
-    const Sched sc = sched_of(d, &grid, 2, 1, lay);
+    const Sched sc = sched_of(d, &grid, 2, BWD_CTAS, lay);
     const int tps = p.Wl / TW;
-    const size_t smem = sizeof(float) * (2 * NSTAGE * G::TILE + BWD_WARPS * WSLOT) + NSTAGE * sizeof(uint64_t);
+    const size_t smem = sizeof(float) * (2 * BWD_NSTAGE * G::TILE + BWD_WARPS * WSLOT) + BWD_NSTAGE * sizeof(uint64_t);
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
         const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
@@ -950,10 +954,11 @@ hc_status launch_shard_partials(const float* tile_part, float* gwp, float* gbp, 
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
     // row shards: the backward splits its weight-gradient runs at row-shard ends,
-    // which must fall on the 64-row tile boundaries
+    // which must fall on row-tile boundaries (64-row multiples: whole tiles of
+    // both passes)
     return d->groups == d->C_in && d->C_out == d->C_in && d->kh == d->kw && (K == 3 || K == 5 || K == 7) &&
            d->stride == 1 && d->padding == (K - 1) / 2 && p.Wl % TW == 0 &&
-           (p.Sh == 1 || p.Hlo % Geo<3, BWD_WARPS>::TH == 0) &&
+           (p.Sh == 1 || p.Hlo % 64 == 0) &&
            (long long)d->N * d->C_in * (d->W / TW) < (1LL << 31);
 }
 
