@@ -455,9 +455,10 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
     using G = Geo<K, BWD_WARPS>;
     constexpr int P = G::P, TH = G::TH, KK = K * K;
     extern __shared__ __align__(1024) float smem[];
-    float* tiles = smem;                              // [BWD_NSTAGE][gy, x][TILE]
-    float* red = smem + 2 * BWD_NSTAGE * G::TILE;         // [BWD_WARPS][KK + 1]
+    float* tiles = smem;                                   // [BWD_NSTAGE][gy, x][TILE]
+    float* red = smem + 2 * BWD_NSTAGE * G::TILE;          // [BWD_WARPS][KK + 1]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + BWD_WARPS * WSLOT);
+    RowJobs& rj = *reinterpret_cast<RowJobs*>(full + BWD_NSTAGE);  // the issuer's cursor (row shards)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = (sc.H + TH - 1) / TH;
     // Without row shards the CTA's jobs are a contiguous run of (item, row tile)
@@ -484,12 +485,11 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
     // tile; with row shards as RowJobs walks them.
     const int tpr = ntiles / a.Sh;  // row tiles per row shard (row shards only)
 
-    // The issuer thread issues the jobs in order; its cursor ((in_, ic, ict, it), or rj with
-    // row shards) advances one job at a time (no divisions).
+    // The issuer thread issues the jobs in order; its cursor ((in_, ic, ict, it), or rj in
+    // shared memory with row shards: no registers held by every thread) advances one job
+    // at a time (no divisions).
     int in_ = 0, ic = 0, ict = 0, it = t0;
-    RowJobs rj{};
     if (!ROWS) sc.decode(i0, in_, ic, ict);
-    else rj.start(sc, i0, i1);
     auto issue = [&](int q) {
         (void)q;
         int n, c, ct, t;
@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
     const int issuer = BWD_WARPS * 32;
     if (tid == issuer) {
         for (int s = 0; s < BWD_NSTAGE; s++) mbar_init(full + s, 1);
+        if (ROWS) rj.start(sc, i0, i1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -547,13 +548,17 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
                 on_channel(c);
                 cur_c = c;
             }
+            // A wait that ran out is acted on at the job's end, where every warp meets
+            // (one CTA barrier per job): all warps still run the job (the named barrier
+            // of the weight-gradient flush needs every one of its warps; the stage's
+            // contents are then not valid, and the call reports HC_ERR_TIMEOUT), then
+            // the CTA gives up.
             const bool ok = mbar_wait(full + s, ph);
-            if (__syncthreads_or(!ok)) {
+            work(s, n, c, ct, t, flush);
+            if (__syncthreads_or(!ok)) {  // every warp is done with this stage
                 give_up<BWD_NSTAGE>(full, q, q + BWD_NSTAGE < jobs ? q + BWD_NSTAGE : jobs);
                 return;
             }
-            work(s, n, c, ct, t, flush);
-            __syncthreads();  // every warp is done with this stage
             if (tid == issuer && q + BWD_NSTAGE < jobs) issue(q + BWD_NSTAGE);
             if (++s == BWD_NSTAGE) {
                 s = 0;
@@ -905,7 +910,8 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     // runs of one (c, column tile): gw stays in registers; column tiles side by side in CTA groups
     const Sched sc = sched_of(d, &grid, 2, BWD_CTAS, lay);
     const int tps = p.Wl / TW;
-    const size_t smem = sizeof(float) * (2 * BWD_NSTAGE * G::TILE + BWD_WARPS * WSLOT) + BWD_NSTAGE * sizeof(uint64_t);
+    const size_t smem = sizeof(float) * (2 * BWD_NSTAGE * G::TILE + BWD_WARPS * WSLOT) +
+                        BWD_NSTAGE * sizeof(uint64_t) + sizeof(RowJobs);
     static std::atomic<unsigned long long> attr{0};
     once_per_device(attr, [&] {
         const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
