@@ -960,11 +960,11 @@ hc_status launch_shard_partials(const float* tile_part, float* gwp, float* gbp, 
 bool depthwise_supported(const hc_conv_desc* d, const Plan& p) {
     const int K = d->kh;
     // row shards: the backward splits its weight-gradient runs at row-shard ends,
-    // which must fall on row-tile boundaries (64-row multiples: whole tiles of
-    // both passes)
+    // which must fall on its row-tile boundaries (the forward computes the global
+    // conv whatever the row shards)
     return d->groups == d->C_in && d->C_out == d->C_in && d->kh == d->kw && (K == 3 || K == 5 || K == 7) &&
            d->stride == 1 && d->padding == (K - 1) / 2 && p.Wl % TW == 0 &&
-           (p.Sh == 1 || p.Hlo % 64 == 0) &&
+           (p.Sh == 1 || p.Hlo % Geo<3, BWD_WARPS>::TH == 0) &&
            (long long)d->N * d->C_in * (d->W / TW) < (1LL << 31);
 }
 

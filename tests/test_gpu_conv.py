@@ -116,7 +116,8 @@ CASES = {
     "tc_down2x2s2_grid_2x2": lambda: _rows(tc_strided_case(1, 128, 8, 512, 256, 2, 2), 2),
     "pw_grid_2x4": lambda: _rows(tc_case(1, 256, 8, 256, 128, 1, 4), 2),
     "dw7_grid_2x2": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 2),          # 64-row shards: depthwise
-    "dw7_grid_4x2_direct": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 4),   # 32-row shards: direct
+    "dw7_grid_4x2": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 4),          # 32-row shards: depthwise
+    "dw7_grid_8x2_direct": lambda: _rows(dw_case(1, 2, 128, 256, 7, 2), 8),   # 16-row shards: direct
     "grouped_strided_grid_3x2": lambda: _rows(generic_case(P.cfg_of(2, 6, 12, 16, 4, 3, 2, 2, 2, 2)), 3),
 }
 
@@ -155,11 +156,12 @@ def test_parity_direct(hc, orc, name):
 
 
 def test_grid_family_choice(hc):
-    """Row shards keep the depthwise kernels when each row shard is whole 64-row
-    tiles, and fall back to the direct kernels otherwise."""
+    """Row shards keep the depthwise kernels when each row shard is whole 32-row
+    tiles of the backward, and fall back to the direct kernels otherwise."""
     sel = lambda n: hc.hc_conv2d_select(hc.desc(CASES[n]()[0]), 1)
     assert sel("dw7_grid_2x2") == (0, hc.HC_ALGO_DEPTHWISE)
-    assert sel("dw7_grid_4x2_direct") == (0, hc.HC_ALGO_DIRECT)
+    assert sel("dw7_grid_4x2") == (0, hc.HC_ALGO_DEPTHWISE)
+    assert sel("dw7_grid_8x2_direct") == (0, hc.HC_ALGO_DIRECT)
     assert sel("tc_5x5_grid_2x2") == (0, hc.HC_ALGO_TC_3XTF32)
     assert sel("tc_down2x2s2_grid_2x2") == (0, hc.HC_ALGO_TC_BF16X6)
     assert sel("pw_grid_2x4") == (0, hc.HC_ALGO_TC_BF16X6)
@@ -575,7 +577,7 @@ def test_config3_full_size_sampled(hc, orc):
 
 @pytest.mark.parametrize("name,family", [("dw7_ragged_S4", "DEPTHWISE"), ("dw5_S2", "DEPTHWISE"),
                                          ("dw3_S4", "DEPTHWISE"), ("dw7_grid_2x2", "DEPTHWISE"),
-                                         ("tc_5x5_S2", "TC_3XTF32"),
+                                         ("dw7_grid_4x2", "DEPTHWISE"), ("tc_5x5_S2", "TC_3XTF32"),
                                          ("tc_down2x2s2_S2", "TC_BF16X6"), ("config1_dense5x5", "DIRECT")])
 def test_bwd_residual(hc, orc, name, family):
     """hc_conv2d_bwd_residual: grad_input plus the gradient reaching x along a
