@@ -443,6 +443,8 @@ struct BwdArgs {
     int tiles_per_shard;
     int want_wb;
     int S, Sh, hlo;  // column shards, row shards, rows per row shard (a multiple of TH when Sh > 1)
+    int slots;       // partial slots per (grid shard, c, tile)
+    int pieces;      // without row shards: a slot per piece of a run (else per job)
 };
 
 // ROWS: row shards present (a.Sh > 1); RES: a residual gradient is added to
@@ -624,11 +626,30 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
         for (int u = 0; u < K; u++)
 #pragma unroll
             for (int v = 0; v < K; v++) gw[u][v] = 0.0f;
-        // Partial slots of one (grid shard, c, tile): one per image with row shards,
-        // else one per (image, row tile); a run's total goes to its first slot and
-        // its other slots get zeros, so every slot is written exactly once.
-        const int slots = ROWS ? sc.N : sc.N * ntiles;
-        int run_m0 = -1;  // first slot of the current run
+        // Partial slots of one (grid shard, c, tile), a.slots of them: with row shards
+        // one per image, a run's total in its first slot and zeros in the rest.
+        // Without them either one per piece of a run (a.pieces: the run's jobs in one
+        // CTA range; the piece's index is the number of range starts inside the run
+        // before it, and the run's last piece zeroes the slots that no piece takes)
+        // or one per (image, row tile) as with row shards.  Every slot is written once.
+        const int slots = a.slots;
+        // Only the CTA's first run can start before its range (sc.job_range: every
+        // range holds a job when a.pieces is set): its piece is the CTA's range index
+        // less that of the range holding the run's first job; every later run starts
+        // in this CTA, at piece 0.
+        int next_piece = 0;
+        if (!ROWS && a.pieces) {
+            const bool grouped = sc.tile_fastest == 2;
+            const long long L = (long long)sc.N * ntiles;
+            const long long T = (grouped ? (long long)sc.N * sc.C * (sc.col_tiles / sc.tb) : (long long)sc.items) * ntiles;
+            const long long parts = grouped ? gridDim.x / sc.tb : gridDim.x;
+            const long long g = grouped ? blockIdx.x / sc.tb : blockIdx.x;
+            const long long run0 = (g * T / parts) / L;  // the run of the CTA's first job
+            // the last range index h with h * T / parts <= run0 * L
+            const long long gfirst = ((run0 * L + 1) * parts + T - 1) / T - 1;
+            next_piece = (int)(g - gfirst);
+        }
+        int run_m0 = -1;  // first slot of the current run (piece)
         ring([](int) {},
              [&](int s, int n, int c, int ct, int t, bool flush) {
                  if (RES && !ROWS && a.gx) {
@@ -650,7 +671,10 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
                  }
                  if (!want_wb) return;
                  const int m = ROWS ? n : n * ntiles + t;
-                 if (run_m0 < 0) run_m0 = m;
+                 if (run_m0 < 0) {
+                     run_m0 = !ROWS && a.pieces ? next_piece : m;
+                     next_piece = 0;
+                 }
                  const float* gys = tiles + s * 2 * G::TILE;
                  const float* xs = gys + G::TILE;
 #pragma unroll 1
@@ -694,7 +718,13 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
                      const int r = sc.col(ct) / a.tiles_per_shard, tt = sc.col(ct) - r * a.tiles_per_shard;
                      const int qs = ROWS ? (t * TH) / a.hlo * a.S + r : r;  // grid shard
                      float* slot = a.tile_part + (((long long)qs * sc.C + c) * a.tiles_per_shard + tt) * slots * (KK + 1);
-                     for (int k = run_m0; k <= m; k++) slot[(long long)k * (KK + 1) + wtid] = k == run_m0 ? tot : 0.0f;
+                     if (!ROWS && a.pieces) {
+                         slot[(long long)run_m0 * (KK + 1) + wtid] = tot;
+                         if (t == ntiles - 1 && n == sc.N - 1)  // the run's last piece
+                             for (int k = run_m0 + 1; k < slots; k++) slot[(long long)k * (KK + 1) + wtid] = 0.0f;
+                     } else {
+                         for (int k = run_m0; k <= m; k++) slot[(long long)k * (KK + 1) + wtid] = k == run_m0 ? tot : 0.0f;
+                     }
                  }
                  run_m0 = -1;
              });
@@ -920,7 +950,23 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
                cudaFuncSetAttribute(dw_bwd_kernel<K, false, true>, A, (int)smem) == cudaSuccess &&
                cudaFuncSetAttribute(dw_bwd_kernel<K, true, true>, A, (int)smem) == cudaSuccess;
     });
-    BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo};
+    // partial slots per (grid shard, c, tile): a slot per piece of a run (the run's jobs in
+    // one CTA range) when one launch covers every tile and every range holds a job, so
+    // the shard-partials pass reads a few slots per run instead of one per job
+    int slots = (int)bwd_slots(d, p), pieces = 0;
+    if (p.Sh == 1 && lay.tiles == HC_TILES_ALL && sc.items) {
+        const int ntiles = (d->H + G::TH - 1) / G::TH;
+        const long long L = (long long)d->N * ntiles;
+        const bool grouped = sc.tile_fastest == 2;
+        const long long T = (grouped ? (long long)sc.N * sc.C * (sc.col_tiles / sc.tb) : (long long)sc.items) * ntiles;
+        const long long m = T / (grouped ? grid / sc.tb : grid);  // jobs of the shortest range
+        if (m >= 1) {
+            pieces = 1;
+            const long long most = (L - 1 + m - 1) / m + 1;  // ranges meeting L consecutive jobs
+            slots = (int)(most < L ? most : L);
+        }
+    }
+    BwdArgs a{w, gx, gx ? gres : nullptr, tile_part, tps, want_wb ? 1 : 0, p.S, p.Sh, p.Hlo, slots, pieces};
     const dim3 grd(grid), blk(2 * BWD_WARPS * 32);
     if (sc.items == 0) {
         s = HC_OK;
@@ -936,7 +982,7 @@ hc_status bwd_k(const hc_conv_desc* d, const Plan& p, const float* x, const floa
     }
     if (sc.items) s = launched("dw_bwd_kernel", st);
     if (s || !want_wb || !lay.partials) return s;
-    return launch_shard_partials(tile_part, gwp, gbp, gw, gb, p.Q, d->C_in, (int)(tps * bwd_slots(d, p)), K * K, st);
+    return launch_shard_partials(tile_part, gwp, gbp, gw, gb, p.Q, d->C_in, tps * slots, K * K, st);
 }
 
 }  // namespace
