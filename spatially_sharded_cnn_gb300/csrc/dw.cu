@@ -732,8 +732,7 @@ __global__ void __launch_bounds__(2 * BWD_WARPS * 32, BWD_CTAS)
 }
 
 // Shard partials: gwp[r][c][k] = sum over shard r's slots of the partials (tile
-// tt, then image n and, without row shards, row tile, ascending); gbp[r][c]
-// likewise from the last entry.  One thread per
+// tt, then the tile's slots, ascending); gbp[r][c] likewise from the last entry.  One thread per
 // (c, k) walks the shards in order and also writes the full gradients
 // gw[c][k] / gb[c] (either may be null): the shard partials added from shard 0
 // up, the order hc_conv2d_bwd's shard sum uses.
@@ -858,7 +857,8 @@ hc_status plane_map(CUtensorMap* m, const float* base, const hc_conv_desc* d, in
 }
 
 // Weight-gradient partial slots per (grid shard, channel, column tile) of the
-// backward: one per image with row shards, else one per (image, row tile).
+// backward, at most: one per image with row shards, else one per (image, row
+// tile) (a launch over every tile uses one per piece of a run, no more).
 long long bwd_slots(const hc_conv_desc* d, const Plan& p) {
     constexpr int TH = Geo<3, BWD_WARPS>::TH;  // the same for every K
     return p.Sh > 1 ? (long long)d->N : (long long)d->N * ((d->H + TH - 1) / TH);
